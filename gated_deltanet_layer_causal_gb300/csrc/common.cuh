@@ -1,0 +1,277 @@
+// Shared device helpers of the GDN CUDA library: dtype conversion, warp
+// reductions and a warp-tiled tensor-core product over shared-memory operands.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr int kD = 128;      // d_k = d_v
+constexpr int kChunk = 64;   // chunk length of the WY form
+constexpr int kConvK = 4;    // conv taps
+
+// ----------------------------------------------------------------- dtypes
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <class T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// 4 consecutive elements (16 B for fp32, 8 B for bf16) as a float4
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
+    uint2 u = *reinterpret_cast<const uint2*>(p);
+    __nv_bfloat162 lo = *reinterpret_cast<__nv_bfloat162*>(&u.x);
+    __nv_bfloat162 hi = *reinterpret_cast<__nv_bfloat162*>(&u.y);
+    float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+
+// ----------------------------------------------------------------- math
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + __expf(-x)); }
+__device__ __forceinline__ float siluf_(float x) { return x * sigmoidf_(x); }
+// softplus with torch's linear branch above 20
+__device__ __forceinline__ float softplusf_(float x) { return x > 20.f ? x : log1pf(expf(x)); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ----------------------------------------------------------------- tensor cores
+__device__ __forceinline__ uint32_t f2tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Split of an M x N product over NW warps into 16 x 8 fragments.
+template <int M, int N, int NW>
+struct Tile {
+    static constexpr int MT = M / 16, NT = N / 8;
+    static constexpr int WM = MT < NW ? MT : NW;   // warps along M
+    static constexpr int WN = NW / WM;             // warps along N
+    static constexpr int MPW = MT / WM;            // 16-row fragments per warp
+    static constexpr int NPW = NT / WN;            // 8-col fragments per warp
+    static_assert(M % 16 == 0 && N % 8 == 0, "fragment multiple");
+    static_assert(MT % WM == 0 && NW % WM == 0 && NT % WN == 0, "warp split");
+    using Acc = float[MPW][NPW][4];
+    __device__ static int m0() { return (int)(threadIdx.x / 32 % WM) * MPW * 16; }
+    __device__ static int n0() { return (int)(threadIdx.x / 32 / WM) * NPW * 8; }
+};
+
+template <int M, int N, int NW>
+__device__ __forceinline__ void tile_zero(typename Tile<M, N, NW>::Acc& acc) {
+    using C = Tile<M, N, NW>;
+#pragma unroll
+    for (int i = 0; i < C::MPW; i++)
+#pragma unroll
+        for (int j = 0; j < C::NPW; j++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) acc[i][j][e] = 0.f;
+}
+
+// acc += A * B with A(r, k) = a(r, k), B(k, c) = b(k, c), k in [0, K).
+// a and b read shared memory (or registers); tf32 operands, fp32 accumulate.
+template <int M, int N, int K, int NW, class FA, class FB>
+__device__ __forceinline__ void tile_mma(typename Tile<M, N, NW>::Acc& acc, FA a, FB b) {
+    using C = Tile<M, N, NW>;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int m0 = C::m0(), n0 = C::n0();
+#pragma unroll 2
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t af[C::MPW][4];
+#pragma unroll
+        for (int i = 0; i < C::MPW; i++) {
+            const int r = m0 + i * 16 + g;
+            af[i][0] = f2tf32(a(r, k0 + t));
+            af[i][1] = f2tf32(a(r + 8, k0 + t));
+            af[i][2] = f2tf32(a(r, k0 + t + 4));
+            af[i][3] = f2tf32(a(r + 8, k0 + t + 4));
+        }
+#pragma unroll
+        for (int j = 0; j < C::NPW; j++) {
+            const int c = n0 + j * 8 + g;
+            uint32_t bf[2] = {f2tf32(b(k0 + t, c)), f2tf32(b(k0 + t + 4, c))};
+#pragma unroll
+            for (int i = 0; i < C::MPW; i++) mma_tf32(acc[i][j], af[i], bf);
+        }
+    }
+}
+
+// Visit every accumulator element as f(row, col, value&).
+template <int M, int N, int NW, class F>
+__device__ __forceinline__ void tile_each(typename Tile<M, N, NW>::Acc& acc, F f) {
+    using C = Tile<M, N, NW>;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int m0 = C::m0(), n0 = C::n0();
+#pragma unroll
+    for (int i = 0; i < C::MPW; i++)
+#pragma unroll
+        for (int j = 0; j < C::NPW; j++)
+#pragma unroll
+            for (int e = 0; e < 4; e++)
+                f(m0 + i * 16 + g + (e >> 1) * 8, n0 + j * 8 + 2 * t + (e & 1), acc[i][j][e]);
+}
+
+// Visit accumulator element pairs (same row, columns col and col+1) as
+// f(row, col, v0&, v1&): lets epilogues write 8-byte vectors.
+template <int M, int N, int NW, class F>
+__device__ __forceinline__ void tile_each2(typename Tile<M, N, NW>::Acc& acc, F f) {
+    using C = Tile<M, N, NW>;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int m0 = C::m0(), n0 = C::n0();
+#pragma unroll
+    for (int i = 0; i < C::MPW; i++)
+#pragma unroll
+        for (int j = 0; j < C::NPW; j++)
+#pragma unroll
+            for (int h = 0; h < 2; h++)
+                f(m0 + i * 16 + g + h * 8, n0 + j * 8 + 2 * t, acc[i][j][2 * h],
+                  acc[i][j][2 * h + 1]);
+}
+
+// Row sums of f(row, col, v) over the columns one warp holds: part[wn * M + row]
+// (wn = the warp's position along N).  Summing part over wn in order after a
+// barrier gives a deterministic row reduction.
+template <int M, int N, int NW, class F>
+__device__ __forceinline__ void tile_rowpart(typename Tile<M, N, NW>::Acc& acc, F f, float* part) {
+    using C = Tile<M, N, NW>;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int m0 = C::m0(), n0 = C::n0(), wn = (int)(threadIdx.x / 32 / C::WM);
+#pragma unroll
+    for (int i = 0; i < C::MPW; i++)
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            const int r = m0 + i * 16 + g + h * 8;
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < C::NPW; j++)
+#pragma unroll
+                for (int e = 0; e < 2; e++) s += f(r, n0 + j * 8 + 2 * t + e, acc[i][j][2 * h + e]);
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            if (t == 0) part[wn * M + r] = s;
+        }
+}
+
+// Column sums of f(row, col, v) over the rows one warp holds: part[wm * N + col].
+template <int M, int N, int NW, class F>
+__device__ __forceinline__ void tile_colpart(typename Tile<M, N, NW>::Acc& acc, F f, float* part) {
+    using C = Tile<M, N, NW>;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int m0 = C::m0(), n0 = C::n0(), wm = (int)(threadIdx.x / 32 % C::WM);
+#pragma unroll
+    for (int j = 0; j < C::NPW; j++)
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+            const int c = n0 + j * 8 + 2 * t + e;
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < C::MPW; i++)
+#pragma unroll
+                for (int h = 0; h < 2; h++) s += f(m0 + i * 16 + g + h * 8, c, acc[i][j][2 * h + e]);
+            s += __shfl_xor_sync(0xffffffffu, s, 4);
+            s += __shfl_xor_sync(0xffffffffu, s, 8);
+            s += __shfl_xor_sync(0xffffffffu, s, 16);
+            if (g == 0) part[wm * N + c] = s;
+        }
+}
+
+// Backward of one gated-RMSNorm row held by a warp (4 columns per lane):
+//   n = o rs, dn = dy (1+w) silu(z): do = rs (dn - n mean(dn n)),
+//   dz = dy n (1+w) silu'(z), dw += dy n silu(z).
+struct NormRowGrad {
+    float4 d_o, dz;
+};
+__device__ __forceinline__ NormRowGrad norm_row_bwd(float4 o4, float4 z4, float4 dy4, float4 w4,
+                                                    float eps, float4& dw_acc) {
+    float ss = warp_sum(o4.x * o4.x + o4.y * o4.y + o4.z * o4.z + o4.w * o4.w);
+    float rs = rsqrtf(ss * (1.f / kD) + eps);
+    float o[4] = {o4.x, o4.y, o4.z, o4.w}, z[4] = {z4.x, z4.y, z4.z, z4.w};
+    float dy[4] = {dy4.x, dy4.y, dy4.z, dy4.w}, w[4] = {w4.x, w4.y, w4.z, w4.w};
+    float nn[4], dn[4], sz[4], dsz[4], m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        float s = sigmoidf_(z[i]);
+        sz[i] = z[i] * s;
+        dsz[i] = s * (1.f + z[i] * (1.f - s));
+        nn[i] = o[i] * rs;
+        dn[i] = dy[i] * (1.f + w[i]) * sz[i];
+        m += dn[i] * nn[i];
+    }
+    m = warp_sum(m) * (1.f / kD);
+    float od[4], zd[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        od[i] = rs * (dn[i] - nn[i] * m);
+        zd[i] = dy[i] * nn[i] * (1.f + w[i]) * dsz[i];
+    }
+    dw_acc.x += dy[0] * nn[0] * sz[0];
+    dw_acc.y += dy[1] * nn[1] * sz[1];
+    dw_acc.z += dy[2] * nn[2] * sz[2];
+    dw_acc.w += dy[3] * nn[3] * sz[3];
+    return {make_float4(od[0], od[1], od[2], od[3]), make_float4(zd[0], zd[1], zd[2], zd[3])};
+}
+
+// Inclusive prefix sum of 64 values held two per lane by one warp (in place).
+__device__ __forceinline__ void warp_cumsum64(float* v) {
+    const int lane = threadIdx.x & 31;
+    float a = v[2 * lane], b = v[2 * lane + 1], s = a + b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        float u = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += u;
+    }
+    float ex = s - (a + b);
+    v[2 * lane] = ex + a;
+    v[2 * lane + 1] = ex + a + b;
+}
+
+// T = (I + A)^-1 for strictly lower A [64][lda] (unit lower-triangular
+// inverse) by forward substitution, column by column: T_ij = -sum_{m=j}^{i-1}
+// A_im T_mj.  256 threads: 4 lanes per column split each dot product.
+__device__ __forceinline__ void tril_inverse64(const float* As, int lda, float* Ts, int ldt) {
+    const int tid = threadIdx.x, j = tid >> 2, q = tid & 3;
+    for (int i = q; i < kChunk; i += 4) Ts[i * ldt + j] = (i == j) ? 1.f : 0.f;
+    __syncwarp();
+    const int ibeg = (tid >> 5) * 8 + 1;  // first row any lane of this warp needs
+    for (int i = ibeg; i < kChunk; i++) {
+        float p = 0.f;
+        if (i > j)
+            for (int m = j + q; m < i; m += 4) p += As[i * lda + m] * Ts[m * ldt + j];
+        p += __shfl_xor_sync(0xffffffffu, p, 1);
+        p += __shfl_xor_sync(0xffffffffu, p, 2);
+        if (i > j && q == 0) Ts[i * ldt + j] = -p;
+        __syncwarp();
+    }
+}
+
+// Varlen plan entry of one chunk: first token, length, sequence, chunk within sequence.
+struct ChunkInfo {
+    int32_t start, len, seq, idx;
+};
+
+}  // namespace gdn

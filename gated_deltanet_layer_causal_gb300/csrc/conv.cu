@@ -1,0 +1,310 @@
+// Causal depthwise conv1d (4 taps) + SiLU + per-head L2 norm of q and k.
+//
+// prime-rl #3860 "Summary": the layer runs causal_conv1d over the q/k/v mix with
+// cu_seqlens (the conv restarts at every sequence start); "[main] feat(moe):
+// Support gated delta net for Qwen3-Next (1/4)", "GDN args": conv kernel 4,
+// head dims 128.  L2 normalisation of q and k per (token, k-head), q scaled by
+// d_k^-1/2.
+//
+// HBM-bound.  One warp walks a run of consecutive tokens of one 128-channel
+// head; each lane owns 4 channels (one 16-B fp32 / 8-B bf16 vector), keeps the
+// previous three inputs in registers (each input row is read once), and the
+// per-head sum of squares is a warp shuffle reduction.
+#include "common.cuh"
+#include "kernels.h"
+#include "prof.h"
+
+namespace gdn {
+
+constexpr int kConvWarps = 8;
+constexpr int kConvRun = 64;   // tokens per warp
+
+__device__ __forceinline__ int seq_of(const int32_t* cu, int N, int64_t t) {
+    // last n with cu[n] <= t (sequences may be empty)
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Raw conv input at position p of sequence n (start s): x, else the conv cache, else 0.
+template <class T>
+__device__ __forceinline__ float4 conv_in(const T* x, const T* cs, int64_t p, int64_t s, int n,
+                                          int C, int c) {
+    if (p >= s) return ld4(x + p * C + c);
+    int64_t m = (kConvK - 1) + (p - s);
+    if (cs == nullptr || m < 0) return make_float4(0.f, 0.f, 0.f, 0.f);
+    const T* b = cs + ((int64_t)n * C + c) * (kConvK - 1) + m;
+    return make_float4(to_f(b[0]), to_f(b[kConvK - 1]), to_f(b[2 * (kConvK - 1)]),
+                       to_f(b[3 * (kConvK - 1)]));
+}
+
+__device__ __forceinline__ float conv4(const float (&w)[kConvK], float a3, float a2, float a1,
+                                       float a0) {
+    // w[3] multiplies the current token (a0), w[0] the token three back
+    return w[0] * a3 + w[1] * a2 + w[2] * a1 + w[3] * a0;
+}
+
+template <class T>
+__global__ void __launch_bounds__(kConvWarps * 32)
+conv_fwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* cs_in,
+                const int32_t* __restrict__ cu, int N, int64_t Ttot, int C, int hk,
+                float l2_eps, float q_scale, float* __restrict__ out) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int grp = blockIdx.y;
+    const int c = grp * kD + lane * 4;
+    const int64_t t0 = ((int64_t)blockIdx.x * kConvWarps + warp) * kConvRun;
+    if (t0 >= Ttot) return;
+    const int64_t t1 = min(t0 + (int64_t)kConvRun, Ttot);
+    const bool norm = grp < 2 * hk;
+    const float scale = grp < hk ? q_scale : 1.f;
+    float wr[4][kConvK];
+#pragma unroll
+    for (int ch = 0; ch < 4; ch++)
+#pragma unroll
+        for (int j = 0; j < kConvK; j++) wr[ch][j] = w[(c + ch) * kConvK + j];
+
+    int n = seq_of(cu, N, t0);
+    int64_t s = cu[n], e = cu[n + 1];
+    float4 h1 = conv_in(x, cs_in, t0 - 1, s, n, C, c);
+    float4 h2 = conv_in(x, cs_in, t0 - 2, s, n, C, c);
+    float4 h3 = conv_in(x, cs_in, t0 - 3, s, n, C, c);
+    for (int64_t t = t0; t < t1; t++) {
+        if (t >= e) {  // next (non-empty) sequence starts at t
+            while (cu[n + 1] <= t) n++;
+            s = cu[n];
+            e = cu[n + 1];
+            h1 = conv_in(x, cs_in, t - 1, s, n, C, c);
+            h2 = conv_in(x, cs_in, t - 2, s, n, C, c);
+            h3 = conv_in(x, cs_in, t - 3, s, n, C, c);
+        }
+        const float4 cur = ld4(x + t * C + c);
+        float4 o;
+        o.x = siluf_(conv4(wr[0], h3.x, h2.x, h1.x, cur.x));
+        o.y = siluf_(conv4(wr[1], h3.y, h2.y, h1.y, cur.y));
+        o.z = siluf_(conv4(wr[2], h3.z, h2.z, h1.z, cur.z));
+        o.w = siluf_(conv4(wr[3], h3.w, h2.w, h1.w, cur.w));
+        if (norm) {
+            float ss = warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
+            float r = rsqrtf(ss + l2_eps) * scale;
+            o.x *= r; o.y *= r; o.z *= r; o.w *= r;
+        }
+        st4(out + t * C + c, o);
+        h3 = h2; h2 = h1; h1 = cur;
+    }
+}
+
+// conv_state_out[n, c, m] = input at position end-3+m (from the cache when the
+// sequence is shorter than 3).  Reads all three before writing (alias-safe).
+template <class T>
+__global__ void conv_state_kernel(const T* __restrict__ x, const T* cs_in,
+                                  const int32_t* __restrict__ cu, int N, int C, T* cs_out) {
+    int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)N * C) return;
+    int n = (int)(idx / C), c = (int)(idx % C);
+    int64_t s = cu[n], e = cu[n + 1];
+    float v[kConvK - 1];
+#pragma unroll
+    for (int m = 0; m < kConvK - 1; m++) {
+        int64_t p = e - (kConvK - 1) + m;
+        if (p >= s) v[m] = to_f(x[p * C + c]);
+        else {
+            int64_t mm = (kConvK - 1) + (p - s);
+            v[m] = (cs_in != nullptr && mm >= 0) ? to_f(cs_in[idx * (kConvK - 1) + mm]) : 0.f;
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < kConvK - 1; m++) cs_out[idx * (kConvK - 1) + m] = from_f<T>(v[m]);
+}
+
+// ------------------------------------------------------------------ backward
+// dpre at token t for this lane's 4 channels: recompute conv + SiLU (+ L2) and
+// chain the incoming gradient dqkv through L2 and SiLU.
+template <class T>
+__device__ __forceinline__ float4 conv_dpre(const T* x, const T* cs, const float* dq, int64_t t,
+                                            int64_t s, int n, int C, int c,
+                                            const float (&w)[4][kConvK], bool norm, float scale,
+                                            float l2_eps) {
+    float4 a0 = ld4(x + t * C + c);
+    float4 a1 = conv_in(x, cs, t - 1, s, n, C, c);
+    float4 a2 = conv_in(x, cs, t - 2, s, n, C, c);
+    float4 a3 = conv_in(x, cs, t - 3, s, n, C, c);
+    float p[4] = {conv4(w[0], a3.x, a2.x, a1.x, a0.x), conv4(w[1], a3.y, a2.y, a1.y, a0.y),
+                  conv4(w[2], a3.z, a2.z, a1.z, a0.z), conv4(w[3], a3.w, a2.w, a1.w, a0.w)};
+    float4 g4 = ld4(dq + t * C + c);
+    float gd[4] = {g4.x, g4.y, g4.z, g4.w};
+    float xc[4], sg[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) { sg[i] = sigmoidf_(p[i]); xc[i] = p[i] * sg[i]; }
+    if (norm) {
+        float ss = warp_sum(xc[0] * xc[0] + xc[1] * xc[1] + xc[2] * xc[2] + xc[3] * xc[3]);
+        float r = rsqrtf(ss + l2_eps);
+        float u[4], du[4], dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; i++) { u[i] = xc[i] * r; du[i] = gd[i] * scale; dot += u[i] * du[i]; }
+        dot = warp_sum(dot);
+#pragma unroll
+        for (int i = 0; i < 4; i++) gd[i] = r * (du[i] - u[i] * dot);
+    }
+    float4 o;
+    o.x = gd[0] * sg[0] * (1.f + p[0] * (1.f - sg[0]));
+    o.y = gd[1] * sg[1] * (1.f + p[1] * (1.f - sg[1]));
+    o.z = gd[2] * sg[2] * (1.f + p[2] * (1.f - sg[2]));
+    o.w = gd[3] * sg[3] * (1.f + p[3] * (1.f - sg[3]));
+    return o;
+}
+
+__device__ __forceinline__ float f4(const float4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// One warp per run of tokens (walked backwards), lane = 4 channels.
+// dx[t] = sum_j w[j] dpre[t+3-j] within the sequence; dw partials per CTA
+// (fixed-order sum over the CTA's warps) go to wpart[blockIdx.x][c][j].
+template <class T>
+__global__ void __launch_bounds__(kConvWarps * 32)
+conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* cs_in,
+                const float* __restrict__ dqkv, const int32_t* __restrict__ cu, int N,
+                int64_t Ttot, int C, int hk, float l2_eps, float q_scale, T* __restrict__ dx,
+                float* __restrict__ wpart, float* dcs) {
+    __shared__ float red[kConvWarps][kD][kConvK];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int grp = blockIdx.y;
+    const int c = grp * kD + lane * 4;
+    const bool norm = grp < 2 * hk;
+    const float scale = grp < hk ? q_scale : 1.f;
+    float wr[4][kConvK];
+#pragma unroll
+    for (int ch = 0; ch < 4; ch++)
+#pragma unroll
+        for (int j = 0; j < kConvK; j++) wr[ch][j] = w[(c + ch) * kConvK + j];
+    float dw[4][kConvK];
+#pragma unroll
+    for (int ch = 0; ch < 4; ch++)
+#pragma unroll
+        for (int j = 0; j < kConvK; j++) dw[ch][j] = 0.f;
+
+    const int64_t t0 = ((int64_t)blockIdx.x * kConvWarps + warp) * kConvRun;
+    if (t0 < Ttot) {
+        const int64_t t1 = min(t0 + (int64_t)kConvRun, Ttot);
+        int n = seq_of(cu, N, t1 - 1);
+        int64_t s = cu[n], e = cu[n + 1];
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        // window of dpre at t+1, t+2, t+3 (zero past the sequence end)
+        float4 d1 = (t1 < e) ? conv_dpre(x, cs_in, dqkv, t1, s, n, C, c, wr, norm, scale, l2_eps) : z4;
+        float4 d2 = (t1 + 1 < e) ? conv_dpre(x, cs_in, dqkv, t1 + 1, s, n, C, c, wr, norm, scale, l2_eps) : z4;
+        float4 d3 = (t1 + 2 < e) ? conv_dpre(x, cs_in, dqkv, t1 + 2, s, n, C, c, wr, norm, scale, l2_eps) : z4;
+        for (int64_t t = t1 - 1; t >= t0; t--) {
+            if (t < s) {  // crossed into the previous (non-empty) sequence
+                while (cu[n] > t) n--;
+                s = cu[n];
+                e = cu[n + 1];
+                d1 = d2 = d3 = z4;
+            }
+            float4 d0 = conv_dpre(x, cs_in, dqkv, t, s, n, C, c, wr, norm, scale, l2_eps);
+            float4 o;
+            o.x = wr[0][3] * d0.x + wr[0][2] * d1.x + wr[0][1] * d2.x + wr[0][0] * d3.x;
+            o.y = wr[1][3] * d0.y + wr[1][2] * d1.y + wr[1][1] * d2.y + wr[1][0] * d3.y;
+            o.z = wr[2][3] * d0.z + wr[2][2] * d1.z + wr[2][1] * d2.z + wr[2][0] * d3.z;
+            o.w = wr[3][3] * d0.w + wr[3][2] * d1.w + wr[3][1] * d2.w + wr[3][0] * d3.w;
+            st4(dx + t * C + c, o);
+#pragma unroll
+            for (int j = 0; j < kConvK; j++) {
+                float4 xin = conv_in(x, cs_in, t - (kConvK - 1) + j, s, n, C, c);
+#pragma unroll
+                for (int ch = 0; ch < 4; ch++) dw[ch][j] += f4(d0, ch) * f4(xin, ch);
+            }
+            if (t == s && dcs != nullptr) {
+                // gradient of the conv cache: position s-3+m feeds tokens s..s+m
+#pragma unroll
+                for (int ch = 0; ch < 4; ch++) {
+                    float* o3 = dcs + ((int64_t)n * C + c + ch) * (kConvK - 1);
+                    o3[0] = wr[ch][0] * f4(d0, ch);
+                    o3[1] = wr[ch][0] * f4(d1, ch) + wr[ch][1] * f4(d0, ch);
+                    o3[2] = wr[ch][0] * f4(d2, ch) + wr[ch][1] * f4(d1, ch) + wr[ch][2] * f4(d0, ch);
+                }
+            }
+            d3 = d2; d2 = d1; d1 = d0;
+        }
+    }
+#pragma unroll
+    for (int ch = 0; ch < 4; ch++)
+#pragma unroll
+        for (int j = 0; j < kConvK; j++) red[warp][lane * 4 + ch][j] = dw[ch][j];
+    __syncthreads();
+    for (int i = threadIdx.x; i < kD * kConvK; i += blockDim.x) {
+        float acc = 0.f;
+        for (int wi = 0; wi < kConvWarps; wi++) acc += red[wi][i / kConvK][i % kConvK];
+        wpart[((int64_t)blockIdx.x * C + grp * kD) * kConvK + i] = acc;
+    }
+}
+
+// dconv_w[c, j] = sum over CTA rows of wpart (fixed order).
+__global__ void conv_dw_reduce_kernel(const float* __restrict__ wpart, int nparts, int C,
+                                      float* __restrict__ dw) {
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= C * kConvK) return;
+    float acc = 0.f;
+    for (int p = 0; p < nparts; p++) acc += wpart[(int64_t)p * C * kConvK + i];
+    dw[i] = acc;
+}
+
+// ------------------------------------------------------------------ launchers
+template <class T>
+cudaError_t launch_conv_fwd_t(const ConvArgs& a, cudaStream_t st) {
+    if (a.T > 0) {
+        dim3 grid((unsigned)((a.T + kConvWarps * kConvRun - 1) / (kConvWarps * kConvRun)),
+                  (unsigned)(a.C / kD));
+        GDN_PROF("conv_fwd", st);
+        conv_fwd_kernel<T><<<grid, kConvWarps * 32, 0, st>>>(
+            (const T*)a.x, a.w, (const T*)a.cs_in, a.cu, a.N, a.T, a.C, a.hk, a.l2_eps,
+            a.q_scale, a.qkv);
+    }
+    if (a.cs_out != nullptr && a.N > 0) {
+        int64_t n = (int64_t)a.N * a.C;
+        GDN_PROF("conv_state", st);
+        conv_state_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
+            (const T*)a.x, (const T*)a.cs_in, a.cu, a.N, a.C, (T*)a.cs_out);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_conv_fwd(const ConvArgs& a, cudaStream_t st) {
+    return a.bf16 ? launch_conv_fwd_t<__nv_bfloat16>(a, st) : launch_conv_fwd_t<float>(a, st);
+}
+
+int conv_bwd_parts(int64_t T) {
+    return (int)((T + kConvWarps * kConvRun - 1) / (kConvWarps * kConvRun));
+}
+
+template <class T>
+cudaError_t launch_conv_bwd_t(const ConvArgs& a, cudaStream_t st) {
+    int parts = conv_bwd_parts(a.T);
+    if (a.dcs != nullptr && a.N > 0)
+        cudaMemsetAsync(a.dcs, 0, sizeof(float) * (size_t)a.N * a.C * (kConvK - 1), st);
+    if (parts > 0) {
+        dim3 grid((unsigned)parts, (unsigned)(a.C / kD));
+        {
+            GDN_PROF("conv_bwd", st);
+            conv_bwd_kernel<T><<<grid, kConvWarps * 32, 0, st>>>(
+                (const T*)a.x, a.w, (const T*)a.cs_in, a.dqkv, a.cu, a.N, a.T, a.C, a.hk,
+                a.l2_eps, a.q_scale, (T*)a.dx, a.wpart, a.dcs);
+        }
+        {
+            GDN_PROF("conv_dw_reduce", st);
+            conv_dw_reduce_kernel<<<(a.C * kConvK + 255) / 256, 256, 0, st>>>(a.wpart, parts,
+                                                                              a.C, a.dw);
+        }
+    } else {
+        cudaMemsetAsync(a.dw, 0, sizeof(float) * (size_t)a.C * kConvK, st);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_conv_bwd(const ConvArgs& a, cudaStream_t st) {
+    return a.bf16 ? launch_conv_bwd_t<__nv_bfloat16>(a, st) : launch_conv_bwd_t<float>(a, st);
+}
+
+}  // namespace gdn

@@ -1,0 +1,126 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+struct ChunkInfo;
+
+struct ConvArgs {
+    bool bf16;
+    int N, C, hk;
+    int64_t T;
+    const int32_t* cu;
+    const void* x;
+    const float* w;
+    const void* cs_in;
+    float l2_eps, q_scale;
+    // forward
+    float* qkv;
+    void* cs_out;
+    // backward
+    const float* dqkv;
+    void* dx;
+    float* dw;
+    float* wpart;   // [conv_bwd_parts(T), C, 4] scratch
+    float* dcs;
+};
+cudaError_t launch_conv_fwd(const ConvArgs& a, cudaStream_t st);
+cudaError_t launch_conv_bwd(const ConvArgs& a, cudaStream_t st);
+int conv_bwd_parts(int64_t T);
+
+// Saved-for-backward layout of the chunk forward (all fp32 unless noted).
+struct FwdSaved {
+    int32_t* status;       // device status word
+    ChunkInfo* chunks;     // [NT]
+    int32_t* seq_chunk;    // [N+1] first chunk of each sequence
+    float* gam;            // [T, Hv] in-chunk cumulative gate
+    float* beta;           // [T, Hv]
+    float* W;              // [T, Hv, d]
+    float* U;              // [T, Hv, d]  (U~ from prep, then U)
+    float* S0;             // [NT, Hv, d, d] state at each chunk start
+    float* o;              // [T, Hv, d] core output (before the norm)
+    float* rstd;           // [T, Hv] norm rstd
+};
+
+struct ChunkArgs {
+    bool bf16;
+    int N, NT, hk, hv;
+    int64_t T;
+    const int32_t* cu;
+    const float* qkv;
+    const void *a, *b;
+    const float *A_log, *dt_bias;
+    const float* S_init;
+    const void* z;
+    const float* norm_w;
+    float norm_eps;
+    // forward outputs
+    void* o_out;
+    void* y_out;
+    float* S_final;
+    FwdSaved sv;
+    // backward
+    const void* dy;
+    const float* dS_final;
+    float* dqkv;
+    void *da, *db;
+    float *dA_log, *ddt_bias;
+    void* dz;
+    float* dnorm_w;
+    float* dS_init;
+};
+
+struct BwdScratch {
+    float* dO;       // [T, Hv, d]
+    float* dU;       // [T, Hv, d]
+    float* dS;       // [NT, Hv, d, d] gradient of the state at each chunk end
+    float* dQv;      // [T, Hv, d] per v-head dq^
+    float* dKv;      // [T, Hv, d] per v-head dk^
+    float* dW;       // [T, Hv, d]
+    float* dgam;     // [T, Hv] partial dgamma from the state-facing terms
+    float* dgs;      // [T, Hv] dg (per token)
+    float* nw_part;  // [NT * Hv, d] dnorm_w partials
+};
+
+cudaError_t launch_plan(const int32_t* cu, int N, int64_t T, int NT, FwdSaved sv, cudaStream_t st);
+cudaError_t launch_chunk_fwd(const ChunkArgs& a, cudaStream_t st);
+cudaError_t launch_chunk_bwd(const ChunkArgs& a, const BwdScratch& w, cudaStream_t st);
+
+struct NormArgs {
+    bool bf16;
+    int64_t rows;   // T * Hv
+    const void *o, *z;
+    const float* w;
+    float eps;
+    void* y;
+    float* rstd;
+    const void* dy;
+    void *d_o, *dz;
+    float* dw;
+    float* part;    // [norm_bwd_parts(rows), d]
+};
+cudaError_t launch_norm_fwd(const NormArgs& a, cudaStream_t st);
+cudaError_t launch_norm_bwd(const NormArgs& a, cudaStream_t st);
+int norm_bwd_parts(int64_t rows);
+
+struct StepArgs {
+    bool bf16;
+    int N, hk, hv, C;
+    const void* x;
+    const float* w;
+    void* cs;
+    const void *a, *b;
+    const float *A_log, *dt_bias;
+    const void* z;
+    const float* norm_w;
+    float* S;
+    void *o, *y;
+    float l2_eps, q_scale, norm_eps;
+};
+cudaError_t launch_step(const StepArgs& a, cudaStream_t st);
+
+}  // namespace gdn

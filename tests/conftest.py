@@ -10,3 +10,12 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built():
+    """Build the CUDA library and the oracle once per session (no-op when fresh)."""
+    from gated_deltanet_layer_causal_gb300 import build as b
+    import oracle
+    b.build()
+    oracle.build()
