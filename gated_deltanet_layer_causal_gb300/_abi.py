@@ -27,6 +27,8 @@ GDN_WS_FWD = 0
 GDN_WS_BWD = 1
 GDN_WS_CONV_BWD = 2
 GDN_WS_NORM_BWD = 3
+# rows (tokens * v-heads) gdn_gated_rmsnorm_bwd_noalloc accepts
+GDN_NOALLOC_NORM_BWD_MAX_ROWS = 524288
 
 
 class GdnDims(ctypes.Structure):
@@ -60,6 +62,7 @@ SIGNATURES = {
                       _P, _P, _P, _P, _P, _P, _S, _P],
     "gdn_gated_rmsnorm": [_DP, _P, _P, _P, _P, _P, _P],
     "gdn_gated_rmsnorm_bwd": [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P],
+    "gdn_gated_rmsnorm_bwd_noalloc": [_DP, _P, _P, _P, _P, _P, _P, _P, _P],
     "gdn_recurrent_step": [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "gdn_read_status": [_P, ctypes.POINTER(ctypes.c_int32), _P],
     "gdn_profile_enable": [ctypes.c_int32],

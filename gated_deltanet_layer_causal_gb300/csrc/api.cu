@@ -346,6 +346,28 @@ gdn_status gdn_gated_rmsnorm_bwd(const gdn_dims* dims, const void* o, const void
     return cuda_status(launch_norm_bwd(a, (cudaStream_t)stream));
 }
 
+gdn_status gdn_gated_rmsnorm_bwd_noalloc(const gdn_dims* dims, const void* o, const void* z,
+                                         const float* norm_w, const void* dy, void* d_o,
+                                         void* dz, float* dnorm_w, void* stream) {
+    GDN_TRY(check_dims(dims));
+    GDN_NEED(o && aligned16(o) && z && aligned16(z) && norm_w && aligned16(norm_w));
+    GDN_NEED(dy && aligned16(dy) && d_o && aligned16(d_o) && dz && aligned16(dz) && dnorm_w);
+    if (dims->total_tokens * dims->h_v > (int64_t)norm_bwd_noalloc_max_rows())
+        return GDN_ERR_WORKSPACE;
+    NormArgs a{};
+    a.bf16 = dims->io_dtype == GDN_BF16;
+    a.rows = dims->total_tokens * dims->h_v;
+    a.o = o;
+    a.z = z;
+    a.w = norm_w;
+    a.eps = dims->norm_eps;
+    a.dy = dy;
+    a.d_o = d_o;
+    a.dz = dz;
+    a.dw = dnorm_w;
+    return cuda_status(launch_norm_bwd_noalloc(a, (cudaStream_t)stream));
+}
+
 gdn_status gdn_recurrent_step(const gdn_dims* dims, const void* x_t, const float* conv_w,
                               void* conv_state, const void* a_t, const void* b_t,
                               const float* A_log, const float* dt_bias, const void* z_t,

@@ -106,6 +106,8 @@ struct NormArgs {
 cudaError_t launch_norm_fwd(const NormArgs& a, cudaStream_t st);
 cudaError_t launch_norm_bwd(const NormArgs& a, cudaStream_t st);
 int norm_bwd_parts(int64_t rows);
+cudaError_t launch_norm_bwd_noalloc(const NormArgs& a, cudaStream_t st);
+int norm_bwd_noalloc_max_rows();
 
 struct StepArgs {
     bool bf16;

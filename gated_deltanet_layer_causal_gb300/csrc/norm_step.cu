@@ -12,6 +12,8 @@
 // sequences -- conv-cache update, conv + SiLU, L2 norms, gates, the rank-1
 // state update S <- e^g S + beta (v - e^g S k) k^T, o = S q, and the norm.
 // HBM-bound on the fp32 state, which is read once and written once.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "prof.h"
@@ -118,6 +120,51 @@ static cudaError_t norm_bwd_t(const NormArgs& a, cudaStream_t st) {
 }
 cudaError_t launch_norm_bwd(const NormArgs& a, cudaStream_t st) {
     return a.bf16 ? norm_bwd_t<__nv_bfloat16>(a, st) : norm_bwd_t<float>(a, st);
+}
+
+// ------------------------------------------------------------------ allocation-free backward
+// Scratch of gdn_gated_rmsnorm_bwd_noalloc: the dnorm_w partial sums (one row of
+// kD floats per CTA of kNormRowsPerCta rows) live in this file-scope array
+// instead of a caller workspace.  Every device that loads the library holds it
+// (4 MiB) until the process exits.
+constexpr int kNoAllocParts = 8192;
+static __device__ __align__(256) float g_norm_bwd_scratch[kNoAllocParts * kD];
+
+int norm_bwd_noalloc_max_rows() { return kNoAllocParts * kNormRowsPerCta; }
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+float* g_scratch_dev[kMaxDevices] = {};   // device address of the array, per device
+}  // namespace
+
+// Device address of g_norm_bwd_scratch on the current device.  Host code only
+// sees a host-side stand-in for the array, so the address is looked up once
+// per device (on its first use, with that device current) and cached.
+static cudaError_t norm_bwd_noalloc_scratch(float** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (g_scratch_dev[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_norm_bwd_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_dev[dev] = static_cast<float*>(p);
+    }
+    *out = g_scratch_dev[dev];
+    return cudaSuccess;
+}
+
+cudaError_t launch_norm_bwd_noalloc(const NormArgs& a, cudaStream_t st) {
+    if (a.rows > (int64_t)norm_bwd_noalloc_max_rows()) return cudaErrorInvalidValue;
+    NormArgs b = a;
+    cudaError_t e = norm_bwd_noalloc_scratch(&b.part);
+    if (e != cudaSuccess) return e;
+    // each CTA writes its whole partial row before the column sum reads it,
+    // so the array's previous contents never matter
+    return launch_norm_bwd(b, st);
 }
 
 // ------------------------------------------------------------------ decode step

@@ -162,6 +162,30 @@ gdn_status gdn_gated_rmsnorm_bwd(const gdn_dims* dims, const void* o, const void
                                  const float* norm_w, const void* dy, void* do_out, void* dz_out,
                                  float* dnorm_w_out, void* ws, size_t ws_bytes, void* stream);
 
+/* Allocation-free variant of gdn_gated_rmsnorm_bwd, for callers that cannot
+ * hand the library a workspace: code running inside a serving runtime that
+ * owns all device memory through its own pool and forbids new device
+ * allocations after start-up, plugins that hold no allocator handle, and
+ * loops that must not call cudaMalloc/cudaFree because cudaFree synchronises
+ * the whole device.  Same inputs and outputs as gdn_gated_rmsnorm_bwd (the
+ * caller still owns o, z, norm_w, dy, do_out, dz_out, dnorm_w_out); the
+ * dnorm_w partial sums go to a 4 MiB array built into the library instead of
+ * `ws`.  The pages have no counterpart of this entry point.
+ *  - Size limit: total_tokens * h_v <= GDN_NOALLOC_NORM_BWD_MAX_ROWS, else
+ *    GDN_ERR_WORKSPACE with nothing launched.
+ *  - It calls no cudaMalloc / cudaFree and no allocating routine.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array: calls that overlap on the
+ *    GPU (other streams, other host threads) race on it -- serialise them.
+ *    The array keeps the last call's contents; every partial a call reads it
+ *    first writes itself, so nothing needs clearing between calls. */
+#define GDN_NOALLOC_NORM_BWD_MAX_ROWS 524288
+gdn_status gdn_gated_rmsnorm_bwd_noalloc(const gdn_dims* dims, const void* o, const void* z,
+                                         const float* norm_w, const void* dy, void* do_out,
+                                         void* dz_out, float* dnorm_w_out, void* stream);
+
 /* One recurrent decode step for a batch of num_seqs independent sequences
  * (total_tokens must equal num_seqs): updates conv_state [N, C, 3] and state
  * [N, h_v, d_v, d_k] (fp32) in place and writes y_t [N, h_v, d_v] and, if not
