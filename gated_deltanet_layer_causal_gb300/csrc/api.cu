@@ -67,6 +67,7 @@ FwdSaved carve_fwd(void* ws, const gdn_dims* d, int NT, size_t* bytes) {
     s.status = c.take<int32_t>(kAlign / 4);
     s.chunks = c.take<ChunkInfo>((size_t)NT);
     s.seq_chunk = c.take<int32_t>((size_t)d->num_seqs + 1);
+    s.T = d->total_tokens;
     s.gam = c.take<float>(T * H);
     s.beta = c.take<float>(T * H);
     s.W = c.take<float>(T * H * kD);
@@ -83,6 +84,7 @@ BwdScratch carve_bwd(void* ws, const gdn_dims* d, int NT, int32_t** status, size
     const size_t T = (size_t)d->total_tokens, H = (size_t)d->h_v;
     BwdScratch s;
     *status = c.take<int32_t>(kAlign / 4);
+    s.status = *status;
     s.dO = c.take<float>(T * H * kD);
     s.dU = c.take<float>(T * H * kD);
     s.dQv = c.take<float>(T * H * kD);
@@ -91,7 +93,9 @@ BwdScratch carve_bwd(void* ws, const gdn_dims* d, int NT, int32_t** status, size
     s.dS = c.take<float>((size_t)NT * H * kD * kD);
     s.dgam = c.take<float>(T * H);
     s.dgs = c.take<float>(T * H);
-    s.nw_part = c.take<float>((size_t)NT * H * kD + (size_t)NT * H * 2);
+    // dnorm_w partials [NT*H][kD], gate partials [NT*H][2], column-sum stage [512][kD]
+    s.nw_part = c.take<float>((size_t)NT * H * kD + (size_t)NT * H * 2 + 512 * kD);
+    s.Tm = c.take<float>((size_t)NT * H * 64 * 64);
     *bytes = c.off;
     return s;
 }

@@ -19,6 +19,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "prof.h"
+#include "umma.cuh"
 
 namespace gdn {
 
@@ -27,44 +28,52 @@ constexpr int kL4 = 132, kL8 = 136, kM4 = 68, kM8 = 72;
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
 // gam with padding rows continuing the last valid value (keeps Gam finite)
-__device__ __forceinline__ void load_gam(float* gam, const float* src, const ChunkInfo& ci,
-                                         int hv, int h) {
+__device__ __forceinline__ void load_gam(float* gam, const FwdSaved& sv, const ChunkInfo& ci,
+                                         int h) {
     const int tid = threadIdx.x;
-    if (tid < 64) gam[tid] = src[(int64_t)(ci.start + min(tid, ci.len - 1)) * hv + h];
+    if (tid < 64) gam[tid] = sv.gam[(int64_t)h * sv.T + ci.start + min(tid, ci.len - 1)];
 }
 
 // ------------------------------------------------------------------ B1: local
-// grid (NT, Hv), 256 threads.  Gated-norm backward (dO, dz, dnorm_w partials)
-// and dU_local = P^T dO.
-constexpr size_t kB1Smem = sizeof(float) * (2 * 64 * kL4 + 64 * kL8 + 64 * kM8 + 64);
+// grid (NT, Hv), 256 threads, tcgen05.  Gated-norm backward (dO, dz, dnorm_w
+// partials) on the CUDA cores, then
+//   D1 = K Q^T (64 x 64)  ->  P^T[j][i] = D1[j][i] e^{gam_i-gam_j} [i >= j]
+//   D2 = P^T dO           ->  dU_local (64 x 128)
+// Shared memory: Q, K K-major 32 KB each, dO rows 34 KB, dO^T (rows a,
+// k = token) 32 KB, P^T 16 KB.  Tensor memory: 192 fp32 columns (256 allocated).
+constexpr int kB1Floats = 64 * 128 * 2 + 64 * kL4 + 128 * 64 + 64 * 64;
+constexpr size_t kB1Smem = sizeof(float) * (kB1Floats + 64 + 16) + 64;
 
 template <class IO>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 1)
 bwd_local_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z, const float* norm_w,
                  float norm_eps, const IO* __restrict__ dy, IO* dz, FwdSaved sv, BwdScratch w) {
-    extern __shared__ float sm[];
-    float* Qs = sm;
-    float* Ks = Qs + 64 * kL4;
-    float* dOs = Ks + 64 * kL4;
-    float* Ps = dOs + 64 * kL8;
-    float* gam = Ps + 64 * kM8;
+    extern __shared__ __align__(128) float sm[];
+    float* Qs = sm;                    // [64][128] K-major
+    float* Ks = Qs + 64 * 128;         // [64][128] K-major
+    float* dOr = Ks + 64 * 128;        // [64][kL4] row-major dO
+    float* dOT = dOr + 64 * kL4;       // [128 (a)][64 (i)] K-major
+    float* PT = dOT + 128 * 64;        // [64 (j)][64 (i)] K-major
+    float* gam = PT + 64 * 64;
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(gam + 64 + 16);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
+    __shared__ float4 red[8][32];
     const ChunkInfo ci = sv.chunks[blockIdx.x];
     if (ci.len == 0) return;
     const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
     const int lane = tid & 31, warp = tid >> 5;
     const int C = (2 * hk + hv) * kD;
+    auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
     for (int idx = tid; idx < 64 * 32; idx += 256) {
-        int r = idx >> 5, c4 = (idx & 31) * 4;
-        float4 q4 = zero4(), k4 = zero4();
-        if (r < L) {
-            int64_t t = ci.start + r;
-            q4 = ld4(qkv + t * C + kh * kD + c4);
-            k4 = ld4(qkv + t * C + (int64_t)hk * kD + kh * kD + c4);
-        }
-        st4(Qs + r * kL4 + c4, q4);
-        st4(Ks + r * kL4 + c4, k4);
+        const int r = idx >> 5, c = (idx & 31) * 4;
+        cp_async16(Qs + umma::kidx(r, c, 128), qkv + row(r) * C + kh * kD + c, r < L);
+        cp_async16(Ks + umma::kidx(r, c, 128), qkv + row(r) * C + (int64_t)hk * kD + kh * kD + c,
+                   r < L);
     }
-    load_gam(gam, sv.gam, ci, hv, h);
+    cp_async_commit();
+    load_gam(gam, sv, ci, h);
+    if (warp == 0) umma::tmem_alloc(tslot, 256);
+    if (tid == 0) umma::mbar_init(mbar, 1);
     // norm backward, one warp per row
     float4 wacc = zero4();
     const float4 w4 = z ? ld4(norm_w + lane * 4) : zero4();
@@ -82,258 +91,363 @@ bwd_local_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z, con
             }
             st4(w.dO + off, d4);
         }
-        st4(dOs + r * kL8 + lane * 4, d4);
+        st4(dOr + r * kL4 + lane * 4, d4);
     }
-    if (z) {
-        __shared__ float4 red[8][32];
-        red[warp][lane] = wacc;
-        __syncthreads();
-        if (warp == 0) {
-            float4 s = red[0][lane];
-            for (int i = 1; i < 8; i++) {
-                s.x += red[i][lane].x; s.y += red[i][lane].y;
-                s.z += red[i][lane].z; s.w += red[i][lane].w;
+    if (z) red[warp][lane] = wacc;
+    cp_async_wait<0>();
+    __syncthreads();
+    umma::tf32r_inplace(Qs, 2 * 64 * 128);
+    if (z && warp == 0) {
+        float4 s = red[0][lane];
+        for (int i = 1; i < 8; i++) {
+            s.x += red[i][lane].x; s.y += red[i][lane].y;
+            s.z += red[i][lane].z; s.w += red[i][lane].w;
+        }
+        st4(w.nw_part + ((int64_t)blockIdx.x * hv + h) * kD + lane * 4, s);
+    }
+    for (int idx = tid; idx < 128 * 16; idx += 256) {   // dO^T: lane = a, 4 tokens per store
+        const int a = idx & 127, i4 = idx >> 7;
+        *reinterpret_cast<float4*>(dOT + umma::kidx(a, 4 * i4, 64)) = umma::tf32r(
+            make_float4(dOr[(4 * i4 + 0) * kL4 + a], dOr[(4 * i4 + 1) * kL4 + a],
+                        dOr[(4 * i4 + 2) * kL4 + a], dOr[(4 * i4 + 3) * kL4 + a]));
+    }
+    umma::fence_smem_to_async();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t tD1 = tmem, tD2 = tmem + 64;
+    if (tid == 0) {
+        umma::mma_tf32(tD1, Ks, 128, Qs, 128, 64, 64, 128, false);
+        umma::commit(mbar);
+    }
+    bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+    umma::fence_after_sync();
+    const int win = warp & 3, half = warp >> 2;
+    const int j = win * 16 + lane;     // row of D1 = key index j
+    if (ok) {
+        for (int cc = 0; cc < 32; cc += 16) {
+            float v[16];
+            const int i0 = half * 32 + cc;
+            umma::tmem_ld16(umma::tmem_at(tD1, i0), v);
+            if (lane < 16) {
+#pragma unroll
+                for (int u = 0; u < 16; u += 4) {
+                    const int i = i0 + u;
+                    float4 p;
+                    p.x = (i + 0 >= j) ? v[u + 0] * expf(gam[i + 0] - gam[j]) : 0.f;
+                    p.y = (i + 1 >= j) ? v[u + 1] * expf(gam[i + 1] - gam[j]) : 0.f;
+                    p.z = (i + 2 >= j) ? v[u + 2] * expf(gam[i + 2] - gam[j]) : 0.f;
+                    p.w = (i + 3 >= j) ? v[u + 3] * expf(gam[i + 3] - gam[j]) : 0.f;
+                    *reinterpret_cast<float4*>(PT + umma::kidx(j, i, 64)) = umma::tf32r(p);
+                }
             }
-            st4(w.nw_part + ((int64_t)blockIdx.x * hv + h) * kD + lane * 4, s);
         }
     }
+    umma::fence_smem_to_async();
+    umma::fence_before_sync();
     __syncthreads();
-    {
-        typename Tile<64, 64, 8>::Acc acc;
-        tile_zero<64, 64, 8>(acc);
-        tile_mma<64, 64, kD, 8>(acc, [&](int r, int k) { return Qs[r * kL4 + k]; },
-                                [&](int k, int c) { return Ks[c * kL4 + k]; });
-        tile_each<64, 64, 8>(acc, [&](int r, int c, float& v) {
-            Ps[r * kM8 + c] = (c <= r) ? v * expf(gam[r] - gam[c]) : 0.f;
-        });
+    umma::fence_after_sync();
+    if (ok && tid == 0) {
+        umma::mma_tf32(tD2, PT, 64, dOT, 64, 64, 128, 64, false);
+        umma::commit(mbar);
     }
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
+    umma::fence_after_sync();
+    if (ok) {
+        for (int cc = 0; cc < 64; cc += 16) {
+            float v[16];
+            umma::tmem_ld16(umma::tmem_at(tD2, half * 64 + cc), v);
+            if (lane < 16 && j < L) {
+                float* dst = w.dU + ((int64_t)(ci.start + j) * hv + h) * kD + half * 64 + cc;
+#pragma unroll
+                for (int u = 0; u < 16; u += 4)
+                    st4(dst + u, make_float4(v[u], v[u + 1], v[u + 2], v[u + 3]));
+            }
+        }
+    } else if (tid == 0) {
+        atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
+    }
+    umma::fence_before_sync();
     __syncthreads();
-    typename Tile<64, kD, 8>::Acc acc;
-    tile_zero<64, kD, 8>(acc);
-    tile_mma<64, kD, 64, 8>(acc, [&](int j, int i) { return Ps[i * kM8 + j]; },
-                            [&](int i, int a) { return dOs[i * kL8 + a]; });
-    tile_each2<64, kD, 8>(acc, [&](int r, int c, float& v0, float& v1) {
-        if (r < L)
-            *reinterpret_cast<float2*>(w.dU + ((int64_t)(ci.start + r) * hv + h) * kD + c) =
-                make_float2(v0, v1);
-    });
+    if (warp == 0) umma::tmem_free(tmem, 256);
 }
 
 // ------------------------------------------------------------------ B2: reverse state pass
-// grid (d_v / 32, Hv, N), 128 threads.  Carries a 32-row slice of dS (as
-// dS^T[b][a] in the accumulators) from the last chunk of the sequence to the
-// first; stores dS at every chunk end and completes dU.
-constexpr int kSl = 32, kLdS = kSl + 8;
-constexpr size_t kB2Smem = sizeof(float) * (2 * 64 * kL8 + 2 * 64 * kLdS + kD * kLdS + 3 * 64);
+// grid (d_v / 64, Hv, N), 256 threads, one CTA per SM.  Carries a 64-row slice
+// of dS (as dS^T[b][a] in the accumulators) from the last chunk of the
+// sequence to the first; stores dS at every chunk end and completes dU.  The
+// previous chunk's tiles are fetched with cp.async as soon as their buffers
+// are free: dO / dU_local / gates into the other half of a double buffer at
+// the top of the iteration, K after its product, Q and W after theirs.
+constexpr int kSl = 64, kLdS = kSl + 8;
+constexpr size_t kB2Smem =
+    sizeof(float) * (64 * kL4 + 2 * 64 * kL8 + 4 * 64 * kLdS + kD * kLdS + 2 * 64 + 2 * 64);
 
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(256, 1)
 bwd_state_kernel(const float* __restrict__ qkv, int hk, int hv, const float* dS_final,
                  float* dS_init, FwdSaved sv, BwdScratch w) {
     extern __shared__ float sm[];
-    float* X1 = sm;                    // K, then Q
-    float* X2 = X1 + 64 * kL8;         // W
-    float* dOs = X2 + 64 * kL8;        // [64][kLdS]
-    float* dUs = dOs + 64 * kLdS;      // [64][kLdS]
-    float* dSt = dUs + 64 * kLdS;      // [128][kLdS]
-    float* gam = dSt + kD * kLdS;
-    float* fk = gam + 64;
+    float* Kb = sm;                    // [64][kL4]  K
+    float* Qb = Kb + 64 * kL4;         // [64][kL8]  Q
+    float* Wb = Qb + 64 * kL8;         // [64][kL8]  W
+    float* dOs = Wb + 64 * kL8;        // [2][64][kLdS]
+    float* dUs = dOs + 2 * 64 * kLdS;  // [2][64][kLdS]
+    float* dSt = dUs + 2 * 64 * kLdS;  // [128][kLdS]
+    float* gam = dSt + kD * kLdS;      // [2][64]
+    float* fk = gam + 2 * 64;
     float* eg = fk + 64;
     const int sl = blockIdx.x, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
     const int a0 = sl * kSl, kh = h / (hv / hk);
     const int C = (2 * hk + hv) * kD;
     const int64_t sbase = ((int64_t)n * hv + h) * kD * kD;
-    typename Tile<kD, kSl, 4>::Acc sacc;
-    tile_each<kD, kSl, 4>(sacc, [&](int b, int a, float& v) {
+    auto row = [&](const ChunkInfo& c, int r) { return (int64_t)c.start + min(r, c.len - 1); };
+    auto issue_small = [&](const ChunkInfo& c, int slot) {
+        for (int idx = tid; idx < 64 * kSl / 4; idx += 256) {
+            const int r = idx / (kSl / 4), c4 = (idx % (kSl / 4)) * 4;
+            const int64_t off = (row(c, r) * hv + h) * kD + a0 + c4;
+            cp_async16(dOs + (slot * 64 + r) * kLdS + c4, w.dO + off, r < c.len);
+            cp_async16(dUs + (slot * 64 + r) * kLdS + c4, w.dU + off, r < c.len);
+        }
+        if (tid < 64)
+            cp_async4(gam + slot * 64 + tid, sv.gam + (int64_t)h * sv.T + row(c, tid), true);
+        cp_async_commit();
+    };
+    auto issue_k = [&](const ChunkInfo& c) {
+        for (int idx = tid; idx < 64 * 32; idx += 256) {
+            const int r = idx >> 5, c4 = (idx & 31) * 4;
+            cp_async16(Kb + r * kL4 + c4, qkv + row(c, r) * C + (int64_t)hk * kD + kh * kD + c4,
+                       r < c.len);
+        }
+        cp_async_commit();
+    };
+    auto issue_qw = [&](const ChunkInfo& c) {
+        for (int idx = tid; idx < 64 * 32; idx += 256) {
+            const int r = idx >> 5, c4 = (idx & 31) * 4;
+            cp_async16(Qb + r * kL8 + c4, qkv + row(c, r) * C + kh * kD + c4, r < c.len);
+            cp_async16(Wb + r * kL8 + c4, sv.W + (row(c, r) * hv + h) * kD + c4, r < c.len);
+        }
+        cp_async_commit();
+    };
+    typename Tile<kD, kSl, 8>::Acc sacc;
+    tile_each<kD, kSl, 8>(sacc, [&](int b, int a, float& v) {
         v = dS_final ? dS_final[sbase + (int64_t)(a0 + a) * kD + b] : 0.f;
         dSt[b * kLdS + a] = v;
     });
     const int c0 = sv.seq_chunk[n], c1 = sv.seq_chunk[n + 1];
+    if (c0 < c1) {
+        const ChunkInfo last = sv.chunks[c1 - 1];
+        issue_k(last);
+        issue_qw(last);
+        issue_small(last, 0);
+    }
     for (int ci = c1 - 1; ci >= c0; ci--) {
+        const int slot = (c1 - 1 - ci) & 1;
         const ChunkInfo info = sv.chunks[ci];
         const int L = info.len;
-        __syncthreads();
-        for (int idx = tid; idx < 64 * 32; idx += 128) {
-            int r = idx >> 5, c4 = (idx & 31) * 4;
-            float4 k4 = zero4(), w4 = zero4();
-            if (r < L) {
-                int64_t t = info.start + r;
-                k4 = ld4(qkv + t * C + (int64_t)hk * kD + kh * kD + c4);
-                w4 = ld4(sv.W + (t * hv + h) * kD + c4);
-            }
-            st4(X1 + r * kL8 + c4, k4);
-            st4(X2 + r * kL8 + c4, w4);
-        }
-        for (int idx = tid; idx < 64 * kSl / 4; idx += 128) {
-            int r = idx / (kSl / 4), c4 = (idx % (kSl / 4)) * 4;
-            float4 o4 = zero4(), u4 = zero4();
-            if (r < L) {
-                int64_t off = ((int64_t)(info.start + r) * hv + h) * kD + a0 + c4;
-                o4 = ld4(w.dO + off);
-                u4 = ld4(w.dU + off);
-            }
-            st4(dOs + r * kLdS + c4, o4);
-            st4(dUs + r * kLdS + c4, u4);
-        }
-        load_gam(gam, sv.gam, info, hv, h);
-        // gradient of the state at this chunk's end
+        const bool more = ci - 1 >= c0;
+        const ChunkInfo prev = more ? sv.chunks[ci - 1] : info;
+        cp_async_wait<0>();
+        __syncthreads();                    // everything for chunk ci has landed
+        if (more) issue_small(prev, slot ^ 1);
+        float* dOc = dOs + slot * 64 * kLdS;
+        float* dUc = dUs + slot * 64 * kLdS;
+        const float* gc = gam + slot * 64;
+        // gradient of the state at this chunk's end, stored transposed: dS^T[b][a]
         const int64_t obase = ((int64_t)ci * hv + h) * kD * kD;
-        tile_each2<kD, kSl, 4>(sacc, [&](int b, int a, float& v0, float& v1) {
-            w.dS[obase + (int64_t)(a0 + a) * kD + b] = v0;
-            w.dS[obase + (int64_t)(a0 + a + 1) * kD + b] = v1;
+        tile_each2<kD, kSl, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
+            *reinterpret_cast<float2*>(w.dS + obase + (int64_t)b * kD + a0 + a) =
+                make_float2(v0, v1);
         });
-        __syncthreads();
         if (tid < 64) {
-            fk[tid] = tid < L ? expf(gam[L - 1] - gam[tid]) : 0.f;
-            eg[tid] = tid < L ? expf(gam[tid]) : 0.f;
+            fk[tid] = tid < L ? expf(gc[L - 1] - gc[tid]) : 0.f;
+            eg[tid] = tid < L ? expf(gc[tid]) : 0.f;
         }
         __syncthreads();
         // dU = dU_local + K~ dS^T  (64 x slice)
-        typename Tile<64, kSl, 4>::Acc uacc;
-        tile_zero<64, kSl, 4>(uacc);
-        tile_mma<64, kSl, kD, 4>(uacc, [&](int i, int b) { return fk[i] * X1[i * kL8 + b]; },
+        typename Tile<64, kSl, 8>::Acc uacc;
+        tile_zero<64, kSl, 8>(uacc);
+        tile_mma<64, kSl, kD, 8>(uacc, [&](int i, int b) { return fk[i] * Kb[i * kL4 + b]; },
                                  [&](int b, int a) { return dSt[b * kLdS + a]; });
-        __syncthreads();   // X1 (K) no longer read: load Q over it
-        for (int idx = tid; idx < 64 * 32; idx += 128) {
-            int r = idx >> 5, c4 = (idx & 31) * 4;
-            float4 q4 = zero4();
-            if (r < L) q4 = ld4(qkv + (int64_t)(info.start + r) * C + kh * kD + c4);
-            st4(X1 + r * kL8 + c4, q4);
-        }
-        tile_each<64, kSl, 4>(uacc, [&](int i, int a, float& v) {
-            float u = i < L ? dUs[i * kLdS + a] + v : 0.f;
-            dUs[i * kLdS + a] = u;
+        __syncthreads();                    // K and dS^T reads done
+        if (more) issue_k(prev);
+        tile_each<64, kSl, 8>(uacc, [&](int i, int a, float& v) {
+            const float u = i < L ? dUc[i * kLdS + a] + v : 0.f;
+            dUc[i * kLdS + a] = u;
             if (i < L) w.dU[((int64_t)(info.start + i) * hv + h) * kD + a0 + a] = u;
         });
         __syncthreads();
         // dS^T = e^{gam_L} dS^T + Q~^T dO - W^T dU
-        const float dl = expf(gam[L - 1]);
-        tile_each<kD, kSl, 4>(sacc, [&](int, int, float& v) { v *= dl; });
-        tile_mma<kD, kSl, 64, 4>(sacc, [&](int b, int i) { return eg[i] * X1[i * kL8 + b]; },
-                                 [&](int i, int a) { return dOs[i * kLdS + a]; });
-        tile_mma<kD, kSl, 64, 4>(sacc, [&](int b, int i) { return -X2[i * kL8 + b]; },
-                                 [&](int i, int a) { return dUs[i * kLdS + a]; });
-        tile_each<kD, kSl, 4>(sacc, [&](int b, int a, float& v) { dSt[b * kLdS + a] = v; });
+        const float dl = expf(gc[L - 1]);
+        tile_each<kD, kSl, 8>(sacc, [&](int, int, float& v) { v *= dl; });
+        tile_mma<kD, kSl, 64, 8>(sacc, [&](int b, int i) { return eg[i] * Qb[i * kL8 + b]; },
+                                 [&](int i, int a) { return dOc[i * kLdS + a]; });
+        tile_mma<kD, kSl, 64, 8>(sacc, [&](int b, int i) { return -Wb[i * kL8 + b]; },
+                                 [&](int i, int a) { return dUc[i * kLdS + a]; });
+        __syncthreads();                    // Q, W, dO, dU reads done
+        if (more) issue_qw(prev);
+        tile_each<kD, kSl, 8>(sacc, [&](int b, int a, float& v) { dSt[b * kLdS + a] = v; });
     }
     if (dS_init)
-        tile_each<kD, kSl, 4>(sacc, [&](int b, int a, float& v) {
+        tile_each<kD, kSl, 8>(sacc, [&](int b, int a, float& v) {
             dS_init[sbase + (int64_t)(a0 + a) * kD + b] = v;
         });
 }
 
 // ------------------------------------------------------------------ B3a: state-facing terms
-// grid (NT, Hv), 256 threads.
-//   X = dO S0 -> dQ partial e^gam X, dgam_i += e^{gam_i} X_i . Q_i
-//   dW = -dU S0
-//   dK~ = U dS -> dK partial fk dK~, dgam_j -= Z_j, dgam_L += sum Z + e^{gam_L}<dS, S0>
-constexpr size_t kB3aSmem = sizeof(float) * (kD * kL8 + 2 * 64 * kL4 + 3 * 64 + 2 * 64 + 8);
+// grid (NT, Hv), 256 threads, tcgen05.  Per chunk:
+//   [X; Y] = [dO; dU] S0     (one M=128, N=128, K=128 MMA; X = dO S0, Y = dU S0)
+//   dK~    = U dS            (M=64, N=128, K=128)
+// then dQ partial = e^gam X, dW = -Y, dK partial = fk dK~, and the dgam terms
+//   dgam_i += e^{gam_i} X_i . Q_i,  dgam_j -= Z_j = fk_j dK~_j . K_j,
+//   dgam_{L-1} += sum_j Z_j + e^{gam_L} <dS, S0>.
+// Shared memory (K-major core layout): [dO; dU] 64 KB, S0^T 64 KB, dS^T 64 KB,
+// U 32 KB.  Tensor memory: 256 fp32 columns.
+constexpr int kSfFloats = 128 * 128 * 3 + 64 * 128;
+constexpr size_t kB3aSmem = sizeof(float) * (kSfFloats + 64 * 3 + 2 * 128 + 16) + 64;
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 1)
 bwd_sfacing_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScratch w) {
-    extern __shared__ float sm[];
-    float* Ss = sm;                    // [128][kL8]  S0, then dS
-    float* A1 = Ss + kD * kL8;         // [64][kL4]   dO, then U
-    float* A2 = A1 + 64 * kL4;         // [64][kL4]   dU
-    float* gam = A2 + 64 * kL4;
-    float* eg = gam + 64;
+    extern __shared__ __align__(128) float sm[];
+    float* A1 = sm;                      // [128][128] K-major: rows 0-63 dO, 64-127 dU
+    float* S0T = A1 + 128 * 128;         // [128 (b)][128 (a)] K-major
+    float* DST = S0T + 128 * 128;        // [128 (b)][128 (a)] K-major
+    float* A2 = DST + 128 * 128;         // [64][128] K-major: U
+    float* eg = A2 + 64 * 128;
     float* fk = eg + 64;
-    float* part = fk + 64;             // [2][64]
-    float* red = part + 128;           // [8]
+    float* gam = fk + 64;
+    float* rpart = gam + 64;             // [2][128]
+    float* red = rpart + 2 * 128;        // [16]
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(red + 16);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
     const ChunkInfo ci = sv.chunks[blockIdx.x];
     if (ci.len == 0) return;
     const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
+    const int warp = tid >> 5, lane = tid & 31;
     const int C = (2 * hk + hv) * kD;
     const int64_t sb = ((int64_t)blockIdx.x * hv + h) * kD * kD;
-    for (int idx = tid; idx < kD * 32; idx += 256) {
-        int r = idx >> 5, c4 = (idx & 31) * 4;
-        st4(Ss + r * kL8 + c4, ld4(sv.S0 + sb + r * kD + c4));
-    }
+    auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
+    // ---- stage operands
     for (int idx = tid; idx < 64 * 32; idx += 256) {
-        int r = idx >> 5, c4 = (idx & 31) * 4;
-        float4 o4 = zero4(), u4 = zero4();
-        if (r < L) {
-            int64_t off = ((int64_t)(ci.start + r) * hv + h) * kD + c4;
-            o4 = ld4(w.dO + off);
-            u4 = ld4(w.dU + off);
-        }
-        st4(A1 + r * kL4 + c4, o4);
-        st4(A2 + r * kL4 + c4, u4);
+        const int r = idx >> 5, c = (idx & 31) * 4;
+        const int64_t off = (row(r) * hv + h) * kD + c;
+        cp_async16(A1 + umma::kidx(r, c, 128), w.dO + off, r < L);
+        cp_async16(A1 + umma::kidx(64 + r, c, 128), w.dU + off, r < L);
+        cp_async16(A2 + umma::kidx(r, c, 128), sv.U + off, r < L);
     }
-    load_gam(gam, sv.gam, ci, hv, h);
+    for (int idx = tid; idx < 128 * 32; idx += 256) {     // dS^T rows b, straight
+        const int b = idx >> 5, c = (idx & 31) * 4;
+        cp_async16(DST + umma::kidx(b, c, 128), w.dS + sb + (int64_t)b * kD + c, true);
+    }
+    cp_async_commit();
+    {   // S0 [a][b] -> S0^T rows b: lane = b, four rows a per 16-byte store
+        const float* S0 = sv.S0 + sb;
+        for (int idx = tid; idx < 128 * 32; idx += 256) {
+            const int b = idx & 127, a4 = idx >> 7;
+            float4 v;
+            v.x = S0[(int64_t)(4 * a4 + 0) * kD + b];
+            v.y = S0[(int64_t)(4 * a4 + 1) * kD + b];
+            v.z = S0[(int64_t)(4 * a4 + 2) * kD + b];
+            v.w = S0[(int64_t)(4 * a4 + 3) * kD + b];
+            *reinterpret_cast<float4*>(S0T + umma::kidx(b, 4 * a4, 128)) = v;
+        }
+    }
+    load_gam(gam, sv, ci, h);
+    if (warp == 0) umma::tmem_alloc(tslot, 256);
+    if (tid == 0) umma::mbar_init(mbar, 1);
+    cp_async_wait<0>();
     __syncthreads();
+    {   // <dS, S0> over the staged copies (same layout, same index), before rounding
+        float dot = 0.f;
+        for (int i = tid; i < 128 * 128; i += 256) dot += S0T[i] * DST[i];
+        dot = warp_sum(dot);
+        if (lane == 0) red[warp] = dot;
+    }
+    __syncthreads();
+    umma::tf32r_inplace(A1, kSfFloats);
+    umma::fence_smem_to_async();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    if (tid == 0) {
+        umma::mma_tf32(tmem, A1, 128, S0T, 128, 128, 128, 128, false);
+        umma::mma_tf32(tmem + 128, A2, 128, DST, 128, 64, 128, 128, false);
+        umma::commit(mbar);
+    }
     if (tid < 64) {
         eg[tid] = tid < L ? expf(gam[tid]) : 0.f;
         fk[tid] = tid < L ? expf(gam[L - 1] - gam[tid]) : 0.f;
     }
-    __syncthreads();
-    float dg_row[2] = {0.f, 0.f};   // this thread's share of dgam (rows tid, tid-64 unused)
-    typename Tile<64, kD, 8>::Acc acc;
-    // X = dO S0
-    tile_zero<64, kD, 8>(acc);
-    tile_mma<64, kD, kD, 8>(acc, [&](int i, int a) { return A1[i * kL4 + a]; },
-                            [&](int a, int b) { return Ss[a * kL8 + b]; });
-    tile_each2<64, kD, 8>(acc, [&](int i, int b, float& v0, float& v1) {
-        if (i < L)
-            *reinterpret_cast<float2*>(w.dQv + ((int64_t)(ci.start + i) * hv + h) * kD + b) =
-                make_float2(eg[i] * v0, eg[i] * v1);
-    });
-    tile_rowpart<64, kD, 8>(acc, [&](int i, int b, float v) {
-        return i < L ? eg[i] * v * qkv[(int64_t)(ci.start + i) * C + kh * kD + b] : 0.f;
-    }, part);
-    __syncthreads();
-    if (tid < 64) dg_row[0] = part[tid] + part[64 + tid];
-    // dW = -dU S0
-    tile_zero<64, kD, 8>(acc);
-    tile_mma<64, kD, kD, 8>(acc, [&](int i, int a) { return A2[i * kL4 + a]; },
-                            [&](int a, int b) { return Ss[a * kL8 + b]; });
-    tile_each2<64, kD, 8>(acc, [&](int i, int b, float& v0, float& v1) {
-        if (i < L)
-            *reinterpret_cast<float2*>(w.dW + ((int64_t)(ci.start + i) * hv + h) * kD + b) =
-                make_float2(-v0, -v1);
-    });
-    __syncthreads();
-    // swap in dS (and take <dS, S0> on the way) and U
-    float dot = 0.f;
-    const float* dSg = w.dS + sb;
-    for (int idx = tid; idx < kD * 32; idx += 256) {
-        int r = idx >> 5, c4 = (idx & 31) * 4;
-        float4 s4 = ld4(Ss + r * kL8 + c4), d4 = ld4(dSg + r * kD + c4);
-        dot += s4.x * d4.x + s4.y * d4.y + s4.z * d4.z + s4.w * d4.w;
-        st4(Ss + r * kL8 + c4, d4);
+    const bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+    umma::fence_after_sync();
+    if (!ok) {
+        if (tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
+    } else {
+        const int half = warp >> 2, win = warp & 3;
+        const int c0 = half * 64;
+        // D1: rows 0..127 in lanes 0..127
+        {
+            const int r = win * 32 + lane;
+            float part = 0.f;
+            for (int cc = 0; cc < 64; cc += 16) {
+                float v[16];
+                umma::tmem_ld16(umma::tmem_at(tmem, c0 + cc), v);
+                if (r < 64) {
+                    const int i = r;
+                    if (i < L) {
+                        float* dst = w.dQv + (row(i) * hv + h) * kD + c0 + cc;
+                        const float* q = qkv + row(i) * C + kh * kD + c0 + cc;
+#pragma unroll
+                        for (int u = 0; u < 16; u += 4) {
+                            const float4 q4 = ld4(q + u);
+                            part += v[u] * q4.x + v[u + 1] * q4.y + v[u + 2] * q4.z +
+                                    v[u + 3] * q4.w;
+                            st4(dst + u, make_float4(eg[i] * v[u], eg[i] * v[u + 1],
+                                                     eg[i] * v[u + 2], eg[i] * v[u + 3]));
+                        }
+                    }
+                } else {
+                    const int i = r - 64;
+                    if (i < L) {
+                        float* dst = w.dW + (row(i) * hv + h) * kD + c0 + cc;
+#pragma unroll
+                        for (int u = 0; u < 16; u += 4)
+                            st4(dst + u, make_float4(-v[u], -v[u + 1], -v[u + 2], -v[u + 3]));
+                    }
+                }
+            }
+            if (r < 64) rpart[half * 128 + r] = r < L ? eg[r] * part : 0.f;
+        }
+        // D2 (M = 64): row j = 16 * win + lane for lanes 0..15
+        {
+            const int j = win * 16 + lane;
+            float part = 0.f;
+            for (int cc = 0; cc < 64; cc += 16) {
+                float v[16];
+                umma::tmem_ld16(umma::tmem_at(tmem + 128, c0 + cc), v);
+                if (lane < 16 && j < L) {
+                    float* dst = w.dKv + (row(j) * hv + h) * kD + c0 + cc;
+                    const float* k = qkv + row(j) * C + (int64_t)hk * kD + kh * kD + c0 + cc;
+#pragma unroll
+                    for (int u = 0; u < 16; u += 4) {
+                        const float4 k4 = ld4(k + u);
+                        part += v[u] * k4.x + v[u + 1] * k4.y + v[u + 2] * k4.z + v[u + 3] * k4.w;
+                        st4(dst + u, make_float4(fk[j] * v[u], fk[j] * v[u + 1],
+                                                 fk[j] * v[u + 2], fk[j] * v[u + 3]));
+                    }
+                }
+            }
+            if (lane < 16) rpart[half * 128 + 64 + j] = j < L ? fk[j] * part : 0.f;
+        }
     }
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-        int r = idx >> 5, c4 = (idx & 31) * 4;
-        float4 u4 = zero4();
-        if (r < L) u4 = ld4(sv.U + ((int64_t)(ci.start + r) * hv + h) * kD + c4);
-        st4(A1 + r * kL4 + c4, u4);
-    }
-    dot = warp_sum(dot);
-    if ((tid & 31) == 0) red[tid >> 5] = dot;
+    umma::fence_before_sync();
     __syncthreads();
-    // dK~ = U dS
-    tile_zero<64, kD, 8>(acc);
-    tile_mma<64, kD, kD, 8>(acc, [&](int j, int a) { return A1[j * kL4 + a]; },
-                            [&](int a, int b) { return Ss[a * kL8 + b]; });
-    tile_each2<64, kD, 8>(acc, [&](int j, int b, float& v0, float& v1) {
-        if (j < L)
-            *reinterpret_cast<float2*>(w.dKv + ((int64_t)(ci.start + j) * hv + h) * kD + b) =
-                make_float2(fk[j] * v0, fk[j] * v1);
-    });
-    tile_rowpart<64, kD, 8>(acc, [&](int j, int b, float v) {
-        return j < L ? fk[j] * v * qkv[(int64_t)(ci.start + j) * C + (int64_t)hk * kD + kh * kD + b]
-                     : 0.f;
-    }, part);
-    __syncthreads();
-    if (tid < 64) {
-        float z = part[tid] + part[64 + tid];   // Z_j
-        dg_row[1] = -z;
-        part[tid] = z;                          // reuse for the sum over j
-    }
-    __syncthreads();
+    if (warp == 0) umma::tmem_free(tmem, 256);
+    if (!ok) return;
     if (tid < 64 && tid < L) {
-        float g = dg_row[0] + dg_row[1];
+        float g = (rpart[tid] + rpart[128 + tid]) - (rpart[64 + tid] + rpart[192 + tid]);
         if (tid == L - 1) {
             float zs = 0.f, dd = 0.f;
-            for (int j = 0; j < 64; j++) zs += part[j];
+            for (int j = 0; j < L; j++) zs += rpart[64 + j] + rpart[192 + j];
             for (int i = 0; i < 8; i++) dd += red[i];
             g += zs + expf(gam[L - 1]) * dd;
         }
@@ -341,242 +455,471 @@ bwd_sfacing_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, B
     }
 }
 
-// ------------------------------------------------------------------ B3b: chunk-local terms
-// grid (NT, Hv), 256 threads.  Finishes dQ, dK (per v-head), dV, dbeta, dgam,
-// then dg, da, db and the per-chunk dA_log / ddt_bias partials.
-constexpr size_t kB3bSmem =
-    sizeof(float) * (4 * 64 * kL8 + 3 * 64 * kM4 + 64 * kM8 + 8 * 64 + 2 * 64 + 4 * 64 + 16);
+// ------------------------------------------------------------------ B3b: P / dP terms
+// grid (NT, Hv), 256 threads, tcgen05.
+//   D_qk = Q K^T, D_kk = K K^T, D_dou = dO U^T          (64 x 64 each)
+//   dPm = D_dou (.) Gam (.) [i>=j];  R = dPm (.) D_qk
+//     dgam_i += sum_j R_ij, dgam_j -= sum_i R_ij
+//   A = beta_i Gam_ij D_kk (j < i);  T = (I + A)^-1      (CUDA cores; saved)
+//   D_dq = dPm K,  D_dk = dPm^T Q                        (64 x 128 each)
+// added to the per-v-head dQ / dK partials.
+constexpr int kDpFloats = 4 * 64 * 128 + 2 * 64 * 64 + 64 * 65 + 2 * 64 * kM4;
+constexpr size_t kDpSmem = sizeof(float) * (kDpFloats + 3 * 64 + 2 * 64 + 16) + 64;
 
-template <class IO>
 __global__ void __launch_bounds__(256, 1)
-bwd_local2_kernel(const float* __restrict__ qkv, const IO* __restrict__ av,
-                  const IO* __restrict__ bv, const float* __restrict__ A_log,
-                  const float* __restrict__ dt_bias, int hk, int hv, float* __restrict__ dqkv,
-                  IO* __restrict__ da, IO* __restrict__ db, float* __restrict__ gate_part,
-                  FwdSaved sv, BwdScratch w) {
-    extern __shared__ float sm[];
-    float* B0 = sm;                    // Q, then V      [64][kL8]
-    float* B1 = B0 + 64 * kL8;         // K              [64][kL8]
-    float* B2 = B1 + 64 * kL8;         // dO, then dW    [64][kL8]
-    float* B3 = B2 + 64 * kL8;         // U, then dU     [64][kL8]
-    float* M0 = B3 + 64 * kL8;         // GamKK          [64][kM4]
-    float* M1 = M0 + 64 * kM4;         // dPm, then T    [64][kM4]
-    float* M2 = M1 + 64 * kM4;         // A, dT, dKK     [64][kM4]
-    float* M3 = M2 + 64 * kM4;         // Y              [64][kM8]
-    float* gam = M3 + 64 * kM8;
-    float* eg = gam + 64;
-    float* bet = eg + 64;
-    float* be = bet + 64;
-    float* dgs = be + 64;              // dgam accumulated here
-    float* dbs = dgs + 64;             // dbeta accumulated here
-    float* rk = dbs + 64;              // scratch row values
-    float* sc = rk + 64;               // scratch
-    float* rpart = sc + 64;            // [2][64]
-    float* cpart = rpart + 128;        // [4][64]
-    float* red = cpart + 256;          // [16]
+bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScratch w) {
+    extern __shared__ __align__(128) float sm[];
+    float* Qs = sm;                    // [64][128] K-major   (later Q^T: [128][64])
+    float* Ks = Qs + 64 * 128;         // [64][128] K-major   (later K^T: [128][64])
+    float* dOs = Ks + 64 * 128;        // [64][128] K-major
+    float* Us = dOs + 64 * 128;        // [64][128] K-major
+    float* dPR = Us + 64 * 128;        // [64 (i)][64 (j)] K-major
+    float* dPC = dPR + 64 * 64;        // [64 (j)][64 (i)] K-major
+    float* Rm = dPC + 64 * 64;         // [64][65] row-major R
+    float* As = Rm + 64 * 65;          // [64][kM4] row-major A
+    float* Tr = As + 64 * kM4;         // [64][kM4] row-major T
+    float* gam = Tr + 64 * kM4;
+    float* bet = gam + 64;
+    float* dgl = bet + 64;             // local dgam
+    float* rpart = dgl + 64;           // [2][64]
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(rpart + 128 + 16);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
     const ChunkInfo ci = sv.chunks[blockIdx.x];
     if (ci.len == 0) return;
     const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
+    const int warp = tid >> 5, lane = tid & 31;
     const int C = (2 * hk + hv) * kD;
-    auto tok = [&](int i) { return (int64_t)(ci.start + i); };
-    auto vrow = [&](int i) { return (tok(i) * hv + h) * kD; };
-    // ---- phase 1: Q, K, dO, U
+    auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
+    const float* qb = qkv + kh * kD;
+    const float* kb = qkv + (int64_t)hk * kD + kh * kD;
     for (int idx = tid; idx < 64 * 32; idx += 256) {
-        int r = idx >> 5, c4 = (idx & 31) * 4;
-        float4 q4 = zero4(), k4 = zero4(), o4 = zero4(), u4 = zero4();
-        if (r < L) {
-            q4 = ld4(qkv + tok(r) * C + kh * kD + c4);
-            k4 = ld4(qkv + tok(r) * C + (int64_t)hk * kD + kh * kD + c4);
-            o4 = ld4(w.dO + vrow(r) + c4);
-            u4 = ld4(sv.U + vrow(r) + c4);
-        }
-        st4(B0 + r * kL8 + c4, q4);
-        st4(B1 + r * kL8 + c4, k4);
-        st4(B2 + r * kL8 + c4, o4);
-        st4(B3 + r * kL8 + c4, u4);
+        const int r = idx >> 5, c = (idx & 31) * 4;
+        const int64_t vo = (row(r) * hv + h) * kD + c;
+        cp_async16(Qs + umma::kidx(r, c, 128), qb + row(r) * C + c, r < L);
+        cp_async16(Ks + umma::kidx(r, c, 128), kb + row(r) * C + c, r < L);
+        cp_async16(dOs + umma::kidx(r, c, 128), w.dO + vo, r < L);
+        cp_async16(Us + umma::kidx(r, c, 128), sv.U + vo, r < L);
     }
-    load_gam(gam, sv.gam, ci, hv, h);
+    cp_async_commit();
+    load_gam(gam, sv, ci, h);
+    if (tid < 64) bet[tid] = tid < L ? sv.beta[(int64_t)h * sv.T + ci.start + tid] : 0.f;
+    if (warp == 0) umma::tmem_alloc(tslot, 512);
+    if (tid == 0) umma::mbar_init(mbar, 1);
+    cp_async_wait<0>();
+    __syncthreads();
+    umma::tf32r_inplace(Qs, 4 * 64 * 128);   // Q, K, dO, U
+    umma::fence_smem_to_async();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t tQK = tmem, tKK = tmem + 64, tDOU = tmem + 128, tDQ = tmem + 256,
+                   tDK = tmem + 384;
+    if (tid == 0) {
+        umma::mma_tf32(tQK, Qs, 128, Ks, 128, 64, 64, 128, false);
+        umma::mma_tf32(tKK, Ks, 128, Ks, 128, 64, 64, 128, false);
+        umma::mma_tf32(tDOU, dOs, 128, Us, 128, 64, 64, 128, false);
+        umma::commit(mbar);
+    }
+    bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+    umma::fence_after_sync();
+    const int win = warp & 3, half = warp >> 2;
+    const int i = win * 16 + lane;     // D row (lanes 0..15)
+    if (ok) {
+        float rsum = 0.f;
+        for (int cc = 0; cc < 32; cc += 16) {
+            float qk[16], kk[16], du[16];
+            const int j0 = half * 32 + cc;
+            umma::tmem_ld16(umma::tmem_at(tQK, j0), qk);
+            umma::tmem_ld16(umma::tmem_at(tKK, j0), kk);
+            umma::tmem_ld16(umma::tmem_at(tDOU, j0), du);
+            if (lane < 16) {
+#pragma unroll
+                for (int u = 0; u < 16; u += 4) {
+                    float dp[4];
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const int j = j0 + u + q;
+                        const float gm = (j <= i) ? expf(gam[i] - gam[j]) : 0.f;
+                        dp[q] = du[u + q] * gm;
+                        const float R = dp[q] * qk[u + q];
+                        rsum += R;
+                        Rm[i * 65 + j] = R;
+                        As[i * kM4 + j] = (j < i) ? bet[i] * gm * kk[u + q] : 0.f;
+                        dPC[umma::kidx(j, i, 64)] = umma::tf32r(dp[q]);
+                    }
+                    *reinterpret_cast<float4*>(dPR + umma::kidx(i, j0 + u, 64)) =
+                        umma::tf32r(make_float4(dp[0], dp[1], dp[2], dp[3]));
+                }
+            }
+        }
+        if (lane < 16) rpart[half * 64 + i] = rsum;
+    }
+    __syncthreads();
+    // the first MMAs are done: Q^T and K^T (rows b, k = token) replace dO and U
+    float* QT = dOs;
+    float* KT = Us;
+    for (int idx = tid; idx < 128 * 16; idx += 256) {
+        const int bcol = idx & 127, j4 = idx >> 7;
+        float4 q4, k4;
+        q4.x = 4 * j4 + 0 < L ? qb[row(4 * j4 + 0) * C + bcol] : 0.f;
+        q4.y = 4 * j4 + 1 < L ? qb[row(4 * j4 + 1) * C + bcol] : 0.f;
+        q4.z = 4 * j4 + 2 < L ? qb[row(4 * j4 + 2) * C + bcol] : 0.f;
+        q4.w = 4 * j4 + 3 < L ? qb[row(4 * j4 + 3) * C + bcol] : 0.f;
+        k4.x = 4 * j4 + 0 < L ? kb[row(4 * j4 + 0) * C + bcol] : 0.f;
+        k4.y = 4 * j4 + 1 < L ? kb[row(4 * j4 + 1) * C + bcol] : 0.f;
+        k4.z = 4 * j4 + 2 < L ? kb[row(4 * j4 + 2) * C + bcol] : 0.f;
+        k4.w = 4 * j4 + 3 < L ? kb[row(4 * j4 + 3) * C + bcol] : 0.f;
+        *reinterpret_cast<float4*>(QT + umma::kidx(bcol, 4 * j4, 64)) = umma::tf32r(q4);
+        *reinterpret_cast<float4*>(KT + umma::kidx(bcol, 4 * j4, 64)) = umma::tf32r(k4);
+    }
+    if (tid < 64) {   // dgam from R: row sums minus column sums (fixed order)
+        float cs = 0.f;
+        for (int r = 0; r < 64; r++) cs += Rm[r * 65 + tid];
+        dgl[tid] = (rpart[tid] + rpart[64 + tid]) - cs;
+    }
+    umma::fence_smem_to_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    if (ok && tid == 0) {
+        umma::mma_tf32(tDQ, dPR, 64, KT, 64, 64, 128, 64, false);
+        umma::mma_tf32(tDK, dPC, 64, QT, 64, 64, 128, 64, false);
+        umma::commit(mbar);
+    }
+    // the triangular solve overlaps the MMAs
+    tril_inverse64(As, kM4, Tr, kM4);
+    __syncthreads();
+    {
+        float* Tg = w.Tm + ((int64_t)blockIdx.x * hv + h) * 64 * 64;
+        for (int idx = tid; idx < 64 * 16; idx += 256) {
+            const int r = idx >> 4, c = (idx & 15) * 4;
+            st4(Tg + r * 64 + c, make_float4(Tr[r * kM4 + c], Tr[r * kM4 + c + 1],
+                                             Tr[r * kM4 + c + 2], Tr[r * kM4 + c + 3]));
+        }
+    }
+    if (tid < 64 && tid < L) w.dgam[(int64_t)(ci.start + tid) * hv + h] += dgl[tid];
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
+    umma::fence_after_sync();
+    if (ok) {
+        for (int cc = 0; cc < 64; cc += 16) {
+            float vq[16], vk[16];
+            umma::tmem_ld16(umma::tmem_at(tDQ, half * 64 + cc), vq);
+            umma::tmem_ld16(umma::tmem_at(tDK, half * 64 + cc), vk);
+            if (lane < 16 && i < L) {
+                const int64_t off = (row(i) * hv + h) * kD + half * 64 + cc;
+#pragma unroll
+                for (int u = 0; u < 16; u += 4) {
+                    float4 q = ld4(w.dQv + off + u), k = ld4(w.dKv + off + u);
+                    q.x += vq[u]; q.y += vq[u + 1]; q.z += vq[u + 2]; q.w += vq[u + 3];
+                    k.x += vk[u]; k.y += vk[u + 1]; k.z += vk[u + 2]; k.w += vk[u + 3];
+                    st4(w.dQv + off + u, q);
+                    st4(w.dKv + off + u, k);
+                }
+            }
+        }
+    } else if (tid == 0) {
+        atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) umma::tmem_free(tmem, 512);
+}
+
+// ------------------------------------------------------------------ B3c: WY terms and gates
+// grid (NT, Hv), 256 threads, tcgen05.  With T from bwd_dp_kernel:
+//   D_kk = K K^T, D_dt1 = dW K^T, D_dt2 = dU V^T          (64 x 64)
+//   D_tw = T^T [dW | dU]                                  (64 x 256)
+//   dT = D_dt1 diag(beta e^gam) + D_dt2 diag(beta)
+//   dV = diag(beta) T^T dU ; dK += diag(beta e^gam) T^T dW
+//   dbeta_j += e^{gam_j} (T^T dW)_j . K_j + (T^T dU)_j . V_j ; dgam_j += beta_j e^{gam_j} (..)
+//   Y^T = T dT^T ; dA = -T^T Y (strictly lower) ; dKK = dA (.) beta_j Gam
+//   dbeta_j += sum_m dA (.) GamKK ; dgam_j += beta_j (..) ; dgam_m -= sum_j beta_j (..)
+//   dK += dKK K + dKK^T K
+// then dg = reverse in-chunk cumsum of the total dgam, and the gate gradients.
+constexpr int kWyFloats = 4 * 64 * 128 + 256 * 64 + 64 * 64;   // stage-1 operands
+constexpr size_t kWySmem = sizeof(float) * (kWyFloats + 10 * 64 + 2 * 64 + 16) + 64;
+
+template <class IO>
+__global__ void __launch_bounds__(256, 1)
+bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO* __restrict__ bv,
+              const float* __restrict__ A_log, const float* __restrict__ dt_bias, int hk, int hv,
+              float* __restrict__ dqkv, IO* __restrict__ da, IO* __restrict__ db,
+              float* __restrict__ gate_part, FwdSaved sv, BwdScratch w) {
+    extern __shared__ __align__(128) float sm[];
+    // stage 1
+    float* Ks = sm;                    // [64][128] K-major
+    float* Vs = Ks + 64 * 128;
+    float* dWs = Vs + 64 * 128;
+    float* dUs = dWs + 64 * 128;
+    float* BW = dUs + 64 * 128;        // [256][64] K-major: dW^T rows b, dU^T rows 128 + a
+    float* TC = BW + 256 * 64;         // [64 (j)][64 (i)] K-major T^T (kept to the end)
+    // stage 2 (overlays the stage-1 operands below TC)
+    float* GKK = sm;                   // [64][kM4] row-major Gam (.) KK (strict lower)
+    float* DTR = GKK + 64 * kM4;       // [64 (i)][64 (j)] K-major dT
+    float* TR = DTR + 64 * 64;         // [64 (m)][64 (j)] K-major T
+    float* YT = TR + 64 * 64;          // [64 (m)][64 (i)] K-major Y^T
+    float* dKR = YT + 64 * 64;         // [64 (j)][64 (m)] K-major dKK
+    float* dKC = dKR + 64 * 64;        // [64 (j)][64 (m)] K-major dKK^T
+    float* KT = dKC + 64 * 64;         // [128 (b)][64 (m)] K-major K^T
+    float* Rm = KT + 128 * 64;         // [64][65] row-major
+    float* gam = TC + 64 * 64;
+    float* eg = gam + 64;
+    float* bet = eg + 64;
+    float* be = bet + 64;
+    float* dgs = be + 64;
+    float* dbs = dgs + 64;
+    float* sc = dbs + 64;
+    float* rk = sc + 64;
+    float* red = rk + 64;              // [64]
+    float* rp = red + 64;              // [2][64]
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(rp + 128 + 16);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
+    const ChunkInfo ci = sv.chunks[blockIdx.x];
+    if (ci.len == 0) return;
+    const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int C = (2 * hk + hv) * kD;
+    auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
+    auto vrow = [&](int r) { return (row(r) * hv + h) * kD; };
+    const float* kb = qkv + (int64_t)hk * kD + kh * kD;
+    const float* vb = qkv + (int64_t)2 * hk * kD + h * kD;
+    const float* Tg = w.Tm + ((int64_t)blockIdx.x * hv + h) * 64 * 64;
+    for (int idx = tid; idx < 64 * 32; idx += 256) {
+        const int r = idx >> 5, c = (idx & 31) * 4;
+        cp_async16(Ks + umma::kidx(r, c, 128), kb + row(r) * C + c, r < L);
+        cp_async16(Vs + umma::kidx(r, c, 128), vb + row(r) * C + c, r < L);
+        cp_async16(dWs + umma::kidx(r, c, 128), w.dW + vrow(r) + c, r < L);
+        cp_async16(dUs + umma::kidx(r, c, 128), w.dU + vrow(r) + c, r < L);
+    }
+    cp_async_commit();
+    for (int idx = tid; idx < 256 * 16; idx += 256) {   // [dW^T ; dU^T]: lane = column
+        const int n = idx & 255, i4 = idx >> 8;
+        const float* src = n < 128 ? w.dW + n : w.dU + (n - 128);
+        float4 v;
+        v.x = 4 * i4 + 0 < L ? src[vrow(4 * i4 + 0)] : 0.f;
+        v.y = 4 * i4 + 1 < L ? src[vrow(4 * i4 + 1)] : 0.f;
+        v.z = 4 * i4 + 2 < L ? src[vrow(4 * i4 + 2)] : 0.f;
+        v.w = 4 * i4 + 3 < L ? src[vrow(4 * i4 + 3)] : 0.f;
+        *reinterpret_cast<float4*>(BW + umma::kidx(n, 4 * i4, 64)) = v;
+    }
+    for (int idx = tid; idx < 64 * 16; idx += 256) {    // T^T: lane = j
+        const int j = idx & 63, i4 = idx >> 6;
+        *reinterpret_cast<float4*>(TC + umma::kidx(j, 4 * i4, 64)) =
+            make_float4(Tg[(4 * i4 + 0) * 64 + j], Tg[(4 * i4 + 1) * 64 + j],
+                        Tg[(4 * i4 + 2) * 64 + j], Tg[(4 * i4 + 3) * 64 + j]);
+    }
+    load_gam(gam, sv, ci, h);
     if (tid < 64) {
-        float b = tid < L ? sv.beta[tok(tid) * hv + h] : 0.f;
-        bet[tid] = b;
+        bet[tid] = tid < L ? sv.beta[(int64_t)h * sv.T + ci.start + tid] : 0.f;
         dgs[tid] = 0.f;
         dbs[tid] = 0.f;
     }
+    if (warp == 0) umma::tmem_alloc(tslot, 512);
+    if (tid == 0) umma::mbar_init(mbar, 1);
     __syncthreads();
     if (tid < 64) {
         eg[tid] = tid < L ? expf(gam[tid]) : 0.f;
         be[tid] = bet[tid] * eg[tid];
     }
-    {
-        typename Tile<64, 64, 8>::Acc qk, dou;
-        tile_zero<64, 64, 8>(qk);
-        tile_zero<64, 64, 8>(dou);
-        tile_mma<64, 64, kD, 8>(qk, [&](int i, int b) { return B0[i * kL8 + b]; },
-                                [&](int b, int j) { return B1[j * kL8 + b]; });
-        tile_mma<64, 64, kD, 8>(dou, [&](int i, int a) { return B2[i * kL8 + a]; },
-                                [&](int a, int j) { return B3[j * kL8 + a]; });
-        // dPm = dOU (.) Gam (.) M ; R = dPm (.) QK  (dgam_i += sum_j R, dgam_j -= sum_i R)
-        tile_each<64, 64, 8>(dou, [&](int i, int j, float& v) {
-            float gm = (j <= i) ? expf(gam[i] - gam[j]) : 0.f;
-            v *= gm;
-            M1[i * kM4 + j] = v;
-        });
-        // elementwise R into dou (fragments of qk and dou align)
-        {
-            using TL = Tile<64, 64, 8>;
-#pragma unroll
-            for (int a = 0; a < TL::MPW; a++)
-#pragma unroll
-                for (int b = 0; b < TL::NPW; b++)
-#pragma unroll
-                    for (int e = 0; e < 4; e++) dou[a][b][e] *= qk[a][b][e];
-        }
-        tile_rowpart<64, 64, 8>(dou, [&](int, int, float v) { return v; }, rpart);
-        tile_colpart<64, 64, 8>(dou, [&](int, int, float v) { return v; }, cpart);
-    }
+    cp_async_wait<0>();
     __syncthreads();
-    if (tid < 64)
-        dgs[tid] += (rpart[tid] + rpart[64 + tid]) -
-                    (cpart[tid] + cpart[64 + tid] + cpart[128 + tid] + cpart[192 + tid]);
-    typename Tile<64, kD, 8>::Acc dk;
-    tile_zero<64, kD, 8>(dk);
-    {
-        typename Tile<64, kD, 8>::Acc dq;
-        tile_zero<64, kD, 8>(dq);
-        tile_mma<64, kD, 64, 8>(dq, [&](int i, int j) { return M1[i * kM4 + j]; },
-                                [&](int j, int b) { return B1[j * kL8 + b]; });
-        tile_each2<64, kD, 8>(dq, [&](int i, int b, float& v0, float& v1) {
-            if (i < L) {
-                float2* p = reinterpret_cast<float2*>(w.dQv + vrow(i) + b);
-                float2 o = *p;
-                *p = make_float2(o.x + v0, o.y + v1);
+    umma::tf32r_inplace(Ks, kWyFloats);   // K, V, dW, dU, [dW^T; dU^T], T^T
+    umma::fence_smem_to_async();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    // columns: KK 0-63 (later T^T Y), dT1 64-127 and dT2 128-191 (later Y^T, then the
+    // 128-column dKK product), T^T [dW | dU] 256-511 (read again at the very end)
+    const uint32_t tKK = tmem, tDT1 = tmem + 64, tDT2 = tmem + 128, tX = tmem + 64,
+                   tTW = tmem + 256;
+    if (tid == 0) {
+        umma::mma_tf32(tKK, Ks, 128, Ks, 128, 64, 64, 128, false);
+        umma::mma_tf32(tDT1, dWs, 128, Ks, 128, 64, 64, 128, false);
+        umma::mma_tf32(tDT2, dUs, 128, Vs, 128, 64, 64, 128, false);
+        umma::mma_tf32(tTW, TC, 64, BW, 64, 64, 256, 64, false);
+        umma::commit(mbar);
+    }
+    bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+    umma::fence_after_sync();
+    const int win = warp & 3, half = warp >> 2;
+    const int r = win * 16 + lane;     // D row (lanes 0..15)
+    const bool live = lane < 16;
+    if (ok) {
+        // Gam (.) KK and dT from the 64-column products
+        for (int cc = 0; cc < 32; cc += 16) {
+            float kk[16], t1[16], t2[16];
+            const int j0 = half * 32 + cc;
+            umma::tmem_ld16(umma::tmem_at(tKK, j0), kk);
+            umma::tmem_ld16(umma::tmem_at(tDT1, j0), t1);
+            umma::tmem_ld16(umma::tmem_at(tDT2, j0), t2);
+            if (live) {
+#pragma unroll
+                for (int u = 0; u < 16; u += 4) {
+                    float d[4];
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const int j = j0 + u + q;
+                        GKK[r * kM4 + j] = (j < r) ? expf(gam[r] - gam[j]) * kk[u + q] : 0.f;
+                        d[q] = t1[u + q] * be[j] + t2[u + q] * bet[j];
+                    }
+                    *reinterpret_cast<float4*>(DTR + umma::kidx(r, j0 + u, 64)) =
+                        umma::tf32r(make_float4(d[0], d[1], d[2], d[3]));
+                }
             }
-        });
-        tile_mma<64, kD, 64, 8>(dk, [&](int j, int i) { return M1[i * kM4 + j]; },
-                                [&](int i, int b) { return B0[i * kL8 + b]; });
-    }
-    __syncthreads();
-    // ---- phase 2: V, dW, dU (K stays)
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-        int r = idx >> 5, c4 = (idx & 31) * 4;
-        float4 v4 = zero4(), w4 = zero4(), u4 = zero4();
-        if (r < L) {
-            v4 = ld4(qkv + tok(r) * C + (int64_t)2 * hk * kD + h * kD + c4);
-            w4 = ld4(w.dW + vrow(r) + c4);
-            u4 = ld4(w.dU + vrow(r) + c4);
         }
-        st4(B0 + r * kL8 + c4, v4);
-        st4(B2 + r * kL8 + c4, w4);
-        st4(B3 + r * kL8 + c4, u4);
-    }
-    {
-        typename Tile<64, 64, 8>::Acc kk;
-        tile_zero<64, 64, 8>(kk);
-        tile_mma<64, 64, kD, 8>(kk, [&](int i, int b) { return B1[i * kL8 + b]; },
-                                [&](int b, int j) { return B1[j * kL8 + b]; });
-        tile_each<64, 64, 8>(kk, [&](int i, int j, float& v) {
-            float gkk = (j < i) ? expf(gam[i] - gam[j]) * v : 0.f;
-            M0[i * kM4 + j] = gkk;
-            M2[i * kM4 + j] = bet[i] * gkk;
-        });
-    }
-    __syncthreads();
-    tril_inverse64(M2, kM4, M1, kM4);
-    __syncthreads();
-    {   // dT = dW (D_be K)^T + dU (D_b V)^T
-        typename Tile<64, 64, 8>::Acc dt;
-        tile_zero<64, 64, 8>(dt);
-        tile_mma<64, 64, kD, 8>(dt, [&](int i, int b) { return B2[i * kL8 + b]; },
-                                [&](int b, int j) { return be[j] * B1[j * kL8 + b]; });
-        tile_mma<64, 64, kD, 8>(dt, [&](int i, int a) { return B3[i * kL8 + a]; },
-                                [&](int a, int j) { return bet[j] * B0[j * kL8 + a]; });
-        tile_each<64, 64, 8>(dt, [&](int i, int j, float& v) { M2[i * kM4 + j] = v; });
-    }
-    {   // T^T dW: dK += D_be (.), dbeta_j += e^gam_j r_j, dgam_j += be_j r_j
-        typename Tile<64, kD, 8>::Acc x;
-        tile_zero<64, kD, 8>(x);
-        tile_mma<64, kD, 64, 8>(x, [&](int j, int i) { return M1[i * kM4 + j]; },
-                                [&](int i, int b) { return B2[i * kL8 + b]; });
-        tile_rowpart<64, kD, 8>(x, [&](int j, int b, float v) { return v * B1[j * kL8 + b]; },
-                                rpart);
-        using TW = Tile<64, kD, 8>;
-        const int lane = tid & 31, g = lane >> 2;
-        const int m0 = TW::m0();
+        // T^T dW (half 0) and T^T dU (half 1): dV, dbeta / dgam dot products
+        float rsum = 0.f;
+        for (int cc = 0; cc < 128; cc += 16) {
+            float v[16];
+            umma::tmem_ld16(umma::tmem_at(tTW, half * 128 + cc), v);
+            if (live && r < L) {
+                if (half == 0) {
+                    const float* kr = kb + row(r) * C + cc;
 #pragma unroll
-        for (int a = 0; a < TW::MPW; a++)
+                    for (int u = 0; u < 16; u += 4) {
+                        const float4 k4 = ld4(kr + u);
+                        rsum += v[u] * k4.x + v[u + 1] * k4.y + v[u + 2] * k4.z + v[u + 3] * k4.w;
+                    }
+                } else {
+                    const float* vr = vb + row(r) * C + cc;
+                    float* dv = dqkv + row(r) * C + (int64_t)2 * hk * kD + h * kD + cc;
 #pragma unroll
-            for (int b = 0; b < TW::NPW; b++)
-#pragma unroll
-                for (int e = 0; e < 4; e++) dk[a][b][e] += be[m0 + a * 16 + g + (e >> 1) * 8] * x[a][b][e];
+                    for (int u = 0; u < 16; u += 4) {
+                        const float4 v4 = ld4(vr + u);
+                        rsum += v[u] * v4.x + v[u + 1] * v4.y + v[u + 2] * v4.z + v[u + 3] * v4.w;
+                        st4(dv + u, make_float4(bet[r] * v[u], bet[r] * v[u + 1],
+                                                bet[r] * v[u + 2], bet[r] * v[u + 3]));
+                    }
+                }
+            }
+        }
+        if (live) rp[half * 64 + r] = rsum;
     }
     __syncthreads();
     if (tid < 64) {
-        float r = rpart[tid] + rpart[64 + tid];
-        dbs[tid] += eg[tid] * r;
-        dgs[tid] += be[tid] * r;
+        dbs[tid] += eg[tid] * rp[tid] + rp[64 + tid];
+        dgs[tid] += be[tid] * rp[tid];
     }
-    {   // T^T dU: dV = D_b (.), dbeta_j += sum_a (.) V
-        typename Tile<64, kD, 8>::Acc x;
-        tile_zero<64, kD, 8>(x);
-        tile_mma<64, kD, 64, 8>(x, [&](int j, int i) { return M1[i * kM4 + j]; },
-                                [&](int i, int a) { return B3[i * kL8 + a]; });
-        tile_each2<64, kD, 8>(x, [&](int j, int a, float& v0, float& v1) {
-            if (j < L)
-                *reinterpret_cast<float2*>(dqkv + tok(j) * C + (int64_t)2 * hk * kD + h * kD + a) =
-                    make_float2(bet[j] * v0, bet[j] * v1);
-        });
-        tile_rowpart<64, kD, 8>(x, [&](int j, int a, float v) { return v * B0[j * kL8 + a]; },
-                                rpart);
+    // stage 2 operands: T rows (for Y^T = T dT^T) and K^T (for the dKK products)
+    for (int idx = tid; idx < 64 * 16; idx += 256) {
+        const int m = idx >> 4, c = (idx & 15) * 4;
+        *reinterpret_cast<float4*>(TR + umma::kidx(m, c, 64)) = umma::tf32r(ld4(Tg + m * 64 + c));
     }
+    for (int idx = tid; idx < 128 * 16; idx += 256) {
+        const int bcol = idx & 127, m4 = idx >> 7;
+        float4 k4;
+        k4.x = 4 * m4 + 0 < L ? kb[row(4 * m4 + 0) * C + bcol] : 0.f;
+        k4.y = 4 * m4 + 1 < L ? kb[row(4 * m4 + 1) * C + bcol] : 0.f;
+        k4.z = 4 * m4 + 2 < L ? kb[row(4 * m4 + 2) * C + bcol] : 0.f;
+        k4.w = 4 * m4 + 3 < L ? kb[row(4 * m4 + 3) * C + bcol] : 0.f;
+        *reinterpret_cast<float4*>(KT + umma::kidx(bcol, 4 * m4, 64)) = umma::tf32r(k4);
+    }
+    umma::fence_smem_to_async();
+    umma::fence_before_sync();
     __syncthreads();
-    if (tid < 64) dbs[tid] += rpart[tid] + rpart[64 + tid];
-    {   // Y = dT T^T
-        typename Tile<64, 64, 8>::Acc y;
-        tile_zero<64, 64, 8>(y);
-        tile_mma<64, 64, 64, 8>(y, [&](int i, int j) { return M2[i * kM4 + j]; },
-                                [&](int j, int m) { return M1[m * kM4 + j]; });
-        tile_each<64, 64, 8>(y, [&](int i, int m, float& v) { M3[i * kM8 + m] = v; });
+    umma::fence_after_sync();
+    if (ok && tid == 0) {
+        umma::mma_tf32(tX, TR, 64, DTR, 64, 64, 64, 64, false);     // Y^T = T dT^T
+        umma::commit(mbar);
     }
-    __syncthreads();
-    {   // dA = -T^T Y (strictly lower) ; dKK = dA beta_j Gam ; dbeta, dgam
-        typename Tile<64, 64, 8>::Acc x;
-        tile_zero<64, 64, 8>(x);
-        tile_mma<64, 64, 64, 8>(x, [&](int j, int i) { return M1[i * kM4 + j]; },
-                                [&](int i, int m) { return M3[i * kM8 + m]; });
-        tile_each<64, 64, 8>(x, [&](int j, int m, float& v) {
-            float dA = (m < j) ? -v : 0.f;
-            v = dA * M0[j * kM4 + m];       // dA (.) GamKK
-            M2[j * kM4 + m] = (m < j) ? dA * bet[j] * expf(gam[j] - gam[m]) : 0.f;
-        });
-        tile_rowpart<64, 64, 8>(x, [&](int, int, float v) { return v; }, rpart);
-        tile_colpart<64, 64, 8>(x, [&](int j, int, float v) { return bet[j] * v; }, cpart);
-    }
-    __syncthreads();
-    if (tid < 64) {
-        float r = rpart[tid] + rpart[64 + tid];
-        dbs[tid] += r;
-        dgs[tid] += bet[tid] * r -
-                    (cpart[tid] + cpart[64 + tid] + cpart[128 + tid] + cpart[192 + tid]);
-    }
-    // dK += dKK K + dKK^T K
-    tile_mma<64, kD, 64, 8>(dk, [&](int j, int m) { return M2[j * kM4 + m]; },
-                            [&](int m, int b) { return B1[m * kL8 + b]; });
-    tile_mma<64, kD, 64, 8>(dk, [&](int j, int m) { return M2[m * kM4 + j]; },
-                            [&](int m, int b) { return B1[m * kL8 + b]; });
-    tile_each2<64, kD, 8>(dk, [&](int j, int b, float& v0, float& v1) {
-        if (j < L) {
-            float2* p = reinterpret_cast<float2*>(w.dKv + vrow(j) + b);
-            float2 o = *p;
-            *p = make_float2(o.x + v0, o.y + v1);
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
+    umma::fence_after_sync();
+    if (ok) {
+        for (int cc = 0; cc < 32; cc += 16) {
+            float v[16];
+            const int i0 = half * 32 + cc;
+            umma::tmem_ld16(umma::tmem_at(tX, i0), v);
+            if (live)
+#pragma unroll
+                for (int u = 0; u < 16; u += 4)
+                    *reinterpret_cast<float4*>(YT + umma::kidx(r, i0 + u, 64)) =
+                        umma::tf32r(make_float4(v[u], v[u + 1], v[u + 2], v[u + 3]));
         }
-    });
+    }
+    umma::fence_smem_to_async();
+    umma::fence_before_sync();
     __syncthreads();
-    // ---- phase 3: dg = reverse cumsum of dgam; gates
-    if (tid < 64) sc[tid] = tid < L ? dgs[tid] + w.dgam[tok(tid) * hv + h] : 0.f;
+    umma::fence_after_sync();
+    if (ok && tid == 0) {
+        umma::mma_tf32(tKK, TC, 64, YT, 64, 64, 64, 64, false);     // T^T Y  (= -dA)
+        umma::commit(mbar);
+    }
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
+    umma::fence_after_sync();
+    if (ok) {
+        float rsum = 0.f;
+        for (int cc = 0; cc < 32; cc += 16) {
+            float v[16];
+            const int m0 = half * 32 + cc;
+            umma::tmem_ld16(umma::tmem_at(tKK, m0), v);
+            if (live) {
+#pragma unroll
+                for (int u = 0; u < 16; u += 4) {
+                    float dk[4];
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const int m = m0 + u + q;
+                        const float dA = (m < r) ? -v[u + q] : 0.f;
+                        const float x = dA * GKK[r * kM4 + m];
+                        rsum += x;
+                        Rm[r * 65 + m] = bet[r] * x;
+                        dk[q] = (m < r) ? dA * bet[r] * expf(gam[r] - gam[m]) : 0.f;
+                        dKC[umma::kidx(m, r, 64)] = umma::tf32r(dk[q]);
+                    }
+                    *reinterpret_cast<float4*>(dKR + umma::kidx(r, m0 + u, 64)) =
+                        umma::tf32r(make_float4(dk[0], dk[1], dk[2], dk[3]));
+                }
+            }
+        }
+        if (live) rp[half * 64 + r] = rsum;
+    }
+    umma::fence_smem_to_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    if (ok && tid == 0) {
+        umma::mma_tf32(tX, dKR, 64, KT, 64, 64, 128, 64, false);    // dKK K
+        umma::mma_tf32(tX, dKC, 64, KT, 64, 64, 128, 64, true);     // + dKK^T K
+        umma::commit(mbar);
+    }
+    if (tid < 64) {
+        float cs = 0.f;
+        for (int j = 0; j < 64; j++) cs += Rm[j * 65 + tid];
+        const float rsA = rp[tid] + rp[64 + tid];
+        dbs[tid] += rsA;
+        dgs[tid] += bet[tid] * rsA - cs;
+    }
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
+    umma::fence_after_sync();
+    if (ok) {
+        for (int cc = 0; cc < 64; cc += 16) {
+            float vk[16], vw[16];
+            umma::tmem_ld16(umma::tmem_at(tX, half * 64 + cc), vk);
+            umma::tmem_ld16(umma::tmem_at(tTW, half * 64 + cc), vw);
+            if (live && r < L) {
+                const int64_t off = vrow(r) + half * 64 + cc;
+#pragma unroll
+                for (int u = 0; u < 16; u += 4) {
+                    float4 k = ld4(w.dKv + off + u);
+                    k.x += vk[u] + be[r] * vw[u];
+                    k.y += vk[u + 1] + be[r] * vw[u + 1];
+                    k.z += vk[u + 2] + be[r] * vw[u + 2];
+                    k.w += vk[u + 3] + be[r] * vw[u + 3];
+                    st4(w.dKv + off + u, k);
+                }
+            }
+        }
+    } else if (tid == 0) {
+        atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) umma::tmem_free(tmem, 512);
+    if (!ok) return;
+    // ---- dg = reverse cumsum of dgam; gates
+    if (tid < 64) sc[tid] = tid < L ? dgs[tid] + w.dgam[(int64_t)(ci.start + tid) * hv + h] : 0.f;
     __syncthreads();
     if (tid < 32) {
-        // reverse inclusive scan over 64 values, two per lane
-        const int lane = tid;
         float a = sc[63 - 2 * lane], b = sc[62 - 2 * lane], s = a + b;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -590,22 +933,23 @@ bwd_local2_kernel(const float* __restrict__ qkv, const IO* __restrict__ av,
     __syncthreads();
     float gterm = 0.f, dterm = 0.f;
     if (tid < L) {
+        const int64_t t = ci.start + tid;
         const float dg = rk[tid];
         const float Aexp = expf(A_log[h]);
-        const float xa = to_f(av[tok(tid) * hv + h]) + dt_bias[h];
+        const float xa = to_f(av[t * hv + h]) + dt_bias[h];
         const float gval = -Aexp * softplusf_(xa);
         const float dav = dg * (-Aexp) * sigmoidf_(xa);
         const float bb = bet[tid];
-        da[tok(tid) * hv + h] = from_f<IO>(dav);
-        db[tok(tid) * hv + h] = from_f<IO>(dbs[tid] * bb * (1.f - bb));
-        w.dgs[tok(tid) * hv + h] = dg;
+        da[t * hv + h] = from_f<IO>(dav);
+        db[t * hv + h] = from_f<IO>(dbs[tid] * bb * (1.f - bb));
+        w.dgs[t * hv + h] = dg;
         gterm = dg * gval;
         dterm = dav;
     }
     if (tid < 64) {
         gterm = warp_sum(gterm);
         dterm = warp_sum(dterm);
-        if ((tid & 31) == 0) { red[tid >> 5] = gterm; red[2 + (tid >> 5)] = dterm; }
+        if (lane == 0) { red[warp] = gterm; red[2 + warp] = dterm; }
     }
     __syncthreads();
     if (tid == 0) {
@@ -649,13 +993,31 @@ __global__ void gate_reduce_kernel(const float* __restrict__ part, int NT, int h
     if (ddt_bias) ddt_bias[h] = b;
 }
 
-__global__ void colsum2_kernel(const float* __restrict__ part, int64_t nparts, int cols,
-                               float* __restrict__ out) {
-    int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= cols) return;
+// Deterministic two-level column sum of part [nparts][kD]: stage 1, block b
+// sums rows [b*per, (b+1)*per) in order into tmp[b]; stage 2 sums tmp rows in
+// order (8 row groups per column, then the 8 group sums in order).
+constexpr int kColsumBlocks = 512;
+__global__ void colsum_stage1_kernel(const float* __restrict__ part, int64_t nparts,
+                                     float* __restrict__ tmp) {
+    const int c = threadIdx.x;   // kD threads
+    const int64_t per = (nparts + kColsumBlocks - 1) / kColsumBlocks;
+    const int64_t r0 = blockIdx.x * per, r1 = min(nparts, r0 + per);
     float acc = 0.f;
-    for (int64_t p = 0; p < nparts; p++) acc += part[p * cols + i];
-    out[i] = acc;
+    for (int64_t r = r0; r < r1; r++) acc += part[r * kD + c];
+    tmp[blockIdx.x * kD + c] = acc;
+}
+__global__ void colsum_stage2_kernel(const float* __restrict__ tmp, float* __restrict__ out) {
+    __shared__ float red[8][kD];
+    const int c = threadIdx.x % kD, g = threadIdx.x / kD;   // 8 * kD threads
+    float acc = 0.f;
+    for (int r = g; r < kColsumBlocks; r += 8) acc += tmp[r * kD + c];
+    red[g][c] = acc;
+    __syncthreads();
+    if (g == 0) {
+        float s = 0.f;
+        for (int i = 0; i < 8; i++) s += red[i][c];
+        out[c] = s;
+    }
 }
 
 // ------------------------------------------------------------------ launcher
@@ -669,8 +1031,10 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
                              (int)kB2Smem);
         cudaFuncSetAttribute(bwd_sfacing_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kB3aSmem);
-        cudaFuncSetAttribute(bwd_local2_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kB3bSmem);
+        cudaFuncSetAttribute(bwd_dp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kDpSmem);
+        cudaFuncSetAttribute(bwd_wy_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kWySmem);
         attr = true;
     }
     float* gate_part = w.nw_part + (size_t)a.NT * a.hv * kD;
@@ -682,7 +1046,7 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
     }
     if (a.N > 0) {
         GDN_PROF("chunk_bwd_state", st);
-        bwd_state_kernel<<<dim3(kD / kSl, a.hv, a.N), 128, kB2Smem, st>>>(
+        bwd_state_kernel<<<dim3(kD / kSl, a.hv, a.N), 256, kB2Smem, st>>>(
             a.qkv, a.hk, a.hv, a.dS_final, a.dS_init, a.sv, w);
     }
     if (a.NT > 0) {
@@ -691,8 +1055,12 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
             bwd_sfacing_kernel<<<dim3(a.NT, a.hv), 256, kB3aSmem, st>>>(a.qkv, a.hk, a.hv, a.sv,
                                                                           w);
         }
+        {
+            GDN_PROF("chunk_bwd_dp", st);
+            bwd_dp_kernel<<<dim3(a.NT, a.hv), 256, kDpSmem, st>>>(a.qkv, a.hk, a.hv, a.sv, w);
+        }
         GDN_PROF("chunk_bwd_wy", st);
-        bwd_local2_kernel<IO><<<dim3(a.NT, a.hv), 256, kB3bSmem, st>>>(
+        bwd_wy_kernel<IO><<<dim3(a.NT, a.hv), 256, kWySmem, st>>>(
             a.qkv, (const IO*)a.a, (const IO*)a.b, a.A_log, a.dt_bias, a.hk, a.hv, a.dqkv,
             (IO*)a.da, (IO*)a.db, gate_part, a.sv, w);
     }
@@ -714,8 +1082,14 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
     }
     if (a.z && a.dnorm_w) {
         if (a.NT > 0) {
-            GDN_PROF("norm_w_reduce", st);
-            colsum2_kernel<<<1, kD, 0, st>>>(w.nw_part, (int64_t)a.NT * a.hv, kD, a.dnorm_w);
+            float* tmp = w.nw_part + (size_t)a.NT * a.hv * kD + (size_t)a.NT * a.hv * 2;
+            {
+                GDN_PROF("norm_w_reduce", st);
+                colsum_stage1_kernel<<<kColsumBlocks, kD, 0, st>>>(w.nw_part,
+                                                                   (int64_t)a.NT * a.hv, tmp);
+            }
+            GDN_PROF("norm_w_reduce2", st);
+            colsum_stage2_kernel<<<1, 8 * kD, 0, st>>>(tmp, a.dnorm_w);
         } else
             cudaMemsetAsync(a.dnorm_w, 0, sizeof(float) * kD, st);
     }

@@ -20,6 +20,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "prof.h"
+#include "umma.cuh"
 
 namespace gdn {
 
@@ -69,272 +70,400 @@ __global__ void plan_kernel(const int32_t* __restrict__ cu, int N, int64_t T, in
 }
 
 // ------------------------------------------------------------------ prep
-// grid (NT, Hv), 256 threads.  Gates, in-chunk cumsum, A, T, W, U~.
+// grid (NT, Hv), 256 threads, tcgen05.  Gates and their in-chunk cumsum, then
+//   D1 = K K^T (64 x 64)  ->  A = beta_i e^{gam_i-gam_j} D1 (j < i)
+//   T  = (I + A)^-1        (forward substitution on the CUDA cores)
+//   D2 = T [diag(beta e^gam) K | diag(beta) V]   (one M=64, N=256, K=64 MMA)
+// giving W = D2[:, :128] and U~ = D2[:, 128:].
 constexpr int kLdK = 132, kLdV = 136, kLdA = 68;
-constexpr size_t kPrepSmem = sizeof(float) * (64 * kLdK + 64 * kLdV + 2 * 64 * kLdA + 3 * 64);
+constexpr int kPrepFloats = 64 * 128 + 256 * 64 + 2 * 64 * kLdA + 64 * 64;
+constexpr size_t kPrepSmem = sizeof(float) * (kPrepFloats + 3 * 64 + 16) + 64;
 
 template <class IO>
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256, 1)
 prep_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO* __restrict__ bv,
             const float* __restrict__ A_log, const float* __restrict__ dt_bias, int hk, int hv,
             FwdSaved sv) {
-    extern __shared__ float sm[];
-    float* Ks = sm;
-    float* Vs = Ks + 64 * kLdK;
-    float* As = Vs + 64 * kLdV;
-    float* Ts = As + 64 * kLdA;
-    float* gam = Ts + 64 * kLdA;
+    extern __shared__ __align__(128) float sm[];
+    float* Ks = sm;                    // [64][128] K-major
+    float* Bs = Ks + 64 * 128;         // [256 (c | a)][64 (j)] K-major: (be K)^T ; (beta V)^T
+    float* As = Bs + 256 * 64;         // [64][kLdA] row-major A
+    float* Tr = As + 64 * kLdA;        // [64][kLdA] row-major T
+    float* Tk = Tr + 64 * kLdA;        // [64][64] K-major T
+    float* gam = Tk + 64 * 64;
     float* bet = gam + 64;
     float* be = bet + 64;
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(be + 64 + 16);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
     const ChunkInfo ci = sv.chunks[blockIdx.x];
     if (ci.len == 0) return;
-    const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x;
+    const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
+    const int warp = tid >> 5, lane = tid & 31;
     const int C = (2 * hk + hv) * kD;
+    auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
     const float* kbase = qkv + (int64_t)hk * kD + kh * kD;
     const float* vbase = qkv + (int64_t)2 * hk * kD + h * kD;
     for (int idx = tid; idx < 64 * 32; idx += 256) {
-        int r = idx >> 5, c4 = (idx & 31) * 4;
-        float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
-        if (r < ci.len) {
-            int64_t row = (int64_t)(ci.start + r) * C;
-            kk = ld4(kbase + row + c4);
-            vv = ld4(vbase + row + c4);
-        }
-        st4(Ks + r * kLdK + c4, kk);
-        st4(Vs + r * kLdV + c4, vv);
+        const int r = idx >> 5, c = (idx & 31) * 4;
+        cp_async16(Ks + umma::kidx(r, c, 128), kbase + row(r) * C + c, r < L);
     }
+    cp_async_commit();
     if (tid < 64) {
         float g = 0.f, b = 0.f;
-        if (tid < ci.len) {
-            int64_t t = ci.start + tid;
+        if (tid < L) {
+            const int64_t t = ci.start + tid;
             g = -expf(A_log[h]) * softplusf_(to_f(av[t * hv + h]) + dt_bias[h]);
             b = sigmoidf_(to_f(bv[t * hv + h]));
         }
         gam[tid] = g;
         bet[tid] = b;
     }
+    if (warp == 0) umma::tmem_alloc(tslot, 512);
+    if (tid == 0) umma::mbar_init(mbar, 1);
     __syncthreads();
     if (tid < 32) warp_cumsum64(gam);
     __syncthreads();
     if (tid < 64) {
         be[tid] = bet[tid] * expf(gam[tid]);
-        if (tid < ci.len) {
-            int64_t t = ci.start + tid;
-            sv.gam[t * hv + h] = gam[tid];
-            sv.beta[t * hv + h] = bet[tid];
+        if (tid < L) {
+            sv.gam[(int64_t)h * sv.T + ci.start + tid] = gam[tid];
+            sv.beta[(int64_t)h * sv.T + ci.start + tid] = bet[tid];
         }
     }
-    {
-        using TL = Tile<64, 64, 8>;
-        typename TL::Acc acc;
-        tile_zero<64, 64, 8>(acc);
-        tile_mma<64, 64, kD, 8>(acc, [&](int r, int k) { return Ks[r * kLdK + k]; },
-                                [&](int k, int c) { return Ks[c * kLdK + k]; });
-        tile_each<64, 64, 8>(acc, [&](int r, int c, float& v) {
-            As[r * kLdA + c] = (c < r) ? bet[r] * expf(gam[r] - gam[c]) * v : 0.f;
-        });
+    __syncthreads();
+    // B operand rows: c (0..127) = be_j K[j][c], 128 + a = beta_j V[j][a]; lane = column
+    for (int idx = tid; idx < 256 * 16; idx += 256) {
+        const int n = idx & 255, j4 = idx >> 8;
+        const float* src = n < 128 ? kbase + n : vbase + (n - 128);
+        const float* sc = n < 128 ? be : bet;
+        float4 v;
+        v.x = 4 * j4 + 0 < L ? sc[4 * j4 + 0] * src[row(4 * j4 + 0) * C] : 0.f;
+        v.y = 4 * j4 + 1 < L ? sc[4 * j4 + 1] * src[row(4 * j4 + 1) * C] : 0.f;
+        v.z = 4 * j4 + 2 < L ? sc[4 * j4 + 2] * src[row(4 * j4 + 2) * C] : 0.f;
+        v.w = 4 * j4 + 3 < L ? sc[4 * j4 + 3] * src[row(4 * j4 + 3) * C] : 0.f;
+        *reinterpret_cast<float4*>(Bs + umma::kidx(n, 4 * j4, 64)) = v;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    umma::tf32r_inplace(Ks, 64 * 128 + 256 * 64);   // K and the B operand (contiguous)
+    umma::fence_smem_to_async();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t tD1 = tmem, tD2 = tmem + 256;
+    if (tid == 0) {
+        umma::mma_tf32(tD1, Ks, 128, Ks, 128, 64, 64, 128, false);
+        umma::commit(mbar);
+    }
+    bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+    umma::fence_after_sync();
+    const int win = warp & 3, half = warp >> 2;
+    const int i = win * 16 + lane;
+    if (ok) {
+        for (int cc = 0; cc < 32; cc += 16) {
+            float v[16];
+            const int j0 = half * 32 + cc;
+            umma::tmem_ld16(umma::tmem_at(tD1, j0), v);
+            if (lane < 16)
+#pragma unroll
+                for (int u = 0; u < 16; u++) {
+                    const int j = j0 + u;
+                    As[i * kLdA + j] = (j < i) ? bet[i] * expf(gam[i] - gam[j]) * v[u] : 0.f;
+                }
+        }
     }
     __syncthreads();
-    tril_inverse64(As, kLdA, Ts, kLdA);
+    tril_inverse64(As, kLdA, Tr, kLdA);
     __syncthreads();
-    using TW = Tile<64, kD, 8>;
-    typename TW::Acc acc;
-    tile_zero<64, kD, 8>(acc);
-    tile_mma<64, kD, 64, 8>(acc, [&](int r, int k) { return Ts[r * kLdA + k]; },
-                            [&](int k, int c) { return be[k] * Ks[k * kLdK + c]; });
-    tile_each2<64, kD, 8>(acc, [&](int r, int c, float& v0, float& v1) {
-        if (r < ci.len)
-            *reinterpret_cast<float2*>(sv.W + ((int64_t)(ci.start + r) * hv + h) * kD + c) =
-                make_float2(v0, v1);
-    });
-    tile_zero<64, kD, 8>(acc);
-    tile_mma<64, kD, 64, 8>(acc, [&](int r, int k) { return Ts[r * kLdA + k]; },
-                            [&](int k, int c) { return bet[k] * Vs[k * kLdV + c]; });
-    tile_each2<64, kD, 8>(acc, [&](int r, int c, float& v0, float& v1) {
-        if (r < ci.len)
-            *reinterpret_cast<float2*>(sv.U + ((int64_t)(ci.start + r) * hv + h) * kD + c) =
-                make_float2(v0, v1);
-    });
+    for (int idx = tid; idx < 64 * 16; idx += 256) {   // T -> K-major rows i
+        const int r = idx >> 4, c = (idx & 15) * 4;
+        *reinterpret_cast<float4*>(Tk + umma::kidx(r, c, 64)) = umma::tf32r(
+            make_float4(Tr[r * kLdA + c], Tr[r * kLdA + c + 1], Tr[r * kLdA + c + 2],
+                        Tr[r * kLdA + c + 3]));
+    }
+    umma::fence_smem_to_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    if (ok && tid == 0) {
+        umma::mma_tf32(tD2, Tk, 64, Bs, 64, 64, 256, 64, false);
+        umma::commit(mbar);
+    }
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
+    umma::fence_after_sync();
+    if (ok) {
+        // warp half 0 -> W (columns 0..127), half 1 -> U~ (128..255)
+        float* dstbase = half == 0 ? sv.W : sv.U;
+        for (int cc = 0; cc < 128; cc += 16) {
+            float v[16];
+            umma::tmem_ld16(umma::tmem_at(tD2, half * 128 + cc), v);
+            if (lane < 16 && i < L) {
+                float* dst = dstbase + ((int64_t)(ci.start + i) * hv + h) * kD + cc;
+#pragma unroll
+                for (int u = 0; u < 16; u += 4)
+                    st4(dst + u, make_float4(v[u], v[u + 1], v[u + 2], v[u + 3]));
+            }
+        }
+    } else if (tid == 0) {
+        atomicExch(sv.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) umma::tmem_free(tmem, 512);
 }
 
 // ------------------------------------------------------------------ state pass
-// grid (d_v / kSlice, Hv, N), 128 threads.  Rows a of S evolve independently
-// (k, beta, g are shared by all rows), so each CTA carries a 32-row slice of
-// the fp32 state -- kept transposed, S^T[b][a], in the MMA accumulators --
-// through all chunks of its sequence.
-constexpr int kSlice = 32;
-constexpr int kLdS = kSlice + 8;   // 40: conflict-free as a K-major operand
-constexpr size_t kStateSmem =
-    sizeof(float) * (64 * kLdK + 64 * kLdV + 64 * kLdS + kD * kLdS + 2 * 64);
+// grid (d_v / kSlice, Hv, N), 256 threads, one CTA per SM.  Rows a of S evolve
+// independently (k, beta, g are shared by all rows), so each CTA carries a
+// 64-row slice of the fp32 state -- kept transposed, S^T[b][a], in the MMA
+// accumulators -- through all chunks of its sequence.  The next chunk's W, K,
+// U~ slice and gates are fetched with cp.async into the other half of a
+// double buffer while the current chunk is computed.
+constexpr int kSlice = 64;
+constexpr int kLdS = kSlice + 8;   // 72: conflict-free as a K-major operand
+struct StateStage {
+    float W[64 * kLdK];
+    float K[64 * kLdV];
+    float U[64 * kLdS];            // U~ slice, overwritten in place by U
+    float gam[64];
+};
+constexpr size_t kStateSmem = sizeof(float) * (2 * (64 * kLdK + 64 * kLdV + 64 * kLdS + 64) +
+                                               kD * kLdS + 64);
 
-__global__ void __launch_bounds__(128)
+__device__ __forceinline__ void state_fwd_issue(StateStage& st, const ChunkInfo& info,
+                                                const float* __restrict__ qkv, int hk, int hv,
+                                                int kh, int h, int a0, const FwdSaved& sv) {
+    const int tid = threadIdx.x, L = info.len;
+    const int C = (2 * hk + hv) * kD;
+    for (int idx = tid; idx < 64 * 32; idx += 256) {
+        const int r = idx >> 5, c4 = (idx & 31) * 4;
+        const int64_t t = info.start + min(r, L - 1);
+        cp_async16(st.W + r * kLdK + c4, sv.W + (t * hv + h) * kD + c4, r < L);
+        cp_async16(st.K + r * kLdV + c4, qkv + t * C + (int64_t)hk * kD + kh * kD + c4, r < L);
+    }
+    for (int idx = tid; idx < 64 * kSlice / 4; idx += 256) {
+        const int r = idx / (kSlice / 4), c4 = (idx % (kSlice / 4)) * 4;
+        const int64_t t = info.start + min(r, L - 1);
+        cp_async16(st.U + r * kLdS + c4, sv.U + (t * hv + h) * kD + a0 + c4, r < L);
+    }
+    if (tid < 64)   // gate rows start at any token: 4-byte copies
+        cp_async4(st.gam + tid, sv.gam + (int64_t)h * sv.T + info.start + min(tid, L - 1),
+                  tid < L);
+    cp_async_commit();
+}
+
+__global__ void __launch_bounds__(256, 1)
 state_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const float* S_init,
                  float* S_final, FwdSaved sv) {
     extern __shared__ float sm[];
-    float* Ws = sm;                    // [64][kLdK]
-    float* Ks = Ws + 64 * kLdK;        // [64][kLdV]
-    float* Us = Ks + 64 * kLdV;        // [64][kLdS]
-    float* St = Us + 64 * kLdS;        // [128][kLdS]  S^T slice
-    float* gam = St + kD * kLdS;       // [64]
-    float* fk = gam + 64;              // [64] exp(gam_L - gam_i)
+    StateStage* stage = reinterpret_cast<StateStage*>(sm);
+    float* St = sm + 2 * (sizeof(StateStage) / sizeof(float));   // [128][kLdS]  S^T slice
+    float* fk = St + kD * kLdS;                                   // [64] exp(gam_L - gam_i)
     const int sl = blockIdx.x, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
     const int a0 = sl * kSlice, kh = h / (hv / hk);
-    const int C = (2 * hk + hv) * kD;
-    using TS = Tile<kD, kSlice, 4>;    // S^T: rows b (d_k), cols a (slice)
-    using TU = Tile<64, kSlice, 4>;
+    using TS = Tile<kD, kSlice, 8>;    // S^T: rows b (d_k), cols a (slice)
+    using TU = Tile<64, kSlice, 8>;
     typename TS::Acc sacc;
     const int64_t sbase = ((int64_t)n * hv + h) * kD * kD;
-    tile_each<kD, kSlice, 4>(sacc, [&](int b, int a, float& v) {
+    tile_each<kD, kSlice, 8>(sacc, [&](int b, int a, float& v) {
         v = S_init ? S_init[sbase + (int64_t)(a0 + a) * kD + b] : 0.f;
         St[b * kLdS + a] = v;
     });
     const int c0 = sv.seq_chunk[n], c1 = sv.seq_chunk[n + 1];
+    if (c0 < c1) state_fwd_issue(stage[0], sv.chunks[c0], qkv, hk, hv, kh, h, a0, sv);
     for (int ci = c0; ci < c1; ci++) {
+        StateStage& cur = stage[(ci - c0) & 1];
         const ChunkInfo info = sv.chunks[ci];
         const int L = info.len;
-        __syncthreads();
-        for (int idx = tid; idx < 64 * 32; idx += 128) {
-            int r = idx >> 5, c4 = (idx & 31) * 4;
-            float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f), k4 = w4;
-            if (r < L) {
-                int64_t t = info.start + r;
-                w4 = ld4(sv.W + (t * hv + h) * kD + c4);
-                k4 = ld4(qkv + t * C + (int64_t)hk * kD + kh * kD + c4);
-            }
-            st4(Ws + r * kLdK + c4, w4);
-            st4(Ks + r * kLdV + c4, k4);
+        if (ci + 1 < c1) {
+            state_fwd_issue(stage[(ci - c0 + 1) & 1], sv.chunks[ci + 1], qkv, hk, hv, kh, h, a0,
+                            sv);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
         }
-        for (int idx = tid; idx < 64 * kSlice / 4; idx += 128) {
-            int r = idx / (kSlice / 4), c4 = (idx % (kSlice / 4)) * 4;
-            float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < L) u4 = ld4(sv.U + ((int64_t)(info.start + r) * hv + h) * kD + a0 + c4);
-            st4(Us + r * kLdS + c4, u4);
-        }
-        if (tid < 64) gam[tid] = tid < L ? sv.gam[(int64_t)(info.start + tid) * hv + h] : 0.f;
         // state at the chunk start, for the output and the backward
         const int64_t obase = ((int64_t)ci * hv + h) * kD * kD;
-        tile_each2<kD, kSlice, 4>(sacc, [&](int b, int a, float& v0, float& v1) {
+        tile_each2<kD, kSlice, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
             sv.S0[obase + (int64_t)(a0 + a) * kD + b] = v0;
             sv.S0[obase + (int64_t)(a0 + a + 1) * kD + b] = v1;
         });
-        __syncthreads();
-        if (tid < 64) fk[tid] = tid < L ? expf(gam[L - 1] - gam[tid]) : 0.f;
+        __syncthreads();   // this chunk's tiles have landed (and St is current)
+        if (tid < 64) fk[tid] = tid < L ? expf(cur.gam[L - 1] - cur.gam[tid]) : 0.f;
         // U = U~ - W S^T   (64 x slice)
         typename TU::Acc uacc;
-        tile_zero<64, kSlice, 4>(uacc);
-        tile_mma<64, kSlice, kD, 4>(uacc, [&](int i, int b) { return Ws[i * kLdK + b]; },
+        tile_zero<64, kSlice, 8>(uacc);
+        tile_mma<64, kSlice, kD, 8>(uacc, [&](int i, int b) { return cur.W[i * kLdK + b]; },
                                     [&](int b, int a) { return St[b * kLdS + a]; });
-        __syncthreads();
-        tile_each<64, kSlice, 4>(uacc, [&](int i, int a, float& v) {
-            float u = i < L ? Us[i * kLdS + a] - v : 0.f;
-            Us[i * kLdS + a] = u;
+        tile_each<64, kSlice, 8>(uacc, [&](int i, int a, float& v) {
+            const float u = i < L ? cur.U[i * kLdS + a] - v : 0.f;
+            cur.U[i * kLdS + a] = u;
             if (i < L) sv.U[((int64_t)(info.start + i) * hv + h) * kD + a0 + a] = u;
         });
         __syncthreads();
         // S^T = e^{gam_L} S^T + (diag(fk) K)^T U
-        const float dl = expf(gam[L - 1]);
-        tile_each<kD, kSlice, 4>(sacc, [&](int, int, float& v) { v *= dl; });
-        tile_mma<kD, kSlice, 64, 4>(sacc, [&](int b, int i) { return fk[i] * Ks[i * kLdV + b]; },
-                                    [&](int i, int a) { return Us[i * kLdS + a]; });
-        tile_each<kD, kSlice, 4>(sacc, [&](int b, int a, float& v) { St[b * kLdS + a] = v; });
+        const float dl = expf(cur.gam[L - 1]);
+        tile_each<kD, kSlice, 8>(sacc, [&](int, int, float& v) { v *= dl; });
+        tile_mma<kD, kSlice, 64, 8>(sacc, [&](int b, int i) { return fk[i] * cur.K[i * kLdV + b]; },
+                                    [&](int i, int a) { return cur.U[i * kLdS + a]; });
+        __syncthreads();   // reads of cur, St and fk are done
+        tile_each<kD, kSlice, 8>(sacc, [&](int b, int a, float& v) { St[b * kLdS + a] = v; });
     }
     if (S_final)
-        tile_each<kD, kSlice, 4>(sacc, [&](int b, int a, float& v) {
+        tile_each<kD, kSlice, 8>(sacc, [&](int b, int a, float& v) {
             S_final[sbase + (int64_t)(a0 + a) * kD + b] = v;
         });
 }
 
 // ------------------------------------------------------------------ output + norm
-// grid (NT, Hv), 256 threads.
-constexpr size_t kOutSmem =
-    sizeof(float) * (64 * kLdK * 2 + 64 * kLdV + kD * kLdK + 64 * kLdA + 2 * 64);
+// grid (NT, Hv), 256 threads, tcgen05.
+//   D1 = Q K^T (64 x 64),  D3 = Q S0^T (64 x 128)       -- issued together
+//   P  = D1 (.) e^{gam_i - gam_j} (.) [i >= j]          -- staged K-major
+//   D2 = P U (64 x 128)
+//   O  = D2 + e^{gam_i} D3 ; y = O rsqrt(mean(O^2)+eps) (1+w) silu(z)
+// Shared memory (K-major core layout): Q, K 32 KB each, S0 (rows a) 64 KB,
+// U^T (rows a, k = token) 32 KB, P 16 KB.  Tensor memory: 320 fp32 columns.
+constexpr int kOutFloats = 64 * 128 * 2 + 128 * 128 + 128 * 64 + 64 * 64;
+constexpr size_t kOutSmem = sizeof(float) * (kOutFloats + 64 * 2 + 2 * 64 + 16) + 64;
 
 template <class IO>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 1)
 out_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z,
                const float* norm_w, float norm_eps, IO* o_out, IO* y_out, FwdSaved sv) {
-    extern __shared__ float sm[];
-    float* Qs = sm;                    // [64][kLdK]   (later O)
-    float* Ks = Qs + 64 * kLdK;        // [64][kLdK]
-    float* Us = Ks + 64 * kLdK;        // [64][kLdV]
-    float* Ss = Us + 64 * kLdV;        // [128][kLdK]  S0[a][b]
-    float* Ps = Ss + kD * kLdK;        // [64][kLdA]
-    float* gam = Ps + 64 * kLdA;
+    extern __shared__ __align__(128) float sm[];
+    float* Qs = sm;                    // [64][128]  K-major
+    float* Ks = Qs + 64 * 128;         // [64][128]
+    float* Ss = Ks + 64 * 128;         // [128 (a)][128 (b)]
+    float* UT = Ss + 128 * 128;        // [128 (a)][64 (j)]
+    float* Ps = UT + 128 * 64;         // [64 (i)][64 (j)]
+    float* gam = Ps + 64 * 64;
     float* eg = gam + 64;
+    float* ssq = eg + 64;              // [2][64] partial sums of squares
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(ssq + 2 * 64 + 16);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
     const ChunkInfo ci = sv.chunks[blockIdx.x];
     if (ci.len == 0) return;
     const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
+    const int warp = tid >> 5, lane = tid & 31;
     const int C = (2 * hk + hv) * kD;
+    auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
     for (int idx = tid; idx < 64 * 32; idx += 256) {
-        int r = idx >> 5, c4 = (idx & 31) * 4;
-        float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f), k4 = q4, u4 = q4;
-        if (r < L) {
-            int64_t t = ci.start + r;
-            q4 = ld4(qkv + t * C + kh * kD + c4);
-            k4 = ld4(qkv + t * C + (int64_t)hk * kD + kh * kD + c4);
-            u4 = ld4(sv.U + (t * hv + h) * kD + c4);
-        }
-        st4(Qs + r * kLdK + c4, q4);
-        st4(Ks + r * kLdK + c4, k4);
-        st4(Us + r * kLdV + c4, u4);
+        const int r = idx >> 5, c = (idx & 31) * 4;
+        cp_async16(Qs + umma::kidx(r, c, 128), qkv + row(r) * C + kh * kD + c, r < L);
+        cp_async16(Ks + umma::kidx(r, c, 128), qkv + row(r) * C + (int64_t)hk * kD + kh * kD + c,
+                   r < L);
     }
     const float* S0 = sv.S0 + ((int64_t)blockIdx.x * hv + h) * kD * kD;
-    for (int idx = tid; idx < kD * 32; idx += 256) {
-        int r = idx >> 5, c4 = (idx & 31) * 4;
-        st4(Ss + r * kLdK + c4, ld4(S0 + r * kD + c4));
+    for (int idx = tid; idx < 128 * 32; idx += 256) {
+        const int r = idx >> 5, c = (idx & 31) * 4;
+        cp_async16(Ss + umma::kidx(r, c, 128), S0 + r * kD + c, true);
+    }
+    cp_async_commit();
+    for (int idx = tid; idx < 128 * 16; idx += 256) {   // U^T: lane = a, 4 tokens per store
+        const int a = idx & 127, j4 = idx >> 7;
+        float4 v;
+        v.x = 4 * j4 + 0 < L ? sv.U[(row(4 * j4 + 0) * hv + h) * kD + a] : 0.f;
+        v.y = 4 * j4 + 1 < L ? sv.U[(row(4 * j4 + 1) * hv + h) * kD + a] : 0.f;
+        v.z = 4 * j4 + 2 < L ? sv.U[(row(4 * j4 + 2) * hv + h) * kD + a] : 0.f;
+        v.w = 4 * j4 + 3 < L ? sv.U[(row(4 * j4 + 3) * hv + h) * kD + a] : 0.f;
+        *reinterpret_cast<float4*>(UT + umma::kidx(a, 4 * j4, 64)) = v;
     }
     if (tid < 64) {  // padding rows continue the last gate value (g = 0)
-        float g = sv.gam[(int64_t)(ci.start + min(tid, L - 1)) * hv + h];
+        const float g = sv.gam[(int64_t)h * sv.T + row(tid)];
         gam[tid] = g;
         eg[tid] = tid < L ? expf(g) : 0.f;
     }
+    if (warp == 0) umma::tmem_alloc(tslot, 512);
+    if (tid == 0) umma::mbar_init(mbar, 1);
+    cp_async_wait<0>();
     __syncthreads();
-    {
-        using TL = Tile<64, 64, 8>;
-        typename TL::Acc acc;
-        tile_zero<64, 64, 8>(acc);
-        tile_mma<64, 64, kD, 8>(acc, [&](int r, int k) { return Qs[r * kLdK + k]; },
-                                [&](int k, int c) { return Ks[c * kLdK + k]; });
-        tile_each<64, 64, 8>(acc, [&](int r, int c, float& v) {
-            Ps[r * kLdA + c] = (c <= r) ? v * expf(gam[r] - gam[c]) : 0.f;
-        });
+    umma::tf32r_inplace(Qs, 64 * 128 * 2 + 128 * 128 + 128 * 64);   // Q, K, S0, U^T
+    umma::fence_smem_to_async();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t tD1 = tmem, tD3 = tmem + 64, tD2 = tmem + 192;
+    if (tid == 0) {
+        umma::mma_tf32(tD1, Qs, 128, Ks, 128, 64, 64, 128, false);
+        umma::mma_tf32(tD3, Qs, 128, Ss, 128, 64, 128, 128, false);
+        umma::commit(mbar);
     }
+    bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+    umma::fence_after_sync();
+    const int win = warp & 3, half = warp >> 2;
+    const int i = win * 16 + lane;     // row held by lanes 0..15 (M = 64 layout)
+    if (ok) {   // P = D1 (.) Gam (.) M  -> K-major rows i
+        for (int cc = 0; cc < 32; cc += 16) {
+            float v[16];
+            const int j0 = half * 32 + cc;
+            umma::tmem_ld16(umma::tmem_at(tD1, j0), v);
+            if (lane < 16) {
+#pragma unroll
+                for (int u = 0; u < 16; u += 4) {
+                    float4 p;
+                    const int j = j0 + u;
+                    p.x = (j + 0 <= i) ? v[u + 0] * expf(gam[i] - gam[j + 0]) : 0.f;
+                    p.y = (j + 1 <= i) ? v[u + 1] * expf(gam[i] - gam[j + 1]) : 0.f;
+                    p.z = (j + 2 <= i) ? v[u + 2] * expf(gam[i] - gam[j + 2]) : 0.f;
+                    p.w = (j + 3 <= i) ? v[u + 3] * expf(gam[i] - gam[j + 3]) : 0.f;
+                    *reinterpret_cast<float4*>(Ps + umma::kidx(i, j, 64)) = umma::tf32r(p);
+                }
+            }
+        }
+    }
+    umma::fence_smem_to_async();
+    umma::fence_before_sync();
     __syncthreads();
-    using TO = Tile<64, kD, 8>;
-    typename TO::Acc acc;
-    tile_zero<64, kD, 8>(acc);
-    tile_mma<64, kD, 64, 8>(acc, [&](int r, int k) { return Ps[r * kLdA + k]; },
-                            [&](int k, int c) { return Us[k * kLdV + c]; });
-    tile_mma<64, kD, kD, 8>(acc, [&](int r, int k) { return eg[r] * Qs[r * kLdK + k]; },
-                            [&](int k, int c) { return Ss[c * kLdK + k]; });
+    umma::fence_after_sync();
+    if (ok && tid == 0) {
+        umma::mma_tf32(tD2, Ps, 64, UT, 64, 64, 128, 64, false);
+        umma::commit(mbar);
+    }
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
+    umma::fence_after_sync();
+    float o[64];
+    float ss = 0.f;
+    if (ok) {
+        for (int cc = 0; cc < 64; cc += 16) {
+            float v2[16], v3[16];
+            umma::tmem_ld16(umma::tmem_at(tD2, half * 64 + cc), v2);
+            umma::tmem_ld16(umma::tmem_at(tD3, half * 64 + cc), v3);
+#pragma unroll
+            for (int u = 0; u < 16; u++) {
+                const float x = v2[u] + eg[i & 63] * v3[u];
+                o[cc + u] = x;
+                ss += x * x;
+            }
+        }
+        if (lane < 16) ssq[half * 64 + i] = ss;
+    } else if (tid == 0) {
+        atomicExch(sv.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
+    }
+    umma::fence_before_sync();
     __syncthreads();
-    float* Os = Qs;
-    tile_each2<64, kD, 8>(acc, [&](int r, int c, float& v0, float& v1) {
-        *reinterpret_cast<float2*>(Os + r * kLdK + c) = make_float2(v0, v1);
-    });
-    __syncthreads();
-    // gated RMSNorm, one warp per row, lane = 4 columns
-    const int lane = tid & 31, warp = tid >> 5;
-    float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (z) w4 = ld4(norm_w + lane * 4);
-    for (int r = warp; r < L; r += 8) {
-        const int64_t t = ci.start + r;
-        const int64_t off = (t * hv + h) * kD + lane * 4;
-        float4 o4 = ld4(Os + r * kLdK + lane * 4);
-        st4(sv.o + off, o4);
-        if (o_out) st4(o_out + off, o4);
+    if (warp == 0) umma::tmem_free(tmem, 512);
+    if (!ok || lane >= 16 || i >= L) return;
+    const int64_t t = ci.start + i;
+    const int64_t off = (t * hv + h) * kD + half * 64;
+    float rs = 0.f;
+    if (z) rs = rsqrtf((ssq[i] + ssq[64 + i]) * (1.f / kD) + norm_eps);
+#pragma unroll
+    for (int u = 0; u < 64; u += 4) {
+        const float4 o4 = make_float4(o[u], o[u + 1], o[u + 2], o[u + 3]);
+        st4(sv.o + off + u, o4);
+        if (o_out) st4(o_out + off + u, o4);
         if (z) {
-            float ss = warp_sum(o4.x * o4.x + o4.y * o4.y + o4.z * o4.z + o4.w * o4.w);
-            float rs = rsqrtf(ss * (1.f / kD) + norm_eps);
-            float4 z4 = ld4(z + off), y4;
+            const float4 w4 = ld4(norm_w + half * 64 + u);
+            const float4 z4 = ld4(z + off + u);
+            float4 y4;
             y4.x = o4.x * rs * (1.f + w4.x) * siluf_(z4.x);
             y4.y = o4.y * rs * (1.f + w4.y) * siluf_(z4.y);
             y4.z = o4.z * rs * (1.f + w4.z) * siluf_(z4.z);
             y4.w = o4.w * rs * (1.f + w4.w) * siluf_(z4.w);
-            st4(y_out + off, y4);
-            if (lane == 0) sv.rstd[t * hv + h] = rs;
+            st4(y_out + off + u, y4);
         }
     }
+    if (z && half == 0) sv.rstd[t * hv + h] = rs;
 }
 
 // ------------------------------------------------------------------ launchers
@@ -364,7 +493,7 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
     }
     if (a.N > 0) {
         GDN_PROF("chunk_state_fwd", st);
-        state_fwd_kernel<<<dim3(kD / kSlice, a.hv, a.N), 128, kStateSmem, st>>>(
+        state_fwd_kernel<<<dim3(kD / kSlice, a.hv, a.N), 256, kStateSmem, st>>>(
             a.qkv, a.hk, a.hv, a.S_init, a.S_final, a.sv);
     }
     if (a.NT > 0) {

@@ -51,6 +51,30 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// ----------------------------------------------------------------- async copies
+// 16-byte global->shared copy that bypasses L1; with pred false it writes 16
+// zero bytes and reads nothing (src must still be a valid address).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool pred) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    const int n = pred ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n)
+                 : "memory");
+}
+// 4-byte variant (through L1) for rows that start at an arbitrary element.
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem, bool pred) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    const int n = pred ? 4 : 0;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(s), "l"(gmem), "r"(n)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 // ----------------------------------------------------------------- tensor cores
 __device__ __forceinline__ uint32_t f2tf32(float x) {
     uint32_t r;

@@ -37,8 +37,9 @@ struct FwdSaved {
     int32_t* status;       // device status word
     ChunkInfo* chunks;     // [NT]
     int32_t* seq_chunk;    // [N+1] first chunk of each sequence
-    float* gam;            // [T, Hv] in-chunk cumulative gate
-    float* beta;           // [T, Hv]
+    int64_t T;             // total tokens
+    float* gam;            // [Hv, T] in-chunk cumulative gate (head-major)
+    float* beta;           // [Hv, T]
     float* W;              // [T, Hv, d]
     float* U;              // [T, Hv, d]  (U~ from prep, then U)
     float* S0;             // [NT, Hv, d, d] state at each chunk start
@@ -75,15 +76,17 @@ struct ChunkArgs {
 };
 
 struct BwdScratch {
+    int32_t* status; // device status word of the backward workspace
     float* dO;       // [T, Hv, d]
     float* dU;       // [T, Hv, d]
-    float* dS;       // [NT, Hv, d, d] gradient of the state at each chunk end
+    float* dS;       // [NT, Hv, d_k, d_v] gradient of the state at each chunk end, transposed
     float* dQv;      // [T, Hv, d] per v-head dq^
     float* dKv;      // [T, Hv, d] per v-head dk^
     float* dW;       // [T, Hv, d]
     float* dgam;     // [T, Hv] partial dgamma from the state-facing terms
     float* dgs;      // [T, Hv] dg (per token)
     float* nw_part;  // [NT * Hv, d] dnorm_w partials
+    float* Tm;       // [NT * Hv, 64, 64] (I + A)^-1 per chunk, row-major
 };
 
 cudaError_t launch_plan(const int32_t* cu, int N, int64_t T, int NT, FwdSaved sv, cudaStream_t st);

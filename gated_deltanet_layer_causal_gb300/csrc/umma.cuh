@@ -1,0 +1,154 @@
+// tcgen05 (5th-generation tensor core) helpers for sm_103a: tensor-memory
+// allocation, shared-memory matrix descriptors, MMA issue, commit to an
+// mbarrier, bounded waits, and tensor-memory loads.
+//
+// Operands live in shared memory in the no-swizzle K-major layout: an R x Kd
+// fp32 (tf32) tile is a grid of core matrices of 8 rows x 16 bytes (4
+// elements); core (r/8, k/4) sits at float offset ((r/8)*(Kd/4) + k/4)*32 and
+// row r%8 of it at +4*(r%8).  Adjacent cores along K are 128 B apart (the
+// descriptor's leading byte offset), adjacent 8-row groups (Kd/4)*128 B apart
+// (stride byte offset).  One 16-byte piece of a row-major global row is one
+// core-matrix row, so row-major tiles stage with plain 16-byte copies.
+//
+// Accumulators (fp32) live in tensor memory.  For M = 128, row i of D is lane
+// i; for M = 64, row i is lane (i % 16) + 32 * (i / 16).  Warp w reads lanes
+// 32*(w%4) .. 32*(w%4)+31.
+#pragma once
+
+#include <stdint.h>
+
+namespace gdn {
+namespace umma {
+
+__device__ __forceinline__ int kidx(int r, int k, int Kd) {
+    return (((r >> 3) * (Kd >> 2) + (k >> 2)) << 5) + ((r & 7) << 2) + (k & 3);
+}
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Descriptor of the K = 8 slice starting at column k0 of an R x Kd K-major tile.
+__device__ __forceinline__ uint64_t desc(const float* tile, int k0, int Kd) {
+    const uint32_t a = saddr(tile) + (uint32_t)(k0 >> 2) * 128u;
+    uint64_t d = (uint64_t)((a >> 4) & 0x3FFFu);
+    d |= (uint64_t)(128u >> 4) << 16;                          // leading byte offset
+    d |= (uint64_t)(((uint32_t)(Kd >> 2) * 128u) >> 4) << 32;  // stride byte offset
+    d |= (uint64_t)1 << 46;                                    // descriptor version
+    return d;                                                  // no swizzle, base offset 0
+}
+
+// Instruction descriptor: D fp32, A and B tf32, both K-major, M x N.
+__device__ __forceinline__ uint32_t idesc_tf32(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// D[M x N] (+)= A[M x K] * B[N x K]^T.  Issued by one thread.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, const float* A, int lda_k,
+                                         const float* B, int ldb_k, int M, int N, int K,
+                                         bool accumulate) {
+    const uint32_t id = idesc_tf32(M, N);
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        const uint64_t ad = desc(A, k0, lda_k), bd = desc(B, k0, ldb_k);
+        const uint32_t acc = (accumulate || k0 > 0) ? 1u : 0u;
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+            "l"(ad), "l"(bd), "r"(id), "r"(acc));
+    }
+}
+
+// Arrive on `mbar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void commit(uint64_t* mbar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+            saddr(mbar)));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* mbar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(saddr(mbar)), "r"(count));
+    asm volatile("fence.mbarrier_init.release.cluster;\n");
+}
+
+// Wait for phase `parity` of `mbar` to complete, at most `limit` polls.
+// Returns false (and the caller flags an error) if it gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, int limit = 1 << 24) {
+    uint32_t done = 0;
+    for (int it = 0; it < limit && !done; it++) {
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            "selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(saddr(mbar)), "r"(parity));
+    }
+    return done != 0;
+}
+
+// Generic-proxy shared-memory writes -> visible to the tensor core.
+__device__ __forceinline__ void fence_smem_to_async() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+
+// Tensor-memory allocation (whole warp).  The base address lands in *slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                     saddr(slot)),
+                 "r"(ncols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+}
+__device__ __forceinline__ void tmem_free(uint32_t base, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(base),
+                 "r"(ncols));
+}
+
+// 16 consecutive fp32 columns of this thread's lane, starting at `taddr`
+// (lane field already set to the warp's 32-lane window).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// Round to the nearest tf32 value (ties away from zero).  The tensor core reads
+// only the top 19 bits of an fp32 operand (it truncates), so operands are
+// rounded when they are written to shared memory: rounding then happens once,
+// to nearest, instead of being a truncation biased towards zero.
+__device__ __forceinline__ float tf32r(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+__device__ __forceinline__ float4 tf32r(float4 v) {
+    return make_float4(tf32r(v.x), tf32r(v.y), tf32r(v.z), tf32r(v.w));
+}
+// Round n floats (n % 4 == 0, 16-byte aligned) in place; whole CTA.
+__device__ __forceinline__ void tf32r_inplace(float* p, int n) {
+    for (int i = threadIdx.x * 4; i < n; i += blockDim.x * 4) {
+        float4* q = reinterpret_cast<float4*>(p + i);
+        *q = tf32r(*q);
+    }
+}
+
+// Tensor-memory address of (lane window of this warp, column col).
+__device__ __forceinline__ uint32_t tmem_at(uint32_t base, int col) {
+    const uint32_t lane0 = (uint32_t)((threadIdx.x >> 5) & 3) * 32u;
+    return base + (lane0 << 16) + (uint32_t)col;
+}
+
+}  // namespace umma
+}  // namespace gdn

@@ -36,6 +36,7 @@ def _check_group(out, ref, ch, heads, backward):
         errs["db"] = rel(f64(out["db"][:, heads]), ref["db"])
         errs["dA_log"] = rel(f64(out["dA_log"][heads]), ref["dA_log"])
         errs["ddt_bias"] = rel(f64(out["ddt_bias"][heads]), ref["ddt_bias"])
+    print("\nerrors: " + ", ".join(f"{k}={v:.2e}" for k, v in errs.items()))
     bad = {k: e for k, e in errs.items() if e > (TOL_STATE if k == "S_final" else TOL)}
     assert not bad, f"{bad} (all: {errs})"
     return errs

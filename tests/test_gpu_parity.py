@@ -25,6 +25,7 @@ def _cmp_group(out, ref, w, ch, heads, backward, tag=""):
         errs["db"] = rel(f64(out["db"])[:, heads], ref["db"])
         errs["dA_log"] = rel(f64(out["dA_log"])[heads], ref["dA_log"])
         errs["ddt_bias"] = rel(f64(out["ddt_bias"])[heads], ref["ddt_bias"])
+    print(f"\n{tag} errors: " + ", ".join(f"{k}={v:.2e}" for k, v in errs.items()))
     for k, e in errs.items():
         tol = TOL_STATE if k == "S_final" else TOL
         assert e <= tol, f"{tag} {k}: rel err {e:.3e} > {tol:.0e}  (all: {errs})"
