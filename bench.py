@@ -167,25 +167,28 @@ class Step:
 
 
 def kernel_cost(name: str, w: synth.Workload, NT: int):
-    """Algorithmic bytes of one launch of an HBM-bound kernel: the tensors it
-    must read and write, each once (its interface).  Notation: io = bytes per
-    activation, tk = one [T, H_k, d] fp32 tensor, tv = one [T, H_v, d] fp32
-    tensor, S = the per-chunk states [NT, H_v, d, d] fp32, g = [T, H_v] fp32."""
+    """Algorithmic bytes of one launch of a kernel: the tensors its interface
+    must read and write, each once.  Notation: io = bytes per activation,
+    tk = one [T, H_k, d] fp32 tensor, tv = one [T, H_v, d] fp32 tensor (or the
+    same bytes as per-chunk tiles), S = per-chunk states [NT, H_v, d, d] fp32,
+    Tt = per-chunk 64 x 64 tiles [NT, H_v] fp32, g = [T, H_v] fp32,
+    act = [T, H_v, d] in the I/O dtype."""
     T, C, H, Hk = w.T, w.C, w.h_v, w.h_k
     io = 2 if w.io == "bf16" else 4
     tk, tv = T * Hk * D * 4, T * H * D * 4
-    S, g, act = NT * H * D * D * 4, T * H * 4, T * H * D * io
+    S, Tt, g, act = NT * H * D * D * 4, NT * H * 64 * 64 * 4, T * H * 4, T * H * D * io
+    gates = 2 * T * H * io
     table = {
         "conv_fwd": T * C * io + T * C * 4,
         "conv_bwd": 2 * T * C * io + T * C * 4,
-        "chunk_prep": tk + tv + 2 * T * H * io + 2 * tv + 2 * g,
-        "chunk_state_fwd": tv + tk + tv + g + tv + S,
+        "chunk_prep": tk + tv + gates + 2 * tv + 2 * g,
+        "chunk_state_fwd": 2 * tv + tk + g + tv + 2 * S,
         "chunk_out_fwd": 2 * tk + tv + S + g + act + act + tv + g,
         "chunk_bwd_local": 2 * tk + tv + 2 * act + g + tv + act + tv,
-        "chunk_bwd_state": 2 * tk + 3 * tv + g + tv + S,
-        "chunk_bwd_sfacing": 2 * S + 3 * tv + 2 * tk + g + 3 * tv + g,
-        "chunk_bwd_wy": 2 * tk + tv + 4 * tv + 2 * tv + 3 * g + 2 * T * H * io + 2 * tv + tv
-                        + 2 * T * H * io,
+        "chunk_bwd_state": 2 * tk + 3 * tv + g + 2 * tv + S,
+        "chunk_bwd_sfacing": 2 * S + 3 * tv + 2 * tk + g + 4 * tv + g,
+        "chunk_bwd_dp": 2 * tk + 2 * tv + 3 * g + 2 * tv + 2 * tv + 2 * Tt + g,
+        "chunk_bwd_wy": tk + tv + 4 * tv + 2 * Tt + 3 * g + gates + tv + 2 * tv + gates + g,
         "gva_sum": 2 * tv + 2 * tk,
     }
     return "hbm", table.get(name), "B"
@@ -286,7 +289,8 @@ def run_ours(args, rank, world, dev):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "tokens": w.T, "seqs": w.N, "h_k": w.h_k,
                        "h_v": w.h_v, "d_k": D, "d_v": D, "chunk": 64, "conv_k": 4,
-                       "io": w.io, "state": "fp32", "mma": "tf32 mma.sync",
+                       "io": w.io, "state": "fp32",
+                       "mma": "tf32 tcgen05 (chunk kernels), tf32 mma.sync (state passes)",
                        "passes": "fwd+bwd (conv, chunk rule, fused gated norm)",
                        "l2": "inputs larger than L2 (x alone is %.2f GB)" % (
                            w.T * w.C * 2 / 1e9),

@@ -74,20 +74,32 @@ bwd_local_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z, con
     load_gam(gam, sv, ci, h);
     if (warp == 0) umma::tmem_alloc(tslot, 256);
     if (tid == 0) umma::mbar_init(mbar, 1);
-    // norm backward, one warp per row
+    // norm backward, one warp per row; a warp's 8 rows are loaded before any is used
     float4 wacc = zero4();
     const float4 w4 = z ? ld4(norm_w + lane * 4) : zero4();
-    for (int r = warp; r < 64; r += 8) {
+    float4 o8[8], z8[8], y8[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        const int r = warp + 8 * k;
+        const int64_t off = (row(r) * hv + h) * kD + lane * 4;
+        y8[k] = ld4(dy + off);
+        if (z) {
+            o8[k] = ld4(sv.o + off);
+            z8[k] = ld4(z + off);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        const int r = warp + 8 * k;
         float4 d4 = zero4();
         if (r < L) {
             const int64_t off = ((int64_t)(ci.start + r) * hv + h) * kD + lane * 4;
             if (z) {
-                NormRowGrad gr = norm_row_bwd(ld4(sv.o + off), ld4(z + off), ld4(dy + off), w4,
-                                              norm_eps, wacc);
+                NormRowGrad gr = norm_row_bwd(o8[k], z8[k], y8[k], w4, norm_eps, wacc);
                 d4 = gr.d_o;
                 st4(dz + off, gr.dz);
             } else {
-                d4 = ld4(dy + off);
+                d4 = y8[k];
             }
             st4(w.dO + off, d4);
         }
@@ -252,10 +264,11 @@ bwd_state_kernel(const float* __restrict__ qkv, int hk, int hv, const float* dS_
         float* dOc = dOs + slot * 64 * kLdS;
         float* dUc = dUs + slot * 64 * kLdS;
         const float* gc = gam + slot * 64;
-        // gradient of the state at this chunk's end, stored transposed: dS^T[b][a]
+        // gradient of the state at this chunk's end, stored as a K-major tile with
+        // rows b (the layout the state-facing kernel feeds to the tensor cores)
         const int64_t obase = ((int64_t)ci * hv + h) * kD * kD;
         tile_each2<kD, kSl, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
-            *reinterpret_cast<float2*>(w.dS + obase + (int64_t)b * kD + a0 + a) =
+            *reinterpret_cast<float2*>(w.dS + obase + umma::kidx(b, a0 + a, kD)) =
                 make_float2(v0, v1);
         });
         if (tid < 64) {
@@ -270,10 +283,12 @@ bwd_state_kernel(const float* __restrict__ qkv, int hk, int hv, const float* dS_
                                  [&](int b, int a) { return dSt[b * kLdS + a]; });
         __syncthreads();                    // K and dS^T reads done
         if (more) issue_k(prev);
+        float* dUt = w.dUt + ((int64_t)ci * hv + h) * kD * 64;
         tile_each<64, kSl, 8>(uacc, [&](int i, int a, float& v) {
             const float u = i < L ? dUc[i * kLdS + a] + v : 0.f;
             dUc[i * kLdS + a] = u;
             if (i < L) w.dU[((int64_t)(info.start + i) * hv + h) * kD + a0 + a] = u;
+            dUt[umma::kidx(a0 + a, i, 64)] = umma::tf32r(u);
         });
         __syncthreads();
         // dS^T = e^{gam_L} dS^T + Q~^T dO - W^T dU
@@ -334,23 +349,12 @@ bwd_sfacing_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, B
         cp_async16(A1 + umma::kidx(64 + r, c, 128), w.dU + off, r < L);
         cp_async16(A2 + umma::kidx(r, c, 128), sv.U + off, r < L);
     }
-    for (int idx = tid; idx < 128 * 32; idx += 256) {     // dS^T rows b, straight
-        const int b = idx >> 5, c = (idx & 31) * 4;
-        cp_async16(DST + umma::kidx(b, c, 128), w.dS + sb + (int64_t)b * kD + c, true);
+    // dS^T and S0^T are stored as K-major tiles with rows b: straight copies
+    for (int idx = tid; idx < 128 * 32; idx += 256) {
+        cp_async16(DST + idx * 4, w.dS + sb + idx * 4, true);
+        cp_async16(S0T + idx * 4, sv.S0b + sb + idx * 4, true);
     }
     cp_async_commit();
-    {   // S0 [a][b] -> S0^T rows b: lane = b, four rows a per 16-byte store
-        const float* S0 = sv.S0 + sb;
-        for (int idx = tid; idx < 128 * 32; idx += 256) {
-            const int b = idx & 127, a4 = idx >> 7;
-            float4 v;
-            v.x = S0[(int64_t)(4 * a4 + 0) * kD + b];
-            v.y = S0[(int64_t)(4 * a4 + 1) * kD + b];
-            v.z = S0[(int64_t)(4 * a4 + 2) * kD + b];
-            v.w = S0[(int64_t)(4 * a4 + 3) * kD + b];
-            *reinterpret_cast<float4*>(S0T + umma::kidx(b, 4 * a4, 128)) = v;
-        }
-    }
     load_gam(gam, sv, ci, h);
     if (warp == 0) umma::tmem_alloc(tslot, 256);
     if (tid == 0) umma::mbar_init(mbar, 1);
@@ -407,12 +411,16 @@ bwd_sfacing_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, B
                     }
                 } else {
                     const int i = r - 64;
+                    float* dWt = w.dWt + ((int64_t)blockIdx.x * hv + h) * kD * 64;
                     if (i < L) {
                         float* dst = w.dW + (row(i) * hv + h) * kD + c0 + cc;
 #pragma unroll
                         for (int u = 0; u < 16; u += 4)
                             st4(dst + u, make_float4(-v[u], -v[u + 1], -v[u + 2], -v[u + 3]));
                     }
+#pragma unroll
+                    for (int u = 0; u < 16; u++)
+                        dWt[umma::kidx(c0 + cc + u, i, 64)] = i < L ? umma::tf32r(-v[u]) : 0.f;
                 }
             }
             if (r < 64) rpart[half * 128 + r] = r < L ? eg[r] * part : 0.f;
@@ -522,6 +530,14 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
     }
     bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
+    // the first products are complete: fetch Q and K rows (row-major) into the
+    // dO / U space while the epilogue runs
+    for (int idx = tid; idx < 64 * 32; idx += 256) {
+        const int r = idx >> 5, c = (idx & 31) * 4;
+        cp_async16(dOs + r * 128 + c, qb + row(r) * C + c, r < L);
+        cp_async16(Us + r * 128 + c, kb + row(r) * C + c, r < L);
+    }
+    cp_async_commit();
     const int win = warp & 3, half = warp >> 2;
     const int i = win * 16 + lane;     // D row (lanes 0..15)
     if (ok) {
@@ -555,23 +571,14 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
         if (lane < 16) rpart[half * 64 + i] = rsum;
     }
     __syncthreads();
-    // the first MMAs are done: Q^T and K^T (rows b, k = token) replace dO and U
-    float* QT = dOs;
-    float* KT = Us;
-    for (int idx = tid; idx < 128 * 16; idx += 256) {
-        const int bcol = idx & 127, j4 = idx >> 7;
-        float4 q4, k4;
-        q4.x = 4 * j4 + 0 < L ? qb[row(4 * j4 + 0) * C + bcol] : 0.f;
-        q4.y = 4 * j4 + 1 < L ? qb[row(4 * j4 + 1) * C + bcol] : 0.f;
-        q4.z = 4 * j4 + 2 < L ? qb[row(4 * j4 + 2) * C + bcol] : 0.f;
-        q4.w = 4 * j4 + 3 < L ? qb[row(4 * j4 + 3) * C + bcol] : 0.f;
-        k4.x = 4 * j4 + 0 < L ? kb[row(4 * j4 + 0) * C + bcol] : 0.f;
-        k4.y = 4 * j4 + 1 < L ? kb[row(4 * j4 + 1) * C + bcol] : 0.f;
-        k4.z = 4 * j4 + 2 < L ? kb[row(4 * j4 + 2) * C + bcol] : 0.f;
-        k4.w = 4 * j4 + 3 < L ? kb[row(4 * j4 + 3) * C + bcol] : 0.f;
-        *reinterpret_cast<float4*>(QT + umma::kidx(bcol, 4 * j4, 64)) = umma::tf32r(q4);
-        *reinterpret_cast<float4*>(KT + umma::kidx(bcol, 4 * j4, 64)) = umma::tf32r(k4);
-    }
+    // the first MMAs are done: Q and K rows (row-major, in the dO / U space) are
+    // transposed into Q^T and K^T (rows b, k = token) in the Q / K space
+    float* QT = Qs;
+    float* KT = Ks;
+    cp_async_wait<0>();
+    __syncthreads();
+    umma::transpose_rows_to_kmajor(QT, dOs, 128, nullptr);
+    umma::transpose_rows_to_kmajor(KT, Us, 128, nullptr);
     if (tid < 64) {   // dgam from R: row sums minus column sums (fixed order)
         float cs = 0.f;
         for (int r = 0; r < 64; r++) cs += Rm[r * 65 + tid];
@@ -587,14 +594,18 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
         umma::commit(mbar);
     }
     // the triangular solve overlaps the MMAs
-    tril_inverse64(As, kM4, Tr, kM4);
+    tril_inverse64(As, kM4, Tr, kM4, Rm);     // R is consumed: scratch
     __syncthreads();
-    {
-        float* Tg = w.Tm + ((int64_t)blockIdx.x * hv + h) * 64 * 64;
+    {   // T as K-major rows i and as K-major rows j (T^T), tf32-rounded MMA operands
+        float* Tg = w.Tm + ((int64_t)blockIdx.x * hv + h) * 2 * 64 * 64;
         for (int idx = tid; idx < 64 * 16; idx += 256) {
-            const int r = idx >> 4, c = (idx & 15) * 4;
-            st4(Tg + r * 64 + c, make_float4(Tr[r * kM4 + c], Tr[r * kM4 + c + 1],
-                                             Tr[r * kM4 + c + 2], Tr[r * kM4 + c + 3]));
+            const int r = idx & 63, c4 = idx >> 6;
+            st4(Tg + umma::kidx(r, 4 * c4, 64),
+                umma::tf32r(make_float4(Tr[r * kM4 + 4 * c4], Tr[r * kM4 + 4 * c4 + 1],
+                                        Tr[r * kM4 + 4 * c4 + 2], Tr[r * kM4 + 4 * c4 + 3])));
+            st4(Tg + 64 * 64 + umma::kidx(r, 4 * c4, 64),
+                umma::tf32r(make_float4(Tr[(4 * c4) * kM4 + r], Tr[(4 * c4 + 1) * kM4 + r],
+                                        Tr[(4 * c4 + 2) * kM4 + r], Tr[(4 * c4 + 3) * kM4 + r])));
         }
     }
     if (tid < 64 && tid < L) w.dgam[(int64_t)(ci.start + tid) * hv + h] += dgl[tid];
@@ -662,6 +673,7 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
     float* dKC = dKR + 64 * 64;        // [64 (j)][64 (m)] K-major dKK^T
     float* KT = dKC + 64 * 64;         // [128 (b)][64 (m)] K-major K^T
     float* Rm = KT + 128 * 64;         // [64][65] row-major
+    float* Kr = Rm + 64 * 65;          // [64][128] row-major K (staging for K^T)
     float* gam = TC + 64 * 64;
     float* eg = gam + 64;
     float* bet = eg + 64;
@@ -683,7 +695,8 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
     auto vrow = [&](int r) { return (row(r) * hv + h) * kD; };
     const float* kb = qkv + (int64_t)hk * kD + kh * kD;
     const float* vb = qkv + (int64_t)2 * hk * kD + h * kD;
-    const float* Tg = w.Tm + ((int64_t)blockIdx.x * hv + h) * 64 * 64;
+    const float* Tg = w.Tm + ((int64_t)blockIdx.x * hv + h) * 2 * 64 * 64;   // T, then T^T
+    const int64_t tile = (int64_t)blockIdx.x * hv + h;
     for (int idx = tid; idx < 64 * 32; idx += 256) {
         const int r = idx >> 5, c = (idx & 31) * 4;
         cp_async16(Ks + umma::kidx(r, c, 128), kb + row(r) * C + c, r < L);
@@ -691,23 +704,13 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
         cp_async16(dWs + umma::kidx(r, c, 128), w.dW + vrow(r) + c, r < L);
         cp_async16(dUs + umma::kidx(r, c, 128), w.dU + vrow(r) + c, r < L);
     }
+    // [dW^T ; dU^T] and T^T arrive as K-major tiles written by their producers
+    for (int idx = tid; idx < 128 * 16; idx += 256) {
+        cp_async16(BW + idx * 4, w.dWt + tile * kD * 64 + idx * 4, true);
+        cp_async16(BW + 128 * 64 + idx * 4, w.dUt + tile * kD * 64 + idx * 4, true);
+    }
+    for (int idx = tid; idx < 64 * 16; idx += 256) cp_async16(TC + idx * 4, Tg + 64 * 64 + idx * 4, true);
     cp_async_commit();
-    for (int idx = tid; idx < 256 * 16; idx += 256) {   // [dW^T ; dU^T]: lane = column
-        const int n = idx & 255, i4 = idx >> 8;
-        const float* src = n < 128 ? w.dW + n : w.dU + (n - 128);
-        float4 v;
-        v.x = 4 * i4 + 0 < L ? src[vrow(4 * i4 + 0)] : 0.f;
-        v.y = 4 * i4 + 1 < L ? src[vrow(4 * i4 + 1)] : 0.f;
-        v.z = 4 * i4 + 2 < L ? src[vrow(4 * i4 + 2)] : 0.f;
-        v.w = 4 * i4 + 3 < L ? src[vrow(4 * i4 + 3)] : 0.f;
-        *reinterpret_cast<float4*>(BW + umma::kidx(n, 4 * i4, 64)) = v;
-    }
-    for (int idx = tid; idx < 64 * 16; idx += 256) {    // T^T: lane = j
-        const int j = idx & 63, i4 = idx >> 6;
-        *reinterpret_cast<float4*>(TC + umma::kidx(j, 4 * i4, 64)) =
-            make_float4(Tg[(4 * i4 + 0) * 64 + j], Tg[(4 * i4 + 1) * 64 + j],
-                        Tg[(4 * i4 + 2) * 64 + j], Tg[(4 * i4 + 3) * 64 + j]);
-    }
     load_gam(gam, sv, ci, h);
     if (tid < 64) {
         bet[tid] = tid < L ? sv.beta[(int64_t)h * sv.T + ci.start + tid] : 0.f;
@@ -723,7 +726,7 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
     }
     cp_async_wait<0>();
     __syncthreads();
-    umma::tf32r_inplace(Ks, kWyFloats);   // K, V, dW, dU, [dW^T; dU^T], T^T
+    umma::tf32r_inplace(Ks, 4 * 64 * 128);   // K, V, dW, dU (the tiles arrive rounded)
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -741,6 +744,13 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
     }
     bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
+    // stage-1 operands are consumed: fetch T and the K rows for stage 2
+    for (int idx = tid; idx < 64 * 16; idx += 256) cp_async16(TR + idx * 4, Tg + idx * 4, true);
+    for (int idx = tid; idx < 64 * 32; idx += 256) {
+        const int rr = idx >> 5, c = (idx & 31) * 4;
+        cp_async16(Kr + rr * 128 + c, kb + row(rr) * C + c, rr < L);
+    }
+    cp_async_commit();
     const int win = warp & 3, half = warp >> 2;
     const int r = win * 16 + lane;     // D row (lanes 0..15)
     const bool live = lane < 16;
@@ -800,20 +810,10 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
         dbs[tid] += eg[tid] * rp[tid] + rp[64 + tid];
         dgs[tid] += be[tid] * rp[tid];
     }
-    // stage 2 operands: T rows (for Y^T = T dT^T) and K^T (for the dKK products)
-    for (int idx = tid; idx < 64 * 16; idx += 256) {
-        const int m = idx >> 4, c = (idx & 15) * 4;
-        *reinterpret_cast<float4*>(TR + umma::kidx(m, c, 64)) = umma::tf32r(ld4(Tg + m * 64 + c));
-    }
-    for (int idx = tid; idx < 128 * 16; idx += 256) {
-        const int bcol = idx & 127, m4 = idx >> 7;
-        float4 k4;
-        k4.x = 4 * m4 + 0 < L ? kb[row(4 * m4 + 0) * C + bcol] : 0.f;
-        k4.y = 4 * m4 + 1 < L ? kb[row(4 * m4 + 1) * C + bcol] : 0.f;
-        k4.z = 4 * m4 + 2 < L ? kb[row(4 * m4 + 2) * C + bcol] : 0.f;
-        k4.w = 4 * m4 + 3 < L ? kb[row(4 * m4 + 3) * C + bcol] : 0.f;
-        *reinterpret_cast<float4*>(KT + umma::kidx(bcol, 4 * m4, 64)) = umma::tf32r(k4);
-    }
+    // stage 2 operands: T arrived as a K-major tile; K^T from the staged K rows
+    cp_async_wait<0>();
+    __syncthreads();
+    umma::transpose_rows_to_kmajor(KT, Kr, 128, nullptr);
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();

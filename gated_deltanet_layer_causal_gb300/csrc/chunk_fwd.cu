@@ -76,7 +76,7 @@ __global__ void plan_kernel(const int32_t* __restrict__ cu, int N, int64_t T, in
 //   D2 = T [diag(beta e^gam) K | diag(beta) V]   (one M=64, N=256, K=64 MMA)
 // giving W = D2[:, :128] and U~ = D2[:, 128:].
 constexpr int kLdK = 132, kLdV = 136, kLdA = 68;
-constexpr int kPrepFloats = 64 * 128 + 256 * 64 + 2 * 64 * kLdA + 64 * 64;
+constexpr int kPrepFloats = 64 * 128 + 256 * 64 + 2 * 64 * kLdA + 64 * 64 + 2 * 64 * kLdK;
 constexpr size_t kPrepSmem = sizeof(float) * (kPrepFloats + 3 * 64 + 16) + 64;
 
 template <class IO>
@@ -90,7 +90,9 @@ prep_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO* 
     float* As = Bs + 256 * 64;         // [64][kLdA] row-major A
     float* Tr = As + 64 * kLdA;        // [64][kLdA] row-major T
     float* Tk = Tr + 64 * kLdA;        // [64][64] K-major T
-    float* gam = Tk + 64 * 64;
+    float* Kr = Tk + 64 * 64;          // [64][kLdK] row-major K (staging)
+    float* Vr = Kr + 64 * kLdK;        // [64][kLdK] row-major V (staging)
+    float* gam = Vr + 64 * kLdK;
     float* bet = gam + 64;
     float* be = bet + 64;
     uint64_t* mbar = reinterpret_cast<uint64_t*>(be + 64 + 16);
@@ -106,6 +108,8 @@ prep_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO* 
     for (int idx = tid; idx < 64 * 32; idx += 256) {
         const int r = idx >> 5, c = (idx & 31) * 4;
         cp_async16(Ks + umma::kidx(r, c, 128), kbase + row(r) * C + c, r < L);
+        cp_async16(Kr + r * kLdK + c, kbase + row(r) * C + c, r < L);
+        cp_async16(Vr + r * kLdK + c, vbase + row(r) * C + c, r < L);
     }
     cp_async_commit();
     if (tid < 64) {
@@ -131,21 +135,12 @@ prep_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO* 
         }
     }
     __syncthreads();
-    // B operand rows: c (0..127) = be_j K[j][c], 128 + a = beta_j V[j][a]; lane = column
-    for (int idx = tid; idx < 256 * 16; idx += 256) {
-        const int n = idx & 255, j4 = idx >> 8;
-        const float* src = n < 128 ? kbase + n : vbase + (n - 128);
-        const float* sc = n < 128 ? be : bet;
-        float4 v;
-        v.x = 4 * j4 + 0 < L ? sc[4 * j4 + 0] * src[row(4 * j4 + 0) * C] : 0.f;
-        v.y = 4 * j4 + 1 < L ? sc[4 * j4 + 1] * src[row(4 * j4 + 1) * C] : 0.f;
-        v.z = 4 * j4 + 2 < L ? sc[4 * j4 + 2] * src[row(4 * j4 + 2) * C] : 0.f;
-        v.w = 4 * j4 + 3 < L ? sc[4 * j4 + 3] * src[row(4 * j4 + 3) * C] : 0.f;
-        *reinterpret_cast<float4*>(Bs + umma::kidx(n, 4 * j4, 64)) = v;
-    }
     cp_async_wait<0>();
     __syncthreads();
-    umma::tf32r_inplace(Ks, 64 * 128 + 256 * 64);   // K and the B operand (contiguous)
+    // B operand: rows c (0..127) = be_j K[j][c], rows 128 + a = beta_j V[j][a]
+    umma::transpose_rows_to_kmajor(Bs, Kr, kLdK, be);
+    umma::transpose_rows_to_kmajor(Bs + 128 * 64, Vr, kLdK, bet);
+    umma::tf32r_inplace(Ks, 64 * 128);
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -173,7 +168,7 @@ prep_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO* 
         }
     }
     __syncthreads();
-    tril_inverse64(As, kLdA, Tr, kLdA);
+    tril_inverse64(As, kLdA, Tr, kLdA, Tk);   // Tk doubles as scratch
     __syncthreads();
     for (int idx = tid; idx < 64 * 16; idx += 256) {   // T -> K-major rows i
         const int r = idx >> 4, c = (idx & 15) * 4;
@@ -282,11 +277,14 @@ state_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const float* S_i
         } else {
             cp_async_wait<0>();
         }
-        // state at the chunk start, for the output and the backward
+        // state at the chunk start, for the output and the backward, written in
+        // the two K-major tile layouts its consumers feed to the tensor cores
         const int64_t obase = ((int64_t)ci * hv + h) * kD * kD;
         tile_each2<kD, kSlice, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
-            sv.S0[obase + (int64_t)(a0 + a) * kD + b] = v0;
-            sv.S0[obase + (int64_t)(a0 + a + 1) * kD + b] = v1;
+            sv.S0[obase + umma::kidx(a0 + a, b, kD)] = v0;
+            sv.S0[obase + umma::kidx(a0 + a + 1, b, kD)] = v1;
+            *reinterpret_cast<float2*>(sv.S0b + obase + umma::kidx(b, a0 + a, kD)) =
+                make_float2(v0, v1);
         });
         __syncthreads();   // this chunk's tiles have landed (and St is current)
         if (tid < 64) fk[tid] = tid < L ? expf(cur.gam[L - 1] - cur.gam[tid]) : 0.f;
@@ -323,7 +321,7 @@ state_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const float* S_i
 //   O  = D2 + e^{gam_i} D3 ; y = O rsqrt(mean(O^2)+eps) (1+w) silu(z)
 // Shared memory (K-major core layout): Q, K 32 KB each, S0 (rows a) 64 KB,
 // U^T (rows a, k = token) 32 KB, P 16 KB.  Tensor memory: 320 fp32 columns.
-constexpr int kOutFloats = 64 * 128 * 2 + 128 * 128 + 128 * 64 + 64 * 64;
+constexpr int kOutFloats = 64 * 128 * 2 + 128 * 128 + 128 * 64 + 64 * 64 + 64 * kLdK;
 constexpr size_t kOutSmem = sizeof(float) * (kOutFloats + 64 * 2 + 2 * 64 + 16) + 64;
 
 template <class IO>
@@ -336,7 +334,8 @@ out_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z,
     float* Ss = Ks + 64 * 128;         // [128 (a)][128 (b)]
     float* UT = Ss + 128 * 128;        // [128 (a)][64 (j)]
     float* Ps = UT + 128 * 64;         // [64 (i)][64 (j)]
-    float* gam = Ps + 64 * 64;
+    float* Ur = Ps + 64 * 64;          // [64][kLdK] row-major U (staging)
+    float* gam = Ur + 64 * kLdK;
     float* eg = gam + 64;
     float* ssq = eg + 64;              // [2][64] partial sums of squares
     uint64_t* mbar = reinterpret_cast<uint64_t*>(ssq + 2 * 64 + 16);
@@ -353,21 +352,13 @@ out_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z,
         cp_async16(Ks + umma::kidx(r, c, 128), qkv + row(r) * C + (int64_t)hk * kD + kh * kD + c,
                    r < L);
     }
-    const float* S0 = sv.S0 + ((int64_t)blockIdx.x * hv + h) * kD * kD;
-    for (int idx = tid; idx < 128 * 32; idx += 256) {
+    const float* S0 = sv.S0 + ((int64_t)blockIdx.x * hv + h) * kD * kD;   // K-major rows a
+    for (int idx = tid; idx < 128 * 32; idx += 256) cp_async16(Ss + idx * 4, S0 + idx * 4, true);
+    for (int idx = tid; idx < 64 * 32; idx += 256) {
         const int r = idx >> 5, c = (idx & 31) * 4;
-        cp_async16(Ss + umma::kidx(r, c, 128), S0 + r * kD + c, true);
+        cp_async16(Ur + r * kLdK + c, sv.U + (row(r) * hv + h) * kD + c, r < L);
     }
     cp_async_commit();
-    for (int idx = tid; idx < 128 * 16; idx += 256) {   // U^T: lane = a, 4 tokens per store
-        const int a = idx & 127, j4 = idx >> 7;
-        float4 v;
-        v.x = 4 * j4 + 0 < L ? sv.U[(row(4 * j4 + 0) * hv + h) * kD + a] : 0.f;
-        v.y = 4 * j4 + 1 < L ? sv.U[(row(4 * j4 + 1) * hv + h) * kD + a] : 0.f;
-        v.z = 4 * j4 + 2 < L ? sv.U[(row(4 * j4 + 2) * hv + h) * kD + a] : 0.f;
-        v.w = 4 * j4 + 3 < L ? sv.U[(row(4 * j4 + 3) * hv + h) * kD + a] : 0.f;
-        *reinterpret_cast<float4*>(UT + umma::kidx(a, 4 * j4, 64)) = v;
-    }
     if (tid < 64) {  // padding rows continue the last gate value (g = 0)
         const float g = sv.gam[(int64_t)h * sv.T + row(tid)];
         gam[tid] = g;
@@ -377,7 +368,8 @@ out_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z,
     if (tid == 0) umma::mbar_init(mbar, 1);
     cp_async_wait<0>();
     __syncthreads();
-    umma::tf32r_inplace(Qs, 64 * 128 * 2 + 128 * 128 + 128 * 64);   // Q, K, S0, U^T
+    umma::tf32r_inplace(Qs, 64 * 128 * 2 + 128 * 128);   // Q, K, S0
+    umma::transpose_rows_to_kmajor(UT, Ur, kLdK, nullptr);
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();

@@ -275,22 +275,68 @@ __device__ __forceinline__ void warp_cumsum64(float* v) {
 }
 
 // T = (I + A)^-1 for strictly lower A [64][lda] (unit lower-triangular
-// inverse) by forward substitution, column by column: T_ij = -sum_{m=j}^{i-1}
-// A_im T_mj.  256 threads: 4 lanes per column split each dot product.
-__device__ __forceinline__ void tril_inverse64(const float* As, int lda, float* Ts, int ldt) {
-    const int tid = threadIdx.x, j = tid >> 2, q = tid & 3;
-    for (int i = q; i < kChunk; i += 4) Ts[i * ldt + j] = (i == j) ? 1.f : 0.f;
-    __syncwarp();
-    const int ibeg = (tid >> 5) * 8 + 1;  // first row any lane of this warp needs
-    for (int i = ibeg; i < kChunk; i++) {
-        float p = 0.f;
-        if (i > j)
-            for (int m = j + q; m < i; m += 4) p += As[i * lda + m] * Ts[m * ldt + j];
-        p += __shfl_xor_sync(0xffffffffu, p, 1);
-        p += __shfl_xor_sync(0xffffffffu, p, 2);
-        if (i > j && q == 0) Ts[i * ldt + j] = -p;
-        __syncwarp();
+// inverse), 256 threads.  Blocked: the four 16 x 16 diagonal blocks by forward
+// substitution (T_ij = -sum_{m=j}^{i-1} A_im T_mj, one thread per column), then
+// two merge levels of the block formula
+//   [[L11, 0], [L21, L22]]^-1 = [[T11, 0], [-T22 L21 T11, T22]]
+// (16 -> 32, then 32 -> 64) as small products on the CUDA cores.
+// X is 32 x 32 scratch.
+__device__ __forceinline__ void tril_inverse64(const float* As, int lda, float* Ts, int ldt,
+                                               float* X) {
+    const int tid = threadIdx.x;
+    for (int e = tid; e < kChunk * kChunk; e += 256) Ts[(e >> 6) * ldt + (e & 63)] = 0.f;
+    __syncthreads();
+    if (tid < kChunk) {   // diagonal blocks: thread = column j
+        const int j = tid, end = (j | 15) + 1;
+        Ts[j * ldt + j] = 1.f;
+        for (int i = j + 1; i < end; i++) {
+            float acc = 0.f;
+            for (int m = j; m < i; m++) acc += As[i * lda + m] * Ts[m * ldt + j];
+            Ts[i * ldt + j] = -acc;
+        }
     }
+    __syncthreads();
+    // 16 -> 32: for the pairs (0,1) and (2,3) of 16-blocks, X = L21 T11, T21 = -T22 X
+    {
+        const int p = tid >> 7, e = tid & 127;          // pair, element group
+        const int r0 = 32 * p, r1 = r0 + 16;
+#pragma unroll
+        for (int q = 0; q < 2; q++) {
+            const int i = (e >> 4) + 8 * q, jj = e & 15;
+            float acc = 0.f;
+            for (int m = 0; m < 16; m++) acc += As[(r1 + i) * lda + r0 + m] * Ts[(r0 + m) * ldt + r0 + jj];
+            X[p * 256 + i * 16 + jj] = acc;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 2; q++) {
+            const int i = (e >> 4) + 8 * q, jj = e & 15;
+            float acc = 0.f;
+            for (int m = 0; m <= i; m++) acc += Ts[(r1 + i) * ldt + r1 + m] * X[p * 256 + m * 16 + jj];
+            Ts[(r1 + i) * ldt + r0 + jj] = -acc;
+        }
+    }
+    __syncthreads();
+    // 32 -> 64: X = L21 T11 (32 x 32), T21 = -T22 X
+    {
+        const int jj = tid & 31, i0 = tid >> 5;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int i = i0 + 8 * q;
+            float acc = 0.f;
+            for (int m = 0; m < 32; m++) acc += As[(32 + i) * lda + m] * Ts[m * ldt + jj];
+            X[i * 32 + jj] = acc;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int i = i0 + 8 * q;
+            float acc = 0.f;
+            for (int m = 0; m <= i; m++) acc += Ts[(32 + i) * ldt + 32 + m] * X[m * 32 + jj];
+            Ts[(32 + i) * ldt + jj] = -acc;
+        }
+    }
+    __syncthreads();
 }
 
 // Varlen plan entry of one chunk: first token, length, sequence, chunk within sequence.

@@ -144,6 +144,24 @@ __device__ __forceinline__ void tf32r_inplace(float* p, int n) {
     }
 }
 
+// Row-major smem tile R [64 tokens][ldr] (128 columns) -> K-major tile
+// [128 (column)][64 (token)], rows optionally scaled per token, tf32-rounded.
+// Reads: lanes take consecutive columns of one row; writes: 8 consecutive
+// columns fill 8 distinct 16-byte bank groups -- no bank conflicts.
+__device__ __forceinline__ void transpose_rows_to_kmajor(float* dst, const float* R, int ldr,
+                                                         const float* scale) {
+    for (int idx = threadIdx.x; idx < 128 * 16; idx += blockDim.x) {
+        const int c = idx & 127, j4 = idx >> 7;
+        float4 v = make_float4(R[(4 * j4 + 0) * ldr + c], R[(4 * j4 + 1) * ldr + c],
+                               R[(4 * j4 + 2) * ldr + c], R[(4 * j4 + 3) * ldr + c]);
+        if (scale) {
+            v.x *= scale[4 * j4 + 0]; v.y *= scale[4 * j4 + 1];
+            v.z *= scale[4 * j4 + 2]; v.w *= scale[4 * j4 + 3];
+        }
+        *reinterpret_cast<float4*>(dst + kidx(c, 4 * j4, 64)) = tf32r(v);
+    }
+}
+
 // Tensor-memory address of (lane window of this warp, column col).
 __device__ __forceinline__ uint32_t tmem_at(uint32_t base, int col) {
     const uint32_t lane0 = (uint32_t)((threadIdx.x >> 5) & 3) * 32u;
