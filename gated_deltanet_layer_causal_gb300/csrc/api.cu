@@ -90,6 +90,9 @@ BwdScratch carve_bwd(void* ws, const gdn_dims* d, int NT, int32_t** status, size
     s.dU = c.take<float>(T * H * kD);
     s.dQv = c.take<float>(T * H * kD);
     s.dKv = c.take<float>(T * H * kD);
+    s.dQv2 = c.take<float>(T * H * kD);
+    s.dKv2 = c.take<float>(T * H * kD);
+    s.dKv3 = c.take<float>(T * H * kD);
     s.dW = c.take<float>(T * H * kD);
     s.dS = c.take<float>((size_t)NT * H * kD * kD);
     s.dgam = c.take<float>(T * H);

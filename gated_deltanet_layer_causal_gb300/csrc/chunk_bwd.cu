@@ -383,6 +383,18 @@ bwd_sfacing_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, B
     }
     const bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
+    // the products are complete: stage the Q and K rows the dgam dot products
+    // need into the S0 / dS space (row-major, padded: conflict-free row reads)
+    float* Qr = S0T;
+    float* Kr = S0T + 64 * 132;
+    for (int idx = tid; idx < 64 * 32; idx += 256) {
+        const int r = idx >> 5, c = (idx & 31) * 4;
+        cp_async16(Qr + r * 132 + c, qkv + row(r) * C + kh * kD + c, r < L);
+        cp_async16(Kr + r * 132 + c, qkv + row(r) * C + (int64_t)hk * kD + kh * kD + c, r < L);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
     if (!ok) {
         if (tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
     } else {
@@ -399,7 +411,7 @@ bwd_sfacing_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, B
                     const int i = r;
                     if (i < L) {
                         float* dst = w.dQv + (row(i) * hv + h) * kD + c0 + cc;
-                        const float* q = qkv + row(i) * C + kh * kD + c0 + cc;
+                        const float* q = Qr + i * 132 + c0 + cc;
 #pragma unroll
                         for (int u = 0; u < 16; u += 4) {
                             const float4 q4 = ld4(q + u);
@@ -434,7 +446,7 @@ bwd_sfacing_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, B
                 umma::tmem_ld16(umma::tmem_at(tmem + 128, c0 + cc), v);
                 if (lane < 16 && j < L) {
                     float* dst = w.dKv + (row(j) * hv + h) * kD + c0 + cc;
-                    const float* k = qkv + row(j) * C + (int64_t)hk * kD + kh * kD + c0 + cc;
+                    const float* k = Kr + j * 132 + c0 + cc;
 #pragma unroll
                     for (int u = 0; u < 16; u += 4) {
                         const float4 k4 = ld4(k + u);
@@ -620,11 +632,8 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
                 const int64_t off = (row(i) * hv + h) * kD + half * 64 + cc;
 #pragma unroll
                 for (int u = 0; u < 16; u += 4) {
-                    float4 q = ld4(w.dQv + off + u), k = ld4(w.dKv + off + u);
-                    q.x += vq[u]; q.y += vq[u + 1]; q.z += vq[u + 2]; q.w += vq[u + 3];
-                    k.x += vk[u]; k.y += vk[u + 1]; k.z += vk[u + 2]; k.w += vk[u + 3];
-                    st4(w.dQv + off + u, q);
-                    st4(w.dKv + off + u, k);
+                    st4(w.dQv2 + off + u, make_float4(vq[u], vq[u + 1], vq[u + 2], vq[u + 3]));
+                    st4(w.dKv2 + off + u, make_float4(vk[u], vk[u + 1], vk[u + 2], vk[u + 3]));
                 }
             }
         }
@@ -899,14 +908,10 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
             if (live && r < L) {
                 const int64_t off = vrow(r) + half * 64 + cc;
 #pragma unroll
-                for (int u = 0; u < 16; u += 4) {
-                    float4 k = ld4(w.dKv + off + u);
-                    k.x += vk[u] + be[r] * vw[u];
-                    k.y += vk[u + 1] + be[r] * vw[u + 1];
-                    k.z += vk[u + 2] + be[r] * vw[u + 2];
-                    k.w += vk[u + 3] + be[r] * vw[u + 3];
-                    st4(w.dKv + off + u, k);
-                }
+                for (int u = 0; u < 16; u += 4)
+                    st4(w.dKv3 + off + u,
+                        make_float4(vk[u] + be[r] * vw[u], vk[u + 1] + be[r] * vw[u + 1],
+                                    vk[u + 2] + be[r] * vw[u + 2], vk[u + 3] + be[r] * vw[u + 3]));
             }
         }
     } else if (tid == 0) {
@@ -961,7 +966,9 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
 // ------------------------------------------------------------------ B4: GVA sum
 // dqkv q/k channels of k-head kh = sum over its G v-heads in order j = 0..G-1.
 __global__ void gva_sum_kernel(const float* __restrict__ dQv, const float* __restrict__ dKv,
-                               int64_t T, int hk, int hv, float* __restrict__ dqkv) {
+                               const float* __restrict__ dQv2, const float* __restrict__ dKv2,
+                               const float* __restrict__ dKv3, int64_t T, int hk, int hv,
+                               float* __restrict__ dqkv) {
     const int G = hv / hk, C = (2 * hk + hv) * kD;
     int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // over T * hk * 32
     if (idx >= T * hk * 32) return;
@@ -971,7 +978,11 @@ __global__ void gva_sum_kernel(const float* __restrict__ dQv, const float* __res
     float4 q = zero4(), k = zero4();
     for (int j = 0; j < G; j++) {
         const int64_t off = (t * hv + kh * G + j) * kD + c4;
-        float4 a = ld4(dQv + off), b = ld4(dKv + off);
+        const float4 a1 = ld4(dQv + off), a2 = ld4(dQv2 + off);
+        const float4 b1 = ld4(dKv + off), b2 = ld4(dKv2 + off), b3 = ld4(dKv3 + off);
+        const float4 a = make_float4(a1.x + a2.x, a1.y + a2.y, a1.z + a2.z, a1.w + a2.w);
+        const float4 b = make_float4(b1.x + b2.x + b3.x, b1.y + b2.y + b3.y, b1.z + b2.z + b3.z,
+                                     b1.w + b2.w + b3.w);
         q.x += a.x; q.y += a.y; q.z += a.z; q.w += a.w;
         k.x += b.x; k.y += b.y; k.z += b.z; k.w += b.w;
     }
@@ -1067,7 +1078,7 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
     if (a.T > 0) {
         int64_t n = a.T * a.hk * 32;
         GDN_PROF("gva_sum", st);
-        gva_sum_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(w.dQv, w.dKv, a.T, a.hk,
+        gva_sum_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(w.dQv, w.dKv, w.dQv2, w.dKv2, w.dKv3, a.T, a.hk,
                                                                     a.hv, a.dqkv);
     }
     if (a.dA_log || a.ddt_bias) {

@@ -370,6 +370,19 @@ out_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z,
     __syncthreads();
     umma::tf32r_inplace(Qs, 64 * 128 * 2 + 128 * 128);   // Q, K, S0
     umma::transpose_rows_to_kmajor(UT, Ur, kLdK, nullptr);
+    __syncthreads();
+    // U rows are transposed: their space takes the z rows for the norm epilogue
+    constexpr int kZPitch = kD * (int)sizeof(IO) + 16;    // bytes; conflict-free row reads
+    char* Zs = reinterpret_cast<char*>(Ur);
+    if (z) {
+        constexpr int kPieces = kD * (int)sizeof(IO) / 16;
+        for (int idx = tid; idx < 64 * kPieces; idx += 256) {
+            const int r = idx / kPieces, p = idx % kPieces;
+            cp_async16(Zs + r * kZPitch + p * 16,
+                       reinterpret_cast<const char*>(z + (row(r) * hv + h) * kD) + p * 16, r < L);
+        }
+    }
+    cp_async_commit();
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -431,6 +444,7 @@ out_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z,
     } else if (tid == 0) {
         atomicExch(sv.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
     }
+    cp_async_wait<0>();
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 512);
@@ -446,7 +460,7 @@ out_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z,
         if (o_out) st4(o_out + off + u, o4);
         if (z) {
             const float4 w4 = ld4(norm_w + half * 64 + u);
-            const float4 z4 = ld4(z + off + u);
+            const float4 z4 = ld4(reinterpret_cast<const IO*>(Zs + i * kZPitch) + half * 64 + u);
             float4 y4;
             y4.x = o4.x * rs * (1.f + w4.x) * siluf_(z4.x);
             y4.y = o4.y * rs * (1.f + w4.y) * siluf_(z4.y);

@@ -81,8 +81,11 @@ struct BwdScratch {
     float* dO;       // [T, Hv, d]
     float* dU;       // [T, Hv, d]
     float* dS;       // [NT, Hv, d_k, d_v] gradient of the state at each chunk end, transposed
-    float* dQv;      // [T, Hv, d] per v-head dq^
-    float* dKv;      // [T, Hv, d] per v-head dk^
+    float* dQv;      // [T, Hv, d] per v-head dq^, state-facing part
+    float* dKv;      // [T, Hv, d] per v-head dk^, state-facing part
+    float* dQv2;     // [T, Hv, d] per v-head dq^, P / dP part
+    float* dKv2;     // [T, Hv, d] per v-head dk^, P / dP part
+    float* dKv3;     // [T, Hv, d] per v-head dk^, WY part
     float* dW;       // [T, Hv, d]
     float* dgam;     // [T, Hv] partial dgamma from the state-facing terms
     float* dgs;      // [T, Hv] dg (per token)
