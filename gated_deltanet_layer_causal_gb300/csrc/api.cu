@@ -74,6 +74,7 @@ FwdSaved carve_fwd(void* ws, const gdn_dims* d, int NT, size_t* bytes) {
     s.U = c.take<float>(T * H * kD);
     s.S0 = c.take<float>((size_t)NT * H * kD * kD);
     s.S0b = c.take<float>((size_t)NT * H * kD * kD);
+    s.Tm = c.take<float>((size_t)NT * H * 2 * 64 * 64);
     s.o = c.take<float>(T * H * kD);
     s.rstd = c.take<float>(T * H);
     *bytes = c.off;
@@ -99,9 +100,6 @@ BwdScratch carve_bwd(void* ws, const gdn_dims* d, int NT, int32_t** status, size
     s.dgs = c.take<float>(T * H);
     // dnorm_w partials [NT*H][kD], gate partials [NT*H][2], column-sum stage [512][kD]
     s.nw_part = c.take<float>((size_t)NT * H * kD + (size_t)NT * H * 2 + 512 * kD);
-    s.Tm = c.take<float>((size_t)NT * H * 2 * 64 * 64);
-    s.dWt = c.take<float>((size_t)NT * H * kD * 64);
-    s.dUt = c.take<float>((size_t)NT * H * kD * 64);
     *bytes = c.off;
     return s;
 }

@@ -23,7 +23,7 @@
 
 namespace gdn {
 
-constexpr int kL4 = 132, kL8 = 136, kM4 = 68, kM8 = 72;
+constexpr int kL4 = 132, kL8 = 136;
 
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
@@ -64,17 +64,8 @@ bwd_local_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z, con
     const int lane = tid & 31, warp = tid >> 5;
     const int C = (2 * hk + hv) * kD;
     auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-        const int r = idx >> 5, c = (idx & 31) * 4;
-        cp_async16(Qs + umma::kidx(r, c, 128), qkv + row(r) * C + kh * kD + c, r < L);
-        cp_async16(Ks + umma::kidx(r, c, 128), qkv + row(r) * C + (int64_t)hk * kD + kh * kD + c,
-                   r < L);
-    }
-    cp_async_commit();
-    load_gam(gam, sv, ci, h);
-    if (warp == 0) umma::tmem_alloc(tslot, 256);
-    if (tid == 0) umma::mbar_init(mbar, 1);
-    // norm backward, one warp per row; a warp's 8 rows are loaded before any is used
+    // norm backward, one warp per row; a warp's 8 rows are loaded before any is
+    // used, and ahead of the Q / K tiles
     float4 wacc = zero4();
     const float4 w4 = z ? ld4(norm_w + lane * 4) : zero4();
     float4 o8[8], z8[8], y8[8];
@@ -88,6 +79,16 @@ bwd_local_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z, con
             z8[k] = ld4(z + off);
         }
     }
+    for (int idx = tid; idx < 64 * 32; idx += 256) {
+        const int r = idx >> 5, c = (idx & 31) * 4;
+        cp_async16(Qs + umma::kidx(r, c, 128), qkv + row(r) * C + kh * kD + c, r < L);
+        cp_async16(Ks + umma::kidx(r, c, 128), qkv + row(r) * C + (int64_t)hk * kD + kh * kD + c,
+                   r < L);
+    }
+    cp_async_commit();
+    load_gam(gam, sv, ci, h);
+    if (warp == 0) umma::tmem_alloc(tslot, 256);
+    if (tid == 0) umma::mbar_init(mbar, 1);
 #pragma unroll
     for (int k = 0; k < 8; k++) {
         const int r = warp + 8 * k;
@@ -283,12 +284,10 @@ bwd_state_kernel(const float* __restrict__ qkv, int hk, int hv, const float* dS_
                                  [&](int b, int a) { return dSt[b * kLdS + a]; });
         __syncthreads();                    // K and dS^T reads done
         if (more) issue_k(prev);
-        float* dUt = w.dUt + ((int64_t)ci * hv + h) * kD * 64;
         tile_each<64, kSl, 8>(uacc, [&](int i, int a, float& v) {
             const float u = i < L ? dUc[i * kLdS + a] + v : 0.f;
             dUc[i * kLdS + a] = u;
             if (i < L) w.dU[((int64_t)(info.start + i) * hv + h) * kD + a0 + a] = u;
-            dUt[umma::kidx(a0 + a, i, 64)] = umma::tf32r(u);
         });
         __syncthreads();
         // dS^T = e^{gam_L} dS^T + Q~^T dO - W^T dU
@@ -423,16 +422,12 @@ bwd_sfacing_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, B
                     }
                 } else {
                     const int i = r - 64;
-                    float* dWt = w.dWt + ((int64_t)blockIdx.x * hv + h) * kD * 64;
                     if (i < L) {
                         float* dst = w.dW + (row(i) * hv + h) * kD + c0 + cc;
 #pragma unroll
                         for (int u = 0; u < 16; u += 4)
                             st4(dst + u, make_float4(-v[u], -v[u + 1], -v[u + 2], -v[u + 3]));
                     }
-#pragma unroll
-                    for (int u = 0; u < 16; u++)
-                        dWt[umma::kidx(c0 + cc + u, i, 64)] = i < L ? umma::tf32r(-v[u]) : 0.f;
                 }
             }
             if (r < 64) rpart[half * 128 + r] = r < L ? eg[r] * part : 0.f;
@@ -477,14 +472,16 @@ bwd_sfacing_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, B
 
 // ------------------------------------------------------------------ B3b: P / dP terms
 // grid (NT, Hv), 256 threads, tcgen05.
-//   D_qk = Q K^T, D_kk = K K^T, D_dou = dO U^T          (64 x 64 each)
+//   D_qk = Q K^T, D_dou = dO U^T                         (64 x 64 each)
 //   dPm = D_dou (.) Gam (.) [i>=j];  R = dPm (.) D_qk
 //     dgam_i += sum_j R_ij, dgam_j -= sum_i R_ij
-//   A = beta_i Gam_ij D_kk (j < i);  T = (I + A)^-1      (CUDA cores; saved)
 //   D_dq = dPm K,  D_dk = dPm^T Q                        (64 x 128 each)
-// added to the per-v-head dQ / dK partials.
-constexpr int kDpFloats = 4 * 64 * 128 + 2 * 64 * 64 + 64 * 65 + 2 * 64 * kM4;
-constexpr size_t kDpSmem = sizeof(float) * (kDpFloats + 3 * 64 + 2 * 64 + 16) + 64;
+// added to the per-v-head dQ / dK partials.  Shared memory: Q, K, dO, U
+// K-major 32 KB each (Q, K later hold Q^T, K^T), dPm in both orientations
+// 16 KB each, R 16 KB.  Tensor memory: 256 fp32 columns (D_dq / D_dk reuse the
+// columns of the first products once those are read).
+constexpr int kDpFloats = 4 * 64 * 128 + 2 * 64 * 64 + 64 * 65;
+constexpr size_t kDpSmem = sizeof(float) * (kDpFloats + 64 + 64 + 2 * 64 + 16) + 64;
 
 __global__ void __launch_bounds__(256, 1)
 bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScratch w) {
@@ -496,11 +493,8 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
     float* dPR = Us + 64 * 128;        // [64 (i)][64 (j)] K-major
     float* dPC = dPR + 64 * 64;        // [64 (j)][64 (i)] K-major
     float* Rm = dPC + 64 * 64;         // [64][65] row-major R
-    float* As = Rm + 64 * 65;          // [64][kM4] row-major A
-    float* Tr = As + 64 * kM4;         // [64][kM4] row-major T
-    float* gam = Tr + 64 * kM4;
-    float* bet = gam + 64;
-    float* dgl = bet + 64;             // local dgam
+    float* gam = Rm + 64 * 65;
+    float* dgl = gam + 64;             // local dgam
     float* rpart = dgl + 64;           // [2][64]
     uint64_t* mbar = reinterpret_cast<uint64_t*>(rpart + 128 + 16);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
@@ -522,8 +516,7 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
     }
     cp_async_commit();
     load_gam(gam, sv, ci, h);
-    if (tid < 64) bet[tid] = tid < L ? sv.beta[(int64_t)h * sv.T + ci.start + tid] : 0.f;
-    if (warp == 0) umma::tmem_alloc(tslot, 512);
+    if (warp == 0) umma::tmem_alloc(tslot, 256);
     if (tid == 0) umma::mbar_init(mbar, 1);
     cp_async_wait<0>();
     __syncthreads();
@@ -532,11 +525,9 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t tQK = tmem, tKK = tmem + 64, tDOU = tmem + 128, tDQ = tmem + 256,
-                   tDK = tmem + 384;
+    const uint32_t tQK = tmem, tDOU = tmem + 64, tDQ = tmem, tDK = tmem + 128;
     if (tid == 0) {
         umma::mma_tf32(tQK, Qs, 128, Ks, 128, 64, 64, 128, false);
-        umma::mma_tf32(tKK, Ks, 128, Ks, 128, 64, 64, 128, false);
         umma::mma_tf32(tDOU, dOs, 128, Us, 128, 64, 64, 128, false);
         umma::commit(mbar);
     }
@@ -555,10 +546,9 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
     if (ok) {
         float rsum = 0.f;
         for (int cc = 0; cc < 32; cc += 16) {
-            float qk[16], kk[16], du[16];
+            float qk[16], du[16];
             const int j0 = half * 32 + cc;
             umma::tmem_ld16(umma::tmem_at(tQK, j0), qk);
-            umma::tmem_ld16(umma::tmem_at(tKK, j0), kk);
             umma::tmem_ld16(umma::tmem_at(tDOU, j0), du);
             if (lane < 16) {
 #pragma unroll
@@ -572,7 +562,6 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
                         const float R = dp[q] * qk[u + q];
                         rsum += R;
                         Rm[i * 65 + j] = R;
-                        As[i * kM4 + j] = (j < i) ? bet[i] * gm * kk[u + q] : 0.f;
                         dPC[umma::kidx(j, i, 64)] = umma::tf32r(dp[q]);
                     }
                     *reinterpret_cast<float4*>(dPR + umma::kidx(i, j0 + u, 64)) =
@@ -582,6 +571,7 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
         }
         if (lane < 16) rpart[half * 64 + i] = rsum;
     }
+    umma::fence_before_sync();
     __syncthreads();
     // the first MMAs are done: Q and K rows (row-major, in the dO / U space) are
     // transposed into Q^T and K^T (rows b, k = token) in the Q / K space
@@ -591,11 +581,6 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
     __syncthreads();
     umma::transpose_rows_to_kmajor(QT, dOs, 128, nullptr);
     umma::transpose_rows_to_kmajor(KT, Us, 128, nullptr);
-    if (tid < 64) {   // dgam from R: row sums minus column sums (fixed order)
-        float cs = 0.f;
-        for (int r = 0; r < 64; r++) cs += Rm[r * 65 + tid];
-        dgl[tid] = (rpart[tid] + rpart[64 + tid]) - cs;
-    }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
@@ -605,22 +590,12 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
         umma::mma_tf32(tDK, dPC, 64, QT, 64, 64, 128, 64, false);
         umma::commit(mbar);
     }
-    // the triangular solve overlaps the MMAs
-    tril_inverse64(As, kM4, Tr, kM4, Rm);     // R is consumed: scratch
-    __syncthreads();
-    {   // T as K-major rows i and as K-major rows j (T^T), tf32-rounded MMA operands
-        float* Tg = w.Tm + ((int64_t)blockIdx.x * hv + h) * 2 * 64 * 64;
-        for (int idx = tid; idx < 64 * 16; idx += 256) {
-            const int r = idx & 63, c4 = idx >> 6;
-            st4(Tg + umma::kidx(r, 4 * c4, 64),
-                umma::tf32r(make_float4(Tr[r * kM4 + 4 * c4], Tr[r * kM4 + 4 * c4 + 1],
-                                        Tr[r * kM4 + 4 * c4 + 2], Tr[r * kM4 + 4 * c4 + 3])));
-            st4(Tg + 64 * 64 + umma::kidx(r, 4 * c4, 64),
-                umma::tf32r(make_float4(Tr[(4 * c4) * kM4 + r], Tr[(4 * c4 + 1) * kM4 + r],
-                                        Tr[(4 * c4 + 2) * kM4 + r], Tr[(4 * c4 + 3) * kM4 + r])));
-        }
+    if (tid < 64) {   // dgam from R: row sums minus column sums (fixed order)
+        float cs = 0.f;
+        for (int r = 0; r < 64; r++) cs += Rm[r * 65 + tid];
+        dgl[tid] = (rpart[tid] + rpart[64 + tid]) - cs;
+        if (tid < L) w.dgam[(int64_t)(ci.start + tid) * hv + h] += dgl[tid];
     }
-    if (tid < 64 && tid < L) w.dgam[(int64_t)(ci.start + tid) * hv + h] += dgl[tid];
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
     umma::fence_after_sync();
     if (ok) {
@@ -642,7 +617,7 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
     }
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_free(tmem, 512);
+    if (warp == 0) umma::tmem_free(tmem, 256);
 }
 
 // ------------------------------------------------------------------ B3c: WY terms and gates
@@ -673,16 +648,16 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
     float* dUs = dWs + 64 * 128;
     float* BW = dUs + 64 * 128;        // [256][64] K-major: dW^T rows b, dU^T rows 128 + a
     float* TC = BW + 256 * 64;         // [64 (j)][64 (i)] K-major T^T (kept to the end)
-    // stage 2 (overlays the stage-1 operands below TC)
-    float* GKK = sm;                   // [64][kM4] row-major Gam (.) KK (strict lower)
-    float* DTR = GKK + 64 * kM4;       // [64 (i)][64 (j)] K-major dT
+    // stage 2 overlays dW, dU and [dW^T ; dU^T] once the first products are
+    // complete; K and V stay for the epilogue's dot products (R later over V)
+    float* GKK = dWs;                  // [64][64] K-major Gam (.) KK (strict lower)
+    float* DTR = GKK + 64 * 64;        // [64 (i)][64 (j)] K-major dT
     float* TR = DTR + 64 * 64;         // [64 (m)][64 (j)] K-major T
     float* YT = TR + 64 * 64;          // [64 (m)][64 (i)] K-major Y^T
     float* dKR = YT + 64 * 64;         // [64 (j)][64 (m)] K-major dKK
     float* dKC = dKR + 64 * 64;        // [64 (j)][64 (m)] K-major dKK^T
     float* KT = dKC + 64 * 64;         // [128 (b)][64 (m)] K-major K^T
-    float* Rm = KT + 128 * 64;         // [64][65] row-major
-    float* Kr = Rm + 64 * 65;          // [64][128] row-major K (staging for K^T)
+    float* Rm = Vs;                    // [64][65] row-major
     float* gam = TC + 64 * 64;
     float* eg = gam + 64;
     float* bet = eg + 64;
@@ -704,8 +679,7 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
     auto vrow = [&](int r) { return (row(r) * hv + h) * kD; };
     const float* kb = qkv + (int64_t)hk * kD + kh * kD;
     const float* vb = qkv + (int64_t)2 * hk * kD + h * kD;
-    const float* Tg = w.Tm + ((int64_t)blockIdx.x * hv + h) * 2 * 64 * 64;   // T, then T^T
-    const int64_t tile = (int64_t)blockIdx.x * hv + h;
+    const float* Tg = sv.Tm + ((int64_t)blockIdx.x * hv + h) * 2 * 64 * 64;   // T, then T^T
     for (int idx = tid; idx < 64 * 32; idx += 256) {
         const int r = idx >> 5, c = (idx & 31) * 4;
         cp_async16(Ks + umma::kidx(r, c, 128), kb + row(r) * C + c, r < L);
@@ -713,11 +687,7 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
         cp_async16(dWs + umma::kidx(r, c, 128), w.dW + vrow(r) + c, r < L);
         cp_async16(dUs + umma::kidx(r, c, 128), w.dU + vrow(r) + c, r < L);
     }
-    // [dW^T ; dU^T] and T^T arrive as K-major tiles written by their producers
-    for (int idx = tid; idx < 128 * 16; idx += 256) {
-        cp_async16(BW + idx * 4, w.dWt + tile * kD * 64 + idx * 4, true);
-        cp_async16(BW + 128 * 64 + idx * 4, w.dUt + tile * kD * 64 + idx * 4, true);
-    }
+    // T^T arrives as a K-major tile written by the forward
     for (int idx = tid; idx < 64 * 16; idx += 256) cp_async16(TC + idx * 4, Tg + 64 * 64 + idx * 4, true);
     cp_async_commit();
     load_gam(gam, sv, ci, h);
@@ -735,7 +705,10 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
     }
     cp_async_wait<0>();
     __syncthreads();
-    umma::tf32r_inplace(Ks, 4 * 64 * 128);   // K, V, dW, dU (the tiles arrive rounded)
+    umma::tf32r_inplace(Ks, 4 * 64 * 128);   // K, V, dW, dU (T^T arrives rounded)
+    __syncthreads();
+    umma::transpose_kmajor_64x128(BW, dWs);   // [dW^T ; dU^T]: rows b, k = token
+    umma::transpose_kmajor_64x128(BW + 128 * 64, dUs);
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -753,12 +726,8 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
     }
     bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
-    // stage-1 operands are consumed: fetch T and the K rows for stage 2
+    // dW, dU and their transposes are consumed: fetch T for stage 2
     for (int idx = tid; idx < 64 * 16; idx += 256) cp_async16(TR + idx * 4, Tg + idx * 4, true);
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-        const int rr = idx >> 5, c = (idx & 31) * 4;
-        cp_async16(Kr + rr * 128 + c, kb + row(rr) * C + c, rr < L);
-    }
     cp_async_commit();
     const int win = warp & 3, half = warp >> 2;
     const int r = win * 16 + lane;     // D row (lanes 0..15)
@@ -774,13 +743,15 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
             if (live) {
 #pragma unroll
                 for (int u = 0; u < 16; u += 4) {
-                    float d[4];
+                    float d[4], g[4];
 #pragma unroll
                     for (int q = 0; q < 4; q++) {
                         const int j = j0 + u + q;
-                        GKK[r * kM4 + j] = (j < r) ? expf(gam[r] - gam[j]) * kk[u + q] : 0.f;
+                        g[q] = (j < r) ? expf(gam[r] - gam[j]) * kk[u + q] : 0.f;
                         d[q] = t1[u + q] * be[j] + t2[u + q] * bet[j];
                     }
+                    *reinterpret_cast<float4*>(GKK + umma::kidx(r, j0 + u, 64)) =
+                        make_float4(g[0], g[1], g[2], g[3]);
                     *reinterpret_cast<float4*>(DTR + umma::kidx(r, j0 + u, 64)) =
                         umma::tf32r(make_float4(d[0], d[1], d[2], d[3]));
                 }
@@ -793,18 +764,18 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
             umma::tmem_ld16(umma::tmem_at(tTW, half * 128 + cc), v);
             if (live && r < L) {
                 if (half == 0) {
-                    const float* kr = kb + row(r) * C + cc;
 #pragma unroll
                     for (int u = 0; u < 16; u += 4) {
-                        const float4 k4 = ld4(kr + u);
+                        const float4 k4 =
+                            *reinterpret_cast<const float4*>(Ks + umma::kidx(r, cc + u, 128));
                         rsum += v[u] * k4.x + v[u + 1] * k4.y + v[u + 2] * k4.z + v[u + 3] * k4.w;
                     }
                 } else {
-                    const float* vr = vb + row(r) * C + cc;
                     float* dv = dqkv + row(r) * C + (int64_t)2 * hk * kD + h * kD + cc;
 #pragma unroll
                     for (int u = 0; u < 16; u += 4) {
-                        const float4 v4 = ld4(vr + u);
+                        const float4 v4 =
+                            *reinterpret_cast<const float4*>(Vs + umma::kidx(r, cc + u, 128));
                         rsum += v[u] * v4.x + v[u + 1] * v4.y + v[u + 2] * v4.z + v[u + 3] * v4.w;
                         st4(dv + u, make_float4(bet[r] * v[u], bet[r] * v[u + 1],
                                                 bet[r] * v[u + 2], bet[r] * v[u + 3]));
@@ -819,10 +790,9 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
         dbs[tid] += eg[tid] * rp[tid] + rp[64 + tid];
         dgs[tid] += be[tid] * rp[tid];
     }
-    // stage 2 operands: T arrived as a K-major tile; K^T from the staged K rows
+    // stage 2 operands: T arrived as a K-major tile; K^T from the K tile
     cp_async_wait<0>();
-    __syncthreads();
-    umma::transpose_rows_to_kmajor(KT, Kr, 128, nullptr);
+    umma::transpose_kmajor_64x128(KT, Ks);
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
@@ -869,7 +839,7 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
                     for (int q = 0; q < 4; q++) {
                         const int m = m0 + u + q;
                         const float dA = (m < r) ? -v[u + q] : 0.f;
-                        const float x = dA * GKK[r * kM4 + m];
+                        const float x = dA * GKK[umma::kidx(r, m, 64)];
                         rsum += x;
                         Rm[r * 65 + m] = bet[r] * x;
                         dk[q] = (m < r) ? dA * bet[r] * expf(gam[r] - gam[m]) : 0.f;

@@ -107,7 +107,6 @@ prep_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO* 
     const float* vbase = qkv + (int64_t)2 * hk * kD + h * kD;
     for (int idx = tid; idx < 64 * 32; idx += 256) {
         const int r = idx >> 5, c = (idx & 31) * 4;
-        cp_async16(Ks + umma::kidx(r, c, 128), kbase + row(r) * C + c, r < L);
         cp_async16(Kr + r * kLdK + c, kbase + row(r) * C + c, r < L);
         cp_async16(Vr + r * kLdK + c, vbase + row(r) * C + c, r < L);
     }
@@ -140,7 +139,11 @@ prep_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO* 
     // B operand: rows c (0..127) = be_j K[j][c], rows 128 + a = beta_j V[j][a]
     umma::transpose_rows_to_kmajor(Bs, Kr, kLdK, be);
     umma::transpose_rows_to_kmajor(Bs + 128 * 64, Vr, kLdK, bet);
-    umma::tf32r_inplace(Ks, 64 * 128);
+    for (int idx = tid; idx < 64 * 32; idx += 256) {   // K rows -> K-major, rounded
+        const int r = (idx >> 8) * 8 + (idx & 7), c = ((idx >> 3) & 31) * 4;
+        *reinterpret_cast<float4*>(Ks + umma::kidx(r, c, 128)) =
+            umma::tf32r(*reinterpret_cast<const float4*>(Kr + r * kLdK + c));
+    }
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -183,6 +186,17 @@ prep_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO* 
     if (ok && tid == 0) {
         umma::mma_tf32(tD2, Tk, 64, Bs, 64, 64, 256, 64, false);
         umma::commit(mbar);
+    }
+    {   // T for the backward, as K-major rows i and as K-major rows j (T^T), rounded
+        float* Tg = sv.Tm + ((int64_t)blockIdx.x * hv + h) * 2 * 64 * 64;
+        for (int idx = tid; idx < 64 * 16; idx += 256) {
+            const int r = idx & 63, c4 = idx >> 6;
+            st4(Tg + umma::kidx(r, 4 * c4, 64),
+                umma::tf32r(*reinterpret_cast<const float4*>(Tr + r * kLdA + 4 * c4)));
+            st4(Tg + 64 * 64 + umma::kidx(r, 4 * c4, 64),
+                umma::tf32r(make_float4(Tr[(4 * c4) * kLdA + r], Tr[(4 * c4 + 1) * kLdA + r],
+                                        Tr[(4 * c4 + 2) * kLdA + r], Tr[(4 * c4 + 3) * kLdA + r])));
+        }
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
     umma::fence_after_sync();
@@ -426,18 +440,27 @@ out_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z,
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
     umma::fence_after_sync();
-    float o[64];
-    float ss = 0.f;
+    // O = D2 + e^{gam_i} D3 is staged row-major in the Q / K space (consumed by
+    // the first products); the norm and the stores then run row by row on all
+    // lanes, one warp per row, fully coalesced
+    float* Or = Qs;                    // [64][kLdK]
     if (ok) {
+        float ss = 0.f;
         for (int cc = 0; cc < 64; cc += 16) {
             float v2[16], v3[16];
             umma::tmem_ld16(umma::tmem_at(tD2, half * 64 + cc), v2);
             umma::tmem_ld16(umma::tmem_at(tD3, half * 64 + cc), v3);
+            if (lane < 16) {
 #pragma unroll
-            for (int u = 0; u < 16; u++) {
-                const float x = v2[u] + eg[i & 63] * v3[u];
-                o[cc + u] = x;
-                ss += x * x;
+                for (int u = 0; u < 16; u += 4) {
+                    float4 x;
+                    x.x = v2[u] + eg[i] * v3[u];
+                    x.y = v2[u + 1] + eg[i] * v3[u + 1];
+                    x.z = v2[u + 2] + eg[i] * v3[u + 2];
+                    x.w = v2[u + 3] + eg[i] * v3[u + 3];
+                    ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+                    *reinterpret_cast<float4*>(Or + i * kLdK + half * 64 + cc + u) = x;
+                }
             }
         }
         if (lane < 16) ssq[half * 64 + i] = ss;
@@ -448,28 +471,26 @@ out_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z,
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 512);
-    if (!ok || lane >= 16 || i >= L) return;
-    const int64_t t = ci.start + i;
-    const int64_t off = (t * hv + h) * kD + half * 64;
-    float rs = 0.f;
-    if (z) rs = rsqrtf((ssq[i] + ssq[64 + i]) * (1.f / kD) + norm_eps);
-#pragma unroll
-    for (int u = 0; u < 64; u += 4) {
-        const float4 o4 = make_float4(o[u], o[u + 1], o[u + 2], o[u + 3]);
-        st4(sv.o + off + u, o4);
-        if (o_out) st4(o_out + off + u, o4);
+    if (!ok) return;
+    const float4 w4 = z ? ld4(norm_w + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = warp; r < L; r += 8) {
+        const int64_t t = ci.start + r;
+        const int64_t off = (t * hv + h) * kD + lane * 4;
+        const float4 o4 = *reinterpret_cast<const float4*>(Or + r * kLdK + lane * 4);
+        st4(sv.o + off, o4);
+        if (o_out) st4(o_out + off, o4);
         if (z) {
-            const float4 w4 = ld4(norm_w + half * 64 + u);
-            const float4 z4 = ld4(reinterpret_cast<const IO*>(Zs + i * kZPitch) + half * 64 + u);
+            const float rs = rsqrtf((ssq[r] + ssq[64 + r]) * (1.f / kD) + norm_eps);
+            const float4 z4 = ld4(reinterpret_cast<const IO*>(Zs + r * kZPitch) + lane * 4);
             float4 y4;
             y4.x = o4.x * rs * (1.f + w4.x) * siluf_(z4.x);
             y4.y = o4.y * rs * (1.f + w4.y) * siluf_(z4.y);
             y4.z = o4.z * rs * (1.f + w4.z) * siluf_(z4.z);
             y4.w = o4.w * rs * (1.f + w4.w) * siluf_(z4.w);
-            st4(y_out + off + u, y4);
+            st4(y_out + off, y4);
+            if (lane == 0) sv.rstd[t * hv + h] = rs;
         }
     }
-    if (z && half == 0) sv.rstd[t * hv + h] = rs;
 }
 
 // ------------------------------------------------------------------ launchers

@@ -286,14 +286,20 @@ __device__ __forceinline__ void tril_inverse64(const float* As, int lda, float* 
     const int tid = threadIdx.x;
     for (int e = tid; e < kChunk * kChunk; e += 256) Ts[(e >> 6) * ldt + (e & 63)] = 0.f;
     __syncthreads();
-    if (tid < kChunk) {   // diagonal blocks: thread = column j
-        const int j = tid, end = (j | 15) + 1;
-        Ts[j * ldt + j] = 1.f;
-        for (int i = j + 1; i < end; i++) {
+    if (tid < kChunk) {   // diagonal blocks: thread = column c, solved in registers
+        // column c of a block's inverse solves (I + A_bb) x = e_c by forward
+        // substitution; columns are independent and A_bb is read by broadcast
+        const int c = tid, b0 = c & ~15, cl = c & 15;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
             float acc = 0.f;
-            for (int m = j; m < i; m++) acc += As[i * lda + m] * Ts[m * ldt + j];
-            Ts[i * ldt + j] = -acc;
+#pragma unroll
+            for (int m = 0; m < i; m++) acc += As[(b0 + i) * lda + b0 + m] * x[m];
+            x[i] = i == cl ? 1.f : (i > cl ? -acc : 0.f);
         }
+#pragma unroll
+        for (int i = 0; i < 16; i++) Ts[(b0 + i) * ldt + c] = x[i];
     }
     __syncthreads();
     // 16 -> 32: for the pairs (0,1) and (2,3) of 16-blocks, X = L21 T11, T21 = -T22 X

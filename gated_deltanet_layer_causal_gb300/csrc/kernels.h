@@ -44,6 +44,7 @@ struct FwdSaved {
     float* U;              // [T, Hv, d]  (U~ from prep, then U)
     float* S0;             // [NT, Hv] tiles: chunk-start state, K-major rows a (row = d_v)
     float* S0b;            // [NT, Hv] tiles: the same state, K-major rows b (row = d_k)
+    float* Tm;             // [NT * Hv][2][64 * 64] (I + A)^-1 per chunk: K-major T, K-major T^T
     float* o;              // [T, Hv, d] core output (before the norm)
     float* rstd;           // [T, Hv] norm rstd
 };
@@ -90,9 +91,6 @@ struct BwdScratch {
     float* dgam;     // [T, Hv] partial dgamma from the state-facing terms
     float* dgs;      // [T, Hv] dg (per token)
     float* nw_part;  // [NT * Hv, d] dnorm_w partials
-    float* Tm;       // [NT * Hv][2][64 * 64] (I + A)^-1 per chunk: K-major T, K-major T^T
-    float* dWt;      // [NT * Hv][128 * 64] dW^T per chunk, K-major rows b (tokens past the end: 0)
-    float* dUt;      // [NT * Hv][128 * 64] dU^T per chunk, K-major rows a (tokens past the end: 0)
 };
 
 cudaError_t launch_plan(const int32_t* cu, int N, int64_t T, int NT, FwdSaved sv, cudaStream_t st);

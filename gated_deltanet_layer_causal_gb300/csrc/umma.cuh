@@ -162,6 +162,22 @@ __device__ __forceinline__ void transpose_rows_to_kmajor(float* dst, const float
     }
 }
 
+// K-major tile [64 rows][128 (K)] -> K-major tile [128 rows][64 (K)] (its
+// transpose), whole CTA.  An 8 x 8 block is two adjacent core matrices (64
+// contiguous floats) on both sides: one warp moves a block per step, reads
+// conflict-free, writes two-way conflicted.
+__device__ __forceinline__ void transpose_kmajor_64x128(float* dst, const float* src) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int rr = lane >> 2, c4 = lane & 3;
+    for (int blk = warp; blk < 128; blk += nw) {
+        const int R8 = blk & 7, C8 = blk >> 3;
+        const float* s = src + (R8 * 32 + 2 * C8) * 32;
+        float* d = dst + (C8 * 16 + 2 * R8) * 32 + (rr >> 2) * 32 + c4 * 4 + (rr & 3);
+        d[0] = s[lane];
+        d[16] = s[lane + 32];
+    }
+}
+
 // Tensor-memory address of (lane window of this warp, column col).
 __device__ __forceinline__ uint32_t tmem_at(uint32_t base, int col) {
     const uint32_t lane0 = (uint32_t)((threadIdx.x >> 5) & 3) * 32u;
