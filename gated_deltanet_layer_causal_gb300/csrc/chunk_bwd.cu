@@ -42,27 +42,29 @@ __device__ __forceinline__ void load_gam(float* gam, const FwdSaved& sv, const C
 // Shared memory: Q, K K-major 32 KB each, dO rows 34 KB, dO^T (rows a,
 // k = token) 32 KB, P^T 16 KB.  Tensor memory: 192 fp32 columns (256 allocated).
 constexpr int kB1Floats = 64 * 128 * 2 + 64 * kL4 + 128 * 64 + 64 * 64;
-constexpr size_t kB1Smem = sizeof(float) * (kB1Floats + 64 + 16) + 64;
+constexpr size_t kB1Smem = sizeof(float) * (kB1Floats + 64 + 16) + 64 + 1024;
 
 template <class IO>
 __global__ void __launch_bounds__(256, 1)
-bwd_local_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z, const float* norm_w,
-                 float norm_eps, const IO* __restrict__ dy, IO* dz, FwdSaved sv, BwdScratch w) {
-    extern __shared__ __align__(128) float sm[];
-    float* Qs = sm;                    // [64][128] K-major
-    float* Ks = Qs + 64 * 128;         // [64][128] K-major
+bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO* z,
+                 const float* norm_w, float norm_eps, const IO* __restrict__ dy, IO* dz,
+                 FwdSaved sv, BwdScratch w) {
+    extern __shared__ float sm_raw[];
+    float* sm = umma::align1024(sm_raw);
+    float* Qs = sm;                    // [64][128] swizzled
+    float* Ks = Qs + 64 * 128;         // [64][128] swizzled
     float* dOr = Ks + 64 * 128;        // [64][kL4] row-major dO
     float* dOT = dOr + 64 * kL4;       // [128 (a)][64 (i)] K-major
     float* PT = dOT + 128 * 64;        // [64 (j)][64 (i)] K-major
     float* gam = PT + 64 * 64;
     uint64_t* mbar = reinterpret_cast<uint64_t*>(gam + 64 + 16);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
+    uint64_t* mbl = mbar + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
     __shared__ float4 red[8][32];
     const ChunkInfo ci = sv.chunks[blockIdx.x];
     if (ci.len == 0) return;
     const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
     const int lane = tid & 31, warp = tid >> 5;
-    const int C = (2 * hk + hv) * kD;
     auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
     // norm backward, one warp per row; a warp's 8 rows are loaded before any is
     // used, and ahead of the Q / K tiles
@@ -79,16 +81,15 @@ bwd_local_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z, con
             z8[k] = ld4(z + off);
         }
     }
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-        const int r = idx >> 5, c = (idx & 31) * 4;
-        cp_async16(Qs + umma::kidx(r, c, 128), qkv + row(r) * C + kh * kD + c, r < L);
-        cp_async16(Ks + umma::kidx(r, c, 128), qkv + row(r) * C + (int64_t)hk * kD + kh * kD + c,
-                   r < L);
+    if (tid == 0) {
+        umma::mbar_init(mbar, 1);
+        umma::mbar_init(mbl, 1);
+        umma::mbar_expect_tx(mbl, 2 * 64 * 128 * 4);
+        umma::tma_rows(Qs, 64, &maps.q, kh, ci.start, mbl);
+        umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
     }
-    cp_async_commit();
     load_gam(gam, sv, ci, h);
     if (warp == 0) umma::tmem_alloc(tslot, 256);
-    if (tid == 0) umma::mbar_init(mbar, 1);
 #pragma unroll
     for (int k = 0; k < 8; k++) {
         const int r = warp + 8 * k;
@@ -107,8 +108,12 @@ bwd_local_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z, con
         st4(dOr + r * kL4 + lane * 4, d4);
     }
     if (z) red[warp][lane] = wacc;
-    cp_async_wait<0>();
-    __syncthreads();
+    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
+    if (L < 64) {   // tail rows belong to the next sequence
+        umma::zero_tail_rows(Qs, 64, 0, L);
+        umma::zero_tail_rows(Ks, 64, 0, L);
+        __syncthreads();
+    }
     umma::tf32r_inplace(Qs, 2 * 64 * 128);
     if (z && warp == 0) {
         float4 s = red[0][lane];
@@ -129,11 +134,11 @@ bwd_local_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z, con
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t tD1 = tmem, tD2 = tmem + 64;
-    if (tid == 0) {
-        umma::mma_tf32(tD1, Ks, 128, Qs, 128, 64, 64, 128, false);
+    if (ok && tid == 0) {
+        umma::mma(tD1, umma::swt(Ks, 64), umma::swt(Qs, 64), 64, 64, 128, false);
         umma::commit(mbar);
     }
-    bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
     const int win = warp & 3, half = warp >> 2;
     const int j = win * 16 + lane;     // row of D1 = key index j
@@ -314,51 +319,56 @@ bwd_state_kernel(const float* __restrict__ qkv, int hk, int hv, const float* dS_
 // then dQ partial = e^gam X, dW = -Y, dK partial = fk dK~, and the dgam terms
 //   dgam_i += e^{gam_i} X_i . Q_i,  dgam_j -= Z_j = fk_j dK~_j . K_j,
 //   dgam_{L-1} += sum_j Z_j + e^{gam_L} <dS, S0>.
-// Shared memory (K-major core layout): [dO; dU] 64 KB, S0^T 64 KB, dS^T 64 KB,
-// U 32 KB.  Tensor memory: 256 fp32 columns.
+// Shared memory: [dO; dU] 64 KB and U 32 KB swizzled (TMA), S0^T and dS^T
+// 64 KB each, K-major rows b (one bulk copy each).  Tensor memory: 256 fp32
+// columns.
 constexpr int kSfFloats = 128 * 128 * 3 + 64 * 128;
-constexpr size_t kB3aSmem = sizeof(float) * (kSfFloats + 64 * 3 + 2 * 128 + 16) + 64;
+constexpr size_t kB3aSmem = sizeof(float) * (kSfFloats + 64 * 3 + 2 * 128 + 16) + 64 + 1024;
 
 __global__ void __launch_bounds__(256, 1)
-bwd_sfacing_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScratch w) {
-    extern __shared__ __align__(128) float sm[];
-    float* A1 = sm;                      // [128][128] K-major: rows 0-63 dO, 64-127 dU
+bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv,
+                   BwdScratch w) {
+    extern __shared__ float sm_raw[];
+    float* sm = umma::align1024(sm_raw);
+    float* A1 = sm;                      // [128][128] swizzled: rows 0-63 dO, 64-127 dU
     float* S0T = A1 + 128 * 128;         // [128 (b)][128 (a)] K-major
     float* DST = S0T + 128 * 128;        // [128 (b)][128 (a)] K-major
-    float* A2 = DST + 128 * 128;         // [64][128] K-major: U
+    float* A2 = DST + 128 * 128;         // [64][128] swizzled: U
     float* eg = A2 + 64 * 128;
     float* fk = eg + 64;
     float* gam = fk + 64;
     float* rpart = gam + 64;             // [2][128]
     float* red = rpart + 2 * 128;        // [16]
     uint64_t* mbar = reinterpret_cast<uint64_t*>(red + 16);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
+    uint64_t* mbl = mbar + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
     const ChunkInfo ci = sv.chunks[blockIdx.x];
     if (ci.len == 0) return;
     const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
     const int warp = tid >> 5, lane = tid & 31;
-    const int C = (2 * hk + hv) * kD;
     const int64_t sb = ((int64_t)blockIdx.x * hv + h) * kD * kD;
     auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
-    // ---- stage operands
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-        const int r = idx >> 5, c = (idx & 31) * 4;
-        const int64_t off = (row(r) * hv + h) * kD + c;
-        cp_async16(A1 + umma::kidx(r, c, 128), w.dO + off, r < L);
-        cp_async16(A1 + umma::kidx(64 + r, c, 128), w.dU + off, r < L);
-        cp_async16(A2 + umma::kidx(r, c, 128), sv.U + off, r < L);
+    // ---- stage operands: row tiles through the TMA; dS^T and S0^T are stored
+    // as K-major tiles with rows b, copied whole
+    if (tid == 0) {
+        umma::mbar_init(mbar, 1);
+        umma::mbar_init(mbl, 1);
+        umma::mbar_expect_tx(mbl, 3 * 64 * 128 * 4 + 2 * 128 * 128 * 4);
+        umma::tma_rows(A1, 128, &maps.dO, h, ci.start, mbl);
+        umma::tma_rows(A1 + 64 * 32, 128, &maps.dU, h, ci.start, mbl);
+        umma::tma_rows(A2, 64, &maps.U, h, ci.start, mbl);
+        umma::bulk_load(DST, w.dS + sb, 128 * 128 * 4, mbl);
+        umma::bulk_load(S0T, sv.S0b + sb, 128 * 128 * 4, mbl);
     }
-    // dS^T and S0^T are stored as K-major tiles with rows b: straight copies
-    for (int idx = tid; idx < 128 * 32; idx += 256) {
-        cp_async16(DST + idx * 4, w.dS + sb + idx * 4, true);
-        cp_async16(S0T + idx * 4, sv.S0b + sb + idx * 4, true);
-    }
-    cp_async_commit();
     load_gam(gam, sv, ci, h);
     if (warp == 0) umma::tmem_alloc(tslot, 256);
-    if (tid == 0) umma::mbar_init(mbar, 1);
-    cp_async_wait<0>();
     __syncthreads();
+    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
+    if (L < 64) {   // tail rows belong to the next sequence
+        umma::zero_tail_rows(A1, 128, 0, L);
+        umma::zero_tail_rows(A1, 128, 64, L);
+        umma::zero_tail_rows(A2, 64, 0, L);
+    }
     {   // <dS, S0> over the staged copies (same layout, same index), before rounding
         float dot = 0.f;
         for (int i = tid; i < 128 * 128; i += 256) dot += S0T[i] * DST[i];
@@ -371,29 +381,27 @@ bwd_sfacing_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, B
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
-    if (tid == 0) {
-        umma::mma_tf32(tmem, A1, 128, S0T, 128, 128, 128, 128, false);
-        umma::mma_tf32(tmem + 128, A2, 128, DST, 128, 64, 128, 128, false);
+    if (ok && tid == 0) {
+        umma::mma(tmem, umma::swt(A1, 128), umma::kmaj(S0T, 128), 128, 128, 128, false);
+        umma::mma(tmem + 128, umma::swt(A2, 64), umma::kmaj(DST, 128), 64, 128, 128, false);
         umma::commit(mbar);
     }
     if (tid < 64) {
         eg[tid] = tid < L ? expf(gam[tid]) : 0.f;
         fk[tid] = tid < L ? expf(gam[L - 1] - gam[tid]) : 0.f;
     }
-    const bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
-    // the products are complete: stage the Q and K rows the dgam dot products
-    // need into the S0 / dS space (row-major, padded: conflict-free row reads)
-    float* Qr = S0T;
-    float* Kr = S0T + 64 * 132;
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-        const int r = idx >> 5, c = (idx & 31) * 4;
-        cp_async16(Qr + r * 132 + c, qkv + row(r) * C + kh * kD + c, r < L);
-        cp_async16(Kr + r * 132 + c, qkv + row(r) * C + (int64_t)hk * kD + kh * kD + c, r < L);
+    // the products are complete: the Q and K tiles the dgam dot products need
+    // come into the S0 space through the TMA
+    float* Qr = S0T;                     // [64][128] swizzled
+    float* Kr = S0T + 64 * 128;          // [64][128] swizzled
+    if (ok && tid == 0) {
+        umma::mbar_expect_tx(mbl, 2 * 64 * 128 * 4);
+        umma::tma_rows(Qr, 64, &maps.q, kh, ci.start, mbl);
+        umma::tma_rows(Kr, 64, &maps.k, kh, ci.start, mbl);
     }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbl, 1));
     if (!ok) {
         if (tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
     } else {
@@ -410,10 +418,10 @@ bwd_sfacing_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, B
                     const int i = r;
                     if (i < L) {
                         float* dst = w.dQv + (row(i) * hv + h) * kD + c0 + cc;
-                        const float* q = Qr + i * 132 + c0 + cc;
 #pragma unroll
                         for (int u = 0; u < 16; u += 4) {
-                            const float4 q4 = ld4(q + u);
+                            const float4 q4 = *reinterpret_cast<const float4*>(
+                                Qr + umma::swz(i, c0 + cc + u, 64));
                             part += v[u] * q4.x + v[u + 1] * q4.y + v[u + 2] * q4.z +
                                     v[u + 3] * q4.w;
                             st4(dst + u, make_float4(eg[i] * v[u], eg[i] * v[u + 1],
@@ -441,10 +449,10 @@ bwd_sfacing_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, B
                 umma::tmem_ld16(umma::tmem_at(tmem + 128, c0 + cc), v);
                 if (lane < 16 && j < L) {
                     float* dst = w.dKv + (row(j) * hv + h) * kD + c0 + cc;
-                    const float* k = Kr + j * 132 + c0 + cc;
 #pragma unroll
                     for (int u = 0; u < 16; u += 4) {
-                        const float4 k4 = ld4(k + u);
+                        const float4 k4 = *reinterpret_cast<const float4*>(
+                            Kr + umma::swz(j, c0 + cc + u, 64));
                         part += v[u] * k4.x + v[u + 1] * k4.y + v[u + 2] * k4.z + v[u + 3] * k4.w;
                         st4(dst + u, make_float4(fk[j] * v[u], fk[j] * v[u + 1],
                                                  fk[j] * v[u + 2], fk[j] * v[u + 3]));
@@ -477,19 +485,21 @@ bwd_sfacing_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, B
 //     dgam_i += sum_j R_ij, dgam_j -= sum_i R_ij
 //   D_dq = dPm K,  D_dk = dPm^T Q                        (64 x 128 each)
 // added to the per-v-head dQ / dK partials.  Shared memory: Q, K, dO, U
-// K-major 32 KB each (Q, K later hold Q^T, K^T), dPm in both orientations
-// 16 KB each, R 16 KB.  Tensor memory: 256 fp32 columns (D_dq / D_dk reuse the
-// columns of the first products once those are read).
+// swizzled 32 KB each (TMA; dO, U later hold Q^T, K^T transposed out of the Q,
+// K tiles), dPm in both orientations 16 KB each, R 16 KB.  Tensor memory: 256
+// fp32 columns (D_dq / D_dk reuse the columns of the first products).
 constexpr int kDpFloats = 4 * 64 * 128 + 2 * 64 * 64 + 64 * 65;
-constexpr size_t kDpSmem = sizeof(float) * (kDpFloats + 64 + 64 + 2 * 64 + 16) + 64;
+constexpr size_t kDpSmem = sizeof(float) * (kDpFloats + 64 + 64 + 2 * 64 + 16) + 64 + 1024;
 
 __global__ void __launch_bounds__(256, 1)
-bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScratch w) {
-    extern __shared__ __align__(128) float sm[];
-    float* Qs = sm;                    // [64][128] K-major   (later Q^T: [128][64])
-    float* Ks = Qs + 64 * 128;         // [64][128] K-major   (later K^T: [128][64])
-    float* dOs = Ks + 64 * 128;        // [64][128] K-major
-    float* Us = dOs + 64 * 128;        // [64][128] K-major
+bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv,
+              BwdScratch w) {
+    extern __shared__ float sm_raw[];
+    float* sm = umma::align1024(sm_raw);
+    float* Qs = sm;                    // [64][128] swizzled
+    float* Ks = Qs + 64 * 128;         // [64][128] swizzled
+    float* dOs = Ks + 64 * 128;        // [64][128] swizzled   (later Q^T: [128][64] K-major)
+    float* Us = dOs + 64 * 128;        // [64][128] swizzled   (later K^T: [128][64] K-major)
     float* dPR = Us + 64 * 128;        // [64 (i)][64 (j)] K-major
     float* dPC = dPR + 64 * 64;        // [64 (j)][64 (i)] K-major
     float* Rm = dPC + 64 * 64;         // [64][65] row-major R
@@ -497,50 +507,46 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
     float* dgl = gam + 64;             // local dgam
     float* rpart = dgl + 64;           // [2][64]
     uint64_t* mbar = reinterpret_cast<uint64_t*>(rpart + 128 + 16);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
+    uint64_t* mbl = mbar + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
     const ChunkInfo ci = sv.chunks[blockIdx.x];
     if (ci.len == 0) return;
     const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
     const int warp = tid >> 5, lane = tid & 31;
-    const int C = (2 * hk + hv) * kD;
     auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
-    const float* qb = qkv + kh * kD;
-    const float* kb = qkv + (int64_t)hk * kD + kh * kD;
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-        const int r = idx >> 5, c = (idx & 31) * 4;
-        const int64_t vo = (row(r) * hv + h) * kD + c;
-        cp_async16(Qs + umma::kidx(r, c, 128), qb + row(r) * C + c, r < L);
-        cp_async16(Ks + umma::kidx(r, c, 128), kb + row(r) * C + c, r < L);
-        cp_async16(dOs + umma::kidx(r, c, 128), w.dO + vo, r < L);
-        cp_async16(Us + umma::kidx(r, c, 128), sv.U + vo, r < L);
+    if (tid == 0) {
+        umma::mbar_init(mbar, 1);
+        umma::mbar_init(mbl, 1);
+        umma::mbar_expect_tx(mbl, 4 * 64 * 128 * 4);
+        umma::tma_rows(Qs, 64, &maps.q, kh, ci.start, mbl);
+        umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
+        umma::tma_rows(dOs, 64, &maps.dO, h, ci.start, mbl);
+        umma::tma_rows(Us, 64, &maps.U, h, ci.start, mbl);
     }
-    cp_async_commit();
     load_gam(gam, sv, ci, h);
     if (warp == 0) umma::tmem_alloc(tslot, 256);
-    if (tid == 0) umma::mbar_init(mbar, 1);
-    cp_async_wait<0>();
     __syncthreads();
+    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
+    if (L < 64) {   // tail rows belong to the next sequence
+        umma::zero_tail_rows(Qs, 64, 0, L);
+        umma::zero_tail_rows(Ks, 64, 0, L);
+        umma::zero_tail_rows(dOs, 64, 0, L);
+        umma::zero_tail_rows(Us, 64, 0, L);
+        __syncthreads();
+    }
     umma::tf32r_inplace(Qs, 4 * 64 * 128);   // Q, K, dO, U
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t tQK = tmem, tDOU = tmem + 64, tDQ = tmem, tDK = tmem + 128;
-    if (tid == 0) {
-        umma::mma_tf32(tQK, Qs, 128, Ks, 128, 64, 64, 128, false);
-        umma::mma_tf32(tDOU, dOs, 128, Us, 128, 64, 64, 128, false);
+    if (ok && tid == 0) {
+        umma::mma(tQK, umma::swt(Qs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
+        umma::mma(tDOU, umma::swt(dOs, 64), umma::swt(Us, 64), 64, 64, 128, false);
         umma::commit(mbar);
     }
-    bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
-    // the first products are complete: fetch Q and K rows (row-major) into the
-    // dO / U space while the epilogue runs
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-        const int r = idx >> 5, c = (idx & 31) * 4;
-        cp_async16(dOs + r * 128 + c, qb + row(r) * C + c, r < L);
-        cp_async16(Us + r * 128 + c, kb + row(r) * C + c, r < L);
-    }
-    cp_async_commit();
     const int win = warp & 3, half = warp >> 2;
     const int i = win * 16 + lane;     // D row (lanes 0..15)
     if (ok) {
@@ -573,14 +579,12 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
     }
     umma::fence_before_sync();
     __syncthreads();
-    // the first MMAs are done: Q and K rows (row-major, in the dO / U space) are
-    // transposed into Q^T and K^T (rows b, k = token) in the Q / K space
-    float* QT = Qs;
-    float* KT = Ks;
-    cp_async_wait<0>();
-    __syncthreads();
-    umma::transpose_rows_to_kmajor(QT, dOs, 128, nullptr);
-    umma::transpose_rows_to_kmajor(KT, Us, 128, nullptr);
+    // the first MMAs are done: Q^T and K^T (rows b, k = token) are transposed
+    // out of the Q and K tiles into the dO / U space
+    float* QT = dOs;
+    float* KT = Us;
+    umma::transpose_sw_to_kmajor(QT, Qs, nullptr);
+    umma::transpose_sw_to_kmajor(KT, Ks, nullptr);
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
@@ -632,17 +636,19 @@ bwd_dp_kernel(const float* __restrict__ qkv, int hk, int hv, FwdSaved sv, BwdScr
 //   dK += dKK K + dKK^T K
 // then dg = reverse in-chunk cumsum of the total dgam, and the gate gradients.
 constexpr int kWyFloats = 4 * 64 * 128 + 256 * 64 + 64 * 64;   // stage-1 operands
-constexpr size_t kWySmem = sizeof(float) * (kWyFloats + 10 * 64 + 2 * 64 + 16) + 64;
+constexpr size_t kWySmem = sizeof(float) * (kWyFloats + 10 * 64 + 2 * 64 + 16) + 64 + 1024;
 
 template <class IO>
 __global__ void __launch_bounds__(256, 1)
-bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO* __restrict__ bv,
-              const float* __restrict__ A_log, const float* __restrict__ dt_bias, int hk, int hv,
-              float* __restrict__ dqkv, IO* __restrict__ da, IO* __restrict__ db,
-              float* __restrict__ gate_part, FwdSaved sv, BwdScratch w) {
-    extern __shared__ __align__(128) float sm[];
-    // stage 1
-    float* Ks = sm;                    // [64][128] K-major
+bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
+              const IO* __restrict__ bv, const float* __restrict__ A_log,
+              const float* __restrict__ dt_bias, int hk, int hv, float* __restrict__ dqkv,
+              IO* __restrict__ da, IO* __restrict__ db, float* __restrict__ gate_part, FwdSaved sv,
+              BwdScratch w) {
+    extern __shared__ float sm_raw[];
+    float* sm = umma::align1024(sm_raw);
+    // stage 1: K, V, dW, dU swizzled (TMA)
+    float* Ks = sm;                    // [64][128] swizzled
     float* Vs = Ks + 64 * 128;
     float* dWs = Vs + 64 * 128;
     float* dUs = dWs + 64 * 128;
@@ -669,7 +675,8 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
     float* red = rk + 64;              // [64]
     float* rp = red + 64;              // [2][64]
     uint64_t* mbar = reinterpret_cast<uint64_t*>(rp + 128 + 16);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
+    uint64_t* mbl = mbar + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
     const ChunkInfo ci = sv.chunks[blockIdx.x];
     if (ci.len == 0) return;
     const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
@@ -677,19 +684,17 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
     const int C = (2 * hk + hv) * kD;
     auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
     auto vrow = [&](int r) { return (row(r) * hv + h) * kD; };
-    const float* kb = qkv + (int64_t)hk * kD + kh * kD;
-    const float* vb = qkv + (int64_t)2 * hk * kD + h * kD;
     const float* Tg = sv.Tm + ((int64_t)blockIdx.x * hv + h) * 2 * 64 * 64;   // T, then T^T
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-        const int r = idx >> 5, c = (idx & 31) * 4;
-        cp_async16(Ks + umma::kidx(r, c, 128), kb + row(r) * C + c, r < L);
-        cp_async16(Vs + umma::kidx(r, c, 128), vb + row(r) * C + c, r < L);
-        cp_async16(dWs + umma::kidx(r, c, 128), w.dW + vrow(r) + c, r < L);
-        cp_async16(dUs + umma::kidx(r, c, 128), w.dU + vrow(r) + c, r < L);
+    if (tid == 0) {   // row tiles through the TMA; T^T, written by the forward, whole
+        umma::mbar_init(mbar, 1);
+        umma::mbar_init(mbl, 1);
+        umma::mbar_expect_tx(mbl, 4 * 64 * 128 * 4 + 64 * 64 * 4);
+        umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
+        umma::tma_rows(Vs, 64, &maps.v, h, ci.start, mbl);
+        umma::tma_rows(dWs, 64, &maps.dW, h, ci.start, mbl);
+        umma::tma_rows(dUs, 64, &maps.dU, h, ci.start, mbl);
+        umma::bulk_load(TC, Tg + 64 * 64, 64 * 64 * 4, mbl);
     }
-    // T^T arrives as a K-major tile written by the forward
-    for (int idx = tid; idx < 64 * 16; idx += 256) cp_async16(TC + idx * 4, Tg + 64 * 64 + idx * 4, true);
-    cp_async_commit();
     load_gam(gam, sv, ci, h);
     if (tid < 64) {
         bet[tid] = tid < L ? sv.beta[(int64_t)h * sv.T + ci.start + tid] : 0.f;
@@ -697,18 +702,23 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
         dbs[tid] = 0.f;
     }
     if (warp == 0) umma::tmem_alloc(tslot, 512);
-    if (tid == 0) umma::mbar_init(mbar, 1);
     __syncthreads();
     if (tid < 64) {
         eg[tid] = tid < L ? expf(gam[tid]) : 0.f;
         be[tid] = bet[tid] * eg[tid];
     }
-    cp_async_wait<0>();
-    __syncthreads();
+    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
+    if (L < 64) {   // tail rows belong to the next sequence
+        umma::zero_tail_rows(Ks, 64, 0, L);
+        umma::zero_tail_rows(Vs, 64, 0, L);
+        umma::zero_tail_rows(dWs, 64, 0, L);
+        umma::zero_tail_rows(dUs, 64, 0, L);
+        __syncthreads();
+    }
     umma::tf32r_inplace(Ks, 4 * 64 * 128);   // K, V, dW, dU (T^T arrives rounded)
     __syncthreads();
-    umma::transpose_kmajor_64x128(BW, dWs);   // [dW^T ; dU^T]: rows b, k = token
-    umma::transpose_kmajor_64x128(BW + 128 * 64, dUs);
+    umma::transpose_sw_to_kmajor(BW, dWs, nullptr);   // [dW^T ; dU^T]: rows b, k = token
+    umma::transpose_sw_to_kmajor(BW + 128 * 64, dUs, nullptr);
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -717,18 +727,20 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
     // 128-column dKK product), T^T [dW | dU] 256-511 (read again at the very end)
     const uint32_t tKK = tmem, tDT1 = tmem + 64, tDT2 = tmem + 128, tX = tmem + 64,
                    tTW = tmem + 256;
-    if (tid == 0) {
-        umma::mma_tf32(tKK, Ks, 128, Ks, 128, 64, 64, 128, false);
-        umma::mma_tf32(tDT1, dWs, 128, Ks, 128, 64, 64, 128, false);
-        umma::mma_tf32(tDT2, dUs, 128, Vs, 128, 64, 64, 128, false);
+    if (ok && tid == 0) {
+        umma::mma(tKK, umma::swt(Ks, 64), umma::swt(Ks, 64), 64, 64, 128, false);
+        umma::mma(tDT1, umma::swt(dWs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
+        umma::mma(tDT2, umma::swt(dUs, 64), umma::swt(Vs, 64), 64, 64, 128, false);
         umma::mma_tf32(tTW, TC, 64, BW, 64, 64, 256, 64, false);
         umma::commit(mbar);
     }
-    bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
     // dW, dU and their transposes are consumed: fetch T for stage 2
-    for (int idx = tid; idx < 64 * 16; idx += 256) cp_async16(TR + idx * 4, Tg + idx * 4, true);
-    cp_async_commit();
+    if (ok && tid == 0) {
+        umma::mbar_expect_tx(mbl, 64 * 64 * 4);
+        umma::bulk_load(TR, Tg, 64 * 64 * 4, mbl);
+    }
     const int win = warp & 3, half = warp >> 2;
     const int r = win * 16 + lane;     // D row (lanes 0..15)
     const bool live = lane < 16;
@@ -767,7 +779,7 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
 #pragma unroll
                     for (int u = 0; u < 16; u += 4) {
                         const float4 k4 =
-                            *reinterpret_cast<const float4*>(Ks + umma::kidx(r, cc + u, 128));
+                            *reinterpret_cast<const float4*>(Ks + umma::swz(r, cc + u, 64));
                         rsum += v[u] * k4.x + v[u + 1] * k4.y + v[u + 2] * k4.z + v[u + 3] * k4.w;
                     }
                 } else {
@@ -775,7 +787,7 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
 #pragma unroll
                     for (int u = 0; u < 16; u += 4) {
                         const float4 v4 =
-                            *reinterpret_cast<const float4*>(Vs + umma::kidx(r, cc + u, 128));
+                            *reinterpret_cast<const float4*>(Vs + umma::swz(r, cc + u, 64));
                         rsum += v[u] * v4.x + v[u + 1] * v4.y + v[u + 2] * v4.z + v[u + 3] * v4.w;
                         st4(dv + u, make_float4(bet[r] * v[u], bet[r] * v[u + 1],
                                                 bet[r] * v[u + 2], bet[r] * v[u + 3]));
@@ -791,8 +803,8 @@ bwd_wy_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO
         dgs[tid] += be[tid] * rp[tid];
     }
     // stage 2 operands: T arrived as a K-major tile; K^T from the K tile
-    cp_async_wait<0>();
-    umma::transpose_kmajor_64x128(KT, Ks);
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbl, 1));
+    umma::transpose_sw_to_kmajor(KT, Ks, nullptr);
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
@@ -1019,10 +1031,21 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
         attr = true;
     }
     float* gate_part = w.nw_part + (size_t)a.NT * a.hv * kD;
+    TileMaps maps{};
     if (a.NT > 0) {
+        const int64_t C = (int64_t)(2 * a.hk + a.hv) * kD, vs = (int64_t)a.hv * kD;
+        cudaError_t e = make_rows_map(&maps.q, a.qkv, a.hk, a.T, C);
+        if (e == cudaSuccess) e = make_rows_map(&maps.k, a.qkv + (int64_t)a.hk * kD, a.hk, a.T, C);
+        if (e == cudaSuccess)
+            e = make_rows_map(&maps.v, a.qkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C);
+        if (e == cudaSuccess) e = make_rows_map(&maps.U, a.sv.U, a.hv, a.T, vs);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dO, w.dO, a.hv, a.T, vs);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dU, w.dU, a.hv, a.T, vs);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dW, w.dW, a.hv, a.T, vs);
+        if (e != cudaSuccess) return e;
         GDN_PROF("chunk_bwd_local", st);
         bwd_local_kernel<IO><<<dim3(a.NT, a.hv), 256, kB1Smem, st>>>(
-            a.qkv, a.hk, a.hv, (const IO*)a.z, a.norm_w, a.norm_eps, (const IO*)a.dy,
+            maps, a.hk, a.hv, (const IO*)a.z, a.norm_w, a.norm_eps, (const IO*)a.dy,
             (IO*)a.dz, a.sv, w);
     }
     if (a.N > 0) {
@@ -1033,16 +1056,16 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
     if (a.NT > 0) {
         {
             GDN_PROF("chunk_bwd_sfacing", st);
-            bwd_sfacing_kernel<<<dim3(a.NT, a.hv), 256, kB3aSmem, st>>>(a.qkv, a.hk, a.hv, a.sv,
+            bwd_sfacing_kernel<<<dim3(a.NT, a.hv), 256, kB3aSmem, st>>>(maps, a.hk, a.hv, a.sv,
                                                                           w);
         }
         {
             GDN_PROF("chunk_bwd_dp", st);
-            bwd_dp_kernel<<<dim3(a.NT, a.hv), 256, kDpSmem, st>>>(a.qkv, a.hk, a.hv, a.sv, w);
+            bwd_dp_kernel<<<dim3(a.NT, a.hv), 256, kDpSmem, st>>>(maps, a.hk, a.hv, a.sv, w);
         }
         GDN_PROF("chunk_bwd_wy", st);
         bwd_wy_kernel<IO><<<dim3(a.NT, a.hv), 256, kWySmem, st>>>(
-            a.qkv, (const IO*)a.a, (const IO*)a.b, a.A_log, a.dt_bias, a.hk, a.hv, a.dqkv,
+            maps, (const IO*)a.a, (const IO*)a.b, a.A_log, a.dt_bias, a.hk, a.hv, a.dqkv,
             (IO*)a.da, (IO*)a.db, gate_part, a.sv, w);
     }
     if (a.T > 0) {

@@ -72,45 +72,44 @@ __global__ void plan_kernel(const int32_t* __restrict__ cu, int N, int64_t T, in
 // ------------------------------------------------------------------ prep
 // grid (NT, Hv), 256 threads, tcgen05.  Gates and their in-chunk cumsum, then
 //   D1 = K K^T (64 x 64)  ->  A = beta_i e^{gam_i-gam_j} D1 (j < i)
-//   T  = (I + A)^-1        (forward substitution on the CUDA cores)
+//   T  = (I + A)^-1        (forward substitution on the CUDA cores; saved)
 //   D2 = T [diag(beta e^gam) K | diag(beta) V]   (one M=64, N=256, K=64 MMA)
-// giving W = D2[:, :128] and U~ = D2[:, 128:].
+// giving W = D2[:, :128] and U~ = D2[:, 128:].  K and V arrive as swizzled
+// tiles through the TMA; the B operand of D2 is transposed out of them.
 constexpr int kLdK = 132, kLdV = 136, kLdA = 68;
-constexpr int kPrepFloats = 64 * 128 + 256 * 64 + 2 * 64 * kLdA + 64 * 64 + 2 * 64 * kLdK;
-constexpr size_t kPrepSmem = sizeof(float) * (kPrepFloats + 3 * 64 + 16) + 64;
+constexpr int kPrepFloats = 2 * 64 * 128 + 256 * 64 + 2 * 64 * kLdA + 64 * 64;
+constexpr size_t kPrepSmem = sizeof(float) * (kPrepFloats + 3 * 64 + 16) + 64 + 1024;
 
 template <class IO>
 __global__ void __launch_bounds__(256, 1)
-prep_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO* __restrict__ bv,
-            const float* __restrict__ A_log, const float* __restrict__ dt_bias, int hk, int hv,
-            FwdSaved sv) {
-    extern __shared__ __align__(128) float sm[];
-    float* Ks = sm;                    // [64][128] K-major
-    float* Bs = Ks + 64 * 128;         // [256 (c | a)][64 (j)] K-major: (be K)^T ; (beta V)^T
+prep_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
+            const IO* __restrict__ bv, const float* __restrict__ A_log,
+            const float* __restrict__ dt_bias, int hk, int hv, FwdSaved sv) {
+    extern __shared__ float sm_raw[];
+    float* sm = umma::align1024(sm_raw);
+    float* Ks = sm;                    // [64][128] swizzled
+    float* Vs = Ks + 64 * 128;         // [64][128] swizzled
+    float* Bs = Vs + 64 * 128;         // [256 (c | a)][64 (j)] K-major: (be K)^T ; (beta V)^T
     float* As = Bs + 256 * 64;         // [64][kLdA] row-major A
     float* Tr = As + 64 * kLdA;        // [64][kLdA] row-major T
     float* Tk = Tr + 64 * kLdA;        // [64][64] K-major T
-    float* Kr = Tk + 64 * 64;          // [64][kLdK] row-major K (staging)
-    float* Vr = Kr + 64 * kLdK;        // [64][kLdK] row-major V (staging)
-    float* gam = Vr + 64 * kLdK;
+    float* gam = Tk + 64 * 64;
     float* bet = gam + 64;
     float* be = bet + 64;
     uint64_t* mbar = reinterpret_cast<uint64_t*>(be + 64 + 16);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
+    uint64_t* mbl = mbar + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
     const ChunkInfo ci = sv.chunks[blockIdx.x];
     if (ci.len == 0) return;
     const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
     const int warp = tid >> 5, lane = tid & 31;
-    const int C = (2 * hk + hv) * kD;
-    auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
-    const float* kbase = qkv + (int64_t)hk * kD + kh * kD;
-    const float* vbase = qkv + (int64_t)2 * hk * kD + h * kD;
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-        const int r = idx >> 5, c = (idx & 31) * 4;
-        cp_async16(Kr + r * kLdK + c, kbase + row(r) * C + c, r < L);
-        cp_async16(Vr + r * kLdK + c, vbase + row(r) * C + c, r < L);
+    if (tid == 0) {
+        umma::mbar_init(mbar, 1);
+        umma::mbar_init(mbl, 1);
+        umma::mbar_expect_tx(mbl, 2 * 64 * 128 * 4);
+        umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
+        umma::tma_rows(Vs, 64, &maps.v, h, ci.start, mbl);
     }
-    cp_async_commit();
     if (tid < 64) {
         float g = 0.f, b = 0.f;
         if (tid < L) {
@@ -122,7 +121,6 @@ prep_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO* 
         bet[tid] = b;
     }
     if (warp == 0) umma::tmem_alloc(tslot, 512);
-    if (tid == 0) umma::mbar_init(mbar, 1);
     __syncthreads();
     if (tid < 32) warp_cumsum64(gam);
     __syncthreads();
@@ -133,27 +131,27 @@ prep_kernel(const float* __restrict__ qkv, const IO* __restrict__ av, const IO* 
             sv.beta[(int64_t)h * sv.T + ci.start + tid] = bet[tid];
         }
     }
-    __syncthreads();
-    cp_async_wait<0>();
-    __syncthreads();
-    // B operand: rows c (0..127) = be_j K[j][c], rows 128 + a = beta_j V[j][a]
-    umma::transpose_rows_to_kmajor(Bs, Kr, kLdK, be);
-    umma::transpose_rows_to_kmajor(Bs + 128 * 64, Vr, kLdK, bet);
-    for (int idx = tid; idx < 64 * 32; idx += 256) {   // K rows -> K-major, rounded
-        const int r = (idx >> 8) * 8 + (idx & 7), c = ((idx >> 3) & 31) * 4;
-        *reinterpret_cast<float4*>(Ks + umma::kidx(r, c, 128)) =
-            umma::tf32r(*reinterpret_cast<const float4*>(Kr + r * kLdK + c));
+    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
+    if (L < 64) {   // tail rows belong to the next sequence
+        umma::zero_tail_rows(Ks, 64, 0, L);
+        umma::zero_tail_rows(Vs, 64, 0, L);
+        __syncthreads();
     }
+    // B operand: rows c (0..127) = be_j K[j][c], rows 128 + a = beta_j V[j][a]
+    umma::transpose_sw_to_kmajor(Bs, Ks, be);
+    umma::transpose_sw_to_kmajor(Bs + 128 * 64, Vs, bet);
+    __syncthreads();
+    umma::tf32r_inplace(Ks, 64 * 128);
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t tD1 = tmem, tD2 = tmem + 256;
-    if (tid == 0) {
-        umma::mma_tf32(tD1, Ks, 128, Ks, 128, 64, 64, 128, false);
+    if (ok && tid == 0) {
+        umma::mma(tD1, umma::swt(Ks, 64), umma::swt(Ks, 64), 64, 64, 128, false);
         umma::commit(mbar);
     }
-    bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
     const int win = warp & 3, half = warp >> 2;
     const int i = win * 16 + lane;
@@ -333,61 +331,64 @@ state_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const float* S_i
 //   P  = D1 (.) e^{gam_i - gam_j} (.) [i >= j]          -- staged K-major
 //   D2 = P U (64 x 128)
 //   O  = D2 + e^{gam_i} D3 ; y = O rsqrt(mean(O^2)+eps) (1+w) silu(z)
-// Shared memory (K-major core layout): Q, K 32 KB each, S0 (rows a) 64 KB,
-// U^T (rows a, k = token) 32 KB, P 16 KB.  Tensor memory: 320 fp32 columns.
+// Shared memory: Q, K, U swizzled 32 KB each (TMA), S0 (K-major rows a) 64 KB
+// (one bulk copy), U^T (rows a, k = token) 32 KB, P 16 KB; the z rows reuse the
+// U space.  Tensor memory: 320 fp32 columns.
 constexpr int kOutFloats = 64 * 128 * 2 + 128 * 128 + 128 * 64 + 64 * 64 + 64 * kLdK;
-constexpr size_t kOutSmem = sizeof(float) * (kOutFloats + 64 * 2 + 2 * 64 + 16) + 64;
+constexpr size_t kOutSmem = sizeof(float) * (kOutFloats + 64 * 2 + 2 * 64 + 16) + 64 + 1024;
 
 template <class IO>
 __global__ void __launch_bounds__(256, 1)
-out_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z,
+out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO* z,
                const float* norm_w, float norm_eps, IO* o_out, IO* y_out, FwdSaved sv) {
-    extern __shared__ __align__(128) float sm[];
-    float* Qs = sm;                    // [64][128]  K-major
-    float* Ks = Qs + 64 * 128;         // [64][128]
-    float* Ss = Ks + 64 * 128;         // [128 (a)][128 (b)]
-    float* UT = Ss + 128 * 128;        // [128 (a)][64 (j)]
-    float* Ps = UT + 128 * 64;         // [64 (i)][64 (j)]
-    float* Ur = Ps + 64 * 64;          // [64][kLdK] row-major U (staging)
-    float* gam = Ur + 64 * kLdK;
+    extern __shared__ float sm_raw[];
+    float* sm = umma::align1024(sm_raw);
+    float* Qs = sm;                    // [64][128] swizzled
+    float* Ks = Qs + 64 * 128;         // [64][128] swizzled
+    float* Ss = Ks + 64 * 128;         // [128 (a)][128 (b)] K-major
+    float* UT = Ss + 128 * 128;        // [128 (a)][64 (j)] K-major
+    float* Ps = UT + 128 * 64;         // [64 (i)][64 (j)] K-major
+    float* Us = Ps + 64 * 64;          // [64][128] swizzled U (then the z rows)
+    float* gam = Us + 64 * kLdK;
     float* eg = gam + 64;
     float* ssq = eg + 64;              // [2][64] partial sums of squares
     uint64_t* mbar = reinterpret_cast<uint64_t*>(ssq + 2 * 64 + 16);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
+    uint64_t* mbl = mbar + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
     const ChunkInfo ci = sv.chunks[blockIdx.x];
     if (ci.len == 0) return;
     const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
     const int warp = tid >> 5, lane = tid & 31;
-    const int C = (2 * hk + hv) * kD;
     auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-        const int r = idx >> 5, c = (idx & 31) * 4;
-        cp_async16(Qs + umma::kidx(r, c, 128), qkv + row(r) * C + kh * kD + c, r < L);
-        cp_async16(Ks + umma::kidx(r, c, 128), qkv + row(r) * C + (int64_t)hk * kD + kh * kD + c,
-                   r < L);
+    if (tid == 0) {
+        umma::mbar_init(mbar, 1);
+        umma::mbar_init(mbl, 1);
+        umma::mbar_expect_tx(mbl, 3 * 64 * 128 * 4 + 128 * 128 * 4);
+        umma::tma_rows(Qs, 64, &maps.q, kh, ci.start, mbl);
+        umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
+        umma::tma_rows(Us, 64, &maps.U, h, ci.start, mbl);
+        umma::bulk_load(Ss, sv.S0 + ((int64_t)blockIdx.x * hv + h) * kD * kD, 128 * 128 * 4, mbl);
     }
-    const float* S0 = sv.S0 + ((int64_t)blockIdx.x * hv + h) * kD * kD;   // K-major rows a
-    for (int idx = tid; idx < 128 * 32; idx += 256) cp_async16(Ss + idx * 4, S0 + idx * 4, true);
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-        const int r = idx >> 5, c = (idx & 31) * 4;
-        cp_async16(Ur + r * kLdK + c, sv.U + (row(r) * hv + h) * kD + c, r < L);
-    }
-    cp_async_commit();
     if (tid < 64) {  // padding rows continue the last gate value (g = 0)
         const float g = sv.gam[(int64_t)h * sv.T + row(tid)];
         gam[tid] = g;
         eg[tid] = tid < L ? expf(g) : 0.f;
     }
     if (warp == 0) umma::tmem_alloc(tslot, 512);
-    if (tid == 0) umma::mbar_init(mbar, 1);
-    cp_async_wait<0>();
     __syncthreads();
+    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
+    if (L < 64) {   // tail rows belong to the next sequence
+        umma::zero_tail_rows(Qs, 64, 0, L);
+        umma::zero_tail_rows(Ks, 64, 0, L);
+        umma::zero_tail_rows(Us, 64, 0, L);
+        __syncthreads();
+    }
     umma::tf32r_inplace(Qs, 64 * 128 * 2 + 128 * 128);   // Q, K, S0
-    umma::transpose_rows_to_kmajor(UT, Ur, kLdK, nullptr);
+    umma::transpose_sw_to_kmajor(UT, Us, nullptr);
     __syncthreads();
-    // U rows are transposed: their space takes the z rows for the norm epilogue
+    // U is transposed: its space takes the z rows for the norm epilogue
     constexpr int kZPitch = kD * (int)sizeof(IO) + 16;    // bytes; conflict-free row reads
-    char* Zs = reinterpret_cast<char*>(Ur);
+    char* Zs = reinterpret_cast<char*>(Us);
     if (z) {
         constexpr int kPieces = kD * (int)sizeof(IO) / 16;
         for (int idx = tid; idx < 64 * kPieces; idx += 256) {
@@ -402,12 +403,12 @@ out_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const IO* z,
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t tD1 = tmem, tD3 = tmem + 64, tD2 = tmem + 192;
-    if (tid == 0) {
-        umma::mma_tf32(tD1, Qs, 128, Ks, 128, 64, 64, 128, false);
-        umma::mma_tf32(tD3, Qs, 128, Ss, 128, 64, 128, 128, false);
+    if (ok && tid == 0) {
+        umma::mma(tD1, umma::swt(Qs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
+        umma::mma(tD3, umma::swt(Qs, 64), umma::kmaj(Ss, 128), 64, 128, 128, false);
         umma::commit(mbar);
     }
-    bool ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
     const int win = warp & 3, half = warp >> 2;
     const int i = win * 16 + lane;     // row held by lanes 0..15 (M = 64 layout)
@@ -513,10 +514,18 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
                              (int)kOutSmem);
         attr = true;
     }
+    TileMaps maps{};
     if (a.NT > 0) {
+        const int64_t C = (int64_t)(2 * a.hk + a.hv) * kD;
+        cudaError_t e = make_rows_map(&maps.q, a.qkv, a.hk, a.T, C);
+        if (e == cudaSuccess) e = make_rows_map(&maps.k, a.qkv + (int64_t)a.hk * kD, a.hk, a.T, C);
+        if (e == cudaSuccess)
+            e = make_rows_map(&maps.v, a.qkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C);
+        if (e == cudaSuccess) e = make_rows_map(&maps.U, a.sv.U, a.hv, a.T, (int64_t)a.hv * kD);
+        if (e != cudaSuccess) return e;
         GDN_PROF("chunk_prep", st);
         prep_kernel<IO><<<dim3(a.NT, a.hv), 256, kPrepSmem, st>>>(
-            a.qkv, (const IO*)a.a, (const IO*)a.b, a.A_log, a.dt_bias, a.hk, a.hv, a.sv);
+            maps, (const IO*)a.a, (const IO*)a.b, a.A_log, a.dt_bias, a.hk, a.hv, a.sv);
     }
     if (a.N > 0) {
         GDN_PROF("chunk_state_fwd", st);
@@ -526,7 +535,7 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
     if (a.NT > 0) {
         GDN_PROF("chunk_out_fwd", st);
         out_fwd_kernel<IO><<<dim3(a.NT, a.hv), 256, kOutSmem, st>>>(
-            a.qkv, a.hk, a.hv, (const IO*)a.z, a.norm_w, a.norm_eps, (IO*)a.o_out,
+            maps, a.hk, a.hv, (const IO*)a.z, a.norm_w, a.norm_eps, (IO*)a.o_out,
             (IO*)a.y_out, a.sv);
     }
     return cudaGetLastError();

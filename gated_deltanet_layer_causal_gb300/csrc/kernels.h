@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI (api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -48,6 +49,17 @@ struct FwdSaved {
     float* o;              // [T, Hv, d] core output (before the norm)
     float* rstd;           // [T, Hv] norm rstd
 };
+
+// Tensor maps of the row tensors the chunk kernels load as 64 x 128 tiles
+// (3-D: {128 columns, heads, tokens}, 64 x 32 boxes, 128-byte swizzle).
+constexpr int kTileCols = 128;
+struct TileMaps {
+    CUtensorMap q, k, v;   // q / k / v channels of the conv output [T, C]
+    CUtensorMap U;         // [T, Hv, d]
+    CUtensorMap dO, dU, dW;
+};
+cudaError_t make_rows_map(CUtensorMap* m, const float* base, int heads, int64_t T,
+                          int64_t token_stride);
 
 struct ChunkArgs {
     bool bf16;

@@ -15,10 +15,18 @@
 // 32*(w%4) .. 32*(w%4)+31.
 #pragma once
 
+#include <cuda.h>
 #include <stdint.h>
 
 namespace gdn {
 namespace umma {
+
+// Shared-memory base rounded up to 1024 bytes (swizzled tiles need it; the
+// dynamic allocation reserves the extra kilobyte).
+__device__ __forceinline__ float* align1024(float* p) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    return p + (((1024u - (a & 1023u)) & 1023u) >> 2);
+}
 
 __device__ __forceinline__ int kidx(int r, int k, int Kd) {
     return (((r >> 3) * (Kd >> 2) + (k >> 2)) << 5) + ((r & 7) << 2) + (k & 3);
@@ -38,6 +46,39 @@ __device__ __forceinline__ uint64_t desc(const float* tile, int k0, int Kd) {
     return d;                                                  // no swizzle, base offset 0
 }
 
+// 128-byte-swizzled K-major tiles, as the tensor-memory-access unit (TMA)
+// writes them: a [rows][128] fp32 tile is four boxes of [rows][32] (128 B per
+// row); within a box, 16-byte piece p of row r sits at piece p ^ (r % 8).
+// Tile bases are 1024-byte aligned.  Float offset of element (r, c):
+__device__ __forceinline__ int swz(int r, int c, int rows) {
+    return ((c >> 5) * rows + r) * 32 + ((((c >> 2) & 7) ^ (r & 7)) << 2) + (c & 3);
+}
+
+// Descriptor of the K = 8 slice at column k0 of a swizzled tile: start inside
+// the 128-byte row, 8-row groups 1024 B apart, layout type 2 (128-byte swizzle).
+__device__ __forceinline__ uint64_t desc_sw(const float* tile, int rows, int k0) {
+    const uint32_t a = saddr(tile) + (uint32_t)((k0 >> 5) * rows * 128 + (k0 & 31) * 4);
+    uint64_t d = (uint64_t)((a >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;                    // leading byte offset (unused here)
+    d |= (uint64_t)(1024u >> 4) << 32;         // stride byte offset
+    d |= (uint64_t)1 << 46;                    // descriptor version
+    d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+    return d;
+}
+
+// An MMA operand in shared memory: a no-swizzle K-major tile (n = its K
+// extent) or a swizzled tile (n = its row count).
+struct Op {
+    const float* p;
+    int n;
+    bool sw;
+};
+__device__ __forceinline__ Op kmaj(const float* p, int kd) { return Op{p, kd, false}; }
+__device__ __forceinline__ Op swt(const float* p, int rows) { return Op{p, rows, true}; }
+__device__ __forceinline__ uint64_t opdesc(const Op& o, int k0) {
+    return o.sw ? desc_sw(o.p, o.n, k0) : desc(o.p, k0, o.n);
+}
+
 // Instruction descriptor: D fp32, A and B tf32, both K-major, M x N.
 __device__ __forceinline__ uint32_t idesc_tf32(int M, int N) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
@@ -51,6 +92,20 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, const float* A, int ld
     const uint32_t id = idesc_tf32(M, N);
     for (int k0 = 0; k0 < K; k0 += 8) {
         const uint64_t ad = desc(A, k0, lda_k), bd = desc(B, k0, ldb_k);
+        const uint32_t acc = (accumulate || k0 > 0) ? 1u : 0u;
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+            "l"(ad), "l"(bd), "r"(id), "r"(acc));
+    }
+}
+
+// The same for operands of either layout.
+__device__ __forceinline__ void mma(uint32_t d_tmem, const Op& A, const Op& B, int M, int N, int K,
+                                    bool accumulate) {
+    const uint32_t id = idesc_tf32(M, N);
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        const uint64_t ad = opdesc(A, k0), bd = opdesc(B, k0);
         const uint32_t acc = (accumulate || k0 > 0) ? 1u : 0u;
         asm volatile(
             "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
@@ -83,6 +138,52 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, int l
             : "r"(saddr(mbar)), "r"(parity));
     }
     return done != 0;
+}
+
+// Arm `mbar` (count 1) for `bytes` of asynchronous copies; the calling thread
+// arrives.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(saddr(mbar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// 64 rows (tokens t0..t0+63) x 128 fp32 of one head through a 3-D tensor map
+// {128, heads, tokens}: four swizzled 64 x 32 boxes into a tile whose boxes
+// are `rows` rows apart (rows = 64, or 128 for the lower half of a stacked
+// tile).  Rows past the end of the tensor arrive as zeros.  32 KB on `mbar`.
+__device__ __forceinline__ void tma_rows(float* dst, int rows, const CUtensorMap* map, int head,
+                                         int t0, uint64_t* mbar) {
+#pragma unroll
+    for (int b = 0; b < 4; b++)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+            "[%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(saddr(dst + b * rows * 32)),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(b * 32), "r"(head), "r"(t0),
+            "r"(saddr(mbar))
+            : "memory");
+}
+
+// Contiguous copy global -> shared (both 16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];\n" ::"r"(saddr(dst)),
+        "l"(src), "r"(bytes), "r"(saddr(mbar))
+        : "memory");
+}
+
+// Zero rows [r0, 64) of the 64-row block at `row0` of a swizzled tile (a chunk
+// shorter than 64 tokens: its tail rows hold the next sequence's tokens).
+// A whole 128-byte row is one box row, so the swizzle does not matter.
+__device__ __forceinline__ void zero_tail_rows(float* tile, int rows, int row0, int r0) {
+    const int n = (64 - r0) * 32;   // floats per box
+    for (int e = threadIdx.x * 4; e < 4 * n; e += blockDim.x * 4) {
+        const int b = e / n, o = e % n;
+        *reinterpret_cast<float4*>(tile + (b * rows + row0 + r0) * 32 + o) =
+            make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 }
 
 // Generic-proxy shared-memory writes -> visible to the tensor core.
@@ -162,19 +263,20 @@ __device__ __forceinline__ void transpose_rows_to_kmajor(float* dst, const float
     }
 }
 
-// K-major tile [64 rows][128 (K)] -> K-major tile [128 rows][64 (K)] (its
-// transpose), whole CTA.  An 8 x 8 block is two adjacent core matrices (64
-// contiguous floats) on both sides: one warp moves a block per step, reads
-// conflict-free, writes two-way conflicted.
-__device__ __forceinline__ void transpose_kmajor_64x128(float* dst, const float* src) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    const int rr = lane >> 2, c4 = lane & 3;
-    for (int blk = warp; blk < 128; blk += nw) {
-        const int R8 = blk & 7, C8 = blk >> 3;
-        const float* s = src + (R8 * 32 + 2 * C8) * 32;
-        float* d = dst + (C8 * 16 + 2 * R8) * 32 + (rr >> 2) * 32 + c4 * 4 + (rr & 3);
-        d[0] = s[lane];
-        d[16] = s[lane + 32];
+// Swizzled tile [64 tokens][128] -> K-major tile [128 (column)][64 (token)],
+// rows optionally scaled per token, tf32-rounded.  Lanes take 32 columns of one
+// token row (a permutation of one 128-byte box row: no bank conflicts).
+__device__ __forceinline__ void transpose_sw_to_kmajor(float* dst, const float* src,
+                                                       const float* scale) {
+    for (int idx = threadIdx.x; idx < 128 * 16; idx += blockDim.x) {
+        const int c = idx & 127, j4 = idx >> 7;
+        float4 v = make_float4(src[swz(4 * j4 + 0, c, 64)], src[swz(4 * j4 + 1, c, 64)],
+                               src[swz(4 * j4 + 2, c, 64)], src[swz(4 * j4 + 3, c, 64)]);
+        if (scale) {
+            v.x *= scale[4 * j4 + 0]; v.y *= scale[4 * j4 + 1];
+            v.z *= scale[4 * j4 + 2]; v.w *= scale[4 * j4 + 3];
+        }
+        *reinterpret_cast<float4*>(dst + kidx(c, 4 * j4, 64)) = tf32r(v);
     }
 }
 
