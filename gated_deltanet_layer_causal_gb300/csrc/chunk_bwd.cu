@@ -171,23 +171,28 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
     umma::fence_after_sync();
+    // dU_local staged as a swizzled tile in the Q space (consumed), stored whole
     if (ok) {
-        for (int cc = 0; cc < 64; cc += 16) {
-            float v[16];
-            umma::tmem_ld16(umma::tmem_at(tD2, half * 64 + cc), v);
-            if (lane < 16 && j < L) {
-                float* dst = w.dU + ((int64_t)(ci.start + j) * hv + h) * kD + half * 64 + cc;
-#pragma unroll
-                for (int u = 0; u < 16; u += 4)
-                    st4(dst + u, make_float4(v[u], v[u + 1], v[u + 2], v[u + 3]));
-            }
-        }
+        float v[32];
+        umma::tmem_ld64_m64(umma::tmem_at(tD2, half * 64), v);
+        umma::frag_to_sw(Qs, v, half * 64, 1.f, 1.f);
     } else if (tid == 0) {
         atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
     }
+    umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 256);
+    if (!ok) return;
+    if (L == 64) {
+        if (tid == 0) {
+            umma::tma_store_rows(&maps.dU, h, ci.start, Qs);
+            umma::bulk_commit();
+            umma::bulk_wait_read();
+        }
+    } else {
+        umma::store_rows_sw(w.dU + ((int64_t)ci.start * hv + h) * kD, (int64_t)hv * kD, Qs, L);
+    }
 }
 
 // ------------------------------------------------------------------ B2: reverse state pass
@@ -347,7 +352,6 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSav
     const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
     const int warp = tid >> 5, lane = tid & 31;
     const int64_t sb = ((int64_t)blockIdx.x * hv + h) * kD * kD;
-    auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
     // ---- stage operands: row tiles through the TMA; dS^T and S0^T are stored
     // as K-major tiles with rows b, copied whole
     if (tid == 0) {
@@ -402,6 +406,11 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSav
         umma::tma_rows(Kr, 64, &maps.k, kh, ci.start, mbl);
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbl, 1));
+    // outputs are staged as swizzled tiles in the consumed operand space and
+    // stored whole: dQ part and dW over [dO; dU], dK part over U
+    float* SQ = A1;                      // [64][128] swizzled
+    float* SW = A1 + 64 * 128;           // [64][128] swizzled
+    float* SK = A2;                      // [64][128] swizzled
     if (!ok) {
         if (tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
     } else {
@@ -415,57 +424,67 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSav
                 float v[16];
                 umma::tmem_ld16(umma::tmem_at(tmem, c0 + cc), v);
                 if (r < 64) {
-                    const int i = r;
-                    if (i < L) {
-                        float* dst = w.dQv + (row(i) * hv + h) * kD + c0 + cc;
+                    const float e = eg[r];
 #pragma unroll
-                        for (int u = 0; u < 16; u += 4) {
-                            const float4 q4 = *reinterpret_cast<const float4*>(
-                                Qr + umma::swz(i, c0 + cc + u, 64));
-                            part += v[u] * q4.x + v[u + 1] * q4.y + v[u + 2] * q4.z +
-                                    v[u + 3] * q4.w;
-                            st4(dst + u, make_float4(eg[i] * v[u], eg[i] * v[u + 1],
-                                                     eg[i] * v[u + 2], eg[i] * v[u + 3]));
-                        }
+                    for (int u = 0; u < 16; u += 4) {
+                        const float4 q4 = *reinterpret_cast<const float4*>(
+                            Qr + umma::swz(r, c0 + cc + u, 64));
+                        part += v[u] * q4.x + v[u + 1] * q4.y + v[u + 2] * q4.z + v[u + 3] * q4.w;
+                        *reinterpret_cast<float4*>(SQ + umma::swz(r, c0 + cc + u, 64)) =
+                            make_float4(e * v[u], e * v[u + 1], e * v[u + 2], e * v[u + 3]);
                     }
                 } else {
-                    const int i = r - 64;
-                    if (i < L) {
-                        float* dst = w.dW + (row(i) * hv + h) * kD + c0 + cc;
 #pragma unroll
-                        for (int u = 0; u < 16; u += 4)
-                            st4(dst + u, make_float4(-v[u], -v[u + 1], -v[u + 2], -v[u + 3]));
-                    }
+                    for (int u = 0; u < 16; u += 4)
+                        *reinterpret_cast<float4*>(SW + umma::swz(r - 64, c0 + cc + u, 64)) =
+                            make_float4(-v[u], -v[u + 1], -v[u + 2], -v[u + 3]);
                 }
             }
             if (r < 64) rpart[half * 128 + r] = r < L ? eg[r] * part : 0.f;
         }
-        // D2 (M = 64): row j = 16 * win + lane for lanes 0..15
+        // D2 (M = 64): rows rl and rl + 8 of this thread's fragment
         {
-            const int j = win * 16 + lane;
-            float part = 0.f;
-            for (int cc = 0; cc < 64; cc += 16) {
-                float v[16];
-                umma::tmem_ld16(umma::tmem_at(tmem + 128, c0 + cc), v);
-                if (lane < 16 && j < L) {
-                    float* dst = w.dKv + (row(j) * hv + h) * kD + c0 + cc;
+            float v[32];
+            umma::tmem_ld64_m64(umma::tmem_at(tmem + 128, c0), v);
+            const int rl = umma::frag_row_lo(), rh = rl + 8;
+            float pl = 0.f, ph = 0.f;
 #pragma unroll
-                    for (int u = 0; u < 16; u += 4) {
-                        const float4 k4 = *reinterpret_cast<const float4*>(
-                            Kr + umma::swz(j, c0 + cc + u, 64));
-                        part += v[u] * k4.x + v[u + 1] * k4.y + v[u + 2] * k4.z + v[u + 3] * k4.w;
-                        st4(dst + u, make_float4(fk[j] * v[u], fk[j] * v[u + 1],
-                                                 fk[j] * v[u + 2], fk[j] * v[u + 3]));
-                    }
-                }
+            for (int k = 0; k < 8; k++) {
+                const int c = c0 + 8 * k + 2 * (lane & 3);
+                const float2 kl = *reinterpret_cast<const float2*>(Kr + umma::swz(rl, c, 64));
+                const float2 kh2 = *reinterpret_cast<const float2*>(Kr + umma::swz(rh, c, 64));
+                pl += v[4 * k] * kl.x + v[4 * k + 1] * kl.y;
+                ph += v[4 * k + 2] * kh2.x + v[4 * k + 3] * kh2.y;
             }
-            if (lane < 16) rpart[half * 128 + 64 + j] = j < L ? fk[j] * part : 0.f;
+            pl += __shfl_xor_sync(0xffffffffu, pl, 1);
+            pl += __shfl_xor_sync(0xffffffffu, pl, 2);
+            ph += __shfl_xor_sync(0xffffffffu, ph, 1);
+            ph += __shfl_xor_sync(0xffffffffu, ph, 2);
+            umma::frag_to_sw(SK, v, c0, fk[rl], fk[rh]);
+            if ((lane & 3) == 0) {
+                rpart[half * 128 + 64 + rl] = rl < L ? fk[rl] * pl : 0.f;
+                rpart[half * 128 + 64 + rh] = rh < L ? fk[rh] * ph : 0.f;
+            }
         }
     }
+    umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 256);
     if (!ok) return;
+    if (L == 64) {
+        if (tid == 0) {
+            umma::tma_store_rows(&maps.dQv, h, ci.start, SQ);
+            umma::tma_store_rows(&maps.dW, h, ci.start, SW);
+            umma::tma_store_rows(&maps.dKv, h, ci.start, SK);
+            umma::bulk_commit();
+        }
+    } else {
+        const int64_t off = ((int64_t)ci.start * hv + h) * kD, st = (int64_t)hv * kD;
+        umma::store_rows_sw(w.dQv + off, st, SQ, L);
+        umma::store_rows_sw(w.dW + off, st, SW, L);
+        umma::store_rows_sw(w.dKv + off, st, SK, L);
+    }
     if (tid < 64 && tid < L) {
         float g = (rpart[tid] + rpart[128 + tid]) - (rpart[64 + tid] + rpart[192 + tid]);
         if (tid == L - 1) {
@@ -476,6 +495,7 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSav
         }
         w.dgam[(int64_t)(ci.start + tid) * hv + h] = g;
     }
+    if (tid == 0) umma::bulk_wait_read();   // the tile stores have read shared memory
 }
 
 // ------------------------------------------------------------------ B3b: P / dP terms
@@ -513,7 +533,6 @@ bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv
     if (ci.len == 0) return;
     const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
     const int warp = tid >> 5, lane = tid & 31;
-    auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
     if (tid == 0) {
         umma::mbar_init(mbar, 1);
         umma::mbar_init(mbl, 1);
@@ -602,26 +621,33 @@ bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
     umma::fence_after_sync();
+    // dQ, dK staged as swizzled tiles in the Q / K space, then stored whole
     if (ok) {
-        for (int cc = 0; cc < 64; cc += 16) {
-            float vq[16], vk[16];
-            umma::tmem_ld16(umma::tmem_at(tDQ, half * 64 + cc), vq);
-            umma::tmem_ld16(umma::tmem_at(tDK, half * 64 + cc), vk);
-            if (lane < 16 && i < L) {
-                const int64_t off = (row(i) * hv + h) * kD + half * 64 + cc;
-#pragma unroll
-                for (int u = 0; u < 16; u += 4) {
-                    st4(w.dQv2 + off + u, make_float4(vq[u], vq[u + 1], vq[u + 2], vq[u + 3]));
-                    st4(w.dKv2 + off + u, make_float4(vk[u], vk[u + 1], vk[u + 2], vk[u + 3]));
-                }
-            }
-        }
+        float v[32];
+        umma::tmem_ld64_m64(umma::tmem_at(tDQ, half * 64), v);
+        umma::frag_to_sw(Qs, v, half * 64, 1.f, 1.f);
+        umma::tmem_ld64_m64(umma::tmem_at(tDK, half * 64), v);
+        umma::frag_to_sw(Ks, v, half * 64, 1.f, 1.f);
     } else if (tid == 0) {
         atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
     }
+    umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 256);
+    if (!ok) return;
+    if (L == 64) {
+        if (tid == 0) {
+            umma::tma_store_rows(&maps.dQv2, h, ci.start, Qs);
+            umma::tma_store_rows(&maps.dKv2, h, ci.start, Ks);
+            umma::bulk_commit();
+            umma::bulk_wait_read();
+        }
+    } else {
+        const int64_t off = ((int64_t)ci.start * hv + h) * kD;
+        umma::store_rows_sw(w.dQv2 + off, (int64_t)hv * kD, Qs, L);
+        umma::store_rows_sw(w.dKv2 + off, (int64_t)hv * kD, Ks, L);
+    }
 }
 
 // ------------------------------------------------------------------ B3c: WY terms and gates
@@ -882,27 +908,38 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
     umma::fence_after_sync();
+    // dK part = dKK product + diag(beta e^gam) T^T dW, staged as a swizzled
+    // tile in the K space (consumed) and stored whole
     if (ok) {
-        for (int cc = 0; cc < 64; cc += 16) {
-            float vk[16], vw[16];
-            umma::tmem_ld16(umma::tmem_at(tX, half * 64 + cc), vk);
-            umma::tmem_ld16(umma::tmem_at(tTW, half * 64 + cc), vw);
-            if (live && r < L) {
-                const int64_t off = vrow(r) + half * 64 + cc;
+        float vk[32], vw[32];
+        umma::tmem_ld64_m64(umma::tmem_at(tX, half * 64), vk);
+        umma::tmem_ld64_m64(umma::tmem_at(tTW, half * 64), vw);
+        const int rl = umma::frag_row_lo();
+        const float bl = be[rl], bh = be[rl + 8];
 #pragma unroll
-                for (int u = 0; u < 16; u += 4)
-                    st4(w.dKv3 + off + u,
-                        make_float4(vk[u] + be[r] * vw[u], vk[u + 1] + be[r] * vw[u + 1],
-                                    vk[u + 2] + be[r] * vw[u + 2], vk[u + 3] + be[r] * vw[u + 3]));
-            }
+        for (int k = 0; k < 8; k++) {
+            vk[4 * k] += bl * vw[4 * k];
+            vk[4 * k + 1] += bl * vw[4 * k + 1];
+            vk[4 * k + 2] += bh * vw[4 * k + 2];
+            vk[4 * k + 3] += bh * vw[4 * k + 3];
         }
+        umma::frag_to_sw(Ks, vk, half * 64, 1.f, 1.f);
     } else if (tid == 0) {
         atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
     }
+    umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 512);
     if (!ok) return;
+    if (L == 64) {
+        if (tid == 0) {
+            umma::tma_store_rows(&maps.dKv3, h, ci.start, Ks);
+            umma::bulk_commit();
+        }
+    } else {
+        umma::store_rows_sw(w.dKv3 + ((int64_t)ci.start * hv + h) * kD, (int64_t)hv * kD, Ks, L);
+    }
     // ---- dg = reverse cumsum of dgam; gates
     if (tid < 64) sc[tid] = tid < L ? dgs[tid] + w.dgam[(int64_t)(ci.start + tid) * hv + h] : 0.f;
     __syncthreads();
@@ -942,6 +979,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     if (tid == 0) {
         gate_part[((int64_t)blockIdx.x * hv + h) * 2 + 0] = red[0] + red[1];
         gate_part[((int64_t)blockIdx.x * hv + h) * 2 + 1] = red[2] + red[3];
+        umma::bulk_wait_read();   // the dK tile store has read its shared memory
     }
 }
 
@@ -1042,6 +1080,13 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
         if (e == cudaSuccess) e = make_rows_map(&maps.dO, w.dO, a.hv, a.T, vs);
         if (e == cudaSuccess) e = make_rows_map(&maps.dU, w.dU, a.hv, a.T, vs);
         if (e == cudaSuccess) e = make_rows_map(&maps.dW, w.dW, a.hv, a.T, vs);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dQv, w.dQv, a.hv, a.T, vs);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dKv, w.dKv, a.hv, a.T, vs);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dQv2, w.dQv2, a.hv, a.T, vs);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dKv2, w.dKv2, a.hv, a.T, vs);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dKv3, w.dKv3, a.hv, a.T, vs);
+        if (e == cudaSuccess)
+            e = make_rows_map(&maps.dv, a.dqkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C);
         if (e != cudaSuccess) return e;
         GDN_PROF("chunk_bwd_local", st);
         bwd_local_kernel<IO><<<dim3(a.NT, a.hv), 256, kB1Smem, st>>>(

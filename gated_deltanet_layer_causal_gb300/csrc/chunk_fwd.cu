@@ -198,25 +198,36 @@ prep_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
     umma::fence_after_sync();
+    // warp half 0 -> W (columns 0..127), half 1 -> U~ (128..255), staged as
+    // swizzled tiles in the K / V space (consumed) and stored whole
     if (ok) {
-        // warp half 0 -> W (columns 0..127), half 1 -> U~ (128..255)
-        float* dstbase = half == 0 ? sv.W : sv.U;
-        for (int cc = 0; cc < 128; cc += 16) {
-            float v[16];
-            umma::tmem_ld16(umma::tmem_at(tD2, half * 128 + cc), v);
-            if (lane < 16 && i < L) {
-                float* dst = dstbase + ((int64_t)(ci.start + i) * hv + h) * kD + cc;
+        float* Sw = half == 0 ? Ks : Vs;
+        float v[32];
 #pragma unroll
-                for (int u = 0; u < 16; u += 4)
-                    st4(dst + u, make_float4(v[u], v[u + 1], v[u + 2], v[u + 3]));
-            }
+        for (int c0 = 0; c0 < 128; c0 += 64) {
+            umma::tmem_ld64_m64(umma::tmem_at(tD2, half * 128 + c0), v);
+            umma::frag_to_sw(Sw, v, c0, 1.f, 1.f);
         }
     } else if (tid == 0) {
         atomicExch(sv.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
     }
+    umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 512);
+    if (!ok) return;
+    if (L == 64) {
+        if (tid == 0) {
+            umma::tma_store_rows(&maps.W, h, ci.start, Ks);
+            umma::tma_store_rows(&maps.U, h, ci.start, Vs);
+            umma::bulk_commit();
+            umma::bulk_wait_read();
+        }
+    } else {
+        const int64_t off = ((int64_t)ci.start * hv + h) * kD;
+        umma::store_rows_sw(sv.W + off, (int64_t)hv * kD, Ks, L);
+        umma::store_rows_sw(sv.U + off, (int64_t)hv * kD, Vs, L);
+    }
 }
 
 // ------------------------------------------------------------------ state pass
@@ -522,6 +533,7 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
         if (e == cudaSuccess)
             e = make_rows_map(&maps.v, a.qkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C);
         if (e == cudaSuccess) e = make_rows_map(&maps.U, a.sv.U, a.hv, a.T, (int64_t)a.hv * kD);
+        if (e == cudaSuccess) e = make_rows_map(&maps.W, a.sv.W, a.hv, a.T, (int64_t)a.hv * kD);
         if (e != cudaSuccess) return e;
         GDN_PROF("chunk_prep", st);
         prep_kernel<IO><<<dim3(a.NT, a.hv), 256, kPrepSmem, st>>>(

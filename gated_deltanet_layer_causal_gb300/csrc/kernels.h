@@ -55,8 +55,10 @@ struct FwdSaved {
 constexpr int kTileCols = 128;
 struct TileMaps {
     CUtensorMap q, k, v;   // q / k / v channels of the conv output [T, C]
-    CUtensorMap U;         // [T, Hv, d]
+    CUtensorMap W, U;      // [T, Hv, d]
     CUtensorMap dO, dU, dW;
+    CUtensorMap dQv, dKv, dQv2, dKv2, dKv3;
+    CUtensorMap dv;        // v channels of the conv-output gradient [T, C]
 };
 cudaError_t make_rows_map(CUtensorMap* m, const float* base, int heads, int64_t T,
                           int64_t token_stride);

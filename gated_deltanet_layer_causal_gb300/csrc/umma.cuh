@@ -280,6 +280,75 @@ __device__ __forceinline__ void transpose_sw_to_kmajor(float* dst, const float* 
     }
 }
 
+// Eight 16x256b loads of an M = 64 accumulator (columns col0 .. col0 + 63 of
+// this warp's 16-lane window, one wait): thread t holds, for column block k,
+// v[4k + j] = D[row0 + t/4 + 8 (j/2)][col0 + 8k + 2 (t%4) + j%2], where row0 =
+// 16 * (warp % 4).  All 32 lanes carry data (the 32x32b shape leaves half of
+// them empty for M = 64).
+__device__ __forceinline__ void tmem_ld64_m64(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+#pragma unroll
+    for (int k = 0; k < 8; k++)
+        asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];\n"
+                     : "=r"(r[4 * k]), "=r"(r[4 * k + 1]), "=r"(r[4 * k + 2]), "=r"(r[4 * k + 3])
+                     : "r"(taddr + 8 * k));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// Write this thread's part of an M = 64 fragment (tmem_ld64_m64) into columns
+// c0 .. c0 + 63 of a swizzled [64][128] tile, rows scaled by s_lo / s_hi (the
+// thread's rows r and r + 8).  Two-float stores, no bank conflicts.
+__device__ __forceinline__ void frag_to_sw(float* tile, const float (&v)[32], int c0, float s_lo,
+                                           float s_hi) {
+    const int lane = threadIdx.x & 31, r = 16 * ((threadIdx.x >> 5) & 3) + (lane >> 2);
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        const int c = c0 + 8 * k + 2 * (lane & 3);
+        *reinterpret_cast<float2*>(tile + swz(r, c, 64)) =
+            make_float2(v[4 * k] * s_lo, v[4 * k + 1] * s_lo);
+        *reinterpret_cast<float2*>(tile + swz(r + 8, c, 64)) =
+            make_float2(v[4 * k + 2] * s_hi, v[4 * k + 3] * s_hi);
+    }
+}
+// Rows of this thread in an M = 64 fragment.
+__device__ __forceinline__ int frag_row_lo() {
+    return 16 * ((threadIdx.x >> 5) & 3) + ((threadIdx.x & 31) >> 2);
+}
+
+// Store a 64-row swizzled tile to 64 rows of a 3-D row tensor through its
+// tensor map (rows past the tensor's end are dropped).  Shared-memory writes
+// must be fenced to the async proxy and synchronised before the call; the
+// caller commits and waits (bulk_commit / bulk_wait_read) before the tile's
+// space is reused or the CTA exits.
+__device__ __forceinline__ void tma_store_rows(const CUtensorMap* map, int head, int t0,
+                                               const float* src) {
+#pragma unroll
+    for (int b = 0; b < 4; b++)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];\n" ::"l"(
+                reinterpret_cast<uint64_t>(map)),
+            "r"(b * 32), "r"(head), "r"(t0), "r"(saddr(src + b * 64 * 32))
+            : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+
+// Rows 0 .. L-1 of a 64-row swizzled tile to a row-major global tensor (row r
+// at dst + r * stride), one warp per row: the path for a chunk shorter than 64
+// tokens, whose remaining rows belong to the next sequence.
+__device__ __forceinline__ void store_rows_sw(float* dst, int64_t stride, const float* src, int L) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int r = warp; r < L; r += nw)
+        *reinterpret_cast<float4*>(dst + r * stride + 4 * lane) =
+            *reinterpret_cast<const float4*>(src + swz(r, 4 * lane, 64));
+}
+
 // Tensor-memory address of (lane window of this warp, column col).
 __device__ __forceinline__ uint32_t tmem_at(uint32_t base, int col) {
     const uint32_t lane0 = (uint32_t)((threadIdx.x >> 5) & 3) * 32u;
