@@ -103,7 +103,7 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO
             } else {
                 d4 = y8[k];
             }
-            st4(w.dO + off, d4);
+            st4(w.dO + off, umma::tf32r(d4));   // only ever a tensor-core operand
         }
         st4(dOr + r * kL4 + lane * 4, d4);
     }
@@ -140,24 +140,22 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
-    const int win = warp & 3, half = warp >> 2;
-    const int j = win * 16 + lane;     // row of D1 = key index j
-    if (ok) {
-        for (int cc = 0; cc < 32; cc += 16) {
-            float v[16];
-            const int i0 = half * 32 + cc;
-            umma::tmem_ld16(umma::tmem_at(tD1, i0), v);
-            if (lane < 16) {
+    const int half = warp >> 2;
+    if (ok) {   // P^T[j][i], 32 columns per warp, all lanes
+        float v[16];
+        umma::tmem_ld_m64<4>(umma::tmem_at(tD1, half * 32), v);
+        const int rl = umma::frag_row_lo(), cf = umma::frag_col();
 #pragma unroll
-                for (int u = 0; u < 16; u += 4) {
-                    const int i = i0 + u;
-                    float4 p;
-                    p.x = (i + 0 >= j) ? v[u + 0] * expf(gam[i + 0] - gam[j]) : 0.f;
-                    p.y = (i + 1 >= j) ? v[u + 1] * expf(gam[i + 1] - gam[j]) : 0.f;
-                    p.z = (i + 2 >= j) ? v[u + 2] * expf(gam[i + 2] - gam[j]) : 0.f;
-                    p.w = (i + 3 >= j) ? v[u + 3] * expf(gam[i + 3] - gam[j]) : 0.f;
-                    *reinterpret_cast<float4*>(PT + umma::kidx(j, i, 64)) = umma::tf32r(p);
-                }
+        for (int hr = 0; hr < 2; hr++) {
+            const int jr = rl + 8 * hr;
+            const float gj = gam[jr];
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const int i = half * 32 + 8 * k + cf;
+                const float p0 = i >= jr ? v[4 * k + 2 * hr] * expf(gam[i] - gj) : 0.f;
+                const float p1 = i + 1 >= jr ? v[4 * k + 2 * hr + 1] * expf(gam[i + 1] - gj) : 0.f;
+                *reinterpret_cast<float2*>(PT + umma::kidx(jr, i, 64)) =
+                    make_float2(umma::tf32r(p0), umma::tf32r(p1));
             }
         }
     }
@@ -297,7 +295,8 @@ bwd_state_kernel(const float* __restrict__ qkv, int hk, int hv, const float* dS_
         tile_each<64, kSl, 8>(uacc, [&](int i, int a, float& v) {
             const float u = i < L ? dUc[i * kLdS + a] + v : 0.f;
             dUc[i * kLdS + a] = u;
-            if (i < L) w.dU[((int64_t)(info.start + i) * hv + h) * kD + a0 + a] = u;
+            // stored rounded: later kernels use dU only as a tensor-core operand
+            if (i < L) w.dU[((int64_t)(info.start + i) * hv + h) * kD + a0 + a] = umma::tf32r(u);
         });
         __syncthreads();
         // dS^T = e^{gam_L} dS^T + Q~^T dO - W^T dU
@@ -380,7 +379,7 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSav
         if (lane == 0) red[warp] = dot;
     }
     __syncthreads();
-    umma::tf32r_inplace(A1, kSfFloats);
+    umma::tf32r_inplace(S0T, 2 * 128 * 128);   // S0^T, dS^T (dO, dU, U arrive rounded)
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -435,9 +434,9 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSav
                     }
                 } else {
 #pragma unroll
-                    for (int u = 0; u < 16; u += 4)
+                    for (int u = 0; u < 16; u += 4)   // dW: a tensor-core operand only, rounded
                         *reinterpret_cast<float4*>(SW + umma::swz(r - 64, c0 + cc + u, 64)) =
-                            make_float4(-v[u], -v[u + 1], -v[u + 2], -v[u + 3]);
+                            umma::tf32r(make_float4(-v[u], -v[u + 1], -v[u + 2], -v[u + 3]));
                 }
             }
             if (r < 64) rpart[half * 128 + r] = r < L ? eg[r] * part : 0.f;
@@ -553,7 +552,7 @@ bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv
         umma::zero_tail_rows(Us, 64, 0, L);
         __syncthreads();
     }
-    umma::tf32r_inplace(Qs, 4 * 64 * 128);   // Q, K, dO, U
+    umma::tf32r_inplace(Qs, 2 * 64 * 128);   // Q, K (dO and U arrive rounded)
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -567,34 +566,47 @@ bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
     const int win = warp & 3, half = warp >> 2;
-    const int i = win * 16 + lane;     // D row (lanes 0..15)
-    if (ok) {
-        float rsum = 0.f;
-        for (int cc = 0; cc < 32; cc += 16) {
-            float qk[16], du[16];
-            const int j0 = half * 32 + cc;
-            umma::tmem_ld16(umma::tmem_at(tQK, j0), qk);
-            umma::tmem_ld16(umma::tmem_at(tDOU, j0), du);
-            if (lane < 16) {
+    float* colp = Rm;                  // [4 row windows][64] column sums of R
+    if (ok) {   // 32 columns per warp, all lanes; R row / column sums by shuffles
+        float qk[16], du[16];
+        umma::tmem_ld_m64<4>(umma::tmem_at(tQK, half * 32), qk);
+        umma::tmem_ld_m64<4>(umma::tmem_at(tDOU, half * 32), du);
+        const int rl = umma::frag_row_lo(), cf = umma::frag_col();
+        float rs[2] = {0.f, 0.f}, cs[4][2];
 #pragma unroll
-                for (int u = 0; u < 16; u += 4) {
-                    float dp[4];
+        for (int k = 0; k < 4; k++) {
+            const int j = half * 32 + 8 * k + cf;
+            cs[k][0] = cs[k][1] = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        const int j = j0 + u + q;
-                        const float gm = (j <= i) ? expf(gam[i] - gam[j]) : 0.f;
-                        dp[q] = du[u + q] * gm;
-                        const float R = dp[q] * qk[u + q];
-                        rsum += R;
-                        Rm[i * 65 + j] = R;
-                        dPC[umma::kidx(j, i, 64)] = umma::tf32r(dp[q]);
-                    }
-                    *reinterpret_cast<float4*>(dPR + umma::kidx(i, j0 + u, 64)) =
-                        umma::tf32r(make_float4(dp[0], dp[1], dp[2], dp[3]));
+            for (int hr = 0; hr < 2; hr++) {
+                const int r = rl + 8 * hr;
+                float d[2];
+#pragma unroll
+                for (int e = 0; e < 2; e++) {
+                    const float gm = j + e <= r ? expf(gam[r] - gam[j + e]) : 0.f;
+                    const float x = du[4 * k + 2 * hr + e] * gm;
+                    const float R = x * qk[4 * k + 2 * hr + e];
+                    rs[hr] += R;
+                    cs[k][e] += R;
+                    d[e] = umma::tf32r(x);
+                    dPC[umma::kidx(j + e, r, 64)] = d[e];
                 }
+                *reinterpret_cast<float2*>(dPR + umma::kidx(r, j, 64)) = make_float2(d[0], d[1]);
             }
         }
-        if (lane < 16) rpart[half * 64 + i] = rsum;
+        rs[0] = umma::row_quad_sum(rs[0]);
+        rs[1] = umma::row_quad_sum(rs[1]);
+        if ((lane & 3) == 0) {
+            rpart[half * 64 + rl] = rs[0];
+            rpart[half * 64 + rl + 8] = rs[1];
+        }
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+                const float c = umma::col_oct_sum(cs[k][e]);
+                if (lane < 4) colp[win * 64 + half * 32 + 8 * k + 2 * lane + e] = c;
+            }
     }
     umma::fence_before_sync();
     __syncthreads();
@@ -614,8 +626,7 @@ bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv
         umma::commit(mbar);
     }
     if (tid < 64) {   // dgam from R: row sums minus column sums (fixed order)
-        float cs = 0.f;
-        for (int r = 0; r < 64; r++) cs += Rm[r * 65 + tid];
+        const float cs = (colp[tid] + colp[64 + tid]) + (colp[128 + tid] + colp[192 + tid]);
         dgl[tid] = (rpart[tid] + rpart[64 + tid]) - cs;
         if (tid < L) w.dgam[(int64_t)(ci.start + tid) * hv + h] += dgl[tid];
     }
@@ -741,7 +752,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         umma::zero_tail_rows(dUs, 64, 0, L);
         __syncthreads();
     }
-    umma::tf32r_inplace(Ks, 4 * 64 * 128);   // K, V, dW, dU (T^T arrives rounded)
+    umma::tf32r_inplace(Ks, 2 * 64 * 128);   // K, V (dW, dU and T^T arrive rounded)
     __syncthreads();
     umma::transpose_sw_to_kmajor(BW, dWs, nullptr);   // [dW^T ; dU^T]: rows b, k = token
     umma::transpose_sw_to_kmajor(BW + 128 * 64, dUs, nullptr);
@@ -768,60 +779,59 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         umma::bulk_load(TR, Tg, 64 * 64 * 4, mbl);
     }
     const int win = warp & 3, half = warp >> 2;
-    const int r = win * 16 + lane;     // D row (lanes 0..15)
-    const bool live = lane < 16;
+    const int rl = umma::frag_row_lo(), cf = umma::frag_col();   // fragment rows rl, rl + 8
     if (ok) {
-        // Gam (.) KK and dT from the 64-column products
-        for (int cc = 0; cc < 32; cc += 16) {
+        {   // Gam (.) KK and dT from the 64-column products, 32 columns per warp
             float kk[16], t1[16], t2[16];
-            const int j0 = half * 32 + cc;
-            umma::tmem_ld16(umma::tmem_at(tKK, j0), kk);
-            umma::tmem_ld16(umma::tmem_at(tDT1, j0), t1);
-            umma::tmem_ld16(umma::tmem_at(tDT2, j0), t2);
-            if (live) {
+            umma::tmem_ld_m64<4>(umma::tmem_at(tKK, half * 32), kk);
+            umma::tmem_ld_m64<4>(umma::tmem_at(tDT1, half * 32), t1);
+            umma::tmem_ld_m64<4>(umma::tmem_at(tDT2, half * 32), t2);
 #pragma unroll
-                for (int u = 0; u < 16; u += 4) {
-                    float d[4], g[4];
+            for (int hr = 0; hr < 2; hr++) {
+                const int r = rl + 8 * hr;
+                const float gr = gam[r];
 #pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        const int j = j0 + u + q;
-                        g[q] = (j < r) ? expf(gam[r] - gam[j]) * kk[u + q] : 0.f;
-                        d[q] = t1[u + q] * be[j] + t2[u + q] * bet[j];
-                    }
-                    *reinterpret_cast<float4*>(GKK + umma::kidx(r, j0 + u, 64)) =
-                        make_float4(g[0], g[1], g[2], g[3]);
-                    *reinterpret_cast<float4*>(DTR + umma::kidx(r, j0 + u, 64)) =
-                        umma::tf32r(make_float4(d[0], d[1], d[2], d[3]));
+                for (int k = 0; k < 4; k++) {
+                    const int j = half * 32 + 8 * k + cf, q = 4 * k + 2 * hr;
+                    const float g0 = j < r ? expf(gr - gam[j]) * kk[q] : 0.f;
+                    const float g1 = j + 1 < r ? expf(gr - gam[j + 1]) * kk[q + 1] : 0.f;
+                    const float d0 = t1[q] * be[j] + t2[q] * bet[j];
+                    const float d1 = t1[q + 1] * be[j + 1] + t2[q + 1] * bet[j + 1];
+                    *reinterpret_cast<float2*>(GKK + umma::kidx(r, j, 64)) = make_float2(g0, g1);
+                    *reinterpret_cast<float2*>(DTR + umma::kidx(r, j, 64)) =
+                        make_float2(umma::tf32r(d0), umma::tf32r(d1));
                 }
             }
         }
-        // T^T dW (half 0) and T^T dU (half 1): dV, dbeta / dgam dot products
-        float rsum = 0.f;
-        for (int cc = 0; cc < 128; cc += 16) {
-            float v[16];
-            umma::tmem_ld16(umma::tmem_at(tTW, half * 128 + cc), v);
-            if (live && r < L) {
-                if (half == 0) {
+        {   // T^T dW (half 0) and T^T dU (half 1): dV, dbeta / dgam dot products
+            float rs[2] = {0.f, 0.f};
+            float* dvb = dqkv + (int64_t)2 * hk * kD + h * kD;
 #pragma unroll
-                    for (int u = 0; u < 16; u += 4) {
-                        const float4 k4 =
-                            *reinterpret_cast<const float4*>(Ks + umma::swz(r, cc + u, 64));
-                        rsum += v[u] * k4.x + v[u + 1] * k4.y + v[u + 2] * k4.z + v[u + 3] * k4.w;
-                    }
-                } else {
-                    float* dv = dqkv + row(r) * C + (int64_t)2 * hk * kD + h * kD + cc;
+            for (int c0 = 0; c0 < 128; c0 += 64) {
+                float v[32];
+                umma::tmem_ld64_m64(umma::tmem_at(tTW, half * 128 + c0), v);
+                const float* X = half == 0 ? Ks : Vs;
 #pragma unroll
-                    for (int u = 0; u < 16; u += 4) {
-                        const float4 v4 =
-                            *reinterpret_cast<const float4*>(Vs + umma::swz(r, cc + u, 64));
-                        rsum += v[u] * v4.x + v[u + 1] * v4.y + v[u + 2] * v4.z + v[u + 3] * v4.w;
-                        st4(dv + u, make_float4(bet[r] * v[u], bet[r] * v[u + 1],
-                                                bet[r] * v[u + 2], bet[r] * v[u + 3]));
+                for (int hr = 0; hr < 2; hr++) {
+                    const int r = rl + 8 * hr;
+#pragma unroll
+                    for (int k = 0; k < 8; k++) {
+                        const int c = c0 + 8 * k + cf, q = 4 * k + 2 * hr;
+                        const float2 x2 = *reinterpret_cast<const float2*>(X + umma::swz(r, c, 64));
+                        rs[hr] += v[q] * x2.x + v[q + 1] * x2.y;
+                        if (half == 1 && r < L)
+                            *reinterpret_cast<float2*>(dvb + row(r) * C + c) =
+                                make_float2(bet[r] * v[q], bet[r] * v[q + 1]);
                     }
                 }
             }
+            rs[0] = umma::row_quad_sum(rs[0]);
+            rs[1] = umma::row_quad_sum(rs[1]);
+            if ((lane & 3) == 0) {
+                rp[half * 64 + rl] = rl < L ? rs[0] : 0.f;
+                rp[half * 64 + rl + 8] = rl + 8 < L ? rs[1] : 0.f;
+            }
         }
-        if (live) rp[half * 64 + r] = rsum;
     }
     __syncthreads();
     if (tid < 64) {
@@ -841,17 +851,17 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
     umma::fence_after_sync();
-    if (ok) {
-        for (int cc = 0; cc < 32; cc += 16) {
-            float v[16];
-            const int i0 = half * 32 + cc;
-            umma::tmem_ld16(umma::tmem_at(tX, i0), v);
-            if (live)
+    if (ok) {   // Y^T, 32 columns per warp, all lanes
+        float v[16];
+        umma::tmem_ld_m64<4>(umma::tmem_at(tX, half * 32), v);
 #pragma unroll
-                for (int u = 0; u < 16; u += 4)
-                    *reinterpret_cast<float4*>(YT + umma::kidx(r, i0 + u, 64)) =
-                        umma::tf32r(make_float4(v[u], v[u + 1], v[u + 2], v[u + 3]));
-        }
+        for (int hr = 0; hr < 2; hr++)
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const int c = half * 32 + 8 * k + cf, q = 4 * k + 2 * hr;
+                *reinterpret_cast<float2*>(YT + umma::kidx(rl + 8 * hr, c, 64)) =
+                    make_float2(umma::tf32r(v[q]), umma::tf32r(v[q + 1]));
+            }
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
@@ -863,32 +873,46 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
-    if (ok) {
-        float rsum = 0.f;
-        for (int cc = 0; cc < 32; cc += 16) {
-            float v[16];
-            const int m0 = half * 32 + cc;
-            umma::tmem_ld16(umma::tmem_at(tKK, m0), v);
-            if (live) {
+    float* colp = Rm;                  // [4 row windows][64] column sums of beta_r x
+    if (ok) {   // dA = -(T^T Y) strictly lower; 32 columns per warp, all lanes
+        float v[16];
+        umma::tmem_ld_m64<4>(umma::tmem_at(tKK, half * 32), v);
+        float rs[2] = {0.f, 0.f}, cs[4][2];
 #pragma unroll
-                for (int u = 0; u < 16; u += 4) {
-                    float dk[4];
+        for (int k = 0; k < 4; k++) {
+            const int m = half * 32 + 8 * k + cf;
+            cs[k][0] = cs[k][1] = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        const int m = m0 + u + q;
-                        const float dA = (m < r) ? -v[u + q] : 0.f;
-                        const float x = dA * GKK[umma::kidx(r, m, 64)];
-                        rsum += x;
-                        Rm[r * 65 + m] = bet[r] * x;
-                        dk[q] = (m < r) ? dA * bet[r] * expf(gam[r] - gam[m]) : 0.f;
-                        dKC[umma::kidx(m, r, 64)] = umma::tf32r(dk[q]);
-                    }
-                    *reinterpret_cast<float4*>(dKR + umma::kidx(r, m0 + u, 64)) =
-                        umma::tf32r(make_float4(dk[0], dk[1], dk[2], dk[3]));
+            for (int hr = 0; hr < 2; hr++) {
+                const int r = rl + 8 * hr;
+                const float br = bet[r], gr = gam[r];
+                const float2 gk = *reinterpret_cast<const float2*>(GKK + umma::kidx(r, m, 64));
+                float dk[2];
+#pragma unroll
+                for (int e = 0; e < 2; e++) {
+                    const float dA = m + e < r ? -v[4 * k + 2 * hr + e] : 0.f;
+                    const float x = dA * (e == 0 ? gk.x : gk.y);
+                    rs[hr] += x;
+                    cs[k][e] += br * x;
+                    dk[e] = umma::tf32r(m + e < r ? dA * br * expf(gr - gam[m + e]) : 0.f);
+                    dKC[umma::kidx(m + e, r, 64)] = dk[e];
                 }
+                *reinterpret_cast<float2*>(dKR + umma::kidx(r, m, 64)) = make_float2(dk[0], dk[1]);
             }
         }
-        if (live) rp[half * 64 + r] = rsum;
+        rs[0] = umma::row_quad_sum(rs[0]);
+        rs[1] = umma::row_quad_sum(rs[1]);
+        if ((lane & 3) == 0) {
+            rp[half * 64 + rl] = rs[0];
+            rp[half * 64 + rl + 8] = rs[1];
+        }
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+                const float c = umma::col_oct_sum(cs[k][e]);
+                if (lane < 4) colp[win * 64 + half * 32 + 8 * k + 2 * lane + e] = c;
+            }
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
@@ -900,8 +924,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         umma::commit(mbar);
     }
     if (tid < 64) {
-        float cs = 0.f;
-        for (int j = 0; j < 64; j++) cs += Rm[j * 65 + tid];
+        const float cs = (colp[tid] + colp[64 + tid]) + (colp[128 + tid] + colp[192 + tid]);
         const float rsA = rp[tid] + rp[64 + tid];
         dbs[tid] += rsA;
         dgs[tid] += bet[tid] * rsA - cs;

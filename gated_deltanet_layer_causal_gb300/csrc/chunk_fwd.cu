@@ -102,7 +102,7 @@ prep_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     const ChunkInfo ci = sv.chunks[blockIdx.x];
     if (ci.len == 0) return;
     const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
-    const int warp = tid >> 5, lane = tid & 31;
+    const int warp = tid >> 5;
     if (tid == 0) {
         umma::mbar_init(mbar, 1);
         umma::mbar_init(mbl, 1);
@@ -153,19 +153,22 @@ prep_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
-    const int win = warp & 3, half = warp >> 2;
-    const int i = win * 16 + lane;
-    if (ok) {
-        for (int cc = 0; cc < 32; cc += 16) {
-            float v[16];
-            const int j0 = half * 32 + cc;
-            umma::tmem_ld16(umma::tmem_at(tD1, j0), v);
-            if (lane < 16)
+    const int half = warp >> 2;
+    if (ok) {   // A = beta_i e^{gam_i - gam_j} D1 (j < i); 32 columns per warp, all lanes
+        float v[16];
+        umma::tmem_ld_m64<4>(umma::tmem_at(tD1, half * 32), v);
+        const int rl = umma::frag_row_lo(), cf = umma::frag_col();
 #pragma unroll
-                for (int u = 0; u < 16; u++) {
-                    const int j = j0 + u;
-                    As[i * kLdA + j] = (j < i) ? bet[i] * expf(gam[i] - gam[j]) * v[u] : 0.f;
-                }
+        for (int hr = 0; hr < 2; hr++) {
+            const int r = rl + 8 * hr;
+            const float br = bet[r], gr = gam[r];
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const int j = half * 32 + 8 * k + cf;
+                *reinterpret_cast<float2*>(As + r * kLdA + j) = make_float2(
+                    j < r ? br * expf(gr - gam[j]) * v[4 * k + 2 * hr] : 0.f,
+                    j + 1 < r ? br * expf(gr - gam[j + 1]) * v[4 * k + 2 * hr + 1] : 0.f);
+            }
         }
     }
     __syncthreads();
@@ -206,6 +209,9 @@ prep_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
 #pragma unroll
         for (int c0 = 0; c0 < 128; c0 += 64) {
             umma::tmem_ld64_m64(umma::tmem_at(tD2, half * 128 + c0), v);
+            if (half == 0)   // W is only ever a tensor-core operand: stored rounded
+#pragma unroll
+                for (int k = 0; k < 32; k++) v[k] = umma::tf32r(v[k]);
             umma::frag_to_sw(Sw, v, c0, 1.f, 1.f);
         }
     } else if (tid == 0) {
@@ -304,8 +310,8 @@ state_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const float* S_i
         // the two K-major tile layouts its consumers feed to the tensor cores
         const int64_t obase = ((int64_t)ci * hv + h) * kD * kD;
         tile_each2<kD, kSlice, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
-            sv.S0[obase + umma::kidx(a0 + a, b, kD)] = v0;
-            sv.S0[obase + umma::kidx(a0 + a + 1, b, kD)] = v1;
+            sv.S0[obase + umma::kidx(a0 + a, b, kD)] = umma::tf32r(v0);   // MMA operand only
+            sv.S0[obase + umma::kidx(a0 + a + 1, b, kD)] = umma::tf32r(v1);
             *reinterpret_cast<float2*>(sv.S0b + obase + umma::kidx(b, a0 + a, kD)) =
                 make_float2(v0, v1);
         });
@@ -319,7 +325,8 @@ state_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const float* S_i
         tile_each<64, kSlice, 8>(uacc, [&](int i, int a, float& v) {
             const float u = i < L ? cur.U[i * kLdS + a] - v : 0.f;
             cur.U[i * kLdS + a] = u;
-            if (i < L) sv.U[((int64_t)(info.start + i) * hv + h) * kD + a0 + a] = u;
+            // stored rounded: later kernels use U only as a tensor-core operand
+            if (i < L) sv.U[((int64_t)(info.start + i) * hv + h) * kD + a0 + a] = umma::tf32r(u);
         });
         __syncthreads();
         // S^T = e^{gam_L} S^T + (diag(fk) K)^T U
@@ -394,7 +401,7 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO* 
         umma::zero_tail_rows(Us, 64, 0, L);
         __syncthreads();
     }
-    umma::tf32r_inplace(Qs, 64 * 128 * 2 + 128 * 128);   // Q, K, S0
+    umma::tf32r_inplace(Qs, 64 * 128 * 2);   // Q, K (S0 and U arrive rounded)
     umma::transpose_sw_to_kmajor(UT, Us, nullptr);
     __syncthreads();
     // U is transposed: its space takes the z rows for the norm epilogue
@@ -423,22 +430,21 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO* 
     umma::fence_after_sync();
     const int win = warp & 3, half = warp >> 2;
     const int i = win * 16 + lane;     // row held by lanes 0..15 (M = 64 layout)
-    if (ok) {   // P = D1 (.) Gam (.) M  -> K-major rows i
-        for (int cc = 0; cc < 32; cc += 16) {
-            float v[16];
-            const int j0 = half * 32 + cc;
-            umma::tmem_ld16(umma::tmem_at(tD1, j0), v);
-            if (lane < 16) {
+    if (ok) {   // P = D1 (.) Gam (.) M  -> K-major rows i; 32 columns per warp, all lanes
+        float v[16];
+        umma::tmem_ld_m64<4>(umma::tmem_at(tD1, half * 32), v);
+        const int rl = umma::frag_row_lo(), cf = umma::frag_col();
 #pragma unroll
-                for (int u = 0; u < 16; u += 4) {
-                    float4 p;
-                    const int j = j0 + u;
-                    p.x = (j + 0 <= i) ? v[u + 0] * expf(gam[i] - gam[j + 0]) : 0.f;
-                    p.y = (j + 1 <= i) ? v[u + 1] * expf(gam[i] - gam[j + 1]) : 0.f;
-                    p.z = (j + 2 <= i) ? v[u + 2] * expf(gam[i] - gam[j + 2]) : 0.f;
-                    p.w = (j + 3 <= i) ? v[u + 3] * expf(gam[i] - gam[j + 3]) : 0.f;
-                    *reinterpret_cast<float4*>(Ps + umma::kidx(i, j, 64)) = umma::tf32r(p);
-                }
+        for (int hr = 0; hr < 2; hr++) {
+            const int r = rl + 8 * hr;
+            const float gr = gam[r];
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const int j = half * 32 + 8 * k + cf;
+                const float p0 = j <= r ? v[4 * k + 2 * hr] * expf(gr - gam[j]) : 0.f;
+                const float p1 = j + 1 <= r ? v[4 * k + 2 * hr + 1] * expf(gr - gam[j + 1]) : 0.f;
+                *reinterpret_cast<float2*>(Ps + umma::kidx(r, j, 64)) =
+                    make_float2(umma::tf32r(p0), umma::tf32r(p1));
             }
         }
     }

@@ -285,16 +285,20 @@ __device__ __forceinline__ void transpose_sw_to_kmajor(float* dst, const float* 
 // v[4k + j] = D[row0 + t/4 + 8 (j/2)][col0 + 8k + 2 (t%4) + j%2], where row0 =
 // 16 * (warp % 4).  All 32 lanes carry data (the 32x32b shape leaves half of
 // them empty for M = 64).
-__device__ __forceinline__ void tmem_ld64_m64(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
+template <int NB>
+__device__ __forceinline__ void tmem_ld_m64(uint32_t taddr, float (&v)[4 * NB]) {
+    uint32_t r[4 * NB];
 #pragma unroll
-    for (int k = 0; k < 8; k++)
+    for (int k = 0; k < NB; k++)
         asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];\n"
                      : "=r"(r[4 * k]), "=r"(r[4 * k + 1]), "=r"(r[4 * k + 2]), "=r"(r[4 * k + 3])
                      : "r"(taddr + 8 * k));
     asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 4 * NB; i++) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld64_m64(uint32_t taddr, float (&v)[32]) {
+    tmem_ld_m64<8>(taddr, v);
 }
 
 // Write this thread's part of an M = 64 fragment (tmem_ld64_m64) into columns
@@ -312,9 +316,22 @@ __device__ __forceinline__ void frag_to_sw(float* tile, const float (&v)[32], in
             make_float2(v[4 * k + 2] * s_hi, v[4 * k + 3] * s_hi);
     }
 }
-// Rows of this thread in an M = 64 fragment.
+// Rows of this thread in an M = 64 fragment (the other one is 8 further), and
+// the first of its two columns in each 8-column block.
 __device__ __forceinline__ int frag_row_lo() {
     return 16 * ((threadIdx.x >> 5) & 3) + ((threadIdx.x & 31) >> 2);
+}
+__device__ __forceinline__ int frag_col() { return 2 * (threadIdx.x & 3); }
+// Sum over the four lanes that share a fragment row.
+__device__ __forceinline__ float row_quad_sum(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+// Sum over the eight lanes that share fragment columns (rows r .. r + 7).
+__device__ __forceinline__ float col_oct_sum(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 8);
+    return x + __shfl_xor_sync(0xffffffffu, x, 16);
 }
 
 // Store a 64-row swizzled tile to 64 rows of a 3-D row tensor through its
