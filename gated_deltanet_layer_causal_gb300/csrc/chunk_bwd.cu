@@ -23,7 +23,7 @@
 
 namespace gdn {
 
-constexpr int kL4 = 132, kL8 = 136;
+constexpr int kL4 = 132;
 
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
@@ -197,63 +197,72 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO
 // grid (d_v / 64, Hv, N), 256 threads, one CTA per SM.  Carries a 64-row slice
 // of dS (as dS^T[b][a] in the accumulators) from the last chunk of the
 // sequence to the first; stores dS at every chunk end and completes dU.  The
-// previous chunk's tiles are fetched with cp.async as soon as their buffers
-// are free: dO / dU_local / gates into the other half of a double buffer at
-// the top of the iteration, K after its product, Q and W after theirs.
-constexpr int kSl = 64, kLdS = kSl + 8;
-constexpr size_t kB2Smem =
-    sizeof(float) * (64 * kL4 + 2 * 64 * kL8 + 4 * 64 * kLdS + kD * kLdS + 2 * 64 + 2 * 64);
+// previous chunk's tiles come through the TMA as soon as their buffers are
+// free: the dO / dU_local slices into the other half of a double buffer at the
+// top of the iteration, K after its product, Q and W after theirs.  The
+// rounded copy of the dS slice that feeds the tensor cores, dSt, and the
+// rounded -dU operand are K-major tiles read without conversion.
+constexpr int kSl = 64;
+constexpr size_t kB2Smem = sizeof(float) * (3 * 64 * 128 + 4 * 64 * kSl + kSl * kD + kSl * 64 +
+                                            2 * 64 + 64) +
+                           4 * 8 + 1024;
 
 __global__ void __launch_bounds__(256, 1)
-bwd_state_kernel(const float* __restrict__ qkv, int hk, int hv, const float* dS_final,
+bwd_state_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const float* dS_final,
                  float* dS_init, FwdSaved sv, BwdScratch w) {
-    extern __shared__ float sm[];
-    float* Kb = sm;                    // [64][kL4]  K
-    float* Qb = Kb + 64 * kL4;         // [64][kL8]  Q
-    float* Wb = Qb + 64 * kL8;         // [64][kL8]  W
-    float* dOs = Wb + 64 * kL8;        // [2][64][kLdS]
-    float* dUs = dOs + 2 * 64 * kLdS;  // [2][64][kLdS]
-    float* dSt = dUs + 2 * 64 * kLdS;  // [128][kLdS]
-    float* gam = dSt + kD * kLdS;      // [2][64]
-    float* fk = gam + 2 * 64;
-    float* eg = fk + 64;
+    extern __shared__ float sm_raw[];
+    float* sm = umma::align1024(sm_raw);
+    float* Kb = sm;                    // [64][128] swizzled K
+    float* Qb = Kb + 64 * 128;         // [64][128] swizzled Q
+    float* Wb = Qb + 64 * 128;         // [64][128] swizzled W (arrives rounded)
+    float* dOs = Wb + 64 * 128;        // [2][64][kSl] swizzled dO slices (arrive rounded)
+    float* dUs = dOs + 2 * 64 * kSl;   // [2][64][kSl] swizzled dU_local slices
+    float* dSt = dUs + 2 * 64 * kSl;   // [64 (a)][128 (b)] K-major, rounded
+    float* Ub = dSt + kSl * kD;        // [64 (a)][64 (i)] K-major: -dU, rounded
+    float* gam = Ub + kSl * 64;        // [2][64]
+    float* eg = gam + 2 * 64;
+    uint64_t* mb = reinterpret_cast<uint64_t*>(eg + 64);   // K, Q/W, slices [2]
     const int sl = blockIdx.x, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
     const int a0 = sl * kSl, kh = h / (hv / hk);
-    const int C = (2 * hk + hv) * kD;
     const int64_t sbase = ((int64_t)n * hv + h) * kD * kD;
     auto row = [&](const ChunkInfo& c, int r) { return (int64_t)c.start + min(r, c.len - 1); };
+    if (tid == 0)
+        for (int i = 0; i < 4; i++) umma::mbar_init(&mb[i], 1);
     auto issue_small = [&](const ChunkInfo& c, int slot) {
-        for (int idx = tid; idx < 64 * kSl / 4; idx += 256) {
-            const int r = idx / (kSl / 4), c4 = (idx % (kSl / 4)) * 4;
-            const int64_t off = (row(c, r) * hv + h) * kD + a0 + c4;
-            cp_async16(dOs + (slot * 64 + r) * kLdS + c4, w.dO + off, r < c.len);
-            cp_async16(dUs + (slot * 64 + r) * kLdS + c4, w.dU + off, r < c.len);
+        if (tid == 0) {
+            float* o = dOs + slot * 64 * kSl;
+            float* u = dUs + slot * 64 * kSl;
+            umma::mbar_expect_tx(&mb[2 + slot], 2 * 64 * kSl * 4);
+            umma::tma_box(o, &maps.dO, a0, h, c.start, &mb[2 + slot]);
+            umma::tma_box(o + 64 * 32, &maps.dO, a0 + 32, h, c.start, &mb[2 + slot]);
+            umma::tma_box(u, &maps.dU, a0, h, c.start, &mb[2 + slot]);
+            umma::tma_box(u + 64 * 32, &maps.dU, a0 + 32, h, c.start, &mb[2 + slot]);
         }
         if (tid < 64)
             cp_async4(gam + slot * 64 + tid, sv.gam + (int64_t)h * sv.T + row(c, tid), true);
         cp_async_commit();
     };
     auto issue_k = [&](const ChunkInfo& c) {
-        for (int idx = tid; idx < 64 * 32; idx += 256) {
-            const int r = idx >> 5, c4 = (idx & 31) * 4;
-            cp_async16(Kb + r * kL4 + c4, qkv + row(c, r) * C + (int64_t)hk * kD + kh * kD + c4,
-                       r < c.len);
+        if (tid == 0) {
+            umma::mbar_expect_tx(&mb[0], 64 * 128 * 4);
+            umma::tma_rows(Kb, 64, &maps.k, kh, c.start, &mb[0]);
         }
-        cp_async_commit();
     };
     auto issue_qw = [&](const ChunkInfo& c) {
-        for (int idx = tid; idx < 64 * 32; idx += 256) {
-            const int r = idx >> 5, c4 = (idx & 31) * 4;
-            cp_async16(Qb + r * kL8 + c4, qkv + row(c, r) * C + kh * kD + c4, r < c.len);
-            cp_async16(Wb + r * kL8 + c4, sv.W + (row(c, r) * hv + h) * kD + c4, r < c.len);
+        if (tid == 0) {
+            umma::mbar_expect_tx(&mb[1], 2 * 64 * 128 * 4);
+            umma::tma_rows(Qb, 64, &maps.q, kh, c.start, &mb[1]);
+            umma::tma_rows(Wb, 64, &maps.W, h, c.start, &mb[1]);
         }
-        cp_async_commit();
     };
     typename Tile<kD, kSl, 8>::Acc sacc;
-    tile_each<kD, kSl, 8>(sacc, [&](int b, int a, float& v) {
-        v = dS_final ? dS_final[sbase + (int64_t)(a0 + a) * kD + b] : 0.f;
-        dSt[b * kLdS + a] = v;
+    tile_each2<kD, kSl, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
+        v0 = dS_final ? dS_final[sbase + (int64_t)(a0 + a) * kD + b] : 0.f;
+        v1 = dS_final ? dS_final[sbase + (int64_t)(a0 + a + 1) * kD + b] : 0.f;
+        dSt[umma::kidx(a, b, kD)] = umma::tf32r(v0);
+        dSt[umma::kidx(a + 1, b, kD)] = umma::tf32r(v1);
     });
+    __syncthreads();   // barriers initialised
     const int c0 = sv.seq_chunk[n], c1 = sv.seq_chunk[n + 1];
     if (c0 < c1) {
         const ChunkInfo last = sv.chunks[c1 - 1];
@@ -261,17 +270,20 @@ bwd_state_kernel(const float* __restrict__ qkv, int hk, int hv, const float* dS_
         issue_qw(last);
         issue_small(last, 0);
     }
-    for (int ci = c1 - 1; ci >= c0; ci--) {
-        const int slot = (c1 - 1 - ci) & 1;
+    bool ok = true;
+    const int lane = tid & 31, rg = Tile<64, kSl, 8>::m0() + (lane >> 2);   // dU rows rg, rg + 8
+    for (int ci = c1 - 1; ci >= c0 && ok; ci--) {
+        const int it = c1 - 1 - ci, slot = it & 1;
         const ChunkInfo info = sv.chunks[ci];
         const int L = info.len;
         const bool more = ci - 1 >= c0;
         const ChunkInfo prev = more ? sv.chunks[ci - 1] : info;
         cp_async_wait<0>();
-        __syncthreads();                    // everything for chunk ci has landed
+        ok = __syncthreads_and(umma::mbar_wait(&mb[2 + slot], (it >> 1) & 1));
+        if (!ok) break;
         if (more) issue_small(prev, slot ^ 1);
-        float* dOc = dOs + slot * 64 * kLdS;
-        float* dUc = dUs + slot * 64 * kLdS;
+        const float* dOc = dOs + slot * 64 * kSl;
+        const float* dUc = dUs + slot * 64 * kSl;
         const float* gc = gam + slot * 64;
         // gradient of the state at this chunk's end, stored as a K-major tile with
         // rows b (the layout the state-facing kernel feeds to the tensor cores)
@@ -280,35 +292,55 @@ bwd_state_kernel(const float* __restrict__ qkv, int hk, int hv, const float* dS_
             *reinterpret_cast<float2*>(w.dS + obase + umma::kidx(b, a0 + a, kD)) =
                 make_float2(v0, v1);
         });
-        if (tid < 64) {
-            fk[tid] = tid < L ? expf(gc[L - 1] - gc[tid]) : 0.f;
-            eg[tid] = tid < L ? expf(gc[tid]) : 0.f;
-        }
-        __syncthreads();
-        // dU = dU_local + K~ dS^T  (64 x slice)
+        if (tid < 64) eg[tid] = tid < L ? expf(gc[tid]) : 0.f;
+        const float gL = gc[L - 1];
+        const float f0 = rg < L ? expf(gL - gc[rg]) : 0.f;
+        const float f1 = rg + 8 < L ? expf(gL - gc[rg + 8]) : 0.f;
+        ok = __syncthreads_and(umma::mbar_wait(&mb[0], it & 1));   // K; eg visible
+        if (!ok) break;
+        // dU = dU_local + diag(fk) K dS^T  (64 x slice)
         typename Tile<64, kSl, 8>::Acc uacc;
         tile_zero<64, kSl, 8>(uacc);
-        tile_mma<64, kSl, kD, 8>(uacc, [&](int i, int b) { return fk[i] * Kb[i * kL4 + b]; },
-                                 [&](int b, int a) { return dSt[b * kLdS + a]; });
-        __syncthreads();                    // K and dS^T reads done
+        tile_mma_bits<64, kSl, kD, 8>(
+            uacc, [&](int i, int b) { return f2tf32(Kb[umma::swz(i, b, 64)]); },
+            [&](int b, int a) { return __float_as_uint(dSt[umma::kidx(a, b, kD)]); });
+        __syncthreads();                    // K and dSt reads done
         if (more) issue_k(prev);
-        tile_each<64, kSl, 8>(uacc, [&](int i, int a, float& v) {
-            const float u = i < L ? dUc[i * kLdS + a] + v : 0.f;
-            dUc[i * kLdS + a] = u;
-            // stored rounded: later kernels use dU only as a tensor-core operand
-            if (i < L) w.dU[((int64_t)(info.start + i) * hv + h) * kD + a0 + a] = umma::tf32r(u);
+        tile_each2<64, kSl, 8>(uacc, [&](int i, int a, float& v0, float& v1) {
+            float u0 = 0.f, u1 = 0.f;
+            if (i < L) {
+                const float f = i == rg ? f0 : f1;
+                const float2 ul = *reinterpret_cast<const float2*>(dUc + umma::swz(i, a, 64));
+                u0 = ul.x + f * v0;
+                u1 = ul.y + f * v1;
+                // stored rounded: later kernels use dU only as a tensor-core operand
+                *reinterpret_cast<float2*>(w.dU + ((int64_t)(info.start + i) * hv + h) * kD +
+                                           a0 + a) = make_float2(umma::tf32r(u0), umma::tf32r(u1));
+            }
+            Ub[umma::kidx(a, i, 64)] = umma::tf32r(-u0);
+            Ub[umma::kidx(a + 1, i, 64)] = umma::tf32r(-u1);
         });
-        __syncthreads();
+        ok = __syncthreads_and(umma::mbar_wait(&mb[1], it & 1));   // Q, W; Ub complete
+        if (!ok) break;
         // dS^T = e^{gam_L} dS^T + Q~^T dO - W^T dU
-        const float dl = expf(gc[L - 1]);
+        const float dl = expf(gL);
         tile_each<kD, kSl, 8>(sacc, [&](int, int, float& v) { v *= dl; });
-        tile_mma<kD, kSl, 64, 8>(sacc, [&](int b, int i) { return eg[i] * Qb[i * kL8 + b]; },
-                                 [&](int i, int a) { return dOc[i * kLdS + a]; });
-        tile_mma<kD, kSl, 64, 8>(sacc, [&](int b, int i) { return -Wb[i * kL8 + b]; },
-                                 [&](int i, int a) { return dUc[i * kLdS + a]; });
-        __syncthreads();                    // Q, W, dO, dU reads done
+        tile_mma_bits<kD, kSl, 64, 8>(
+            sacc, [&](int b, int i) { return f2tf32(eg[i] * Qb[umma::swz(i, b, 64)]); },
+            [&](int i, int a) { return __float_as_uint(dOc[umma::swz(i, a, 64)]); });
+        tile_mma_bits<kD, kSl, 64, 8>(
+            sacc, [&](int b, int i) { return __float_as_uint(Wb[umma::swz(i, b, 64)]); },
+            [&](int i, int a) { return __float_as_uint(Ub[umma::kidx(a, i, 64)]); });
+        __syncthreads();                    // Q, W, dO, Ub reads done
         if (more) issue_qw(prev);
-        tile_each<kD, kSl, 8>(sacc, [&](int b, int a, float& v) { dSt[b * kLdS + a] = v; });
+        tile_each2<kD, kSl, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
+            dSt[umma::kidx(a, b, kD)] = umma::tf32r(v0);
+            dSt[umma::kidx(a + 1, b, kD)] = umma::tf32r(v1);
+        });
+    }
+    if (!ok) {
+        if (tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
+        return;
     }
     if (dS_init)
         tile_each<kD, kSl, 8>(sacc, [&](int b, int a, float& v) {
@@ -1100,6 +1132,7 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
         if (e == cudaSuccess)
             e = make_rows_map(&maps.v, a.qkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C);
         if (e == cudaSuccess) e = make_rows_map(&maps.U, a.sv.U, a.hv, a.T, vs);
+        if (e == cudaSuccess) e = make_rows_map(&maps.W, a.sv.W, a.hv, a.T, vs);
         if (e == cudaSuccess) e = make_rows_map(&maps.dO, w.dO, a.hv, a.T, vs);
         if (e == cudaSuccess) e = make_rows_map(&maps.dU, w.dU, a.hv, a.T, vs);
         if (e == cudaSuccess) e = make_rows_map(&maps.dW, w.dW, a.hv, a.T, vs);
@@ -1119,7 +1152,7 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
     if (a.N > 0) {
         GDN_PROF("chunk_bwd_state", st);
         bwd_state_kernel<<<dim3(kD / kSl, a.hv, a.N), 256, kB2Smem, st>>>(
-            a.qkv, a.hk, a.hv, a.dS_final, a.dS_init, a.sv, w);
+            maps, a.hk, a.hv, a.dS_final, a.dS_init, a.sv, w);
     }
     if (a.NT > 0) {
         {

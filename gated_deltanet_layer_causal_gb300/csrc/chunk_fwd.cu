@@ -76,7 +76,7 @@ __global__ void plan_kernel(const int32_t* __restrict__ cu, int N, int64_t T, in
 //   D2 = T [diag(beta e^gam) K | diag(beta) V]   (one M=64, N=256, K=64 MMA)
 // giving W = D2[:, :128] and U~ = D2[:, 128:].  K and V arrive as swizzled
 // tiles through the TMA; the B operand of D2 is transposed out of them.
-constexpr int kLdK = 132, kLdV = 136, kLdA = 68;
+constexpr int kLdK = 132, kLdA = 68;
 constexpr int kPrepFloats = 2 * 64 * 128 + 256 * 64 + 2 * 64 * kLdA + 64 * 64;
 constexpr size_t kPrepSmem = sizeof(float) * (kPrepFloats + 3 * 64 + 16) + 64 + 1024;
 
@@ -240,102 +240,133 @@ prep_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
 // grid (d_v / kSlice, Hv, N), 256 threads, one CTA per SM.  Rows a of S evolve
 // independently (k, beta, g are shared by all rows), so each CTA carries a
 // 64-row slice of the fp32 state -- kept transposed, S^T[b][a], in the MMA
-// accumulators -- through all chunks of its sequence.  The next chunk's W, K,
-// U~ slice and gates are fetched with cp.async into the other half of a
-// double buffer while the current chunk is computed.
+// accumulators -- through all chunks of its sequence.  The next chunk's W, K
+// and U~ slice arrive through the TMA into the other half of a double buffer
+// while the current chunk is computed.  A tf32-rounded copy of the state
+// slice, St, is held in exactly the layout of its slice of the chunk-start
+// state tile (K-major rows a): it feeds the tensor cores without conversion
+// and leaves as one bulk copy per chunk.
 constexpr int kSlice = 64;
-constexpr int kLdS = kSlice + 8;   // 72: conflict-free as a K-major operand
-struct StateStage {
-    float W[64 * kLdK];
-    float K[64 * kLdV];
-    float U[64 * kLdS];            // U~ slice, overwritten in place by U
-    float gam[64];
+struct StateStage {                // one chunk's operands (a multiple of 1 KB)
+    float W[64 * 128];             // swizzled, arrives rounded
+    float K[64 * 128];             // swizzled
+    float U[64 * kSlice];          // U~ slice: two swizzled 64 x 32 boxes
+    float gam[256];                // 64 used
 };
-constexpr size_t kStateSmem = sizeof(float) * (2 * (64 * kLdK + 64 * kLdV + 64 * kLdS + 64) +
-                                               kD * kLdS + 64);
-
-__device__ __forceinline__ void state_fwd_issue(StateStage& st, const ChunkInfo& info,
-                                                const float* __restrict__ qkv, int hk, int hv,
-                                                int kh, int h, int a0, const FwdSaved& sv) {
-    const int tid = threadIdx.x, L = info.len;
-    const int C = (2 * hk + hv) * kD;
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-        const int r = idx >> 5, c4 = (idx & 31) * 4;
-        const int64_t t = info.start + min(r, L - 1);
-        cp_async16(st.W + r * kLdK + c4, sv.W + (t * hv + h) * kD + c4, r < L);
-        cp_async16(st.K + r * kLdV + c4, qkv + t * C + (int64_t)hk * kD + kh * kD + c4, r < L);
-    }
-    for (int idx = tid; idx < 64 * kSlice / 4; idx += 256) {
-        const int r = idx / (kSlice / 4), c4 = (idx % (kSlice / 4)) * 4;
-        const int64_t t = info.start + min(r, L - 1);
-        cp_async16(st.U + r * kLdS + c4, sv.U + (t * hv + h) * kD + a0 + c4, r < L);
-    }
-    if (tid < 64)   // gate rows start at any token: 4-byte copies
-        cp_async4(st.gam + tid, sv.gam + (int64_t)h * sv.T + info.start + min(tid, L - 1),
-                  tid < L);
-    cp_async_commit();
-}
+constexpr int kStageFloats = (int)(sizeof(StateStage) / sizeof(float));
+static_assert(sizeof(StateStage) % 1024 == 0, "stage alignment");
+constexpr size_t kStateSmem =
+    sizeof(float) * (2 * kStageFloats + kSlice * kD + kSlice * 64) + 2 * 8 + 1024;
 
 __global__ void __launch_bounds__(256, 1)
-state_fwd_kernel(const float* __restrict__ qkv, int hk, int hv, const float* S_init,
+state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const float* S_init,
                  float* S_final, FwdSaved sv) {
-    extern __shared__ float sm[];
+    extern __shared__ float sm_raw[];
+    float* sm = umma::align1024(sm_raw);
     StateStage* stage = reinterpret_cast<StateStage*>(sm);
-    float* St = sm + 2 * (sizeof(StateStage) / sizeof(float));   // [128][kLdS]  S^T slice
-    float* fk = St + kD * kLdS;                                   // [64] exp(gam_L - gam_i)
+    float* St = sm + 2 * kStageFloats;      // [64 (a)][128 (b)] K-major, rounded
+    float* Ub = St + kSlice * kD;           // [64 (a)][64 (i)] K-major: fk_i U[i][a], rounded
+    uint64_t* mb = reinterpret_cast<uint64_t*>(Ub + kSlice * 64);   // [2] stage barriers
     const int sl = blockIdx.x, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
     const int a0 = sl * kSlice, kh = h / (hv / hk);
     using TS = Tile<kD, kSlice, 8>;    // S^T: rows b (d_k), cols a (slice)
     using TU = Tile<64, kSlice, 8>;
     typename TS::Acc sacc;
     const int64_t sbase = ((int64_t)n * hv + h) * kD * kD;
-    tile_each<kD, kSlice, 8>(sacc, [&](int b, int a, float& v) {
-        v = S_init ? S_init[sbase + (int64_t)(a0 + a) * kD + b] : 0.f;
-        St[b * kLdS + a] = v;
+    if (tid == 0) {
+        umma::mbar_init(&mb[0], 1);
+        umma::mbar_init(&mb[1], 1);
+    }
+    tile_each2<kD, kSlice, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
+        v0 = S_init ? S_init[sbase + (int64_t)(a0 + a) * kD + b] : 0.f;
+        v1 = S_init ? S_init[sbase + (int64_t)(a0 + a + 1) * kD + b] : 0.f;
+        St[umma::kidx(a, b, kD)] = umma::tf32r(v0);
+        St[umma::kidx(a + 1, b, kD)] = umma::tf32r(v1);
     });
+    umma::fence_smem_to_async();
+    __syncthreads();   // barriers initialised, St written
     const int c0 = sv.seq_chunk[n], c1 = sv.seq_chunk[n + 1];
-    if (c0 < c1) state_fwd_issue(stage[0], sv.chunks[c0], qkv, hk, hv, kh, h, a0, sv);
-    for (int ci = c0; ci < c1; ci++) {
-        StateStage& cur = stage[(ci - c0) & 1];
+    auto issue = [&](int s, const ChunkInfo& info) {   // tiles: one thread; gates: 64
+        if (tid == 0) {
+            umma::mbar_expect_tx(&mb[s], (2 * 64 * 128 + 64 * kSlice) * 4);
+            umma::tma_rows(stage[s].W, 64, &maps.W, h, info.start, &mb[s]);
+            umma::tma_rows(stage[s].K, 64, &maps.k, kh, info.start, &mb[s]);
+            umma::tma_box(stage[s].U, &maps.U, a0, h, info.start, &mb[s]);
+            umma::tma_box(stage[s].U + 64 * 32, &maps.U, a0 + 32, h, info.start, &mb[s]);
+        }
+        if (tid < 64)   // gate rows start at any token: 4-byte copies
+            cp_async4(stage[s].gam + tid,
+                      sv.gam + (int64_t)h * sv.T + info.start + min(tid, info.len - 1),
+                      tid < info.len);
+        cp_async_commit();
+    };
+    if (c0 < c1) issue(0, sv.chunks[c0]);
+    bool ok = true;
+    const int lane = tid & 31, rg = TU::m0() + (lane >> 2);   // this thread's U rows rg, rg + 8
+    for (int ci = c0; ci < c1 && ok; ci++) {
+        const int s = (ci - c0) & 1;
+        StateStage& cur = stage[s];
         const ChunkInfo info = sv.chunks[ci];
         const int L = info.len;
         if (ci + 1 < c1) {
-            state_fwd_issue(stage[(ci - c0 + 1) & 1], sv.chunks[ci + 1], qkv, hk, hv, kh, h, a0,
-                            sv);
+            issue(s ^ 1, sv.chunks[ci + 1]);
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
         }
-        // state at the chunk start, for the output and the backward, written in
-        // the two K-major tile layouts its consumers feed to the tensor cores
+        // chunk-start state in the layout with rows b (exact), from the accumulators
         const int64_t obase = ((int64_t)ci * hv + h) * kD * kD;
         tile_each2<kD, kSlice, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
-            sv.S0[obase + umma::kidx(a0 + a, b, kD)] = umma::tf32r(v0);   // MMA operand only
-            sv.S0[obase + umma::kidx(a0 + a + 1, b, kD)] = umma::tf32r(v1);
             *reinterpret_cast<float2*>(sv.S0b + obase + umma::kidx(b, a0 + a, kD)) =
                 make_float2(v0, v1);
         });
-        __syncthreads();   // this chunk's tiles have landed (and St is current)
-        if (tid < 64) fk[tid] = tid < L ? expf(cur.gam[L - 1] - cur.gam[tid]) : 0.f;
+        ok = __syncthreads_and(umma::mbar_wait(&mb[s], ((ci - c0) >> 1) & 1));
+        if (!ok) break;
+        if (tid == 0) {   // ... and with rows a (rounded; an MMA operand only): St whole
+            umma::bulk_store(sv.S0 + obase + (int64_t)a0 * kD, St, kSlice * kD * 4);
+            umma::bulk_commit();
+        }
+        const float gL = cur.gam[L - 1];
+        const float f0 = rg < L ? expf(gL - cur.gam[rg]) : 0.f;
+        const float f1 = rg + 8 < L ? expf(gL - cur.gam[rg + 8]) : 0.f;
         // U = U~ - W S^T   (64 x slice)
         typename TU::Acc uacc;
         tile_zero<64, kSlice, 8>(uacc);
-        tile_mma<64, kSlice, kD, 8>(uacc, [&](int i, int b) { return cur.W[i * kLdK + b]; },
-                                    [&](int b, int a) { return St[b * kLdS + a]; });
-        tile_each<64, kSlice, 8>(uacc, [&](int i, int a, float& v) {
-            const float u = i < L ? cur.U[i * kLdS + a] - v : 0.f;
-            cur.U[i * kLdS + a] = u;
-            // stored rounded: later kernels use U only as a tensor-core operand
-            if (i < L) sv.U[((int64_t)(info.start + i) * hv + h) * kD + a0 + a] = umma::tf32r(u);
+        tile_mma_bits<64, kSlice, kD, 8>(
+            uacc, [&](int i, int b) { return __float_as_uint(cur.W[umma::swz(i, b, 64)]); },
+            [&](int b, int a) { return __float_as_uint(St[umma::kidx(a, b, kD)]); });
+        tile_each2<64, kSlice, 8>(uacc, [&](int i, int a, float& v0, float& v1) {
+            float u0 = 0.f, u1 = 0.f;
+            if (i < L) {
+                const float2 ut = *reinterpret_cast<const float2*>(cur.U + umma::swz(i, a, 64));
+                u0 = ut.x - v0;
+                u1 = ut.y - v1;
+                // stored rounded: later kernels use U only as a tensor-core operand
+                *reinterpret_cast<float2*>(sv.U + ((int64_t)(info.start + i) * hv + h) * kD +
+                                           a0 + a) = make_float2(umma::tf32r(u0), umma::tf32r(u1));
+            }
+            const float f = i == rg ? f0 : f1;
+            Ub[umma::kidx(a, i, 64)] = umma::tf32r(f * u0);
+            Ub[umma::kidx(a + 1, i, 64)] = umma::tf32r(f * u1);
         });
-        __syncthreads();
-        // S^T = e^{gam_L} S^T + (diag(fk) K)^T U
-        const float dl = expf(cur.gam[L - 1]);
+        __syncthreads();   // Ub complete
+        // S^T = e^{gam_L} S^T + K^T (diag(fk) U)
+        const float dl = expf(gL);
         tile_each<kD, kSlice, 8>(sacc, [&](int, int, float& v) { v *= dl; });
-        tile_mma<kD, kSlice, 64, 8>(sacc, [&](int b, int i) { return fk[i] * cur.K[i * kLdV + b]; },
-                                    [&](int i, int a) { return cur.U[i * kLdS + a]; });
-        __syncthreads();   // reads of cur, St and fk are done
-        tile_each<kD, kSlice, 8>(sacc, [&](int b, int a, float& v) { St[b * kLdS + a] = v; });
+        tile_mma_bits<kD, kSlice, 64, 8>(
+            sacc, [&](int b, int i) { return f2tf32(cur.K[umma::swz(i, b, 64)]); },
+            [&](int i, int a) { return __float_as_uint(Ub[umma::kidx(a, i, 64)]); });
+        if (tid == 0) umma::bulk_wait_read();   // the chunk-start copy has read St
+        __syncthreads();   // reads of cur, St and Ub are done
+        tile_each2<kD, kSlice, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
+            St[umma::kidx(a, b, kD)] = umma::tf32r(v0);
+            St[umma::kidx(a + 1, b, kD)] = umma::tf32r(v1);
+        });
+        umma::fence_smem_to_async();   // St -> the next chunk's bulk copy
+    }
+    if (!ok) {
+        if (tid == 0) atomicExch(sv.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
+        return;
     }
     if (S_final)
         tile_each<kD, kSlice, 8>(sacc, [&](int b, int a, float& v) {
@@ -548,7 +579,7 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
     if (a.N > 0) {
         GDN_PROF("chunk_state_fwd", st);
         state_fwd_kernel<<<dim3(kD / kSlice, a.hv, a.N), 256, kStateSmem, st>>>(
-            a.qkv, a.hk, a.hv, a.S_init, a.S_final, a.sv);
+            maps, a.hk, a.hv, a.S_init, a.S_final, a.sv);
     }
     if (a.NT > 0) {
         GDN_PROF("chunk_out_fwd", st);

@@ -145,6 +145,34 @@ __device__ __forceinline__ void tile_mma(typename Tile<M, N, NW>::Acc& acc, FA a
     }
 }
 
+// The same with operands given as tf32 bit patterns (already rounded, or
+// converted by the caller), so pre-rounded tiles skip the conversion.
+template <int M, int N, int K, int NW, class FA, class FB>
+__device__ __forceinline__ void tile_mma_bits(typename Tile<M, N, NW>::Acc& acc, FA a, FB b) {
+    using C = Tile<M, N, NW>;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int m0 = C::m0(), n0 = C::n0();
+#pragma unroll 2
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t af[C::MPW][4];
+#pragma unroll
+        for (int i = 0; i < C::MPW; i++) {
+            const int r = m0 + i * 16 + g;
+            af[i][0] = a(r, k0 + t);
+            af[i][1] = a(r + 8, k0 + t);
+            af[i][2] = a(r, k0 + t + 4);
+            af[i][3] = a(r + 8, k0 + t + 4);
+        }
+#pragma unroll
+        for (int j = 0; j < C::NPW; j++) {
+            const int c = n0 + j * 8 + g;
+            uint32_t bf[2] = {b(k0 + t, c), b(k0 + t + 4, c)};
+#pragma unroll
+            for (int i = 0; i < C::MPW; i++) mma_tf32(acc[i][j], af[i], bf);
+        }
+    }
+}
+
 // Visit every accumulator element as f(row, col, value&).
 template <int M, int N, int NW, class F>
 __device__ __forceinline__ void tile_each(typename Tile<M, N, NW>::Acc& acc, F f) {

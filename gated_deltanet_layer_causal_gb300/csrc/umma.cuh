@@ -164,6 +164,25 @@ __device__ __forceinline__ void tma_rows(float* dst, int rows, const CUtensorMap
             : "memory");
 }
 
+// One swizzled 64 x 32 box (columns x .. x + 31 of rows t0 .. t0 + 63 of one
+// head) into dst.  8 KB on `mbar`.
+__device__ __forceinline__ void tma_box(float* dst, const CUtensorMap* map, int x, int head,
+                                        int t0, uint64_t* mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(saddr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(head), "r"(t0), "r"(saddr(mbar))
+        : "memory");
+}
+
+// Contiguous copy shared -> global (both 16-byte aligned, bytes % 16 == 0), in
+// the calling thread's bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst),
+                 "r"(saddr(src)), "r"(bytes)
+                 : "memory");
+}
+
 // Contiguous copy global -> shared (both 16-byte aligned, bytes % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* mbar) {
