@@ -40,10 +40,13 @@ UNIT = "tokens/s"
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="qwen38_flash_64k", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--tokens", type=int, default=0,
+                   help="profiling case: only the first TOKENS tokens of the workload, as one "
+                        "sequence (0 = the whole workload)")
     p.add_argument("--e2e-steps", type=int, default=2)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -166,6 +169,26 @@ class Step:
     INPUTS = ["x", "conv_w", "a", "b", "A_log", "dt_bias", "z", "norm_w", "dy", "cu_seqlens"]
 
 
+# Measured DRAM bytes (read + write) per launch on the 64k-token workload:
+# dram__bytes_read.sum + dram__bytes_write.sum of each kernel from one ncu
+# capture of the first 8192 tokens, times 8 (every kernel's work is
+# proportional to the chunks it processes).  Valid for the kernels as captured;
+# a kernel changed since then reports null.
+TRAFFIC_64K = {
+    "conv_fwd": 3649505280,
+    "chunk_prep": 6570291200,
+    "chunk_state_fwd": 11317725184,
+    "chunk_out_fwd": 8939784192,
+    "chunk_bwd_local": 8007192576,
+    "chunk_bwd_state": 10358249472,
+    "chunk_bwd_sfacing": 17131732992,
+    "chunk_bwd_dp": 7226800128,
+    "chunk_bwd_wy": 10072883200,
+    "gva_sum": 9021515776,
+    "conv_bwd": 5434595328,
+}
+
+
 def kernel_cost(name: str, w: synth.Workload, NT: int):
     """Algorithmic bytes of one launch of a kernel: the tensors its interface
     must read and write, each once.  Notation: io = bytes per activation,
@@ -181,15 +204,15 @@ def kernel_cost(name: str, w: synth.Workload, NT: int):
     table = {
         "conv_fwd": T * C * io + T * C * 4,
         "conv_bwd": 2 * T * C * io + T * C * 4,
-        "chunk_prep": tk + tv + gates + 2 * tv + 2 * g,
+        "chunk_prep": tk + tv + gates + 2 * tv + 2 * g + 2 * Tt,
         "chunk_state_fwd": 2 * tv + tk + g + tv + 2 * S,
         "chunk_out_fwd": 2 * tk + tv + S + g + act + act + tv + g,
         "chunk_bwd_local": 2 * tk + tv + 2 * act + g + tv + act + tv,
-        "chunk_bwd_state": 2 * tk + 3 * tv + g + 2 * tv + S,
-        "chunk_bwd_sfacing": 2 * S + 3 * tv + 2 * tk + g + 4 * tv + g,
-        "chunk_bwd_dp": 2 * tk + 2 * tv + 3 * g + 2 * tv + 2 * tv + 2 * Tt + g,
-        "chunk_bwd_wy": tk + tv + 4 * tv + 2 * Tt + 3 * g + gates + tv + 2 * tv + gates + g,
-        "gva_sum": 2 * tv + 2 * tk,
+        "chunk_bwd_state": 2 * tk + 3 * tv + g + tv + S,
+        "chunk_bwd_sfacing": 2 * S + 3 * tv + 2 * tk + g + 3 * tv + g,
+        "chunk_bwd_dp": 2 * tk + 2 * tv + g + 2 * tv + 2 * g,
+        "chunk_bwd_wy": tk + tv + 2 * tv + 2 * Tt + 3 * g + gates + 2 * tv + gates + g,
+        "gva_sum": 5 * tv + 2 * tk,
     }
     return "hbm", table.get(name), "B"
 
@@ -197,6 +220,8 @@ def kernel_cost(name: str, w: synth.Workload, NT: int):
 def run_ours(args, rank, world, dev):
     w = synth.WORKLOADS[args.workload]
     w = w.replace(seed=w.seed + 1000 * rank)
+    if args.tokens:
+        w = w.replace(name=f"{w.name}[first {args.tokens} tokens]", seq_lens=(args.tokens,))
     inp = synth.make_inputs(w, with_grad=True)
     step = Step(w, inp, dev)
     NT = sum((L + 63) // 64 for L in w.seq_lens)
@@ -244,7 +269,10 @@ def run_ours(args, rank, world, dev):
     hbm_peak = hbm_peak or 6800.0
     achieved = amount / (avg_ms / 1e3) / 1e9 if amount else None
     roof = {"kernel": name, "bound": bound, "achieved": achieved, "peak": hbm_peak,
-            "unit": "GB/s", "frac": achieved / hbm_peak if achieved else None, "traffic": None,
+            "unit": "GB/s", "frac": achieved / hbm_peak if achieved else None,
+            "traffic": (TRAFFIC_64K.get(name) if args.workload == "qwen38_flash_64k"
+                        and not args.tokens else None),
+            "traffic_unit": "B per launch",
             "peak_source": peak_src, "avg_launch_ms": avg_ms,
             "step_share": tot_ms / sum(v[1] for v in prof.values())}
     path_bytes = w.T * (2 * w.C * 2 + 4 * w.h_v * 2 + 2 * w.h_v * D * 2) \
