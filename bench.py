@@ -179,7 +179,6 @@ TRAFFIC_64K = {
     "chunk_prep": 6570291200,
     "chunk_state_fwd": 11317725184,
     "chunk_out_fwd": 8939784192,
-    "chunk_bwd_local": 8007192576,
     "chunk_bwd_state": 10358249472,
     "chunk_bwd_sfacing": 17131732992,
     "chunk_bwd_dp": 7226800128,
@@ -207,7 +206,8 @@ def kernel_cost(name: str, w: synth.Workload, NT: int):
         "chunk_prep": tk + tv + gates + 2 * tv + 2 * g + 2 * Tt,
         "chunk_state_fwd": 2 * tv + tk + g + tv + 2 * S,
         "chunk_out_fwd": 2 * tk + tv + S + g + act + act + tv + g,
-        "chunk_bwd_local": 2 * tk + tv + 2 * act + g + tv + act + tv,
+        "chunk_norm_bwd": tv + 2 * act + tv + act,
+        "chunk_bwd_local": 2 * tk + tv + g + tv,
         "chunk_bwd_state": 2 * tk + 3 * tv + g + tv + S,
         "chunk_bwd_sfacing": 2 * S + 3 * tv + 2 * tk + g + 3 * tv + g,
         "chunk_bwd_dp": 2 * tk + 2 * tv + g + 2 * tv + 2 * g,

@@ -23,7 +23,6 @@
 
 namespace gdn {
 
-constexpr int kL4 = 132;
 
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
@@ -34,101 +33,94 @@ __device__ __forceinline__ void load_gam(float* gam, const FwdSaved& sv, const C
     if (tid < 64) gam[tid] = sv.gam[(int64_t)h * sv.T + ci.start + min(tid, ci.len - 1)];
 }
 
-// ------------------------------------------------------------------ B1: local
-// grid (NT, Hv), 256 threads, tcgen05.  Gated-norm backward (dO, dz, dnorm_w
-// partials) on the CUDA cores, then
-//   D1 = K Q^T (64 x 64)  ->  P^T[j][i] = D1[j][i] e^{gam_i-gam_j} [i >= j]
-//   D2 = P^T dO           ->  dU_local (64 x 128)
-// Shared memory: Q, K K-major 32 KB each, dO rows 34 KB, dO^T (rows a,
-// k = token) 32 KB, P^T 16 KB.  Tensor memory: 192 fp32 columns (256 allocated).
-constexpr int kB1Floats = 64 * 128 * 2 + 64 * kL4 + 128 * 64 + 64 * 64;
-constexpr size_t kB1Smem = sizeof(float) * (kB1Floats + 64 + 16) + 64 + 1024;
-
+// ------------------------------------------------------------------ B0: gated-norm backward
+// rows = T * Hv rows of d_v = 128, one warp per row, 64 rows per CTA (many CTAs
+// per SM: a streaming pass).  dO is stored fp32 and tf32-rounded (it is only
+// ever a tensor-core operand), dz in the I/O dtype, one dnorm_w partial row per
+// CTA.  Without z there is no norm: dO = dy.
+constexpr int kNormRows = 64;
 template <class IO>
-__global__ void __launch_bounds__(256, 1)
-bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO* z,
-                 const float* norm_w, float norm_eps, const IO* __restrict__ dy, IO* dz,
-                 FwdSaved sv, BwdScratch w) {
-    extern __shared__ float sm_raw[];
-    float* sm = umma::align1024(sm_raw);
-    float* Qs = sm;                    // [64][128] swizzled
-    float* Ks = Qs + 64 * 128;         // [64][128] swizzled
-    float* dOr = Ks + 64 * 128;        // [64][kL4] row-major dO
-    float* dOT = dOr + 64 * kL4;       // [128 (a)][64 (i)] K-major
-    float* PT = dOT + 128 * 64;        // [64 (j)][64 (i)] K-major
-    float* gam = PT + 64 * 64;
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(gam + 64 + 16);
-    uint64_t* mbl = mbar + 1;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
+__global__ void __launch_bounds__(256)
+chunk_norm_bwd_kernel(const float* __restrict__ o, const IO* __restrict__ z,
+                      const float* __restrict__ norm_w, float norm_eps, const IO* __restrict__ dy,
+                      int64_t rows, float* __restrict__ dO, IO* __restrict__ dz,
+                      float* __restrict__ part) {
     __shared__ float4 red[8][32];
-    const ChunkInfo ci = sv.chunks[blockIdx.x];
-    if (ci.len == 0) return;
-    const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
-    const int lane = tid & 31, warp = tid >> 5;
-    auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
-    // norm backward, one warp per row; a warp's 8 rows are loaded before any is
-    // used, and ahead of the Q / K tiles
-    float4 wacc = zero4();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float4 w4 = z ? ld4(norm_w + lane * 4) : zero4();
-    float4 o8[8], z8[8], y8[8];
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-        const int r = warp + 8 * k;
-        const int64_t off = (row(r) * hv + h) * kD + lane * 4;
-        y8[k] = ld4(dy + off);
+    float4 acc = zero4();
+    const int64_t r0 = (int64_t)blockIdx.x * kNormRows, r1 = min(r0 + kNormRows, rows);
+    for (int64_t r = r0 + warp; r < r1; r += 8) {
+        const int64_t off = r * kD + lane * 4;
+        const float4 dy4 = ld4(dy + off);
+        float4 d4 = dy4;
         if (z) {
-            o8[k] = ld4(sv.o + off);
-            z8[k] = ld4(z + off);
+            const NormRowGrad gr = norm_row_bwd(ld4(o + off), ld4(z + off), dy4, w4, norm_eps, acc);
+            d4 = gr.d_o;
+            st4(dz + off, gr.dz);
         }
+        st4(dO + off, umma::tf32r(d4));
     }
-    if (tid == 0) {
-        umma::mbar_init(mbar, 1);
-        umma::mbar_init(mbl, 1);
-        umma::mbar_expect_tx(mbl, 2 * 64 * 128 * 4);
-        umma::tma_rows(Qs, 64, &maps.q, kh, ci.start, mbl);
-        umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
-    }
-    load_gam(gam, sv, ci, h);
-    if (warp == 0) umma::tmem_alloc(tslot, 256);
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-        const int r = warp + 8 * k;
-        float4 d4 = zero4();
-        if (r < L) {
-            const int64_t off = ((int64_t)(ci.start + r) * hv + h) * kD + lane * 4;
-            if (z) {
-                NormRowGrad gr = norm_row_bwd(o8[k], z8[k], y8[k], w4, norm_eps, wacc);
-                d4 = gr.d_o;
-                st4(dz + off, gr.dz);
-            } else {
-                d4 = y8[k];
-            }
-            st4(w.dO + off, umma::tf32r(d4));   // only ever a tensor-core operand
-        }
-        st4(dOr + r * kL4 + lane * 4, d4);
-    }
-    if (z) red[warp][lane] = wacc;
-    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
-    if (L < 64) {   // tail rows belong to the next sequence
-        umma::zero_tail_rows(Qs, 64, 0, L);
-        umma::zero_tail_rows(Ks, 64, 0, L);
-        __syncthreads();
-    }
-    umma::tf32r_inplace(Qs, 2 * 64 * 128);
-    if (z && warp == 0) {
+    if (!z) return;
+    red[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0) {
         float4 s = red[0][lane];
         for (int i = 1; i < 8; i++) {
             s.x += red[i][lane].x; s.y += red[i][lane].y;
             s.z += red[i][lane].z; s.w += red[i][lane].w;
         }
-        st4(w.nw_part + ((int64_t)blockIdx.x * hv + h) * kD + lane * 4, s);
+        st4(part + (int64_t)blockIdx.x * kD + lane * 4, s);
     }
-    for (int idx = tid; idx < 128 * 16; idx += 256) {   // dO^T: lane = a, 4 tokens per store
-        const int a = idx & 127, i4 = idx >> 7;
-        *reinterpret_cast<float4*>(dOT + umma::kidx(a, 4 * i4, 64)) = umma::tf32r(
-            make_float4(dOr[(4 * i4 + 0) * kL4 + a], dOr[(4 * i4 + 1) * kL4 + a],
-                        dOr[(4 * i4 + 2) * kL4 + a], dOr[(4 * i4 + 3) * kL4 + a]));
+}
+
+// ------------------------------------------------------------------ B1: local
+// grid (NT, Hv), 256 threads, tcgen05.
+//   D1 = K Q^T (64 x 64)  ->  P^T[j][i] = D1[j][i] e^{gam_i-gam_j} [i >= j]
+//   D2 = P^T dO           ->  dU_local (64 x 128)
+// Shared memory: Q, K, dO swizzled 32 KB each (TMA), dO^T (rows a, k = token)
+// 32 KB, P^T 16 KB.  Tensor memory: 192 fp32 columns (256 allocated).
+constexpr int kB1Floats = 64 * 128 * 3 + 128 * 64 + 64 * 64;
+constexpr size_t kB1Smem = sizeof(float) * (kB1Floats + 64 + 16) + 64 + 1024;
+
+__global__ void __launch_bounds__(256, 1)
+bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv,
+                 BwdScratch w) {
+    extern __shared__ float sm_raw[];
+    float* sm = umma::align1024(sm_raw);
+    float* Qs = sm;                    // [64][128] swizzled
+    float* Ks = Qs + 64 * 128;         // [64][128] swizzled
+    float* dOs = Ks + 64 * 128;        // [64][128] swizzled dO (arrives rounded)
+    float* dOT = dOs + 64 * 128;       // [128 (a)][64 (i)] K-major
+    float* PT = dOT + 128 * 64;        // [64 (j)][64 (i)] K-major
+    float* gam = PT + 64 * 64;
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(gam + 64 + 16);
+    uint64_t* mbl = mbar + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
+    const ChunkInfo ci = sv.chunks[blockIdx.x];
+    if (ci.len == 0) return;
+    const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
+    const int warp = tid >> 5;
+    if (tid == 0) {
+        umma::mbar_init(mbar, 1);
+        umma::mbar_init(mbl, 1);
+        umma::mbar_expect_tx(mbl, 3 * 64 * 128 * 4);
+        umma::tma_rows(Qs, 64, &maps.q, kh, ci.start, mbl);
+        umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
+        umma::tma_rows(dOs, 64, &maps.dO, h, ci.start, mbl);
     }
+    load_gam(gam, sv, ci, h);
+    if (warp == 0) umma::tmem_alloc(tslot, 256);
+    __syncthreads();
+    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
+    if (L < 64) {   // tail rows belong to the next sequence
+        umma::zero_tail_rows(Qs, 64, 0, L);
+        umma::zero_tail_rows(Ks, 64, 0, L);
+        umma::zero_tail_rows(dOs, 64, 0, L);
+        __syncthreads();
+    }
+    umma::tf32r_inplace(Qs, 2 * 64 * 128);
+    umma::transpose_sw_to_kmajor(dOT, dOs, nullptr);   // dO^T: rows a, k = token
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -1111,7 +1103,7 @@ template <class IO>
 static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStream_t st) {
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(bwd_local_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(bwd_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kB1Smem);
         cudaFuncSetAttribute(bwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kB2Smem);
@@ -1144,10 +1136,16 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
         if (e == cudaSuccess)
             e = make_rows_map(&maps.dv, a.dqkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C);
         if (e != cudaSuccess) return e;
+        const int64_t rows = a.T * a.hv;
+        {
+            GDN_PROF("chunk_norm_bwd", st);
+            chunk_norm_bwd_kernel<IO><<<(unsigned)((rows + kNormRows - 1) / kNormRows), 256, 0,
+                                        st>>>(a.sv.o, (const IO*)a.z, a.norm_w, a.norm_eps,
+                                              (const IO*)a.dy, rows, w.dO, (IO*)a.dz,
+                                              w.nw_part);
+        }
         GDN_PROF("chunk_bwd_local", st);
-        bwd_local_kernel<IO><<<dim3(a.NT, a.hv), 256, kB1Smem, st>>>(
-            maps, a.hk, a.hv, (const IO*)a.z, a.norm_w, a.norm_eps, (const IO*)a.dy,
-            (IO*)a.dz, a.sv, w);
+        bwd_local_kernel<<<dim3(a.NT, a.hv), 256, kB1Smem, st>>>(maps, a.hk, a.hv, a.sv, w);
     }
     if (a.N > 0) {
         GDN_PROF("chunk_bwd_state", st);
@@ -1190,8 +1188,8 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
             float* tmp = w.nw_part + (size_t)a.NT * a.hv * kD + (size_t)a.NT * a.hv * 2;
             {
                 GDN_PROF("norm_w_reduce", st);
-                colsum_stage1_kernel<<<kColsumBlocks, kD, 0, st>>>(w.nw_part,
-                                                                   (int64_t)a.NT * a.hv, tmp);
+                colsum_stage1_kernel<<<kColsumBlocks, kD, 0, st>>>(
+                    w.nw_part, (a.T * a.hv + kNormRows - 1) / kNormRows, tmp);
             }
             GDN_PROF("norm_w_reduce2", st);
             colsum_stage2_kernel<<<1, 8 * kD, 0, st>>>(tmp, a.dnorm_w);
