@@ -293,9 +293,16 @@ bwd_state_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         // dU = dU_local + diag(fk) K dS^T  (64 x slice)
         typename Tile<64, kSl, 8>::Acc uacc;
         tile_zero<64, kSl, 8>(uacc);
-        tile_mma_bits<64, kSl, kD, 8>(
-            uacc, [&](int i, int b) { return f2tf32(Kb[umma::swz(i, b, 64)]); },
-            [&](int b, int a) { return __float_as_uint(dSt[umma::kidx(a, b, kD)]); });
+        tile_mma_frag<64, kSl, kD, 8>(
+            uacc,
+            [&](int r0, int k0, uint32_t(&f)[4]) {
+                ldsm_a(f, r0, k0, [&](int r, int c) { return Kb + umma::swz(r, c, 64); });
+#pragma unroll
+                for (int e = 0; e < 4; e++) f[e] = f2tf32(__uint_as_float(f[e]));
+            },
+            [&](int k0, int n0, uint32_t(&f)[4]) {
+                ldsm_b2(f, k0, n0, [&](int n, int k) { return dSt + umma::kidx(n, k, kD); });
+            });
         __syncthreads();                    // K and dSt reads done
         if (more) issue_k(prev);
         tile_each2<64, kSl, 8>(uacc, [&](int i, int a, float& v0, float& v1) {
@@ -320,9 +327,18 @@ bwd_state_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         tile_mma_bits<kD, kSl, 64, 8>(
             sacc, [&](int b, int i) { return f2tf32(eg[i] * Qb[umma::swz(i, b, 64)]); },
             [&](int i, int a) { return __float_as_uint(dOc[umma::swz(i, a, 64)]); });
-        tile_mma_bits<kD, kSl, 64, 8>(
-            sacc, [&](int b, int i) { return __float_as_uint(Wb[umma::swz(i, b, 64)]); },
-            [&](int i, int a) { return __float_as_uint(Ub[umma::kidx(a, i, 64)]); });
+        tile_mma_frag<kD, kSl, 64, 8>(
+            sacc,
+            [&](int r0, int k0, uint32_t(&f)[4]) {   // A(b, i) = W[i][b]: element loads
+                const int g = lane >> 2, t = lane & 3;
+                f[0] = __float_as_uint(Wb[umma::swz(k0 + t, r0 + g, 64)]);
+                f[1] = __float_as_uint(Wb[umma::swz(k0 + t, r0 + g + 8, 64)]);
+                f[2] = __float_as_uint(Wb[umma::swz(k0 + t + 4, r0 + g, 64)]);
+                f[3] = __float_as_uint(Wb[umma::swz(k0 + t + 4, r0 + g + 8, 64)]);
+            },
+            [&](int k0, int n0, uint32_t(&f)[4]) {
+                ldsm_b2(f, k0, n0, [&](int n, int k) { return Ub + umma::kidx(n, k, 64); });
+            });
         __syncthreads();                    // Q, W, dO, Ub reads done
         if (more) issue_qw(prev);
         tile_each2<kD, kSl, 8>(sacc, [&](int b, int a, float& v0, float& v1) {

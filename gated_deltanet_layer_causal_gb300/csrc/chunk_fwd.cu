@@ -332,9 +332,14 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         // U = U~ - W S^T   (64 x slice)
         typename TU::Acc uacc;
         tile_zero<64, kSlice, 8>(uacc);
-        tile_mma_bits<64, kSlice, kD, 8>(
-            uacc, [&](int i, int b) { return __float_as_uint(cur.W[umma::swz(i, b, 64)]); },
-            [&](int b, int a) { return __float_as_uint(St[umma::kidx(a, b, kD)]); });
+        tile_mma_frag<64, kSlice, kD, 8>(
+            uacc,
+            [&](int r0, int k0, uint32_t(&f)[4]) {
+                ldsm_a(f, r0, k0, [&](int r, int c) { return cur.W + umma::swz(r, c, 64); });
+            },
+            [&](int k0, int n0, uint32_t(&f)[4]) {
+                ldsm_b2(f, k0, n0, [&](int n, int k) { return St + umma::kidx(n, k, kD); });
+            });
         tile_each2<64, kSlice, 8>(uacc, [&](int i, int a, float& v0, float& v1) {
             float u0 = 0.f, u1 = 0.f;
             if (i < L) {
@@ -353,9 +358,18 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         // S^T = e^{gam_L} S^T + K^T (diag(fk) U)
         const float dl = expf(gL);
         tile_each<kD, kSlice, 8>(sacc, [&](int, int, float& v) { v *= dl; });
-        tile_mma_bits<kD, kSlice, 64, 8>(
-            sacc, [&](int b, int i) { return f2tf32(cur.K[umma::swz(i, b, 64)]); },
-            [&](int i, int a) { return __float_as_uint(Ub[umma::kidx(a, i, 64)]); });
+        tile_mma_frag<kD, kSlice, 64, 8>(
+            sacc,
+            [&](int r0, int k0, uint32_t(&f)[4]) {   // A(b, i) = K[i][b]: element loads
+                const int g = lane >> 2, t = lane & 3;
+                f[0] = f2tf32(cur.K[umma::swz(k0 + t, r0 + g, 64)]);
+                f[1] = f2tf32(cur.K[umma::swz(k0 + t, r0 + g + 8, 64)]);
+                f[2] = f2tf32(cur.K[umma::swz(k0 + t + 4, r0 + g, 64)]);
+                f[3] = f2tf32(cur.K[umma::swz(k0 + t + 4, r0 + g + 8, 64)]);
+            },
+            [&](int k0, int n0, uint32_t(&f)[4]) {
+                ldsm_b2(f, k0, n0, [&](int n, int k) { return Ub + umma::kidx(n, k, 64); });
+            });
         if (tid == 0) umma::bulk_wait_read();   // the chunk-start copy has read St
         __syncthreads();   // reads of cur, St and Ub are done
         tile_each2<kD, kSlice, 8>(sacc, [&](int b, int a, float& v0, float& v1) {

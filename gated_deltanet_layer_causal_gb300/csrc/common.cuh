@@ -173,6 +173,58 @@ __device__ __forceinline__ void tile_mma_bits(typename Tile<M, N, NW>::Acc& acc,
     }
 }
 
+// Four 8 x 8 matrices of 16-bit elements (8 rows of 16 bytes each; lane l
+// gives the address of row l % 8 of matrix l / 8).  For 32-bit (tf32) data a
+// matrix is 8 rows x 4 values, and thread t receives (row t / 4, value t % 4):
+// exactly the m16n8k8 tf32 fragment pattern.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const float* row_addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(row_addr))));
+}
+// The A fragment (rows r0 .. r0 + 15, columns k0 .. k0 + 7) of a matrix whose
+// 4-value row pieces are 16-byte aligned at addr(row, col), col % 4 == 0.
+template <class F>
+__device__ __forceinline__ void ldsm_a(uint32_t (&a)[4], int r0, int k0, F addr) {
+    const int l = threadIdx.x & 31, m = l >> 3;
+    ldsm_x4(a, addr(r0 + (l & 7) + 8 * (m & 1), k0 + 4 * (m >> 1)));
+}
+// The B fragments of two n-blocks (n0 .. n0 + 7 -> b[0], b[1]; n0 + 8 .. -> b[2],
+// b[3]) of B(k, n) stored with rows n: addr(n, k), k % 4 == 0.
+template <class F>
+__device__ __forceinline__ void ldsm_b2(uint32_t (&b)[4], int k0, int n0, F addr) {
+    const int l = threadIdx.x & 31, m = l >> 3;
+    ldsm_x4(b, addr(n0 + (l & 7) + 8 * (m >> 1), k0 + 4 * (m & 1)));
+}
+
+// acc += A * B with whole fragments supplied by the caller: fa(r0, k0, a[4])
+// fills the A fragment of rows r0 .. r0 + 15, fb(k0, n0, b[4]) the B fragments
+// of the two n-blocks n0 and n0 + 8 (as tf32 bit patterns), so operands in
+// fragment-friendly layouts load with ldmatrix.
+template <int M, int N, int K, int NW, class FA, class FB>
+__device__ __forceinline__ void tile_mma_frag(typename Tile<M, N, NW>::Acc& acc, FA fa, FB fb) {
+    using C = Tile<M, N, NW>;
+    static_assert(C::NPW % 2 == 0, "pairs of n-blocks");
+    const int m0 = C::m0(), n0 = C::n0();
+#pragma unroll 2
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t af[C::MPW][4];
+#pragma unroll
+        for (int i = 0; i < C::MPW; i++) fa(m0 + i * 16, k0, af[i]);
+#pragma unroll
+        for (int j = 0; j < C::NPW; j += 2) {
+            uint32_t bf[4];
+            fb(k0, n0 + j * 8, bf);
+            const uint32_t b0[2] = {bf[0], bf[1]}, b1[2] = {bf[2], bf[3]};
+#pragma unroll
+            for (int i = 0; i < C::MPW; i++) {
+                mma_tf32(acc[i][j], af[i], b0);
+                mma_tf32(acc[i][j + 1], af[i], b1);
+            }
+        }
+    }
+}
+
 // Visit every accumulator element as f(row, col, value&).
 template <int M, int N, int NW, class F>
 __device__ __forceinline__ void tile_each(typename Tile<M, N, NW>::Acc& acc, F f) {
