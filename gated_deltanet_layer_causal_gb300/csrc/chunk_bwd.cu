@@ -773,11 +773,20 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         umma::bulk_load(TC, Tg + 64 * 64, 64 * 64 * 4, mbl);
     }
     load_gam(gam, sv, ci, h);
+    // the gate inputs and the dgam terms of the other kernels are loaded now and
+    // used at the very end
+    float xa = 0.f, dgam_in = 0.f;
     if (tid < 64) {
         bet[tid] = tid < L ? sv.beta[(int64_t)h * sv.T + ci.start + tid] : 0.f;
         dgs[tid] = 0.f;
         dbs[tid] = 0.f;
+        if (tid < L) {
+            const int64_t t = ci.start + tid;
+            xa = to_f(av[t * hv + h]) + dt_bias[h];
+            dgam_in = w.dgam[t * hv + h];
+        }
     }
+    const float Aexp = expf(A_log[h]);
     if (warp == 0) umma::tmem_alloc(tslot, 512);
     __syncthreads();
     if (tid < 64) {
@@ -1004,7 +1013,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         umma::store_rows_sw(w.dKv3 + ((int64_t)ci.start * hv + h) * kD, (int64_t)hv * kD, Ks, L);
     }
     // ---- dg = reverse cumsum of dgam; gates
-    if (tid < 64) sc[tid] = tid < L ? dgs[tid] + w.dgam[(int64_t)(ci.start + tid) * hv + h] : 0.f;
+    if (tid < 64) sc[tid] = tid < L ? dgs[tid] + dgam_in : 0.f;
     __syncthreads();
     if (tid < 32) {
         float a = sc[63 - 2 * lane], b = sc[62 - 2 * lane], s = a + b;
@@ -1022,8 +1031,6 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     if (tid < L) {
         const int64_t t = ci.start + tid;
         const float dg = rk[tid];
-        const float Aexp = expf(A_log[h]);
-        const float xa = to_f(av[t * hv + h]) + dt_bias[h];
         const float gval = -Aexp * softplusf_(xa);
         const float dav = dg * (-Aexp) * sigmoidf_(xa);
         const float bb = bet[tid];

@@ -126,14 +126,16 @@ template <class T>
 __device__ __forceinline__ float4 conv_dpre(const T* x, const T* cs, const float* dq, int64_t t,
                                             int64_t s, int n, int C, int c,
                                             const float (&w)[4][kConvK], bool norm, float scale,
-                                            float l2_eps) {
-    float4 a0 = ld4(x + t * C + c);
-    float4 a1 = conv_in(x, cs, t - 1, s, n, C, c);
-    float4 a2 = conv_in(x, cs, t - 2, s, n, C, c);
-    float4 a3 = conv_in(x, cs, t - 3, s, n, C, c);
+                                            float l2_eps);
+
+// Gradient at the conv output pre-activation of token t (backward through SiLU
+// and, for q / k channels, the L2 norm and the q scale), given the conv inputs
+// a0 = x[t], a1 = x[t-1], a2 = x[t-2], a3 = x[t-3] and the incoming gradient g4.
+__device__ __forceinline__ float4 conv_dpre_w(float4 a0, float4 a1, float4 a2, float4 a3,
+                                              float4 g4, const float (&w)[4][kConvK], bool norm,
+                                              float scale, float l2_eps) {
     float p[4] = {conv4(w[0], a3.x, a2.x, a1.x, a0.x), conv4(w[1], a3.y, a2.y, a1.y, a0.y),
                   conv4(w[2], a3.z, a2.z, a1.z, a0.z), conv4(w[3], a3.w, a2.w, a1.w, a0.w)};
-    float4 g4 = ld4(dq + t * C + c);
     float gd[4] = {g4.x, g4.y, g4.z, g4.w};
     float xc[4], sg[4];
 #pragma unroll
@@ -154,6 +156,16 @@ __device__ __forceinline__ float4 conv_dpre(const T* x, const T* cs, const float
     o.z = gd[2] * sg[2] * (1.f + p[2] * (1.f - sg[2]));
     o.w = gd[3] * sg[3] * (1.f + p[3] * (1.f - sg[3]));
     return o;
+}
+
+template <class T>
+__device__ __forceinline__ float4 conv_dpre(const T* x, const T* cs, const float* dq, int64_t t,
+                                            int64_t s, int n, int C, int c,
+                                            const float (&w)[4][kConvK], bool norm, float scale,
+                                            float l2_eps) {
+    return conv_dpre_w(ld4(x + t * C + c), conv_in(x, cs, t - 1, s, n, C, c),
+                       conv_in(x, cs, t - 2, s, n, C, c), conv_in(x, cs, t - 3, s, n, C, c),
+                       ld4(dq + t * C + c), w, norm, scale, l2_eps);
 }
 
 __device__ __forceinline__ float f4(const float4& v, int i) {
@@ -196,26 +208,38 @@ conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
         float4 d1 = (t1 < e) ? conv_dpre(x, cs_in, dqkv, t1, s, n, C, c, wr, norm, scale, l2_eps) : z4;
         float4 d2 = (t1 + 1 < e) ? conv_dpre(x, cs_in, dqkv, t1 + 1, s, n, C, c, wr, norm, scale, l2_eps) : z4;
         float4 d3 = (t1 + 2 < e) ? conv_dpre(x, cs_in, dqkv, t1 + 2, s, n, C, c, wr, norm, scale, l2_eps) : z4;
+        // walking backwards: a register window holds x[t], x[t-1], x[t-2], x[t-3];
+        // each step loads one new x row and the next dq row ahead of use
+        float4 xw0 = conv_in(x, cs_in, t1 - 1, s, n, C, c);
+        float4 xw1 = conv_in(x, cs_in, t1 - 2, s, n, C, c);
+        float4 xw2 = conv_in(x, cs_in, t1 - 3, s, n, C, c);
+        float4 xw3 = conv_in(x, cs_in, t1 - 4, s, n, C, c);
+        float4 g = ld4(dqkv + (t1 - 1) * C + c);
         for (int64_t t = t1 - 1; t >= t0; t--) {
             if (t < s) {  // crossed into the previous (non-empty) sequence
                 while (cu[n] > t) n--;
                 s = cu[n];
                 e = cu[n + 1];
                 d1 = d2 = d3 = z4;
+                xw0 = conv_in(x, cs_in, t, s, n, C, c);
+                xw1 = conv_in(x, cs_in, t - 1, s, n, C, c);
+                xw2 = conv_in(x, cs_in, t - 2, s, n, C, c);
+                xw3 = conv_in(x, cs_in, t - 3, s, n, C, c);
             }
-            float4 d0 = conv_dpre(x, cs_in, dqkv, t, s, n, C, c, wr, norm, scale, l2_eps);
+            const float4 xn = conv_in(x, cs_in, t - 4, s, n, C, c);   // for step t - 1
+            const float4 gn = t > t0 ? ld4(dqkv + (t - 1) * C + c) : z4;
+            const float4 d0 = conv_dpre_w(xw0, xw1, xw2, xw3, g, wr, norm, scale, l2_eps);
             float4 o;
             o.x = wr[0][3] * d0.x + wr[0][2] * d1.x + wr[0][1] * d2.x + wr[0][0] * d3.x;
             o.y = wr[1][3] * d0.y + wr[1][2] * d1.y + wr[1][1] * d2.y + wr[1][0] * d3.y;
             o.z = wr[2][3] * d0.z + wr[2][2] * d1.z + wr[2][1] * d2.z + wr[2][0] * d3.z;
             o.w = wr[3][3] * d0.w + wr[3][2] * d1.w + wr[3][1] * d2.w + wr[3][0] * d3.w;
             st4(dx + t * C + c, o);
+            const float4 xin[kConvK] = {xw3, xw2, xw1, xw0};   // x[t - 3 + j]
 #pragma unroll
-            for (int j = 0; j < kConvK; j++) {
-                float4 xin = conv_in(x, cs_in, t - (kConvK - 1) + j, s, n, C, c);
+            for (int j = 0; j < kConvK; j++)
 #pragma unroll
-                for (int ch = 0; ch < 4; ch++) dw[ch][j] += f4(d0, ch) * f4(xin, ch);
-            }
+                for (int ch = 0; ch < 4; ch++) dw[ch][j] += f4(d0, ch) * f4(xin[j], ch);
             if (t == s && dcs != nullptr) {
                 // gradient of the conv cache: position s-3+m feeds tokens s..s+m
 #pragma unroll
@@ -227,6 +251,8 @@ conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
                 }
             }
             d3 = d2; d2 = d1; d1 = d0;
+            xw0 = xw1; xw1 = xw2; xw2 = xw3; xw3 = xn;
+            g = gn;
         }
     }
 #pragma unroll
