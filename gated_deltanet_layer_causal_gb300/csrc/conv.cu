@@ -176,7 +176,7 @@ __device__ __forceinline__ float f4(const float4& v, int i) {
 // dx[t] = sum_j w[j] dpre[t+3-j] within the sequence; dw partials per CTA
 // (fixed-order sum over the CTA's warps) go to wpart[blockIdx.x][c][j].
 template <class T>
-__global__ void __launch_bounds__(kConvWarps * 32)
+__global__ void __launch_bounds__(kConvWarps * 32, 2)
 conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* cs_in,
                 const float* __restrict__ dqkv, const int32_t* __restrict__ cu, int N,
                 int64_t Ttot, int C, int hk, float l2_eps, float q_scale, T* __restrict__ dx,
@@ -208,51 +208,100 @@ conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
         float4 d1 = (t1 < e) ? conv_dpre(x, cs_in, dqkv, t1, s, n, C, c, wr, norm, scale, l2_eps) : z4;
         float4 d2 = (t1 + 1 < e) ? conv_dpre(x, cs_in, dqkv, t1 + 1, s, n, C, c, wr, norm, scale, l2_eps) : z4;
         float4 d3 = (t1 + 2 < e) ? conv_dpre(x, cs_in, dqkv, t1 + 2, s, n, C, c, wr, norm, scale, l2_eps) : z4;
-        // walking backwards: a register window holds x[t], x[t-1], x[t-2], x[t-3];
-        // each step loads one new x row and the next dq row ahead of use
-        float4 xw0 = conv_in(x, cs_in, t1 - 1, s, n, C, c);
-        float4 xw1 = conv_in(x, cs_in, t1 - 2, s, n, C, c);
-        float4 xw2 = conv_in(x, cs_in, t1 - 3, s, n, C, c);
-        float4 xw3 = conv_in(x, cs_in, t1 - 4, s, n, C, c);
-        float4 g = ld4(dqkv + (t1 - 1) * C + c);
-        for (int64_t t = t1 - 1; t >= t0; t--) {
-            if (t < s) {  // crossed into the previous (non-empty) sequence
-                while (cu[n] > t) n--;
-                s = cu[n];
-                e = cu[n + 1];
-                d1 = d2 = d3 = z4;
-                xw0 = conv_in(x, cs_in, t, s, n, C, c);
-                xw1 = conv_in(x, cs_in, t - 1, s, n, C, c);
-                xw2 = conv_in(x, cs_in, t - 2, s, n, C, c);
-                xw3 = conv_in(x, cs_in, t - 3, s, n, C, c);
-            }
-            const float4 xn = conv_in(x, cs_in, t - 4, s, n, C, c);   // for step t - 1
-            const float4 gn = t > t0 ? ld4(dqkv + (t - 1) * C + c) : z4;
-            const float4 d0 = conv_dpre_w(xw0, xw1, xw2, xw3, g, wr, norm, scale, l2_eps);
-            float4 o;
-            o.x = wr[0][3] * d0.x + wr[0][2] * d1.x + wr[0][1] * d2.x + wr[0][0] * d3.x;
-            o.y = wr[1][3] * d0.y + wr[1][2] * d1.y + wr[1][1] * d2.y + wr[1][0] * d3.y;
-            o.z = wr[2][3] * d0.z + wr[2][2] * d1.z + wr[2][1] * d2.z + wr[2][0] * d3.z;
-            o.w = wr[3][3] * d0.w + wr[3][2] * d1.w + wr[3][1] * d2.w + wr[3][0] * d3.w;
-            st4(dx + t * C + c, o);
-            const float4 xin[kConvK] = {xw3, xw2, xw1, xw0};   // x[t - 3 + j]
+        if (s <= t0 && (t1 - t0) % 4 == 0) {
+            // the whole run lies in one sequence: four tokens per step, whose
+            // dpre chains are independent; xr[k] = x[tb - 6 + k], three rows
+            // carried from step to step
+            float4 xr[7];
 #pragma unroll
-            for (int j = 0; j < kConvK; j++)
+            for (int k = 0; k < 7; k++) xr[k] = conv_in(x, cs_in, t1 - 7 + k, s, n, C, c);
+            for (int64_t tb = t1 - 1; tb >= t0; tb -= 4) {
+                float4 gq[4], dd[4];
 #pragma unroll
-                for (int ch = 0; ch < 4; ch++) dw[ch][j] += f4(d0, ch) * f4(xin[j], ch);
-            if (t == s && dcs != nullptr) {
-                // gradient of the conv cache: position s-3+m feeds tokens s..s+m
+                for (int u = 0; u < 4; u++) gq[u] = ld4(dqkv + (tb - u) * C + c);
 #pragma unroll
-                for (int ch = 0; ch < 4; ch++) {
-                    float* o3 = dcs + ((int64_t)n * C + c + ch) * (kConvK - 1);
-                    o3[0] = wr[ch][0] * f4(d0, ch);
-                    o3[1] = wr[ch][0] * f4(d1, ch) + wr[ch][1] * f4(d0, ch);
-                    o3[2] = wr[ch][0] * f4(d2, ch) + wr[ch][1] * f4(d1, ch) + wr[ch][2] * f4(d0, ch);
+                for (int u = 0; u < 4; u++)
+                    dd[u] = conv_dpre_w(xr[6 - u], xr[5 - u], xr[4 - u], xr[3 - u], gq[u], wr, norm,
+                                        scale, l2_eps);
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    const int64_t t = tb - u;
+                    const float4 d0 = dd[u];
+                    float4 o;
+                    o.x = wr[0][3] * d0.x + wr[0][2] * d1.x + wr[0][1] * d2.x + wr[0][0] * d3.x;
+                    o.y = wr[1][3] * d0.y + wr[1][2] * d1.y + wr[1][1] * d2.y + wr[1][0] * d3.y;
+                    o.z = wr[2][3] * d0.z + wr[2][2] * d1.z + wr[2][1] * d2.z + wr[2][0] * d3.z;
+                    o.w = wr[3][3] * d0.w + wr[3][2] * d1.w + wr[3][1] * d2.w + wr[3][0] * d3.w;
+                    st4(dx + t * C + c, o);
+#pragma unroll
+                    for (int j = 0; j < kConvK; j++)
+#pragma unroll
+                        for (int ch = 0; ch < 4; ch++) dw[ch][j] += f4(d0, ch) * f4(xr[3 - u + j], ch);
+                    if (t == s && dcs != nullptr) {
+#pragma unroll
+                        for (int ch = 0; ch < 4; ch++) {
+                            float* o3 = dcs + ((int64_t)n * C + c + ch) * (kConvK - 1);
+                            o3[0] = wr[ch][0] * f4(d0, ch);
+                            o3[1] = wr[ch][0] * f4(d1, ch) + wr[ch][1] * f4(d0, ch);
+                            o3[2] = wr[ch][0] * f4(d2, ch) + wr[ch][1] * f4(d1, ch) +
+                                    wr[ch][2] * f4(d0, ch);
+                        }
+                    }
+                    d3 = d2; d2 = d1; d1 = d0;
+                }
+                if (tb - 4 >= t0) {   // next step: x[tb - 10 .. tb - 4]
+                    xr[4] = xr[0]; xr[5] = xr[1]; xr[6] = xr[2];
+#pragma unroll
+                    for (int k = 0; k < 4; k++) xr[k] = conv_in(x, cs_in, tb - 10 + k, s, n, C, c);
                 }
             }
-            d3 = d2; d2 = d1; d1 = d0;
-            xw0 = xw1; xw1 = xw2; xw2 = xw3; xw3 = xn;
-            g = gn;
+        } else {
+            // walking backwards: a register window holds x[t], x[t-1], x[t-2], x[t-3];
+            // each step loads one new x row and the next dq row ahead of use
+            float4 xw0 = conv_in(x, cs_in, t1 - 1, s, n, C, c);
+            float4 xw1 = conv_in(x, cs_in, t1 - 2, s, n, C, c);
+            float4 xw2 = conv_in(x, cs_in, t1 - 3, s, n, C, c);
+            float4 xw3 = conv_in(x, cs_in, t1 - 4, s, n, C, c);
+            float4 g = ld4(dqkv + (t1 - 1) * C + c);
+            for (int64_t t = t1 - 1; t >= t0; t--) {
+                if (t < s) {  // crossed into the previous (non-empty) sequence
+                    while (cu[n] > t) n--;
+                    s = cu[n];
+                    e = cu[n + 1];
+                    d1 = d2 = d3 = z4;
+                    xw0 = conv_in(x, cs_in, t, s, n, C, c);
+                    xw1 = conv_in(x, cs_in, t - 1, s, n, C, c);
+                    xw2 = conv_in(x, cs_in, t - 2, s, n, C, c);
+                    xw3 = conv_in(x, cs_in, t - 3, s, n, C, c);
+                }
+                const float4 xn = conv_in(x, cs_in, t - 4, s, n, C, c);   // for step t - 1
+                const float4 gn = t > t0 ? ld4(dqkv + (t - 1) * C + c) : z4;
+                const float4 d0 = conv_dpre_w(xw0, xw1, xw2, xw3, g, wr, norm, scale, l2_eps);
+                float4 o;
+                o.x = wr[0][3] * d0.x + wr[0][2] * d1.x + wr[0][1] * d2.x + wr[0][0] * d3.x;
+                o.y = wr[1][3] * d0.y + wr[1][2] * d1.y + wr[1][1] * d2.y + wr[1][0] * d3.y;
+                o.z = wr[2][3] * d0.z + wr[2][2] * d1.z + wr[2][1] * d2.z + wr[2][0] * d3.z;
+                o.w = wr[3][3] * d0.w + wr[3][2] * d1.w + wr[3][1] * d2.w + wr[3][0] * d3.w;
+                st4(dx + t * C + c, o);
+                const float4 xin[kConvK] = {xw3, xw2, xw1, xw0};   // x[t - 3 + j]
+    #pragma unroll
+                for (int j = 0; j < kConvK; j++)
+    #pragma unroll
+                    for (int ch = 0; ch < 4; ch++) dw[ch][j] += f4(d0, ch) * f4(xin[j], ch);
+                if (t == s && dcs != nullptr) {
+                    // gradient of the conv cache: position s-3+m feeds tokens s..s+m
+    #pragma unroll
+                    for (int ch = 0; ch < 4; ch++) {
+                        float* o3 = dcs + ((int64_t)n * C + c + ch) * (kConvK - 1);
+                        o3[0] = wr[ch][0] * f4(d0, ch);
+                        o3[1] = wr[ch][0] * f4(d1, ch) + wr[ch][1] * f4(d0, ch);
+                        o3[2] = wr[ch][0] * f4(d2, ch) + wr[ch][1] * f4(d1, ch) + wr[ch][2] * f4(d0, ch);
+                    }
+                }
+                d3 = d2; d2 = d1; d1 = d0;
+                xw0 = xw1; xw1 = xw2; xw2 = xw3; xw3 = xn;
+                g = gn;
+            }
         }
     }
 #pragma unroll
