@@ -97,6 +97,7 @@ BwdScratch carve_bwd(void* ws, const gdn_dims* d, int NT, int32_t** status, size
     s.dW = c.take<float>(T * H * kD);
     s.dS = c.take<float>((size_t)NT * H * kD * kD);
     s.dgam = c.take<float>(T * H);
+    s.dgam2 = c.take<float>(T * H);
     s.dgs = c.take<float>(T * H);
     // dnorm_w partials [NT*H][kD], gate partials [NT*H][2], column-sum stage [512][kD]
     s.nw_part = c.take<float>((size_t)NT * H * kD + (size_t)NT * H * 2 + 512 * kD);

@@ -21,6 +21,8 @@
 #include "prof.h"
 #include "umma.cuh"
 
+#include <mutex>
+
 namespace gdn {
 
 
@@ -668,7 +670,7 @@ bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv
     if (tid < 64) {   // dgam from R: row sums minus column sums (fixed order)
         const float cs = (colp[tid] + colp[64 + tid]) + (colp[128 + tid] + colp[192 + tid]);
         dgl[tid] = (rpart[tid] + rpart[64 + tid]) - cs;
-        if (tid < L) w.dgam[(int64_t)(ci.start + tid) * hv + h] += dgl[tid];
+        if (tid < L) w.dgam2[(int64_t)(ci.start + tid) * hv + h] = dgl[tid];
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
     umma::fence_after_sync();
@@ -783,7 +785,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         if (tid < L) {
             const int64_t t = ci.start + tid;
             xa = to_f(av[t * hv + h]) + dt_bias[h];
-            dgam_in = w.dgam[t * hv + h];
+            dgam_in = w.dgam[t * hv + h] + w.dgam2[t * hv + h];
         }
     }
     const float Aexp = expf(A_log[h]);
@@ -1122,6 +1124,48 @@ __global__ void colsum_stage2_kernel(const float* __restrict__ tmp, float* __res
 }
 
 // ------------------------------------------------------------------ launcher
+// The reverse state pass runs one CTA per (64-row slice, head, sequence) and
+// leaves most SMs idle for its whole duration; the P / dP kernel does not
+// depend on it, so it runs beside it: the state pass goes to a high-priority
+// side stream forked from and joined back into the caller's stream.  The side
+// stream and its two events are created once per device; the fork / join
+// sequence is enqueued under a lock, so concurrent calls on one device do not
+// interleave their events.
+namespace {
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxSideDevices = 64;
+std::mutex g_side_mu;
+SideStream g_side[kMaxSideDevices];
+
+// The current device's side stream, or nullptr (then everything runs on the
+// caller's stream).  Called with g_side_mu held.
+SideStream* side_stream() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) return nullptr;
+    SideStream& ss = g_side[dev];
+    if (ss.s == nullptr) {
+        int lo = 0, hi = 0;
+        cudaStream_t s = nullptr;
+        cudaEvent_t f = nullptr, j = nullptr;
+        if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess ||
+            cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, hi) != cudaSuccess)
+            return nullptr;
+        if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+            cudaStreamDestroy(s);
+            return nullptr;
+        }
+        ss.s = s;
+        ss.fork = f;
+        ss.join = j;
+    }
+    return &ss;
+}
+}  // namespace
+
 template <class IO>
 static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStream_t st) {
     static bool attr = false;
@@ -1170,20 +1214,37 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
         GDN_PROF("chunk_bwd_local", st);
         bwd_local_kernel<<<dim3(a.NT, a.hv), 256, kB1Smem, st>>>(maps, a.hk, a.hv, a.sv, w);
     }
-    if (a.N > 0) {
-        GDN_PROF("chunk_bwd_state", st);
-        bwd_state_kernel<<<dim3(kD / kSl, a.hv, a.N), 256, kB2Smem, st>>>(
-            maps, a.hk, a.hv, a.dS_final, a.dS_init, a.sv, w);
+    std::unique_lock<std::mutex> lk(g_side_mu);
+    SideStream* ss = side_stream();
+    if (a.N > 0) {   // reverse state pass, beside the P / dP kernel
+        cudaStream_t sst = st;
+        if (ss != nullptr && cudaEventRecord(ss->fork, st) == cudaSuccess &&
+            cudaStreamWaitEvent(ss->s, ss->fork, 0) == cudaSuccess)
+            sst = ss->s;
+        {
+            GDN_PROF("chunk_bwd_state", sst);
+            bwd_state_kernel<<<dim3(kD / kSl, a.hv, a.N), 256, kB2Smem, sst>>>(
+                maps, a.hk, a.hv, a.dS_final, a.dS_init, a.sv, w);
+        }
+        if (sst != st) {
+            cudaError_t e = cudaEventRecord(ss->join, sst);
+            if (a.NT > 0) {
+                GDN_PROF("chunk_bwd_dp", st);
+                bwd_dp_kernel<<<dim3(a.NT, a.hv), 256, kDpSmem, st>>>(maps, a.hk, a.hv, a.sv, w);
+            }
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ss->join, 0);
+            if (e != cudaSuccess) return e;
+        } else if (a.NT > 0) {
+            GDN_PROF("chunk_bwd_dp", st);
+            bwd_dp_kernel<<<dim3(a.NT, a.hv), 256, kDpSmem, st>>>(maps, a.hk, a.hv, a.sv, w);
+        }
     }
+    lk.unlock();
     if (a.NT > 0) {
         {
             GDN_PROF("chunk_bwd_sfacing", st);
             bwd_sfacing_kernel<<<dim3(a.NT, a.hv), 256, kB3aSmem, st>>>(maps, a.hk, a.hv, a.sv,
                                                                           w);
-        }
-        {
-            GDN_PROF("chunk_bwd_dp", st);
-            bwd_dp_kernel<<<dim3(a.NT, a.hv), 256, kDpSmem, st>>>(maps, a.hk, a.hv, a.sv, w);
         }
         GDN_PROF("chunk_bwd_wy", st);
         bwd_wy_kernel<IO><<<dim3(a.NT, a.hv), 256, kWySmem, st>>>(

@@ -103,6 +103,7 @@ struct BwdScratch {
     float* dKv3;     // [T, Hv, d] per v-head dk^, WY part
     float* dW;       // [T, Hv, d]
     float* dgam;     // [T, Hv] partial dgamma from the state-facing terms
+    float* dgam2;    // [T, Hv] the P / dP kernel's dgam terms (it runs beside the state pass)
     float* dgs;      // [T, Hv] dg (per token)
     float* nw_part;  // [NT * Hv, d] dnorm_w partials
 };
