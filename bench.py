@@ -176,7 +176,6 @@ class Step:
 # a kernel changed since then reports null.
 TRAFFIC_64K = {
     "conv_fwd": 3649505280,
-    "chunk_prep": 6570291200,
     "chunk_state_fwd": 11317725184,
     "chunk_out_fwd": 8939784192,
     "chunk_bwd_state": 10358249472,
@@ -203,7 +202,8 @@ def kernel_cost(name: str, w: synth.Workload, NT: int):
     table = {
         "conv_fwd": T * C * io + T * C * 4,
         "conv_bwd": 2 * T * C * io + T * C * 4,
-        "chunk_prep": tk + tv + gates + 2 * tv + 2 * g + 2 * Tt,
+        "gates": gates + 2 * g,
+        "chunk_prep": tk + tv + 2 * g + 2 * tv + 2 * Tt,
         "chunk_state_fwd": 2 * tv + tk + g + tv + 2 * S,
         "chunk_out_fwd": 2 * tk + tv + S + g + act + act + tv + g,
         "chunk_norm_bwd": tv + 2 * act + tv + act,

@@ -69,8 +69,51 @@ __global__ void plan_kernel(const int32_t* __restrict__ cu, int N, int64_t T, in
     if (tid == nth - 1) seq_chunk[N] = NT;
 }
 
+// ------------------------------------------------------------------ gates
+// grid (NT, ceil(Hv / 8)), 256 threads: one warp per (chunk, v-head), two tokens
+// per lane.  g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b); gam = the
+// in-chunk inclusive cumsum of g (a warp scan), stored head-major with beta.
+template <class IO>
+__global__ void __launch_bounds__(256)
+gates_kernel(const IO* __restrict__ av, const IO* __restrict__ bv, const float* __restrict__ A_log,
+             const float* __restrict__ dt_bias, int hv, FwdSaved sv) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y * 8 + warp;
+    const ChunkInfo ci = sv.chunks[blockIdx.x];
+    if (h >= hv || ci.len == 0) return;
+    const int L = ci.len;
+    const float Aexp = expf(A_log[h]), db = dt_bias[h];
+    float g[2], b[2];
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+        const int j = 2 * lane + e;
+        g[e] = b[e] = 0.f;
+        if (j < L) {
+            const int64_t t = ci.start + j;
+            g[e] = -Aexp * softplusf_(to_f(av[t * hv + h]) + db);
+            b[e] = sigmoidf_(to_f(bv[t * hv + h]));
+        }
+    }
+    float s = g[0] + g[1];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += u;
+    }
+    const float ex = s - (g[0] + g[1]);
+    const float gam[2] = {ex + g[0], ex + g[0] + g[1]};
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+        const int j = 2 * lane + e;
+        if (j < L) {
+            sv.gam[(int64_t)h * sv.T + ci.start + j] = gam[e];
+            sv.beta[(int64_t)h * sv.T + ci.start + j] = b[e];
+        }
+    }
+}
+
 // ------------------------------------------------------------------ prep
-// grid (NT, Hv), 256 threads, tcgen05.  Gates and their in-chunk cumsum, then
+// grid (NT, Hv), 256 threads, tcgen05.  With the gates from gates_kernel,
 //   D1 = K K^T (64 x 64)  ->  A = beta_i e^{gam_i-gam_j} D1 (j < i)
 //   T  = (I + A)^-1        (forward substitution on the CUDA cores; saved)
 //   D2 = T [diag(beta e^gam) K | diag(beta) V]   (one M=64, N=256, K=64 MMA)
@@ -80,11 +123,8 @@ constexpr int kLdK = 132, kLdA = 68;
 constexpr int kPrepFloats = 2 * 64 * 128 + 256 * 64 + 2 * 64 * kLdA + 64 * 64;
 constexpr size_t kPrepSmem = sizeof(float) * (kPrepFloats + 3 * 64 + 16) + 64 + 1024;
 
-template <class IO>
 __global__ void __launch_bounds__(256, 1)
-prep_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
-            const IO* __restrict__ bv, const float* __restrict__ A_log,
-            const float* __restrict__ dt_bias, int hk, int hv, FwdSaved sv) {
+prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv) {
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
     float* Ks = sm;                    // [64][128] swizzled
@@ -110,27 +150,15 @@ prep_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
         umma::tma_rows(Vs, 64, &maps.v, h, ci.start, mbl);
     }
-    if (tid < 64) {
-        float g = 0.f, b = 0.f;
-        if (tid < L) {
-            const int64_t t = ci.start + tid;
-            g = -expf(A_log[h]) * softplusf_(to_f(av[t * hv + h]) + dt_bias[h]);
-            b = sigmoidf_(to_f(bv[t * hv + h]));
-        }
-        gam[tid] = g;
-        bet[tid] = b;
+    if (tid < 64) {   // padding rows continue the last gam (g = 0), beta = 0
+        const float gm = sv.gam[(int64_t)h * sv.T + ci.start + min(tid, L - 1)];
+        const float bt = tid < L ? sv.beta[(int64_t)h * sv.T + ci.start + tid] : 0.f;
+        gam[tid] = gm;
+        bet[tid] = bt;
+        be[tid] = bt * expf(gm);
     }
     if (warp == 0) umma::tmem_alloc(tslot, 512);
     __syncthreads();
-    if (tid < 32) warp_cumsum64(gam);
-    __syncthreads();
-    if (tid < 64) {
-        be[tid] = bet[tid] * expf(gam[tid]);
-        if (tid < L) {
-            sv.gam[(int64_t)h * sv.T + ci.start + tid] = gam[tid];
-            sv.beta[(int64_t)h * sv.T + ci.start + tid] = bet[tid];
-        }
-    }
     bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
     if (L < 64) {   // tail rows belong to the next sequence
         umma::zero_tail_rows(Ks, 64, 0, L);
@@ -568,7 +596,7 @@ template <class IO>
 static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(prep_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kPrepSmem);
         cudaFuncSetAttribute(state_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kStateSmem);
@@ -578,6 +606,11 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
     }
     TileMaps maps{};
     if (a.NT > 0) {
+        {
+            GDN_PROF("gates", st);
+            gates_kernel<IO><<<dim3(a.NT, (a.hv + 7) / 8), 256, 0, st>>>(
+                (const IO*)a.a, (const IO*)a.b, a.A_log, a.dt_bias, a.hv, a.sv);
+        }
         const int64_t C = (int64_t)(2 * a.hk + a.hv) * kD;
         cudaError_t e = make_rows_map(&maps.q, a.qkv, a.hk, a.T, C);
         if (e == cudaSuccess) e = make_rows_map(&maps.k, a.qkv + (int64_t)a.hk * kD, a.hk, a.T, C);
@@ -587,8 +620,7 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
         if (e == cudaSuccess) e = make_rows_map(&maps.W, a.sv.W, a.hv, a.T, (int64_t)a.hv * kD);
         if (e != cudaSuccess) return e;
         GDN_PROF("chunk_prep", st);
-        prep_kernel<IO><<<dim3(a.NT, a.hv), 256, kPrepSmem, st>>>(
-            maps, (const IO*)a.a, (const IO*)a.b, a.A_log, a.dt_bias, a.hk, a.hv, a.sv);
+        prep_kernel<<<dim3(a.NT, a.hv), 256, kPrepSmem, st>>>(maps, a.hk, a.hv, a.sv);
     }
     if (a.N > 0) {
         GDN_PROF("chunk_state_fwd", st);
