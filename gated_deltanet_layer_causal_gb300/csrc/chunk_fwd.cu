@@ -265,47 +265,51 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv) 
 }
 
 // ------------------------------------------------------------------ state pass
-// grid (d_v / kSlice, Hv, N), 256 threads, one CTA per SM.  Rows a of S evolve
+// grid (3, Hv, N), 256 threads, one CTA per SM.  Rows a of S evolve
 // independently (k, beta, g are shared by all rows), so each CTA carries a
-// 64-row slice of the fp32 state -- kept transposed, S^T[b][a], in the MMA
-// accumulators -- through all chunks of its sequence.  The next chunk's W, K
-// and U~ slice arrive through the TMA into the other half of a double buffer
-// while the current chunk is computed.  A tf32-rounded copy of the state
-// slice, St, is held in exactly the layout of its slice of the chunk-start
-// state tile (K-major rows a): it feeds the tensor cores without conversion
-// and leaves as one bulk copy per chunk.
-constexpr int kSlice = 64;
+// slice of rows of the fp32 state -- kept transposed, S^T[b][a], in the MMA
+// accumulators -- through all chunks of its sequence: rows 0-47, 48-95 and
+// 96-127, so that 3 * Hv CTAs occupy most SMs.  The next chunk's W, K and U~
+// slice arrive through the TMA into the other half of a double buffer while
+// the current chunk is computed.  A tf32-rounded copy of the state slice, St,
+// is held in exactly the layout of its slice of the chunk-start state tile
+// (K-major rows a): it feeds the tensor cores without conversion and leaves as
+// one bulk copy per chunk.
+constexpr int kSliceMax = 48;
 struct StateStage {                // one chunk's operands (a multiple of 1 KB)
     float W[64 * 128];             // swizzled, arrives rounded
     float K[64 * 128];             // swizzled
-    float U[64 * kSlice];          // U~ slice: two swizzled 64 x 32 boxes
+    float U[64 * 64];              // U~ columns a0 .. a0 + 63: two swizzled 64 x 32 boxes
     float gam[256];                // 64 used
 };
 constexpr int kStageFloats = (int)(sizeof(StateStage) / sizeof(float));
 static_assert(sizeof(StateStage) % 1024 == 0, "stage alignment");
 constexpr size_t kStateSmem =
-    sizeof(float) * (2 * kStageFloats + kSlice * kD + kSlice * 64) + 2 * 8 + 1024;
+    sizeof(float) * (2 * kStageFloats + kSliceMax * kD + kSliceMax * 64 + 64 * 8) + 2 * 8 +
+    1024;
 
-__global__ void __launch_bounds__(256, 1)
-state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const float* S_init,
-                 float* S_final, FwdSaved sv) {
-    extern __shared__ float sm_raw[];
-    float* sm = umma::align1024(sm_raw);
+template <int SW>
+__device__ __forceinline__ void state_fwd_slice(const TileMaps& maps, int hk, int hv, int a0,
+                                                const float* S_init, float* S_final,
+                                                const FwdSaved& sv, float* sm) {
     StateStage* stage = reinterpret_cast<StateStage*>(sm);
-    float* St = sm + 2 * kStageFloats;      // [64 (a)][128 (b)] K-major, rounded
-    float* Ub = St + kSlice * kD;           // [64 (a)][64 (i)] K-major: fk_i U[i][a], rounded
-    uint64_t* mb = reinterpret_cast<uint64_t*>(Ub + kSlice * 64);   // [2] stage barriers
-    const int sl = blockIdx.x, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
-    const int a0 = sl * kSlice, kh = h / (hv / hk);
-    using TS = Tile<kD, kSlice, 8>;    // S^T: rows b (d_k), cols a (slice)
-    using TU = Tile<64, kSlice, 8>;
+    float* St = sm + 2 * kStageFloats;      // [SW (a)][128 (b)] K-major, rounded
+    float* Ub = St + kSliceMax * kD;        // [SW (a)][64 (i)] K-major: fk_i U[i][a], rounded
+    // (the ldmatrix pair loads of an odd n-block count read up to 8 rows past St
+    // and Ub: the padding keeps them inside shared memory)
+    uint64_t* mb = reinterpret_cast<uint64_t*>(Ub + kSliceMax * 64 + 64 * 8);   // [2]
+    const int h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
+    const int kh = h / (hv / hk);
+    constexpr int NB = (SW + 31) / 32;      // U~ boxes of 32 columns
+    using TS = Tile<kD, SW, 8>;    // S^T: rows b (d_k), cols a (slice)
+    using TU = Tile<64, SW, 8>;
     typename TS::Acc sacc;
     const int64_t sbase = ((int64_t)n * hv + h) * kD * kD;
     if (tid == 0) {
         umma::mbar_init(&mb[0], 1);
         umma::mbar_init(&mb[1], 1);
     }
-    tile_each2<kD, kSlice, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
+    tile_each2<kD, SW, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
         v0 = S_init ? S_init[sbase + (int64_t)(a0 + a) * kD + b] : 0.f;
         v1 = S_init ? S_init[sbase + (int64_t)(a0 + a + 1) * kD + b] : 0.f;
         St[umma::kidx(a, b, kD)] = umma::tf32r(v0);
@@ -316,11 +320,13 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
     const int c0 = sv.seq_chunk[n], c1 = sv.seq_chunk[n + 1];
     auto issue = [&](int s, const ChunkInfo& info) {   // tiles: one thread; gates: 64
         if (tid == 0) {
-            umma::mbar_expect_tx(&mb[s], (2 * 64 * 128 + 64 * kSlice) * 4);
+            umma::mbar_expect_tx(&mb[s], (2 * 64 * 128 + NB * 64 * 32) * 4);
             umma::tma_rows(stage[s].W, 64, &maps.W, h, info.start, &mb[s]);
             umma::tma_rows(stage[s].K, 64, &maps.k, kh, info.start, &mb[s]);
-            umma::tma_box(stage[s].U, &maps.U, a0, h, info.start, &mb[s]);
-            umma::tma_box(stage[s].U + 64 * 32, &maps.U, a0 + 32, h, info.start, &mb[s]);
+#pragma unroll
+            for (int bx = 0; bx < NB; bx++)
+                umma::tma_box(stage[s].U + bx * 64 * 32, &maps.U, a0 + 32 * bx, h, info.start,
+                              &mb[s]);
         }
         if (tid < 64)   // gate rows start at any token: 4-byte copies
             cp_async4(stage[s].gam + tid,
@@ -344,14 +350,14 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         }
         // chunk-start state in the layout with rows b (exact), from the accumulators
         const int64_t obase = ((int64_t)ci * hv + h) * kD * kD;
-        tile_each2<kD, kSlice, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
+        tile_each2<kD, SW, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
             *reinterpret_cast<float2*>(sv.S0b + obase + umma::kidx(b, a0 + a, kD)) =
                 make_float2(v0, v1);
         });
         ok = __syncthreads_and(umma::mbar_wait(&mb[s], ((ci - c0) >> 1) & 1));
         if (!ok) break;
         if (tid == 0) {   // ... and with rows a (rounded; an MMA operand only): St whole
-            umma::bulk_store(sv.S0 + obase + (int64_t)a0 * kD, St, kSlice * kD * 4);
+            umma::bulk_store(sv.S0 + obase + (int64_t)a0 * kD, St, SW * kD * 4);
             umma::bulk_commit();
         }
         const float gL = cur.gam[L - 1];
@@ -359,16 +365,16 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         const float f1 = rg + 8 < L ? expf(gL - cur.gam[rg + 8]) : 0.f;
         // U = U~ - W S^T   (64 x slice)
         typename TU::Acc uacc;
-        tile_zero<64, kSlice, 8>(uacc);
-        tile_mma_frag<64, kSlice, kD, 8>(
+        tile_zero<64, SW, 8>(uacc);
+        tile_mma_frag<64, SW, kD, 8>(
             uacc,
             [&](int r0, int k0, uint32_t(&f)[4]) {
                 ldsm_a(f, r0, k0, [&](int r, int c) { return cur.W + umma::swz(r, c, 64); });
             },
             [&](int k0, int n0, uint32_t(&f)[4]) {
-                ldsm_b2(f, k0, n0, [&](int n, int k) { return St + umma::kidx(n, k, kD); });
+                ldsm_b2(f, k0, n0, [&](int nn, int k) { return St + umma::kidx(nn, k, kD); });
             });
-        tile_each2<64, kSlice, 8>(uacc, [&](int i, int a, float& v0, float& v1) {
+        tile_each2<64, SW, 8>(uacc, [&](int i, int a, float& v0, float& v1) {
             float u0 = 0.f, u1 = 0.f;
             if (i < L) {
                 const float2 ut = *reinterpret_cast<const float2*>(cur.U + umma::swz(i, a, 64));
@@ -385,8 +391,8 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         __syncthreads();   // Ub complete
         // S^T = e^{gam_L} S^T + K^T (diag(fk) U)
         const float dl = expf(gL);
-        tile_each<kD, kSlice, 8>(sacc, [&](int, int, float& v) { v *= dl; });
-        tile_mma_frag<kD, kSlice, 64, 8>(
+        tile_each<kD, SW, 8>(sacc, [&](int, int, float& v) { v *= dl; });
+        tile_mma_frag<kD, SW, 64, 8>(
             sacc,
             [&](int r0, int k0, uint32_t(&f)[4]) {   // A(b, i) = K[i][b]: element loads
                 const int g = lane >> 2, t = lane & 3;
@@ -396,11 +402,11 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
                 f[3] = f2tf32(cur.K[umma::swz(k0 + t + 4, r0 + g + 8, 64)]);
             },
             [&](int k0, int n0, uint32_t(&f)[4]) {
-                ldsm_b2(f, k0, n0, [&](int n, int k) { return Ub + umma::kidx(n, k, 64); });
+                ldsm_b2(f, k0, n0, [&](int nn, int k) { return Ub + umma::kidx(nn, k, 64); });
             });
         if (tid == 0) umma::bulk_wait_read();   // the chunk-start copy has read St
         __syncthreads();   // reads of cur, St and Ub are done
-        tile_each2<kD, kSlice, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
+        tile_each2<kD, SW, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
             St[umma::kidx(a, b, kD)] = umma::tf32r(v0);
             St[umma::kidx(a + 1, b, kD)] = umma::tf32r(v1);
         });
@@ -411,9 +417,20 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         return;
     }
     if (S_final)
-        tile_each<kD, kSlice, 8>(sacc, [&](int b, int a, float& v) {
+        tile_each<kD, SW, 8>(sacc, [&](int b, int a, float& v) {
             S_final[sbase + (int64_t)(a0 + a) * kD + b] = v;
         });
+}
+
+__global__ void __launch_bounds__(256, 1)
+state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const float* S_init,
+                 float* S_final, FwdSaved sv) {
+    extern __shared__ float sm_raw[];
+    float* sm = umma::align1024(sm_raw);
+    if (blockIdx.x < 2)
+        state_fwd_slice<48>(maps, hk, hv, 48 * (int)blockIdx.x, S_init, S_final, sv, sm);
+    else
+        state_fwd_slice<32>(maps, hk, hv, 96, S_init, S_final, sv, sm);
 }
 
 // ------------------------------------------------------------------ output + norm
@@ -624,7 +641,7 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
     }
     if (a.N > 0) {
         GDN_PROF("chunk_state_fwd", st);
-        state_fwd_kernel<<<dim3(kD / kSlice, a.hv, a.N), 256, kStateSmem, st>>>(
+        state_fwd_kernel<<<dim3(3, a.hv, a.N), 256, kStateSmem, st>>>(
             maps, a.hk, a.hv, a.S_init, a.S_final, a.sv);
     }
     if (a.NT > 0) {

@@ -200,11 +200,12 @@ __device__ __forceinline__ void ldsm_b2(uint32_t (&b)[4], int k0, int n0, F addr
 // acc += A * B with whole fragments supplied by the caller: fa(r0, k0, a[4])
 // fills the A fragment of rows r0 .. r0 + 15, fb(k0, n0, b[4]) the B fragments
 // of the two n-blocks n0 and n0 + 8 (as tf32 bit patterns), so operands in
-// fragment-friendly layouts load with ldmatrix.
+// fragment-friendly layouts load with ldmatrix.  With an odd number of n-blocks
+// per warp the last call reads one block past the warp's columns (the caller's
+// address function must stay inside shared memory there); it is not used.
 template <int M, int N, int K, int NW, class FA, class FB>
 __device__ __forceinline__ void tile_mma_frag(typename Tile<M, N, NW>::Acc& acc, FA fa, FB fb) {
     using C = Tile<M, N, NW>;
-    static_assert(C::NPW % 2 == 0, "pairs of n-blocks");
     const int m0 = C::m0(), n0 = C::n0();
 #pragma unroll 2
     for (int k0 = 0; k0 < K; k0 += 8) {
@@ -212,14 +213,14 @@ __device__ __forceinline__ void tile_mma_frag(typename Tile<M, N, NW>::Acc& acc,
 #pragma unroll
         for (int i = 0; i < C::MPW; i++) fa(m0 + i * 16, k0, af[i]);
 #pragma unroll
-        for (int j = 0; j < C::NPW; j += 2) {
+        for (int j = 0; j < C::NPW; j += 2) {   // an odd count loads one block more, unused
             uint32_t bf[4];
             fb(k0, n0 + j * 8, bf);
             const uint32_t b0[2] = {bf[0], bf[1]}, b1[2] = {bf[2], bf[3]};
 #pragma unroll
             for (int i = 0; i < C::MPW; i++) {
                 mma_tf32(acc[i][j], af[i], b0);
-                mma_tf32(acc[i][j + 1], af[i], b1);
+                if (j + 1 < C::NPW) mma_tf32(acc[i][j + 1], af[i], b1);
             }
         }
     }
