@@ -80,22 +80,23 @@ chunk_norm_bwd_kernel(const float* __restrict__ o, const IO* __restrict__ z,
 // grid (NT, Hv), 256 threads, tcgen05.
 //   D1 = K Q^T (64 x 64)  ->  P^T[j][i] = D1[j][i] e^{gam_i-gam_j} [i >= j]
 //   D2 = P^T dO           ->  dU_local (64 x 128)
-// Shared memory: Q, K, dO swizzled 32 KB each (TMA), dO^T (rows a, k = token)
-// 32 KB, P^T 16 KB.  Tensor memory: 192 fp32 columns (256 allocated).
-constexpr int kB1Floats = 64 * 128 * 3 + 128 * 64 + 64 * 64;
+// Shared memory: Q, K swizzled and dO MN-major, 32 KB each (TMA; dO is the B
+// operand of P^T dO, contracted over tokens, so it is read as loaded); P^T
+// (16 KB) takes the K space once K Q^T is done.  About 97 KB: two CTAs per SM.
+// Tensor memory: 192 fp32 columns (256 allocated).
+constexpr int kB1Floats = 64 * 128 * 3;
 constexpr size_t kB1Smem = sizeof(float) * (kB1Floats + 64 + 16) + 64 + 1024;
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, 2)
 bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv,
                  BwdScratch w) {
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
     float* Qs = sm;                    // [64][128] swizzled
     float* Ks = Qs + 64 * 128;         // [64][128] swizzled
-    float* dOs = Ks + 64 * 128;        // [64][128] swizzled dO (arrives rounded)
-    float* dOT = dOs + 64 * 128;       // [128 (a)][64 (i)] K-major
-    float* PT = dOT + 128 * 64;        // [64 (j)][64 (i)] K-major
-    float* gam = PT + 64 * 64;
+    float* dOs = Ks + 64 * 128;        // [64 (i)][128 (a)] MN-major dO (arrives rounded)
+    float* PT = Ks;                    // [64 (j)][64 (i)] K-major, after K Q^T
+    float* gam = dOs + 64 * 128;
     uint64_t* mbar = reinterpret_cast<uint64_t*>(gam + 64 + 16);
     uint64_t* mbl = mbar + 1;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
@@ -109,7 +110,7 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
         umma::mbar_expect_tx(mbl, 3 * 64 * 128 * 4);
         umma::tma_rows(Qs, 64, &maps.q, kh, ci.start, mbl);
         umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
-        umma::tma_rows(dOs, 64, &maps.dO, h, ci.start, mbl);
+        umma::tma_rows(dOs, 64, &maps.dO_mn, h, ci.start, mbl);
     }
     load_gam(gam, sv, ci, h);
     if (warp == 0) umma::tmem_alloc(tslot, 256);
@@ -122,7 +123,6 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
         __syncthreads();
     }
     umma::tf32r_inplace(Qs, 2 * 64 * 128);
-    umma::transpose_sw_to_kmajor(dOT, dOs, nullptr);   // dO^T: rows a, k = token
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -158,7 +158,7 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
     __syncthreads();
     umma::fence_after_sync();
     if (ok && tid == 0) {
-        umma::mma_tf32(tD2, PT, 64, dOT, 64, 64, 128, 64, false);
+        umma::mma(tD2, umma::kmaj(PT, 64), umma::mnt(dOs), 64, 128, 64, false);
         umma::commit(mbar);
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
@@ -1195,6 +1195,13 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
         if (e == cudaSuccess) e = make_rows_map(&maps.dO, w.dO, a.hv, a.T, vs);
         if (e == cudaSuccess) e = make_rows_map(&maps.dU, w.dU, a.hv, a.T, vs);
         if (e == cudaSuccess) e = make_rows_map(&maps.dW, w.dW, a.hv, a.T, vs);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dO_mn, w.dO, a.hv, a.T, vs, true);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dU_mn, w.dU, a.hv, a.T, vs, true);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dW_mn, w.dW, a.hv, a.T, vs, true);
+        if (e == cudaSuccess)
+            e = make_rows_map(&maps.k_mn, a.qkv + (int64_t)a.hk * kD, a.hk, a.T, C, true);
+        if (e == cudaSuccess)
+            e = make_rows_map(&maps.q_mn, a.qkv, a.hk, a.T, C, true);
         if (e == cudaSuccess) e = make_rows_map(&maps.dQv, w.dQv, a.hv, a.T, vs);
         if (e == cudaSuccess) e = make_rows_map(&maps.dKv, w.dKv, a.hv, a.T, vs);
         if (e == cudaSuccess) e = make_rows_map(&maps.dQv2, w.dQv2, a.hv, a.T, vs);

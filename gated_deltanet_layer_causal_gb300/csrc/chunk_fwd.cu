@@ -439,10 +439,11 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
 //   P  = D1 (.) e^{gam_i - gam_j} (.) [i >= j]          -- staged K-major
 //   D2 = P U (64 x 128)
 //   O  = D2 + e^{gam_i} D3 ; y = O rsqrt(mean(O^2)+eps) (1+w) silu(z)
-// Shared memory: Q, K, U swizzled 32 KB each (TMA), S0 (K-major rows a) 64 KB
-// (one bulk copy), U^T (rows a, k = token) 32 KB, P 16 KB; the z rows reuse the
-// U space.  Tensor memory: 320 fp32 columns.
-constexpr int kOutFloats = 64 * 128 * 2 + 128 * 128 + 128 * 64 + 64 * 64 + 64 * kLdK;
+// Shared memory: Q, K swizzled 32 KB each and U MN-major 32 KB (TMA; U is the
+// B operand of P U, contracted over tokens, so it is read as loaded), S0
+// (K-major rows a) 64 KB (one bulk copy), P 16 KB, the z rows 33 KB.  Tensor
+// memory: 320 fp32 columns.
+constexpr int kOutFloats = 64 * 128 * 2 + 128 * 128 + 64 * 128 + 64 * 64 + 64 * kLdK;
 constexpr size_t kOutSmem = sizeof(float) * (kOutFloats + 64 * 2 + 2 * 64 + 16) + 64 + 1024;
 
 template <class IO>
@@ -454,10 +455,10 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO* 
     float* Qs = sm;                    // [64][128] swizzled
     float* Ks = Qs + 64 * 128;         // [64][128] swizzled
     float* Ss = Ks + 64 * 128;         // [128 (a)][128 (b)] K-major
-    float* UT = Ss + 128 * 128;        // [128 (a)][64 (j)] K-major
-    float* Ps = UT + 128 * 64;         // [64 (i)][64 (j)] K-major
-    float* Us = Ps + 64 * 64;          // [64][128] swizzled U (then the z rows)
-    float* gam = Us + 64 * kLdK;
+    float* Us = Ss + 128 * 128;        // [64 (j)][128 (a)] MN-major U (arrives rounded)
+    float* Ps = Us + 64 * 128;         // [64 (i)][64 (j)] K-major
+    char* Zs = reinterpret_cast<char*>(Ps + 64 * 64);   // z rows, kZPitch bytes apart
+    float* gam = Ps + 64 * 64 + 64 * kLdK;
     float* eg = gam + 64;
     float* ssq = eg + 64;              // [2][64] partial sums of squares
     uint64_t* mbar = reinterpret_cast<uint64_t*>(ssq + 2 * 64 + 16);
@@ -474,7 +475,7 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO* 
         umma::mbar_expect_tx(mbl, 3 * 64 * 128 * 4 + 128 * 128 * 4);
         umma::tma_rows(Qs, 64, &maps.q, kh, ci.start, mbl);
         umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
-        umma::tma_rows(Us, 64, &maps.U, h, ci.start, mbl);
+        umma::tma_rows(Us, 64, &maps.U_mn, h, ci.start, mbl);
         umma::bulk_load(Ss, sv.S0 + ((int64_t)blockIdx.x * hv + h) * kD * kD, 128 * 128 * 4, mbl);
     }
     if (tid < 64) {  // padding rows continue the last gate value (g = 0)
@@ -483,20 +484,7 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO* 
         eg[tid] = tid < L ? expf(g) : 0.f;
     }
     if (warp == 0) umma::tmem_alloc(tslot, 512);
-    __syncthreads();
-    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
-    if (L < 64) {   // tail rows belong to the next sequence
-        umma::zero_tail_rows(Qs, 64, 0, L);
-        umma::zero_tail_rows(Ks, 64, 0, L);
-        umma::zero_tail_rows(Us, 64, 0, L);
-        __syncthreads();
-    }
-    umma::tf32r_inplace(Qs, 64 * 128 * 2);   // Q, K (S0 and U arrive rounded)
-    umma::transpose_sw_to_kmajor(UT, Us, nullptr);
-    __syncthreads();
-    // U is transposed: its space takes the z rows for the norm epilogue
     constexpr int kZPitch = kD * (int)sizeof(IO) + 16;    // bytes; conflict-free row reads
-    char* Zs = reinterpret_cast<char*>(Us);
     if (z) {
         constexpr int kPieces = kD * (int)sizeof(IO) / 16;
         for (int idx = tid; idx < 64 * kPieces; idx += 256) {
@@ -506,6 +494,15 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO* 
         }
     }
     cp_async_commit();
+    __syncthreads();
+    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
+    if (L < 64) {   // tail rows belong to the next sequence
+        umma::zero_tail_rows(Qs, 64, 0, L);
+        umma::zero_tail_rows(Ks, 64, 0, L);
+        umma::zero_tail_rows(Us, 64, 0, L);
+        __syncthreads();
+    }
+    umma::tf32r_inplace(Qs, 64 * 128 * 2);   // Q, K (S0 and U arrive rounded)
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -543,7 +540,7 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO* 
     __syncthreads();
     umma::fence_after_sync();
     if (ok && tid == 0) {
-        umma::mma_tf32(tD2, Ps, 64, UT, 64, 64, 128, 64, false);
+        umma::mma(tD2, umma::kmaj(Ps, 64), umma::mnt(Us), 64, 128, 64, false);
         umma::commit(mbar);
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
@@ -635,6 +632,8 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
             e = make_rows_map(&maps.v, a.qkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C);
         if (e == cudaSuccess) e = make_rows_map(&maps.U, a.sv.U, a.hv, a.T, (int64_t)a.hv * kD);
         if (e == cudaSuccess) e = make_rows_map(&maps.W, a.sv.W, a.hv, a.T, (int64_t)a.hv * kD);
+        if (e == cudaSuccess)
+            e = make_rows_map(&maps.U_mn, a.sv.U, a.hv, a.T, (int64_t)a.hv * kD, true);
         if (e != cudaSuccess) return e;
         GDN_PROF("chunk_prep", st);
         prep_kernel<<<dim3(a.NT, a.hv), 256, kPrepSmem, st>>>(maps, a.hk, a.hv, a.sv);

@@ -51,7 +51,10 @@ struct FwdSaved {
 };
 
 // Tensor maps of the row tensors the chunk kernels load as 64 x 128 tiles
-// (3-D: {128 columns, heads, tokens}, 64 x 32 boxes, 128-byte swizzle).
+// (3-D: {128 columns, heads, tokens}, 64 x 32 boxes).  The K-major maps use the
+// 128-byte swizzle with 16-byte atoms; the *_mn maps the 128-byte swizzle with
+// 32-byte atoms, the layout in which the tensor core reads a tile whose rows
+// (tokens) are the contraction dimension -- an MN-major operand.
 constexpr int kTileCols = 128;
 struct TileMaps {
     CUtensorMap q, k, v;   // q / k / v channels of the conv output [T, C]
@@ -59,9 +62,10 @@ struct TileMaps {
     CUtensorMap dO, dU, dW;
     CUtensorMap dQv, dKv, dQv2, dKv2, dKv3;
     CUtensorMap dv;        // v channels of the conv-output gradient [T, C]
+    CUtensorMap q_mn, k_mn, v_mn, U_mn, dO_mn, dU_mn, dW_mn;
 };
 cudaError_t make_rows_map(CUtensorMap* m, const float* base, int heads, int64_t T,
-                          int64_t token_stride);
+                          int64_t token_stride, bool mn_major = false);
 
 struct ChunkArgs {
     bool bf16;

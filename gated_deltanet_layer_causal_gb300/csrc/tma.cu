@@ -30,7 +30,7 @@ EncodeTiled encoder() {
 }  // namespace
 
 cudaError_t make_rows_map(CUtensorMap* m, const float* base, int heads, int64_t T,
-                          int64_t token_stride) {
+                          int64_t token_stride, bool mn_major) {
     const EncodeTiled enc = encoder();
     if (enc == nullptr) return cudaErrorNotSupported;
     const cuuint64_t dims[3] = {(cuuint64_t)kTileCols, (cuuint64_t)heads, (cuuint64_t)T};
@@ -40,7 +40,9 @@ cudaError_t make_rows_map(CUtensorMap* m, const float* base, int heads, int64_t 
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims,
                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           mn_major ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B
+                                    : CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

@@ -66,17 +66,37 @@ __device__ __forceinline__ uint64_t desc_sw(const float* tile, int rows, int k0)
     return d;
 }
 
+// MN-major tile: 64 rows of the contraction dimension (tokens) x 128 columns,
+// four boxes of [64][32] in the 128-byte swizzle with 32-byte atoms (32-byte
+// chunk c of row r sits at chunk c ^ (r % 4)).  The tensor core reads K = 8 rows
+// per step as two 4-row groups 512 B apart, 32-column atoms one box (8 KB)
+// apart: layout type 1, start address 1 KB-aligned at every step.
+__device__ __forceinline__ uint64_t desc_mn(const float* tile, int k0) {
+    const uint32_t a = saddr(tile) + (uint32_t)(k0 >> 3) * 1024u;
+    uint64_t d = (uint64_t)((a >> 4) & 0x3FFFu);
+    d |= (uint64_t)((64u * 128u) >> 4) << 16;   // leading byte offset: next 32-column atom
+    d |= (uint64_t)(512u >> 4) << 32;           // stride byte offset: next 4-row group
+    d |= (uint64_t)1 << 46;                     // descriptor version
+    d |= (uint64_t)1 << 61;                     // 128-byte swizzle, 32-byte atoms
+    return d;
+}
+// Float offset of element (r, c) of an MN-major tile.
+__device__ __forceinline__ int swz_mn(int r, int c) {
+    return ((c >> 5) * 64 + r) * 32 + ((((c >> 3) & 3) ^ (r & 3)) << 3) + (c & 7);
+}
+
 // An MMA operand in shared memory: a no-swizzle K-major tile (n = its K
-// extent) or a swizzled tile (n = its row count).
+// extent), a swizzled K-major tile (n = its row count) or an MN-major tile.
 struct Op {
     const float* p;
     int n;
-    bool sw;
+    int kind;   // 0 no-swizzle K-major, 1 swizzled K-major, 2 MN-major
 };
-__device__ __forceinline__ Op kmaj(const float* p, int kd) { return Op{p, kd, false}; }
-__device__ __forceinline__ Op swt(const float* p, int rows) { return Op{p, rows, true}; }
+__device__ __forceinline__ Op kmaj(const float* p, int kd) { return Op{p, kd, 0}; }
+__device__ __forceinline__ Op swt(const float* p, int rows) { return Op{p, rows, 1}; }
+__device__ __forceinline__ Op mnt(const float* p) { return Op{p, 64, 2}; }
 __device__ __forceinline__ uint64_t opdesc(const Op& o, int k0) {
-    return o.sw ? desc_sw(o.p, o.n, k0) : desc(o.p, k0, o.n);
+    return o.kind == 2 ? desc_mn(o.p, k0) : o.kind == 1 ? desc_sw(o.p, o.n, k0) : desc(o.p, k0, o.n);
 }
 
 // Instruction descriptor: D fp32, A and B tf32, both K-major, M x N.
@@ -103,7 +123,8 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, const float* A, int ld
 // The same for operands of either layout.
 __device__ __forceinline__ void mma(uint32_t d_tmem, const Op& A, const Op& B, int M, int N, int K,
                                     bool accumulate) {
-    const uint32_t id = idesc_tf32(M, N);
+    const uint32_t id = idesc_tf32(M, N) | (A.kind == 2 ? 1u << 15 : 0u) |
+                        (B.kind == 2 ? 1u << 16 : 0u);   // MN-major ("transposed") operands
     for (int k0 = 0; k0 < K; k0 += 8) {
         const uint64_t ad = opdesc(A, k0), bd = opdesc(B, k0);
         const uint32_t acc = (accumulate || k0 > 0) ? 1u : 0u;
