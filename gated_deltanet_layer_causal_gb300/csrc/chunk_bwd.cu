@@ -731,8 +731,9 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     float* Vs = Ks + 64 * 128;
     float* dWs = Vs + 64 * 128;
     float* dUs = dWs + 64 * 128;
-    float* BW = dUs + 64 * 128;        // [256][64] K-major: dW^T rows b, dU^T rows 128 + a
-    float* TC = BW + 256 * 64;         // [64 (j)][64 (i)] K-major T^T (kept to the end)
+    float* dWm = dUs + 64 * 128;       // [64 (j)][128 (b)] MN-major dW (arrives rounded)
+    float* dUm = dWm + 64 * 128;       // [64 (j)][128 (a)] MN-major dU (arrives rounded)
+    float* TC = dUm + 64 * 128;        // [64 (j)][64 (i)] K-major T^T (kept to the end)
     // stage 2 overlays dW, dU and [dW^T ; dU^T] once the first products are
     // complete; K and V stay for the epilogue's dot products (R later over V)
     float* GKK = dWs;                  // [64][64] K-major Gam (.) KK (strict lower)
@@ -741,7 +742,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     float* YT = TR + 64 * 64;          // [64 (m)][64 (i)] K-major Y^T
     float* dKR = YT + 64 * 64;         // [64 (j)][64 (m)] K-major dKK
     float* dKC = dKR + 64 * 64;        // [64 (j)][64 (m)] K-major dKK^T
-    float* KT = dKC + 64 * 64;         // [128 (b)][64 (m)] K-major K^T
+    float* Km = dKC + 64 * 64;         // [64 (m)][128 (b)] MN-major K (over dU_mn, after stage 1)
     float* Rm = Vs;                    // [64][65] row-major
     float* gam = TC + 64 * 64;
     float* eg = gam + 64;
@@ -767,11 +768,13 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     if (tid == 0) {   // row tiles through the TMA; T^T, written by the forward, whole
         umma::mbar_init(mbar, 1);
         umma::mbar_init(mbl, 1);
-        umma::mbar_expect_tx(mbl, 4 * 64 * 128 * 4 + 64 * 64 * 4);
+        umma::mbar_expect_tx(mbl, 6 * 64 * 128 * 4 + 64 * 64 * 4);
         umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
         umma::tma_rows(Vs, 64, &maps.v, h, ci.start, mbl);
         umma::tma_rows(dWs, 64, &maps.dW, h, ci.start, mbl);
         umma::tma_rows(dUs, 64, &maps.dU, h, ci.start, mbl);
+        umma::tma_rows(dWm, 64, &maps.dW_mn, h, ci.start, mbl);
+        umma::tma_rows(dUm, 64, &maps.dU_mn, h, ci.start, mbl);
         umma::bulk_load(TC, Tg + 64 * 64, 64 * 64 * 4, mbl);
     }
     load_gam(gam, sv, ci, h);
@@ -801,12 +804,12 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         umma::zero_tail_rows(Vs, 64, 0, L);
         umma::zero_tail_rows(dWs, 64, 0, L);
         umma::zero_tail_rows(dUs, 64, 0, L);
+        umma::zero_tail_rows(dWm, 64, 0, L);
+        umma::zero_tail_rows(dUm, 64, 0, L);
         __syncthreads();
     }
     umma::tf32r_inplace(Ks, 2 * 64 * 128);   // K, V (dW, dU and T^T arrive rounded)
     __syncthreads();
-    umma::transpose_sw_to_kmajor(BW, dWs, nullptr);   // [dW^T ; dU^T]: rows b, k = token
-    umma::transpose_sw_to_kmajor(BW + 128 * 64, dUs, nullptr);
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -819,15 +822,17 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         umma::mma(tKK, umma::swt(Ks, 64), umma::swt(Ks, 64), 64, 64, 128, false);
         umma::mma(tDT1, umma::swt(dWs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
         umma::mma(tDT2, umma::swt(dUs, 64), umma::swt(Vs, 64), 64, 64, 128, false);
-        umma::mma_tf32(tTW, TC, 64, BW, 64, 64, 256, 64, false);
+        umma::mma(tTW, umma::kmaj(TC, 64), umma::mnt(dWm), 64, 128, 64, false);
+        umma::mma(tTW + 128, umma::kmaj(TC, 64), umma::mnt(dUm), 64, 128, 64, false);
         umma::commit(mbar);
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
-    // dW, dU and their transposes are consumed: fetch T for stage 2
+    // dW, dU (both layouts) are consumed: fetch T and K as an MN-major tile for stage 2
     if (ok && tid == 0) {
-        umma::mbar_expect_tx(mbl, 64 * 64 * 4);
+        umma::mbar_expect_tx(mbl, 64 * 64 * 4 + 64 * 128 * 4);
         umma::bulk_load(TR, Tg, 64 * 64 * 4, mbl);
+        umma::tma_rows(Km, 64, &maps.k_mn, kh, ci.start, mbl);
     }
     const int win = warp & 3, half = warp >> 2;
     const int rl = umma::frag_row_lo(), cf = umma::frag_col();   // fragment rows rl, rl + 8
@@ -889,9 +894,13 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         dbs[tid] += eg[tid] * rp[tid] + rp[64 + tid];
         dgs[tid] += be[tid] * rp[tid];
     }
-    // stage 2 operands: T arrived as a K-major tile; K^T from the K tile
+    // stage 2 operands: T arrived as a K-major tile, K as an MN-major tile
     ok = __syncthreads_and(ok && umma::mbar_wait(mbl, 1));
-    umma::transpose_sw_to_kmajor(KT, Ks, nullptr);
+    if (L < 64) {
+        umma::zero_tail_rows(Km, 64, 0, L);
+        __syncthreads();
+    }
+    umma::tf32r_inplace(Km, 64 * 128);
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
@@ -970,8 +979,8 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     __syncthreads();
     umma::fence_after_sync();
     if (ok && tid == 0) {
-        umma::mma_tf32(tX, dKR, 64, KT, 64, 64, 128, 64, false);    // dKK K
-        umma::mma_tf32(tX, dKC, 64, KT, 64, 64, 128, 64, true);     // + dKK^T K
+        umma::mma(tX, umma::kmaj(dKR, 64), umma::mnt(Km), 64, 128, 64, false);   // dKK K
+        umma::mma(tX, umma::kmaj(dKC, 64), umma::mnt(Km), 64, 128, 64, true);    // + dKK^T K
         umma::commit(mbar);
     }
     if (tid < 64) {

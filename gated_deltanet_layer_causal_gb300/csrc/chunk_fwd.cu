@@ -116,24 +116,26 @@ gates_kernel(const IO* __restrict__ av, const IO* __restrict__ bv, const float* 
 // grid (NT, Hv), 256 threads, tcgen05.  With the gates from gates_kernel,
 //   D1 = K K^T (64 x 64)  ->  A = beta_i e^{gam_i-gam_j} D1 (j < i)
 //   T  = (I + A)^-1        (forward substitution on the CUDA cores; saved)
-//   D2 = T [diag(beta e^gam) K | diag(beta) V]   (one M=64, N=256, K=64 MMA)
-// giving W = D2[:, :128] and U~ = D2[:, 128:].  K and V arrive as swizzled
-// tiles through the TMA; the B operand of D2 is transposed out of them.
+//   W = (T diag(beta e^gam)) K,  U~ = (T diag(beta)) V      (M=64, N=128, K=64 each)
+// K arrives twice through the TMA, as a K-major tile for K K^T and as an
+// MN-major tile for W (contracted over tokens), V once, MN-major; the gate
+// scalings go into the two A tiles, so no tile is transposed.
 constexpr int kLdK = 132, kLdA = 68;
-constexpr int kPrepFloats = 2 * 64 * 128 + 256 * 64 + 2 * 64 * kLdA + 64 * 64;
+constexpr int kPrepFloats = 3 * 64 * 128 + 2 * 64 * kLdA + 2 * 64 * 64;
 constexpr size_t kPrepSmem = sizeof(float) * (kPrepFloats + 3 * 64 + 16) + 64 + 1024;
 
 __global__ void __launch_bounds__(256, 1)
 prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv) {
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
-    float* Ks = sm;                    // [64][128] swizzled
-    float* Vs = Ks + 64 * 128;         // [64][128] swizzled
-    float* Bs = Vs + 64 * 128;         // [256 (c | a)][64 (j)] K-major: (be K)^T ; (beta V)^T
-    float* As = Bs + 256 * 64;         // [64][kLdA] row-major A
+    float* Ks = sm;                    // [64][128] swizzled K-major K
+    float* Km = Ks + 64 * 128;         // [64 (j)][128 (c)] MN-major K
+    float* Vm = Km + 64 * 128;         // [64 (j)][128 (a)] MN-major V
+    float* As = Vm + 64 * 128;         // [64][kLdA] row-major A
     float* Tr = As + 64 * kLdA;        // [64][kLdA] row-major T
-    float* Tk = Tr + 64 * kLdA;        // [64][64] K-major T
-    float* gam = Tk + 64 * 64;
+    float* Tk = Tr + 64 * kLdA;        // [64][64] K-major T diag(beta e^gam)
+    float* Tv = Tk + 64 * 64;          // [64][64] K-major T diag(beta)
+    float* gam = Tv + 64 * 64;
     float* bet = gam + 64;
     float* be = bet + 64;
     uint64_t* mbar = reinterpret_cast<uint64_t*>(be + 64 + 16);
@@ -146,9 +148,10 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv) 
     if (tid == 0) {
         umma::mbar_init(mbar, 1);
         umma::mbar_init(mbl, 1);
-        umma::mbar_expect_tx(mbl, 2 * 64 * 128 * 4);
+        umma::mbar_expect_tx(mbl, 3 * 64 * 128 * 4);
         umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
-        umma::tma_rows(Vs, 64, &maps.v, h, ci.start, mbl);
+        umma::tma_rows(Km, 64, &maps.k_mn, kh, ci.start, mbl);
+        umma::tma_rows(Vm, 64, &maps.v_mn, h, ci.start, mbl);
     }
     if (tid < 64) {   // padding rows continue the last gam (g = 0), beta = 0
         const float gm = sv.gam[(int64_t)h * sv.T + ci.start + min(tid, L - 1)];
@@ -162,14 +165,11 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv) 
     bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
     if (L < 64) {   // tail rows belong to the next sequence
         umma::zero_tail_rows(Ks, 64, 0, L);
-        umma::zero_tail_rows(Vs, 64, 0, L);
+        umma::zero_tail_rows(Km, 64, 0, L);
+        umma::zero_tail_rows(Vm, 64, 0, L);
         __syncthreads();
     }
-    // B operand: rows c (0..127) = be_j K[j][c], rows 128 + a = beta_j V[j][a]
-    umma::transpose_sw_to_kmajor(Bs, Ks, be);
-    umma::transpose_sw_to_kmajor(Bs + 128 * 64, Vs, bet);
-    __syncthreads();
-    umma::tf32r_inplace(Ks, 64 * 128);
+    umma::tf32r_inplace(Ks, 3 * 64 * 128);   // K (both layouts), V
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -202,18 +202,21 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv) 
     __syncthreads();
     tril_inverse64(As, kLdA, Tr, kLdA, Tk);   // Tk doubles as scratch
     __syncthreads();
-    for (int idx = tid; idx < 64 * 16; idx += 256) {   // T -> K-major rows i
+    for (int idx = tid; idx < 64 * 16; idx += 256) {   // T diag(.) -> K-major rows i
         const int r = idx >> 4, c = (idx & 15) * 4;
+        const float4 t4 = *reinterpret_cast<const float4*>(Tr + r * kLdA + c);
         *reinterpret_cast<float4*>(Tk + umma::kidx(r, c, 64)) = umma::tf32r(
-            make_float4(Tr[r * kLdA + c], Tr[r * kLdA + c + 1], Tr[r * kLdA + c + 2],
-                        Tr[r * kLdA + c + 3]));
+            make_float4(t4.x * be[c], t4.y * be[c + 1], t4.z * be[c + 2], t4.w * be[c + 3]));
+        *reinterpret_cast<float4*>(Tv + umma::kidx(r, c, 64)) = umma::tf32r(
+            make_float4(t4.x * bet[c], t4.y * bet[c + 1], t4.z * bet[c + 2], t4.w * bet[c + 3]));
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     if (ok && tid == 0) {
-        umma::mma_tf32(tD2, Tk, 64, Bs, 64, 64, 256, 64, false);
+        umma::mma(tD2, umma::kmaj(Tk, 64), umma::mnt(Km), 64, 128, 64, false);
+        umma::mma(tD2 + 128, umma::kmaj(Tv, 64), umma::mnt(Vm), 64, 128, 64, false);
         umma::commit(mbar);
     }
     {   // T for the backward, as K-major rows i and as K-major rows j (T^T), rounded
@@ -232,7 +235,7 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv) 
     // warp half 0 -> W (columns 0..127), half 1 -> U~ (128..255), staged as
     // swizzled tiles in the K / V space (consumed) and stored whole
     if (ok) {
-        float* Sw = half == 0 ? Ks : Vs;
+        float* Sw = half == 0 ? Ks : Km;
         float v[32];
 #pragma unroll
         for (int c0 = 0; c0 < 128; c0 += 64) {
@@ -253,14 +256,14 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv) 
     if (L == 64) {
         if (tid == 0) {
             umma::tma_store_rows(&maps.W, h, ci.start, Ks);
-            umma::tma_store_rows(&maps.U, h, ci.start, Vs);
+            umma::tma_store_rows(&maps.U, h, ci.start, Km);
             umma::bulk_commit();
             umma::bulk_wait_read();
         }
     } else {
         const int64_t off = ((int64_t)ci.start * hv + h) * kD;
         umma::store_rows_sw(sv.W + off, (int64_t)hv * kD, Ks, L);
-        umma::store_rows_sw(sv.U + off, (int64_t)hv * kD, Vs, L);
+        umma::store_rows_sw(sv.U + off, (int64_t)hv * kD, Km, L);
     }
 }
 
@@ -634,6 +637,10 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
         if (e == cudaSuccess) e = make_rows_map(&maps.W, a.sv.W, a.hv, a.T, (int64_t)a.hv * kD);
         if (e == cudaSuccess)
             e = make_rows_map(&maps.U_mn, a.sv.U, a.hv, a.T, (int64_t)a.hv * kD, true);
+        if (e == cudaSuccess)
+            e = make_rows_map(&maps.k_mn, a.qkv + (int64_t)a.hk * kD, a.hk, a.T, C, true);
+        if (e == cudaSuccess)
+            e = make_rows_map(&maps.v_mn, a.qkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C, true);
         if (e != cudaSuccess) return e;
         GDN_PROF("chunk_prep", st);
         prep_kernel<<<dim3(a.NT, a.hv), 256, kPrepSmem, st>>>(maps, a.hk, a.hv, a.sv);
