@@ -546,8 +546,9 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSav
 //     dgam_i += sum_j R_ij, dgam_j -= sum_i R_ij
 //   D_dq = dPm K,  D_dk = dPm^T Q                        (64 x 128 each)
 // added to the per-v-head dQ / dK partials.  Shared memory: Q, K, dO, U
-// swizzled 32 KB each (TMA; dO, U later hold Q^T, K^T transposed out of the Q,
-// K tiles), dPm in both orientations 16 KB each, R 16 KB.  Tensor memory: 256
+// swizzled 32 KB each (TMA; once the first products are done, the dO / U space
+// takes Q and K again as MN-major tiles, the B operands of the products over
+// tokens), dPm in both orientations 16 KB each, R 16 KB.  Tensor memory: 256
 // fp32 columns (D_dq / D_dk reuse the columns of the first products).
 constexpr int kDpFloats = 4 * 64 * 128 + 2 * 64 * 64 + 64 * 65;
 constexpr size_t kDpSmem = sizeof(float) * (kDpFloats + 64 + 64 + 2 * 64 + 16) + 64 + 1024;
@@ -559,8 +560,8 @@ bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv
     float* sm = umma::align1024(sm_raw);
     float* Qs = sm;                    // [64][128] swizzled
     float* Ks = Qs + 64 * 128;         // [64][128] swizzled
-    float* dOs = Ks + 64 * 128;        // [64][128] swizzled   (later Q^T: [128][64] K-major)
-    float* Us = dOs + 64 * 128;        // [64][128] swizzled   (later K^T: [128][64] K-major)
+    float* dOs = Ks + 64 * 128;        // [64][128] swizzled   (later Q, MN-major)
+    float* Us = dOs + 64 * 128;        // [64][128] swizzled   (later K, MN-major)
     float* dPR = Us + 64 * 128;        // [64 (i)][64 (j)] K-major
     float* dPC = dPR + 64 * 64;        // [64 (j)][64 (i)] K-major
     float* Rm = dPC + 64 * 64;         // [64][65] row-major R
@@ -607,6 +608,15 @@ bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv
     }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
+    // dO and U are consumed: Q and K come again as MN-major tiles while the
+    // epilogue runs
+    float* Qm = dOs;
+    float* Km = Us;
+    if (ok && tid == 0) {
+        umma::mbar_expect_tx(mbl, 2 * 64 * 128 * 4);
+        umma::tma_rows(Qm, 64, &maps.q_mn, kh, ci.start, mbl);
+        umma::tma_rows(Km, 64, &maps.k_mn, kh, ci.start, mbl);
+    }
     const int win = warp & 3, half = warp >> 2;
     float* colp = Rm;                  // [4 row windows][64] column sums of R
     if (ok) {   // 32 columns per warp, all lanes; R row / column sums by shuffles
@@ -652,19 +662,20 @@ bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv
     }
     umma::fence_before_sync();
     __syncthreads();
-    // the first MMAs are done: Q^T and K^T (rows b, k = token) are transposed
-    // out of the Q and K tiles into the dO / U space
-    float* QT = dOs;
-    float* KT = Us;
-    umma::transpose_sw_to_kmajor(QT, Qs, nullptr);
-    umma::transpose_sw_to_kmajor(KT, Ks, nullptr);
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbl, 1));
+    if (L < 64) {
+        umma::zero_tail_rows(Qm, 64, 0, L);
+        umma::zero_tail_rows(Km, 64, 0, L);
+        __syncthreads();
+    }
+    umma::tf32r_inplace(Qm, 2 * 64 * 128);
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     if (ok && tid == 0) {
-        umma::mma_tf32(tDQ, dPR, 64, KT, 64, 64, 128, 64, false);
-        umma::mma_tf32(tDK, dPC, 64, QT, 64, 64, 128, 64, false);
+        umma::mma(tDQ, umma::kmaj(dPR, 64), umma::mnt(Km), 64, 128, 64, false);
+        umma::mma(tDK, umma::kmaj(dPC, 64), umma::mnt(Qm), 64, 128, 64, false);
         umma::commit(mbar);
     }
     if (tid < 64) {   // dgam from R: row sums minus column sums (fixed order)
