@@ -71,7 +71,43 @@ conv_fwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
     float4 h1 = conv_in(x, cs_in, t0 - 1, s, n, C, c);
     float4 h2 = conv_in(x, cs_in, t0 - 2, s, n, C, c);
     float4 h3 = conv_in(x, cs_in, t0 - 3, s, n, C, c);
-    for (int64_t t = t0; t < t1; t++) {
+    int64_t t = t0;
+    if (t1 <= e) {
+        // the whole run lies in one sequence: four tokens per step, loaded
+        // together, with independent reductions
+        for (; t + 4 <= t1; t += 4) {
+            float4 xs[4], o[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) xs[u] = ld4(x + (t + u) * C + c);
+            const float4 hw[7] = {h3, h2, h1, xs[0], xs[1], xs[2], xs[3]};   // x[t-3 .. t+3]
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                o[u].x = siluf_(conv4(wr[0], hw[u].x, hw[u + 1].x, hw[u + 2].x, hw[u + 3].x));
+                o[u].y = siluf_(conv4(wr[1], hw[u].y, hw[u + 1].y, hw[u + 2].y, hw[u + 3].y));
+                o[u].z = siluf_(conv4(wr[2], hw[u].z, hw[u + 1].z, hw[u + 2].z, hw[u + 3].z));
+                o[u].w = siluf_(conv4(wr[3], hw[u].w, hw[u + 1].w, hw[u + 2].w, hw[u + 3].w));
+            }
+            if (norm) {
+                float ss[4];
+#pragma unroll
+                for (int u = 0; u < 4; u++)
+                    ss[u] = o[u].x * o[u].x + o[u].y * o[u].y + o[u].z * o[u].z + o[u].w * o[u].w;
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+                    for (int u = 0; u < 4; u++) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], m);
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    const float r = rsqrtf(ss[u] + l2_eps) * scale;
+                    o[u].x *= r; o[u].y *= r; o[u].z *= r; o[u].w *= r;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u++) st4(out + (t + u) * C + c, o[u]);
+            h3 = xs[1]; h2 = xs[2]; h1 = xs[3];
+        }
+    }
+    for (; t < t1; t++) {
         if (t >= e) {  // next (non-empty) sequence starts at t
             while (cu[n + 1] <= t) n++;
             s = cu[n];
