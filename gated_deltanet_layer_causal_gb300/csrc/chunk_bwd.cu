@@ -1102,18 +1102,33 @@ __global__ void gva_sum_kernel(const float* __restrict__ dQv, const float* __res
     st4(dqkv + t * C + (int64_t)hk * kD + kh * kD + c4, k);
 }
 
-// dA_log[h] = sum over chunks of part[c][h][0]; ddt_bias[h] likewise [1]; fixed order.
-__global__ void gate_reduce_kernel(const float* __restrict__ part, int NT, int hv, float* dA_log,
-                                   float* ddt_bias) {
-    int h = blockIdx.x * blockDim.x + threadIdx.x;
-    if (h >= hv) return;
+// dA_log[h] = sum over chunks of part[c][h][0]; ddt_bias[h] likewise [1].
+// One block per head: thread i sums chunks i, i + kGateThreads, ... in order,
+// then a fixed tree over the threads (deterministic).
+constexpr int kGateThreads = 256;
+__global__ void __launch_bounds__(kGateThreads)
+gate_reduce_kernel(const float* __restrict__ part, int NT, int hv, float* dA_log, float* ddt_bias) {
+    __shared__ float2 red[kGateThreads];
+    const int h = blockIdx.x;
     float a = 0.f, b = 0.f;
-    for (int c = 0; c < NT; c++) {
-        a += part[((int64_t)c * hv + h) * 2 + 0];
-        b += part[((int64_t)c * hv + h) * 2 + 1];
+    for (int c = threadIdx.x; c < NT; c += kGateThreads) {
+        const float2 v = *reinterpret_cast<const float2*>(part + ((int64_t)c * hv + h) * 2);
+        a += v.x;
+        b += v.y;
     }
-    if (dA_log) dA_log[h] = a;
-    if (ddt_bias) ddt_bias[h] = b;
+    red[threadIdx.x] = make_float2(a, b);
+    __syncthreads();
+    for (int m = kGateThreads / 2; m > 0; m >>= 1) {
+        if (threadIdx.x < m) {
+            red[threadIdx.x].x += red[threadIdx.x + m].x;
+            red[threadIdx.x].y += red[threadIdx.x + m].y;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        if (dA_log) dA_log[h] = red[0].x;
+        if (ddt_bias) ddt_bias[h] = red[0].y;
+    }
 }
 
 // Deterministic two-level column sum of part [nparts][kD]: stage 1, block b
@@ -1287,8 +1302,8 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
     if (a.dA_log || a.ddt_bias) {
         if (a.NT > 0) {
             GDN_PROF("gate_reduce", st);
-            gate_reduce_kernel<<<(a.hv + 127) / 128, 128, 0, st>>>(gate_part, a.NT, a.hv,
-                                                                   a.dA_log, a.ddt_bias);
+            gate_reduce_kernel<<<a.hv, kGateThreads, 0, st>>>(gate_part, a.NT, a.hv, a.dA_log,
+                                                              a.ddt_bias);
         } else {
             if (a.dA_log) cudaMemsetAsync(a.dA_log, 0, sizeof(float) * a.hv, st);
             if (a.ddt_bias) cudaMemsetAsync(a.ddt_bias, 0, sizeof(float) * a.hv, st);

@@ -67,6 +67,18 @@ __device__ __forceinline__ void cp_async4(void* smem, const void* gmem, bool pre
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(s), "l"(gmem), "r"(n)
                  : "memory");
 }
+// 8-byte variant (through L1), e.g. four bf16 elements.
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+// Four consecutive elements of type T (16 B fp32, 8 B bf16).
+__device__ __forceinline__ void cp_async_row4(float* smem, const float* g) {
+    cp_async16(smem, g, true);
+}
+__device__ __forceinline__ void cp_async_row4(__nv_bfloat16* smem, const __nv_bfloat16* g) {
+    cp_async8(smem, g);
+}
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;\n" ::: "memory");
 }

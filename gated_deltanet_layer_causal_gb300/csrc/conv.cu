@@ -18,6 +18,15 @@ namespace gdn {
 
 constexpr int kConvWarps = 8;
 constexpr int kConvRun = 64;   // tokens per warp
+constexpr int kConvRing = 3;   // backward: four-token steps each lane holds in its copy ring
+
+// Backward shared memory: per lane a ring of kConvRing steps, each four rows of
+// the incoming gradient (float4) and four new input rows (4 x T); reused for
+// the dw reduction at the end.
+template <class T>
+constexpr size_t conv_bwd_smem() {
+    return (size_t)kConvRing * 4 * kConvWarps * 32 * (sizeof(float4) + 4 * sizeof(T));
+}
 
 __device__ __forceinline__ int seq_of(const int32_t* cu, int N, int64_t t) {
     // last n with cu[n] <= t (sequences may be empty)
@@ -217,7 +226,11 @@ conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
                 const float* __restrict__ dqkv, const int32_t* __restrict__ cu, int N,
                 int64_t Ttot, int C, int hk, float l2_eps, float q_scale, T* __restrict__ dx,
                 float* __restrict__ wpart, float* dcs) {
-    __shared__ float red[kConvWarps][kD][kConvK];
+    extern __shared__ __align__(16) unsigned char conv_smem[];
+    constexpr int kThr = kConvWarps * 32;
+    float4* dq_ring = reinterpret_cast<float4*>(conv_smem);                   // [ring][4][kThr]
+    T* x_ring = reinterpret_cast<T*>(conv_smem + kConvRing * 4 * kThr * sizeof(float4));   // [ring][4][kThr][4]
+    auto red = reinterpret_cast<float (*)[kD][kConvK]>(conv_smem);            // [warp][kD][kConvK]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int grp = blockIdx.y;
     const int c = grp * kD + lane * 4;
@@ -246,15 +259,45 @@ conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
         float4 d3 = (t1 + 2 < e) ? conv_dpre(x, cs_in, dqkv, t1 + 2, s, n, C, c, wr, norm, scale, l2_eps) : z4;
         if (s <= t0 && (t1 - t0) % 4 == 0) {
             // the whole run lies in one sequence: four tokens per step, whose
-            // dpre chains are independent; xr[k] = x[tb - 6 + k], three rows
-            // carried from step to step
+            // dpre chains are independent.  Step i covers tokens tb..tb-3
+            // (tb = t1-1-4i) and the inputs xr[k] = x[tb - 6 + k]: xr[4..6]
+            // carried from the step before, xr[0..3] new.  Each lane copies its
+            // own gradient rows and new input rows kConvRing-1 steps ahead into
+            // its ring slots (cp.async), so loads stay in flight while it
+            // computes; rows before the sequence start come from the cache.
+            const int nsteps = (int)((t1 - t0) / 4);
+            const int tid = threadIdx.x;
+            auto issue = [&](int i) {
+                if (i < nsteps) {
+                    const int slot = i % kConvRing;
+                    const int64_t tb = t1 - 1 - 4 * (int64_t)i;
+#pragma unroll
+                    for (int u = 0; u < 4; u++)
+                        cp_async16(&dq_ring[(slot * 4 + u) * kThr + tid], dqkv + (tb - u) * C + c, true);
+#pragma unroll
+                    for (int k = 0; k < 4; k++)
+                        if (tb - 6 + k >= s)
+                            cp_async_row4(&x_ring[((slot * 4 + k) * kThr + tid) * 4], x + (tb - 6 + k) * C + c);
+                }
+                cp_async_commit();
+            };
             float4 xr[7];
 #pragma unroll
-            for (int k = 0; k < 7; k++) xr[k] = conv_in(x, cs_in, t1 - 7 + k, s, n, C, c);
-            for (int64_t tb = t1 - 1; tb >= t0; tb -= 4) {
+            for (int k = 4; k < 7; k++) xr[k] = ld4(x + (t1 - 7 + k) * C + c);
+#pragma unroll
+            for (int i = 0; i < kConvRing - 1; i++) issue(i);
+            for (int i = 0; i < nsteps; i++) {
+                const int64_t tb = t1 - 1 - 4 * (int64_t)i;
+                issue(i + kConvRing - 1);   // the slot step i-1 used
+                cp_async_wait<kConvRing - 1>();
+                const int slot = i % kConvRing;
                 float4 gq[4], dd[4];
 #pragma unroll
-                for (int u = 0; u < 4; u++) gq[u] = ld4(dqkv + (tb - u) * C + c);
+                for (int u = 0; u < 4; u++) gq[u] = dq_ring[(slot * 4 + u) * kThr + tid];
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+                    xr[k] = (tb - 6 + k >= s) ? ld4(&x_ring[((slot * 4 + k) * kThr + tid) * 4])
+                                              : conv_in(x, cs_in, tb - 6 + k, s, n, C, c);
 #pragma unroll
                 for (int u = 0; u < 4; u++)
                     dd[u] = conv_dpre_w(xr[6 - u], xr[5 - u], xr[4 - u], xr[3 - u], gq[u], wr, norm,
@@ -285,12 +328,9 @@ conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
                     }
                     d3 = d2; d2 = d1; d1 = d0;
                 }
-                if (tb - 4 >= t0) {   // next step: x[tb - 10 .. tb - 4]
-                    xr[4] = xr[0]; xr[5] = xr[1]; xr[6] = xr[2];
-#pragma unroll
-                    for (int k = 0; k < 4; k++) xr[k] = conv_in(x, cs_in, tb - 10 + k, s, n, C, c);
-                }
+                xr[4] = xr[0]; xr[5] = xr[1]; xr[6] = xr[2];
             }
+            cp_async_wait<0>();
         } else {
             // walking backwards: a register window holds x[t], x[t-1], x[t-2], x[t-3];
             // each step loads one new x row and the next dq row ahead of use
@@ -340,6 +380,7 @@ conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
             }
         }
     }
+    __syncthreads();   // every warp is done with its ring
 #pragma unroll
     for (int ch = 0; ch < 4; ch++)
 #pragma unroll
@@ -397,9 +438,18 @@ cudaError_t launch_conv_bwd_t(const ConvArgs& a, cudaStream_t st) {
         cudaMemsetAsync(a.dcs, 0, sizeof(float) * (size_t)a.N * a.C * (kConvK - 1), st);
     if (parts > 0) {
         dim3 grid((unsigned)parts, (unsigned)(a.C / kD));
+        static_assert(conv_bwd_smem<float>() >= sizeof(float) * kConvWarps * kD * kConvK &&
+                          conv_bwd_smem<__nv_bfloat16>() >= sizeof(float) * kConvWarps * kD * kConvK,
+                      "the ring holds the dw reduction");
+        static bool attr = false;
+        if (!attr) {
+            cudaFuncSetAttribute(conv_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)conv_bwd_smem<T>());
+            attr = true;
+        }
         {
             GDN_PROF("conv_bwd", st);
-            conv_bwd_kernel<T><<<grid, kConvWarps * 32, 0, st>>>(
+            conv_bwd_kernel<T><<<grid, kConvWarps * 32, conv_bwd_smem<T>(), st>>>(
                 (const T*)a.x, a.w, (const T*)a.cs_in, a.dqkv, a.cu, a.N, a.T, a.C, a.hk,
                 a.l2_eps, a.q_scale, (T*)a.dx, a.wpart, a.dcs);
         }
