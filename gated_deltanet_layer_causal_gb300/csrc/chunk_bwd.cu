@@ -188,18 +188,20 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
 }
 
 // ------------------------------------------------------------------ B2: reverse state pass
-// grid (d_v / 64, Hv, N), 256 threads, one CTA per SM.  Carries a 64-row slice
-// of dS (as dS^T[b][a] in the accumulators) from the last chunk of the
-// sequence to the first; stores dS at every chunk end and completes dU.  The
-// previous chunk's tiles come through the TMA as soon as their buffers are
-// free: the dO / dU_local slices into the other half of a double buffer at the
-// top of the iteration, K after its product, Q and W after theirs.  The
-// rounded copy of the dS slice that feeds the tensor cores, dSt, and the
-// rounded -dU operand are K-major tiles read without conversion.
+// grid (d_v / 64, Hv, N), 256 threads, tcgen05, one CTA per SM.  Carries a
+// 64-row slice (rows a) of dS from the last chunk of the sequence to the
+// first, in registers laid out like an M = 64 accumulator, and per chunk:
+//   D1 = K dS_slice^T                          (M = 64 tokens, N = 64, K = 128)
+//   dU = dU_local + diag(fk) D1                -> global (rounded) and Ub = -dU^T
+//   D2 = (diag(e^gam) dO)^T Q + Ub W           (M = 64, N = 128, K = 64 tokens)
+//   dS = e^{gam_L} dS + D2
+// storing dS at every chunk end.  K arrives swizzled, Q and W MN-major (they
+// are contracted over tokens); K and Q are rounded in place.  The dO /
+// dU_local slices are double-buffered; K is refetched as soon as D1 is done,
+// Q and W as soon as D2 is.  Tensor memory: D1 64 columns, D2 128.
 constexpr int kSl = 64;
-constexpr size_t kB2Smem = sizeof(float) * (3 * 64 * 128 + 4 * 64 * kSl + kSl * kD + kSl * 64 +
-                                            2 * 64 + 64) +
-                           4 * 8 + 1024;
+constexpr int kB2Floats = 3 * 64 * 128 + 4 * 64 * kSl + kSl * kD + 2 * kSl * 64 + 3 * 64;
+constexpr size_t kB2Smem = sizeof(float) * kB2Floats + 5 * 8 + 8 + 1024;
 
 __global__ void __launch_bounds__(256, 1)
 bwd_state_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const float* dS_final,
@@ -207,21 +209,25 @@ bwd_state_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
     float* Kb = sm;                    // [64][128] swizzled K
-    float* Qb = Kb + 64 * 128;         // [64][128] swizzled Q
-    float* Wb = Qb + 64 * 128;         // [64][128] swizzled W (arrives rounded)
-    float* dOs = Wb + 64 * 128;        // [2][64][kSl] swizzled dO slices (arrive rounded)
+    float* Qm = Kb + 64 * 128;         // [64 (i)][128 (b)] MN-major Q
+    float* Wm = Qm + 64 * 128;         // [64 (i)][128 (b)] MN-major W (arrives rounded)
+    float* dOs = Wm + 64 * 128;        // [2][64][kSl] swizzled dO slices (arrive rounded)
     float* dUs = dOs + 2 * 64 * kSl;   // [2][64][kSl] swizzled dU_local slices
     float* dSt = dUs + 2 * 64 * kSl;   // [64 (a)][128 (b)] K-major, rounded
     float* Ub = dSt + kSl * kD;        // [64 (a)][64 (i)] K-major: -dU, rounded
-    float* gam = Ub + kSl * 64;        // [2][64]
+    float* dOt = Ub + kSl * 64;        // [64 (a)][64 (i)] K-major: e^{gam_i} dO[i][a], rounded
+    float* gam = dOt + kSl * 64;       // [2][64]
     float* eg = gam + 2 * 64;
-    uint64_t* mb = reinterpret_cast<uint64_t*>(eg + 64);   // K, Q/W, slices [2]
+    uint64_t* mb = reinterpret_cast<uint64_t*>(eg + 64);   // K, Q/W, slices [2], MMA
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mb + 5);
     const int sl = blockIdx.x, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
+    const int warp = tid >> 5, half = warp >> 2;
     const int a0 = sl * kSl, kh = h / (hv / hk);
     const int64_t sbase = ((int64_t)n * hv + h) * kD * kD;
     auto row = [&](const ChunkInfo& c, int r) { return (int64_t)c.start + min(r, c.len - 1); };
     if (tid == 0)
-        for (int i = 0; i < 4; i++) umma::mbar_init(&mb[i], 1);
+        for (int i = 0; i < 5; i++) umma::mbar_init(&mb[i], 1);
+    if (warp == 0) umma::tmem_alloc(tslot, 256);
     auto issue_small = [&](const ChunkInfo& c, int slot) {
         if (tid == 0) {
             float* o = dOs + slot * 64 * kSl;
@@ -237,41 +243,64 @@ bwd_state_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         cp_async_commit();
     };
     auto issue_k = [&](const ChunkInfo& c) {
-        if (tid == 0) {
-            umma::mbar_expect_tx(&mb[0], 64 * 128 * 4);
-            umma::tma_rows(Kb, 64, &maps.k, kh, c.start, &mb[0]);
-        }
+        umma::mbar_expect_tx(&mb[0], 64 * 128 * 4);
+        umma::tma_rows(Kb, 64, &maps.k, kh, c.start, &mb[0]);
     };
     auto issue_qw = [&](const ChunkInfo& c) {
-        if (tid == 0) {
-            umma::mbar_expect_tx(&mb[1], 2 * 64 * 128 * 4);
-            umma::tma_rows(Qb, 64, &maps.q, kh, c.start, &mb[1]);
-            umma::tma_rows(Wb, 64, &maps.W, h, c.start, &mb[1]);
-        }
+        umma::mbar_expect_tx(&mb[1], 2 * 64 * 128 * 4);
+        umma::tma_rows(Qm, 64, &maps.q_mn, kh, c.start, &mb[1]);
+        umma::tma_rows(Wm, 64, &maps.W_mn, h, c.start, &mb[1]);
     };
-    typename Tile<kD, kSl, 8>::Acc sacc;
-    tile_each2<kD, kSl, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
-        v0 = dS_final ? dS_final[sbase + (int64_t)(a0 + a) * kD + b] : 0.f;
-        v1 = dS_final ? dS_final[sbase + (int64_t)(a0 + a + 1) * kD + b] : 0.f;
-        dSt[umma::kidx(a, b, kD)] = umma::tf32r(v0);
-        dSt[umma::kidx(a + 1, b, kD)] = umma::tf32r(v1);
-    });
-    __syncthreads();   // barriers initialised
+    // this thread's part of the slice: rows a = rl, rl + 8, columns
+    // b = 64 half + 8k + cf, + 1 (k < 8); ds[4k + 2hr + e] = dS[rl + 8hr][b + e]
+    const int rl = umma::frag_row_lo(), cf = umma::frag_col();
+    float ds[32];
+#pragma unroll
+    for (int k = 0; k < 8; k++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const int a = rl + 8 * (e >> 1), b = 64 * half + 8 * k + cf + (e & 1);
+            ds[4 * k + e] = dS_final ? dS_final[sbase + (int64_t)(a0 + a) * kD + b] : 0.f;
+        }
+    auto write_dst = [&]() {
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+#pragma unroll
+            for (int hr = 0; hr < 2; hr++)
+                *reinterpret_cast<float2*>(dSt + umma::kidx(rl + 8 * hr, 64 * half + 8 * k + cf, kD)) =
+                    make_float2(umma::tf32r(ds[4 * k + 2 * hr]), umma::tf32r(ds[4 * k + 2 * hr + 1]));
+    };
+    write_dst();
+    __syncthreads();   // barriers initialised, tensor memory allocated
+    umma::fence_after_sync();
+    const uint32_t tmem = *tslot, tD1 = tmem, tD2 = tmem + 64;
     const int c0 = sv.seq_chunk[n], c1 = sv.seq_chunk[n + 1];
     if (c0 < c1) {
         const ChunkInfo last = sv.chunks[c1 - 1];
-        issue_k(last);
-        issue_qw(last);
+        if (tid == 0) {
+            issue_k(last);
+            issue_qw(last);
+        }
         issue_small(last, 0);
     }
     bool ok = true;
-    const int lane = tid & 31, rg = Tile<64, kSl, 8>::m0() + (lane >> 2);   // dU rows rg, rg + 8
     for (int ci = c1 - 1; ci >= c0 && ok; ci--) {
         const int it = c1 - 1 - ci, slot = it & 1;
         const ChunkInfo info = sv.chunks[ci];
         const int L = info.len;
         const bool more = ci - 1 >= c0;
         const ChunkInfo prev = more ? sv.chunks[ci - 1] : info;
+        // gradient of the state at this chunk's end, stored as a K-major tile with
+        // rows b (the layout the state-facing kernel feeds to the tensor cores)
+        {
+            float* o = w.dS + ((int64_t)ci * hv + h) * kD * kD;
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+#pragma unroll
+                for (int e = 0; e < 4; e++)
+                    o[umma::kidx(64 * half + 8 * k + cf + (e & 1), a0 + rl + 8 * (e >> 1), kD)] =
+                        ds[4 * k + e];
+        }
         cp_async_wait<0>();
         ok = __syncthreads_and(umma::mbar_wait(&mb[2 + slot], (it >> 1) & 1));
         if (!ok) break;
@@ -279,83 +308,97 @@ bwd_state_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         const float* dOc = dOs + slot * 64 * kSl;
         const float* dUc = dUs + slot * 64 * kSl;
         const float* gc = gam + slot * 64;
-        // gradient of the state at this chunk's end, stored as a K-major tile with
-        // rows b (the layout the state-facing kernel feeds to the tensor cores)
-        const int64_t obase = ((int64_t)ci * hv + h) * kD * kD;
-        tile_each2<kD, kSl, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
-            *reinterpret_cast<float2*>(w.dS + obase + umma::kidx(b, a0 + a, kD)) =
-                make_float2(v0, v1);
-        });
         if (tid < 64) eg[tid] = tid < L ? expf(gc[tid]) : 0.f;
         const float gL = gc[L - 1];
-        const float f0 = rg < L ? expf(gL - gc[rg]) : 0.f;
-        const float f1 = rg + 8 < L ? expf(gL - gc[rg + 8]) : 0.f;
         ok = __syncthreads_and(umma::mbar_wait(&mb[0], it & 1));   // K; eg visible
         if (!ok) break;
-        // dU = dU_local + diag(fk) K dS^T  (64 x slice)
-        typename Tile<64, kSl, 8>::Acc uacc;
-        tile_zero<64, kSl, 8>(uacc);
-        tile_mma_frag<64, kSl, kD, 8>(
-            uacc,
-            [&](int r0, int k0, uint32_t(&f)[4]) {
-                ldsm_a(f, r0, k0, [&](int r, int c) { return Kb + umma::swz(r, c, 64); });
+        umma::tf32r_inplace(Kb, 64 * 128);
+        umma::fence_smem_to_async();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {
+            umma::mma(tD1, umma::swt(Kb, 64), umma::kmaj(dSt, kD), 64, kSl, kD, false);
+            umma::commit(&mb[4]);
+        }
+        // while D1 runs: dOt = (diag(e^gam) dO)^T, and Q rounded once it is in
+        for (int idx = tid; idx < kSl * 16; idx += 256) {
+            const int a = idx & (kSl - 1), i4 = idx / kSl;
+            float4 v = make_float4(dOc[umma::swz(4 * i4, a, 64)] * eg[4 * i4],
+                                   dOc[umma::swz(4 * i4 + 1, a, 64)] * eg[4 * i4 + 1],
+                                   dOc[umma::swz(4 * i4 + 2, a, 64)] * eg[4 * i4 + 2],
+                                   dOc[umma::swz(4 * i4 + 3, a, 64)] * eg[4 * i4 + 3]);
+            *reinterpret_cast<float4*>(dOt + umma::kidx(a, 4 * i4, 64)) = umma::tf32r(v);
+        }
+        ok = umma::mbar_wait(&mb[1], it & 1);   // Q, W
+        if (ok) umma::tf32r_inplace(Qm, 64 * 128);
+        ok = __syncthreads_and(ok && umma::mbar_wait(&mb[4], 0));   // D1
+        umma::fence_after_sync();
+        if (ok && more && tid == 0) issue_k(prev);   // K consumed
+        if (ok) {   // dU = dU_local + fk D1: rows i = rl, rl + 8, columns a = 32 half + 8k + cf, + 1
+            float v[16];
+            umma::tmem_ld_m64<4>(umma::tmem_at(tD1, 32 * half), v);
 #pragma unroll
-                for (int e = 0; e < 4; e++) f[e] = f2tf32(__uint_as_float(f[e]));
-            },
-            [&](int k0, int n0, uint32_t(&f)[4]) {
-                ldsm_b2(f, k0, n0, [&](int n, int k) { return dSt + umma::kidx(n, k, kD); });
-            });
-        __syncthreads();                    // K and dSt reads done
-        if (more) issue_k(prev);
-        tile_each2<64, kSl, 8>(uacc, [&](int i, int a, float& v0, float& v1) {
-            float u0 = 0.f, u1 = 0.f;
-            if (i < L) {
-                const float f = i == rg ? f0 : f1;
-                const float2 ul = *reinterpret_cast<const float2*>(dUc + umma::swz(i, a, 64));
-                u0 = ul.x + f * v0;
-                u1 = ul.y + f * v1;
-                // stored rounded: later kernels use dU only as a tensor-core operand
-                *reinterpret_cast<float2*>(w.dU + ((int64_t)(info.start + i) * hv + h) * kD +
-                                           a0 + a) = make_float2(umma::tf32r(u0), umma::tf32r(u1));
+            for (int hr = 0; hr < 2; hr++) {
+                const int i = rl + 8 * hr;
+                const float f = i < L ? expf(gL - gc[i]) : 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const int a = 32 * half + 8 * k + cf;
+                    float u0 = 0.f, u1 = 0.f;
+                    if (i < L) {
+                        const float2 ul = *reinterpret_cast<const float2*>(dUc + umma::swz(i, a, 64));
+                        u0 = ul.x + f * v[4 * k + 2 * hr];
+                        u1 = ul.y + f * v[4 * k + 2 * hr + 1];
+                        // stored rounded: later kernels use dU only as a tensor-core operand
+                        *reinterpret_cast<float2*>(w.dU + ((int64_t)(info.start + i) * hv + h) * kD +
+                                                   a0 + a) = make_float2(umma::tf32r(u0), umma::tf32r(u1));
+                    }
+                    Ub[umma::kidx(a, i, 64)] = umma::tf32r(-u0);
+                    Ub[umma::kidx(a + 1, i, 64)] = umma::tf32r(-u1);
+                }
             }
-            Ub[umma::kidx(a, i, 64)] = umma::tf32r(-u0);
-            Ub[umma::kidx(a + 1, i, 64)] = umma::tf32r(-u1);
-        });
-        ok = __syncthreads_and(umma::mbar_wait(&mb[1], it & 1));   // Q, W; Ub complete
+        }
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (ok && tid == 0) {
+            umma::mma(tD2, umma::kmaj(dOt, 64), umma::mnt(Qm), 64, kD, 64, false);
+            umma::mma(tD2, umma::kmaj(Ub, 64), umma::mnt(Wm), 64, kD, 64, true);
+            umma::commit(&mb[4]);
+        }
+        ok = __syncthreads_and(ok && umma::mbar_wait(&mb[4], 1));   // D2
+        umma::fence_after_sync();
         if (!ok) break;
-        // dS^T = e^{gam_L} dS^T + Q~^T dO - W^T dU
-        const float dl = expf(gL);
-        tile_each<kD, kSl, 8>(sacc, [&](int, int, float& v) { v *= dl; });
-        tile_mma_bits<kD, kSl, 64, 8>(
-            sacc, [&](int b, int i) { return f2tf32(eg[i] * Qb[umma::swz(i, b, 64)]); },
-            [&](int i, int a) { return __float_as_uint(dOc[umma::swz(i, a, 64)]); });
-        tile_mma_frag<kD, kSl, 64, 8>(
-            sacc,
-            [&](int r0, int k0, uint32_t(&f)[4]) {   // A(b, i) = W[i][b]: element loads
-                const int g = lane >> 2, t = lane & 3;
-                f[0] = __float_as_uint(Wb[umma::swz(k0 + t, r0 + g, 64)]);
-                f[1] = __float_as_uint(Wb[umma::swz(k0 + t, r0 + g + 8, 64)]);
-                f[2] = __float_as_uint(Wb[umma::swz(k0 + t + 4, r0 + g, 64)]);
-                f[3] = __float_as_uint(Wb[umma::swz(k0 + t + 4, r0 + g + 8, 64)]);
-            },
-            [&](int k0, int n0, uint32_t(&f)[4]) {
-                ldsm_b2(f, k0, n0, [&](int n, int k) { return Ub + umma::kidx(n, k, 64); });
-            });
-        __syncthreads();                    // Q, W, dO, Ub reads done
-        if (more) issue_qw(prev);
-        tile_each2<kD, kSl, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
-            dSt[umma::kidx(a, b, kD)] = umma::tf32r(v0);
-            dSt[umma::kidx(a + 1, b, kD)] = umma::tf32r(v1);
-        });
+        if (more && tid == 0) issue_qw(prev);   // Q, W consumed
+        {
+            float v[32];
+            umma::tmem_ld64_m64(umma::tmem_at(tD2, 64 * half), v);
+            const float dl = expf(gL);
+#pragma unroll
+            for (int e = 0; e < 32; e++) ds[e] = dl * ds[e] + v[e];
+        }
+        write_dst();
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        __syncthreads();
     }
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) umma::tmem_free(tmem, 256);
     if (!ok) {
         if (tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
         return;
     }
-    if (dS_init)
-        tile_each<kD, kSl, 8>(sacc, [&](int b, int a, float& v) {
-            dS_init[sbase + (int64_t)(a0 + a) * kD + b] = v;
-        });
+    if (dS_init) {
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+#pragma unroll
+            for (int hr = 0; hr < 2; hr++)
+                *reinterpret_cast<float2*>(dS_init + sbase + (int64_t)(a0 + rl + 8 * hr) * kD +
+                                           64 * half + 8 * k + cf) =
+                    make_float2(ds[4 * k + 2 * hr], ds[4 * k + 2 * hr + 1]);
+    }
 }
 
 // ------------------------------------------------------------------ B3a: state-facing terms
@@ -1233,6 +1276,7 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
         if (e == cudaSuccess) e = make_rows_map(&maps.dO_mn, w.dO, a.hv, a.T, vs, true);
         if (e == cudaSuccess) e = make_rows_map(&maps.dU_mn, w.dU, a.hv, a.T, vs, true);
         if (e == cudaSuccess) e = make_rows_map(&maps.dW_mn, w.dW, a.hv, a.T, vs, true);
+        if (e == cudaSuccess) e = make_rows_map(&maps.W_mn, a.sv.W, a.hv, a.T, vs, true);
         if (e == cudaSuccess)
             e = make_rows_map(&maps.k_mn, a.qkv + (int64_t)a.hk * kD, a.hk, a.T, C, true);
         if (e == cudaSuccess)

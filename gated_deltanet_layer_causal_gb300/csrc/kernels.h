@@ -62,7 +62,7 @@ struct TileMaps {
     CUtensorMap dO, dU, dW;
     CUtensorMap dQv, dKv, dQv2, dKv2, dKv3;
     CUtensorMap dv;        // v channels of the conv-output gradient [T, C]
-    CUtensorMap q_mn, k_mn, v_mn, U_mn, dO_mn, dU_mn, dW_mn;
+    CUtensorMap q_mn, k_mn, v_mn, U_mn, W_mn, dO_mn, dU_mn, dW_mn;
 };
 cudaError_t make_rows_map(CUtensorMap* m, const float* base, int heads, int64_t T,
                           int64_t token_stride, bool mn_major = false);
