@@ -127,7 +127,7 @@ class Step:
         io = w.torch_dtype
         f32 = torch.float32
         self.cu_host = inp["cu_seqlens"].contiguous()
-        self.dims = _abi.dims(N, T, w.h_k, w.h_v, io == torch.bfloat16)
+        self.dims = _abi.dims(N, T, w.h_k, w.h_v, io == torch.bfloat16, qkv_tf32=True)
         ws = {}
         for kind in (_abi.GDN_WS_FWD, _abi.GDN_WS_BWD, _abi.GDN_WS_CONV_BWD):
             n = ctypes.c_size_t(0)

@@ -45,6 +45,7 @@ class GdnDims(ctypes.Structure):
         ("io_dtype", ctypes.c_int32),
         ("l2_eps", ctypes.c_float),
         ("norm_eps", ctypes.c_float),
+        ("qkv_tf32", ctypes.c_int32),
     ]
 
 
@@ -111,9 +112,10 @@ def call(name: str, *args) -> None:
 
 
 def dims(num_seqs, total_tokens, h_k, h_v, io_bf16, l2_eps=1e-6, norm_eps=1e-6, d=128,
-         conv_k=4, chunk=64) -> GdnDims:
+         conv_k=4, chunk=64, qkv_tf32=False) -> GdnDims:
     return GdnDims(int(num_seqs), int(total_tokens), int(h_k), int(h_v), d, d, conv_k, chunk,
-                   GDN_BF16 if io_bf16 else GDN_F32, float(l2_eps), float(norm_eps))
+                   GDN_BF16 if io_bf16 else GDN_F32, float(l2_eps), float(norm_eps),
+                   1 if qkv_tf32 else 0)
 
 
 def launch_count() -> int:

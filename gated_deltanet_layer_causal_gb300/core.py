@@ -42,10 +42,11 @@ def _check(t, name, dtype=None, device=None):
         raise ValueError(f"{name} must be on {device}")
 
 
-def _dims(x_or_T, N, h_k, h_v, io_dtype, l2_eps=1e-6, norm_eps=1e-6):
+def _dims(x_or_T, N, h_k, h_v, io_dtype, l2_eps=1e-6, norm_eps=1e-6, qkv_tf32=False):
     if io_dtype not in _IO:
         raise ValueError(f"io dtype must be fp32 or bf16, got {io_dtype}")
-    return _abi.dims(N, x_or_T, h_k, h_v, io_dtype == torch.bfloat16, l2_eps, norm_eps)
+    return _abi.dims(N, x_or_T, h_k, h_v, io_dtype == torch.bfloat16, l2_eps, norm_eps,
+                     qkv_tf32=qkv_tf32)
 
 
 def workspace_size(kind, T, N, h_k, h_v, cu_host, io_dtype=torch.bfloat16) -> int:
@@ -63,15 +64,18 @@ def _workspace(kind, T, N, h_k, h_v, cu_host, io_dtype, device):
 
 # ------------------------------------------------------------------ conv
 def conv1d_silu(x, conv_w, cu_seqlens, h_k, h_v, conv_state=None, output_conv_state=False,
-                cu_host=None, l2_eps=1e-6):
-    """Causal conv1d + SiLU + L2(q, k) -> (qkv fp32 [T, C], conv_state_out or None)."""
+                cu_host=None, l2_eps=1e-6, qkv_tf32=False):
+    """Causal conv1d + SiLU + L2(q, k) -> (qkv fp32 [T, C], conv_state_out or None).
+
+    qkv_tf32: round qkv to nearest tf32 (for chunk_fwd / chunk_bwd called with
+    qkv_tf32=True, which then skip their own rounding of the q / k / v tiles)."""
     T, C = x.shape
     N = cu_seqlens.numel() - 1
     _check(x, "x", device=x.device)
     _check(conv_w, "conv_w", torch.float32, x.device)
     _check(conv_state, "conv_state", x.dtype, x.device)
     cu_host, cup = _cu_host(cu_seqlens, cu_host)
-    d = _dims(T, N, h_k, h_v, x.dtype, l2_eps)
+    d = _dims(T, N, h_k, h_v, x.dtype, l2_eps, qkv_tf32=qkv_tf32)
     qkv = torch.empty(T, C, dtype=torch.float32, device=x.device)
     cs_out = torch.empty(N, C, 3, dtype=x.dtype, device=x.device) if output_conv_state else None
     _abi.call("gdn_conv1d_silu", ctypes.byref(d), _ptr(cu_seqlens), cup, _ptr(x), _ptr(conv_w),
@@ -101,8 +105,9 @@ def conv1d_silu_bwd(x, conv_w, cu_seqlens, h_k, h_v, dqkv, conv_state=None,
 # ------------------------------------------------------------------ chunked rule
 def chunk_fwd(qkv, a, b, A_log, dt_bias, cu_seqlens, h_k, h_v, initial_state=None, z=None,
               norm_w=None, output_final_state=False, return_o=False, cu_host=None,
-              norm_eps=1e-6, fwd_ws=None):
-    """Gated delta rule (+ fused gated norm when z is given).
+              norm_eps=1e-6, fwd_ws=None, qkv_tf32=False):
+    """Gated delta rule (+ fused gated norm when z is given).  qkv_tf32: qkv holds
+    tf32 values (conv1d_silu(..., qkv_tf32=True)).
 
     Returns dict(y, o, final_state, fwd_ws); fwd_ws must be kept for chunk_bwd."""
     T = qkv.shape[0]
@@ -116,7 +121,7 @@ def chunk_fwd(qkv, a, b, A_log, dt_bias, cu_seqlens, h_k, h_v, initial_state=Non
                  (initial_state, "initial_state")):
         _check(t, n, torch.float32, dev)
     cu_host, cup = _cu_host(cu_seqlens, cu_host)
-    d = _dims(T, N, h_k, h_v, io, norm_eps=norm_eps)
+    d = _dims(T, N, h_k, h_v, io, norm_eps=norm_eps, qkv_tf32=qkv_tf32)
     if fwd_ws is None:
         fwd_ws = _workspace(_abi.GDN_WS_FWD, T, N, h_k, h_v, cu_host, io, dev)
     y = torch.empty(T, h_v, 128, dtype=io, device=dev) if z is not None else None
@@ -131,7 +136,7 @@ def chunk_fwd(qkv, a, b, A_log, dt_bias, cu_seqlens, h_k, h_v, initial_state=Non
 
 def chunk_bwd(qkv, a, b, A_log, dt_bias, cu_seqlens, h_k, h_v, fwd_ws, dy, initial_state=None,
               z=None, norm_w=None, dfinal_state=None, want_dinitial_state=False, cu_host=None,
-              norm_eps=1e-6, bwd_ws=None):
+              norm_eps=1e-6, bwd_ws=None, qkv_tf32=False):
     """Backward of chunk_fwd -> dict(dqkv, da, db, dA_log, ddt_bias, dz, dnorm_w, dinitial_state)."""
     T = qkv.shape[0]
     N = cu_seqlens.numel() - 1
@@ -140,7 +145,7 @@ def chunk_bwd(qkv, a, b, A_log, dt_bias, cu_seqlens, h_k, h_v, fwd_ws, dy, initi
     _check(dy, "dy", io, dev)
     _check(dfinal_state, "dfinal_state", torch.float32, dev)
     cu_host, cup = _cu_host(cu_seqlens, cu_host)
-    d = _dims(T, N, h_k, h_v, io, norm_eps=norm_eps)
+    d = _dims(T, N, h_k, h_v, io, norm_eps=norm_eps, qkv_tf32=qkv_tf32)
     if bwd_ws is None:
         bwd_ws = _workspace(_abi.GDN_WS_BWD, T, N, h_k, h_v, cu_host, io, dev)
     dqkv = torch.empty_like(qkv)

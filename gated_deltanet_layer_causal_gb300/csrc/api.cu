@@ -29,6 +29,7 @@ gdn_status check_dims(const gdn_dims* d) {
     if (d->io_dtype != GDN_F32 && d->io_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
     if (d->total_tokens >= (int64_t)1 << 31) return GDN_ERR_UNSUPPORTED;
     if (!(d->l2_eps >= 0.f) || !(d->norm_eps >= 0.f)) return GDN_ERR_INVALID_ARG;
+    if (d->qkv_tf32 != 0 && d->qkv_tf32 != 1) return GDN_ERR_INVALID_ARG;
     return GDN_OK;
 }
 
@@ -68,6 +69,7 @@ FwdSaved carve_fwd(void* ws, const gdn_dims* d, int NT, size_t* bytes) {
     s.chunks = c.take<ChunkInfo>((size_t)NT);
     s.seq_chunk = c.take<int32_t>((size_t)d->num_seqs + 1);
     s.T = d->total_tokens;
+    s.qkv_tf32 = d->qkv_tf32;
     s.gam = c.take<float>(T * H);
     s.beta = c.take<float>(T * H);
     s.W = c.take<float>(T * H * kD);
@@ -189,6 +191,7 @@ gdn_status gdn_conv1d_silu(const gdn_dims* dims, const int32_t* cu, const int32_
     a.q_scale = 1.f / sqrtf((float)kD);
     a.qkv = qkv;
     a.cs_out = cs_out;
+    a.round_tf32 = dims->qkv_tf32 != 0;
     return cuda_status(launch_conv_fwd(a, (cudaStream_t)stream));
 }
 

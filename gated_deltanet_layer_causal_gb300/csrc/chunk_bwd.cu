@@ -122,7 +122,7 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
         umma::zero_tail_rows(dOs, 64, 0, L);
         __syncthreads();
     }
-    umma::tf32r_inplace(Qs, 2 * 64 * 128);
+    if (!sv.qkv_tf32) umma::tf32r_inplace(Qs, 2 * 64 * 128);
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -312,7 +312,7 @@ bwd_state_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         const float gL = gc[L - 1];
         ok = __syncthreads_and(umma::mbar_wait(&mb[0], it & 1));   // K; eg visible
         if (!ok) break;
-        umma::tf32r_inplace(Kb, 64 * 128);
+        if (!sv.qkv_tf32) umma::tf32r_inplace(Kb, 64 * 128);
         umma::fence_smem_to_async();
         __syncthreads();
         umma::fence_after_sync();
@@ -330,7 +330,7 @@ bwd_state_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
             *reinterpret_cast<float4*>(dOt + umma::kidx(a, 4 * i4, 64)) = umma::tf32r(v);
         }
         ok = umma::mbar_wait(&mb[1], it & 1);   // Q, W
-        if (ok) umma::tf32r_inplace(Qm, 64 * 128);
+        if (ok && !sv.qkv_tf32) umma::tf32r_inplace(Qm, 64 * 128);
         ok = __syncthreads_and(ok && umma::mbar_wait(&mb[4], 0));   // D1
         umma::fence_after_sync();
         if (ok && more && tid == 0) issue_k(prev);   // K consumed
@@ -638,7 +638,7 @@ bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv
         umma::zero_tail_rows(Us, 64, 0, L);
         __syncthreads();
     }
-    umma::tf32r_inplace(Qs, 2 * 64 * 128);   // Q, K (dO and U arrive rounded)
+    if (!sv.qkv_tf32) umma::tf32r_inplace(Qs, 2 * 64 * 128);   // Q, K (dO and U arrive rounded)
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -711,7 +711,7 @@ bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv
         umma::zero_tail_rows(Km, 64, 0, L);
         __syncthreads();
     }
-    umma::tf32r_inplace(Qm, 2 * 64 * 128);
+    if (!sv.qkv_tf32) umma::tf32r_inplace(Qm, 2 * 64 * 128);
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
@@ -862,7 +862,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         umma::zero_tail_rows(dUm, 64, 0, L);
         __syncthreads();
     }
-    umma::tf32r_inplace(Ks, 2 * 64 * 128);   // K, V (dW, dU and T^T arrive rounded)
+    if (!sv.qkv_tf32) umma::tf32r_inplace(Ks, 2 * 64 * 128);   // K, V (dW, dU and T^T arrive rounded)
     __syncthreads();
     umma::fence_smem_to_async();
     __syncthreads();
@@ -954,7 +954,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         umma::zero_tail_rows(Km, 64, 0, L);
         __syncthreads();
     }
-    umma::tf32r_inplace(Km, 64 * 128);
+    if (!sv.qkv_tf32) umma::tf32r_inplace(Km, 64 * 128);
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();

@@ -169,7 +169,7 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv) 
         umma::zero_tail_rows(Vm, 64, 0, L);
         __syncthreads();
     }
-    umma::tf32r_inplace(Ks, 3 * 64 * 128);   // K (both layouts), V
+    if (!sv.qkv_tf32) umma::tf32r_inplace(Ks, 3 * 64 * 128);   // K (both layouts), V
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();
@@ -505,7 +505,7 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO* 
         umma::zero_tail_rows(Us, 64, 0, L);
         __syncthreads();
     }
-    umma::tf32r_inplace(Qs, 64 * 128 * 2);   // Q, K (S0 and U arrive rounded)
+    if (!sv.qkv_tf32) umma::tf32r_inplace(Qs, 64 * 128 * 2);   // Q, K (S0 and U arrive rounded)
     umma::fence_smem_to_async();
     __syncthreads();
     umma::fence_after_sync();

@@ -93,6 +93,11 @@ __device__ __forceinline__ uint32_t f2tf32(float x) {
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
     return r;
 }
+// Four values rounded to nearest tf32, kept as fp32.
+__device__ __forceinline__ float4 tf32_round(float4 v) {
+    return make_float4(__uint_as_float(f2tf32(v.x)), __uint_as_float(f2tf32(v.y)),
+                       __uint_as_float(f2tf32(v.z)), __uint_as_float(f2tf32(v.w)));
+}
 
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
                                          const uint32_t (&b)[2]) {

@@ -60,7 +60,7 @@ template <class T>
 __global__ void __launch_bounds__(kConvWarps * 32)
 conv_fwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* cs_in,
                 const int32_t* __restrict__ cu, int N, int64_t Ttot, int C, int hk,
-                float l2_eps, float q_scale, float* __restrict__ out) {
+                float l2_eps, float q_scale, bool rnd, float* __restrict__ out) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int grp = blockIdx.y;
     const int c = grp * kD + lane * 4;
@@ -112,7 +112,7 @@ conv_fwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; u++) st4(out + (t + u) * C + c, o[u]);
+            for (int u = 0; u < 4; u++) st4(out + (t + u) * C + c, rnd ? tf32_round(o[u]) : o[u]);
             h3 = xs[1]; h2 = xs[2]; h1 = xs[3];
         }
     }
@@ -136,7 +136,7 @@ conv_fwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
             float r = rsqrtf(ss + l2_eps) * scale;
             o.x *= r; o.y *= r; o.z *= r; o.w *= r;
         }
-        st4(out + t * C + c, o);
+        st4(out + t * C + c, rnd ? tf32_round(o) : o);
         h3 = h2; h2 = h1; h1 = cur;
     }
 }
@@ -412,7 +412,7 @@ cudaError_t launch_conv_fwd_t(const ConvArgs& a, cudaStream_t st) {
         GDN_PROF("conv_fwd", st);
         conv_fwd_kernel<T><<<grid, kConvWarps * 32, 0, st>>>(
             (const T*)a.x, a.w, (const T*)a.cs_in, a.cu, a.N, a.T, a.C, a.hk, a.l2_eps,
-            a.q_scale, a.qkv);
+            a.q_scale, a.round_tf32, a.qkv);
     }
     if (a.cs_out != nullptr && a.N > 0) {
         int64_t n = (int64_t)a.N * a.C;

@@ -22,6 +22,7 @@ struct ConvArgs {
     // forward
     float* qkv;
     void* cs_out;
+    bool round_tf32;   // qkv rounded to nearest tf32
     // backward
     const float* dqkv;
     void* dx;
@@ -39,6 +40,7 @@ struct FwdSaved {
     ChunkInfo* chunks;     // [NT]
     int32_t* seq_chunk;    // [N+1] first chunk of each sequence
     int64_t T;             // total tokens
+    int32_t qkv_tf32;      // qkv holds tf32 values: q / k / v tiles are not rounded again
     float* gam;            // [Hv, T] in-chunk cumulative gate (head-major)
     float* beta;           // [Hv, T]
     float* W;              // [T, Hv, d]

@@ -80,7 +80,18 @@ typedef struct {
     int32_t io_dtype;      /* gdn_dtype of the activations                  */
     float l2_eps;          /* eps inside the q/k L2 norm (1e-6 typical)      */
     float norm_eps;        /* eps inside the gated RMSNorm (1e-6 typical)    */
+    int32_t qkv_tf32;      /* 0 or 1, see below                               */
 } gdn_dims;
+
+/* qkv_tf32 = 1: the conv output qkv carries tf32 values (fp32 storage, 10
+ * fraction bits).  gdn_conv1d_silu then rounds its output to nearest tf32, and
+ * gdn_chunk_fwd / gdn_chunk_bwd, whose tensor-core products read q, k and v
+ * at tf32 precision in any case, use the tiles as loaded instead of rounding
+ * each one again; only their few elementwise uses of q, k, v (gate-gradient
+ * dot products) see the rounded values.  With 1, the qkv passed to the chunk
+ * entry points must be tf32 values (as gdn_conv1d_silu writes them): other
+ * values reach the tensor cores truncated.  qkv_tf32 = 0: qkv is exact fp32
+ * and rounded where the tensor cores read it.  Other entry points ignore it. */
 
 /* Workspace kinds for gdn_workspace_size(). */
 enum {

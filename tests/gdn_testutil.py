@@ -70,8 +70,9 @@ def oracle_group(inp: dict, w: synth.Workload, kh: int, backward: bool, S0=None,
 
 
 def gpu_run(inp: dict, w: synth.Workload, backward: bool, S0=None, dS=None, conv_state=None,
-            dev="cuda"):
-    """Whole core through the C ABI: conv -> chunk fwd (fused norm) [-> chunk bwd -> conv bwd]."""
+            dev="cuda", qkv_tf32=True):
+    """Whole core through the C ABI: conv -> chunk fwd (fused norm) [-> chunk bwd -> conv bwd].
+    qkv_tf32=True is the setting bench.py runs (qkv stored at tf32 precision)."""
     g = lambda k: inp[k].to(dev)
     x, cw, a, b = g("x"), g("conv_w"), g("a"), g("b")
     A_log, dtb, z, nw = g("A_log"), g("dt_bias"), g("z"), g("norm_w")
@@ -79,16 +80,16 @@ def gpu_run(inp: dict, w: synth.Workload, backward: bool, S0=None, dS=None, conv
     s0 = None if S0 is None else S0.to(dev)
     cs = None if conv_state is None else conv_state.to(dev)
     qkv, cs_out = core.conv1d_silu(x, cw, cu, w.h_k, w.h_v, conv_state=cs,
-                                   output_conv_state=True, cu_host=cu_host)
+                                   output_conv_state=True, cu_host=cu_host, qkv_tf32=qkv_tf32)
     r = core.chunk_fwd(qkv, a, b, A_log, dtb, cu, w.h_k, w.h_v, s0, z, nw,
-                       output_final_state=True, return_o=True, cu_host=cu_host)
+                       output_final_state=True, return_o=True, cu_host=cu_host, qkv_tf32=qkv_tf32)
     out = dict(qkv=qkv, y=r["y"], o=r["o"], S=r["final_state"], conv_state=cs_out)
     out["status_fwd"] = core.read_status(r["fwd_ws"])
     if backward:
         dS_d = None if dS is None else dS.to(dev)
         gr = core.chunk_bwd(qkv, a, b, A_log, dtb, cu, w.h_k, w.h_v, r["fwd_ws"], g("dy"), s0, z,
                             nw, dfinal_state=dS_d, want_dinitial_state=s0 is not None,
-                            cu_host=cu_host)
+                            cu_host=cu_host, qkv_tf32=qkv_tf32)
         dx, dw, dcs = core.conv1d_silu_bwd(x, cw, cu, w.h_k, w.h_v, gr["dqkv"], conv_state=cs,
                                            want_dconv_state=cs is not None, cu_host=cu_host)
         out.update(gr)

@@ -76,7 +76,8 @@ def test_bad_cu_seqlens_rejected(lib, cu, why):
 @pytest.mark.parametrize("field,value,code", [
     ("d_k", 64, _abi.GDN_ERR_UNSUPPORTED), ("conv_k", 3, _abi.GDN_ERR_UNSUPPORTED),
     ("chunk", 32, _abi.GDN_ERR_UNSUPPORTED), ("h_v", 5, _abi.GDN_ERR_INVALID_ARG),
-    ("io_dtype", 7, _abi.GDN_ERR_UNSUPPORTED), ("h_k", 0, _abi.GDN_ERR_INVALID_ARG)])
+    ("io_dtype", 7, _abi.GDN_ERR_UNSUPPORTED), ("h_k", 0, _abi.GDN_ERR_INVALID_ARG),
+    ("qkv_tf32", 2, _abi.GDN_ERR_INVALID_ARG)])
 def test_bad_dims_rejected(lib, field, value, code):
     d = _abi.dims(1, 64, 2, 4, True)
     setattr(d, field, value)

@@ -43,12 +43,15 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("qkv_tf32", [False, True])
 @pytest.mark.parametrize("lens,hk,hv,io,dtb", SMALL)
-def test_forward_backward_small(lens, hk, hv, io, dtb):
+def test_forward_backward_small(lens, hk, hv, io, dtb, qkv_tf32):
+    """Both qkv precisions: exact fp32 (the chunk kernels round each q / k / v
+    tile they feed to the tensor cores) and tf32 (the conv rounds once)."""
     w = synth.Workload("small", lens, hk, hv, io=io, backward=True, seed=sum(lens) + hv,
                        dt_bias=dtb)
     inp = synth.make_inputs(w)
-    out = gpu_run(inp, w, backward=True)
+    out = gpu_run(inp, w, backward=True, qkv_tf32=qkv_tf32)
     assert out["status_fwd"] == 0
     for kh in range(hk):
         ref, ch, heads = oracle_group(inp, w, kh, backward=True)
@@ -57,12 +60,17 @@ def test_forward_backward_small(lens, hk, hv, io, dtb):
     full = oracle.backward(**_full_args(inp, w), dy=synth.to_f64(inp["dy"]))
     assert rel(f64(out["dnorm_w"]), full["dnorm_w"]) <= TOL
     assert rel(f64(out["o"]), full["fwd"]["o"]) <= TOL
-    # post-conv activations
+    # post-conv activations: fp32 within 1e-5; tf32 values (the low 13 of the
+    # 23 fraction bits zero) within half a tf32 unit (2^-11) more
     q = f64(out["qkv"])
     T = w.T
-    assert rel(q[:, :hk * 128].reshape(T, hk, 128), full["fwd"]["qh"]) <= 1e-5
-    assert rel(q[:, hk * 128:2 * hk * 128].reshape(T, hk, 128), full["fwd"]["kh"]) <= 1e-5
-    assert rel(q[:, 2 * hk * 128:].reshape(T, hv, 128), full["fwd"]["v"]) <= 1e-5
+    tol_act = 1e-5 + (2.0 ** -11 if qkv_tf32 else 0.0)
+    assert rel(q[:, :hk * 128].reshape(T, hk, 128), full["fwd"]["qh"]) <= tol_act
+    assert rel(q[:, hk * 128:2 * hk * 128].reshape(T, hk, 128), full["fwd"]["kh"]) <= tol_act
+    assert rel(q[:, 2 * hk * 128:].reshape(T, hv, 128), full["fwd"]["v"]) <= tol_act
+    if qkv_tf32:
+        bits = out["qkv"].contiguous().view(torch.int32)
+        assert int((bits & 0x1FFF).count_nonzero()) == 0
 
 
 def _full_args(inp, w, S0=None, cs=None):
