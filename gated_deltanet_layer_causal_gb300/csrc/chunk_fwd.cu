@@ -437,168 +437,216 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
 }
 
 // ------------------------------------------------------------------ output + norm
-// grid (NT, Hv), 256 threads, tcgen05.
+// Persistent: one CTA per SM walks the (chunk, head) tiles t = blockIdx.x,
+// + gridDim.x, ... (chunk = t % NT, head = t / NT).  Per tile, tcgen05:
 //   D1 = Q K^T (64 x 64),  D3 = Q S0^T (64 x 128)       -- issued together
 //   P  = D1 (.) e^{gam_i - gam_j} (.) [i >= j]          -- staged K-major
 //   D2 = P U (64 x 128)
 //   O  = D2 + e^{gam_i} D3 ; y = O rsqrt(mean(O^2)+eps) (1+w) silu(z)
 // Shared memory: Q, K swizzled 32 KB each and U MN-major 32 KB (TMA; U is the
 // B operand of P U, contracted over tokens, so it is read as loaded), S0
-// (K-major rows a) 64 KB (one bulk copy), P 16 KB, the z rows 33 KB.  Tensor
-// memory: 320 fp32 columns.
+// (K-major rows a) 64 KB (one bulk copy), P 16 KB, the z rows 33 KB.  The next
+// tile's Q, K and S0 are requested as soon as D1 and D3 are done, its U and z
+// rows once this tile's O (staged over U) has been stored; its chunk entry and
+// gate values are loaded into registers meanwhile.  Tensor memory: 320 fp32
+// columns, allocated once.
 constexpr int kOutFloats = 64 * 128 * 2 + 128 * 128 + 64 * 128 + 64 * 64 + 64 * kLdK;
 constexpr size_t kOutSmem = sizeof(float) * (kOutFloats + 64 * 2 + 2 * 64 + 16) + 64 + 1024;
 
 template <class IO>
 __global__ void __launch_bounds__(256, 1)
-out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const IO* z,
+out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, const IO* z,
                const float* norm_w, float norm_eps, IO* o_out, IO* y_out, FwdSaved sv) {
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
     float* Qs = sm;                    // [64][128] swizzled
     float* Ks = Qs + 64 * 128;         // [64][128] swizzled
     float* Ss = Ks + 64 * 128;         // [128 (a)][128 (b)] K-major
-    float* Us = Ss + 128 * 128;        // [64 (j)][128 (a)] MN-major U (arrives rounded)
+    float* Us = Ss + 128 * 128;        // [64 (j)][128 (a)] MN-major U; then O, swizzled
     float* Ps = Us + 64 * 128;         // [64 (i)][64 (j)] K-major
     char* Zs = reinterpret_cast<char*>(Ps + 64 * 64);   // z rows, kZPitch bytes apart
     float* gam = Ps + 64 * 64 + 64 * kLdK;
     float* eg = gam + 64;
     float* ssq = eg + 64;              // [2][64] partial sums of squares
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(ssq + 2 * 64 + 16);
-    uint64_t* mbl = mbar + 1;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
-    const ChunkInfo ci = sv.chunks[blockIdx.x];
-    if (ci.len == 0) return;
-    const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
-    const int warp = tid >> 5, lane = tid & 31;
-    auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(ssq + 2 * 64 + 16);   // MMA
+    uint64_t* mA = mbar + 1;           // Q, K, S0
+    uint64_t* mU = mA + 1;             // U
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mU + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ntiles = NT * hv;
+    int t = blockIdx.x;
+    if (t >= ntiles) return;
+    ChunkInfo ci = sv.chunks[t % NT];
+    if (ci.len == 0) return;   // the device check of cu_seqlens failed: every chunk is empty
+    constexpr int kZPitch = kD * (int)sizeof(IO) + 16;    // bytes; conflict-free row reads
+    auto issue_a = [&](const ChunkInfo& c, int tile) {   // one thread
+        const int h = tile / NT, kh = h / (hv / hk);
+        umma::mbar_expect_tx(mA, 2 * 64 * 128 * 4 + 128 * 128 * 4);
+        umma::tma_rows(Qs, 64, &maps.q, kh, c.start, mA);
+        umma::tma_rows(Ks, 64, &maps.k, kh, c.start, mA);
+        umma::bulk_load(Ss, sv.S0 + ((int64_t)(tile % NT) * hv + h) * kD * kD, 128 * 128 * 4, mA);
+    };
+    auto issue_u = [&](const ChunkInfo& c, int tile) {   // one thread
+        umma::mbar_expect_tx(mU, 64 * 128 * 4);
+        umma::tma_rows(Us, 64, &maps.U_mn, tile / NT, c.start, mU);
+    };
+    auto issue_z = [&](const ChunkInfo& c, int tile) {   // all threads, one cp.async group
+        if (z) {
+            constexpr int kPieces = kD * (int)sizeof(IO) / 16;
+            const int h = tile / NT;
+            for (int idx = tid; idx < 64 * kPieces; idx += 256) {
+                const int r = idx / kPieces, p = idx % kPieces;
+                const int64_t tr = (int64_t)c.start + min(r, c.len - 1);
+                cp_async16(Zs + r * kZPitch + p * 16,
+                           reinterpret_cast<const char*>(z + (tr * hv + h) * kD) + p * 16, r < c.len);
+            }
+        }
+        cp_async_commit();
+    };
+    // padding rows continue the last gate value (g = 0)
+    auto gam_of = [&](const ChunkInfo& c, int tile) {
+        return tid < 64 ? sv.gam[(int64_t)(tile / NT) * sv.T + c.start + min(tid, c.len - 1)] : 0.f;
+    };
     if (tid == 0) {
         umma::mbar_init(mbar, 1);
-        umma::mbar_init(mbl, 1);
-        umma::mbar_expect_tx(mbl, 3 * 64 * 128 * 4 + 128 * 128 * 4);
-        umma::tma_rows(Qs, 64, &maps.q, kh, ci.start, mbl);
-        umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
-        umma::tma_rows(Us, 64, &maps.U_mn, h, ci.start, mbl);
-        umma::bulk_load(Ss, sv.S0 + ((int64_t)blockIdx.x * hv + h) * kD * kD, 128 * 128 * 4, mbl);
+        umma::mbar_init(mA, 1);
+        umma::mbar_init(mU, 1);
+        issue_a(ci, t);
+        issue_u(ci, t);
     }
-    if (tid < 64) {  // padding rows continue the last gate value (g = 0)
-        const float g = sv.gam[(int64_t)h * sv.T + row(tid)];
-        gam[tid] = g;
-        eg[tid] = tid < L ? expf(g) : 0.f;
-    }
+    issue_z(ci, t);
+    float g_cur = gam_of(ci, t);
     if (warp == 0) umma::tmem_alloc(tslot, 512);
-    constexpr int kZPitch = kD * (int)sizeof(IO) + 16;    // bytes; conflict-free row reads
-    if (z) {
-        constexpr int kPieces = kD * (int)sizeof(IO) / 16;
-        for (int idx = tid; idx < 64 * kPieces; idx += 256) {
-            const int r = idx / kPieces, p = idx % kPieces;
-            cp_async16(Zs + r * kZPitch + p * 16,
-                       reinterpret_cast<const char*>(z + (row(r) * hv + h) * kD) + p * 16, r < L);
-        }
-    }
-    cp_async_commit();
-    __syncthreads();
-    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
-    if (L < 64) {   // tail rows belong to the next sequence
-        umma::zero_tail_rows(Qs, 64, 0, L);
-        umma::zero_tail_rows(Ks, 64, 0, L);
-        umma::zero_tail_rows(Us, 64, 0, L);
-        __syncthreads();
-    }
-    if (!sv.qkv_tf32) umma::tf32r_inplace(Qs, 64 * 128 * 2);   // Q, K (S0 and U arrive rounded)
-    umma::fence_smem_to_async();
+    umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t tD1 = tmem, tD3 = tmem + 64, tD2 = tmem + 192;
-    if (ok && tid == 0) {
-        umma::mma(tD1, umma::swt(Qs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
-        umma::mma(tD3, umma::swt(Qs, 64), umma::kmaj(Ss, 128), 64, 128, 128, false);
-        umma::commit(mbar);
-    }
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
-    umma::fence_after_sync();
     const int win = warp & 3, half = warp >> 2;
     const int i = win * 16 + lane;     // row held by lanes 0..15 (M = 64 layout)
-    if (ok) {   // P = D1 (.) Gam (.) M  -> K-major rows i; 32 columns per warp, all lanes
-        float v[16];
-        umma::tmem_ld_m64<4>(umma::tmem_at(tD1, half * 32), v);
-        const int rl = umma::frag_row_lo(), cf = umma::frag_col();
-#pragma unroll
-        for (int hr = 0; hr < 2; hr++) {
-            const int r = rl + 8 * hr;
-            const float gr = gam[r];
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                const int j = half * 32 + 8 * k + cf;
-                const float p0 = j <= r ? v[4 * k + 2 * hr] * expf(gr - gam[j]) : 0.f;
-                const float p1 = j + 1 <= r ? v[4 * k + 2 * hr + 1] * expf(gr - gam[j + 1]) : 0.f;
-                *reinterpret_cast<float2*>(Ps + umma::kidx(r, j, 64)) =
-                    make_float2(umma::tf32r(p0), umma::tf32r(p1));
-            }
+    const float4 w4 = z ? ld4(norm_w + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    bool ok = true;
+    for (int it = 0;; it++) {
+        const int h = t / NT, L = ci.len;
+        const int tn = t + (int)gridDim.x;
+        const ChunkInfo cn = tn < ntiles ? sv.chunks[tn % NT] : ci;
+        if (tid < 64) {
+            gam[tid] = g_cur;
+            eg[tid] = tid < L ? expf(g_cur) : 0.f;
         }
-    }
-    umma::fence_smem_to_async();
-    umma::fence_before_sync();
-    __syncthreads();
-    umma::fence_after_sync();
-    if (ok && tid == 0) {
-        umma::mma(tD2, umma::kmaj(Ps, 64), umma::mnt(Us), 64, 128, 64, false);
-        umma::commit(mbar);
-    }
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
-    umma::fence_after_sync();
-    // O = D2 + e^{gam_i} D3 is staged row-major in the Q / K space (consumed by
-    // the first products); the norm and the stores then run row by row on all
-    // lanes, one warp per row, fully coalesced
-    float* Or = Qs;                    // [64][kLdK]
-    if (ok) {
-        float ss = 0.f;
-        for (int cc = 0; cc < 64; cc += 16) {
-            float v2[16], v3[16];
-            umma::tmem_ld16(umma::tmem_at(tD2, half * 64 + cc), v2);
-            umma::tmem_ld16(umma::tmem_at(tD3, half * 64 + cc), v3);
-            if (lane < 16) {
+        ok = __syncthreads_and(umma::mbar_wait(mA, it & 1));   // Q, K, S0; gam visible
+        if (!ok) break;
+        if (L < 64) {   // tail rows belong to the next sequence
+            umma::zero_tail_rows(Qs, 64, 0, L);
+            umma::zero_tail_rows(Ks, 64, 0, L);
+            __syncthreads();
+        }
+        if (!sv.qkv_tf32) umma::tf32r_inplace(Qs, 64 * 128 * 2);   // Q, K (S0 and U arrive rounded)
+        umma::fence_smem_to_async();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {
+            umma::mma(tD1, umma::swt(Qs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
+            umma::mma(tD3, umma::swt(Qs, 64), umma::kmaj(Ss, 128), 64, 128, 128, false);
+            umma::commit(mbar);
+        }
+        ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+        umma::fence_after_sync();
+        if (!ok) break;
+        const bool next = tn < ntiles && cn.len > 0;
+        if (next && tid == 0) issue_a(cn, tn);   // Q, K, S0 consumed
+        const float g_next = next ? gam_of(cn, tn) : 0.f;
+        {   // P = D1 (.) Gam (.) M  -> K-major rows i; 32 columns per warp, all lanes
+            float v[16];
+            umma::tmem_ld_m64<4>(umma::tmem_at(tD1, half * 32), v);
+            const int rl = umma::frag_row_lo(), cf = umma::frag_col();
 #pragma unroll
-                for (int u = 0; u < 16; u += 4) {
-                    float4 x;
-                    x.x = v2[u] + eg[i] * v3[u];
-                    x.y = v2[u + 1] + eg[i] * v3[u + 1];
-                    x.z = v2[u + 2] + eg[i] * v3[u + 2];
-                    x.w = v2[u + 3] + eg[i] * v3[u + 3];
-                    ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
-                    *reinterpret_cast<float4*>(Or + i * kLdK + half * 64 + cc + u) = x;
+            for (int hr = 0; hr < 2; hr++) {
+                const int r = rl + 8 * hr;
+                const float gr = gam[r];
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const int j = half * 32 + 8 * k + cf;
+                    const float p0 = j <= r ? v[4 * k + 2 * hr] * expf(gr - gam[j]) : 0.f;
+                    const float p1 = j + 1 <= r ? v[4 * k + 2 * hr + 1] * expf(gr - gam[j + 1]) : 0.f;
+                    *reinterpret_cast<float2*>(Ps + umma::kidx(r, j, 64)) =
+                        make_float2(umma::tf32r(p0), umma::tf32r(p1));
                 }
             }
         }
-        if (lane < 16) ssq[half * 64 + i] = ss;
-    } else if (tid == 0) {
-        atomicExch(sv.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
+        ok = umma::mbar_wait(mU, it & 1);   // U
+        if (ok && L < 64) umma::zero_tail_rows(Us, 64, 0, L);   // each thread: its own pieces
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        ok = __syncthreads_and(ok);
+        umma::fence_after_sync();
+        if (!ok) break;
+        if (tid == 0) {
+            umma::mma(tD2, umma::kmaj(Ps, 64), umma::mnt(Us), 64, 128, 64, false);
+            umma::commit(mbar);
+        }
+        ok = __syncthreads_and(umma::mbar_wait(mbar, 1));
+        umma::fence_after_sync();
+        if (!ok) break;
+        // O = D2 + e^{gam_i} D3, staged as a swizzled tile over U (consumed);
+        // the norm and the stores then run row by row on all lanes, one warp
+        // per row, fully coalesced
+        float* Or = Us;
+        {
+            float ss = 0.f;
+            for (int cc = 0; cc < 64; cc += 16) {
+                float v2[16], v3[16];
+                umma::tmem_ld16(umma::tmem_at(tD2, half * 64 + cc), v2);
+                umma::tmem_ld16(umma::tmem_at(tD3, half * 64 + cc), v3);
+                if (lane < 16) {
+#pragma unroll
+                    for (int u = 0; u < 16; u += 4) {
+                        float4 x;
+                        x.x = v2[u] + eg[i] * v3[u];
+                        x.y = v2[u + 1] + eg[i] * v3[u + 1];
+                        x.z = v2[u + 2] + eg[i] * v3[u + 2];
+                        x.w = v2[u + 3] + eg[i] * v3[u + 3];
+                        ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+                        *reinterpret_cast<float4*>(Or + umma::swz(i, half * 64 + cc + u, 64)) = x;
+                    }
+                }
+            }
+            if (lane < 16) ssq[half * 64 + i] = ss;
+        }
+        cp_async_wait<0>();   // z rows
+        umma::fence_before_sync();
+        __syncthreads();
+        for (int r = warp; r < L; r += 8) {
+            const int64_t tok = ci.start + r;
+            const int64_t off = (tok * hv + h) * kD + lane * 4;
+            const float4 o4 = *reinterpret_cast<const float4*>(Or + umma::swz(r, lane * 4, 64));
+            st4(sv.o + off, o4);
+            if (o_out) st4(o_out + off, o4);
+            if (z) {
+                const float rs = rsqrtf((ssq[r] + ssq[64 + r]) * (1.f / kD) + norm_eps);
+                const float4 z4 = ld4(reinterpret_cast<const IO*>(Zs + r * kZPitch) + lane * 4);
+                float4 y4;
+                y4.x = o4.x * rs * (1.f + w4.x) * siluf_(z4.x);
+                y4.y = o4.y * rs * (1.f + w4.y) * siluf_(z4.y);
+                y4.z = o4.z * rs * (1.f + w4.z) * siluf_(z4.z);
+                y4.w = o4.w * rs * (1.f + w4.w) * siluf_(z4.w);
+                st4(y_out + off, y4);
+                if (lane == 0) sv.rstd[tok * hv + h] = rs;
+            }
+        }
+        umma::fence_smem_to_async();   // O staging -> the next U load
+        __syncthreads();               // O, z and the sums of squares are read
+        if (!next) break;
+        if (tid == 0) issue_u(cn, tn);
+        issue_z(cn, tn);
+        g_cur = g_next;
+        ci = cn;
+        t = tn;
     }
-    cp_async_wait<0>();
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 512);
-    if (!ok) return;
-    const float4 w4 = z ? ld4(norm_w + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int r = warp; r < L; r += 8) {
-        const int64_t t = ci.start + r;
-        const int64_t off = (t * hv + h) * kD + lane * 4;
-        const float4 o4 = *reinterpret_cast<const float4*>(Or + r * kLdK + lane * 4);
-        st4(sv.o + off, o4);
-        if (o_out) st4(o_out + off, o4);
-        if (z) {
-            const float rs = rsqrtf((ssq[r] + ssq[64 + r]) * (1.f / kD) + norm_eps);
-            const float4 z4 = ld4(reinterpret_cast<const IO*>(Zs + r * kZPitch) + lane * 4);
-            float4 y4;
-            y4.x = o4.x * rs * (1.f + w4.x) * siluf_(z4.x);
-            y4.y = o4.y * rs * (1.f + w4.y) * siluf_(z4.y);
-            y4.z = o4.z * rs * (1.f + w4.z) * siluf_(z4.z);
-            y4.w = o4.w * rs * (1.f + w4.w) * siluf_(z4.w);
-            st4(y_out + off, y4);
-            if (lane == 0) sv.rstd[t * hv + h] = rs;
-        }
-    }
+    if (!ok && tid == 0) atomicExch(sv.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
 }
 
 // ------------------------------------------------------------------ launchers
@@ -651,9 +699,14 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
             maps, a.hk, a.hv, a.S_init, a.S_final, a.sv);
     }
     if (a.NT > 0) {
+        int dev = 0, nsm = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        const int ntiles = a.NT * a.hv;
         GDN_PROF("chunk_out_fwd", st);
-        out_fwd_kernel<IO><<<dim3(a.NT, a.hv), 256, kOutSmem, st>>>(
-            maps, a.hk, a.hv, (const IO*)a.z, a.norm_w, a.norm_eps, (IO*)a.o_out,
+        out_fwd_kernel<IO><<<min(ntiles, nsm), 256, kOutSmem, st>>>(
+            maps, a.hk, a.hv, a.NT, (const IO*)a.z, a.norm_w, a.norm_eps, (IO*)a.o_out,
             (IO*)a.y_out, a.sv);
     }
     return cudaGetLastError();
