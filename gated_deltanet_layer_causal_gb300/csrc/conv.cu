@@ -19,6 +19,12 @@ namespace gdn {
 constexpr int kConvWarps = 8;
 constexpr int kConvRun = 64;   // tokens per warp
 constexpr int kConvRing = 3;   // backward: four-token steps each lane holds in its copy ring
+constexpr int kConvFwdRing = 4;   // forward: the same, input rows only
+
+template <class T>
+constexpr size_t conv_fwd_smem() {
+    return (size_t)kConvFwdRing * 4 * kConvWarps * 32 * 4 * sizeof(T);
+}
 
 // Backward shared memory: per lane a ring of kConvRing steps, each four rows of
 // the incoming gradient (float4) and four new input rows (4 x T); reused for
@@ -61,6 +67,8 @@ __global__ void __launch_bounds__(kConvWarps * 32)
 conv_fwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* cs_in,
                 const int32_t* __restrict__ cu, int N, int64_t Ttot, int C, int hk,
                 float l2_eps, float q_scale, bool rnd, float* __restrict__ out) {
+    extern __shared__ __align__(16) unsigned char conv_fwd_smem_raw[];
+    T* ring = reinterpret_cast<T*>(conv_fwd_smem_raw);   // [ring][4][threads][4]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int grp = blockIdx.y;
     const int c = grp * kD + lane * 4;
@@ -82,12 +90,29 @@ conv_fwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
     float4 h3 = conv_in(x, cs_in, t0 - 3, s, n, C, c);
     int64_t t = t0;
     if (t1 <= e) {
-        // the whole run lies in one sequence: four tokens per step, loaded
-        // together, with independent reductions
-        for (; t + 4 <= t1; t += 4) {
+        // the whole run lies in one sequence: four tokens per step with
+        // independent reductions; each lane copies its own input rows
+        // kConvFwdRing-1 steps ahead into its ring slots (cp.async)
+        constexpr int kThr = kConvWarps * 32;
+        const int tid = threadIdx.x, nsteps = (int)((t1 - t0) / 4);
+        auto issue = [&](int i) {
+            if (i < nsteps) {
+#pragma unroll
+                for (int u = 0; u < 4; u++)
+                    cp_async_row4(&ring[(((i % kConvFwdRing) * 4 + u) * kThr + tid) * 4],
+                                  x + (t0 + 4 * (int64_t)i + u) * C + c);
+            }
+            cp_async_commit();
+        };
+#pragma unroll
+        for (int i = 0; i < kConvFwdRing - 1; i++) issue(i);
+        for (int i = 0; i < nsteps; i++, t += 4) {
+            issue(i + kConvFwdRing - 1);   // the slot step i-1 used
+            cp_async_wait<kConvFwdRing - 1>();
             float4 xs[4], o[4];
 #pragma unroll
-            for (int u = 0; u < 4; u++) xs[u] = ld4(x + (t + u) * C + c);
+            for (int u = 0; u < 4; u++)
+                xs[u] = ld4(&ring[(((i % kConvFwdRing) * 4 + u) * kThr + tid) * 4]);
             const float4 hw[7] = {h3, h2, h1, xs[0], xs[1], xs[2], xs[3]};   // x[t-3 .. t+3]
 #pragma unroll
             for (int u = 0; u < 4; u++) {
@@ -115,6 +140,7 @@ conv_fwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
             for (int u = 0; u < 4; u++) st4(out + (t + u) * C + c, rnd ? tf32_round(o[u]) : o[u]);
             h3 = xs[1]; h2 = xs[2]; h1 = xs[3];
         }
+        cp_async_wait<0>();
     }
     for (; t < t1; t++) {
         if (t >= e) {  // next (non-empty) sequence starts at t
@@ -186,14 +212,20 @@ __device__ __forceinline__ float4 conv_dpre_w(float4 a0, float4 a1, float4 a2, f
 #pragma unroll
     for (int i = 0; i < 4; i++) { sg[i] = sigmoidf_(p[i]); xc[i] = p[i] * sg[i]; }
     if (norm) {
-        float ss = warp_sum(xc[0] * xc[0] + xc[1] * xc[1] + xc[2] * xc[2] + xc[3] * xc[3]);
-        float r = rsqrtf(ss + l2_eps);
-        float u[4], du[4], dot = 0.f;
+        // with u = xc r, r = (|xc|^2 + eps)^-1/2 and du = scale g:
+        //   d xc = r (du - u (u . du)),  u . du = r scale (xc . g),
+        // so |xc|^2 and xc . g come from one (two-value) warp reduction
+        float ss = xc[0] * xc[0] + xc[1] * xc[1] + xc[2] * xc[2] + xc[3] * xc[3];
+        float xg = xc[0] * gd[0] + xc[1] * gd[1] + xc[2] * gd[2] + xc[3] * gd[3];
 #pragma unroll
-        for (int i = 0; i < 4; i++) { u[i] = xc[i] * r; du[i] = gd[i] * scale; dot += u[i] * du[i]; }
-        dot = warp_sum(dot);
+        for (int m = 16; m >= 1; m >>= 1) {
+            ss += __shfl_xor_sync(0xffffffffu, ss, m);
+            xg += __shfl_xor_sync(0xffffffffu, xg, m);
+        }
+        const float r = rsqrtf(ss + l2_eps);
+        const float rs = r * scale, c = r * r * xg;
 #pragma unroll
-        for (int i = 0; i < 4; i++) gd[i] = r * (du[i] - u[i] * dot);
+        for (int i = 0; i < 4; i++) gd[i] = rs * (gd[i] - xc[i] * c);
     }
     float4 o;
     o.x = gd[0] * sg[0] * (1.f + p[0] * (1.f - sg[0]));
@@ -409,8 +441,14 @@ cudaError_t launch_conv_fwd_t(const ConvArgs& a, cudaStream_t st) {
     if (a.T > 0) {
         dim3 grid((unsigned)((a.T + kConvWarps * kConvRun - 1) / (kConvWarps * kConvRun)),
                   (unsigned)(a.C / kD));
+        static bool attr = false;
+        if (!attr) {
+            cudaFuncSetAttribute(conv_fwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)conv_fwd_smem<T>());
+            attr = true;
+        }
         GDN_PROF("conv_fwd", st);
-        conv_fwd_kernel<T><<<grid, kConvWarps * 32, 0, st>>>(
+        conv_fwd_kernel<T><<<grid, kConvWarps * 32, conv_fwd_smem<T>(), st>>>(
             (const T*)a.x, a.w, (const T*)a.cs_in, a.cu, a.N, a.T, a.C, a.hk, a.l2_eps,
             a.q_scale, a.round_tf32, a.qkv);
     }
