@@ -175,15 +175,19 @@ class Step:
 # proportional to the chunks it processes).  Valid for the kernels as captured;
 # a kernel changed since then reports null.
 TRAFFIC_64K = {
-    "conv_fwd": 3649505280,
-    "chunk_state_fwd": 11317725184,
-    "chunk_out_fwd": 8939784192,
-    "chunk_bwd_state": 10358249472,
-    "chunk_bwd_sfacing": 17131732992,
-    "chunk_bwd_dp": 7226800128,
-    "chunk_bwd_wy": 10072883200,
-    "gva_sum": 9021515776,
-    "conv_bwd": 5434595328,
+    "conv_fwd": 3621126144,
+    "gates": 12664832,
+    "chunk_prep": 6532542464,
+    "chunk_state_fwd": 13292943360,
+    "chunk_out_fwd": 8940701696,
+    "chunk_norm_bwd": 5314938880,
+    "chunk_bwd_local": 4016697344,
+    "chunk_bwd_state": 10367154176,
+    "chunk_bwd_dp": 7216646144,
+    "chunk_bwd_sfacing": 17125507072,
+    "chunk_bwd_wy": 10132076544,
+    "gva_sum": 9019969536,
+    "conv_bwd": 5590620160,
 }
 
 
@@ -318,7 +322,9 @@ def run_ours(args, rank, world, dev):
             "config": {"workload": w.name, "tokens": w.T, "seqs": w.N, "h_k": w.h_k,
                        "h_v": w.h_v, "d_k": D, "d_v": D, "chunk": 64, "conv_k": 4,
                        "io": w.io, "state": "fp32",
-                       "mma": "tf32 tcgen05 (chunk kernels), tf32 mma.sync (state passes)",
+                       "mma": "tf32 tcgen05 (chunk kernels, reverse state pass), "
+                              "tf32 mma.sync (forward state pass)",
+                       "qkv": "conv output stored at tf32 precision",
                        "passes": "fwd+bwd (conv, chunk rule, fused gated norm)",
                        "l2": "inputs larger than L2 (x alone is %.2f GB)" % (
                            w.T * w.C * 2 / 1e9),
