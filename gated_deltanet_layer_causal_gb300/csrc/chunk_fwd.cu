@@ -113,19 +113,24 @@ gates_kernel(const IO* __restrict__ av, const IO* __restrict__ bv, const float* 
 }
 
 // ------------------------------------------------------------------ prep
-// grid (NT, Hv), 256 threads, tcgen05.  With the gates from gates_kernel,
+// Persistent: one CTA per SM walks the (chunk, head) tiles t = blockIdx.x,
+// + gridDim.x, ... (chunk = t % NT, head = t / NT).  Per tile, tcgen05, with
+// the gates from gates_kernel:
 //   D1 = K K^T (64 x 64)  ->  A = beta_i e^{gam_i-gam_j} D1 (j < i)
 //   T  = (I + A)^-1        (forward substitution on the CUDA cores; saved)
 //   W = (T diag(beta e^gam)) K,  U~ = (T diag(beta)) V      (M=64, N=128, K=64 each)
 // K arrives twice through the TMA, as a K-major tile for K K^T and as an
 // MN-major tile for W (contracted over tokens), V once, MN-major; the gate
-// scalings go into the two A tiles, so no tile is transposed.
+// scalings go into the two A tiles, so no tile is transposed.  W and U~ are
+// staged over the A / T scratch, so the next tile's K and V are requested as
+// soon as the second products are done; its chunk entry and gates are loaded
+// into registers meanwhile.  Tensor memory allocated once.
 constexpr int kLdK = 132, kLdA = 68;
 constexpr int kPrepFloats = 3 * 64 * 128 + 2 * 64 * kLdA + 2 * 64 * 64;
 constexpr size_t kPrepSmem = sizeof(float) * (kPrepFloats + 3 * 64 + 16) + 64 + 1024;
 
 __global__ void __launch_bounds__(256, 1)
-prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv) {
+prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSaved sv) {
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
     float* Ks = sm;                    // [64][128] swizzled K-major K
@@ -135,136 +140,175 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv) 
     float* Tr = As + 64 * kLdA;        // [64][kLdA] row-major T
     float* Tk = Tr + 64 * kLdA;        // [64][64] K-major T diag(beta e^gam)
     float* Tv = Tk + 64 * 64;          // [64][64] K-major T diag(beta)
+    float* Wst = As;                   // [64][128] swizzled W, over A and T (1 KB-aligned)
+    float* Ust = Tk;                   // [64][128] swizzled U~, over Tk and Tv (1 KB-aligned)
     float* gam = Tv + 64 * 64;
     float* bet = gam + 64;
     float* be = bet + 64;
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(be + 64 + 16);
-    uint64_t* mbl = mbar + 1;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
-    const ChunkInfo ci = sv.chunks[blockIdx.x];
-    if (ci.len == 0) return;
-    const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
-    const int warp = tid >> 5;
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(be + 64 + 16);   // MMA
+    uint64_t* mA = mbar + 1;           // K, K (MN-major), V
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mA + 1);
+    static_assert(2 * 64 * kLdA >= 64 * 128 && (3 * 64 * 128 * 4) % 1024 == 0 &&
+                      ((3 * 64 * 128 + 2 * 64 * kLdA) * 4) % 1024 == 0,
+                  "staging tiles fit the A / T scratch and are 1 KB-aligned");
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int ntiles = NT * hv;
+    int t = blockIdx.x;
+    if (t >= ntiles) return;
+    ChunkInfo ci = sv.chunks[t % NT];
+    if (ci.len == 0) return;   // the device check of cu_seqlens failed: every chunk is empty
+    auto issue = [&](const ChunkInfo& c, int tile) {   // one thread
+        const int h = tile / NT, kh = h / (hv / hk);
+        umma::mbar_expect_tx(mA, 3 * 64 * 128 * 4);
+        umma::tma_rows(Ks, 64, &maps.k, kh, c.start, mA);
+        umma::tma_rows(Km, 64, &maps.k_mn, kh, c.start, mA);
+        umma::tma_rows(Vm, 64, &maps.v_mn, h, c.start, mA);
+    };
+    // padding rows continue the last gam (g = 0), beta = 0
+    auto gates_of = [&](const ChunkInfo& c, int tile, float& gm, float& bt) {
+        const int h = tile / NT;
+        gm = tid < 64 ? sv.gam[(int64_t)h * sv.T + c.start + min(tid, c.len - 1)] : 0.f;
+        bt = tid < c.len ? sv.beta[(int64_t)h * sv.T + c.start + tid] : 0.f;
+    };
     if (tid == 0) {
         umma::mbar_init(mbar, 1);
-        umma::mbar_init(mbl, 1);
-        umma::mbar_expect_tx(mbl, 3 * 64 * 128 * 4);
-        umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
-        umma::tma_rows(Km, 64, &maps.k_mn, kh, ci.start, mbl);
-        umma::tma_rows(Vm, 64, &maps.v_mn, h, ci.start, mbl);
+        umma::mbar_init(mA, 1);
+        issue(ci, t);
     }
-    if (tid < 64) {   // padding rows continue the last gam (g = 0), beta = 0
-        const float gm = sv.gam[(int64_t)h * sv.T + ci.start + min(tid, L - 1)];
-        const float bt = tid < L ? sv.beta[(int64_t)h * sv.T + ci.start + tid] : 0.f;
-        gam[tid] = gm;
-        bet[tid] = bt;
-        be[tid] = bt * expf(gm);
-    }
+    float g_cur = 0.f, b_cur = 0.f;
+    gates_of(ci, t, g_cur, b_cur);
     if (warp == 0) umma::tmem_alloc(tslot, 512);
-    __syncthreads();
-    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
-    if (L < 64) {   // tail rows belong to the next sequence
-        umma::zero_tail_rows(Ks, 64, 0, L);
-        umma::zero_tail_rows(Km, 64, 0, L);
-        umma::zero_tail_rows(Vm, 64, 0, L);
-        __syncthreads();
-    }
-    if (!sv.qkv_tf32) umma::tf32r_inplace(Ks, 3 * 64 * 128);   // K (both layouts), V
-    umma::fence_smem_to_async();
+    umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t tD1 = tmem, tD2 = tmem + 256;
-    if (ok && tid == 0) {
-        umma::mma(tD1, umma::swt(Ks, 64), umma::swt(Ks, 64), 64, 64, 128, false);
-        umma::commit(mbar);
-    }
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
-    umma::fence_after_sync();
     const int half = warp >> 2;
-    if (ok) {   // A = beta_i e^{gam_i - gam_j} D1 (j < i); 32 columns per warp, all lanes
-        float v[16];
-        umma::tmem_ld_m64<4>(umma::tmem_at(tD1, half * 32), v);
-        const int rl = umma::frag_row_lo(), cf = umma::frag_col();
+    bool ok = true;
+    for (int it = 0;; it++) {
+        const int h = t / NT, L = ci.len;
+        const int tn = t + (int)gridDim.x;
+        const ChunkInfo cn = tn < ntiles ? sv.chunks[tn % NT] : ci;
+        if (tid < 64) {
+            gam[tid] = g_cur;
+            bet[tid] = b_cur;
+            be[tid] = b_cur * expf(g_cur);
+        }
+        if (tid == 0) umma::bulk_wait_read();   // the last tile's stores have read W / U~
+        ok = __syncthreads_and(umma::mbar_wait(mA, it & 1));   // K, V; gates visible
+        if (!ok) break;
+        if (L < 64) {   // tail rows belong to the next sequence
+            umma::zero_tail_rows(Ks, 64, 0, L);
+            umma::zero_tail_rows(Km, 64, 0, L);
+            umma::zero_tail_rows(Vm, 64, 0, L);
+            __syncthreads();
+        }
+        if (!sv.qkv_tf32) umma::tf32r_inplace(Ks, 3 * 64 * 128);   // K (both layouts), V
+        umma::fence_smem_to_async();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {
+            umma::mma(tD1, umma::swt(Ks, 64), umma::swt(Ks, 64), 64, 64, 128, false);
+            umma::commit(mbar);
+        }
+        ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+        umma::fence_after_sync();
+        if (!ok) break;
+        {   // A = beta_i e^{gam_i - gam_j} D1 (j < i); 32 columns per warp, all lanes
+            float v[16];
+            umma::tmem_ld_m64<4>(umma::tmem_at(tD1, half * 32), v);
+            const int rl = umma::frag_row_lo(), cf = umma::frag_col();
 #pragma unroll
-        for (int hr = 0; hr < 2; hr++) {
-            const int r = rl + 8 * hr;
-            const float br = bet[r], gr = gam[r];
+            for (int hr = 0; hr < 2; hr++) {
+                const int r = rl + 8 * hr;
+                const float br = bet[r], gr = gam[r];
 #pragma unroll
-            for (int k = 0; k < 4; k++) {
-                const int j = half * 32 + 8 * k + cf;
-                *reinterpret_cast<float2*>(As + r * kLdA + j) = make_float2(
-                    j < r ? br * expf(gr - gam[j]) * v[4 * k + 2 * hr] : 0.f,
-                    j + 1 < r ? br * expf(gr - gam[j + 1]) * v[4 * k + 2 * hr + 1] : 0.f);
+                for (int k = 0; k < 4; k++) {
+                    const int j = half * 32 + 8 * k + cf;
+                    *reinterpret_cast<float2*>(As + r * kLdA + j) = make_float2(
+                        j < r ? br * expf(gr - gam[j]) * v[4 * k + 2 * hr] : 0.f,
+                        j + 1 < r ? br * expf(gr - gam[j + 1]) * v[4 * k + 2 * hr + 1] : 0.f);
+                }
             }
         }
-    }
-    __syncthreads();
-    tril_inverse64(As, kLdA, Tr, kLdA, Tk);   // Tk doubles as scratch
-    __syncthreads();
-    for (int idx = tid; idx < 64 * 16; idx += 256) {   // T diag(.) -> K-major rows i
-        const int r = idx >> 4, c = (idx & 15) * 4;
-        const float4 t4 = *reinterpret_cast<const float4*>(Tr + r * kLdA + c);
-        *reinterpret_cast<float4*>(Tk + umma::kidx(r, c, 64)) = umma::tf32r(
-            make_float4(t4.x * be[c], t4.y * be[c + 1], t4.z * be[c + 2], t4.w * be[c + 3]));
-        *reinterpret_cast<float4*>(Tv + umma::kidx(r, c, 64)) = umma::tf32r(
-            make_float4(t4.x * bet[c], t4.y * bet[c + 1], t4.z * bet[c + 2], t4.w * bet[c + 3]));
-    }
-    umma::fence_smem_to_async();
-    umma::fence_before_sync();
-    __syncthreads();
-    umma::fence_after_sync();
-    if (ok && tid == 0) {
-        umma::mma(tD2, umma::kmaj(Tk, 64), umma::mnt(Km), 64, 128, 64, false);
-        umma::mma(tD2 + 128, umma::kmaj(Tv, 64), umma::mnt(Vm), 64, 128, 64, false);
-        umma::commit(mbar);
-    }
-    {   // T for the backward, as K-major rows i and as K-major rows j (T^T), rounded
-        float* Tg = sv.Tm + ((int64_t)blockIdx.x * hv + h) * 2 * 64 * 64;
-        for (int idx = tid; idx < 64 * 16; idx += 256) {
-            const int r = idx & 63, c4 = idx >> 6;
-            st4(Tg + umma::kidx(r, 4 * c4, 64),
-                umma::tf32r(*reinterpret_cast<const float4*>(Tr + r * kLdA + 4 * c4)));
-            st4(Tg + 64 * 64 + umma::kidx(r, 4 * c4, 64),
-                umma::tf32r(make_float4(Tr[(4 * c4) * kLdA + r], Tr[(4 * c4 + 1) * kLdA + r],
-                                        Tr[(4 * c4 + 2) * kLdA + r], Tr[(4 * c4 + 3) * kLdA + r])));
+        __syncthreads();
+        const bool next = tn < ntiles && cn.len > 0;   // the entry has arrived by now
+        float g_next = 0.f, b_next = 0.f;
+        if (next) gates_of(cn, tn, g_next, b_next);
+        tril_inverse64(As, kLdA, Tr, kLdA, Tk);   // Tk doubles as scratch
+        __syncthreads();
+        for (int idx = tid; idx < 64 * 16; idx += 256) {   // T diag(.) -> K-major rows i
+            const int r = idx >> 4, c = (idx & 15) * 4;
+            const float4 t4 = *reinterpret_cast<const float4*>(Tr + r * kLdA + c);
+            *reinterpret_cast<float4*>(Tk + umma::kidx(r, c, 64)) = umma::tf32r(
+                make_float4(t4.x * be[c], t4.y * be[c + 1], t4.z * be[c + 2], t4.w * be[c + 3]));
+            *reinterpret_cast<float4*>(Tv + umma::kidx(r, c, 64)) = umma::tf32r(
+                make_float4(t4.x * bet[c], t4.y * bet[c + 1], t4.z * bet[c + 2], t4.w * bet[c + 3]));
         }
-    }
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
-    umma::fence_after_sync();
-    // warp half 0 -> W (columns 0..127), half 1 -> U~ (128..255), staged as
-    // swizzled tiles in the K / V space (consumed) and stored whole
-    if (ok) {
-        float* Sw = half == 0 ? Ks : Km;
-        float v[32];
-#pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 64) {
-            umma::tmem_ld64_m64(umma::tmem_at(tD2, half * 128 + c0), v);
-            if (half == 0)   // W is only ever a tensor-core operand: stored rounded
-#pragma unroll
-                for (int k = 0; k < 32; k++) v[k] = umma::tf32r(v[k]);
-            umma::frag_to_sw(Sw, v, c0, 1.f, 1.f);
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {
+            umma::mma(tD2, umma::kmaj(Tk, 64), umma::mnt(Km), 64, 128, 64, false);
+            umma::mma(tD2 + 128, umma::kmaj(Tv, 64), umma::mnt(Vm), 64, 128, 64, false);
+            umma::commit(mbar);
         }
-    } else if (tid == 0) {
-        atomicExch(sv.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
+        {   // T for the backward, as K-major rows i and as K-major rows j (T^T), rounded
+            float* Tg = sv.Tm + ((int64_t)(t % NT) * hv + h) * 2 * 64 * 64;
+            for (int idx = tid; idx < 64 * 16; idx += 256) {
+                const int r = idx & 63, c4 = idx >> 6;
+                st4(Tg + umma::kidx(r, 4 * c4, 64),
+                    umma::tf32r(*reinterpret_cast<const float4*>(Tr + r * kLdA + 4 * c4)));
+                st4(Tg + 64 * 64 + umma::kidx(r, 4 * c4, 64),
+                    umma::tf32r(make_float4(Tr[(4 * c4) * kLdA + r], Tr[(4 * c4 + 1) * kLdA + r],
+                                            Tr[(4 * c4 + 2) * kLdA + r], Tr[(4 * c4 + 3) * kLdA + r])));
+            }
+        }
+        ok = __syncthreads_and(umma::mbar_wait(mbar, 1));
+        umma::fence_after_sync();
+        if (!ok) break;
+        if (next && tid == 0) issue(cn, tn);   // K, K (MN-major) and V consumed
+        // warp half 0 -> W (columns 0..127), half 1 -> U~ (128..255), staged as
+        // swizzled tiles over the A / T scratch and stored whole
+        {
+            float* Sw = half == 0 ? Wst : Ust;
+            float v[32];
+#pragma unroll
+            for (int c0 = 0; c0 < 128; c0 += 64) {
+                umma::tmem_ld64_m64(umma::tmem_at(tD2, half * 128 + c0), v);
+                if (half == 0)   // W is only ever a tensor-core operand: stored rounded
+#pragma unroll
+                    for (int k = 0; k < 32; k++) v[k] = umma::tf32r(v[k]);
+                umma::frag_to_sw(Sw, v, c0, 1.f, 1.f);
+            }
+        }
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        if (L == 64) {
+            if (tid == 0) {
+                umma::tma_store_rows(&maps.W, h, ci.start, Wst);
+                umma::tma_store_rows(&maps.U, h, ci.start, Ust);
+                umma::bulk_commit();
+            }
+        } else {
+            const int64_t off = ((int64_t)ci.start * hv + h) * kD;
+            umma::store_rows_sw(sv.W + off, (int64_t)hv * kD, Wst, L);
+            umma::store_rows_sw(sv.U + off, (int64_t)hv * kD, Ust, L);
+            __syncthreads();
+        }
+        if (!next) break;
+        g_cur = g_next;
+        b_cur = b_next;
+        ci = cn;
+        t = tn;
     }
-    umma::fence_smem_to_async();
+    if (tid == 0) umma::bulk_wait_read();
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 512);
-    if (!ok) return;
-    if (L == 64) {
-        if (tid == 0) {
-            umma::tma_store_rows(&maps.W, h, ci.start, Ks);
-            umma::tma_store_rows(&maps.U, h, ci.start, Km);
-            umma::bulk_commit();
-            umma::bulk_wait_read();
-        }
-    } else {
-        const int64_t off = ((int64_t)ci.start * hv + h) * kD;
-        umma::store_rows_sw(sv.W + off, (int64_t)hv * kD, Ks, L);
-        umma::store_rows_sw(sv.U + off, (int64_t)hv * kD, Km, L);
-    }
+    if (!ok && tid == 0) atomicExch(sv.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
 }
 
 // ------------------------------------------------------------------ state pass
@@ -690,8 +734,12 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
         if (e == cudaSuccess)
             e = make_rows_map(&maps.v_mn, a.qkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C, true);
         if (e != cudaSuccess) return e;
+        int dev = 0, nsm = 0;
+        e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
         GDN_PROF("chunk_prep", st);
-        prep_kernel<<<dim3(a.NT, a.hv), 256, kPrepSmem, st>>>(maps, a.hk, a.hv, a.sv);
+        prep_kernel<<<min(a.NT * a.hv, nsm), 256, kPrepSmem, st>>>(maps, a.hk, a.hv, a.NT, a.sv);
     }
     if (a.N > 0) {
         GDN_PROF("chunk_state_fwd", st);
