@@ -175,19 +175,19 @@ class Step:
 # proportional to the chunks it processes).  Valid for the kernels as captured;
 # a kernel changed since then reports null.
 TRAFFIC_64K = {
-    "conv_fwd": 3619905536,
-    "gates": 12670976,
-    "chunk_prep": 6526447616,
-    "chunk_state_fwd": 13296275456,
-    "chunk_out_fwd": 8943708160,
-    "chunk_norm_bwd": 5314924544,
-    "chunk_bwd_local": 4019826688,
-    "chunk_bwd_state": 10366859264,
-    "chunk_bwd_dp": 7216392192,
-    "chunk_bwd_sfacing": 17132238848,
-    "chunk_bwd_wy": 10132508672,
-    "gva_sum": 9019389952,
-    "conv_bwd": 5589868544,
+    "conv_fwd": 3617740800,
+    "gates": 12664832,
+    "chunk_prep": 6524026880,
+    "chunk_state_fwd": 13298647040,
+    "chunk_out_fwd": 8936091648,
+    "chunk_norm_bwd": 5315977216,
+    "chunk_bwd_local": 4016160768,
+    "chunk_bwd_state": 10366060544,
+    "chunk_bwd_dp": 7217473536,
+    "chunk_bwd_sfacing": 17370228736,
+    "chunk_bwd_wy": 10128762880,
+    "gva_sum": 9020360704,
+    "conv_bwd": 5590226944,
 }
 
 

@@ -402,20 +402,23 @@ bwd_state_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
 }
 
 // ------------------------------------------------------------------ B3a: state-facing terms
-// grid (NT, Hv), 256 threads, tcgen05.  Per chunk:
+// Persistent: one CTA per SM walks the (chunk, head) tiles t = blockIdx.x,
+// + gridDim.x, ... (chunk = t % NT, head = t / NT).  Per tile, tcgen05:
 //   [X; Y] = [dO; dU] S0     (one M=128, N=128, K=128 MMA; X = dO S0, Y = dU S0)
 //   dK~    = U dS            (M=64, N=128, K=128)
 // then dQ partial = e^gam X, dW = -Y, dK partial = fk dK~, and the dgam terms
 //   dgam_i += e^{gam_i} X_i . Q_i,  dgam_j -= Z_j = fk_j dK~_j . K_j,
 //   dgam_{L-1} += sum_j Z_j + e^{gam_L} <dS, S0>.
 // Shared memory: [dO; dU] 64 KB and U 32 KB swizzled (TMA), S0^T and dS^T
-// 64 KB each, K-major rows b (one bulk copy each).  Tensor memory: 256 fp32
-// columns.
+// 64 KB each, K-major rows b (one bulk copy each).  dS^T is free once the
+// products are done and takes the next tile's at once; the other tiles hold
+// this tile's Q, K and staged outputs until its stores have read them.
+// Tensor memory: 256 fp32 columns, allocated once.
 constexpr int kSfFloats = 128 * 128 * 3 + 64 * 128;
 constexpr size_t kB3aSmem = sizeof(float) * (kSfFloats + 64 * 3 + 2 * 128 + 16) + 64 + 1024;
 
 __global__ void __launch_bounds__(256, 1)
-bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv,
+bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSaved sv,
                    BwdScratch w) {
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
@@ -428,78 +431,101 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSav
     float* gam = fk + 64;
     float* rpart = gam + 64;             // [2][128]
     float* red = rpart + 2 * 128;        // [16]
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(red + 16);
-    uint64_t* mbl = mbar + 1;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
-    const ChunkInfo ci = sv.chunks[blockIdx.x];
-    if (ci.len == 0) return;
-    const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
-    const int warp = tid >> 5, lane = tid & 31;
-    const int64_t sb = ((int64_t)blockIdx.x * hv + h) * kD * kD;
-    // ---- stage operands: row tiles through the TMA; dS^T and S0^T are stored
-    // as K-major tiles with rows b, copied whole
-    if (tid == 0) {
-        umma::mbar_init(mbar, 1);
-        umma::mbar_init(mbl, 1);
-        umma::mbar_expect_tx(mbl, 3 * 64 * 128 * 4 + 2 * 128 * 128 * 4);
-        umma::tma_rows(A1, 128, &maps.dO, h, ci.start, mbl);
-        umma::tma_rows(A1 + 64 * 32, 128, &maps.dU, h, ci.start, mbl);
-        umma::tma_rows(A2, 64, &maps.U, h, ci.start, mbl);
-        umma::bulk_load(DST, w.dS + sb, 128 * 128 * 4, mbl);
-        umma::bulk_load(S0T, sv.S0b + sb, 128 * 128 * 4, mbl);
-    }
-    load_gam(gam, sv, ci, h);
-    if (warp == 0) umma::tmem_alloc(tslot, 256);
-    __syncthreads();
-    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
-    if (L < 64) {   // tail rows belong to the next sequence
-        umma::zero_tail_rows(A1, 128, 0, L);
-        umma::zero_tail_rows(A1, 128, 64, L);
-        umma::zero_tail_rows(A2, 64, 0, L);
-    }
-    {   // <dS, S0> over the staged copies (same layout, same index), before rounding
-        float dot = 0.f;
-        for (int i = tid; i < 128 * 128; i += 256) dot += S0T[i] * DST[i];
-        dot = warp_sum(dot);
-        if (lane == 0) red[warp] = dot;
-    }
-    __syncthreads();
-    umma::tf32r_inplace(S0T, 2 * 128 * 128);   // S0^T, dS^T (dO, dU, U arrive rounded)
-    umma::fence_smem_to_async();
-    __syncthreads();
-    umma::fence_after_sync();
-    const uint32_t tmem = *tslot;
-    if (ok && tid == 0) {
-        umma::mma(tmem, umma::swt(A1, 128), umma::kmaj(S0T, 128), 128, 128, 128, false);
-        umma::mma(tmem + 128, umma::swt(A2, 64), umma::kmaj(DST, 128), 64, 128, 128, false);
-        umma::commit(mbar);
-    }
-    if (tid < 64) {
-        eg[tid] = tid < L ? expf(gam[tid]) : 0.f;
-        fk[tid] = tid < L ? expf(gam[L - 1] - gam[tid]) : 0.f;
-    }
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
-    umma::fence_after_sync();
-    // the products are complete: the Q and K tiles the dgam dot products need
-    // come into the S0 space through the TMA
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(red + 16);   // MMA
+    uint64_t* mS = mbar + 1;             // [dO; dU], U, S0^T
+    uint64_t* mD = mS + 1;               // dS^T
+    uint64_t* mQ = mD + 1;               // Q, K (dgam dot products)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mQ + 1);
+    // the products' operands are consumed after the first wait: Q and K come into
+    // the S0 space; the outputs are staged as swizzled tiles in the consumed
+    // operand space and stored whole: dQ part and dW over [dO; dU], dK part over U
     float* Qr = S0T;                     // [64][128] swizzled
     float* Kr = S0T + 64 * 128;          // [64][128] swizzled
-    if (ok && tid == 0) {
-        umma::mbar_expect_tx(mbl, 2 * 64 * 128 * 4);
-        umma::tma_rows(Qr, 64, &maps.q, kh, ci.start, mbl);
-        umma::tma_rows(Kr, 64, &maps.k, kh, ci.start, mbl);
-    }
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbl, 1));
-    // outputs are staged as swizzled tiles in the consumed operand space and
-    // stored whole: dQ part and dW over [dO; dU], dK part over U
     float* SQ = A1;                      // [64][128] swizzled
     float* SW = A1 + 64 * 128;           // [64][128] swizzled
     float* SK = A2;                      // [64][128] swizzled
-    if (!ok) {
-        if (tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
-    } else {
-        const int half = warp >> 2, win = warp & 3;
-        const int c0 = half * 64;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ntiles = NT * hv;
+    int t = blockIdx.x;
+    if (t >= ntiles) return;
+    ChunkInfo ci = sv.chunks[t % NT];
+    if (ci.len == 0) return;   // the device check of cu_seqlens failed: every chunk is empty
+    auto sbase = [&](int tile) { return ((int64_t)(tile % NT) * hv + tile / NT) * kD * kD; };
+    auto issue_main = [&](const ChunkInfo& c, int tile) {   // one thread
+        const int h = tile / NT;
+        umma::mbar_expect_tx(mS, 3 * 64 * 128 * 4 + 128 * 128 * 4);
+        umma::tma_rows(A1, 128, &maps.dO, h, c.start, mS);
+        umma::tma_rows(A1 + 64 * 32, 128, &maps.dU, h, c.start, mS);
+        umma::tma_rows(A2, 64, &maps.U, h, c.start, mS);
+        umma::bulk_load(S0T, sv.S0b + sbase(tile), 128 * 128 * 4, mS);
+    };
+    auto issue_ds = [&](int tile) {   // one thread
+        umma::mbar_expect_tx(mD, 128 * 128 * 4);
+        umma::bulk_load(DST, w.dS + sbase(tile), 128 * 128 * 4, mD);
+    };
+    auto gam_of = [&](const ChunkInfo& c, int tile) {
+        return tid < 64 ? sv.gam[(int64_t)(tile / NT) * sv.T + c.start + min(tid, c.len - 1)] : 0.f;
+    };
+    if (tid == 0) {
+        for (int k = 0; k < 4; k++) umma::mbar_init(&mbar[k], 1);
+        issue_main(ci, t);
+        issue_ds(t);
+    }
+    float g_cur = gam_of(ci, t);
+    if (warp == 0) umma::tmem_alloc(tslot, 256);
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const int half = warp >> 2, win = warp & 3;
+    const int c0 = half * 64;
+    bool ok = true;
+    for (int it = 0;; it++) {
+        const int h = t / NT, kh = h / (hv / hk), L = ci.len;
+        const int tn = t + (int)gridDim.x;
+        const ChunkInfo cn = tn < ntiles ? sv.chunks[tn % NT] : ci;
+        if (tid < 64) gam[tid] = g_cur;
+        ok = umma::mbar_wait(mS, it & 1);
+        ok = __syncthreads_and(ok && umma::mbar_wait(mD, it & 1));   // gam visible
+        if (!ok) break;
+        if (L < 64) {   // tail rows belong to the next sequence
+            umma::zero_tail_rows(A1, 128, 0, L);
+            umma::zero_tail_rows(A1, 128, 64, L);
+            umma::zero_tail_rows(A2, 64, 0, L);
+        }
+        {   // <dS, S0> over the staged copies (same layout, same index), before rounding
+            float dot = 0.f;
+            for (int i = tid; i < 128 * 128; i += 256) dot += S0T[i] * DST[i];
+            dot = warp_sum(dot);
+            if (lane == 0) red[warp] = dot;
+        }
+        __syncthreads();
+        umma::tf32r_inplace(S0T, 2 * 128 * 128);   // S0^T, dS^T (dO, dU, U arrive rounded)
+        umma::fence_smem_to_async();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {
+            umma::mma(tmem, umma::swt(A1, 128), umma::kmaj(S0T, 128), 128, 128, 128, false);
+            umma::mma(tmem + 128, umma::swt(A2, 64), umma::kmaj(DST, 128), 64, 128, 128, false);
+            umma::commit(mbar);
+        }
+        if (tid < 64) {
+            eg[tid] = tid < L ? expf(gam[tid]) : 0.f;
+            fk[tid] = tid < L ? expf(gam[L - 1] - gam[tid]) : 0.f;
+        }
+        ok = __syncthreads_and(umma::mbar_wait(mbar, it & 1));
+        umma::fence_after_sync();
+        if (!ok) break;
+        const bool next = tn < ntiles && cn.len > 0;
+        if (tid == 0) {
+            umma::mbar_expect_tx(mQ, 2 * 64 * 128 * 4);
+            umma::tma_rows(Qr, 64, &maps.q, kh, ci.start, mQ);
+            umma::tma_rows(Kr, 64, &maps.k, kh, ci.start, mQ);
+            if (next) issue_ds(tn);   // dS^T consumed by the product and the dot product
+        }
+        const float g_next = next ? gam_of(cn, tn) : 0.f;
+        ok = __syncthreads_and(umma::mbar_wait(mQ, it & 1));
+        if (!ok) break;
         // D1: rows 0..127 in lanes 0..127
         {
             const int r = win * 32 + lane;
@@ -550,36 +576,47 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSav
                 rpart[half * 128 + 64 + rh] = rh < L ? fk[rh] * ph : 0.f;
             }
         }
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        if (L == 64) {
+            if (tid == 0) {
+                umma::tma_store_rows(&maps.dQv, h, ci.start, SQ);
+                umma::tma_store_rows(&maps.dW, h, ci.start, SW);
+                umma::tma_store_rows(&maps.dKv, h, ci.start, SK);
+                umma::bulk_commit();
+            }
+        } else {
+            const int64_t off = ((int64_t)ci.start * hv + h) * kD, st = (int64_t)hv * kD;
+            umma::store_rows_sw(w.dQv + off, st, SQ, L);
+            umma::store_rows_sw(w.dW + off, st, SW, L);
+            umma::store_rows_sw(w.dKv + off, st, SK, L);
+        }
+        if (tid < 64 && tid < L) {
+            float g = (rpart[tid] + rpart[128 + tid]) - (rpart[64 + tid] + rpart[192 + tid]);
+            if (tid == L - 1) {
+                float zs = 0.f, dd = 0.f;
+                for (int j = 0; j < L; j++) zs += rpart[64 + j] + rpart[192 + j];
+                for (int i = 0; i < 8; i++) dd += red[i];
+                g += zs + expf(gam[L - 1]) * dd;
+            }
+            w.dgam[(int64_t)(ci.start + tid) * hv + h] = g;
+        }
+        __syncthreads();   // staged tiles, Q / K, sums: read (or handed to the stores)
+        if (!next) break;
+        if (tid == 0) {
+            umma::bulk_wait_read();   // the tile stores have read [dO; dU] and U space
+            issue_main(cn, tn);
+        }
+        g_cur = g_next;
+        ci = cn;
+        t = tn;
     }
-    umma::fence_smem_to_async();
+    if (tid == 0) umma::bulk_wait_read();   // the tile stores have read shared memory
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 256);
-    if (!ok) return;
-    if (L == 64) {
-        if (tid == 0) {
-            umma::tma_store_rows(&maps.dQv, h, ci.start, SQ);
-            umma::tma_store_rows(&maps.dW, h, ci.start, SW);
-            umma::tma_store_rows(&maps.dKv, h, ci.start, SK);
-            umma::bulk_commit();
-        }
-    } else {
-        const int64_t off = ((int64_t)ci.start * hv + h) * kD, st = (int64_t)hv * kD;
-        umma::store_rows_sw(w.dQv + off, st, SQ, L);
-        umma::store_rows_sw(w.dW + off, st, SW, L);
-        umma::store_rows_sw(w.dKv + off, st, SK, L);
-    }
-    if (tid < 64 && tid < L) {
-        float g = (rpart[tid] + rpart[128 + tid]) - (rpart[64 + tid] + rpart[192 + tid]);
-        if (tid == L - 1) {
-            float zs = 0.f, dd = 0.f;
-            for (int j = 0; j < L; j++) zs += rpart[64 + j] + rpart[192 + j];
-            for (int i = 0; i < 8; i++) dd += red[i];
-            g += zs + expf(gam[L - 1]) * dd;
-        }
-        w.dgam[(int64_t)(ci.start + tid) * hv + h] = g;
-    }
-    if (tid == 0) umma::bulk_wait_read();   // the tile stores have read shared memory
+    if (!ok && tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
 }
 
 // ------------------------------------------------------------------ B3b: P / dP terms
@@ -1328,9 +1365,14 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
     lk.unlock();
     if (a.NT > 0) {
         {
+            int dev = 0, nsm = 0;
+            cudaError_t e = cudaGetDevice(&dev);
+            if (e == cudaSuccess)
+                e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return e;
             GDN_PROF("chunk_bwd_sfacing", st);
-            bwd_sfacing_kernel<<<dim3(a.NT, a.hv), 256, kB3aSmem, st>>>(maps, a.hk, a.hv, a.sv,
-                                                                          w);
+            bwd_sfacing_kernel<<<min(a.NT * a.hv, nsm), 256, kB3aSmem, st>>>(maps, a.hk, a.hv,
+                                                                               a.NT, a.sv, w);
         }
         GDN_PROF("chunk_bwd_wy", st);
         bwd_wy_kernel<IO><<<dim3(a.NT, a.hv), 256, kWySmem, st>>>(
