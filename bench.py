@@ -175,19 +175,19 @@ class Step:
 # proportional to the chunks it processes).  Valid for the kernels as captured;
 # a kernel changed since then reports null.
 TRAFFIC_64K = {
-    "conv_fwd": 3617740800,
+    "conv_fwd": 3618197504,
     "gates": 12664832,
-    "chunk_prep": 6524026880,
-    "chunk_state_fwd": 13298647040,
-    "chunk_out_fwd": 8936091648,
-    "chunk_norm_bwd": 5315977216,
-    "chunk_bwd_local": 4016160768,
-    "chunk_bwd_state": 10366060544,
-    "chunk_bwd_dp": 7217473536,
-    "chunk_bwd_sfacing": 17370228736,
-    "chunk_bwd_wy": 10128762880,
-    "gva_sum": 9020360704,
-    "conv_bwd": 5590226944,
+    "chunk_prep": 6525761536,
+    "chunk_state_fwd": 13307377664,
+    "chunk_out_fwd": 8944007168,
+    "chunk_norm_bwd": 5314086912,
+    "chunk_bwd_local": 4016205824,
+    "chunk_bwd_state": 10369161216,
+    "chunk_bwd_dp": 7217242112,
+    "chunk_bwd_sfacing": 17421240320,
+    "chunk_bwd_wy": 10134188032,
+    "gva_sum": 9022685184,
+    "conv_bwd": 5592219648,
 }
 
 

@@ -795,7 +795,9 @@ bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv
 }
 
 // ------------------------------------------------------------------ B3c: WY terms and gates
-// grid (NT, Hv), 256 threads, tcgen05.  With T from bwd_dp_kernel:
+// Persistent: one CTA per SM walks the (chunk, head) tiles t = blockIdx.x,
+// + gridDim.x, ... (chunk = t % NT, head = t / NT).  Per tile, tcgen05, with T
+// saved by the forward:
 //   D_kk = K K^T, D_dt1 = dW K^T, D_dt2 = dU V^T          (64 x 64)
 //   D_tw = T^T [dW | dU]                                  (64 x 256)
 //   dT = D_dt1 diag(beta e^gam) + D_dt2 diag(beta)
@@ -805,6 +807,10 @@ bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv
 //   dbeta_j += sum_m dA (.) GamKK ; dgam_j += beta_j (..) ; dgam_m -= sum_j beta_j (..)
 //   dK += dKK K + dKK^T K
 // then dg = reverse in-chunk cumsum of the total dgam, and the gate gradients.
+// The next tile's operands are requested in three groups as their space frees
+// up: dW, dU (K-major) and T^T once dA is formed, dW, dU (MN-major) and V once
+// the last product is done, K once this tile's dK store has read it; its gate
+// inputs are loaded into registers meanwhile.  Tensor memory allocated once.
 constexpr int kWyFloats = 4 * 64 * 128 + 256 * 64 + 64 * 64;   // stage-1 operands
 constexpr size_t kWySmem = sizeof(float) * (kWyFloats + 10 * 64 + 2 * 64 + 16) + 64 + 1024;
 
@@ -812,7 +818,7 @@ template <class IO>
 __global__ void __launch_bounds__(256, 1)
 bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
               const IO* __restrict__ bv, const float* __restrict__ A_log,
-              const float* __restrict__ dt_bias, int hk, int hv, float* __restrict__ dqkv,
+              const float* __restrict__ dt_bias, int hk, int hv, int NT, float* __restrict__ dqkv,
               IO* __restrict__ da, IO* __restrict__ db, float* __restrict__ gate_part, FwdSaved sv,
               BwdScratch w) {
     extern __shared__ float sm_raw[];
@@ -824,7 +830,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     float* dUs = dWs + 64 * 128;
     float* dWm = dUs + 64 * 128;       // [64 (j)][128 (b)] MN-major dW (arrives rounded)
     float* dUm = dWm + 64 * 128;       // [64 (j)][128 (a)] MN-major dU (arrives rounded)
-    float* TC = dUm + 64 * 128;        // [64 (j)][64 (i)] K-major T^T (kept to the end)
+    float* TC = dUm + 64 * 128;        // [64 (j)][64 (i)] K-major T^T
     // stage 2 overlays dW, dU and [dW^T ; dU^T] once the first products are
     // complete; K and V stay for the epilogue's dot products (R later over V)
     float* GKK = dWs;                  // [64][64] K-major Gam (.) KK (strict lower)
@@ -845,63 +851,67 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     float* rk = sc + 64;
     float* red = rk + 64;              // [64]
     float* rp = red + 64;              // [2][64]
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(rp + 128 + 16);
-    uint64_t* mbl = mbar + 1;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
-    const ChunkInfo ci = sv.chunks[blockIdx.x];
-    if (ci.len == 0) return;
-    const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
-    const int warp = tid >> 5, lane = tid & 31;
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(rp + 128 + 16);   // MMA
+    uint64_t* mW = mbar + 1;           // dW, dU (K-major), T^T
+    uint64_t* mM = mW + 1;             // dW, dU (MN-major), V
+    uint64_t* mK = mM + 1;             // K
+    uint64_t* mT = mK + 1;             // stage 2: T, K (MN-major)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mT + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int C = (2 * hk + hv) * kD;
-    auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
-    auto vrow = [&](int r) { return (row(r) * hv + h) * kD; };
-    const float* Tg = sv.Tm + ((int64_t)blockIdx.x * hv + h) * 2 * 64 * 64;   // T, then T^T
-    if (tid == 0) {   // row tiles through the TMA; T^T, written by the forward, whole
-        umma::mbar_init(mbar, 1);
-        umma::mbar_init(mbl, 1);
-        umma::mbar_expect_tx(mbl, 6 * 64 * 128 * 4 + 64 * 64 * 4);
-        umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
-        umma::tma_rows(Vs, 64, &maps.v, h, ci.start, mbl);
-        umma::tma_rows(dWs, 64, &maps.dW, h, ci.start, mbl);
-        umma::tma_rows(dUs, 64, &maps.dU, h, ci.start, mbl);
-        umma::tma_rows(dWm, 64, &maps.dW_mn, h, ci.start, mbl);
-        umma::tma_rows(dUm, 64, &maps.dU_mn, h, ci.start, mbl);
-        umma::bulk_load(TC, Tg + 64 * 64, 64 * 64 * 4, mbl);
-    }
-    load_gam(gam, sv, ci, h);
-    // the gate inputs and the dgam terms of the other kernels are loaded now and
-    // used at the very end
-    float xa = 0.f, dgam_in = 0.f;
-    if (tid < 64) {
-        bet[tid] = tid < L ? sv.beta[(int64_t)h * sv.T + ci.start + tid] : 0.f;
-        dgs[tid] = 0.f;
-        dbs[tid] = 0.f;
-        if (tid < L) {
-            const int64_t t = ci.start + tid;
-            xa = to_f(av[t * hv + h]) + dt_bias[h];
-            dgam_in = w.dgam[t * hv + h] + w.dgam2[t * hv + h];
+    const int ntiles = NT * hv;
+    int t = blockIdx.x;
+    if (t >= ntiles) return;
+    ChunkInfo ci = sv.chunks[t % NT];
+    if (ci.len == 0) return;   // the device check of cu_seqlens failed: every chunk is empty
+    auto Tg_of = [&](int tile) {   // T, then T^T, written by the forward
+        return sv.Tm + ((int64_t)(tile % NT) * hv + tile / NT) * 2 * 64 * 64;
+    };
+    auto issue_w = [&](const ChunkInfo& c, int tile) {   // one thread
+        const int h = tile / NT;
+        umma::mbar_expect_tx(mW, 2 * 64 * 128 * 4 + 64 * 64 * 4);
+        umma::tma_rows(dWs, 64, &maps.dW, h, c.start, mW);
+        umma::tma_rows(dUs, 64, &maps.dU, h, c.start, mW);
+        umma::bulk_load(TC, Tg_of(tile) + 64 * 64, 64 * 64 * 4, mW);
+    };
+    auto issue_m = [&](const ChunkInfo& c, int tile) {   // one thread
+        const int h = tile / NT;
+        umma::mbar_expect_tx(mM, 3 * 64 * 128 * 4);
+        umma::tma_rows(dWm, 64, &maps.dW_mn, h, c.start, mM);
+        umma::tma_rows(dUm, 64, &maps.dU_mn, h, c.start, mM);
+        umma::tma_rows(Vs, 64, &maps.v, h, c.start, mM);
+    };
+    auto issue_k = [&](const ChunkInfo& c, int tile) {   // one thread
+        const int kh = tile / NT / (hv / hk);
+        umma::mbar_expect_tx(mK, 64 * 128 * 4);
+        umma::tma_rows(Ks, 64, &maps.k, kh, c.start, mK);
+    };
+    // gate inputs of a tile for thread tid < 64: gam, beta, a + dt_bias and the
+    // dgam terms of the other kernels (used at the very end)
+    struct Gates { float g, b, xa, dgin; };
+    auto gates_of = [&](const ChunkInfo& c, int tile) {
+        Gates q{0.f, 0.f, 0.f, 0.f};
+        if (tid < 64) {
+            const int h = tile / NT;
+            q.g = sv.gam[(int64_t)h * sv.T + c.start + min(tid, c.len - 1)];
+            if (tid < c.len) {
+                const int64_t tok = c.start + tid;
+                q.b = sv.beta[(int64_t)h * sv.T + tok];
+                q.xa = to_f(av[tok * hv + h]) + dt_bias[h];
+                q.dgin = w.dgam[tok * hv + h] + w.dgam2[tok * hv + h];
+            }
         }
+        return q;
+    };
+    if (tid == 0) {
+        for (int k = 0; k < 5; k++) umma::mbar_init(&mbar[k], 1);
+        issue_w(ci, t);
+        issue_m(ci, t);
+        issue_k(ci, t);
     }
-    const float Aexp = expf(A_log[h]);
+    Gates gcur = gates_of(ci, t);
     if (warp == 0) umma::tmem_alloc(tslot, 512);
-    __syncthreads();
-    if (tid < 64) {
-        eg[tid] = tid < L ? expf(gam[tid]) : 0.f;
-        be[tid] = bet[tid] * eg[tid];
-    }
-    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
-    if (L < 64) {   // tail rows belong to the next sequence
-        umma::zero_tail_rows(Ks, 64, 0, L);
-        umma::zero_tail_rows(Vs, 64, 0, L);
-        umma::zero_tail_rows(dWs, 64, 0, L);
-        umma::zero_tail_rows(dUs, 64, 0, L);
-        umma::zero_tail_rows(dWm, 64, 0, L);
-        umma::zero_tail_rows(dUm, 64, 0, L);
-        __syncthreads();
-    }
-    if (!sv.qkv_tf32) umma::tf32r_inplace(Ks, 2 * 64 * 128);   // K, V (dW, dU and T^T arrive rounded)
-    __syncthreads();
-    umma::fence_smem_to_async();
+    umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
@@ -909,250 +919,301 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     // 128-column dKK product), T^T [dW | dU] 256-511 (read again at the very end)
     const uint32_t tKK = tmem, tDT1 = tmem + 64, tDT2 = tmem + 128, tX = tmem + 64,
                    tTW = tmem + 256;
-    if (ok && tid == 0) {
-        umma::mma(tKK, umma::swt(Ks, 64), umma::swt(Ks, 64), 64, 64, 128, false);
-        umma::mma(tDT1, umma::swt(dWs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
-        umma::mma(tDT2, umma::swt(dUs, 64), umma::swt(Vs, 64), 64, 64, 128, false);
-        umma::mma(tTW, umma::kmaj(TC, 64), umma::mnt(dWm), 64, 128, 64, false);
-        umma::mma(tTW + 128, umma::kmaj(TC, 64), umma::mnt(dUm), 64, 128, 64, false);
-        umma::commit(mbar);
-    }
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
-    umma::fence_after_sync();
-    // dW, dU (both layouts) are consumed: fetch T and K as an MN-major tile for stage 2
-    if (ok && tid == 0) {
-        umma::mbar_expect_tx(mbl, 64 * 64 * 4 + 64 * 128 * 4);
-        umma::bulk_load(TR, Tg, 64 * 64 * 4, mbl);
-        umma::tma_rows(Km, 64, &maps.k_mn, kh, ci.start, mbl);
-    }
     const int win = warp & 3, half = warp >> 2;
     const int rl = umma::frag_row_lo(), cf = umma::frag_col();   // fragment rows rl, rl + 8
-    if (ok) {
-        {   // Gam (.) KK and dT from the 64-column products, 32 columns per warp
-            float kk[16], t1[16], t2[16];
-            umma::tmem_ld_m64<4>(umma::tmem_at(tKK, half * 32), kk);
-            umma::tmem_ld_m64<4>(umma::tmem_at(tDT1, half * 32), t1);
-            umma::tmem_ld_m64<4>(umma::tmem_at(tDT2, half * 32), t2);
-#pragma unroll
-            for (int hr = 0; hr < 2; hr++) {
-                const int r = rl + 8 * hr;
-                const float gr = gam[r];
-#pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    const int j = half * 32 + 8 * k + cf, q = 4 * k + 2 * hr;
-                    const float g0 = j < r ? expf(gr - gam[j]) * kk[q] : 0.f;
-                    const float g1 = j + 1 < r ? expf(gr - gam[j + 1]) * kk[q + 1] : 0.f;
-                    const float d0 = t1[q] * be[j] + t2[q] * bet[j];
-                    const float d1 = t1[q + 1] * be[j + 1] + t2[q + 1] * bet[j + 1];
-                    *reinterpret_cast<float2*>(GKK + umma::kidx(r, j, 64)) = make_float2(g0, g1);
-                    *reinterpret_cast<float2*>(DTR + umma::kidx(r, j, 64)) =
-                        make_float2(umma::tf32r(d0), umma::tf32r(d1));
-                }
-            }
+    bool ok = true;
+    for (int it = 0;; it++) {
+        const int h = t / NT, kh = h / (hv / hk), L = ci.len, chunk = t % NT;
+        const int tn = t + (int)gridDim.x;
+        const ChunkInfo cn = tn < ntiles ? sv.chunks[tn % NT] : ci;
+        auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
+        const float Aexp = expf(A_log[h]);
+        if (tid < 64) {
+            gam[tid] = gcur.g;
+            bet[tid] = gcur.b;
+            dgs[tid] = 0.f;
+            dbs[tid] = 0.f;
+            eg[tid] = tid < L ? expf(gcur.g) : 0.f;
+            be[tid] = gcur.b * (tid < L ? expf(gcur.g) : 0.f);
         }
-        {   // T^T dW (half 0) and T^T dU (half 1): dV, dbeta / dgam dot products
-            float rs[2] = {0.f, 0.f};
-            float* dvb = dqkv + (int64_t)2 * hk * kD + h * kD;
-#pragma unroll
-            for (int c0 = 0; c0 < 128; c0 += 64) {
-                float v[32];
-                umma::tmem_ld64_m64(umma::tmem_at(tTW, half * 128 + c0), v);
-                const float* X = half == 0 ? Ks : Vs;
+        ok = umma::mbar_wait(mW, it & 1) && umma::mbar_wait(mM, it & 1);
+        ok = __syncthreads_and(ok && umma::mbar_wait(mK, it & 1));   // gates visible
+        if (!ok) break;
+        if (L < 64) {   // tail rows belong to the next sequence
+            umma::zero_tail_rows(Ks, 64, 0, L);
+            umma::zero_tail_rows(Vs, 64, 0, L);
+            umma::zero_tail_rows(dWs, 64, 0, L);
+            umma::zero_tail_rows(dUs, 64, 0, L);
+            umma::zero_tail_rows(dWm, 64, 0, L);
+            umma::zero_tail_rows(dUm, 64, 0, L);
+            __syncthreads();
+        }
+        if (!sv.qkv_tf32) umma::tf32r_inplace(Ks, 2 * 64 * 128);   // K, V (dW, dU and T^T arrive rounded)
+        __syncthreads();
+        umma::fence_smem_to_async();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {
+            umma::mma(tKK, umma::swt(Ks, 64), umma::swt(Ks, 64), 64, 64, 128, false);
+            umma::mma(tDT1, umma::swt(dWs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
+            umma::mma(tDT2, umma::swt(dUs, 64), umma::swt(Vs, 64), 64, 64, 128, false);
+            umma::mma(tTW, umma::kmaj(TC, 64), umma::mnt(dWm), 64, 128, 64, false);
+            umma::mma(tTW + 128, umma::kmaj(TC, 64), umma::mnt(dUm), 64, 128, 64, false);
+            umma::commit(mbar);
+        }
+        ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+        umma::fence_after_sync();
+        if (!ok) break;
+        // dW, dU (both layouts) are consumed: fetch T and K as an MN-major tile for stage 2
+        if (tid == 0) {
+            umma::mbar_expect_tx(mT, 64 * 64 * 4 + 64 * 128 * 4);
+            umma::bulk_load(TR, Tg_of(t), 64 * 64 * 4, mT);
+            umma::tma_rows(Km, 64, &maps.k_mn, kh, ci.start, mT);
+        }
+        {
+            {   // Gam (.) KK and dT from the 64-column products, 32 columns per warp
+                float kk[16], t1[16], t2[16];
+                umma::tmem_ld_m64<4>(umma::tmem_at(tKK, half * 32), kk);
+                umma::tmem_ld_m64<4>(umma::tmem_at(tDT1, half * 32), t1);
+                umma::tmem_ld_m64<4>(umma::tmem_at(tDT2, half * 32), t2);
 #pragma unroll
                 for (int hr = 0; hr < 2; hr++) {
                     const int r = rl + 8 * hr;
+                    const float gr = gam[r];
 #pragma unroll
-                    for (int k = 0; k < 8; k++) {
-                        const int c = c0 + 8 * k + cf, q = 4 * k + 2 * hr;
-                        const float2 x2 = *reinterpret_cast<const float2*>(X + umma::swz(r, c, 64));
-                        rs[hr] += v[q] * x2.x + v[q + 1] * x2.y;
-                        if (half == 1 && r < L)
-                            *reinterpret_cast<float2*>(dvb + row(r) * C + c) =
-                                make_float2(bet[r] * v[q], bet[r] * v[q + 1]);
+                    for (int k = 0; k < 4; k++) {
+                        const int j = half * 32 + 8 * k + cf, q = 4 * k + 2 * hr;
+                        const float g0 = j < r ? expf(gr - gam[j]) * kk[q] : 0.f;
+                        const float g1 = j + 1 < r ? expf(gr - gam[j + 1]) * kk[q + 1] : 0.f;
+                        const float d0 = t1[q] * be[j] + t2[q] * bet[j];
+                        const float d1 = t1[q + 1] * be[j + 1] + t2[q + 1] * bet[j + 1];
+                        *reinterpret_cast<float2*>(GKK + umma::kidx(r, j, 64)) = make_float2(g0, g1);
+                        *reinterpret_cast<float2*>(DTR + umma::kidx(r, j, 64)) =
+                            make_float2(umma::tf32r(d0), umma::tf32r(d1));
                     }
+                }
+            }
+            {   // T^T dW (half 0) and T^T dU (half 1): dV, dbeta / dgam dot products
+                float rs[2] = {0.f, 0.f};
+                float* dvb = dqkv + (int64_t)2 * hk * kD + h * kD;
+#pragma unroll
+                for (int c0 = 0; c0 < 128; c0 += 64) {
+                    float v[32];
+                    umma::tmem_ld64_m64(umma::tmem_at(tTW, half * 128 + c0), v);
+                    const float* X = half == 0 ? Ks : Vs;
+#pragma unroll
+                    for (int hr = 0; hr < 2; hr++) {
+                        const int r = rl + 8 * hr;
+#pragma unroll
+                        for (int k = 0; k < 8; k++) {
+                            const int c = c0 + 8 * k + cf, q = 4 * k + 2 * hr;
+                            const float2 x2 = *reinterpret_cast<const float2*>(X + umma::swz(r, c, 64));
+                            rs[hr] += v[q] * x2.x + v[q + 1] * x2.y;
+                            if (half == 1 && r < L)
+                                *reinterpret_cast<float2*>(dvb + row(r) * C + c) =
+                                    make_float2(bet[r] * v[q], bet[r] * v[q + 1]);
+                        }
+                    }
+                }
+                rs[0] = umma::row_quad_sum(rs[0]);
+                rs[1] = umma::row_quad_sum(rs[1]);
+                if ((lane & 3) == 0) {
+                    rp[half * 64 + rl] = rl < L ? rs[0] : 0.f;
+                    rp[half * 64 + rl + 8] = rl + 8 < L ? rs[1] : 0.f;
+                }
+            }
+        }
+        __syncthreads();
+        if (tid < 64) {
+            dbs[tid] += eg[tid] * rp[tid] + rp[64 + tid];
+            dgs[tid] += be[tid] * rp[tid];
+        }
+        const bool next = tn < ntiles && cn.len > 0;   // the entry has arrived by now
+        const Gates gnext = next ? gates_of(cn, tn) : Gates{0.f, 0.f, 0.f, 0.f};
+        // stage 2 operands: T arrived as a K-major tile, K as an MN-major tile
+        ok = __syncthreads_and(umma::mbar_wait(mT, it & 1));
+        if (!ok) break;
+        if (L < 64) {
+            umma::zero_tail_rows(Km, 64, 0, L);
+            __syncthreads();
+        }
+        if (!sv.qkv_tf32) umma::tf32r_inplace(Km, 64 * 128);
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {
+            umma::mma_tf32(tX, TR, 64, DTR, 64, 64, 64, 64, false);     // Y^T = T dT^T
+            umma::commit(mbar);
+        }
+        ok = __syncthreads_and(umma::mbar_wait(mbar, 1));
+        umma::fence_after_sync();
+        if (!ok) break;
+        {   // Y^T, 32 columns per warp, all lanes
+            float v[16];
+            umma::tmem_ld_m64<4>(umma::tmem_at(tX, half * 32), v);
+#pragma unroll
+            for (int hr = 0; hr < 2; hr++)
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const int c = half * 32 + 8 * k + cf, q = 4 * k + 2 * hr;
+                    *reinterpret_cast<float2*>(YT + umma::kidx(rl + 8 * hr, c, 64)) =
+                        make_float2(umma::tf32r(v[q]), umma::tf32r(v[q + 1]));
+                }
+        }
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {
+            umma::mma_tf32(tKK, TC, 64, YT, 64, 64, 64, 64, false);     // T^T Y  (= -dA)
+            umma::commit(mbar);
+        }
+        ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
+        umma::fence_after_sync();
+        if (!ok) break;
+        float* colp = Rm;                  // [4 row windows][64] column sums of beta_r x
+        {   // dA = -(T^T Y) strictly lower; 32 columns per warp, all lanes
+            float v[16];
+            umma::tmem_ld_m64<4>(umma::tmem_at(tKK, half * 32), v);
+            float rs[2] = {0.f, 0.f}, cs[4][2];
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const int m = half * 32 + 8 * k + cf;
+                cs[k][0] = cs[k][1] = 0.f;
+#pragma unroll
+                for (int hr = 0; hr < 2; hr++) {
+                    const int r = rl + 8 * hr;
+                    const float br = bet[r], gr = gam[r];
+                    const float2 gk = *reinterpret_cast<const float2*>(GKK + umma::kidx(r, m, 64));
+                    float dk[2];
+#pragma unroll
+                    for (int e = 0; e < 2; e++) {
+                        const float dA = m + e < r ? -v[4 * k + 2 * hr + e] : 0.f;
+                        const float x = dA * (e == 0 ? gk.x : gk.y);
+                        rs[hr] += x;
+                        cs[k][e] += br * x;
+                        dk[e] = umma::tf32r(m + e < r ? dA * br * expf(gr - gam[m + e]) : 0.f);
+                        dKC[umma::kidx(m + e, r, 64)] = dk[e];
+                    }
+                    *reinterpret_cast<float2*>(dKR + umma::kidx(r, m, 64)) = make_float2(dk[0], dk[1]);
                 }
             }
             rs[0] = umma::row_quad_sum(rs[0]);
             rs[1] = umma::row_quad_sum(rs[1]);
             if ((lane & 3) == 0) {
-                rp[half * 64 + rl] = rl < L ? rs[0] : 0.f;
-                rp[half * 64 + rl + 8] = rl + 8 < L ? rs[1] : 0.f;
+                rp[half * 64 + rl] = rs[0];
+                rp[half * 64 + rl + 8] = rs[1];
             }
-        }
-    }
-    __syncthreads();
-    if (tid < 64) {
-        dbs[tid] += eg[tid] * rp[tid] + rp[64 + tid];
-        dgs[tid] += be[tid] * rp[tid];
-    }
-    // stage 2 operands: T arrived as a K-major tile, K as an MN-major tile
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbl, 1));
-    if (L < 64) {
-        umma::zero_tail_rows(Km, 64, 0, L);
-        __syncthreads();
-    }
-    if (!sv.qkv_tf32) umma::tf32r_inplace(Km, 64 * 128);
-    umma::fence_smem_to_async();
-    umma::fence_before_sync();
-    __syncthreads();
-    umma::fence_after_sync();
-    if (ok && tid == 0) {
-        umma::mma_tf32(tX, TR, 64, DTR, 64, 64, 64, 64, false);     // Y^T = T dT^T
-        umma::commit(mbar);
-    }
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
-    umma::fence_after_sync();
-    if (ok) {   // Y^T, 32 columns per warp, all lanes
-        float v[16];
-        umma::tmem_ld_m64<4>(umma::tmem_at(tX, half * 32), v);
 #pragma unroll
-        for (int hr = 0; hr < 2; hr++)
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                const int c = half * 32 + 8 * k + cf, q = 4 * k + 2 * hr;
-                *reinterpret_cast<float2*>(YT + umma::kidx(rl + 8 * hr, c, 64)) =
-                    make_float2(umma::tf32r(v[q]), umma::tf32r(v[q + 1]));
-            }
-    }
-    umma::fence_smem_to_async();
-    umma::fence_before_sync();
-    __syncthreads();
-    umma::fence_after_sync();
-    if (ok && tid == 0) {
-        umma::mma_tf32(tKK, TC, 64, YT, 64, 64, 64, 64, false);     // T^T Y  (= -dA)
-        umma::commit(mbar);
-    }
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
-    umma::fence_after_sync();
-    float* colp = Rm;                  // [4 row windows][64] column sums of beta_r x
-    if (ok) {   // dA = -(T^T Y) strictly lower; 32 columns per warp, all lanes
-        float v[16];
-        umma::tmem_ld_m64<4>(umma::tmem_at(tKK, half * 32), v);
-        float rs[2] = {0.f, 0.f}, cs[4][2];
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const int m = half * 32 + 8 * k + cf;
-            cs[k][0] = cs[k][1] = 0.f;
-#pragma unroll
-            for (int hr = 0; hr < 2; hr++) {
-                const int r = rl + 8 * hr;
-                const float br = bet[r], gr = gam[r];
-                const float2 gk = *reinterpret_cast<const float2*>(GKK + umma::kidx(r, m, 64));
-                float dk[2];
+            for (int k = 0; k < 4; k++)
 #pragma unroll
                 for (int e = 0; e < 2; e++) {
-                    const float dA = m + e < r ? -v[4 * k + 2 * hr + e] : 0.f;
-                    const float x = dA * (e == 0 ? gk.x : gk.y);
-                    rs[hr] += x;
-                    cs[k][e] += br * x;
-                    dk[e] = umma::tf32r(m + e < r ? dA * br * expf(gr - gam[m + e]) : 0.f);
-                    dKC[umma::kidx(m + e, r, 64)] = dk[e];
+                    const float c = umma::col_oct_sum(cs[k][e]);
+                    if (lane < 4) colp[win * 64 + half * 32 + 8 * k + 2 * lane + e] = c;
                 }
-                *reinterpret_cast<float2*>(dKR + umma::kidx(r, m, 64)) = make_float2(dk[0], dk[1]);
+        }
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {
+            umma::mma(tX, umma::kmaj(dKR, 64), umma::mnt(Km), 64, 128, 64, false);   // dKK K
+            umma::mma(tX, umma::kmaj(dKC, 64), umma::mnt(Km), 64, 128, 64, true);    // + dKK^T K
+            umma::commit(mbar);
+            // Gam (.) KK, dT, T, Y^T and T^T are consumed: the next tile's dW, dU, T^T
+            if (next) issue_w(cn, tn);
+        }
+        if (tid < 64) {
+            const float cs = (colp[tid] + colp[64 + tid]) + (colp[128 + tid] + colp[192 + tid]);
+            const float rsA = rp[tid] + rp[64 + tid];
+            dbs[tid] += rsA;
+            dgs[tid] += bet[tid] * rsA - cs;
+        }
+        ok = __syncthreads_and(umma::mbar_wait(mbar, 1));
+        umma::fence_after_sync();
+        if (!ok) break;
+        // dKK, K (MN-major) and V (with the column sums over it) are consumed: the
+        // next tile's dW, dU (MN-major) and V
+        if (next && tid == 0) issue_m(cn, tn);
+        // dK part = dKK product + diag(beta e^gam) T^T dW, staged as a swizzled
+        // tile in the K space (consumed) and stored whole
+        {
+            float vk[32], vw[32];
+            umma::tmem_ld64_m64(umma::tmem_at(tX, half * 64), vk);
+            umma::tmem_ld64_m64(umma::tmem_at(tTW, half * 64), vw);
+            const float bl = be[rl], bh = be[rl + 8];
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                vk[4 * k] += bl * vw[4 * k];
+                vk[4 * k + 1] += bl * vw[4 * k + 1];
+                vk[4 * k + 2] += bh * vw[4 * k + 2];
+                vk[4 * k + 3] += bh * vw[4 * k + 3];
             }
+            umma::frag_to_sw(Ks, vk, half * 64, 1.f, 1.f);
         }
-        rs[0] = umma::row_quad_sum(rs[0]);
-        rs[1] = umma::row_quad_sum(rs[1]);
-        if ((lane & 3) == 0) {
-            rp[half * 64 + rl] = rs[0];
-            rp[half * 64 + rl + 8] = rs[1];
-        }
-#pragma unroll
-        for (int k = 0; k < 4; k++)
-#pragma unroll
-            for (int e = 0; e < 2; e++) {
-                const float c = umma::col_oct_sum(cs[k][e]);
-                if (lane < 4) colp[win * 64 + half * 32 + 8 * k + 2 * lane + e] = c;
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        if (L == 64) {
+            if (tid == 0) {
+                umma::tma_store_rows(&maps.dKv3, h, ci.start, Ks);
+                umma::bulk_commit();
             }
-    }
-    umma::fence_smem_to_async();
-    umma::fence_before_sync();
-    __syncthreads();
-    umma::fence_after_sync();
-    if (ok && tid == 0) {
-        umma::mma(tX, umma::kmaj(dKR, 64), umma::mnt(Km), 64, 128, 64, false);   // dKK K
-        umma::mma(tX, umma::kmaj(dKC, 64), umma::mnt(Km), 64, 128, 64, true);    // + dKK^T K
-        umma::commit(mbar);
-    }
-    if (tid < 64) {
-        const float cs = (colp[tid] + colp[64 + tid]) + (colp[128 + tid] + colp[192 + tid]);
-        const float rsA = rp[tid] + rp[64 + tid];
-        dbs[tid] += rsA;
-        dgs[tid] += bet[tid] * rsA - cs;
-    }
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
-    umma::fence_after_sync();
-    // dK part = dKK product + diag(beta e^gam) T^T dW, staged as a swizzled
-    // tile in the K space (consumed) and stored whole
-    if (ok) {
-        float vk[32], vw[32];
-        umma::tmem_ld64_m64(umma::tmem_at(tX, half * 64), vk);
-        umma::tmem_ld64_m64(umma::tmem_at(tTW, half * 64), vw);
-        const int rl = umma::frag_row_lo();
-        const float bl = be[rl], bh = be[rl + 8];
-#pragma unroll
-        for (int k = 0; k < 8; k++) {
-            vk[4 * k] += bl * vw[4 * k];
-            vk[4 * k + 1] += bl * vw[4 * k + 1];
-            vk[4 * k + 2] += bh * vw[4 * k + 2];
-            vk[4 * k + 3] += bh * vw[4 * k + 3];
+        } else {
+            umma::store_rows_sw(w.dKv3 + ((int64_t)ci.start * hv + h) * kD, (int64_t)hv * kD, Ks, L);
         }
-        umma::frag_to_sw(Ks, vk, half * 64, 1.f, 1.f);
-    } else if (tid == 0) {
-        atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
+        // ---- dg = reverse cumsum of dgam; gates
+        if (tid < 64) sc[tid] = tid < L ? dgs[tid] + gcur.dgin : 0.f;
+        __syncthreads();
+        if (tid < 32) {
+            float a = sc[63 - 2 * lane], b = sc[62 - 2 * lane], s = a + b;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                float u = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += u;
+            }
+            float ex = s - (a + b);
+            rk[63 - 2 * lane] = ex + a;
+            rk[62 - 2 * lane] = ex + a + b;
+        }
+        __syncthreads();
+        float gterm = 0.f, dterm = 0.f;
+        if (tid < L) {
+            const int64_t tok = ci.start + tid;
+            const float dg = rk[tid];
+            const float gval = -Aexp * softplusf_(gcur.xa);
+            const float dav = dg * (-Aexp) * sigmoidf_(gcur.xa);
+            const float bb = bet[tid];
+            da[tok * hv + h] = from_f<IO>(dav);
+            db[tok * hv + h] = from_f<IO>(dbs[tid] * bb * (1.f - bb));
+            w.dgs[tok * hv + h] = dg;
+            gterm = dg * gval;
+            dterm = dav;
+        }
+        if (tid < 64) {
+            gterm = warp_sum(gterm);
+            dterm = warp_sum(dterm);
+            if (lane == 0) { red[warp] = gterm; red[2 + warp] = dterm; }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            gate_part[((int64_t)chunk * hv + h) * 2 + 0] = red[0] + red[1];
+            gate_part[((int64_t)chunk * hv + h) * 2 + 1] = red[2] + red[3];
+            umma::bulk_wait_read();   // the dK tile store has read its shared memory
+            if (next) issue_k(cn, tn);
+        }
+        __syncthreads();   // gate sums and the tile's scalars are read
+        if (!next) break;
+        gcur = gnext;
+        ci = cn;
+        t = tn;
     }
-    umma::fence_smem_to_async();
+    if (tid == 0) umma::bulk_wait_read();
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 512);
-    if (!ok) return;
-    if (L == 64) {
-        if (tid == 0) {
-            umma::tma_store_rows(&maps.dKv3, h, ci.start, Ks);
-            umma::bulk_commit();
-        }
-    } else {
-        umma::store_rows_sw(w.dKv3 + ((int64_t)ci.start * hv + h) * kD, (int64_t)hv * kD, Ks, L);
-    }
-    // ---- dg = reverse cumsum of dgam; gates
-    if (tid < 64) sc[tid] = tid < L ? dgs[tid] + dgam_in : 0.f;
-    __syncthreads();
-    if (tid < 32) {
-        float a = sc[63 - 2 * lane], b = sc[62 - 2 * lane], s = a + b;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            float u = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += u;
-        }
-        float ex = s - (a + b);
-        rk[63 - 2 * lane] = ex + a;
-        rk[62 - 2 * lane] = ex + a + b;
-    }
-    __syncthreads();
-    float gterm = 0.f, dterm = 0.f;
-    if (tid < L) {
-        const int64_t t = ci.start + tid;
-        const float dg = rk[tid];
-        const float gval = -Aexp * softplusf_(xa);
-        const float dav = dg * (-Aexp) * sigmoidf_(xa);
-        const float bb = bet[tid];
-        da[t * hv + h] = from_f<IO>(dav);
-        db[t * hv + h] = from_f<IO>(dbs[tid] * bb * (1.f - bb));
-        w.dgs[t * hv + h] = dg;
-        gterm = dg * gval;
-        dterm = dav;
-    }
-    if (tid < 64) {
-        gterm = warp_sum(gterm);
-        dterm = warp_sum(dterm);
-        if (lane == 0) { red[warp] = gterm; red[2 + warp] = dterm; }
-    }
-    __syncthreads();
-    if (tid == 0) {
-        gate_part[((int64_t)blockIdx.x * hv + h) * 2 + 0] = red[0] + red[1];
-        gate_part[((int64_t)blockIdx.x * hv + h) * 2 + 1] = red[2] + red[3];
-        umma::bulk_wait_read();   // the dK tile store has read its shared memory
-    }
+    if (!ok && tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
 }
 
 // ------------------------------------------------------------------ B4: GVA sum
@@ -1374,9 +1435,13 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
             bwd_sfacing_kernel<<<min(a.NT * a.hv, nsm), 256, kB3aSmem, st>>>(maps, a.hk, a.hv,
                                                                                a.NT, a.sv, w);
         }
+        int dev = 0, nsm = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
         GDN_PROF("chunk_bwd_wy", st);
-        bwd_wy_kernel<IO><<<dim3(a.NT, a.hv), 256, kWySmem, st>>>(
-            maps, (const IO*)a.a, (const IO*)a.b, a.A_log, a.dt_bias, a.hk, a.hv, a.dqkv,
+        bwd_wy_kernel<IO><<<min(a.NT * a.hv, nsm), 256, kWySmem, st>>>(
+            maps, (const IO*)a.a, (const IO*)a.b, a.A_log, a.dt_bias, a.hk, a.hv, a.NT, a.dqkv,
             (IO*)a.da, (IO*)a.db, gate_part, a.sv, w);
     }
     if (a.T > 0) {

@@ -134,62 +134,6 @@ __device__ __forceinline__ void tile_zero(typename Tile<M, N, NW>::Acc& acc) {
             for (int e = 0; e < 4; e++) acc[i][j][e] = 0.f;
 }
 
-// acc += A * B with A(r, k) = a(r, k), B(k, c) = b(k, c), k in [0, K).
-// a and b read shared memory (or registers); tf32 operands, fp32 accumulate.
-template <int M, int N, int K, int NW, class FA, class FB>
-__device__ __forceinline__ void tile_mma(typename Tile<M, N, NW>::Acc& acc, FA a, FB b) {
-    using C = Tile<M, N, NW>;
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int m0 = C::m0(), n0 = C::n0();
-#pragma unroll 2
-    for (int k0 = 0; k0 < K; k0 += 8) {
-        uint32_t af[C::MPW][4];
-#pragma unroll
-        for (int i = 0; i < C::MPW; i++) {
-            const int r = m0 + i * 16 + g;
-            af[i][0] = f2tf32(a(r, k0 + t));
-            af[i][1] = f2tf32(a(r + 8, k0 + t));
-            af[i][2] = f2tf32(a(r, k0 + t + 4));
-            af[i][3] = f2tf32(a(r + 8, k0 + t + 4));
-        }
-#pragma unroll
-        for (int j = 0; j < C::NPW; j++) {
-            const int c = n0 + j * 8 + g;
-            uint32_t bf[2] = {f2tf32(b(k0 + t, c)), f2tf32(b(k0 + t + 4, c))};
-#pragma unroll
-            for (int i = 0; i < C::MPW; i++) mma_tf32(acc[i][j], af[i], bf);
-        }
-    }
-}
-
-// The same with operands given as tf32 bit patterns (already rounded, or
-// converted by the caller), so pre-rounded tiles skip the conversion.
-template <int M, int N, int K, int NW, class FA, class FB>
-__device__ __forceinline__ void tile_mma_bits(typename Tile<M, N, NW>::Acc& acc, FA a, FB b) {
-    using C = Tile<M, N, NW>;
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int m0 = C::m0(), n0 = C::n0();
-#pragma unroll 2
-    for (int k0 = 0; k0 < K; k0 += 8) {
-        uint32_t af[C::MPW][4];
-#pragma unroll
-        for (int i = 0; i < C::MPW; i++) {
-            const int r = m0 + i * 16 + g;
-            af[i][0] = a(r, k0 + t);
-            af[i][1] = a(r + 8, k0 + t);
-            af[i][2] = a(r, k0 + t + 4);
-            af[i][3] = a(r + 8, k0 + t + 4);
-        }
-#pragma unroll
-        for (int j = 0; j < C::NPW; j++) {
-            const int c = n0 + j * 8 + g;
-            uint32_t bf[2] = {b(k0 + t, c), b(k0 + t + 4, c)};
-#pragma unroll
-            for (int i = 0; i < C::MPW; i++) mma_tf32(acc[i][j], af[i], bf);
-        }
-    }
-}
-
 // Four 8 x 8 matrices of 16-bit elements (8 rows of 16 bytes each; lane l
 // gives the address of row l % 8 of matrix l / 8).  For 32-bit (tf32) data a
 // matrix is 8 rows x 4 values, and thread t receives (row t / 4, value t % 4):
@@ -275,53 +219,6 @@ __device__ __forceinline__ void tile_each2(typename Tile<M, N, NW>::Acc& acc, F 
                   acc[i][j][2 * h + 1]);
 }
 
-// Row sums of f(row, col, v) over the columns one warp holds: part[wn * M + row]
-// (wn = the warp's position along N).  Summing part over wn in order after a
-// barrier gives a deterministic row reduction.
-template <int M, int N, int NW, class F>
-__device__ __forceinline__ void tile_rowpart(typename Tile<M, N, NW>::Acc& acc, F f, float* part) {
-    using C = Tile<M, N, NW>;
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int m0 = C::m0(), n0 = C::n0(), wn = (int)(threadIdx.x / 32 / C::WM);
-#pragma unroll
-    for (int i = 0; i < C::MPW; i++)
-#pragma unroll
-        for (int h = 0; h < 2; h++) {
-            const int r = m0 + i * 16 + g + h * 8;
-            float s = 0.f;
-#pragma unroll
-            for (int j = 0; j < C::NPW; j++)
-#pragma unroll
-                for (int e = 0; e < 2; e++) s += f(r, n0 + j * 8 + 2 * t + e, acc[i][j][2 * h + e]);
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (t == 0) part[wn * M + r] = s;
-        }
-}
-
-// Column sums of f(row, col, v) over the rows one warp holds: part[wm * N + col].
-template <int M, int N, int NW, class F>
-__device__ __forceinline__ void tile_colpart(typename Tile<M, N, NW>::Acc& acc, F f, float* part) {
-    using C = Tile<M, N, NW>;
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int m0 = C::m0(), n0 = C::n0(), wm = (int)(threadIdx.x / 32 % C::WM);
-#pragma unroll
-    for (int j = 0; j < C::NPW; j++)
-#pragma unroll
-        for (int e = 0; e < 2; e++) {
-            const int c = n0 + j * 8 + 2 * t + e;
-            float s = 0.f;
-#pragma unroll
-            for (int i = 0; i < C::MPW; i++)
-#pragma unroll
-                for (int h = 0; h < 2; h++) s += f(m0 + i * 16 + g + h * 8, c, acc[i][j][2 * h + e]);
-            s += __shfl_xor_sync(0xffffffffu, s, 4);
-            s += __shfl_xor_sync(0xffffffffu, s, 8);
-            s += __shfl_xor_sync(0xffffffffu, s, 16);
-            if (g == 0) part[wm * N + c] = s;
-        }
-}
-
 // Backward of one gated-RMSNorm row held by a warp (4 columns per lane):
 //   n = o rs, dn = dy (1+w) silu(z): do = rs (dn - n mean(dn n)),
 //   dz = dy n (1+w) silu'(z), dw += dy n silu(z).
@@ -356,20 +253,6 @@ __device__ __forceinline__ NormRowGrad norm_row_bwd(float4 o4, float4 z4, float4
     dw_acc.z += dy[2] * nn[2] * sz[2];
     dw_acc.w += dy[3] * nn[3] * sz[3];
     return {make_float4(od[0], od[1], od[2], od[3]), make_float4(zd[0], zd[1], zd[2], zd[3])};
-}
-
-// Inclusive prefix sum of 64 values held two per lane by one warp (in place).
-__device__ __forceinline__ void warp_cumsum64(float* v) {
-    const int lane = threadIdx.x & 31;
-    float a = v[2 * lane], b = v[2 * lane + 1], s = a + b;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        float u = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += u;
-    }
-    float ex = s - (a + b);
-    v[2 * lane] = ex + a;
-    v[2 * lane + 1] = ex + a + b;
 }
 
 // T = (I + A)^-1 for strictly lower A [64][lda] (unit lower-triangular

@@ -285,41 +285,6 @@ __device__ __forceinline__ void tf32r_inplace(float* p, int n) {
     }
 }
 
-// Row-major smem tile R [64 tokens][ldr] (128 columns) -> K-major tile
-// [128 (column)][64 (token)], rows optionally scaled per token, tf32-rounded.
-// Reads: lanes take consecutive columns of one row; writes: 8 consecutive
-// columns fill 8 distinct 16-byte bank groups -- no bank conflicts.
-__device__ __forceinline__ void transpose_rows_to_kmajor(float* dst, const float* R, int ldr,
-                                                         const float* scale) {
-    for (int idx = threadIdx.x; idx < 128 * 16; idx += blockDim.x) {
-        const int c = idx & 127, j4 = idx >> 7;
-        float4 v = make_float4(R[(4 * j4 + 0) * ldr + c], R[(4 * j4 + 1) * ldr + c],
-                               R[(4 * j4 + 2) * ldr + c], R[(4 * j4 + 3) * ldr + c]);
-        if (scale) {
-            v.x *= scale[4 * j4 + 0]; v.y *= scale[4 * j4 + 1];
-            v.z *= scale[4 * j4 + 2]; v.w *= scale[4 * j4 + 3];
-        }
-        *reinterpret_cast<float4*>(dst + kidx(c, 4 * j4, 64)) = tf32r(v);
-    }
-}
-
-// Swizzled tile [64 tokens][128] -> K-major tile [128 (column)][64 (token)],
-// rows optionally scaled per token, tf32-rounded.  Lanes take 32 columns of one
-// token row (a permutation of one 128-byte box row: no bank conflicts).
-__device__ __forceinline__ void transpose_sw_to_kmajor(float* dst, const float* src,
-                                                       const float* scale) {
-    for (int idx = threadIdx.x; idx < 128 * 16; idx += blockDim.x) {
-        const int c = idx & 127, j4 = idx >> 7;
-        float4 v = make_float4(src[swz(4 * j4 + 0, c, 64)], src[swz(4 * j4 + 1, c, 64)],
-                               src[swz(4 * j4 + 2, c, 64)], src[swz(4 * j4 + 3, c, 64)]);
-        if (scale) {
-            v.x *= scale[4 * j4 + 0]; v.y *= scale[4 * j4 + 1];
-            v.z *= scale[4 * j4 + 2]; v.w *= scale[4 * j4 + 3];
-        }
-        *reinterpret_cast<float4*>(dst + kidx(c, 4 * j4, 64)) = tf32r(v);
-    }
-}
-
 // Eight 16x256b loads of an M = 64 accumulator (columns col0 .. col0 + 63 of
 // this warp's 16-lane window, one wait): thread t holds, for column block k,
 // v[4k + j] = D[row0 + t/4 + 8 (j/2)][col0 + 8k + 2 (t%4) + j%2], where row0 =
