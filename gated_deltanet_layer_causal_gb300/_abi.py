@@ -31,6 +31,10 @@ GDN_WS_NORM_BWD = 3
 GDN_NOALLOC_NORM_BWD_MAX_ROWS = 524288
 
 
+# GDN_ABI_VERSION of include/gdn.h that GdnDims and SIGNATURES mirror
+ABI_VERSION = 200
+
+
 class GdnDims(ctypes.Structure):
     """Mirror of gdn_dims."""
     _fields_ = [
@@ -93,6 +97,9 @@ def load():
     lib.gdn_launch_count.restype = ctypes.c_int64
     lib.gdn_abi_version.argtypes = []
     lib.gdn_abi_version.restype = ctypes.c_int32
+    if lib.gdn_abi_version() != ABI_VERSION:
+        raise RuntimeError(f"libgdn.so at {LIB_PATH} has ABI {lib.gdn_abi_version()}, this "
+                           f"binding expects {ABI_VERSION}: rebuild it")
     _lib = lib
     return lib
 

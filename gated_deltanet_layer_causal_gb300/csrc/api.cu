@@ -134,7 +134,7 @@ gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_E
 
 extern "C" {
 
-int32_t gdn_abi_version(void) { return 100; }
+int32_t gdn_abi_version(void) { return GDN_ABI_VERSION; }
 
 const char* gdn_status_string(gdn_status s) {
     switch (s) {

@@ -229,7 +229,9 @@ gdn_status gdn_profile_report(char* buf, size_t buf_bytes);
 /* Human-readable name of a status code (static storage). */
 const char* gdn_status_string(gdn_status status);
 
-/* ABI version of this header (major * 100 + minor). */
+/* ABI version of this header (major * 100 + minor); the major number changes
+ * whenever a struct or a signature changes (2.00: gdn_dims.qkv_tf32). */
+#define GDN_ABI_VERSION 200
 int32_t gdn_abi_version(void);
 
 #ifdef __cplusplus

@@ -4,6 +4,7 @@ only entry points that fail validation (and so never touch CUDA) are called."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 import torch
@@ -36,7 +37,7 @@ def test_header_declares_the_core_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared():
         assert hasattr(lib, name), name
-    assert lib.gdn_abi_version() == 100
+    assert lib.gdn_abi_version() == _abi.ABI_VERSION
 
 
 def test_status_strings(lib):
@@ -63,6 +64,25 @@ def test_workspace_sizes(lib):
     assert st == 0 and bwd > fwd / 2
     st, _ = _ws(lib, d, [0, 65, 130], _abi.GDN_WS_CONV_BWD)
     assert st == 0
+
+
+def test_dims_struct_layout_matches_the_header(tmp_path):
+    """ctypes' GdnDims has gdn_dims' size and field offsets (gcc on the header)."""
+    fields = [f for f, _ in _abi.GdnDims._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text(
+        "#include <stddef.h>\n#include <stdio.h>\n#include \"gdn.h\"\n"
+        "int main(void) {\n  printf(\"%zu\", sizeof(gdn_dims));\n"
+        + "".join(f'  printf(" %zu", offsetof(gdn_dims, {f}));\n' for f in fields)
+        + "  printf(\" %d\\n\", GDN_ABI_VERSION);\n  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)],
+                   check=True)
+    out = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(_abi.GdnDims)
+    assert out[1:-1] == [getattr(_abi.GdnDims, f).offset for f in fields]
+    assert out[-1] == _abi.ABI_VERSION
 
 
 @pytest.mark.parametrize("cu,why", [([0, 70, 60], "decreasing"), ([1, 65, 130], "cu[0] != 0"),
