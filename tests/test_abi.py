@@ -130,3 +130,10 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_abi, "_lib", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         _abi.load()
+
+
+def test_binding_rejects_a_library_of_another_abi(lib, monkeypatch):
+    monkeypatch.setattr(_abi, "ABI_VERSION", _abi.ABI_VERSION + 1)
+    monkeypatch.setattr(_abi, "_lib", None)
+    with pytest.raises(RuntimeError, match="rebuild"):
+        _abi.load()
