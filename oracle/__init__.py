@@ -72,8 +72,8 @@ def _load():
                                           _U8, _D, _D, _D, _D, _D, _D]),
         "gdn_ref_chunked_fwd": (None, [i, _I32, i, i, i, i, i, _D, _D, _D, _D, _D, _D, _D,
                                        _D]),
-        "gdn_ref_gated_rmsnorm": (None, [i64, i, d, _D, _D, _D, _D, _D]),
-        "gdn_ref_gated_rmsnorm_bwd": (None, [i64, i, d, _D, _D, _D, _D, _D, _D, _D]),
+        "gdn_ref_gated_rmsnorm": (None, [i64, i, d, i, _D, _D, _D, _D, _D]),
+        "gdn_ref_gated_rmsnorm_bwd": (None, [i64, i, d, i, _D, _D, _D, _D, _D, _D, _D]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -241,23 +241,81 @@ def chunked_delta_rule(qh, kh, v, g, beta, cu, S0=None, chunk=64):
     return o, Sf
 
 
-def gated_rmsnorm(o, z, w, eps):
-    """y = o / sqrt(mean(o^2) + eps) * (1 + w) * silu(z) over the last axis."""
+GATES = {"silu": 0, "sigmoid": 1}
+
+
+def gated_rmsnorm(o, z, w, eps, gate="silu"):
+    """y = o / sqrt(mean(o^2) + eps) * (1 + w) * gate(z) over the last axis, gate
+    silu or sigmoid ("prime-rl #3860", "Summary": output_gate_type)."""
     o, z, w = _f64(o), _f64(z), _f64(w)
     d = o.shape[-1]
     y = np.empty_like(o)
     rstd = np.empty(o.shape[:-1])
-    _load().gdn_ref_gated_rmsnorm(o.size // d, d, eps, _p(o), _p(z), _p(w), _p(y), _p(rstd))
+    _load().gdn_ref_gated_rmsnorm(o.size // d, d, eps, GATES[gate], _p(o), _p(z), _p(w), _p(y),
+                                  _p(rstd))
     return y, rstd
 
 
-def gated_rmsnorm_bwd(o, z, w, dy, eps):
+def gated_rmsnorm_bwd(o, z, w, dy, eps, gate="silu"):
     o, z, w, dy = map(_f64, (o, z, w, dy))
     d = o.shape[-1]
     do, dz, dw = np.empty_like(o), np.empty_like(o), np.empty(d)
-    _load().gdn_ref_gated_rmsnorm_bwd(o.size // d, d, eps, _p(o), _p(z), _p(w), _p(dy), _p(do),
-                                      _p(dz), _p(dw))
+    _load().gdn_ref_gated_rmsnorm_bwd(o.size // d, d, eps, GATES[gate], _p(o), _p(z), _p(w),
+                                      _p(dy), _p(do), _p(dz), _p(dw))
     return do, dz, dw
+
+
+def conv_state_out_bwd(cu, dcso, dx, dcs=None):
+    """Gradient of conv_state_out, which copies each sequence's last K-1 conv
+    inputs: the input at position e-(K-1)+m of sequence [s, e) receives
+    dcso[n, :, m] -- in dx when it is a token of the sequence, else in dcs, the
+    gradient of the conv cache it came from (cache slot (K-1) + (p - s)).
+    Adds into dx [T, C] and dcs [N, C, K-1] (nullable) in place."""
+    K1 = dcso.shape[2]
+    for n in range(len(cu) - 1):
+        s, e = int(cu[n]), int(cu[n + 1])
+        for m in range(K1):
+            p = e - K1 + m
+            if p >= s:
+                dx[p] += dcso[n, :, m]
+            elif dcs is not None:
+                dcs[n, :, K1 + (p - s)] += dcso[n, :, m]
+
+
+def group_major_order(hk, hv, dk=128, dv=128):
+    """Flat channel of each group-major channel: x_group[:, j] = x_flat[:, order[j]].
+
+    Flat x is [q (H_k d_k) | k (H_k d_k) | v (H_v d_v)] ("HF's flat layout");
+    group-major puts each k-head group's channels together, [q_kh | k_kh |
+    v_{kh G} .. v_{kh G + G - 1}] for kh = 0 .. H_k - 1 ("[6/8] feat(models): port
+    Qwen3.5 / Qwen3-Next GDN to the head-sharded layer", "What": q/k/v and the
+    conv change layout to group-major)."""
+    G = hv // hk
+    order = []
+    for kh in range(hk):
+        order += range(kh * dk, (kh + 1) * dk)
+        order += range(hk * dk + kh * dk, hk * dk + (kh + 1) * dk)
+        for h in range(kh * G, (kh + 1) * G):
+            order += range(2 * hk * dk + h * dv, 2 * hk * dk + (h + 1) * dv)
+    return np.array(order)
+
+
+def _to_flat(a, order, axis):
+    """Group-major -> flat along `axis` (None passes through)."""
+    if a is None:
+        return None
+    a = np.asarray(a)
+    out = np.empty_like(a)
+    idx = [slice(None)] * a.ndim
+    idx[axis] = order
+    out[tuple(idx)] = a
+    return out
+
+
+def _to_group(a, order, axis):
+    if a is None:
+        return None
+    return np.ascontiguousarray(np.take(a, order, axis=axis))
 
 
 # --------------------------------------------------------------------------- layer
@@ -270,33 +328,64 @@ def _split(xc, hk, hv, dk, dv):
 
 
 def forward(x, conv_w, a, b, A_log, dt_bias, z, norm_w, cu, hk, hv, dk=128, dv=128,
-            S0=None, conv_state=None, l2_eps=1e-6, norm_eps=1e-6, heads=None):
+            S0=None, conv_state=None, l2_eps=1e-6, norm_eps=1e-6, heads=None, gate="silu",
+            layout="flat"):
     """GDN core forward.  Returns a dict with every intermediate.
 
     x [T, C]; conv_w [C, K]; a, b [T, H_v]; A_log, dt_bias [H_v]; z [T, H_v, d_v];
-    norm_w [d_v]; cu int32 [N+1]; S0 [N, H_v, d_v, d_k]; conv_state [N, C, K-1]."""
+    norm_w [d_v]; cu int32 [N+1]; S0 [N, H_v, d_v, d_k]; conv_state [N, C, K-1].
+    gate: "silu" | "sigmoid"; layout: "flat" | "group" -- the channel order of x,
+    conv_w and the conv states (the intermediates pre / xc are always flat)."""
+    if layout == "group":
+        order = group_major_order(hk, hv, dk, dv)
+        f = forward(_to_flat(x, order, 1), _to_flat(conv_w, order, 0), a, b, A_log, dt_bias, z,
+                    norm_w, cu, hk, hv, dk, dv, S0, _to_flat(conv_state, order, 1), l2_eps,
+                    norm_eps, heads, gate)
+        f["conv_state_out"] = _to_group(f["conv_state_out"], order, 1)
+        return f
     pre, xc, cso = conv_silu(x, conv_w, cu, conv_state)
     q, k, v = _split(xc, hk, hv, dk, dv)
     qh = l2norm(q, l2_eps, dk ** -0.5)
     kh = l2norm(k, l2_eps, 1.0)
     g, beta = gates(a, b, A_log, dt_bias)
     o, Sf = delta_rule(qh, kh, v, g, beta, cu, S0, heads)
-    y, rstd = gated_rmsnorm(o, z, norm_w, norm_eps)
+    y, rstd = gated_rmsnorm(o, z, norm_w, norm_eps, gate)
     return dict(pre=pre, xc=xc, qh=qh, kh=kh, v=v, g=g, beta=beta, o=o, y=y, S_final=Sf,
                 conv_state_out=cso, rstd=rstd)
 
 
 def backward(x, conv_w, a, b, A_log, dt_bias, z, norm_w, cu, hk, hv, dy, dk=128, dv=128,
-             S0=None, conv_state=None, dS_final=None, l2_eps=1e-6, norm_eps=1e-6, heads=None):
+             S0=None, conv_state=None, dS_final=None, l2_eps=1e-6, norm_eps=1e-6, heads=None,
+             norm=True, gate="silu", layout="flat", dconv_state_out=None):
     """GDN core backward (reverse mode through :func:`forward`).
 
     Returns dx, dconv_w, da, db, dA_log, ddt_bias, dz, dnorm_w, dS0, dconv_state
     and the intermediate gradients dq^, dk^, dv, dg, dbeta, do.  With ``heads``
     (whole k-head groups) only those heads' gradients are exact; dnorm_w and the
-    channels of other heads are then partial."""
+    channels of other heads are then partial.  ``norm=False``: the core without
+    the gated norm -- dy is the gradient of o itself (z and norm_w unused; dz and
+    dnorm_w are None).  dconv_state_out: gradient of the conv_state_out output
+    [N, C, K-1] (nullable).  layout / gate as in :func:`forward`."""
+    if layout == "group":
+        order = group_major_order(hk, hv, dk, dv)
+        r = backward(_to_flat(x, order, 1), _to_flat(conv_w, order, 0), a, b, A_log, dt_bias, z,
+                     norm_w, cu, hk, hv, dy, dk, dv, S0, _to_flat(conv_state, order, 1),
+                     dS_final, l2_eps, norm_eps, heads, norm, gate,
+                     dconv_state_out=_to_flat(dconv_state_out, order, 1))
+        r["dx"] = _to_group(r["dx"], order, 1)
+        r["dconv_w"] = _to_group(r["dconv_w"], order, 0)
+        r["dconv_state"] = _to_group(r["dconv_state"], order, 1)
+        r["fwd"]["conv_state_out"] = _to_group(r["fwd"]["conv_state_out"], order, 1)
+        return r
+    if not norm:   # the norm stage is computed but receives no gradient
+        z = np.zeros((x.shape[0], hv, dv)) if z is None else z
+        norm_w = np.zeros(dv) if norm_w is None else norm_w
     f = forward(x, conv_w, a, b, A_log, dt_bias, z, norm_w, cu, hk, hv, dk, dv, S0, conv_state,
-                l2_eps, norm_eps, heads)
-    do, dz, dnw = gated_rmsnorm_bwd(f["o"], z, norm_w, dy, norm_eps)
+                l2_eps, norm_eps, heads, gate)
+    if norm:
+        do, dz, dnw = gated_rmsnorm_bwd(f["o"], z, norm_w, dy, norm_eps, gate)
+    else:
+        do, dz, dnw = _f64(dy), None, None
     dqh, dkh, dvv, dg, dbeta, dS0 = delta_rule_bwd(f["qh"], f["kh"], f["v"], f["g"], f["beta"],
                                                    cu, do, S0, dS_final, heads)
     q, k, _ = _split(f["xc"], hk, hv, dk, dv)
@@ -305,6 +394,8 @@ def backward(x, conv_w, a, b, A_log, dt_bias, z, norm_w, cu, hk, hv, dy, dk=128,
     T = x.shape[0]
     dxc = np.concatenate([dq.reshape(T, -1), dkk.reshape(T, -1), dvv.reshape(T, -1)], axis=1)
     dx, dcw, dcs = conv_silu_bwd(x, conv_w, cu, dxc, conv_state)
+    if dconv_state_out is not None:
+        conv_state_out_bwd(cu, _f64(dconv_state_out), dx, dcs)
     da, db, dA, ddt = gates_bwd(a, b, A_log, dt_bias, dg, dbeta)
     return dict(dx=dx, dconv_w=dcw, da=da, db=db, dA_log=dA, ddt_bias=ddt, dz=dz, dnorm_w=dnw,
                 dS0=dS0, dconv_state=dcs, dqh=dqh, dkh=dkh, dv=dvv, dg=dg, dbeta=dbeta, do=do,
@@ -312,7 +403,7 @@ def backward(x, conv_w, a, b, A_log, dt_bias, z, norm_w, cu, hk, hv, dy, dk=128,
 
 
 def decode_step(x_t, conv_w, conv_state, a_t, b_t, A_log, dt_bias, z_t, norm_w, S, hk, hv,
-                dk=128, dv=128, l2_eps=1e-6, norm_eps=1e-6):
+                dk=128, dv=128, l2_eps=1e-6, norm_eps=1e-6, gate="silu", layout="flat"):
     """One recurrent decode step for a batch of N independent sequences.
 
     It is the forward of N sequences of length 1 that start from the given
@@ -321,5 +412,36 @@ def decode_step(x_t, conv_w, conv_state, a_t, b_t, A_log, dt_bias, z_t, norm_w, 
     N = x_t.shape[0]
     cu = np.arange(N + 1, dtype=np.int32)
     f = forward(x_t, conv_w, a_t, b_t, A_log, dt_bias, z_t, norm_w, cu, hk, hv, dk, dv, S,
-                conv_state, l2_eps, norm_eps)
+                conv_state, l2_eps, norm_eps, gate=gate, layout=layout)
     return f["y"], f["o"], f["S_final"], f["conv_state_out"]
+
+
+# --------------------------------------------------------------------------- whole layer
+def layer_backward(hidden, W_qkv, W_z, W_b, W_a, W_out, conv_w, A_log, dt_bias, norm_w, cu, hk,
+                   hv, dout, d=128, gate="silu", layout="flat", act=None):
+    """The GDN layer around the core: four input projections, the core, one output
+    projection (library matmuls in fp64), forward and reverse mode.
+
+    hidden [T, D_h]; W_qkv [C, D_h]; W_z [H_v d, D_h]; W_b, W_a [H_v, D_h];
+    W_out [D_h, H_v d]; dout [T, D_h].  act (nullable): the layer's activation
+    storage, applied to each projection's output (e.g. rounding to bf16 when the
+    layer keeps its activations in bf16).  Returns the output and the gradients
+    of hidden and of every weight."""
+    hidden, dout = _f64(hidden), _f64(dout)
+    W_qkv, W_z, W_b, W_a, W_out = map(_f64, (W_qkv, W_z, W_b, W_a, W_out))
+    act = act or (lambda v: v)
+    T = hidden.shape[0]
+    x = act(hidden @ W_qkv.T)
+    z = act(hidden @ W_z.T).reshape(T, hv, d)
+    b = act(hidden @ W_b.T)
+    a = act(hidden @ W_a.T)
+    dy = (dout @ W_out).reshape(T, hv, d)
+    r = backward(x, conv_w, a, b, A_log, dt_bias, z, norm_w, cu, hk, hv, dy, d, d, gate=gate,
+                 layout=layout)
+    y = r["fwd"]["y"].reshape(T, hv * d)
+    dz = r["dz"].reshape(T, hv * d)
+    return dict(out=y @ W_out.T, dhidden=r["dx"] @ W_qkv + dz @ W_z + r["db"] @ W_b
+                + r["da"] @ W_a, dW_qkv=r["dx"].T @ hidden, dW_z=dz.T @ hidden,
+                dW_b=r["db"].T @ hidden, dW_a=r["da"].T @ hidden, dW_out=dout.T @ y,
+                dconv_w=r["dconv_w"], dA_log=r["dA_log"], ddt_bias=r["ddt_bias"],
+                dnorm_w=r["dnorm_w"])

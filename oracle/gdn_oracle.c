@@ -28,7 +28,8 @@
  *   gates:  g = -exp(A_log[h]) * softplus(a + dt_bias[h]) ;  beta = sigmoid(b)
  *   rule:   S_t = exp(g_t) S_{t-1} (I - beta_t k^_t k^_t^T) + beta_t v_t k^_t^T
  *           o_t = S_t q^_t          (S is [d_v x d_k]; fp64 here)
- *   norm:   y = o / sqrt(mean(o^2) + eps) * (1 + w) * silu(z)
+ *   norm:   y = o / sqrt(mean(o^2) + eps) * (1 + w) * gate(z), gate = silu
+ *           or sigmoid
  * v-head h reads the q^/k^ of k-head floor(h / (H_v/H_k)).
  *
  * Pins (tests/test_oracle_*.py): the token recurrence against the naive chunked
@@ -481,11 +482,21 @@ void gdn_ref_chunked_fwd(int N, const int32_t *cu, int hk, int hv, int dk, int d
 /* ------------------------------------------------------------------------ */
 /* Zero-centred gated RMSNorm ([P2] "Summary": ZeroCenteredRMSNorm; [P3]      */
 /* --apply-layernorm-1p), per (token, v-head) over d_v, weight shared by all  */
-/* heads:  y = o / sqrt(mean(o^2) + eps) * (1 + w) * silu(z)                  */
+/* heads:  y = o / sqrt(mean(o^2) + eps) * (1 + w) * gate(z)                  */
+/* gate: 0 = silu, 1 = sigmoid ([P2] "Summary": the shared GatedDeltaNet      */
+/* takes output_gate_type; Qwen3.8 passes "sigmoid").                         */
 /*   o, z, y [rows, d]; w [d]; rstd [rows] (nullable)                         */
 /* ------------------------------------------------------------------------ */
-void gdn_ref_gated_rmsnorm(int64_t rows, int d, double eps, const double *o, const double *z,
-                           const double *w, double *y, double *rstd)
+static double out_gate(double z, int gate) { return gate ? sigm(z) : silu(z); }
+/* d/dz sigmoid(z) = s (1 - s) */
+static double dout_gate(double z, int gate)
+{
+    if (gate) { double s = sigm(z); return s * (1.0 - s); }
+    return dsilu(z);
+}
+
+void gdn_ref_gated_rmsnorm(int64_t rows, int d, double eps, int gate, const double *o,
+                           const double *z, const double *w, double *y, double *rstd)
 {
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; r++) {
@@ -494,15 +505,15 @@ void gdn_ref_gated_rmsnorm(int64_t rows, int d, double eps, const double *o, con
         double rs = 1.0 / sqrt(ss / d + eps);
         if (rstd) rstd[r] = rs;
         for (int i = 0; i < d; i++)
-            y[r * d + i] = o[r * d + i] * rs * (1.0 + w[i]) * silu(z[r * d + i]);
+            y[r * d + i] = o[r * d + i] * rs * (1.0 + w[i]) * out_gate(z[r * d + i], gate);
     }
 }
 
-/* Backward: with n = o rs, dn = dy (1+w) silu(z):
- *   do = rs (dn - n mean(dn n)) ; dz = dy n (1+w) silu'(z) ; dw = sum_rows dy n silu(z) */
-void gdn_ref_gated_rmsnorm_bwd(int64_t rows, int d, double eps, const double *o, const double *z,
-                               const double *w, const double *dy, double *do_, double *dz,
-                               double *dw)
+/* Backward: with n = o rs, dn = dy (1+w) gate(z):
+ *   do = rs (dn - n mean(dn n)) ; dz = dy n (1+w) gate'(z) ; dw = sum_rows dy n gate(z) */
+void gdn_ref_gated_rmsnorm_bwd(int64_t rows, int d, double eps, int gate, const double *o,
+                               const double *z, const double *w, const double *dy, double *do_,
+                               double *dz, double *dw)
 {
     for (int i = 0; i < d; i++) dw[i] = 0.0;
     for (int64_t r = 0; r < rows; r++) {
@@ -512,17 +523,17 @@ void gdn_ref_gated_rmsnorm_bwd(int64_t rows, int d, double eps, const double *o,
         double m = 0.0;
         for (int i = 0; i < d; i++) {
             double nn = o[r * d + i] * rs;
-            double dn = dy[r * d + i] * (1.0 + w[i]) * silu(z[r * d + i]);
+            double dn = dy[r * d + i] * (1.0 + w[i]) * out_gate(z[r * d + i], gate);
             m += dn * nn;
         }
         m /= d;
         for (int i = 0; i < d; i++) {
             double nn = o[r * d + i] * rs;
             double zz = z[r * d + i];
-            double dn = dy[r * d + i] * (1.0 + w[i]) * silu(zz);
+            double dn = dy[r * d + i] * (1.0 + w[i]) * out_gate(zz, gate);
             do_[r * d + i] = rs * (dn - nn * m);
-            dz[r * d + i] = dy[r * d + i] * nn * (1.0 + w[i]) * dsilu(zz);
-            dw[i] += dy[r * d + i] * nn * silu(zz);
+            dz[r * d + i] = dy[r * d + i] * nn * (1.0 + w[i]) * dout_gate(zz, gate);
+            dw[i] += dy[r * d + i] * nn * out_gate(zz, gate);
         }
     }
 }

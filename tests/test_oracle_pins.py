@@ -159,16 +159,27 @@ def test_conv_against_library():
             np.testing.assert_array_equal(cso[n], hist[:, -(K - 1):])
 
 
-def test_gated_norm_against_library():
+@pytest.mark.parametrize("gate,fn", [("silu", F.silu), ("sigmoid", torch.sigmoid)])
+def test_gated_norm_against_library(gate, fn):
     rng = np.random.default_rng(17)
     o = rng.standard_normal((20, 3, 16))
     z = rng.standard_normal((20, 3, 16))
     w = rng.normal(0, 0.02, size=16)
-    y, rstd = oracle.gated_rmsnorm(o, z, w, 1e-6)
+    y, rstd = oracle.gated_rmsnorm(o, z, w, 1e-6, gate)
     to = torch.from_numpy(o)
-    ref = F.rms_norm(to, (16,), weight=1 + torch.from_numpy(w), eps=1e-6) * F.silu(
+    ref = F.rms_norm(to, (16,), weight=1 + torch.from_numpy(w), eps=1e-6) * fn(
         torch.from_numpy(z))
     np.testing.assert_allclose(y, ref.numpy(), rtol=1e-12, atol=1e-14)
+    # the backward against torch autograd of the same library expression
+    dy = rng.standard_normal(o.shape)
+    to.requires_grad_(True)
+    tz = torch.from_numpy(z).requires_grad_(True)
+    tw = torch.from_numpy(w).requires_grad_(True)
+    (F.rms_norm(to, (16,), weight=1 + tw, eps=1e-6) * fn(tz) * torch.from_numpy(dy)).sum().backward()
+    do, dz, dw = oracle.gated_rmsnorm_bwd(o, z, w, dy, 1e-6, gate)
+    np.testing.assert_allclose(do, to.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dz, tz.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dw, tw.grad.numpy(), rtol=1e-10, atol=1e-12)
 
 
 def test_l2norm_against_library():
@@ -264,10 +275,45 @@ def test_decode_equals_last_step():
     np.testing.assert_array_equal(cs, f["conv_state_out"])
 
 
+def test_group_major_layout_keeps_each_group_contiguous():
+    """Group-major x holds each k-head group's q, k and v heads as one contiguous
+    block of (2 + G) d channels: that block alone, as an H_k = 1 problem (where
+    the flat and group-major orders coincide), gives exactly the group's part of
+    the whole problem -- outputs, final state, conv cache and every gradient."""
+    rng = np.random.default_rng(61)
+    hk, hv, d, G = 3, 6, 4, 2
+    p = _layer(rng, [19, 8], hk, hv, d, dt_bias=-3.0, cache=True, s0=True)
+    f = oracle.forward(**p, layout="group")
+    dy = rng.standard_normal(f["y"].shape)
+    dcso = rng.standard_normal(f["conv_state_out"].shape)
+    r = oracle.backward(**p, dy=dy, layout="group", dconv_state_out=dcso)
+    w = (2 + G) * d
+    for kh in range(hk):
+        ch, hs = slice(kh * w, (kh + 1) * w), slice(kh * G, (kh + 1) * G)
+        q = dict(p, x=p["x"][:, ch], conv_w=p["conv_w"][ch], a=p["a"][:, hs], b=p["b"][:, hs],
+                 A_log=p["A_log"][hs], dt_bias=p["dt_bias"][hs], z=p["z"][:, hs], hk=1, hv=G,
+                 S0=p["S0"][:, hs], conv_state=p["conv_state"][:, ch])
+        fg = oracle.forward(**q)
+        np.testing.assert_allclose(fg["y"], f["y"][:, hs], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(fg["S_final"], f["S_final"][:, hs], rtol=1e-12, atol=1e-13)
+        np.testing.assert_array_equal(fg["conv_state_out"], f["conv_state_out"][:, ch])
+        rg = oracle.backward(**q, dy=dy[:, hs], dconv_state_out=dcso[:, ch])
+        for k in ("dx", "dconv_state"):
+            np.testing.assert_allclose(rg[k], r[k][:, ch], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(rg["dconv_w"], r["dconv_w"][ch], rtol=1e-11, atol=1e-12)
+        for k in ("da", "db", "dz"):
+            np.testing.assert_allclose(rg[k], r[k][:, hs], rtol=1e-11, atol=1e-12)
+    # with a single group the two orders are the same order
+    assert (oracle.group_major_order(1, 3, 4, 4) == np.arange(5 * 4)).all()
+
+
 # --------------------------------------------------------------- pin 4: finite differences
-def _loss(p, dy, dSf):
+def _loss(p, dy, dSf, dcso=None):
     f = oracle.forward(**p)
-    return float(np.sum(f["y"] * dy) + np.sum(f["S_final"] * dSf))
+    L = float(np.sum(f["y"] * dy) + np.sum(f["S_final"] * dSf))
+    if dcso is not None:
+        L += float(np.sum(f["conv_state_out"] * dcso))
+    return L
 
 
 GRAD_OF = {"x": "dx", "conv_w": "dconv_w", "a": "da", "b": "db", "A_log": "dA_log",
@@ -291,6 +337,31 @@ def test_backward_finite_differences(d, hk, hv, dt_bias):
         pp = dict(p, **{name: p[name] + eps * R})
         pm = dict(p, **{name: p[name] - eps * R})
         fd = (_loss(pp, dy, dSf) - _loss(pm, dy, dSf)) / (2 * eps)
+        an = float(np.sum(gr[gname] * R))
+        assert abs(fd - an) <= 1e-6 * max(abs(an), 1e-3), (name, fd, an)
+
+
+@pytest.mark.parametrize("gate,layout,lens", [("sigmoid", "flat", [23, 17]),
+                                              ("silu", "group", [23, 2, 0, 9]),
+                                              ("sigmoid", "group", [1, 30])])
+def test_backward_finite_differences_variants(gate, layout, lens):
+    """The same central differences for the sigmoid output gate, the group-major
+    channel layout, and a loss that also weighs conv_state_out (the gradient a
+    split sequence hands back), with sequences shorter than the conv window."""
+    rng = np.random.default_rng(53 + len(lens))
+    p = _layer(rng, lens, 2, 4, 4, dt_bias=-2.0, cache=True, s0=True)
+    p.update(gate=gate, layout=layout)
+    f = oracle.forward(**p)
+    dy = rng.standard_normal(f["y"].shape)
+    dSf = rng.standard_normal(f["S_final"].shape)
+    dcso = rng.standard_normal(f["conv_state_out"].shape)
+    gr = oracle.backward(**p, dy=dy, dS_final=dSf, dconv_state_out=dcso)
+    eps = 1e-6
+    for name, gname in GRAD_OF.items():
+        R = rng.standard_normal(np.shape(p[name]))
+        pp = dict(p, **{name: p[name] + eps * R})
+        pm = dict(p, **{name: p[name] - eps * R})
+        fd = (_loss(pp, dy, dSf, dcso) - _loss(pm, dy, dSf, dcso)) / (2 * eps)
         an = float(np.sum(gr[gname] * R))
         assert abs(fd - an) <= 1e-6 * max(abs(an), 1e-3), (name, fd, an)
 
