@@ -8,11 +8,13 @@ include/gdn.h); this package is its torch-facing binding:
                               cu_seqlens, h_k, h_v, output_final_state=True)
 
 Lower-level entry points mirror the C ABI: conv1d_silu(_bwd), chunk_fwd,
-chunk_bwd, gated_rmsnorm(_bwd), recurrent_step.
+chunk_bwd, gated_rmsnorm(_bwd), recurrent_step.  GDNLayer wraps the core in
+its input and output projections (the whole layer).
 """
 from .core import (GDNCore, chunk_bwd, chunk_fwd, conv1d_silu, conv1d_silu_bwd, gated_rmsnorm,
                    gated_rmsnorm_bwd, gdn_core, read_status, recurrent_step, workspace_size)
+from .layer import GDNLayer
 
-__all__ = ["GDNCore", "gdn_core", "conv1d_silu", "conv1d_silu_bwd", "chunk_fwd", "chunk_bwd",
+__all__ = ["GDNCore", "GDNLayer", "gdn_core", "conv1d_silu", "conv1d_silu_bwd", "chunk_fwd", "chunk_bwd",
            "gated_rmsnorm", "gated_rmsnorm_bwd", "recurrent_step", "read_status",
            "workspace_size"]

@@ -22,6 +22,13 @@ GDN_ERR_DEVICE_CHECK = 6
 # dtypes (gdn_dtype)
 GDN_F32 = 0
 GDN_BF16 = 1
+# output gates (gdn_gate) and channel layouts (gdn_layout)
+GDN_GATE_SILU = 0
+GDN_GATE_SIGMOID = 1
+GDN_LAYOUT_FLAT = 0
+GDN_LAYOUT_GROUP = 1
+GATES = {"silu": GDN_GATE_SILU, "sigmoid": GDN_GATE_SIGMOID}
+LAYOUTS = {"flat": GDN_LAYOUT_FLAT, "group": GDN_LAYOUT_GROUP}
 # workspace kinds
 GDN_WS_FWD = 0
 GDN_WS_BWD = 1
@@ -32,7 +39,7 @@ GDN_NOALLOC_NORM_BWD_MAX_ROWS = 524288
 
 
 # GDN_ABI_VERSION of include/gdn.h that GdnDims and SIGNATURES mirror
-ABI_VERSION = 200
+ABI_VERSION = 300
 
 
 class GdnDims(ctypes.Structure):
@@ -50,6 +57,8 @@ class GdnDims(ctypes.Structure):
         ("l2_eps", ctypes.c_float),
         ("norm_eps", ctypes.c_float),
         ("qkv_tf32", ctypes.c_int32),
+        ("gate", ctypes.c_int32),
+        ("layout", ctypes.c_int32),
     ]
 
 
@@ -61,7 +70,7 @@ _DP = ctypes.POINTER(GdnDims)
 SIGNATURES = {
     "gdn_workspace_size": [_DP, _P, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
     "gdn_conv1d_silu": [_DP, _P, _P, _P, _P, _P, _P, _P, _P],
-    "gdn_conv1d_silu_bwd": [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P],
+    "gdn_conv1d_silu_bwd": [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P],
     "gdn_chunk_fwd": [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P],
     "gdn_chunk_bwd": [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P, _P, _P, _P, _P,
                       _P, _P, _P, _P, _P, _P, _S, _P],
@@ -70,6 +79,7 @@ SIGNATURES = {
     "gdn_gated_rmsnorm_bwd_noalloc": [_DP, _P, _P, _P, _P, _P, _P, _P, _P],
     "gdn_recurrent_step": [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "gdn_read_status": [_P, ctypes.POINTER(ctypes.c_int32), _P],
+    "gdn_selftest_bounded_wait": [_P, _S, ctypes.c_int32, ctypes.c_int32, _P],
     "gdn_profile_enable": [ctypes.c_int32],
     "gdn_profile_report": [ctypes.c_char_p, _S],
 }
@@ -119,10 +129,12 @@ def call(name: str, *args) -> None:
 
 
 def dims(num_seqs, total_tokens, h_k, h_v, io_bf16, l2_eps=1e-6, norm_eps=1e-6, d=128,
-         conv_k=4, chunk=64, qkv_tf32=False) -> GdnDims:
+         conv_k=4, chunk=64, qkv_tf32=False, gate="silu", layout="flat") -> GdnDims:
+    """gate: "silu" | "sigmoid" (output gate of the gated norm); layout: "flat" |
+    "group" (q/k/v channel order of x, conv_w and the conv states)."""
     return GdnDims(int(num_seqs), int(total_tokens), int(h_k), int(h_v), d, d, conv_k, chunk,
                    GDN_BF16 if io_bf16 else GDN_F32, float(l2_eps), float(norm_eps),
-                   1 if qkv_tf32 else 0)
+                   1 if qkv_tf32 else 0, GATES[gate], LAYOUTS[layout])
 
 
 def launch_count() -> int:

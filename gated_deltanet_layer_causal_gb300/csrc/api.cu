@@ -30,6 +30,8 @@ gdn_status check_dims(const gdn_dims* d) {
     if (d->total_tokens >= (int64_t)1 << 31) return GDN_ERR_UNSUPPORTED;
     if (!(d->l2_eps >= 0.f) || !(d->norm_eps >= 0.f)) return GDN_ERR_INVALID_ARG;
     if (d->qkv_tf32 != 0 && d->qkv_tf32 != 1) return GDN_ERR_INVALID_ARG;
+    if (d->gate != GDN_GATE_SILU && d->gate != GDN_GATE_SIGMOID) return GDN_ERR_INVALID_ARG;
+    if (d->layout != GDN_LAYOUT_FLAT && d->layout != GDN_LAYOUT_GROUP) return GDN_ERR_INVALID_ARG;
     return GDN_OK;
 }
 
@@ -49,6 +51,25 @@ gdn_status check_cu(const gdn_dims* d, const int32_t* cu, int* nt) {
 }
 
 int channels(const gdn_dims* d) { return (2 * d->h_k + d->h_v) * kD; }
+
+ConvArgs conv_args(const gdn_dims* d, const int32_t* cu, const void* x, const float* conv_w,
+                   const void* cs_in) {
+    ConvArgs a{};
+    a.bf16 = d->io_dtype == GDN_BF16;
+    a.group_major = d->layout == GDN_LAYOUT_GROUP;
+    a.N = d->num_seqs;
+    a.C = channels(d);
+    a.hk = d->h_k;
+    a.hv = d->h_v;
+    a.T = d->total_tokens;
+    a.cu = cu;
+    a.x = x;
+    a.w = conv_w;
+    a.cs_in = cs_in;
+    a.l2_eps = d->l2_eps;
+    a.q_scale = 1.f / sqrtf((float)kD);
+    return a;
+}
 
 // ---------------------------------------------------------------- workspace carving
 struct Carver {
@@ -177,18 +198,7 @@ gdn_status gdn_conv1d_silu(const gdn_dims* dims, const int32_t* cu, const int32_
     GDN_NEED(cu && aligned16(x) && x && conv_w && aligned16(conv_w) && qkv && aligned16(qkv));
     GDN_NEED(!cs_in || aligned16(cs_in));
     if (dims->num_seqs == 0) return GDN_OK;
-    ConvArgs a{};
-    a.bf16 = dims->io_dtype == GDN_BF16;
-    a.N = dims->num_seqs;
-    a.C = channels(dims);
-    a.hk = dims->h_k;
-    a.T = dims->total_tokens;
-    a.cu = cu;
-    a.x = x;
-    a.w = conv_w;
-    a.cs_in = cs_in;
-    a.l2_eps = dims->l2_eps;
-    a.q_scale = 1.f / sqrtf((float)kD);
+    ConvArgs a = conv_args(dims, cu, x, conv_w, cs_in);
     a.qkv = qkv;
     a.cs_out = cs_out;
     a.round_tf32 = dims->qkv_tf32 != 0;
@@ -197,8 +207,8 @@ gdn_status gdn_conv1d_silu(const gdn_dims* dims, const int32_t* cu, const int32_
 
 gdn_status gdn_conv1d_silu_bwd(const gdn_dims* dims, const int32_t* cu, const int32_t* cu_host,
                                const void* x, const float* conv_w, const void* cs_in,
-                               const float* dqkv, void* dx, float* dconv_w, float* dcs,
-                               void* ws, size_t ws_bytes, void* stream) {
+                               const float* dqkv, const float* dcs_out, void* dx, float* dconv_w,
+                               float* dcs, void* ws, size_t ws_bytes, void* stream) {
     GDN_TRY(check_dims(dims));
     int NT;
     GDN_TRY(check_cu(dims, cu_host, &NT));
@@ -206,19 +216,9 @@ gdn_status gdn_conv1d_silu_bwd(const gdn_dims* dims, const int32_t* cu, const in
     GDN_NEED(dx && aligned16(dx) && dconv_w && (!cs_in || aligned16(cs_in)));
     if (ws == nullptr || ws_bytes < conv_bwd_bytes(dims)) return GDN_ERR_WORKSPACE;
     if (dims->num_seqs == 0) return GDN_OK;
-    ConvArgs a{};
-    a.bf16 = dims->io_dtype == GDN_BF16;
-    a.N = dims->num_seqs;
-    a.C = channels(dims);
-    a.hk = dims->h_k;
-    a.T = dims->total_tokens;
-    a.cu = cu;
-    a.x = x;
-    a.w = conv_w;
-    a.cs_in = cs_in;
-    a.l2_eps = dims->l2_eps;
-    a.q_scale = 1.f / sqrtf((float)kD);
+    ConvArgs a = conv_args(dims, cu, x, conv_w, cs_in);
     a.dqkv = dqkv;
+    a.dcs_out = dcs_out;
     a.dx = dx;
     a.dw = dconv_w;
     a.wpart = reinterpret_cast<float*>(static_cast<char*>(ws) + kAlign);
@@ -249,6 +249,7 @@ static gdn_status fill_chunk_args(ChunkArgs& a, const gdn_dims* dims, int NT, co
     a.z = z;
     a.norm_w = norm_w;
     a.norm_eps = dims->norm_eps;
+    a.gate = dims->gate;
     return GDN_OK;
 }
 
@@ -325,6 +326,7 @@ gdn_status gdn_gated_rmsnorm(const gdn_dims* dims, const void* o, const void* z,
              aligned16(y));
     NormArgs a{};
     a.bf16 = dims->io_dtype == GDN_BF16;
+    a.gate = dims->gate;
     a.rows = dims->total_tokens * dims->h_v;
     a.o = o;
     a.z = z;
@@ -345,6 +347,7 @@ gdn_status gdn_gated_rmsnorm_bwd(const gdn_dims* dims, const void* o, const void
         return GDN_ERR_WORKSPACE;
     NormArgs a{};
     a.bf16 = dims->io_dtype == GDN_BF16;
+    a.gate = dims->gate;
     a.rows = dims->total_tokens * dims->h_v;
     a.o = o;
     a.z = z;
@@ -368,6 +371,7 @@ gdn_status gdn_gated_rmsnorm_bwd_noalloc(const gdn_dims* dims, const void* o, co
         return GDN_ERR_WORKSPACE;
     NormArgs a{};
     a.bf16 = dims->io_dtype == GDN_BF16;
+    a.gate = dims->gate;
     a.rows = dims->total_tokens * dims->h_v;
     a.o = o;
     a.z = z;
@@ -393,6 +397,8 @@ gdn_status gdn_recurrent_step(const gdn_dims* dims, const void* x_t, const float
     GDN_NEED(y_t && aligned16(y_t) && (!o_t || aligned16(o_t)));
     StepArgs a{};
     a.bf16 = dims->io_dtype == GDN_BF16;
+    a.gate = dims->gate;
+    a.group_major = dims->layout == GDN_LAYOUT_GROUP;
     a.N = dims->num_seqs;
     a.hk = dims->h_k;
     a.hv = dims->h_v;

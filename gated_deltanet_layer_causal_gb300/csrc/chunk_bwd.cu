@@ -44,9 +44,9 @@ constexpr int kNormRows = 64;
 template <class IO>
 __global__ void __launch_bounds__(256)
 chunk_norm_bwd_kernel(const float* __restrict__ o, const IO* __restrict__ z,
-                      const float* __restrict__ norm_w, float norm_eps, const IO* __restrict__ dy,
-                      int64_t rows, float* __restrict__ dO, IO* __restrict__ dz,
-                      float* __restrict__ part) {
+                      const float* __restrict__ norm_w, float norm_eps, int gate,
+                      const IO* __restrict__ dy, int64_t rows, float* __restrict__ dO,
+                      IO* __restrict__ dz, float* __restrict__ part) {
     __shared__ float4 red[8][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float4 w4 = z ? ld4(norm_w + lane * 4) : zero4();
@@ -57,7 +57,8 @@ chunk_norm_bwd_kernel(const float* __restrict__ o, const IO* __restrict__ z,
         const float4 dy4 = ld4(dy + off);
         float4 d4 = dy4;
         if (z) {
-            const NormRowGrad gr = norm_row_bwd(ld4(o + off), ld4(z + off), dy4, w4, norm_eps, acc);
+            const NormRowGrad gr =
+                norm_row_bwd(ld4(o + off), ld4(z + off), dy4, w4, norm_eps, acc, gate);
             d4 = gr.d_o;
             st4(dz + off, gr.dz);
         }
@@ -1344,19 +1345,13 @@ SideStream* side_stream() {
 
 template <class IO>
 static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(bwd_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kB1Smem);
-        cudaFuncSetAttribute(bwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kB2Smem);
-        cudaFuncSetAttribute(bwd_sfacing_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kB3aSmem);
-        cudaFuncSetAttribute(bwd_dp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kDpSmem);
-        cudaFuncSetAttribute(bwd_wy_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kWySmem);
-        attr = true;
+    {
+        cudaError_t e = smem_attr(bwd_local_kernel, kB1Smem);
+        if (e == cudaSuccess) e = smem_attr(bwd_state_kernel, kB2Smem);
+        if (e == cudaSuccess) e = smem_attr(bwd_sfacing_kernel, kB3aSmem);
+        if (e == cudaSuccess) e = smem_attr(bwd_dp_kernel, kDpSmem);
+        if (e == cudaSuccess) e = smem_attr(bwd_wy_kernel<IO>, kWySmem);
+        if (e != cudaSuccess) return e;
     }
     float* gate_part = w.nw_part + (size_t)a.NT * a.hv * kD;
     TileMaps maps{};
@@ -1392,7 +1387,7 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
             GDN_PROF("chunk_norm_bwd", st);
             chunk_norm_bwd_kernel<IO><<<(unsigned)((rows + kNormRows - 1) / kNormRows), 256, 0,
                                         st>>>(a.sv.o, (const IO*)a.z, a.norm_w, a.norm_eps,
-                                              (const IO*)a.dy, rows, w.dO, (IO*)a.dz,
+                                              a.gate, (const IO*)a.dy, rows, w.dO, (IO*)a.dz,
                                               w.nw_part);
         }
         GDN_PROF("chunk_bwd_local", st);

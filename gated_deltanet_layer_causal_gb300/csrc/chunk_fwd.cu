@@ -7,7 +7,7 @@
 //   U = U~ - W S0^T ;  S_end = e^{gam_L} S0 + U^T diag(e^{gam_L-gam}) K
 //                                                            (state, sequential)
 //   O = diag(e^gam) Q S0^T + (Q K^T (.) exp(gam_i-gam_j) (.) [i>=j]) U
-//   y = O rsqrt(mean(O^2)+eps) (1+w) silu(z)                 (out, parallel)
+//   y = O rsqrt(mean(O^2)+eps) (1+w) gate(z)                 (out, parallel)
 // which unrolls S_t = e^{g_t} S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
 // o_t = S_t q_t exactly.  Sources: "[6/8] feat(models): port Qwen3.5 / Qwen3-Next
 // GDN to the head-sharded layer" ("What": grouped value heads, native GVA);
@@ -486,7 +486,7 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
 //   D1 = Q K^T (64 x 64),  D3 = Q S0^T (64 x 128)       -- issued together
 //   P  = D1 (.) e^{gam_i - gam_j} (.) [i >= j]          -- staged K-major
 //   D2 = P U (64 x 128)
-//   O  = D2 + e^{gam_i} D3 ; y = O rsqrt(mean(O^2)+eps) (1+w) silu(z)
+//   O  = D2 + e^{gam_i} D3 ; y = O rsqrt(mean(O^2)+eps) (1+w) gate(z)
 // Shared memory: Q, K swizzled 32 KB each and U MN-major 32 KB (TMA; U is the
 // B operand of P U, contracted over tokens, so it is read as loaded), S0
 // (K-major rows a) 64 KB (one bulk copy), P 16 KB, the z rows 33 KB.  The next
@@ -500,7 +500,7 @@ constexpr size_t kOutSmem = sizeof(float) * (kOutFloats + 64 * 2 + 2 * 64 + 16) 
 template <class IO>
 __global__ void __launch_bounds__(256, 1)
 out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, const IO* z,
-               const float* norm_w, float norm_eps, IO* o_out, IO* y_out, FwdSaved sv) {
+               const float* norm_w, float norm_eps, int gate, IO* o_out, IO* y_out, FwdSaved sv) {
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
     float* Qs = sm;                    // [64][128] swizzled
@@ -669,12 +669,7 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
             if (z) {
                 const float rs = rsqrtf((ssq[r] + ssq[64 + r]) * (1.f / kD) + norm_eps);
                 const float4 z4 = ld4(reinterpret_cast<const IO*>(Zs + r * kZPitch) + lane * 4);
-                float4 y4;
-                y4.x = o4.x * rs * (1.f + w4.x) * siluf_(z4.x);
-                y4.y = o4.y * rs * (1.f + w4.y) * siluf_(z4.y);
-                y4.z = o4.z * rs * (1.f + w4.z) * siluf_(z4.z);
-                y4.w = o4.w * rs * (1.f + w4.w) * siluf_(z4.w);
-                st4(y_out + off, y4);
+                st4(y_out + off, gated_norm4(o4, rs, w4, z4, gate));
                 if (lane == 0) sv.rstd[tok * hv + h] = rs;
             }
         }
@@ -703,15 +698,11 @@ cudaError_t launch_plan(const int32_t* cu, int N, int64_t T, int NT, FwdSaved sv
 
 template <class IO>
 static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kPrepSmem);
-        cudaFuncSetAttribute(state_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kStateSmem);
-        cudaFuncSetAttribute(out_fwd_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kOutSmem);
-        attr = true;
+    {
+        cudaError_t e = smem_attr(prep_kernel, kPrepSmem);
+        if (e == cudaSuccess) e = smem_attr(state_fwd_kernel, kStateSmem);
+        if (e == cudaSuccess) e = smem_attr(out_fwd_kernel<IO>, kOutSmem);
+        if (e != cudaSuccess) return e;
     }
     TileMaps maps{};
     if (a.NT > 0) {
@@ -754,7 +745,7 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
         const int ntiles = a.NT * a.hv;
         GDN_PROF("chunk_out_fwd", st);
         out_fwd_kernel<IO><<<min(ntiles, nsm), 256, kOutSmem, st>>>(
-            maps, a.hk, a.hv, a.NT, (const IO*)a.z, a.norm_w, a.norm_eps, (IO*)a.o_out,
+            maps, a.hk, a.hv, a.NT, (const IO*)a.z, a.norm_w, a.norm_eps, a.gate, (IO*)a.o_out,
             (IO*)a.y_out, a.sv);
     }
     return cudaGetLastError();

@@ -42,6 +42,26 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
 // ----------------------------------------------------------------- math
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + __expf(-x)); }
 __device__ __forceinline__ float siluf_(float x) { return x * sigmoidf_(x); }
+
+// Output gate of the gated norm (prime-rl #3860 "Summary": GatedDeltaNet takes
+// an output_gate_type, "silu" for Qwen3.5, "sigmoid" for Qwen3.8): gate 0 =
+// silu(z), gate 1 = sigmoid(z); and its derivative.
+constexpr int kGateSilu = 0, kGateSigmoid = 1;
+__device__ __forceinline__ float out_gate(float z, int gate) {
+    const float s = sigmoidf_(z);
+    return gate == kGateSigmoid ? s : z * s;
+}
+__device__ __forceinline__ float out_gate_grad(float z, int gate) {
+    const float s = sigmoidf_(z);
+    return gate == kGateSigmoid ? s * (1.f - s) : s * (1.f + z * (1.f - s));
+}
+// y = o rs (1 + w) gate(z) for four columns
+__device__ __forceinline__ float4 gated_norm4(float4 o4, float rs, float4 w4, float4 z4, int gate) {
+    return make_float4(o4.x * rs * (1.f + w4.x) * out_gate(z4.x, gate),
+                       o4.y * rs * (1.f + w4.y) * out_gate(z4.y, gate),
+                       o4.z * rs * (1.f + w4.z) * out_gate(z4.z, gate),
+                       o4.w * rs * (1.f + w4.w) * out_gate(z4.w, gate));
+}
 // softplus with torch's linear branch above 20
 __device__ __forceinline__ float softplusf_(float x) { return x > 20.f ? x : log1pf(expf(x)); }
 
@@ -220,13 +240,13 @@ __device__ __forceinline__ void tile_each2(typename Tile<M, N, NW>::Acc& acc, F 
 }
 
 // Backward of one gated-RMSNorm row held by a warp (4 columns per lane):
-//   n = o rs, dn = dy (1+w) silu(z): do = rs (dn - n mean(dn n)),
-//   dz = dy n (1+w) silu'(z), dw += dy n silu(z).
+//   n = o rs, dn = dy (1+w) gate(z): do = rs (dn - n mean(dn n)),
+//   dz = dy n (1+w) gate'(z), dw += dy n gate(z).
 struct NormRowGrad {
     float4 d_o, dz;
 };
 __device__ __forceinline__ NormRowGrad norm_row_bwd(float4 o4, float4 z4, float4 dy4, float4 w4,
-                                                    float eps, float4& dw_acc) {
+                                                    float eps, float4& dw_acc, int gate) {
     float ss = warp_sum(o4.x * o4.x + o4.y * o4.y + o4.z * o4.z + o4.w * o4.w);
     float rs = rsqrtf(ss * (1.f / kD) + eps);
     float o[4] = {o4.x, o4.y, o4.z, o4.w}, z[4] = {z4.x, z4.y, z4.z, z4.w};
@@ -234,9 +254,8 @@ __device__ __forceinline__ NormRowGrad norm_row_bwd(float4 o4, float4 z4, float4
     float nn[4], dn[4], sz[4], dsz[4], m = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; i++) {
-        float s = sigmoidf_(z[i]);
-        sz[i] = z[i] * s;
-        dsz[i] = s * (1.f + z[i] * (1.f - s));
+        sz[i] = out_gate(z[i], gate);
+        dsz[i] = out_gate_grad(z[i], gate);
         nn[i] = o[i] * rs;
         dn[i] = dy[i] * (1.f + w[i]) * sz[i];
         m += dn[i] * nn[i];

@@ -1,4 +1,6 @@
-// Causal depthwise conv1d (4 taps) + SiLU + per-head L2 norm of q and k.
+// Causal depthwise conv1d (4 taps) + SiLU + per-head L2 norm of q and k, and
+// its backward.  x may hold the q / k / v channels flat or group-major; the
+// output qkv is always flat.
 //
 // prime-rl #3860 "Summary": the layer runs causal_conv1d over the q/k/v mix with
 // cu_seqlens (the conv restarts at every sequence start); "[main] feat(moe):
@@ -62,21 +64,54 @@ __device__ __forceinline__ float conv4(const float (&w)[kConvK], float a3, float
     return w[0] * a3 + w[1] * a2 + w[2] * a1 + w[3] * a0;
 }
 
+// Where x's 128-channel block `blk` goes in the conv output qkv (always the
+// flat [q (h_k heads) | k (h_k) | v (h_v)] order the chunk kernels read) and
+// its role: 0 = q, 1 = k, 2 = v.  Flat x: the same block.  Group-major x
+// ("[6/8] feat(models): port Qwen3.5 / Qwen3-Next GDN to the head-sharded
+// layer", "What": q/k/v and the conv in group-major layout): block
+// kh (2 + G) + r holds q (r = 0), k (r = 1) or v-head kh G + r - 2 of k-head
+// group kh, so a group's channels are contiguous.  conv_w and the conv cache
+// follow x's channel order.
+struct ConvBlock {
+    int out, role;
+};
+__device__ __forceinline__ ConvBlock conv_block(int blk, int hk, int G, bool group_major) {
+    if (!group_major) return ConvBlock{blk, blk < hk ? 0 : blk < 2 * hk ? 1 : 2};
+    const int kh = blk / (2 + G), r = blk % (2 + G);
+    return r == 0 ? ConvBlock{kh, 0}
+         : r == 1 ? ConvBlock{hk + kh, 1}
+                  : ConvBlock{2 * hk + kh * G + r - 2, 2};
+}
+
+// Gradient reaching input x[t] of sequence n ([s, e)) through conv_state_out,
+// which copies the sequence's last three inputs: dcso [N, C, 3] (nullable).
+__device__ __forceinline__ void add_state_out_grad(float4& o, const float* dcso, int n, int C,
+                                                   int c, int64_t t, int64_t e) {
+    if (dcso == nullptr || t < e - (kConvK - 1)) return;
+    const float* g = dcso + ((int64_t)n * C + c) * (kConvK - 1) + (t - (e - (kConvK - 1)));
+    o.x += g[0];
+    o.y += g[kConvK - 1];
+    o.z += g[2 * (kConvK - 1)];
+    o.w += g[3 * (kConvK - 1)];
+}
+
 template <class T>
 __global__ void __launch_bounds__(kConvWarps * 32)
 conv_fwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* cs_in,
-                const int32_t* __restrict__ cu, int N, int64_t Ttot, int C, int hk,
-                float l2_eps, float q_scale, bool rnd, float* __restrict__ out) {
+                const int32_t* __restrict__ cu, int N, int64_t Ttot, int C, int hk, int G,
+                bool group_major, float l2_eps, float q_scale, bool rnd, float* __restrict__ out) {
     extern __shared__ __align__(16) unsigned char conv_fwd_smem_raw[];
     T* ring = reinterpret_cast<T*>(conv_fwd_smem_raw);   // [ring][4][threads][4]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int grp = blockIdx.y;
-    const int c = grp * kD + lane * 4;
+    const int c = grp * kD + lane * 4;   // channel of x, conv_w, the cache
+    const ConvBlock cb = conv_block(grp, hk, G, group_major);
+    const int oc = cb.out * kD + lane * 4;   // channel of qkv
     const int64_t t0 = ((int64_t)blockIdx.x * kConvWarps + warp) * kConvRun;
     if (t0 >= Ttot) return;
     const int64_t t1 = min(t0 + (int64_t)kConvRun, Ttot);
-    const bool norm = grp < 2 * hk;
-    const float scale = grp < hk ? q_scale : 1.f;
+    const bool norm = cb.role < 2;
+    const float scale = cb.role == 0 ? q_scale : 1.f;
     float wr[4][kConvK];
 #pragma unroll
     for (int ch = 0; ch < 4; ch++)
@@ -137,7 +172,7 @@ conv_fwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; u++) st4(out + (t + u) * C + c, rnd ? tf32_round(o[u]) : o[u]);
+            for (int u = 0; u < 4; u++) st4(out + (t + u) * C + oc, rnd ? tf32_round(o[u]) : o[u]);
             h3 = xs[1]; h2 = xs[2]; h1 = xs[3];
         }
         cp_async_wait<0>();
@@ -162,7 +197,7 @@ conv_fwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
             float r = rsqrtf(ss + l2_eps) * scale;
             o.x *= r; o.y *= r; o.z *= r; o.w *= r;
         }
-        st4(out + t * C + c, rnd ? tf32_round(o) : o);
+        st4(out + t * C + oc, rnd ? tf32_round(o) : o);
         h3 = h2; h2 = h1; h1 = cur;
     }
 }
@@ -191,13 +226,6 @@ __global__ void conv_state_kernel(const T* __restrict__ x, const T* cs_in,
 }
 
 // ------------------------------------------------------------------ backward
-// dpre at token t for this lane's 4 channels: recompute conv + SiLU (+ L2) and
-// chain the incoming gradient dqkv through L2 and SiLU.
-template <class T>
-__device__ __forceinline__ float4 conv_dpre(const T* x, const T* cs, const float* dq, int64_t t,
-                                            int64_t s, int n, int C, int c,
-                                            const float (&w)[4][kConvK], bool norm, float scale,
-                                            float l2_eps);
 
 // Gradient at the conv output pre-activation of token t (backward through SiLU
 // and, for q / k channels, the L2 norm and the q scale), given the conv inputs
@@ -235,18 +263,56 @@ __device__ __forceinline__ float4 conv_dpre_w(float4 a0, float4 a1, float4 a2, f
     return o;
 }
 
+// dpre at token t for this lane's 4 channels (x channel c, qkv channel oc):
+// recompute conv + SiLU (+ L2) and chain the incoming gradient dqkv through L2
+// and SiLU.
 template <class T>
 __device__ __forceinline__ float4 conv_dpre(const T* x, const T* cs, const float* dq, int64_t t,
-                                            int64_t s, int n, int C, int c,
+                                            int64_t s, int n, int C, int c, int oc,
                                             const float (&w)[4][kConvK], bool norm, float scale,
                                             float l2_eps) {
     return conv_dpre_w(ld4(x + t * C + c), conv_in(x, cs, t - 1, s, n, C, c),
                        conv_in(x, cs, t - 2, s, n, C, c), conv_in(x, cs, t - 3, s, n, C, c),
-                       ld4(dq + t * C + c), w, norm, scale, l2_eps);
+                       ld4(dq + t * C + oc), w, norm, scale, l2_eps);
 }
 
 __device__ __forceinline__ float f4(const float4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Gradient of the conv cache of sequence n (length L), written at its first
+// token: cache position m (input s - 3 + m) feeds tokens s .. s + 2 - m through
+// taps 0 .. 2 - m, and, for a sequence shorter than 3, conv_state_out copies
+// cache positions L .. 2, so their share of dcso comes back here too.
+__device__ __forceinline__ void conv_cache_grad(float* dcs, const float* dcso, int n, int C, int c,
+                                                int64_t L, const float (&wr)[4][kConvK],
+                                                float4 d0, float4 d1, float4 d2) {
+#pragma unroll
+    for (int ch = 0; ch < 4; ch++) {
+        float* o3 = dcs + ((int64_t)n * C + c + ch) * (kConvK - 1);
+        float g[3] = {wr[ch][0] * f4(d0, ch),
+                      wr[ch][0] * f4(d1, ch) + wr[ch][1] * f4(d0, ch),
+                      wr[ch][0] * f4(d2, ch) + wr[ch][1] * f4(d1, ch) + wr[ch][2] * f4(d0, ch)};
+        if (dcso != nullptr)
+            for (int j = (int)L; j < kConvK - 1; j++)
+                g[j] += dcso[((int64_t)n * C + c + ch) * (kConvK - 1) + j - L];
+        o3[0] = g[0];
+        o3[1] = g[1];
+        o3[2] = g[2];
+    }
+}
+
+// The conv-cache gradient before the backward kernel writes it: zero, except
+// for an empty sequence, whose conv_state_out is its conv_state_in.
+__global__ void conv_cache_grad_init_kernel(const int32_t* __restrict__ cu, int N, int C,
+                                            const float* __restrict__ dcso, float* __restrict__ dcs) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)N * C) return;
+    const int n = (int)(idx / C);
+    const bool empty = cu[n + 1] == cu[n];
+#pragma unroll
+    for (int m = 0; m < kConvK - 1; m++)
+        dcs[idx * (kConvK - 1) + m] = empty && dcso != nullptr ? dcso[idx * (kConvK - 1) + m] : 0.f;
 }
 
 // One warp per run of tokens (walked backwards), lane = 4 channels.
@@ -256,8 +322,9 @@ template <class T>
 __global__ void __launch_bounds__(kConvWarps * 32, 2)
 conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* cs_in,
                 const float* __restrict__ dqkv, const int32_t* __restrict__ cu, int N,
-                int64_t Ttot, int C, int hk, float l2_eps, float q_scale, T* __restrict__ dx,
-                float* __restrict__ wpart, float* dcs) {
+                int64_t Ttot, int C, int hk, int G, bool group_major, float l2_eps,
+                float q_scale, T* __restrict__ dx, float* __restrict__ wpart, float* dcs,
+                const float* __restrict__ dcso) {
     extern __shared__ __align__(16) unsigned char conv_smem[];
     constexpr int kThr = kConvWarps * 32;
     float4* dq_ring = reinterpret_cast<float4*>(conv_smem);                   // [ring][4][kThr]
@@ -265,9 +332,11 @@ conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
     auto red = reinterpret_cast<float (*)[kD][kConvK]>(conv_smem);            // [warp][kD][kConvK]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int grp = blockIdx.y;
-    const int c = grp * kD + lane * 4;
-    const bool norm = grp < 2 * hk;
-    const float scale = grp < hk ? q_scale : 1.f;
+    const int c = grp * kD + lane * 4;   // channel of x, conv_w, dx, the cache
+    const ConvBlock cb = conv_block(grp, hk, G, group_major);
+    const int oc = cb.out * kD + lane * 4;   // channel of dqkv
+    const bool norm = cb.role < 2;
+    const float scale = cb.role == 0 ? q_scale : 1.f;
     float wr[4][kConvK];
 #pragma unroll
     for (int ch = 0; ch < 4; ch++)
@@ -286,9 +355,9 @@ conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
         int64_t s = cu[n], e = cu[n + 1];
         const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
         // window of dpre at t+1, t+2, t+3 (zero past the sequence end)
-        float4 d1 = (t1 < e) ? conv_dpre(x, cs_in, dqkv, t1, s, n, C, c, wr, norm, scale, l2_eps) : z4;
-        float4 d2 = (t1 + 1 < e) ? conv_dpre(x, cs_in, dqkv, t1 + 1, s, n, C, c, wr, norm, scale, l2_eps) : z4;
-        float4 d3 = (t1 + 2 < e) ? conv_dpre(x, cs_in, dqkv, t1 + 2, s, n, C, c, wr, norm, scale, l2_eps) : z4;
+        float4 d1 = (t1 < e) ? conv_dpre(x, cs_in, dqkv, t1, s, n, C, c, oc, wr, norm, scale, l2_eps) : z4;
+        float4 d2 = (t1 + 1 < e) ? conv_dpre(x, cs_in, dqkv, t1 + 1, s, n, C, c, oc, wr, norm, scale, l2_eps) : z4;
+        float4 d3 = (t1 + 2 < e) ? conv_dpre(x, cs_in, dqkv, t1 + 2, s, n, C, c, oc, wr, norm, scale, l2_eps) : z4;
         if (s <= t0 && (t1 - t0) % 4 == 0) {
             // the whole run lies in one sequence: four tokens per step, whose
             // dpre chains are independent.  Step i covers tokens tb..tb-3
@@ -305,7 +374,7 @@ conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
                     const int64_t tb = t1 - 1 - 4 * (int64_t)i;
 #pragma unroll
                     for (int u = 0; u < 4; u++)
-                        cp_async16(&dq_ring[(slot * 4 + u) * kThr + tid], dqkv + (tb - u) * C + c, true);
+                        cp_async16(&dq_ring[(slot * 4 + u) * kThr + tid], dqkv + (tb - u) * C + oc, true);
 #pragma unroll
                     for (int k = 0; k < 4; k++)
                         if (tb - 6 + k >= s)
@@ -343,21 +412,13 @@ conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
                     o.y = wr[1][3] * d0.y + wr[1][2] * d1.y + wr[1][1] * d2.y + wr[1][0] * d3.y;
                     o.z = wr[2][3] * d0.z + wr[2][2] * d1.z + wr[2][1] * d2.z + wr[2][0] * d3.z;
                     o.w = wr[3][3] * d0.w + wr[3][2] * d1.w + wr[3][1] * d2.w + wr[3][0] * d3.w;
+                    add_state_out_grad(o, dcso, n, C, c, t, e);
                     st4(dx + t * C + c, o);
 #pragma unroll
                     for (int j = 0; j < kConvK; j++)
 #pragma unroll
                         for (int ch = 0; ch < 4; ch++) dw[ch][j] += f4(d0, ch) * f4(xr[3 - u + j], ch);
-                    if (t == s && dcs != nullptr) {
-#pragma unroll
-                        for (int ch = 0; ch < 4; ch++) {
-                            float* o3 = dcs + ((int64_t)n * C + c + ch) * (kConvK - 1);
-                            o3[0] = wr[ch][0] * f4(d0, ch);
-                            o3[1] = wr[ch][0] * f4(d1, ch) + wr[ch][1] * f4(d0, ch);
-                            o3[2] = wr[ch][0] * f4(d2, ch) + wr[ch][1] * f4(d1, ch) +
-                                    wr[ch][2] * f4(d0, ch);
-                        }
-                    }
+                    if (t == s && dcs != nullptr) conv_cache_grad(dcs, dcso, n, C, c, e - s, wr, d0, d1, d2);
                     d3 = d2; d2 = d1; d1 = d0;
                 }
                 xr[4] = xr[0]; xr[5] = xr[1]; xr[6] = xr[2];
@@ -370,7 +431,7 @@ conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
             float4 xw1 = conv_in(x, cs_in, t1 - 2, s, n, C, c);
             float4 xw2 = conv_in(x, cs_in, t1 - 3, s, n, C, c);
             float4 xw3 = conv_in(x, cs_in, t1 - 4, s, n, C, c);
-            float4 g = ld4(dqkv + (t1 - 1) * C + c);
+            float4 g = ld4(dqkv + (t1 - 1) * C + oc);
             for (int64_t t = t1 - 1; t >= t0; t--) {
                 if (t < s) {  // crossed into the previous (non-empty) sequence
                     while (cu[n] > t) n--;
@@ -383,29 +444,21 @@ conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
                     xw3 = conv_in(x, cs_in, t - 3, s, n, C, c);
                 }
                 const float4 xn = conv_in(x, cs_in, t - 4, s, n, C, c);   // for step t - 1
-                const float4 gn = t > t0 ? ld4(dqkv + (t - 1) * C + c) : z4;
+                const float4 gn = t > t0 ? ld4(dqkv + (t - 1) * C + oc) : z4;
                 const float4 d0 = conv_dpre_w(xw0, xw1, xw2, xw3, g, wr, norm, scale, l2_eps);
                 float4 o;
                 o.x = wr[0][3] * d0.x + wr[0][2] * d1.x + wr[0][1] * d2.x + wr[0][0] * d3.x;
                 o.y = wr[1][3] * d0.y + wr[1][2] * d1.y + wr[1][1] * d2.y + wr[1][0] * d3.y;
                 o.z = wr[2][3] * d0.z + wr[2][2] * d1.z + wr[2][1] * d2.z + wr[2][0] * d3.z;
                 o.w = wr[3][3] * d0.w + wr[3][2] * d1.w + wr[3][1] * d2.w + wr[3][0] * d3.w;
+                add_state_out_grad(o, dcso, n, C, c, t, e);
                 st4(dx + t * C + c, o);
                 const float4 xin[kConvK] = {xw3, xw2, xw1, xw0};   // x[t - 3 + j]
     #pragma unroll
                 for (int j = 0; j < kConvK; j++)
     #pragma unroll
                     for (int ch = 0; ch < 4; ch++) dw[ch][j] += f4(d0, ch) * f4(xin[j], ch);
-                if (t == s && dcs != nullptr) {
-                    // gradient of the conv cache: position s-3+m feeds tokens s..s+m
-    #pragma unroll
-                    for (int ch = 0; ch < 4; ch++) {
-                        float* o3 = dcs + ((int64_t)n * C + c + ch) * (kConvK - 1);
-                        o3[0] = wr[ch][0] * f4(d0, ch);
-                        o3[1] = wr[ch][0] * f4(d1, ch) + wr[ch][1] * f4(d0, ch);
-                        o3[2] = wr[ch][0] * f4(d2, ch) + wr[ch][1] * f4(d1, ch) + wr[ch][2] * f4(d0, ch);
-                    }
-                }
+                if (t == s && dcs != nullptr) conv_cache_grad(dcs, dcso, n, C, c, e - s, wr, d0, d1, d2);
                 d3 = d2; d2 = d1; d1 = d0;
                 xw0 = xw1; xw1 = xw2; xw2 = xw3; xw3 = xn;
                 g = gn;
@@ -441,16 +494,12 @@ cudaError_t launch_conv_fwd_t(const ConvArgs& a, cudaStream_t st) {
     if (a.T > 0) {
         dim3 grid((unsigned)((a.T + kConvWarps * kConvRun - 1) / (kConvWarps * kConvRun)),
                   (unsigned)(a.C / kD));
-        static bool attr = false;
-        if (!attr) {
-            cudaFuncSetAttribute(conv_fwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)conv_fwd_smem<T>());
-            attr = true;
-        }
+        const cudaError_t e = smem_attr(conv_fwd_kernel<T>, conv_fwd_smem<T>());
+        if (e != cudaSuccess) return e;
         GDN_PROF("conv_fwd", st);
         conv_fwd_kernel<T><<<grid, kConvWarps * 32, conv_fwd_smem<T>(), st>>>(
-            (const T*)a.x, a.w, (const T*)a.cs_in, a.cu, a.N, a.T, a.C, a.hk, a.l2_eps,
-            a.q_scale, a.round_tf32, a.qkv);
+            (const T*)a.x, a.w, (const T*)a.cs_in, a.cu, a.N, a.T, a.C, a.hk, a.hv / a.hk,
+            a.group_major, a.l2_eps, a.q_scale, a.round_tf32, a.qkv);
     }
     if (a.cs_out != nullptr && a.N > 0) {
         int64_t n = (int64_t)a.N * a.C;
@@ -472,24 +521,25 @@ int conv_bwd_parts(int64_t T) {
 template <class T>
 cudaError_t launch_conv_bwd_t(const ConvArgs& a, cudaStream_t st) {
     int parts = conv_bwd_parts(a.T);
-    if (a.dcs != nullptr && a.N > 0)
-        cudaMemsetAsync(a.dcs, 0, sizeof(float) * (size_t)a.N * a.C * (kConvK - 1), st);
+    if (a.dcs != nullptr && a.N > 0) {
+        const int64_t n = (int64_t)a.N * a.C;
+        GDN_PROF("conv_cache_grad_init", st);
+        conv_cache_grad_init_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a.cu, a.N, a.C,
+                                                                                 a.dcs_out, a.dcs);
+    }
     if (parts > 0) {
         dim3 grid((unsigned)parts, (unsigned)(a.C / kD));
         static_assert(conv_bwd_smem<float>() >= sizeof(float) * kConvWarps * kD * kConvK &&
                           conv_bwd_smem<__nv_bfloat16>() >= sizeof(float) * kConvWarps * kD * kConvK,
                       "the ring holds the dw reduction");
-        static bool attr = false;
-        if (!attr) {
-            cudaFuncSetAttribute(conv_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)conv_bwd_smem<T>());
-            attr = true;
-        }
+        const cudaError_t e = smem_attr(conv_bwd_kernel<T>, conv_bwd_smem<T>());
+        if (e != cudaSuccess) return e;
         {
             GDN_PROF("conv_bwd", st);
             conv_bwd_kernel<T><<<grid, kConvWarps * 32, conv_bwd_smem<T>(), st>>>(
                 (const T*)a.x, a.w, (const T*)a.cs_in, a.dqkv, a.cu, a.N, a.T, a.C, a.hk,
-                a.l2_eps, a.q_scale, (T*)a.dx, a.wpart, a.dcs);
+                a.hv / a.hk, a.group_major, a.l2_eps, a.q_scale, (T*)a.dx, a.wpart, a.dcs,
+                a.dcs_out);
         }
         {
             GDN_PROF("conv_dw_reduce", st);

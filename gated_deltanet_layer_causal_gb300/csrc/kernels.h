@@ -10,9 +10,20 @@ namespace gdn {
 
 struct ChunkInfo;
 
+// Raise a kernel's dynamic shared-memory limit on the current device.  The
+// attribute belongs to the device's context, so it is set before every launch
+// that needs more than 48 KB (a host-only call of about a microsecond): right
+// on every device a process drives, after a context is rebuilt, and from any
+// host thread.
+template <class K>
+inline cudaError_t smem_attr(K* kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
 struct ConvArgs {
     bool bf16;
-    int N, C, hk;
+    bool group_major;      // channel layout of x, conv_w, the conv cache and dx
+    int N, C, hk, hv;
     int64_t T;
     const int32_t* cu;
     const void* x;
@@ -28,7 +39,8 @@ struct ConvArgs {
     void* dx;
     float* dw;
     float* wpart;   // [conv_bwd_parts(T), C, 4] scratch
-    float* dcs;
+    float* dcs;             // gradient of cs_in [N, C, 3] (nullable)
+    const float* dcs_out;   // gradient of cs_out [N, C, 3] (nullable)
 };
 cudaError_t launch_conv_fwd(const ConvArgs& a, cudaStream_t st);
 cudaError_t launch_conv_bwd(const ConvArgs& a, cudaStream_t st);
@@ -81,6 +93,7 @@ struct ChunkArgs {
     const void* z;
     const float* norm_w;
     float norm_eps;
+    int gate;              // output gate of the fused norm: kGateSilu / kGateSigmoid
     // forward outputs
     void* o_out;
     void* y_out;
@@ -120,6 +133,7 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a, const BwdScratch& w, cudaStream
 
 struct NormArgs {
     bool bf16;
+    int gate;       // kGateSilu / kGateSigmoid
     int64_t rows;   // T * Hv
     const void *o, *z;
     const float* w;
@@ -139,6 +153,8 @@ int norm_bwd_noalloc_max_rows();
 
 struct StepArgs {
     bool bf16;
+    int gate;              // kGateSilu / kGateSigmoid
+    bool group_major;      // channel layout of x, conv_w and the conv cache
     int N, hk, hv, C;
     const void* x;
     const float* w;

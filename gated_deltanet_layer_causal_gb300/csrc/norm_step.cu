@@ -2,9 +2,9 @@
 // single-token decode step.
 //
 // Norm: prime-rl #3860 "Summary" (ZeroCenteredRMSNorm shared by the GDN
-// layers), "[main] feat(moe): Support gated delta net for Qwen3-Next (1/4)"
-// (--apply-layernorm-1p): y = o rsqrt(mean(o^2) + eps) (1 + w) silu(z) per
-// (token, v-head) over d_v = 128.  HBM-bound: one warp per row, 4 columns per
+// layers; the output gate silu or sigmoid), "[main] feat(moe): Support gated
+// delta net for Qwen3-Next (1/4)" (--apply-layernorm-1p): y = o rsqrt(mean(o^2)
+// + eps) (1 + w) gate(z) per (token, v-head) over d_v = 128.  HBM-bound: one warp per row, 4 columns per
 // lane, warp-shuffle reductions; the weight gradient is summed per CTA and then
 // across CTAs in a fixed order (bitwise reproducible).
 //
@@ -12,8 +12,11 @@
 // sequences -- conv-cache update, conv + SiLU, L2 norms, gates, the rank-1
 // state update S <- e^g S + beta (v - e^g S k) k^T, o = S q, and the norm.
 // HBM-bound on the fp32 state, which is read once and written once.
+#include <cuda.h>
+
 #include <mutex>
 
+#include "../../include/gdn.h"
 #include "common.cuh"
 #include "kernels.h"
 #include "prof.h"
@@ -26,20 +29,16 @@ constexpr int kNormRowsPerCta = 64;
 template <class IO>
 __global__ void __launch_bounds__(kNormWarps * 32)
 norm_fwd_kernel(const IO* __restrict__ o, const IO* __restrict__ z, const float* __restrict__ w,
-                float eps, int64_t rows, IO* __restrict__ y, float* rstd) {
+                float eps, int gate, int64_t rows, IO* __restrict__ y, float* rstd) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float4 w4 = ld4(w + lane * 4);
     for (int64_t r = (int64_t)blockIdx.x * kNormWarps + warp; r < rows;
          r += (int64_t)gridDim.x * kNormWarps) {
         const int64_t off = r * kD + lane * 4;
-        float4 o4 = ld4(o + off), z4 = ld4(z + off), y4;
+        float4 o4 = ld4(o + off), z4 = ld4(z + off);
         float ss = warp_sum(o4.x * o4.x + o4.y * o4.y + o4.z * o4.z + o4.w * o4.w);
         float rs = rsqrtf(ss * (1.f / kD) + eps);
-        y4.x = o4.x * rs * (1.f + w4.x) * siluf_(z4.x);
-        y4.y = o4.y * rs * (1.f + w4.y) * siluf_(z4.y);
-        y4.z = o4.z * rs * (1.f + w4.z) * siluf_(z4.z);
-        y4.w = o4.w * rs * (1.f + w4.w) * siluf_(z4.w);
-        st4(y + off, y4);
+        st4(y + off, gated_norm4(o4, rs, w4, z4, gate));
         if (rstd && lane == 0) rstd[r] = rs;
     }
 }
@@ -47,8 +46,8 @@ norm_fwd_kernel(const IO* __restrict__ o, const IO* __restrict__ z, const float*
 template <class IO>
 __global__ void __launch_bounds__(kNormWarps * 32)
 norm_bwd_kernel(const IO* __restrict__ o, const IO* __restrict__ z, const float* __restrict__ w,
-                const IO* __restrict__ dy, float eps, int64_t rows, IO* __restrict__ d_o,
-                IO* __restrict__ dz, float* __restrict__ part) {
+                const IO* __restrict__ dy, float eps, int gate, int64_t rows,
+                IO* __restrict__ d_o, IO* __restrict__ dz, float* __restrict__ part) {
     __shared__ float4 red[kNormWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float4 w4 = ld4(w + lane * 4);
@@ -57,7 +56,8 @@ norm_bwd_kernel(const IO* __restrict__ o, const IO* __restrict__ z, const float*
     const int64_t r1 = min(r0 + kNormRowsPerCta, rows);
     for (int64_t r = r0 + warp; r < r1; r += kNormWarps) {
         const int64_t off = r * kD + lane * 4;
-        NormRowGrad gr = norm_row_bwd(ld4(o + off), ld4(z + off), ld4(dy + off), w4, eps, acc);
+        NormRowGrad gr =
+            norm_row_bwd(ld4(o + off), ld4(z + off), ld4(dy + off), w4, eps, acc, gate);
         st4(d_o + off, gr.d_o);
         st4(dz + off, gr.dz);
     }
@@ -92,7 +92,7 @@ static cudaError_t norm_fwd_t(const NormArgs& a, cudaStream_t st) {
     if (blocks > 152 * 16) blocks = 152 * 16;
     GDN_PROF("norm_fwd", st);
     norm_fwd_kernel<IO><<<(unsigned)blocks, kNormWarps * 32, 0, st>>>(
-        (const IO*)a.o, (const IO*)a.z, a.w, a.eps, a.rows, (IO*)a.y, a.rstd);
+        (const IO*)a.o, (const IO*)a.z, a.w, a.eps, a.gate, a.rows, (IO*)a.y, a.rstd);
     return cudaGetLastError();
 }
 cudaError_t launch_norm_fwd(const NormArgs& a, cudaStream_t st) {
@@ -109,8 +109,8 @@ static cudaError_t norm_bwd_t(const NormArgs& a, cudaStream_t st) {
     {
         GDN_PROF("norm_bwd", st);
         norm_bwd_kernel<IO><<<parts, kNormWarps * 32, 0, st>>>(
-            (const IO*)a.o, (const IO*)a.z, a.w, (const IO*)a.dy, a.eps, a.rows, (IO*)a.d_o,
-            (IO*)a.dz, a.part);
+            (const IO*)a.o, (const IO*)a.z, a.w, (const IO*)a.dy, a.eps, a.gate, a.rows,
+            (IO*)a.d_o, (IO*)a.dz, a.part);
     }
     {
         GDN_PROF("norm_w_reduce", st);
@@ -130,30 +130,85 @@ cudaError_t launch_norm_bwd(const NormArgs& a, cudaStream_t st) {
 constexpr int kNoAllocParts = 8192;
 static __device__ __align__(256) float g_norm_bwd_scratch[kNoAllocParts * kD];
 
+static_assert(kNoAllocParts * kNormRowsPerCta == GDN_NOALLOC_NORM_BWD_MAX_ROWS,
+              "the header's row limit is the array's capacity");
 int norm_bwd_noalloc_max_rows() { return kNoAllocParts * kNormRowsPerCta; }
 
 namespace {
 constexpr int kMaxDevices = 64;
+
+// The array's device address belongs to the CUDA context that loaded this
+// module: after a context is destroyed and rebuilt (cudaDeviceReset, or the
+// primary context released and retained again) the module is loaded afresh
+// and the array may sit elsewhere.  So the cached address is keyed on the
+// context's process-unique ID, read through the driver entry points (looked
+// up once through the runtime; the library links no driver library).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+struct CtxQuery {
+    CtxGetCurrentFn get_current = nullptr;
+    CtxGetIdFn get_id = nullptr;
+};
+const CtxQuery& ctx_query() {
+    static const CtxQuery q = [] {
+        CtxQuery r;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult st;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &st) == cudaSuccess &&
+            st == cudaDriverEntryPointSuccess)
+            r.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &st) ==
+                cudaSuccess &&
+            st == cudaDriverEntryPointSuccess)
+            r.get_id = reinterpret_cast<CtxGetIdFn>(p);
+        return r;
+    }();
+    return q;
+}
+// ID of the calling thread's current context; false if there is none or the
+// driver cannot tell.
+bool current_ctx_id(unsigned long long* id) {
+    const CtxQuery& q = ctx_query();
+    CUcontext ctx = nullptr;
+    if (q.get_current == nullptr || q.get_id == nullptr) return false;
+    if (q.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return q.get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+struct ScratchAddr {
+    unsigned long long ctx_id = 0;
+    bool valid = false;
+    float* addr = nullptr;
+};
 std::mutex g_scratch_mu;
-float* g_scratch_dev[kMaxDevices] = {};   // device address of the array, per device
+ScratchAddr g_scratch_dev[kMaxDevices];   // per device: the context it was read in
 }  // namespace
 
-// Device address of g_norm_bwd_scratch on the current device.  Host code only
-// sees a host-side stand-in for the array, so the address is looked up once
-// per device (on its first use, with that device current) and cached.
+// Device address of g_norm_bwd_scratch in the current device's context.  Host
+// code only sees a host-side stand-in for the array, so the address is looked
+// up (cudaGetSymbolAddress, with that device current) the first time a context
+// uses it and cached under the context's ID; a rebuilt context looks it up
+// again.  Without the driver's context query it is looked up on every call.
 static cudaError_t norm_bwd_noalloc_scratch(float** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (g_scratch_dev[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_norm_bwd_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_dev[dev] = static_cast<float*>(p);
+    ScratchAddr& slot = g_scratch_dev[dev];
+    unsigned long long id = 0;
+    if (slot.valid && current_ctx_id(&id) && id == slot.ctx_id) {
+        *out = slot.addr;
+        return cudaSuccess;
     }
-    *out = g_scratch_dev[dev];
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_norm_bwd_scratch);   // makes the context current if needed
+    if (e != cudaSuccess) return e;
+    slot.valid = current_ctx_id(&id);
+    slot.ctx_id = id;
+    slot.addr = static_cast<float*>(p);
+    *out = slot.addr;
     return cudaSuccess;
 }
 
@@ -179,15 +234,19 @@ step_kernel(const IO* __restrict__ x, const float* __restrict__ w, IO* cs,
             const IO* __restrict__ av, const IO* __restrict__ bv, const float* __restrict__ A_log,
             const float* __restrict__ dt_bias, const IO* __restrict__ z,
             const float* __restrict__ norm_w, float* __restrict__ S, IO* o_out, IO* y_out,
-            int hk, int hv, float l2_eps, float q_scale, float norm_eps) {
+            int hk, int hv, float l2_eps, float q_scale, float norm_eps, int gate,
+            bool group_major) {
     __shared__ float q[kD], k[kD], v[kMaxGroup][kD], o[kMaxGroup][kD];
     __shared__ float gdec[kMaxGroup], gbeta[kMaxGroup];
     const int kh = blockIdx.x, n = blockIdx.y, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int G = hv / hk, C = (2 * hk + hv) * kD;
-    // conv + SiLU over this CTA's (2 + G) * 128 channels; cache shifts left
+    // conv + SiLU over this CTA's (2 + G) * 128 channels; cache shifts left.
+    // Channel of x / conv_w / the cache: flat [q | k | v], or group-major (the
+    // group's q, k and v heads contiguous), which is this loop's own order.
     for (int i = tid; i < (2 + G) * kD; i += 256) {
-        int c = i < kD ? kh * kD + i
+        int c = group_major ? kh * (2 + G) * kD + i
+              : i < kD ? kh * kD + i
               : i < 2 * kD ? hk * kD + kh * kD + (i - kD)
                            : 2 * hk * kD + kh * G * kD + (i - 2 * kD);
         IO* cc = cs + ((int64_t)n * C + c) * (kConvK - 1);
@@ -246,12 +305,7 @@ step_kernel(const IO* __restrict__ x, const float* __restrict__ w, IO* cs,
         if (o_out) st4(o_out + off, o4);
         float ss = warp_sum(o4.x * o4.x + o4.y * o4.y + o4.z * o4.z + o4.w * o4.w);
         float rs = rsqrtf(ss * (1.f / kD) + norm_eps);
-        float4 z4 = ld4(z + off), y4;
-        y4.x = o4.x * rs * (1.f + w4.x) * siluf_(z4.x);
-        y4.y = o4.y * rs * (1.f + w4.y) * siluf_(z4.y);
-        y4.z = o4.z * rs * (1.f + w4.z) * siluf_(z4.z);
-        y4.w = o4.w * rs * (1.f + w4.w) * siluf_(z4.w);
-        st4(y_out + off, y4);
+        st4(y_out + off, gated_norm4(o4, rs, w4, ld4(z + off), gate));
     }
 }
 
@@ -262,7 +316,7 @@ static cudaError_t step_t(const StepArgs& a, cudaStream_t st) {
     step_kernel<IO><<<dim3(a.hk, a.N), 256, 0, st>>>(
         (const IO*)a.x, a.w, (IO*)a.cs, (const IO*)a.a, (const IO*)a.b, a.A_log, a.dt_bias,
         (const IO*)a.z, a.norm_w, a.S, (IO*)a.o, (IO*)a.y, a.hk, a.hv, a.l2_eps, a.q_scale,
-        a.norm_eps);
+        a.norm_eps, a.gate, a.group_major);
     return cudaGetLastError();
 }
 cudaError_t launch_step(const StepArgs& a, cudaStream_t st) {

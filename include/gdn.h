@@ -28,16 +28,25 @@
  *   gates: g = -exp(A_log[h]) softplus(a + dt_bias[h]),  beta = sigmoid(b) [P3]
  *   rule:  S_t = exp(g_t) S_{t-1} (I - beta_t k^_t k^_t^T) + beta_t v_t k^_t^T,
  *          o_t = S_t q^_t,  S in fp32 [d_v x d_k]
- *   norm:  y = o / sqrt(mean(o^2) + norm_eps) * (1 + w) * silu(z)   [P2][P3]
+ *   norm:  y = o / sqrt(mean(o^2) + norm_eps) * (1 + w) * gate(z),
+ *          gate = silu (default) or sigmoid (dims.gate)          [P2][P3]
  *
  * Layouts (row-major, packed over tokens; T = total tokens, N = sequences,
- * C = 2*h_k*d_k + h_v*d_v conv channels):
- *   x, dx          [T, C]  io dtype, channels [q (h_k*d_k) | k (h_k*d_k) | v]
- *   qkv, dqkv      [T, C]  fp32, same channel order (conv+SiLU+L2 output)
+ * C = 2*h_k*d_k + h_v*d_v conv channels, G = h_v/h_k):
+ *   x, dx          [T, C]  io dtype; channels flat [q (h_k*d_k) | k (h_k*d_k) |
+ *                  v (h_v*d_v)] (dims.layout = GDN_LAYOUT_FLAT, [P1] "What":
+ *                  HF's flat layout) or group-major: for each k-head kh in
+ *                  order, [q_kh | k_kh | v_{kh*G} .. v_{kh*G+G-1}], d channels
+ *                  each (GDN_LAYOUT_GROUP, [P1] "What": q/k/v and the conv in
+ *                  group-major layout).  conv_w, conv_state and their
+ *                  gradients follow x's channel order.
+ *   qkv, dqkv      [T, C]  fp32, always the flat order (conv+SiLU+L2 output,
+ *                  an intermediate between the conv and the chunk entry points)
  *   a, b, da, db   [T, h_v] io dtype
  *   z, o, y, dz    [T, h_v, d_v] io dtype
  *   conv_w         [C, 4] fp32; tap 3 multiplies the current token
  *   conv_state     [N, C, 3] io dtype; [..., m] = input at position start-3+m
+ *                  (gradients of conv states: fp32)
  *   A_log, dt_bias [h_v] fp32;  norm_w [d_v] fp32 (shared by all heads)
  *   states         [N, h_v, d_v, d_k] fp32
  *   cu_seqlens     int32 [N+1], cu[0] = 0, non-decreasing, cu[N] = T.  Entry
@@ -81,7 +90,16 @@ typedef struct {
     float l2_eps;          /* eps inside the q/k L2 norm (1e-6 typical)      */
     float norm_eps;        /* eps inside the gated RMSNorm (1e-6 typical)    */
     int32_t qkv_tf32;      /* 0 or 1, see below                               */
+    int32_t gate;          /* gdn_gate: output gate of the gated norm         */
+    int32_t layout;        /* gdn_layout: q/k/v channel order of x            */
 } gdn_dims;
+
+/* Output gate of the zero-centred gated RMSNorm ([P2] "Summary": the shared
+ * GatedDeltaNet takes output_gate_type; Qwen3.5 uses silu, Qwen3.8 sigmoid). */
+typedef enum { GDN_GATE_SILU = 0, GDN_GATE_SIGMOID = 1 } gdn_gate;
+
+/* Channel order of x / dx / conv_w / conv states (see Layouts above). */
+typedef enum { GDN_LAYOUT_FLAT = 0, GDN_LAYOUT_GROUP = 1 } gdn_layout;
 
 /* qkv_tf32 = 1: the conv output qkv carries tf32 values (fp32 storage, 10
  * fraction bits).  gdn_conv1d_silu then rounds its output to nearest tf32, and
@@ -118,15 +136,19 @@ gdn_status gdn_conv1d_silu(const gdn_dims* dims, const int32_t* cu_seqlens,
                            const void* conv_state_in, float* qkv_out, void* conv_state_out,
                            void* stream);
 
-/* Backward of gdn_conv1d_silu: given dqkv [T, C] fp32 (gradient of its output)
- * writes dx [T, C] (io dtype), dconv_w [C, 4] fp32 and, if not NULL, the
- * gradient of conv_state_in [N, C, 3] fp32.  The conv-state output is not
- * differentiated.  Recomputes the conv from x.  Scratch: GDN_WS_CONV_BWD. */
+/* Backward of gdn_conv1d_silu: given dqkv [T, C] fp32 (gradient of its qkv
+ * output) and, if not NULL, dconv_state_out_grad [N, C, 3] fp32 (gradient of
+ * its conv_state_out: a sequence split across calls hands the gradient of the
+ * next call's conv_state_in back here), writes dx [T, C] (io dtype), dconv_w
+ * [C, 4] fp32 and, if not NULL, dconv_state_in_out [N, C, 3] fp32, the
+ * gradient of conv_state_in.  Recomputes the conv from x.  Scratch:
+ * GDN_WS_CONV_BWD. */
 gdn_status gdn_conv1d_silu_bwd(const gdn_dims* dims, const int32_t* cu_seqlens,
                                const int32_t* cu_seqlens_host, const void* x,
                                const float* conv_w, const void* conv_state_in, const float* dqkv,
-                               void* dx_out, float* dconv_w_out, float* dconv_state_out,
-                               void* ws, size_t ws_bytes, void* stream);
+                               const float* dconv_state_out_grad, void* dx_out,
+                               float* dconv_w_out, float* dconv_state_in_out, void* ws,
+                               size_t ws_bytes, void* stream);
 
 /* Gated delta rule over packed varlen sequences in the chunked WY form
  * (chunk 64), with the gates computed from a, b, A_log, dt_bias, grouped value
@@ -162,7 +184,7 @@ gdn_status gdn_chunk_bwd(const gdn_dims* dims, const int32_t* cu_seqlens,
                          size_t bwd_ws_bytes, void* stream);
 
 /* Zero-centred gated RMSNorm, standalone ([P2] ZeroCenteredRMSNorm, [P3]
- * --apply-layernorm-1p): y = o * rsqrt(mean(o^2) + eps) * (1 + w) * silu(z)
+ * --apply-layernorm-1p): y = o * rsqrt(mean(o^2) + eps) * (1 + w) * gate(z)
  * per (token, v-head) over d_v.  rstd_out [T, h_v] fp32 is nullable. */
 gdn_status gdn_gated_rmsnorm(const gdn_dims* dims, const void* o, const void* z,
                              const float* norm_w, void* y_out, float* rstd_out, void* stream);
@@ -185,9 +207,11 @@ gdn_status gdn_gated_rmsnorm_bwd(const gdn_dims* dims, const void* o, const void
  *  - Size limit: total_tokens * h_v <= GDN_NOALLOC_NORM_BWD_MAX_ROWS, else
  *    GDN_ERR_WORKSPACE with nothing launched.
  *  - It calls no cudaMalloc / cudaFree and no allocating routine.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *  - The first call in a device's CUDA context looks up the array's device
+ *    address (cudaGetSymbolAddress, with that device current) and caches it
+ *    under the context's unique ID; a context rebuilt later (cudaDeviceReset,
+ *    or the primary context released and retained again) looks it up anew.
+ *    Make that first call before any stream capture.
  *  - Every call on a device shares the one array: calls that overlap on the
  *    GPU (other streams, other host threads) race on it -- serialise them.
  *    The array keeps the last call's contents; every partial a call reads it
@@ -211,8 +235,25 @@ gdn_status gdn_recurrent_step(const gdn_dims* dims, const void* x_t, const float
 
 /* Reads the device status word at the start of a GDN_WS_FWD / GDN_WS_BWD /
  * GDN_WS_CONV_BWD workspace (0 = OK, else a gdn_status) and clears it.
- * Synchronises `stream`. */
+ * Synchronises `stream`.
+ * GDN_ERR_DEVICE_TIMEOUT means a kernel gave up a bounded wait (about 2^24
+ * polls) on a copy or a tensor-core product and returned early: that call's
+ * outputs are invalid, and because a copy it had requested may still have
+ * been in flight when it left, treat outputs of later launches on the same
+ * device as untrusted until the CUDA context has been rebuilt. */
 gdn_status gdn_read_status(void* ws, int32_t* code, void* stream);
+
+/* Self-test of that failure path, safe to run on a healthy GPU: one CTA
+ * allocates tensor memory, waits on an mbarrier with at most poll_limit polls
+ * (1 .. 2^24), frees the tensor memory and returns.  arrive = 0: nothing ever
+ * completes the barrier (no copy, product or arrive is pending on it), so the
+ * wait gives up and GDN_ERR_DEVICE_TIMEOUT lands in the status word at the
+ * start of `ws` (>= 4 bytes, 16-byte aligned; read it with gdn_read_status).
+ * arrive = 1: the CTA arrives on the barrier first, the wait succeeds and the
+ * status word is left as it was.  Nothing is in flight when the kernel
+ * returns, so, unlike a real timeout, the device stays trustworthy. */
+gdn_status gdn_selftest_bounded_wait(void* ws, size_t ws_bytes, int32_t poll_limit,
+                                     int32_t arrive, void* stream);
 
 /* Kernel launches the library has made in this process, over all entry points. */
 int64_t gdn_launch_count(void);
@@ -230,8 +271,10 @@ gdn_status gdn_profile_report(char* buf, size_t buf_bytes);
 const char* gdn_status_string(gdn_status status);
 
 /* ABI version of this header (major * 100 + minor); the major number changes
- * whenever a struct or a signature changes (2.00: gdn_dims.qkv_tf32). */
-#define GDN_ABI_VERSION 200
+ * whenever a struct or a signature changes (2.00: gdn_dims.qkv_tf32; 3.00:
+ * gdn_dims.gate and .layout, the conv backward's dconv_state_out_grad), the
+ * minor number when an entry point is added. */
+#define GDN_ABI_VERSION 300
 int32_t gdn_abi_version(void);
 
 #ifdef __cplusplus

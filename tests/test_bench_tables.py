@@ -1,7 +1,9 @@
-"""bench.py's stored DRAM traffic (one ncu capture of the first 8192 tokens,
-times 8) names kernels its algorithmic-byte model knows, and each figure is a
-plausible multiple of that kernel's algorithmic bytes: a stale, mistyped or
-mis-scaled entry fails here.  CPU only."""
+"""bench.py's cost tables.  The stored DRAM traffic (one ncu capture of the
+first 8192 tokens, times 8) names kernels its interface-byte model knows, and
+each figure is a plausible multiple of that kernel's interface bytes: a stale,
+mistyped or mis-scaled entry fails here.  The path-level algorithmic cost is
+the 123.5 kB and about 1.7 TFLOP per 64k step of the method's accounting, and
+every chunk kernel has a tensor-pipe FLOP count.  CPU only."""
 import bench
 from gated_deltanet_layer_causal_gb300 import synth
 
@@ -27,3 +29,23 @@ def test_every_chunk_kernel_has_a_cost():
                  "chunk_norm_bwd", "chunk_bwd_local", "chunk_bwd_state", "chunk_bwd_dp",
                  "chunk_bwd_sfacing", "chunk_bwd_wy", "gva_sum", "conv_bwd"):
         assert bench.kernel_cost(name, W, NT)[1] > 0, name
+
+
+def test_path_cost_is_the_method_accounting():
+    b, f = bench.path_cost(W)
+    assert b == W.T * 123456          # 45.2 kB forward + 78.2 kB backward per token
+    assert 1.6e12 < f < 1.8e12        # ~1.7 TFLOP of products per 64k fwd+bwd step
+    fw = synth.WORKLOADS["qwen35_9b_16k"]
+    b1, _ = bench.path_cost(fw)
+    assert b1 == fw.T * 2 * (fw.C + 2 * fw.h_v + 2 * fw.h_v * 128)   # x, a, b, z in; y out
+
+
+def test_chunk_kernels_have_tensor_flops():
+    total = 0
+    for name in bench.MMAS:
+        f = bench.kernel_flops(name, NT, W.h_v)
+        assert f and f % (NT * W.h_v) == 0, name
+        total += f
+    # every product of the chunked form, recomputed ones included (~1.9 TFLOP)
+    assert 1.8e12 < total < 2.0e12
+    assert bench.kernel_flops("conv_fwd", NT, W.h_v) is None

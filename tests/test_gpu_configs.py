@@ -1,10 +1,14 @@
 """The five workloads at full size, in the launch configuration bench.py uses
-(the same C-ABI calls).  The oracle checks whole k-head groups one by one: heads
-of different groups never interact, so a group's sub-problem (H_k = 1,
-H_v = G, its conv channels) is exactly the full problem restricted to it.
-Each forward workload also runs an extra dt_bias = -6 variant (not one of the
-five): at dt_bias = 0 the state forgets within a token or two, so only the
-variant exercises the state carried across chunks."""
+(the same C-ABI calls).  The Qwen3.5-9B-shaped 16k forward and the 64k
+forward + backward (the benchmark) are held to the oracle on the whole problem:
+every head, o, the final state and every gradient including dnorm_w.  The 128k
+workloads check whole k-head groups: heads of different groups never interact,
+so a group's sub-problem (H_k = 1, H_v = G, its conv channels) is exactly the
+full problem restricted to it.  Every comparison applies the norm-wise,
+max-relative and per-64-token-block measures of gdn_testutil.  Each workload
+also runs an extra dt_bias = -6 variant (not one of the five): at dt_bias = 0
+the state forgets within a token or two, so only the variant exercises the
+state carried across chunks."""
 import gc
 
 import numpy as np
@@ -13,7 +17,7 @@ import torch
 
 import oracle
 from gated_deltanet_layer_causal_gb300 import core, synth
-from gdn_testutil import TOL, TOL_STATE, f64, gpu_run, oracle_group, rel
+from gdn_testutil import (Checker, check_against, f64, full_args, gpu_run, oracle_groups)
 
 pytestmark = pytest.mark.gpu
 
@@ -23,31 +27,16 @@ def _free():
     torch.cuda.empty_cache()
 
 
-def _check_group(out, ref, ch, heads, backward):
-    fw = ref["fwd"] if backward else ref
-    errs = {"y": rel(f64(out["y"][:, heads]), fw["y"]),
-            "S_final": rel(f64(out["S"][:, heads]), fw["S_final"])}
-    if backward:
-        idx = torch.as_tensor(ch, device=out["dx"].device)
-        errs["dx"] = rel(f64(out["dx"].index_select(1, idx)), ref["dx"])
-        errs["dconv_w"] = rel(f64(out["dconv_w"][idx]), ref["dconv_w"])
-        errs["dz"] = rel(f64(out["dz"][:, heads]), ref["dz"])
-        errs["da"] = rel(f64(out["da"][:, heads]), ref["da"])
-        errs["db"] = rel(f64(out["db"][:, heads]), ref["db"])
-        errs["dA_log"] = rel(f64(out["dA_log"][heads]), ref["dA_log"])
-        errs["ddt_bias"] = rel(f64(out["ddt_bias"][heads]), ref["ddt_bias"])
-    print("\nerrors: " + ", ".join(f"{k}={v:.2e}" for k, v in errs.items()))
-    bad = {k: e for k, e in errs.items() if e > (TOL_STATE if k == "S_final" else TOL)}
-    assert not bad, f"{bad} (all: {errs})"
-    return errs
-
-
+# (workload, dt_bias, groups): "all" = the whole-problem oracle in one call;
+# "every" = every k-head group, one oracle call per group (the 64k backward's
+# fp64 intermediates for all heads at once would need ~75 GB of host memory),
+# with dnorm_w, a sum over all heads, checked as the sum of the groups' parts
 CASES = [
-    ("tiny_fp32", 0.0, None), ("tiny_fp32", -6.0, None),
-    ("qwen35_9b_16k", 0.0, (0, 15)), ("qwen35_9b_16k", -6.0, (7,)),
-    ("qwen38_flash_64k", 0.0, (0, 15)), ("qwen38_flash_64k", -6.0, (5,)),
-    ("varlen64_128k", 0.0, (0,)), ("varlen64_128k", -6.0, (11,)),
-    ("long_128k", 0.0, (0,)), ("long_128k", -6.0, (9,)),
+    ("tiny_fp32", 0.0, "all"), ("tiny_fp32", -6.0, "all"),
+    ("qwen35_9b_16k", 0.0, "all"), ("qwen35_9b_16k", -6.0, (7,)),
+    ("qwen38_flash_64k", 0.0, "every"), ("qwen38_flash_64k", -6.0, (5, 10)),
+    ("varlen64_128k", 0.0, (0, 8)), ("varlen64_128k", -6.0, (11,)),
+    ("long_128k", 0.0, (0, 15)), ("long_128k", -6.0, (9,)),
 ]
 
 
@@ -58,18 +47,24 @@ def test_workload(name, dtb, groups):
     inp = synth.make_inputs(w, with_grad=backward)
     out = gpu_run(inp, w, backward=backward)
     assert out["status_fwd"] == 0
-    if groups is None:   # whole problem
-        groups = tuple(range(w.h_k))
-    for kh in groups:
-        ref, ch, heads = oracle_group(inp, w, kh, backward)
-        _check_group(out, ref, ch, heads, backward)
-    if name == "tiny_fp32":   # o itself (the workload's stated output) and dnorm_w
-        full = oracle.backward(
-            **{k: synth.to_f64(inp[k]) for k in ("x", "conv_w", "a", "b", "A_log", "dt_bias",
-                                                   "z", "norm_w")},
-            cu=inp["cu_seqlens"].numpy(), hk=w.h_k, hv=w.h_v, dy=synth.to_f64(inp["dy"]))
-        assert rel(f64(out["o"]), full["fwd"]["o"]) <= TOL
-        assert rel(f64(out["dnorm_w"]), full["dnorm_w"]) <= TOL
+    tag = f"{name} dt_bias={dtb}"
+    if groups == "all":
+        args = full_args(inp, w)
+        ref = (oracle.backward(**args, dy=synth.to_f64(inp["dy"])) if backward
+               else oracle.forward(**args))
+        check_against(out, ref, backward, tag=tag)
+    else:
+        every = groups == "every"
+        groups = range(w.h_k) if every else groups
+        dnw = np.zeros(128)
+        for kh, ref, ch, heads in oracle_groups(inp, w, groups, backward):
+            check_against(out, ref, backward, ch, heads, tag=f"{tag} kh={kh}")
+            if backward:
+                dnw += ref["dnorm_w"]   # this group's heads' share of the sum
+        if every and backward:
+            c = Checker(f"{tag} all groups")
+            c.add("dnorm_w", f64(out["dnorm_w"]), dnw, blocks=False)
+            c.check()
     del out
     _free()
 
@@ -95,9 +90,11 @@ def test_decode_batch_256(dtb):
     ry, ro, rS, rcs = oracle.decode_step(f(inp["x"]), f(inp["conv_w"]), f(cs), f(inp["a"]),
                                          f(inp["b"]), f(inp["A_log"]), f(inp["dt_bias"]),
                                          f(inp["z"]), f(inp["norm_w"]), f(S), w.h_k, w.h_v)
-    assert rel(f64(y), ry) <= TOL
-    assert rel(f64(o), ro) <= TOL
-    assert rel(f64(Sd), rS) <= TOL_STATE
+    c = Checker(f"decode batch {N} dt_bias={dtb}")
+    c.add("y", f64(y), ry)
+    c.add("o", f64(o), ro)
+    c.add("S", f64(Sd), rS, state=True)
+    c.check()
     np.testing.assert_array_equal(f64(csd), rcs)
     del Sd, csd
     _free()
