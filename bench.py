@@ -257,8 +257,10 @@ TRAFFIC_64K = {
 # as (M, N, K) -- the per-unit figure of its tensor-pipe roofline:
 MMAS = {
     "chunk_prep": [(64, 64, 128), (64, 128, 64), (64, 128, 64)],        # K K^T, W, U~
-    "chunk_state_fwd": [(64, 128, 128), (128, 128, 64)],                # W S^T, K^T (fk U)
-    "chunk_out_fwd": [(64, 64, 128), (64, 128, 128), (64, 128, 64)],    # Q K^T, Q S0^T, P U
+    # per 64-row slice (2): the chain M^T S^T, B^T = (fk K)^T U~, -M^T = (fk K)^T W
+    "chunk_state_fwd": [(128, 64, 128), (128, 64, 64), (128, 128, 64)] * 2,
+    # Q K^T, Q S0^T, W S0^T (U = U~ - W S0^T), P U
+    "chunk_out_fwd": [(64, 64, 128), (64, 128, 128), (64, 128, 128), (64, 128, 64)],
     "chunk_bwd_local": [(64, 64, 128), (64, 128, 64)],                  # K Q^T, P^T dO
     "chunk_bwd_state": [(64, 64, 128), (64, 128, 64), (64, 128, 64)] * 2,   # 2 row slices
     "chunk_bwd_dp": [(64, 64, 128), (64, 64, 128), (64, 128, 64), (64, 128, 64)],
@@ -449,8 +451,7 @@ def run_ours(args, rank, world, dev):
             "config": {"workload": w.name, "tokens": w.T, "seqs": w.N, "h_k": w.h_k,
                        "h_v": w.h_v, "d_k": D, "d_v": D, "chunk": 64, "conv_k": 4,
                        "io": w.io, "state": "fp32",
-                       "mma": "tf32 operands, fp32 accumulation: tcgen05 (chunk kernels, "
-                              "reverse state pass), mma.sync (forward state pass)",
+                       "mma": "tf32 operands, fp32 accumulation, tcgen05 (every product)",
                        "qkv": "conv output stored at tf32 precision",
                        "passes": ("fwd+bwd" if w.backward else "fwd") +
                                  " (conv, chunk rule, fused gated norm)",

@@ -4,10 +4,11 @@
 // Per chunk (tokens i = 0..L-1, in-chunk cumulative gate gam_i):
 //   A_ij = beta_i exp(gam_i - gam_j) k_i.k_j (j < i);  T = (I + A)^-1
 //   W = T diag(beta e^gam) K ;  U~ = T diag(beta) V          (prep, parallel)
-//   U = U~ - W S0^T ;  S_end = e^{gam_L} S0 + U^T diag(e^{gam_L-gam}) K
-//                                                            (state, sequential)
+//   S_end = e^{gam_L} S0 + U^T diag(e^{gam_L-gam}) K,  U = U~ - W S0^T
+//         = e^{gam_L} S0 + S0 M + B                        (state, sequential)
+//   U = U~ - W S0^T ;
 //   O = diag(e^gam) Q S0^T + (Q K^T (.) exp(gam_i-gam_j) (.) [i>=j]) U
-//   y = O rsqrt(mean(O^2)+eps) (1+w) gate(z)                 (out, parallel)
+//   y = O rsqrt(mean(O^2)+eps) (1+w) gate(z)             (out, parallel)
 // which unrolls S_t = e^{g_t} S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
 // o_t = S_t q_t exactly.  Sources: "[6/8] feat(models): port Qwen3.5 / Qwen3-Next
 // GDN to the head-sharded layer" ("What": grouped value heads, native GVA);
@@ -15,8 +16,8 @@
 // output_final_state; ZeroCenteredRMSNorm); "[main] feat(moe): Support gated
 // delta net for Qwen3-Next (1/4)" (A_log review comment: decay rate exp(A_log)).
 //
-// All products run on the tensor cores (tf32 operands, fp32 accumulation); the
-// state stays fp32 in registers across the whole sequence.
+// All products run on the tcgen05 tensor cores (tf32 operands, fp32
+// accumulation); the state stays fp32 in registers across the whole sequence.
 #include "common.cuh"
 #include "kernels.h"
 #include "prof.h"
@@ -125,7 +126,7 @@ gates_kernel(const IO* __restrict__ av, const IO* __restrict__ bv, const float* 
 // staged over the A / T scratch, so the next tile's K and V are requested as
 // soon as the second products are done; its chunk entry and gates are loaded
 // into registers meanwhile.  Tensor memory allocated once.
-constexpr int kLdK = 132, kLdA = 68;
+constexpr int kLdA = 68;
 constexpr int kPrepFloats = 3 * 64 * 128 + 2 * 64 * kLdA + 2 * 64 * 64;
 constexpr size_t kPrepSmem = sizeof(float) * (kPrepFloats + 3 * 64 + 16) + 64 + 1024;
 
@@ -312,190 +313,295 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
 }
 
 // ------------------------------------------------------------------ state pass
-// grid (3, Hv, N), 256 threads, one CTA per SM.  Rows a of S evolve
-// independently (k, beta, g are shared by all rows), so each CTA carries a
-// slice of rows of the fp32 state -- kept transposed, S^T[b][a], in the MMA
-// accumulators -- through all chunks of its sequence: rows 0-47, 48-95 and
-// 96-127, so that 3 * Hv CTAs occupy most SMs.  The next chunk's W, K and U~
-// slice arrive through the TMA into the other half of a double buffer while
-// the current chunk is computed.  A tf32-rounded copy of the state slice, St,
-// is held in exactly the layout of its slice of the chunk-start state tile
-// (K-major rows a): it feeds the tensor cores without conversion and leaves as
-// one bulk copy per chunk.
-constexpr int kSliceMax = 48;
-struct StateStage {                // one chunk's operands (a multiple of 1 KB)
-    float W[64 * 128];             // swizzled, arrives rounded
-    float K[64 * 128];             // swizzled
-    float U[64 * 64];              // U~ columns a0 .. a0 + 63: two swizzled 64 x 32 boxes
-    float gam[256];                // 64 used
-};
-constexpr int kStageFloats = (int)(sizeof(StateStage) / sizeof(float));
-static_assert(sizeof(StateStage) % 1024 == 0, "stage alignment");
-constexpr size_t kStateSmem =
-    sizeof(float) * (2 * kStageFloats + kSliceMax * kD + kSliceMax * 64 + 64 * 8) + 2 * 8 +
-    1024;
+// grid (2, Hv, N), 288 threads, one CTA per SM: CTA (slice, head, sequence)
+// carries rows a0 .. a0 + 63 (a0 = 64 slice) of the fp32 state S [d_v x d_k]
+// through the sequence's chunks.  With fk_i = e^{gam_L - gam_i} (0 past the
+// chunk's length), a chunk's update S_end = e^{gam_L} S + U^T diag(fk) K with
+// U = U~ - W S^T is, transposed,
+//   S_end^T = e^{gam_L} S^T + M^T S^T + B^T,   M^T = -(diag(fk) K)^T W  (d_k x d_k),
+//                                              B^T = (diag(fk) K)^T U~  (this CTA's columns),
+// so one product per chunk waits on the state: M^T S^T (M = 128, N = 64,
+// K = 128, tcgen05), with M^T read from tensor memory and S^T from shared
+// memory, accumulated onto B^T.  The e^{gam_L} S term is added in fp32: the
+// state lives in registers and never passes through tf32 itself.
+//
+// Four roles, coupled only by mbarriers (one phase per chunk each):
+//  - loader / product thread (warp 9): requests a chunk's K, W, U~ (TMA,
+//    MN-major, two stages, two chunks ahead) and, once the producers have
+//    scaled them, issues the chunk's M^T and B^T products;
+//  - producers (warps 0-3): scale K by fk and round U~ in place ("scaled");
+//    once the products are done, round M^T to nearest tf32 in tensor memory
+//    and, once S is ready too, declare "M ready" -- so a chunk's products are
+//    issued only after the chain product two chunks back is complete and read,
+//    whose tensor-memory buffers they reuse; each thread's gate values are
+//    read one chunk ahead;
+//  - state warps (warps 4-7): thread (warp 4 + q, lane l) holds S[a][b'] for
+//    b' = 32 q + l and all 64 rows a; once a chunk's chain product is done
+//    they update S and write its tf32 copy (the chain's B operand, "S
+//    ready"), then the chunk-start state outputs;
+//  - chain thread (warp 8): issues each chunk's chain product as soon as S
+//    and M are ready.
+// U itself is formed by the output kernel, which holds S0 anyway.  Outputs per
+// chunk: the chunk-start state rounded to tf32 in the swizzled K-major layout
+// (rows a; an operand of the output kernel) and exact in the K-major layout
+// with rows b (for the backward).
+//
+// Shared memory: S (rows a, swizzled K-major, 64 x 128) 32 KB and two stages
+// of K, W (MN-major, 32 KB each) and the U~ slice (MN-major, 64 x 64, 16 KB).
+// Tensor memory: two chain accumulators (M = 128, 64 columns) and two M^T
+// tiles (128 columns).
+constexpr int kStFloats = 64 * 128;
+constexpr int kStageF = 2 * 64 * 128 + 64 * 64;   // K, W, U~ slice
+constexpr int kStateThreads = 320;
+constexpr size_t kStateSmem = sizeof(float) * (kStFloats + 2 * kStageF) + 7 * 8 + 8 + 1024;
 
-template <int SW>
-__device__ __forceinline__ void state_fwd_slice(const TileMaps& maps, int hk, int hv, int a0,
-                                                const float* S_init, float* S_final,
-                                                const FwdSaved& sv, float* sm) {
-    StateStage* stage = reinterpret_cast<StateStage*>(sm);
-    float* St = sm + 2 * kStageFloats;      // [SW (a)][128 (b)] K-major, rounded
-    float* Ub = St + kSliceMax * kD;        // [SW (a)][64 (i)] K-major: fk_i U[i][a], rounded
-    // (the ldmatrix pair loads of an odd n-block count read up to 8 rows past St
-    // and Ub: the padding keeps them inside shared memory)
-    uint64_t* mb = reinterpret_cast<uint64_t*>(Ub + kSliceMax * 64 + 64 * 8);   // [2]
-    const int h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
-    const int kh = h / (hv / hk);
-    constexpr int NB = (SW + 31) / 32;      // U~ boxes of 32 columns
-    using TS = Tile<kD, SW, 8>;    // S^T: rows b (d_k), cols a (slice)
-    using TU = Tile<64, SW, 8>;
-    typename TS::Acc sacc;
-    const int64_t sbase = ((int64_t)n * hv + h) * kD * kD;
-    if (tid == 0) {
-        umma::mbar_init(&mb[0], 1);
-        umma::mbar_init(&mb[1], 1);
-    }
-    tile_each2<kD, SW, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
-        v0 = S_init ? S_init[sbase + (int64_t)(a0 + a) * kD + b] : 0.f;
-        v1 = S_init ? S_init[sbase + (int64_t)(a0 + a + 1) * kD + b] : 0.f;
-        St[umma::kidx(a, b, kD)] = umma::tf32r(v0);
-        St[umma::kidx(a + 1, b, kD)] = umma::tf32r(v1);
-    });
-    umma::fence_smem_to_async();
-    __syncthreads();   // barriers initialised, St written
-    const int c0 = sv.seq_chunk[n], c1 = sv.seq_chunk[n + 1];
-    auto issue = [&](int s, const ChunkInfo& info) {   // tiles: one thread; gates: 64
-        if (tid == 0) {
-            umma::mbar_expect_tx(&mb[s], (2 * 64 * 128 + NB * 64 * 32) * 4);
-            umma::tma_rows(stage[s].W, 64, &maps.W, h, info.start, &mb[s]);
-            umma::tma_rows(stage[s].K, 64, &maps.k, kh, info.start, &mb[s]);
-#pragma unroll
-            for (int bx = 0; bx < NB; bx++)
-                umma::tma_box(stage[s].U + bx * 64 * 32, &maps.U, a0 + 32 * bx, h, info.start,
-                              &mb[s]);
-        }
-        if (tid < 64)   // gate rows start at any token: 4-byte copies
-            cp_async4(stage[s].gam + tid,
-                      sv.gam + (int64_t)h * sv.T + info.start + min(tid, info.len - 1),
-                      tid < info.len);
-        cp_async_commit();
-    };
-    if (c0 < c1) issue(0, sv.chunks[c0]);
-    bool ok = true;
-    const int lane = tid & 31, rg = TU::m0() + (lane >> 2);   // this thread's U rows rg, rg + 8
-    for (int ci = c0; ci < c1 && ok; ci++) {
-        const int s = (ci - c0) & 1;
-        StateStage& cur = stage[s];
-        const ChunkInfo info = sv.chunks[ci];
-        const int L = info.len;
-        if (ci + 1 < c1) {
-            issue(s ^ 1, sv.chunks[ci + 1]);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        // chunk-start state in the layout with rows b (exact), from the accumulators
-        const int64_t obase = ((int64_t)ci * hv + h) * kD * kD;
-        tile_each2<kD, SW, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
-            *reinterpret_cast<float2*>(sv.S0b + obase + umma::kidx(b, a0 + a, kD)) =
-                make_float2(v0, v1);
-        });
-        ok = __syncthreads_and(umma::mbar_wait(&mb[s], ((ci - c0) >> 1) & 1));
-        if (!ok) break;
-        if (tid == 0) {   // ... and with rows a (rounded; an MMA operand only): St whole
-            umma::bulk_store(sv.S0 + obase + (int64_t)a0 * kD, St, SW * kD * 4);
-            umma::bulk_commit();
-        }
-        const float gL = cur.gam[L - 1];
-        const float f0 = rg < L ? expf(gL - cur.gam[rg]) : 0.f;
-        const float f1 = rg + 8 < L ? expf(gL - cur.gam[rg + 8]) : 0.f;
-        // U = U~ - W S^T   (64 x slice)
-        typename TU::Acc uacc;
-        tile_zero<64, SW, 8>(uacc);
-        tile_mma_frag<64, SW, kD, 8>(
-            uacc,
-            [&](int r0, int k0, uint32_t(&f)[4]) {
-                ldsm_a(f, r0, k0, [&](int r, int c) { return cur.W + umma::swz(r, c, 64); });
-            },
-            [&](int k0, int n0, uint32_t(&f)[4]) {
-                ldsm_b2(f, k0, n0, [&](int nn, int k) { return St + umma::kidx(nn, k, kD); });
-            });
-        tile_each2<64, SW, 8>(uacc, [&](int i, int a, float& v0, float& v1) {
-            float u0 = 0.f, u1 = 0.f;
-            if (i < L) {
-                const float2 ut = *reinterpret_cast<const float2*>(cur.U + umma::swz(i, a, 64));
-                u0 = ut.x - v0;
-                u1 = ut.y - v1;
-                // stored rounded: later kernels use U only as a tensor-core operand
-                *reinterpret_cast<float2*>(sv.U + ((int64_t)(info.start + i) * hv + h) * kD +
-                                           a0 + a) = make_float2(umma::tf32r(u0), umma::tf32r(u1));
-            }
-            const float f = i == rg ? f0 : f1;
-            Ub[umma::kidx(a, i, 64)] = umma::tf32r(f * u0);
-            Ub[umma::kidx(a + 1, i, 64)] = umma::tf32r(f * u1);
-        });
-        __syncthreads();   // Ub complete
-        // S^T = e^{gam_L} S^T + K^T (diag(fk) U)
-        const float dl = expf(gL);
-        tile_each<kD, SW, 8>(sacc, [&](int, int, float& v) { v *= dl; });
-        tile_mma_frag<kD, SW, 64, 8>(
-            sacc,
-            [&](int r0, int k0, uint32_t(&f)[4]) {   // A(b, i) = K[i][b]: element loads
-                const int g = lane >> 2, t = lane & 3;
-                f[0] = f2tf32(cur.K[umma::swz(k0 + t, r0 + g, 64)]);
-                f[1] = f2tf32(cur.K[umma::swz(k0 + t, r0 + g + 8, 64)]);
-                f[2] = f2tf32(cur.K[umma::swz(k0 + t + 4, r0 + g, 64)]);
-                f[3] = f2tf32(cur.K[umma::swz(k0 + t + 4, r0 + g + 8, 64)]);
-            },
-            [&](int k0, int n0, uint32_t(&f)[4]) {
-                ldsm_b2(f, k0, n0, [&](int nn, int k) { return Ub + umma::kidx(nn, k, 64); });
-            });
-        if (tid == 0) umma::bulk_wait_read();   // the chunk-start copy has read St
-        __syncthreads();   // reads of cur, St and Ub are done
-        tile_each2<kD, SW, 8>(sacc, [&](int b, int a, float& v0, float& v1) {
-            St[umma::kidx(a, b, kD)] = umma::tf32r(v0);
-            St[umma::kidx(a + 1, b, kD)] = umma::tf32r(v1);
-        });
-        umma::fence_smem_to_async();   // St -> the next chunk's bulk copy
-    }
-    if (!ok) {
-        if (tid == 0) atomicExch(sv.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
-        return;
-    }
-    if (S_final)
-        tile_each<kD, SW, 8>(sacc, [&](int b, int a, float& v) {
-            S_final[sbase + (int64_t)(a0 + a) * kD + b] = v;
-        });
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(umma::saddr(mbar)) : "memory");
 }
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kStateThreads, 1)
 state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const float* S_init,
                  float* S_final, FwdSaved sv) {
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
-    if (blockIdx.x < 2)
-        state_fwd_slice<48>(maps, hk, hv, 48 * (int)blockIdx.x, S_init, S_final, sv, sm);
-    else
-        state_fwd_slice<32>(maps, hk, hv, 96, S_init, S_final, sv, sm);
+    float* St = sm;                    // [64 (a)][128 (b)] swizzled K-major: S, rounded
+    float* stage = St + kStFloats;     // [2] x {K, W: [64 (i)][128] MN-major; U~: [64 (i)][64 (a)]}
+    uint64_t* mT = reinterpret_cast<uint64_t*>(stage + 2 * kStageF);   // [2] tiles per stage
+    uint64_t* mC = mT + 2;             // chain product done (commit)
+    uint64_t* mP = mC + 1;             // M^T, B^T products done (commit)
+    uint64_t* bSc = mP + 1;            // chunk scaled (producers)
+    uint64_t* bM = bSc + 1;            // M^T rounded (producers)
+    uint64_t* bS = bM + 1;             // S copy written (state warps)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bS + 1);
+    auto Km = [&](int st) { return stage + st * kStageF; };
+    auto Wm = [&](int st) { return stage + st * kStageF + 64 * 128; };
+    auto Um = [&](int st) { return stage + st * kStageF + 2 * 64 * 128; };
+    const int sl = blockIdx.x, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int a0 = 64 * sl, kh = h / (hv / hk);
+    const int64_t sbase = ((int64_t)n * hv + h) * kD * kD;
+    const int c0 = sv.seq_chunk[n], c1 = sv.seq_chunk[n + 1];
+    if (tid == 0) {
+        umma::mbar_init(&mT[0], 1);
+        umma::mbar_init(&mT[1], 1);
+        umma::mbar_init(mC, 1);
+        umma::mbar_init(mP, 1);
+        umma::mbar_init(bSc, 128);
+        umma::mbar_init(bM, 128);
+        umma::mbar_init(bS, 128);
+    }
+    if (warp == 0) umma::tmem_alloc(tslot, 512);
+    umma::fence_before_sync();
+    __syncthreads();   // barriers initialised, tensor memory allocated
+    umma::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t tAcc[2] = {tmem, tmem + 64}, tM[2] = {tmem + 128, tmem + 256};
+    bool ok = true;
+    if (warp < 4) {
+        // ---------------------------------------------------------- producers
+        // thread t scales row i = t / 2 of K (64 columns) and 32 values of U~;
+        // its gate values (gam_i, gam_L) are read one chunk ahead
+        const int i = tid >> 1;
+        auto gates = [&](int c, float& gi, float& gl, int& len) {
+            gi = gl = 0.f;
+            len = 0;
+            if (c >= c1) return;
+            const ChunkInfo info = sv.chunks[c];
+            const float* g = sv.gam + (int64_t)h * sv.T + info.start;
+            gi = g[min(i, info.len - 1)];
+            gl = g[info.len - 1];
+            len = info.len;
+        };
+        float gi, gl, gi_n, gl_n;
+        int len, len_n;
+        gates(c0, gi, gl, len);
+        gates(c0 + 1, gi_n, gl_n, len_n);
+        auto scale = [&](int c) {   // chunk c's tiles have been requested
+            const int it = c - c0, st = it & 1;
+            const bool got = umma::mbar_wait(&mT[st], (it >> 1) & 1);
+            if (got) {
+                const float f = i < len ? expf(gl - gi) : 0.f;
+                float4 kv[16], uv[8];
+                float* kr = Km(st);
+#pragma unroll
+                for (int q = 0; q < 16; q++)
+                    kv[q] = *reinterpret_cast<const float4*>(kr + umma::swz_mn(i, 64 * (tid & 1) + 4 * q));
+#pragma unroll
+                for (int q = 0; q < 8; q++)
+                    uv[q] = *reinterpret_cast<const float4*>(Um(st) + 4 * (tid + 128 * q));
+#pragma unroll
+                for (int q = 0; q < 16; q++)
+                    *reinterpret_cast<float4*>(kr + umma::swz_mn(i, 64 * (tid & 1) + 4 * q)) =
+                        umma::tf32r(make_float4(f * kv[q].x, f * kv[q].y, f * kv[q].z, f * kv[q].w));
+#pragma unroll
+                for (int q = 0; q < 8; q++)   // U~ is stored exact (W arrives rounded)
+                    *reinterpret_cast<float4*>(Um(st) + 4 * (tid + 128 * q)) = umma::tf32r(uv[q]);
+            }
+            umma::fence_smem_to_async();
+            mbar_arrive(bSc);
+            return got;
+        };
+        if (c0 < c1) ok = scale(c0);
+        for (int c = c0; c < c1 && ok; c++) {
+            const int it = c - c0;
+            gi = gi_n;
+            gl = gl_n;
+            len = len_n;
+            gates(c + 2, gi_n, gl_n, len_n);
+            ok = umma::mbar_wait(mP, it & 1);   // chunk c's M^T and B^T are done
+            umma::fence_after_sync();
+            if (!ok) break;
+#pragma unroll
+            for (int cc = 0; cc < 128; cc += 32) {   // M^T = -(accumulator), rounded
+                float v[32];
+                const uint32_t ta = umma::tmem_at(tM[it & 1], cc);
+                umma::tmem_ld32(ta, v);
+#pragma unroll
+                for (int u = 0; u < 32; u++) v[u] = umma::tf32r(-v[u]);
+                umma::tmem_st32(ta, v);
+            }
+            umma::tmem_wait_st();
+            umma::fence_before_sync();
+            // "S ready" for chunk c implies chain product c - 1 is complete and its
+            // accumulator read: after "M ready" the next products may reuse both
+            // of chunk c - 1's tensor-memory buffers
+            ok = umma::mbar_wait(bS, it & 1);
+            mbar_arrive(bM);
+            if (ok && c + 1 < c1) ok = scale(c + 1);
+        }
+    } else if (warp < 8) {
+        // ---------------------------------------------------------- state warps
+        const int q = warp - 4, bp = 32 * q + lane, sid = tid - 128;
+        float s[64];   // s[j] = S[j][bp]
+#pragma unroll
+        for (int j = 0; j < 64; j++)
+            s[j] = S_init ? S_init[sbase + (int64_t)(a0 + j) * kD + bp] : 0.f;
+        // S into St (rounded), "S ready"; then chunk c's start state out: exact
+        // (rows b), and the rounded tile (rows a) as four 8 KB bulk copies --
+        // box x of St (64 rows) is rows a0 .. a0 + 63 of box x of the 128-row tile
+        auto emit = [&](int c) {
+#pragma unroll
+            for (int j = 0; j < 64; j++) St[umma::swz(j, bp, 64)] = umma::tf32r(s[j]);
+            umma::fence_smem_to_async();
+            mbar_arrive(bS);
+            if (c >= c1) return;
+            named_sync(2, 128);
+            if (sid == 0) {
+                float* o = sv.S0 + ((int64_t)c * hv + h) * kD * kD;
+#pragma unroll
+                for (int x = 0; x < 4; x++)
+                    umma::bulk_store(o + (x * 128 + a0) * 32, St + x * 64 * 32, 64 * 32 * 4);
+                umma::bulk_commit();
+            }
+            float* ob = sv.S0b + ((int64_t)c * hv + h) * kD * kD;
+#pragma unroll
+            for (int j = 0; j < 64; j += 4)
+                *reinterpret_cast<float4*>(ob + umma::kidx(bp, a0 + j, kD)) =
+                    make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
+        };
+        // gam_L of chunk c, read one chunk ahead into a register
+        auto gam_last = [&](int c) {
+            if (c >= c1) return 0.f;
+            const ChunkInfo info = sv.chunks[c];
+            return sv.gam[(int64_t)h * sv.T + info.start + info.len - 1];
+        };
+        float gL = gam_last(c0);
+        if (c0 < c1) emit(c0);
+        for (int c = c0; c < c1 && ok; c++) {
+            const int it = c - c0;
+            const float gL_next = gam_last(c + 1);
+            ok = umma::mbar_wait(mC, it & 1);
+            umma::fence_after_sync();
+            if (!ok) break;
+            const float dl = expf(gL);
+            gL = gL_next;
+#pragma unroll
+            for (int cc = 0; cc < 64; cc += 32) {   // S <- e^{gam_L} S + (B + S M)
+                float v[32];
+                umma::tmem_ld32(umma::tmem_at(tAcc[it & 1], cc), v);
+#pragma unroll
+                for (int u = 0; u < 32; u++) s[cc + u] = dl * s[cc + u] + v[u];
+            }
+            if (sid == 0) umma::bulk_wait_read();   // the last start-state copy has read St
+            umma::fence_before_sync();
+            named_sync(2, 128);
+            emit(c + 1);
+        }
+        if (sid == 0) umma::bulk_wait_read();
+        if (ok && S_final)
+#pragma unroll
+            for (int j = 0; j < 64; j++) S_final[sbase + (int64_t)(a0 + j) * kD + bp] = s[j];
+    } else if (tid == 256) {
+        // ---------------------------------------------------------- chain thread
+        for (int c = c0; c < c1 && ok; c++) {
+            const int it = c - c0;
+            ok = umma::mbar_wait(bS, it & 1) && umma::mbar_wait(bM, it & 1);
+            umma::fence_after_sync();
+            if (!ok) break;
+            umma::mma_ta(tAcc[it & 1], tM[it & 1], umma::swt(St, 64), 128, 64, 128, true);
+            umma::commit(mC);
+        }
+    } else if (tid == 288) {
+        // ---------------------------------------------------------- loader / products
+        auto issue = [&](int c) {
+            if (c >= c1) return;
+            const int st = (c - c0) & 1;
+            const ChunkInfo info = sv.chunks[c];
+            umma::mbar_expect_tx(&mT[st], kStageF * 4);
+            umma::tma_rows(Km(st), 64, &maps.k_mn, kh, info.start, &mT[st]);
+            umma::tma_rows(Wm(st), 64, &maps.W_mn, h, info.start, &mT[st]);
+            umma::tma_box(Um(st), &maps.U_mn, a0, h, info.start, &mT[st]);
+            umma::tma_box(Um(st) + 64 * 32, &maps.U_mn, a0 + 32, h, info.start, &mT[st]);
+        };
+        issue(c0);
+        issue(c0 + 1);
+        for (int c = c0; c < c1 && ok; c++) {
+            const int it = c - c0, st = it & 1;
+            ok = umma::mbar_wait(bSc, it & 1);   // chunk c scaled
+            umma::fence_after_sync();
+            if (!ok) break;
+            umma::mma(tAcc[st], umma::mnt(Km(st)), umma::mnt(Um(st)), 128, 64, 64, false);  // B^T
+            umma::mma(tM[st], umma::mnt(Km(st)), umma::mnt(Wm(st)), 128, 128, 64, false);   // -M^T
+            umma::commit(mP);
+            ok = umma::mbar_wait(mP, it & 1);   // stage st consumed
+            if (ok) issue(c + 2);
+        }
+    }
+    umma::fence_before_sync();
+    ok = __syncthreads_and(ok);
+    if (warp == 0) umma::tmem_free(tmem, 512);
+    if (!ok && tid == 0) atomicExch(sv.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
 }
 
 // ------------------------------------------------------------------ output + norm
 // Persistent: one CTA per SM walks the (chunk, head) tiles t = blockIdx.x,
 // + gridDim.x, ... (chunk = t % NT, head = t / NT).  Per tile, tcgen05:
-//   D1 = Q K^T (64 x 64),  D3 = Q S0^T (64 x 128)       -- issued together
+//   D1 = Q K^T (64 x 64),  D3 = Q S0^T,  DU = W S0^T (64 x 128)  -- issued together
+//   U  = U~ - DU  (rounded; the B operand below, and stored for the backward)
 //   P  = D1 (.) e^{gam_i - gam_j} (.) [i >= j]          -- staged K-major
 //   D2 = P U (64 x 128)
 //   O  = D2 + e^{gam_i} D3 ; y = O rsqrt(mean(O^2)+eps) (1+w) gate(z)
-// Shared memory: Q, K swizzled 32 KB each and U MN-major 32 KB (TMA; U is the
-// B operand of P U, contracted over tokens, so it is read as loaded), S0
-// (K-major rows a) 64 KB (one bulk copy), P 16 KB, the z rows 33 KB.  The next
-// tile's Q, K and S0 are requested as soon as D1 and D3 are done, its U and z
-// rows once this tile's O (staged over U) has been stored; its chunk entry and
-// gate values are loaded into registers meanwhile.  Tensor memory: 320 fp32
-// columns, allocated once.
-constexpr int kOutFloats = 64 * 128 * 2 + 128 * 128 + 64 * 128 + 64 * 64 + 64 * kLdK;
+// Shared memory: Q, K, W swizzled 32 KB each, S0 64 KB (swizzled, rows a; one
+// bulk copy), U~ MN-major 32 KB (TMA; U is the B operand of P U, contracted
+// over tokens, so U~ arrives MN-major and U is formed in place), P 16 KB.  The
+// next tile's Q, K, W and S0 are requested as soon as the first products are
+// done, its U~ once this tile's O (staged over U) has been stored; its chunk
+// entry and gate values are loaded into registers meanwhile, and each warp
+// fetches the z rows of its norm rows into registers while the products run.
+// Tensor memory: 448 fp32 columns, allocated once.
+constexpr int kOutFloats = 64 * 128 * 3 + 128 * 128 + 64 * 128 + 64 * 64;
 constexpr size_t kOutSmem = sizeof(float) * (kOutFloats + 64 * 2 + 2 * 64 + 16) + 64 + 1024;
+
+// Rows 0 .. L-1 of a 64-row MN-major tile to a row-major global tensor, one warp per row.
+__device__ __forceinline__ void store_rows_mn(float* dst, int64_t stride, const float* src, int L) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int r = warp; r < L; r += nw)
+        *reinterpret_cast<float4*>(dst + r * stride + 4 * lane) =
+            *reinterpret_cast<const float4*>(src + umma::swz_mn(r, 4 * lane));
+}
 
 template <class IO>
 __global__ void __launch_bounds__(256, 1)
@@ -505,16 +611,16 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
     float* sm = umma::align1024(sm_raw);
     float* Qs = sm;                    // [64][128] swizzled
     float* Ks = Qs + 64 * 128;         // [64][128] swizzled
-    float* Ss = Ks + 64 * 128;         // [128 (a)][128 (b)] K-major
-    float* Us = Ss + 128 * 128;        // [64 (j)][128 (a)] MN-major U; then O, swizzled
+    float* Ws = Ks + 64 * 128;         // [64][128] swizzled (arrives rounded)
+    float* Ss = Ws + 64 * 128;         // [128 (a)][128 (b)] swizzled K-major (arrives rounded)
+    float* Us = Ss + 128 * 128;        // [64 (j)][128 (a)] MN-major U~, then U; then O, swizzled
     float* Ps = Us + 64 * 128;         // [64 (i)][64 (j)] K-major
-    char* Zs = reinterpret_cast<char*>(Ps + 64 * 64);   // z rows, kZPitch bytes apart
-    float* gam = Ps + 64 * 64 + 64 * kLdK;
+    float* gam = Ps + 64 * 64;
     float* eg = gam + 64;
     float* ssq = eg + 64;              // [2][64] partial sums of squares
     uint64_t* mbar = reinterpret_cast<uint64_t*>(ssq + 2 * 64 + 16);   // MMA
-    uint64_t* mA = mbar + 1;           // Q, K, S0
-    uint64_t* mU = mA + 1;             // U
+    uint64_t* mA = mbar + 1;           // Q, K, W, S0
+    uint64_t* mU = mA + 1;             // U~
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mU + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ntiles = NT * hv;
@@ -522,30 +628,17 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
     if (t >= ntiles) return;
     ChunkInfo ci = sv.chunks[t % NT];
     if (ci.len == 0) return;   // the device check of cu_seqlens failed: every chunk is empty
-    constexpr int kZPitch = kD * (int)sizeof(IO) + 16;    // bytes; conflict-free row reads
     auto issue_a = [&](const ChunkInfo& c, int tile) {   // one thread
         const int h = tile / NT, kh = h / (hv / hk);
-        umma::mbar_expect_tx(mA, 2 * 64 * 128 * 4 + 128 * 128 * 4);
+        umma::mbar_expect_tx(mA, 3 * 64 * 128 * 4 + 128 * 128 * 4);
         umma::tma_rows(Qs, 64, &maps.q, kh, c.start, mA);
         umma::tma_rows(Ks, 64, &maps.k, kh, c.start, mA);
+        umma::tma_rows(Ws, 64, &maps.W, h, c.start, mA);
         umma::bulk_load(Ss, sv.S0 + ((int64_t)(tile % NT) * hv + h) * kD * kD, 128 * 128 * 4, mA);
     };
     auto issue_u = [&](const ChunkInfo& c, int tile) {   // one thread
         umma::mbar_expect_tx(mU, 64 * 128 * 4);
         umma::tma_rows(Us, 64, &maps.U_mn, tile / NT, c.start, mU);
-    };
-    auto issue_z = [&](const ChunkInfo& c, int tile) {   // all threads, one cp.async group
-        if (z) {
-            constexpr int kPieces = kD * (int)sizeof(IO) / 16;
-            const int h = tile / NT;
-            for (int idx = tid; idx < 64 * kPieces; idx += 256) {
-                const int r = idx / kPieces, p = idx % kPieces;
-                const int64_t tr = (int64_t)c.start + min(r, c.len - 1);
-                cp_async16(Zs + r * kZPitch + p * 16,
-                           reinterpret_cast<const char*>(z + (tr * hv + h) * kD) + p * 16, r < c.len);
-            }
-        }
-        cp_async_commit();
     };
     // padding rows continue the last gate value (g = 0)
     auto gam_of = [&](const ChunkInfo& c, int tile) {
@@ -558,14 +651,13 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
         issue_a(ci, t);
         issue_u(ci, t);
     }
-    issue_z(ci, t);
     float g_cur = gam_of(ci, t);
     if (warp == 0) umma::tmem_alloc(tslot, 512);
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t tD1 = tmem, tD3 = tmem + 64, tD2 = tmem + 192;
+    const uint32_t tD1 = tmem, tD3 = tmem + 64, tD2 = tmem + 192, tDU = tmem + 320;
     const int win = warp & 3, half = warp >> 2;
     const int i = win * 16 + lane;     // row held by lanes 0..15 (M = 64 layout)
     const float4 w4 = z ? ld4(norm_w + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -578,32 +670,44 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
             gam[tid] = g_cur;
             eg[tid] = tid < L ? expf(g_cur) : 0.f;
         }
-        ok = __syncthreads_and(umma::mbar_wait(mA, it & 1));   // Q, K, S0; gam visible
+        ok = __syncthreads_and(umma::mbar_wait(mA, it & 1));   // Q, K, W, S0; gam visible
         if (!ok) break;
         if (L < 64) {   // tail rows belong to the next sequence
             umma::zero_tail_rows(Qs, 64, 0, L);
             umma::zero_tail_rows(Ks, 64, 0, L);
+            umma::zero_tail_rows(Ws, 64, 0, L);
             __syncthreads();
         }
-        if (!sv.qkv_tf32) umma::tf32r_inplace(Qs, 64 * 128 * 2);   // Q, K (S0 and U arrive rounded)
+        if (!sv.qkv_tf32) umma::tf32r_inplace(Qs, 64 * 128 * 2);   // Q, K (W and S0 arrive rounded)
         umma::fence_smem_to_async();
         __syncthreads();
         umma::fence_after_sync();
         if (tid == 0) {
             umma::mma(tD1, umma::swt(Qs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
-            umma::mma(tD3, umma::swt(Qs, 64), umma::kmaj(Ss, 128), 64, 128, 128, false);
+            umma::mma(tD3, umma::swt(Qs, 64), umma::swt(Ss, 128), 64, 128, 128, false);
+            umma::mma(tDU, umma::swt(Ws, 64), umma::swt(Ss, 128), 64, 128, 128, false);
             umma::commit(mbar);
+        }
+        // this warp's norm rows r = warp + 8 q: their z values, into registers
+        float4 zr[8];
+        if (z) {
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                const int r = warp + 8 * q;
+                zr[q] = r < L ? ld4(z + (((int64_t)ci.start + r) * hv + h) * kD + lane * 4)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
         ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
         umma::fence_after_sync();
         if (!ok) break;
         const bool next = tn < ntiles && cn.len > 0;
-        if (next && tid == 0) issue_a(cn, tn);   // Q, K, S0 consumed
+        if (next && tid == 0) issue_a(cn, tn);   // Q, K, W, S0 consumed
         const float g_next = next ? gam_of(cn, tn) : 0.f;
+        const int rl = umma::frag_row_lo(), cf = umma::frag_col();
         {   // P = D1 (.) Gam (.) M  -> K-major rows i; 32 columns per warp, all lanes
             float v[16];
             umma::tmem_ld_m64<4>(umma::tmem_at(tD1, half * 32), v);
-            const int rl = umma::frag_row_lo(), cf = umma::frag_col();
 #pragma unroll
             for (int hr = 0; hr < 2; hr++) {
                 const int r = rl + 8 * hr;
@@ -618,8 +722,24 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
                 }
             }
         }
-        ok = umma::mbar_wait(mU, it & 1);   // U
-        if (ok && L < 64) umma::zero_tail_rows(Us, 64, 0, L);   // each thread: its own pieces
+        ok = umma::mbar_wait(mU, it & 1);   // U~
+        if (ok) {   // U = U~ - W S0^T in place (rounded), rows past the chunk zero
+            float v[32];
+            umma::tmem_ld64_m64(umma::tmem_at(tDU, 64 * half), v);
+#pragma unroll
+            for (int hr = 0; hr < 2; hr++) {
+                const int r = rl + 8 * hr;
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    const int c = 64 * half + 8 * k + cf;
+                    float2* p = reinterpret_cast<float2*>(Us + umma::swz_mn(r, c));
+                    const float2 u = *p;
+                    *p = r < L ? make_float2(umma::tf32r(u.x - v[4 * k + 2 * hr]),
+                                             umma::tf32r(u.y - v[4 * k + 2 * hr + 1]))
+                               : make_float2(0.f, 0.f);
+                }
+            }
+        }
         umma::fence_smem_to_async();
         umma::fence_before_sync();
         ok = __syncthreads_and(ok);
@@ -629,7 +749,10 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
             umma::mma(tD2, umma::kmaj(Ps, 64), umma::mnt(Us), 64, 128, 64, false);
             umma::commit(mbar);
         }
-        ok = __syncthreads_and(umma::mbar_wait(mbar, 1));
+        // U for the backward (only ever a tensor-core operand: stored rounded), row by
+        // row while P U runs
+        store_rows_mn(sv.U + ((int64_t)ci.start * hv + h) * kD, (int64_t)hv * kD, Us, L);
+        ok = __syncthreads_and(umma::mbar_wait(mbar, 1));   // and the U rows are read
         umma::fence_after_sync();
         if (!ok) break;
         // O = D2 + e^{gam_i} D3, staged as a swizzled tile over U (consumed);
@@ -657,10 +780,12 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
             }
             if (lane < 16) ssq[half * 64 + i] = ss;
         }
-        cp_async_wait<0>();   // z rows
         umma::fence_before_sync();
         __syncthreads();
-        for (int r = warp; r < L; r += 8) {
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            const int r = warp + 8 * q;
+            if (r >= L) break;
             const int64_t tok = ci.start + r;
             const int64_t off = (tok * hv + h) * kD + lane * 4;
             const float4 o4 = *reinterpret_cast<const float4*>(Or + umma::swz(r, lane * 4, 64));
@@ -668,20 +793,19 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
             if (o_out) st4(o_out + off, o4);
             if (z) {
                 const float rs = rsqrtf((ssq[r] + ssq[64 + r]) * (1.f / kD) + norm_eps);
-                const float4 z4 = ld4(reinterpret_cast<const IO*>(Zs + r * kZPitch) + lane * 4);
-                st4(y_out + off, gated_norm4(o4, rs, w4, z4, gate));
+                st4(y_out + off, gated_norm4(o4, rs, w4, zr[q], gate));
                 if (lane == 0) sv.rstd[tok * hv + h] = rs;
             }
         }
-        umma::fence_smem_to_async();   // O staging -> the next U load
-        __syncthreads();               // O, z and the sums of squares are read
+        umma::fence_smem_to_async();   // O staging -> the next U~ load
+        __syncthreads();               // O and the sums of squares are read
         if (!next) break;
         if (tid == 0) issue_u(cn, tn);
-        issue_z(cn, tn);
         g_cur = g_next;
         ci = cn;
         t = tn;
     }
+    if (tid == 0) umma::bulk_wait_read();
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 512);
@@ -721,6 +845,8 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
         if (e == cudaSuccess)
             e = make_rows_map(&maps.U_mn, a.sv.U, a.hv, a.T, (int64_t)a.hv * kD, true);
         if (e == cudaSuccess)
+            e = make_rows_map(&maps.W_mn, a.sv.W, a.hv, a.T, (int64_t)a.hv * kD, true);
+        if (e == cudaSuccess)
             e = make_rows_map(&maps.k_mn, a.qkv + (int64_t)a.hk * kD, a.hk, a.T, C, true);
         if (e == cudaSuccess)
             e = make_rows_map(&maps.v_mn, a.qkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C, true);
@@ -734,7 +860,7 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
     }
     if (a.N > 0) {
         GDN_PROF("chunk_state_fwd", st);
-        state_fwd_kernel<<<dim3(3, a.hv, a.N), 256, kStateSmem, st>>>(
+        state_fwd_kernel<<<dim3(2, a.hv, a.N), kStateThreads, kStateSmem, st>>>(
             maps, a.hk, a.hv, a.S_init, a.S_final, a.sv);
     }
     if (a.NT > 0) {

@@ -108,10 +108,14 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // ----------------------------------------------------------------- tensor cores
+// Round to the nearest tf32 value, ties away from zero, on the bit pattern:
+// fp32 keeps sign and exponent, tf32 the top 10 of the 23 fraction bits, so
+// adding half a tf32 unit (bit 12) to the magnitude bits and clearing the low
+// 13 bits rounds the magnitude half-up -- ties away from zero, for either sign.
+// Finite values round exactly as cvt.rna.tf32.f32 does (an overflow carries
+// into the exponent, as it must); two integer operations, at ALU rate.
 __device__ __forceinline__ uint32_t f2tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
+    return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
 }
 // Four values rounded to nearest tf32, kept as fp32.
 __device__ __forceinline__ float4 tf32_round(float4 v) {

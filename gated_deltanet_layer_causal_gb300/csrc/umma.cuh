@@ -71,22 +71,24 @@ __device__ __forceinline__ uint64_t desc_sw(const float* tile, int rows, int k0)
 // chunk c of row r sits at chunk c ^ (r % 4)).  The tensor core reads K = 8 rows
 // per step as two 4-row groups 512 B apart, 32-column atoms one box (8 KB)
 // apart: layout type 1, start address 1 KB-aligned at every step.
-__device__ __forceinline__ uint64_t desc_mn(const float* tile, int k0) {
+// A tile of `rows` contraction rows (64 or 128) has its atoms rows * 128 B apart.
+__device__ __forceinline__ uint64_t desc_mn(const float* tile, int k0, int rows = 64) {
     const uint32_t a = saddr(tile) + (uint32_t)(k0 >> 3) * 1024u;
     uint64_t d = (uint64_t)((a >> 4) & 0x3FFFu);
-    d |= (uint64_t)((64u * 128u) >> 4) << 16;   // leading byte offset: next 32-column atom
+    d |= (uint64_t)(((uint32_t)rows * 128u) >> 4) << 16;   // leading byte offset: next atom
     d |= (uint64_t)(512u >> 4) << 32;           // stride byte offset: next 4-row group
     d |= (uint64_t)1 << 46;                     // descriptor version
     d |= (uint64_t)1 << 61;                     // 128-byte swizzle, 32-byte atoms
     return d;
 }
-// Float offset of element (r, c) of an MN-major tile.
-__device__ __forceinline__ int swz_mn(int r, int c) {
-    return ((c >> 5) * 64 + r) * 32 + ((((c >> 3) & 3) ^ (r & 3)) << 3) + (c & 7);
+// Float offset of element (r, c) of an MN-major tile of `rows` rows.
+__device__ __forceinline__ int swz_mn(int r, int c, int rows = 64) {
+    return ((c >> 5) * rows + r) * 32 + ((((c >> 3) & 3) ^ (r & 3)) << 3) + (c & 7);
 }
 
 // An MMA operand in shared memory: a no-swizzle K-major tile (n = its K
-// extent), a swizzled K-major tile (n = its row count) or an MN-major tile.
+// extent), a swizzled K-major tile (n = its row count) or an MN-major tile
+// (n = its row count, the contraction extent: 64 or 128).
 struct Op {
     const float* p;
     int n;
@@ -94,9 +96,19 @@ struct Op {
 };
 __device__ __forceinline__ Op kmaj(const float* p, int kd) { return Op{p, kd, 0}; }
 __device__ __forceinline__ Op swt(const float* p, int rows) { return Op{p, rows, 1}; }
-__device__ __forceinline__ Op mnt(const float* p) { return Op{p, 64, 2}; }
+__device__ __forceinline__ Op mnt(const float* p, int rows = 64) { return Op{p, rows, 2}; }
 __device__ __forceinline__ uint64_t opdesc(const Op& o, int k0) {
-    return o.kind == 2 ? desc_mn(o.p, k0) : o.kind == 1 ? desc_sw(o.p, o.n, k0) : desc(o.p, k0, o.n);
+    return o.kind == 2 ? desc_mn(o.p, k0, o.n)
+         : o.kind == 1 ? desc_sw(o.p, o.n, k0) : desc(o.p, k0, o.n);
+}
+
+// Offset, in the descriptor's 16-byte address units, of the K = 8 slice at
+// column k0 from the slice at column 0 (the start-address field is the low 14
+// bits and shared-memory tiles never carry out of it).
+__device__ __forceinline__ uint64_t koff(const Op& o, int k0) {
+    return o.kind == 2 ? (uint64_t)(k0 >> 3) * 64u
+         : o.kind == 1 ? (uint64_t)(((k0 >> 5) * o.n * 128 + (k0 & 31) * 4) >> 4)
+                       : (uint64_t)(k0 >> 2) * 8u;
 }
 
 // Instruction descriptor: D fp32, A and B tf32, both K-major, M x N.
@@ -110,8 +122,10 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, const float* A, int ld
                                          const float* B, int ldb_k, int M, int N, int K,
                                          bool accumulate) {
     const uint32_t id = idesc_tf32(M, N);
+    const uint64_t a0 = desc(A, 0, lda_k), b0 = desc(B, 0, ldb_k);
+#pragma unroll
     for (int k0 = 0; k0 < K; k0 += 8) {
-        const uint64_t ad = desc(A, k0, lda_k), bd = desc(B, k0, ldb_k);
+        const uint64_t ad = a0 + (uint64_t)(k0 >> 2) * 8u, bd = b0 + (uint64_t)(k0 >> 2) * 8u;
         const uint32_t acc = (accumulate || k0 > 0) ? 1u : 0u;
         asm volatile(
             "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
@@ -120,18 +134,39 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, const float* A, int ld
     }
 }
 
-// The same for operands of either layout.
+// The same for operands of either layout.  The descriptors are built once and
+// advanced by a constant per K step (the loop unrolls at the call sites, where
+// K and the layouts are constants).
 __device__ __forceinline__ void mma(uint32_t d_tmem, const Op& A, const Op& B, int M, int N, int K,
                                     bool accumulate) {
     const uint32_t id = idesc_tf32(M, N) | (A.kind == 2 ? 1u << 15 : 0u) |
                         (B.kind == 2 ? 1u << 16 : 0u);   // MN-major ("transposed") operands
+    const uint64_t a0 = opdesc(A, 0), b0 = opdesc(B, 0);
+#pragma unroll
     for (int k0 = 0; k0 < K; k0 += 8) {
-        const uint64_t ad = opdesc(A, k0), bd = opdesc(B, k0);
+        const uint64_t ad = a0 + koff(A, k0), bd = b0 + koff(B, k0);
         const uint32_t acc = (accumulate || k0 > 0) ? 1u : 0u;
         asm volatile(
             "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
             "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
             "l"(ad), "l"(bd), "r"(id), "r"(acc));
+    }
+}
+
+// D[M x N] (+)= A[M x K] * B[N x K]^T with A in tensor memory (row m of A in
+// lane m, element k in column a_tmem + k; M = 128) and B in shared memory.
+__device__ __forceinline__ void mma_ta(uint32_t d_tmem, uint32_t a_tmem, const Op& B, int M, int N,
+                                       int K, bool accumulate) {
+    const uint32_t id = idesc_tf32(M, N) | (B.kind == 2 ? 1u << 16 : 0u);
+    const uint64_t b0 = opdesc(B, 0);
+#pragma unroll
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        const uint64_t bd = b0 + koff(B, k0);
+        const uint32_t acc = (accumulate || k0 > 0) ? 1u : 0u;
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+            "r"(a_tmem + (uint32_t)k0), "l"(bd), "r"(id), "r"(acc));
     }
 }
 
@@ -265,14 +300,70 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 consecutive fp32 columns of this thread's lane (one wait).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+// Store 32 consecutive fp32 columns of this thread's lane (no wait: the caller
+// waits with tmem_wait_st before the columns are read by anything else).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(
+            taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
+// Store 16 consecutive fp32 columns of this thread's lane (the inverse of
+// tmem_ld16), then wait until the stores have completed.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};\n" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
 // Round to the nearest tf32 value (ties away from zero).  The tensor core reads
 // only the top 19 bits of an fp32 operand (it truncates), so operands are
 // rounded when they are written to shared memory: rounding then happens once,
 // to nearest, instead of being a truncation biased towards zero.
 __device__ __forceinline__ float tf32r(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+    // nearest, ties away from zero, on the bit pattern (see f2tf32 in common.cuh)
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
 __device__ __forceinline__ float4 tf32r(float4 v) {
     return make_float4(tf32r(v.x), tf32r(v.y), tf32r(v.z), tf32r(v.w));
