@@ -1,5 +1,6 @@
-// Shared device helpers of the GDN CUDA library: dtype conversion, warp
-// reductions and a warp-tiled tensor-core product over shared-memory operands.
+// Shared device helpers of the GDN CUDA library: dtype conversion, math,
+// warp reductions, asynchronous copies, tf32 rounding, the gated-norm row
+// backward and the unit lower-triangular inverse.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -121,126 +122,6 @@ __device__ __forceinline__ uint32_t f2tf32(float x) {
 __device__ __forceinline__ float4 tf32_round(float4 v) {
     return make_float4(__uint_as_float(f2tf32(v.x)), __uint_as_float(f2tf32(v.y)),
                        __uint_as_float(f2tf32(v.z)), __uint_as_float(f2tf32(v.w)));
-}
-
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
-                                         const uint32_t (&b)[2]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// Split of an M x N product over NW warps into 16 x 8 fragments.
-template <int M, int N, int NW>
-struct Tile {
-    static constexpr int MT = M / 16, NT = N / 8;
-    static constexpr int WM = MT < NW ? MT : NW;   // warps along M
-    static constexpr int WN = NW / WM;             // warps along N
-    static constexpr int MPW = MT / WM;            // 16-row fragments per warp
-    static constexpr int NPW = NT / WN;            // 8-col fragments per warp
-    static_assert(M % 16 == 0 && N % 8 == 0, "fragment multiple");
-    static_assert(MT % WM == 0 && NW % WM == 0 && NT % WN == 0, "warp split");
-    using Acc = float[MPW][NPW][4];
-    __device__ static int m0() { return (int)(threadIdx.x / 32 % WM) * MPW * 16; }
-    __device__ static int n0() { return (int)(threadIdx.x / 32 / WM) * NPW * 8; }
-};
-
-template <int M, int N, int NW>
-__device__ __forceinline__ void tile_zero(typename Tile<M, N, NW>::Acc& acc) {
-    using C = Tile<M, N, NW>;
-#pragma unroll
-    for (int i = 0; i < C::MPW; i++)
-#pragma unroll
-        for (int j = 0; j < C::NPW; j++)
-#pragma unroll
-            for (int e = 0; e < 4; e++) acc[i][j][e] = 0.f;
-}
-
-// Four 8 x 8 matrices of 16-bit elements (8 rows of 16 bytes each; lane l
-// gives the address of row l % 8 of matrix l / 8).  For 32-bit (tf32) data a
-// matrix is 8 rows x 4 values, and thread t receives (row t / 4, value t % 4):
-// exactly the m16n8k8 tf32 fragment pattern.
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const float* row_addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(row_addr))));
-}
-// The A fragment (rows r0 .. r0 + 15, columns k0 .. k0 + 7) of a matrix whose
-// 4-value row pieces are 16-byte aligned at addr(row, col), col % 4 == 0.
-template <class F>
-__device__ __forceinline__ void ldsm_a(uint32_t (&a)[4], int r0, int k0, F addr) {
-    const int l = threadIdx.x & 31, m = l >> 3;
-    ldsm_x4(a, addr(r0 + (l & 7) + 8 * (m & 1), k0 + 4 * (m >> 1)));
-}
-// The B fragments of two n-blocks (n0 .. n0 + 7 -> b[0], b[1]; n0 + 8 .. -> b[2],
-// b[3]) of B(k, n) stored with rows n: addr(n, k), k % 4 == 0.
-template <class F>
-__device__ __forceinline__ void ldsm_b2(uint32_t (&b)[4], int k0, int n0, F addr) {
-    const int l = threadIdx.x & 31, m = l >> 3;
-    ldsm_x4(b, addr(n0 + (l & 7) + 8 * (m >> 1), k0 + 4 * (m & 1)));
-}
-
-// acc += A * B with whole fragments supplied by the caller: fa(r0, k0, a[4])
-// fills the A fragment of rows r0 .. r0 + 15, fb(k0, n0, b[4]) the B fragments
-// of the two n-blocks n0 and n0 + 8 (as tf32 bit patterns), so operands in
-// fragment-friendly layouts load with ldmatrix.  With an odd number of n-blocks
-// per warp the last call reads one block past the warp's columns (the caller's
-// address function must stay inside shared memory there); it is not used.
-template <int M, int N, int K, int NW, class FA, class FB>
-__device__ __forceinline__ void tile_mma_frag(typename Tile<M, N, NW>::Acc& acc, FA fa, FB fb) {
-    using C = Tile<M, N, NW>;
-    const int m0 = C::m0(), n0 = C::n0();
-#pragma unroll 2
-    for (int k0 = 0; k0 < K; k0 += 8) {
-        uint32_t af[C::MPW][4];
-#pragma unroll
-        for (int i = 0; i < C::MPW; i++) fa(m0 + i * 16, k0, af[i]);
-#pragma unroll
-        for (int j = 0; j < C::NPW; j += 2) {   // an odd count loads one block more, unused
-            uint32_t bf[4];
-            fb(k0, n0 + j * 8, bf);
-            const uint32_t b0[2] = {bf[0], bf[1]}, b1[2] = {bf[2], bf[3]};
-#pragma unroll
-            for (int i = 0; i < C::MPW; i++) {
-                mma_tf32(acc[i][j], af[i], b0);
-                if (j + 1 < C::NPW) mma_tf32(acc[i][j + 1], af[i], b1);
-            }
-        }
-    }
-}
-
-// Visit every accumulator element as f(row, col, value&).
-template <int M, int N, int NW, class F>
-__device__ __forceinline__ void tile_each(typename Tile<M, N, NW>::Acc& acc, F f) {
-    using C = Tile<M, N, NW>;
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int m0 = C::m0(), n0 = C::n0();
-#pragma unroll
-    for (int i = 0; i < C::MPW; i++)
-#pragma unroll
-        for (int j = 0; j < C::NPW; j++)
-#pragma unroll
-            for (int e = 0; e < 4; e++)
-                f(m0 + i * 16 + g + (e >> 1) * 8, n0 + j * 8 + 2 * t + (e & 1), acc[i][j][e]);
-}
-
-// Visit accumulator element pairs (same row, columns col and col+1) as
-// f(row, col, v0&, v1&): lets epilogues write 8-byte vectors.
-template <int M, int N, int NW, class F>
-__device__ __forceinline__ void tile_each2(typename Tile<M, N, NW>::Acc& acc, F f) {
-    using C = Tile<M, N, NW>;
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int m0 = C::m0(), n0 = C::n0();
-#pragma unroll
-    for (int i = 0; i < C::MPW; i++)
-#pragma unroll
-        for (int j = 0; j < C::NPW; j++)
-#pragma unroll
-            for (int h = 0; h < 2; h++)
-                f(m0 + i * 16 + g + h * 8, n0 + j * 8 + 2 * t, acc[i][j][2 * h],
-                  acc[i][j][2 * h + 1]);
 }
 
 // Backward of one gated-RMSNorm row held by a warp (4 columns per lane):
