@@ -238,19 +238,19 @@ class DecodeStep:
 # proportional to the chunks it processes).  Valid for the kernels as captured;
 # a kernel changed since then is left out (its traffic reports null).
 TRAFFIC_64K = {
-    "conv_fwd": 3618197504,
-    "gates": 12664832,
-    "chunk_prep": 6525761536,
-    "chunk_state_fwd": 13307377664,
-    "chunk_out_fwd": 8944007168,
-    "chunk_norm_bwd": 5314086912,
-    "chunk_bwd_local": 4016205824,
-    "chunk_bwd_state": 10369161216,
-    "chunk_bwd_dp": 7217242112,
-    "chunk_bwd_sfacing": 17421240320,
-    "chunk_bwd_wy": 10134188032,
-    "gva_sum": 9022685184,
-    "conv_bwd": 5592219648,
+    "conv_fwd": 3620528128,
+    "gates": 12666880,
+    "chunk_prep": 6522421248,
+    "chunk_state_fwd": 9752692736,
+    "chunk_out_fwd": 12132157440,
+    "chunk_norm_bwd": 5315454976,
+    "chunk_bwd_local": 4015650816,
+    "chunk_bwd_state": 10369904640,
+    "chunk_bwd_dp": 7219191808,
+    "chunk_bwd_sfacing": 17378592768,
+    "chunk_bwd_wy": 10133276672,
+    "gva_sum": 9023150080,
+    "conv_bwd": 5371113472,
 }
 
 # tcgen05 / mma.sync products each chunk kernel issues per (chunk, v-head) tile,
@@ -294,8 +294,8 @@ def kernel_cost(name: str, w: synth.Workload, NT: int):
         "conv_bwd": 2 * T * C * io + T * C * 4,
         "gates": gates + 2 * g,
         "chunk_prep": tk + tv + 2 * g + 2 * tv + 2 * Tt,
-        "chunk_state_fwd": 2 * tv + tk + g + tv + 2 * S,
-        "chunk_out_fwd": 2 * tk + tv + S + g + act + act + tv + g,
+        "chunk_state_fwd": 2 * tv + tk + g + 2 * S,
+        "chunk_out_fwd": 2 * tk + 2 * tv + S + g + act + act + 2 * tv + g,
         "chunk_norm_bwd": tv + 2 * act + tv + act,
         "chunk_bwd_local": 2 * tk + tv + g + tv,
         "chunk_bwd_state": 2 * tk + 3 * tv + g + tv + S,
