@@ -241,13 +241,8 @@ TRAFFIC_64K = {
     "conv_fwd": 3620528128,
     "gates": 12666880,
     "chunk_prep": 6522421248,
-    "chunk_state_fwd": 9752692736,
-    "chunk_out_fwd": 12132157440,
     "chunk_norm_bwd": 5315454976,
     "chunk_bwd_local": 4015650816,
-    "chunk_bwd_state": 10369904640,
-    "chunk_bwd_dp": 7219191808,
-    "chunk_bwd_sfacing": 17378592768,
     "chunk_bwd_wy": 10133276672,
     "gva_sum": 9023150080,
     "conv_bwd": 5371113472,
@@ -262,8 +257,9 @@ MMAS = {
     # Q K^T, Q S0^T, W S0^T (U = U~ - W S0^T), P U
     "chunk_out_fwd": [(64, 64, 128), (64, 128, 128), (64, 128, 128), (64, 128, 64)],
     "chunk_bwd_local": [(64, 64, 128), (64, 128, 64)],                  # K Q^T, P^T dO
-    "chunk_bwd_state": [(64, 64, 128), (64, 128, 64), (64, 128, 64)] * 2,   # 2 row slices
-    "chunk_bwd_dp": [(64, 64, 128), (64, 64, 128), (64, 128, 64), (64, 128, 64)],
+    # reverse state pass (2 row slices) and P / dP tiles, one launch
+    "chunk_bwd_state_dp": [(64, 64, 128), (64, 128, 64), (64, 128, 64)] * 2 +
+                          [(64, 64, 128), (64, 64, 128), (64, 128, 64), (64, 128, 64)],
     "chunk_bwd_sfacing": [(128, 128, 128), (64, 128, 128)],            # [dO; dU] S0, U dS
     "chunk_bwd_wy": [(64, 64, 128)] * 3 + [(64, 256, 64), (64, 64, 64), (64, 64, 64),
                                            (64, 128, 64), (64, 128, 64)],
@@ -294,13 +290,13 @@ def kernel_cost(name: str, w: synth.Workload, NT: int):
         "conv_bwd": 2 * T * C * io + T * C * 4,
         "gates": gates + 2 * g,
         "chunk_prep": tk + tv + 2 * g + 2 * tv + 2 * Tt,
-        "chunk_state_fwd": 2 * tv + tk + g + 2 * S,
+        "chunk_state_fwd": 2 * tv + tk + g + S,
         "chunk_out_fwd": 2 * tk + 2 * tv + S + g + act + act + 2 * tv + g,
         "chunk_norm_bwd": tv + 2 * act + tv + act,
         "chunk_bwd_local": 2 * tk + tv + g + tv,
-        "chunk_bwd_state": 2 * tk + 3 * tv + g + tv + S,
+        "chunk_bwd_state_dp": (2 * tk + 3 * tv + g + tv + S) +     # state pass
+                              (2 * tk + 2 * tv + g + 2 * tv + 2 * g),  # P / dP tiles
         "chunk_bwd_sfacing": 2 * S + 3 * tv + 2 * tk + g + 3 * tv + g,
-        "chunk_bwd_dp": 2 * tk + 2 * tv + g + 2 * tv + 2 * g,
         "chunk_bwd_wy": tk + tv + 2 * tv + 2 * Tt + 3 * g + gates + 2 * tv + gates + g,
         "gva_sum": 5 * tv + 2 * tk,
     }

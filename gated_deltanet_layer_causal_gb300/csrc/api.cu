@@ -45,7 +45,8 @@ gdn_status check_cu(const gdn_dims* d, const int32_t* cu, int* nt) {
         if (L < 0) return GDN_ERR_INVALID_ARG;
         chunks += (L + kChunk - 1) / kChunk;
     }
-    if (chunks >= (int64_t)1 << 31) return GDN_ERR_UNSUPPORTED;
+    // chunk-start state rows (chunk, head, row) are tensor-map coordinates: int32
+    if (chunks * d->h_v * kD >= (int64_t)1 << 31) return GDN_ERR_UNSUPPORTED;
     *nt = (int)chunks;
     return GDN_OK;
 }
@@ -96,7 +97,6 @@ FwdSaved carve_fwd(void* ws, const gdn_dims* d, int NT, size_t* bytes) {
     s.W = c.take<float>(T * H * kD);
     s.U = c.take<float>(T * H * kD);
     s.S0 = c.take<float>((size_t)NT * H * kD * kD);
-    s.S0b = c.take<float>((size_t)NT * H * kD * kD);
     s.Tm = c.take<float>((size_t)NT * H * 2 * 64 * 64);
     s.o = c.take<float>(T * H * kD);
     s.rstd = c.take<float>(T * H);
@@ -122,6 +122,7 @@ BwdScratch carve_bwd(void* ws, const gdn_dims* d, int NT, int32_t** status, size
     s.dgam = c.take<float>(T * H);
     s.dgam2 = c.take<float>(T * H);
     s.dgs = c.take<float>(T * H);
+    s.dp_next = c.take<int32_t>(kAlign / 4);
     // dnorm_w partials [NT*H][kD], gate partials [NT*H][2], column-sum stage [512][kD]
     s.nw_part = c.take<float>((size_t)NT * H * kD + (size_t)NT * H * 2 + 512 * kD);
     *bytes = c.off;

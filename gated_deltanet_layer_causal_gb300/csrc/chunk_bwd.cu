@@ -21,7 +21,6 @@
 #include "prof.h"
 #include "umma.cuh"
 
-#include <mutex>
 
 namespace gdn {
 
@@ -101,6 +100,8 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
     uint64_t* mbar = reinterpret_cast<uint64_t*>(gam + 64 + 16);
     uint64_t* mbl = mbar + 1;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
+    // the P / dP kernel, launched after this one, claims its tiles from this counter
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *w.dp_next = 0;
     const ChunkInfo ci = sv.chunks[blockIdx.x];
     if (ci.len == 0) return;
     const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
@@ -189,7 +190,8 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
 }
 
 // ------------------------------------------------------------------ B2: reverse state pass
-// grid (d_v / 64, Hv, N), 256 threads, tcgen05, one CTA per SM.  Carries a
+// One CTA per (slice, head, sequence), 256 threads, tcgen05, one CTA per SM
+// (the first CTAs of the combined launch below).  Carries a
 // 64-row slice (rows a) of dS from the last chunk of the sequence to the
 // first, in registers laid out like an M = 64 accumulator, and per chunk:
 //   D1 = K dS_slice^T                          (M = 64 tokens, N = 64, K = 128)
@@ -204,9 +206,9 @@ constexpr int kSl = 64;
 constexpr int kB2Floats = 3 * 64 * 128 + 4 * 64 * kSl + kSl * kD + 2 * kSl * 64 + 3 * 64;
 constexpr size_t kB2Smem = sizeof(float) * kB2Floats + 5 * 8 + 8 + 1024;
 
-__global__ void __launch_bounds__(256, 1)
-bwd_state_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const float* dS_final,
-                 float* dS_init, FwdSaved sv, BwdScratch w) {
+__device__ __forceinline__ void bwd_state_cta(const TileMaps& maps, int sl, int h, int n, int hk,
+                                              int hv, const float* dS_final, float* dS_init,
+                                              const FwdSaved& sv, const BwdScratch& w) {
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
     float* Kb = sm;                    // [64][128] swizzled K
@@ -221,7 +223,7 @@ bwd_state_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
     float* eg = gam + 2 * 64;
     uint64_t* mb = reinterpret_cast<uint64_t*>(eg + 64);   // K, Q/W, slices [2], MMA
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mb + 5);
-    const int sl = blockIdx.x, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
+    const int tid = threadIdx.x;
     const int warp = tid >> 5, half = warp >> 2;
     const int a0 = sl * kSl, kh = h / (hv / hk);
     const int64_t sbase = ((int64_t)n * hv + h) * kD * kD;
@@ -410,8 +412,9 @@ bwd_state_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
 // then dQ partial = e^gam X, dW = -Y, dK partial = fk dK~, and the dgam terms
 //   dgam_i += e^{gam_i} X_i . Q_i,  dgam_j -= Z_j = fk_j dK~_j . K_j,
 //   dgam_{L-1} += sum_j Z_j + e^{gam_L} <dS, S0>.
-// Shared memory: [dO; dU] 64 KB and U 32 KB swizzled (TMA), S0^T and dS^T
-// 64 KB each, K-major rows b (one bulk copy each).  dS^T is free once the
+// Shared memory: [dO; dU] 64 KB and U 32 KB swizzled, S0 64 KB MN-major (rows a,
+// the contraction dimension of [dO; dU] S0; all by TMA), dS^T 64 KB K-major
+// rows b (one bulk copy).  dS^T is free once the
 // products are done and takes the next tile's at once; the other tiles hold
 // this tile's Q, K and staged outputs until its stores have read them.
 // Tensor memory: 256 fp32 columns, allocated once.
@@ -424,8 +427,8 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
     float* A1 = sm;                      // [128][128] swizzled: rows 0-63 dO, 64-127 dU
-    float* S0T = A1 + 128 * 128;         // [128 (b)][128 (a)] K-major
-    float* DST = S0T + 128 * 128;        // [128 (b)][128 (a)] K-major
+    float* S0m = A1 + 128 * 128;         // [128 (a)][128 (b)] MN-major (arrives rounded)
+    float* DST = S0m + 128 * 128;        // [128 (b)][128 (a)] K-major
     float* A2 = DST + 128 * 128;         // [64][128] swizzled: U
     float* eg = A2 + 64 * 128;
     float* fk = eg + 64;
@@ -440,8 +443,8 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
     // the products' operands are consumed after the first wait: Q and K come into
     // the S0 space; the outputs are staged as swizzled tiles in the consumed
     // operand space and stored whole: dQ part and dW over [dO; dU], dK part over U
-    float* Qr = S0T;                     // [64][128] swizzled
-    float* Kr = S0T + 64 * 128;          // [64][128] swizzled
+    float* Qr = S0m;                     // [64][128] swizzled
+    float* Kr = S0m + 64 * 128;          // [64][128] swizzled
     float* SQ = A1;                      // [64][128] swizzled
     float* SW = A1 + 64 * 128;           // [64][128] swizzled
     float* SK = A2;                      // [64][128] swizzled
@@ -458,7 +461,9 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
         umma::tma_rows(A1, 128, &maps.dO, h, c.start, mS);
         umma::tma_rows(A1 + 64 * 32, 128, &maps.dU, h, c.start, mS);
         umma::tma_rows(A2, 64, &maps.U, h, c.start, mS);
-        umma::bulk_load(S0T, sv.S0b + sbase(tile), 128 * 128 * 4, mS);
+        const int s0row = ((tile % NT) * hv + h) * kD;   // S0 tile rows a = 0 .. 127
+        umma::tma_rows(S0m, 128, &maps.S0_mn, 0, s0row, mS);
+        umma::tma_rows(S0m + 64 * 32, 128, &maps.S0_mn, 0, s0row + 64, mS);
     };
     auto issue_ds = [&](int tile) {   // one thread
         umma::mbar_expect_tx(mD, 128 * 128 * 4);
@@ -494,19 +499,22 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
             umma::zero_tail_rows(A1, 128, 64, L);
             umma::zero_tail_rows(A2, 64, 0, L);
         }
-        {   // <dS, S0> over the staged copies (same layout, same index), before rounding
+        {   // <dS, S0> over the staged tiles, before dS is rounded
             float dot = 0.f;
-            for (int i = tid; i < 128 * 128; i += 256) dot += S0T[i] * DST[i];
+            for (int i = tid; i < 128 * 128; i += 256) {
+                const int a = i >> 7, b = i & 127;
+                dot += S0m[umma::swz_mn(a, b, 128)] * DST[umma::kidx(b, a, 128)];
+            }
             dot = warp_sum(dot);
             if (lane == 0) red[warp] = dot;
         }
         __syncthreads();
-        umma::tf32r_inplace(S0T, 2 * 128 * 128);   // S0^T, dS^T (dO, dU, U arrive rounded)
+        umma::tf32r_inplace(DST, 128 * 128);   // dS^T (dO, dU, U and S0 arrive rounded)
         umma::fence_smem_to_async();
         __syncthreads();
         umma::fence_after_sync();
         if (tid == 0) {
-            umma::mma(tmem, umma::swt(A1, 128), umma::kmaj(S0T, 128), 128, 128, 128, false);
+            umma::mma(tmem, umma::swt(A1, 128), umma::mnt(S0m, 128), 128, 128, 128, false);
             umma::mma(tmem + 128, umma::swt(A2, 64), umma::kmaj(DST, 128), 64, 128, 128, false);
             umma::commit(mbar);
         }
@@ -621,177 +629,227 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
 }
 
 // ------------------------------------------------------------------ B3b: P / dP terms
-// grid (NT, Hv), 256 threads, tcgen05.
+// Persistent: up to one CTA per SM (the last CTAs of the combined launch
+// below), each claiming (chunk, head) tiles from a counter (chunk = t % NT,
+// head = t / NT), so CTAs that start late -- on the SMs the reverse state pass
+// holds -- simply take fewer tiles.  Per tile, tcgen05:
 //   D_qk = Q K^T, D_dou = dO U^T                         (64 x 64 each)
 //   dPm = D_dou (.) Gam (.) [i>=j];  R = dPm (.) D_qk
 //     dgam_i += sum_j R_ij, dgam_j -= sum_i R_ij
 //   D_dq = dPm K,  D_dk = dPm^T Q                        (64 x 128 each)
 // added to the per-v-head dQ / dK partials.  Shared memory: Q, K, dO, U
-// swizzled 32 KB each (TMA; once the first products are done, the dO / U space
-// takes Q and K again as MN-major tiles, the B operands of the products over
-// tokens), dPm in both orientations 16 KB each, R 16 KB.  Tensor memory: 256
-// fp32 columns (D_dq / D_dk reuse the columns of the first products).
-constexpr int kDpFloats = 4 * 64 * 128 + 2 * 64 * 64 + 64 * 65;
-constexpr size_t kDpSmem = sizeof(float) * (kDpFloats + 64 + 64 + 2 * 64 + 16) + 64 + 1024;
+// swizzled 32 KB each (the first products' operands), Q and K again MN-major
+// 32 KB each (the B operands of the products over tokens), dPm in both
+// orientations 16 KB each.  The next tile's swizzled operands are requested as
+// soon as the first products are done, its MN-major ones as soon as the second
+// are; D_dq and D_dk go from tensor memory straight to global memory.  Tensor
+// memory: 256 fp32 columns (D_dq / D_dk reuse the columns of the first
+// products), allocated once.
+constexpr int kDpFloats = 6 * 64 * 128 + 2 * 64 * 64;
+constexpr size_t kDpSmem = sizeof(float) * (kDpFloats + 4 * 64 + 2 * 64 + 64) + 4 * 8 + 8 + 1024;
 
-__global__ void __launch_bounds__(256, 1)
-bwd_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved sv,
-              BwdScratch w) {
+__device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv, int NT,
+                                           const FwdSaved& sv, const BwdScratch& w) {
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
     float* Qs = sm;                    // [64][128] swizzled
     float* Ks = Qs + 64 * 128;         // [64][128] swizzled
-    float* dOs = Ks + 64 * 128;        // [64][128] swizzled   (later Q, MN-major)
-    float* Us = dOs + 64 * 128;        // [64][128] swizzled   (later K, MN-major)
-    float* dPR = Us + 64 * 128;        // [64 (i)][64 (j)] K-major
+    float* dOs = Ks + 64 * 128;        // [64][128] swizzled   (arrives rounded)
+    float* Us = dOs + 64 * 128;        // [64][128] swizzled   (arrives rounded)
+    float* Qm = Us + 64 * 128;         // [64 (i)][128] MN-major
+    float* Km = Qm + 64 * 128;         // [64 (j)][128] MN-major
+    float* dPR = Km + 64 * 128;        // [64 (i)][64 (j)] K-major
     float* dPC = dPR + 64 * 64;        // [64 (j)][64 (i)] K-major
-    float* Rm = dPC + 64 * 64;         // [64][65] row-major R
-    float* gam = Rm + 64 * 65;
-    float* dgl = gam + 64;             // local dgam
-    float* rpart = dgl + 64;           // [2][64]
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(rpart + 128 + 16);
-    uint64_t* mbl = mbar + 1;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
-    const ChunkInfo ci = sv.chunks[blockIdx.x];
-    if (ci.len == 0) return;
-    const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
-    const int warp = tid >> 5, lane = tid & 31;
+    float* colp = dPC + 64 * 64;       // [4 row windows][64] column sums of R
+    float* rpart = colp + 4 * 64;      // [2][64] row sums of R
+    float* gam = rpart + 2 * 64;
+    uint64_t* mA = reinterpret_cast<uint64_t*>(gam + 64);   // swizzled operands
+    uint64_t* mB = mA + 1;             // MN-major operands
+    uint64_t* mM = mB + 1;             // MMA
+    int32_t* claim = reinterpret_cast<int32_t*>(mM + 1);   // [2] claimed tile, slot per parity
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(claim + 2);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ntiles = NT * hv;
+    auto issue_a = [&](int tile) {   // one thread
+        const ChunkInfo c = sv.chunks[tile % NT];
+        if (c.len == 0) return;
+        const int h = tile / NT, kh = h / (hv / hk);
+        umma::mbar_expect_tx(mA, 4 * 64 * 128 * 4);
+        umma::tma_rows(Qs, 64, &maps.q, kh, c.start, mA);
+        umma::tma_rows(Ks, 64, &maps.k, kh, c.start, mA);
+        umma::tma_rows(dOs, 64, &maps.dO, h, c.start, mA);
+        umma::tma_rows(Us, 64, &maps.U, h, c.start, mA);
+    };
+    auto issue_b = [&](int tile) {   // one thread
+        const ChunkInfo c = sv.chunks[tile % NT];
+        if (c.len == 0) return;
+        const int kh = (tile / NT) / (hv / hk);
+        umma::mbar_expect_tx(mB, 2 * 64 * 128 * 4);
+        umma::tma_rows(Qm, 64, &maps.q_mn, kh, c.start, mB);
+        umma::tma_rows(Km, 64, &maps.k_mn, kh, c.start, mB);
+    };
     if (tid == 0) {
-        umma::mbar_init(mbar, 1);
-        umma::mbar_init(mbl, 1);
-        umma::mbar_expect_tx(mbl, 4 * 64 * 128 * 4);
-        umma::tma_rows(Qs, 64, &maps.q, kh, ci.start, mbl);
-        umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
-        umma::tma_rows(dOs, 64, &maps.dO, h, ci.start, mbl);
-        umma::tma_rows(Us, 64, &maps.U, h, ci.start, mbl);
+        umma::mbar_init(mA, 1);
+        umma::mbar_init(mB, 1);
+        umma::mbar_init(mM, 1);
+        const int t0 = atomicAdd(w.dp_next, 1);
+        claim[0] = t0;
+        if (t0 < ntiles) {
+            issue_a(t0);
+            issue_b(t0);
+        }
     }
-    load_gam(gam, sv, ci, h);
     if (warp == 0) umma::tmem_alloc(tslot, 256);
-    __syncthreads();
-    bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
-    if (L < 64) {   // tail rows belong to the next sequence
-        umma::zero_tail_rows(Qs, 64, 0, L);
-        umma::zero_tail_rows(Ks, 64, 0, L);
-        umma::zero_tail_rows(dOs, 64, 0, L);
-        umma::zero_tail_rows(Us, 64, 0, L);
-        __syncthreads();
-    }
-    if (!sv.qkv_tf32) umma::tf32r_inplace(Qs, 2 * 64 * 128);   // Q, K (dO and U arrive rounded)
-    umma::fence_smem_to_async();
+    umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t tQK = tmem, tDOU = tmem + 64, tDQ = tmem, tDK = tmem + 128;
-    if (ok && tid == 0) {
-        umma::mma(tQK, umma::swt(Qs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
-        umma::mma(tDOU, umma::swt(dOs, 64), umma::swt(Us, 64), 64, 64, 128, false);
-        umma::commit(mbar);
-    }
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
-    umma::fence_after_sync();
-    // dO and U are consumed: Q and K come again as MN-major tiles while the
-    // epilogue runs
-    float* Qm = dOs;
-    float* Km = Us;
-    if (ok && tid == 0) {
-        umma::mbar_expect_tx(mbl, 2 * 64 * 128 * 4);
-        umma::tma_rows(Qm, 64, &maps.q_mn, kh, ci.start, mbl);
-        umma::tma_rows(Km, 64, &maps.k_mn, kh, ci.start, mbl);
-    }
     const int win = warp & 3, half = warp >> 2;
-    float* colp = Rm;                  // [4 row windows][64] column sums of R
-    if (ok) {   // 32 columns per warp, all lanes; R row / column sums by shuffles
-        float qk[16], du[16];
-        umma::tmem_ld_m64<4>(umma::tmem_at(tQK, half * 32), qk);
-        umma::tmem_ld_m64<4>(umma::tmem_at(tDOU, half * 32), du);
-        const int rl = umma::frag_row_lo(), cf = umma::frag_col();
-        float rs[2] = {0.f, 0.f}, cs[4][2];
+    const int rl = umma::frag_row_lo(), cf = umma::frag_col();
+    int t = claim[0];
+    bool ok = true;
+    for (int it = 0; t < ntiles; it++) {
+        const ChunkInfo ci = sv.chunks[t % NT];
+        const int h = t / NT, L = ci.len;
+        if (L == 0) break;   // the device check of cu_seqlens failed: every chunk is empty
+        load_gam(gam, sv, ci, h);
+        ok = __syncthreads_and(umma::mbar_wait(mA, it & 1));   // Q, K, dO, U; gam visible
+        if (!ok) break;
+        if (L < 64) {   // tail rows belong to the next sequence
+            umma::zero_tail_rows(Qs, 64, 0, L);
+            umma::zero_tail_rows(Ks, 64, 0, L);
+            umma::zero_tail_rows(dOs, 64, 0, L);
+            umma::zero_tail_rows(Us, 64, 0, L);
+            __syncthreads();
+        }
+        if (!sv.qkv_tf32) umma::tf32r_inplace(Qs, 2 * 64 * 128);   // Q, K
+        umma::fence_smem_to_async();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {
+            umma::mma(tQK, umma::swt(Qs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
+            umma::mma(tDOU, umma::swt(dOs, 64), umma::swt(Us, 64), 64, 64, 128, false);
+            umma::commit(mM);
+            claim[(it + 1) & 1] = atomicAdd(w.dp_next, 1);   // the next tile
+        }
+        ok = __syncthreads_and(umma::mbar_wait(mM, 0));   // the claim is visible too
+        umma::fence_after_sync();
+        if (!ok) break;
+        const int tn = claim[(it + 1) & 1];
+        if (tid == 0 && tn < ntiles) issue_a(tn);   // the swizzled operands are consumed
+        {   // 32 columns per warp, all lanes; R row / column sums by shuffles
+            float qk[16], du[16];
+            umma::tmem_ld_m64<4>(umma::tmem_at(tQK, half * 32), qk);
+            umma::tmem_ld_m64<4>(umma::tmem_at(tDOU, half * 32), du);
+            float rs[2] = {0.f, 0.f}, cs[4][2];
 #pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const int j = half * 32 + 8 * k + cf;
-            cs[k][0] = cs[k][1] = 0.f;
+            for (int k = 0; k < 4; k++) {
+                const int j = half * 32 + 8 * k + cf;
+                cs[k][0] = cs[k][1] = 0.f;
 #pragma unroll
-            for (int hr = 0; hr < 2; hr++) {
-                const int r = rl + 8 * hr;
-                float d[2];
+                for (int hr = 0; hr < 2; hr++) {
+                    const int r = rl + 8 * hr;
+                    float d[2];
+#pragma unroll
+                    for (int e = 0; e < 2; e++) {
+                        const float gm = j + e <= r ? expf(gam[r] - gam[j + e]) : 0.f;
+                        const float x = du[4 * k + 2 * hr + e] * gm;
+                        const float R = x * qk[4 * k + 2 * hr + e];
+                        rs[hr] += R;
+                        cs[k][e] += R;
+                        d[e] = umma::tf32r(x);
+                        dPC[umma::kidx(j + e, r, 64)] = d[e];
+                    }
+                    *reinterpret_cast<float2*>(dPR + umma::kidx(r, j, 64)) = make_float2(d[0], d[1]);
+                }
+            }
+            rs[0] = umma::row_quad_sum(rs[0]);
+            rs[1] = umma::row_quad_sum(rs[1]);
+            if ((lane & 3) == 0) {
+                rpart[half * 64 + rl] = rs[0];
+                rpart[half * 64 + rl + 8] = rs[1];
+            }
+#pragma unroll
+            for (int k = 0; k < 4; k++)
 #pragma unroll
                 for (int e = 0; e < 2; e++) {
-                    const float gm = j + e <= r ? expf(gam[r] - gam[j + e]) : 0.f;
-                    const float x = du[4 * k + 2 * hr + e] * gm;
-                    const float R = x * qk[4 * k + 2 * hr + e];
-                    rs[hr] += R;
-                    cs[k][e] += R;
-                    d[e] = umma::tf32r(x);
-                    dPC[umma::kidx(j + e, r, 64)] = d[e];
+                    const float c = umma::col_oct_sum(cs[k][e]);
+                    if (lane < 4) colp[win * 64 + half * 32 + 8 * k + 2 * lane + e] = c;
                 }
-                *reinterpret_cast<float2*>(dPR + umma::kidx(r, j, 64)) = make_float2(d[0], d[1]);
-            }
         }
-        rs[0] = umma::row_quad_sum(rs[0]);
-        rs[1] = umma::row_quad_sum(rs[1]);
-        if ((lane & 3) == 0) {
-            rpart[half * 64 + rl] = rs[0];
-            rpart[half * 64 + rl + 8] = rs[1];
+        umma::fence_before_sync();
+        ok = __syncthreads_and(umma::mbar_wait(mB, it & 1));   // MN-major Q, K
+        if (!ok) break;
+        if (L < 64) {
+            umma::zero_tail_rows(Qm, 64, 0, L);
+            umma::zero_tail_rows(Km, 64, 0, L);
+            __syncthreads();
         }
-#pragma unroll
-        for (int k = 0; k < 4; k++)
-#pragma unroll
-            for (int e = 0; e < 2; e++) {
-                const float c = umma::col_oct_sum(cs[k][e]);
-                if (lane < 4) colp[win * 64 + half * 32 + 8 * k + 2 * lane + e] = c;
-            }
-    }
-    umma::fence_before_sync();
-    __syncthreads();
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbl, 1));
-    if (L < 64) {
-        umma::zero_tail_rows(Qm, 64, 0, L);
-        umma::zero_tail_rows(Km, 64, 0, L);
+        if (!sv.qkv_tf32) umma::tf32r_inplace(Qm, 2 * 64 * 128);
+        umma::fence_smem_to_async();
         __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {
+            umma::mma(tDQ, umma::kmaj(dPR, 64), umma::mnt(Km), 64, 128, 64, false);
+            umma::mma(tDK, umma::kmaj(dPC, 64), umma::mnt(Qm), 64, 128, 64, false);
+            umma::commit(mM);
+        }
+        if (tid < 64 && tid < L) {   // dgam from R: row sums minus column sums (fixed order)
+            const float cs = (colp[tid] + colp[64 + tid]) + (colp[128 + tid] + colp[192 + tid]);
+            w.dgam2[(int64_t)(ci.start + tid) * hv + h] = (rpart[tid] + rpart[64 + tid]) - cs;
+        }
+        ok = __syncthreads_and(umma::mbar_wait(mM, 1));
+        umma::fence_after_sync();
+        if (!ok) break;
+        if (tid == 0 && tn < ntiles) issue_b(tn);   // the MN-major operands are consumed
+        {   // D_dq, D_dk rows rl, rl + 8 (those inside the chunk) straight to the partials
+            const int64_t o_lo = ((int64_t)(ci.start + rl) * hv + h) * kD;
+            const int64_t o_hi = o_lo + (int64_t)8 * hv * kD;
+            auto put = [&](float* dst, uint32_t tcol) {
+                float v[32];
+                umma::tmem_ld64_m64(umma::tmem_at(tcol, half * 64), v);
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    const int c = half * 64 + 8 * k + cf;
+                    if (rl < L)
+                        *reinterpret_cast<float2*>(dst + o_lo + c) = make_float2(v[4 * k], v[4 * k + 1]);
+                    if (rl + 8 < L)
+                        *reinterpret_cast<float2*>(dst + o_hi + c) =
+                            make_float2(v[4 * k + 2], v[4 * k + 3]);
+                }
+            };
+            put(w.dQv2, tDQ);
+            put(w.dKv2, tDK);
+        }
+        umma::fence_before_sync();
+        __syncthreads();   // tensor memory read before the next tile's products reuse it
+        t = tn;
     }
-    if (!sv.qkv_tf32) umma::tf32r_inplace(Qm, 2 * 64 * 128);
-    umma::fence_smem_to_async();
-    umma::fence_before_sync();
-    __syncthreads();
-    umma::fence_after_sync();
-    if (ok && tid == 0) {
-        umma::mma(tDQ, umma::kmaj(dPR, 64), umma::mnt(Km), 64, 128, 64, false);
-        umma::mma(tDK, umma::kmaj(dPC, 64), umma::mnt(Qm), 64, 128, 64, false);
-        umma::commit(mbar);
-    }
-    if (tid < 64) {   // dgam from R: row sums minus column sums (fixed order)
-        const float cs = (colp[tid] + colp[64 + tid]) + (colp[128 + tid] + colp[192 + tid]);
-        dgl[tid] = (rpart[tid] + rpart[64 + tid]) - cs;
-        if (tid < L) w.dgam2[(int64_t)(ci.start + tid) * hv + h] = dgl[tid];
-    }
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
-    umma::fence_after_sync();
-    // dQ, dK staged as swizzled tiles in the Q / K space, then stored whole
-    if (ok) {
-        float v[32];
-        umma::tmem_ld64_m64(umma::tmem_at(tDQ, half * 64), v);
-        umma::frag_to_sw(Qs, v, half * 64, 1.f, 1.f);
-        umma::tmem_ld64_m64(umma::tmem_at(tDK, half * 64), v);
-        umma::frag_to_sw(Ks, v, half * 64, 1.f, 1.f);
-    } else if (tid == 0) {
-        atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
-    }
-    umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 256);
-    if (!ok) return;
-    if (L == 64) {
-        if (tid == 0) {
-            umma::tma_store_rows(&maps.dQv2, h, ci.start, Qs);
-            umma::tma_store_rows(&maps.dKv2, h, ci.start, Ks);
-            umma::bulk_commit();
-            umma::bulk_wait_read();
-        }
+    if (!ok && tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
+}
+
+// ------------------------------------------------------------------ B2 + B3b in one launch
+// The reverse state pass holds one CTA per (slice, head, sequence) for its whole
+// sequence; for a few long sequences that leaves most SMs free.  One grid: CTAs
+// 0 .. n_state - 1 run the state pass (they come first, so they are resident
+// from the start), the rest run the P / dP tiles (independent of the state pass)
+// and fill the other SMs, then those the state pass frees.  No CTA waits on
+// another.
+constexpr size_t kStateDpSmem = kB2Smem > kDpSmem ? kB2Smem : kDpSmem;
+
+__global__ void __launch_bounds__(256, 1)
+bwd_state_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, int n_state,
+                    const float* dS_final, float* dS_init, FwdSaved sv, BwdScratch w) {
+    const int b = blockIdx.x;
+    if (b < n_state) {
+        const int ns = kD / kSl;
+        bwd_state_cta(maps, b % ns, (b / ns) % hv, b / (ns * hv), hk, hv, dS_final, dS_init, sv, w);
     } else {
-        const int64_t off = ((int64_t)ci.start * hv + h) * kD;
-        umma::store_rows_sw(w.dQv2 + off, (int64_t)hv * kD, Qs, L);
-        umma::store_rows_sw(w.dKv2 + off, (int64_t)hv * kD, Ks, L);
+        bwd_dp_cta(maps, hk, hv, NT, sv, w);
     }
 }
 
@@ -1308,48 +1366,17 @@ __global__ void colsum_stage2_kernel(const float* __restrict__ tmp, float* __res
 // stream and its two events are created once per device; the fork / join
 // sequence is enqueued under a lock, so concurrent calls on one device do not
 // interleave their events.
-namespace {
-struct SideStream {
-    cudaStream_t s = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
-constexpr int kMaxSideDevices = 64;
-std::mutex g_side_mu;
-SideStream g_side[kMaxSideDevices];
-
-// The current device's side stream, or nullptr (then everything runs on the
-// caller's stream).  Called with g_side_mu held.
-SideStream* side_stream() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) return nullptr;
-    SideStream& ss = g_side[dev];
-    if (ss.s == nullptr) {
-        int lo = 0, hi = 0;
-        cudaStream_t s = nullptr;
-        cudaEvent_t f = nullptr, j = nullptr;
-        if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess ||
-            cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, hi) != cudaSuccess)
-            return nullptr;
-        if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
-            cudaStreamDestroy(s);
-            return nullptr;
-        }
-        ss.s = s;
-        ss.fork = f;
-        ss.join = j;
-    }
-    return &ss;
-}
-}  // namespace
 
 template <class IO>
 static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStream_t st) {
+    int nsm = 0;
     {
-        cudaError_t e = smem_attr(bwd_local_kernel, kB1Smem);
-        if (e == cudaSuccess) e = smem_attr(bwd_state_kernel, kB2Smem);
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = smem_attr(bwd_local_kernel, kB1Smem);
+        if (e == cudaSuccess) e = smem_attr(bwd_state_dp_kernel, kStateDpSmem);
         if (e == cudaSuccess) e = smem_attr(bwd_sfacing_kernel, kB3aSmem);
-        if (e == cudaSuccess) e = smem_attr(bwd_dp_kernel, kDpSmem);
         if (e == cudaSuccess) e = smem_attr(bwd_wy_kernel<IO>, kWySmem);
         if (e != cudaSuccess) return e;
     }
@@ -1381,6 +1408,8 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
         if (e == cudaSuccess) e = make_rows_map(&maps.dKv3, w.dKv3, a.hv, a.T, vs);
         if (e == cudaSuccess)
             e = make_rows_map(&maps.dv, a.dqkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C);
+        if (e == cudaSuccess)
+            e = make_rows_map(&maps.S0_mn, a.sv.S0, 1, (int64_t)a.NT * a.hv * kD, kD, true);
         if (e != cudaSuccess) return e;
         const int64_t rows = a.T * a.hv;
         {
@@ -1393,47 +1422,23 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
         GDN_PROF("chunk_bwd_local", st);
         bwd_local_kernel<<<dim3(a.NT, a.hv), 256, kB1Smem, st>>>(maps, a.hk, a.hv, a.sv, w);
     }
-    std::unique_lock<std::mutex> lk(g_side_mu);
-    SideStream* ss = side_stream();
-    if (a.N > 0) {   // reverse state pass, beside the P / dP kernel
-        cudaStream_t sst = st;
-        if (ss != nullptr && cudaEventRecord(ss->fork, st) == cudaSuccess &&
-            cudaStreamWaitEvent(ss->s, ss->fork, 0) == cudaSuccess)
-            sst = ss->s;
-        {
-            GDN_PROF("chunk_bwd_state", sst);
-            bwd_state_kernel<<<dim3(kD / kSl, a.hv, a.N), 256, kB2Smem, sst>>>(
-                maps, a.hk, a.hv, a.dS_final, a.dS_init, a.sv, w);
-        }
-        if (sst != st) {
-            cudaError_t e = cudaEventRecord(ss->join, sst);
-            if (a.NT > 0) {
-                GDN_PROF("chunk_bwd_dp", st);
-                bwd_dp_kernel<<<dim3(a.NT, a.hv), 256, kDpSmem, st>>>(maps, a.hk, a.hv, a.sv, w);
-            }
-            if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ss->join, 0);
-            if (e != cudaSuccess) return e;
-        } else if (a.NT > 0) {
-            GDN_PROF("chunk_bwd_dp", st);
-            bwd_dp_kernel<<<dim3(a.NT, a.hv), 256, kDpSmem, st>>>(maps, a.hk, a.hv, a.sv, w);
+    {
+        // the reverse state pass (CTAs 0 .. n_state - 1) and the P / dP tiles
+        // (persistent CTAs claiming tiles from a counter) in one grid
+        const int n_state = (kD / kSl) * a.hv * a.N;
+        const int n_dp = a.NT > 0 ? min(a.NT * a.hv, nsm) : 0;
+        if (n_state + n_dp > 0) {
+            GDN_PROF("chunk_bwd_state_dp", st);
+            bwd_state_dp_kernel<<<(unsigned)(n_state + n_dp), 256, kStateDpSmem, st>>>(
+                maps, a.hk, a.hv, a.NT, n_state, a.dS_final, a.dS_init, a.sv, w);
         }
     }
-    lk.unlock();
     if (a.NT > 0) {
         {
-            int dev = 0, nsm = 0;
-            cudaError_t e = cudaGetDevice(&dev);
-            if (e == cudaSuccess)
-                e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-            if (e != cudaSuccess) return e;
             GDN_PROF("chunk_bwd_sfacing", st);
             bwd_sfacing_kernel<<<min(a.NT * a.hv, nsm), 256, kB3aSmem, st>>>(maps, a.hk, a.hv,
                                                                                a.NT, a.sv, w);
         }
-        int dev = 0, nsm = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
         GDN_PROF("chunk_bwd_wy", st);
         bwd_wy_kernel<IO><<<min(a.NT * a.hv, nsm), 256, kWySmem, st>>>(
             maps, (const IO*)a.a, (const IO*)a.b, a.A_log, a.dt_bias, a.hk, a.hv, a.NT, a.dqkv,

@@ -313,38 +313,40 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
 }
 
 // ------------------------------------------------------------------ state pass
-// grid (2, Hv, N), 288 threads, one CTA per SM: CTA (slice, head, sequence)
+// grid (2, Hv, N), 320 threads, one CTA per SM: CTA (slice, head, sequence)
 // carries rows a0 .. a0 + 63 (a0 = 64 slice) of the fp32 state S [d_v x d_k]
 // through the sequence's chunks.  With fk_i = e^{gam_L - gam_i} (0 past the
 // chunk's length), a chunk's update S_end = e^{gam_L} S + U^T diag(fk) K with
 // U = U~ - W S^T is, transposed,
 //   S_end^T = e^{gam_L} S^T + M^T S^T + B^T,   M^T = -(diag(fk) K)^T W  (d_k x d_k),
 //                                              B^T = (diag(fk) K)^T U~  (this CTA's columns),
-// so one product per chunk waits on the state: M^T S^T (M = 128, N = 64,
-// K = 128, tcgen05), with M^T read from tensor memory and S^T from shared
-// memory, accumulated onto B^T.  The e^{gam_L} S term is added in fp32: the
-// state lives in registers and never passes through tf32 itself.
+// so one product per chunk waits on the state: M^T S^T (M = 128, K = 128,
+// tcgen05), with M^T read from tensor memory and S^T from shared memory,
+// accumulated onto B^T.  The e^{gam_L} S term is added in fp32: the state lives
+// in registers and never passes through tf32 itself.  That product runs as two
+// halves of 32 rows a (N = 32), each with its own completion and "S ready"
+// barrier: the tensor core computes one half while the state warps update the
+// other, so the chain advances by a half product plus a half update at a time.
 //
 // Four roles, coupled only by mbarriers (one phase per chunk each):
 //  - loader / product thread (warp 9): requests a chunk's K, W, U~ (TMA,
 //    MN-major, two stages, two chunks ahead) and, once the producers have
-//    scaled them, issues the chunk's M^T and B^T products;
+//    scaled them and the state of the chunk before is complete (the chain
+//    product two chunks back done and read, whose tensor-memory buffers they
+//    reuse), issues the chunk's M^T and B^T products;
 //  - producers (warps 0-3): scale K by fk and round U~ in place ("scaled");
 //    once the products are done, round M^T to nearest tf32 in tensor memory
-//    and, once S is ready too, declare "M ready" -- so a chunk's products are
-//    issued only after the chain product two chunks back is complete and read,
-//    whose tensor-memory buffers they reuse; each thread's gate values are
-//    read one chunk ahead;
+//    ("M ready") and scale the next chunk; each thread's gate values are read
+//    one chunk ahead;
 //  - state warps (warps 4-7): thread (warp 4 + q, lane l) holds S[a][b'] for
-//    b' = 32 q + l and all 64 rows a; once a chunk's chain product is done
-//    they update S and write its tf32 copy (the chain's B operand, "S
-//    ready"), then the chunk-start state outputs;
-//  - chain thread (warp 8): issues each chunk's chain product as soon as S
-//    and M are ready.
-// U itself is formed by the output kernel, which holds S0 anyway.  Outputs per
-// chunk: the chunk-start state rounded to tf32 in the swizzled K-major layout
-// (rows a; an operand of the output kernel) and exact in the K-major layout
-// with rows b (for the backward).
+//    b' = 32 q + l and all 64 rows a; once a half of a chunk's chain product is
+//    done they update those 32 rows and write their tf32 copy (the chain's B
+//    operand, "S half ready"), then store the next chunk-start state;
+//  - chain thread (warp 8): issues each half of a chunk's chain product as soon
+//    as M and that half of S are ready.
+// U itself is formed by the output kernel, which holds S0 anyway.  Output per
+// chunk: the chunk-start state rounded to tf32, row-major [a][b] (the output
+// kernel reads it K-major, the backward MN-major, through two tensor maps).
 //
 // Shared memory: S (rows a, swizzled K-major, 64 x 128) 32 KB and two stages
 // of K, W (MN-major, 32 KB each) and the U~ slice (MN-major, 64 x 64, 16 KB).
@@ -353,11 +355,8 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
 constexpr int kStFloats = 64 * 128;
 constexpr int kStageF = 2 * 64 * 128 + 64 * 64;   // K, W, U~ slice
 constexpr int kStateThreads = 320;
-constexpr size_t kStateSmem = sizeof(float) * (kStFloats + 2 * kStageF) + 7 * 8 + 8 + 1024;
+constexpr size_t kStateSmem = sizeof(float) * (kStFloats + 2 * kStageF) + 9 * 8 + 8 + 1024;
 
-__device__ __forceinline__ void named_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
-}
 __device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(umma::saddr(mbar)) : "memory");
 }
@@ -370,12 +369,12 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
     float* St = sm;                    // [64 (a)][128 (b)] swizzled K-major: S, rounded
     float* stage = St + kStFloats;     // [2] x {K, W: [64 (i)][128] MN-major; U~: [64 (i)][64 (a)]}
     uint64_t* mT = reinterpret_cast<uint64_t*>(stage + 2 * kStageF);   // [2] tiles per stage
-    uint64_t* mC = mT + 2;             // chain product done (commit)
-    uint64_t* mP = mC + 1;             // M^T, B^T products done (commit)
+    uint64_t* mC = mT + 2;             // [2] chain product half done (commit)
+    uint64_t* mP = mC + 2;             // M^T, B^T products done (commit)
     uint64_t* bSc = mP + 1;            // chunk scaled (producers)
     uint64_t* bM = bSc + 1;            // M^T rounded (producers)
-    uint64_t* bS = bM + 1;             // S copy written (state warps)
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bS + 1);
+    uint64_t* bS = bM + 1;             // [2] S half copy written (state warps)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bS + 2);
     auto Km = [&](int st) { return stage + st * kStageF; };
     auto Wm = [&](int st) { return stage + st * kStageF + 64 * 128; };
     auto Um = [&](int st) { return stage + st * kStageF + 2 * 64 * 128; };
@@ -385,13 +384,14 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
     const int64_t sbase = ((int64_t)n * hv + h) * kD * kD;
     const int c0 = sv.seq_chunk[n], c1 = sv.seq_chunk[n + 1];
     if (tid == 0) {
-        umma::mbar_init(&mT[0], 1);
-        umma::mbar_init(&mT[1], 1);
-        umma::mbar_init(mC, 1);
+        for (int b = 0; b < 2; b++) {
+            umma::mbar_init(&mT[b], 1);
+            umma::mbar_init(&mC[b], 1);
+            umma::mbar_init(&bS[b], 128);
+        }
         umma::mbar_init(mP, 1);
         umma::mbar_init(bSc, 128);
         umma::mbar_init(bM, 128);
-        umma::mbar_init(bS, 128);
     }
     if (warp == 0) umma::tmem_alloc(tslot, 512);
     umma::fence_before_sync();
@@ -465,42 +465,29 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
             }
             umma::tmem_wait_st();
             umma::fence_before_sync();
-            // "S ready" for chunk c implies chain product c - 1 is complete and its
-            // accumulator read: after "M ready" the next products may reuse both
-            // of chunk c - 1's tensor-memory buffers
-            ok = umma::mbar_wait(bS, it & 1);
             mbar_arrive(bM);
-            if (ok && c + 1 < c1) ok = scale(c + 1);
+            if (c + 1 < c1) ok = scale(c + 1);
         }
     } else if (warp < 8) {
         // ---------------------------------------------------------- state warps
-        const int q = warp - 4, bp = 32 * q + lane, sid = tid - 128;
-        float s[64];   // s[j] = S[j][bp]
+        const int q = warp - 4, bp = 32 * q + lane;
+        float s[64];   // s[j] = S[a0 + j][bp]
 #pragma unroll
         for (int j = 0; j < 64; j++)
             s[j] = S_init ? S_init[sbase + (int64_t)(a0 + j) * kD + bp] : 0.f;
-        // S into St (rounded), "S ready"; then chunk c's start state out: exact
-        // (rows b), and the rounded tile (rows a) as four 8 KB bulk copies --
-        // box x of St (64 rows) is rows a0 .. a0 + 63 of box x of the 128-row tile
-        auto emit = [&](int c) {
+        // rows 32 hf .. 32 hf + 31 into St (rounded), then "S half ready"
+        auto put_half = [&](int hf) {
 #pragma unroll
-            for (int j = 0; j < 64; j++) St[umma::swz(j, bp, 64)] = umma::tf32r(s[j]);
+            for (int j = 0; j < 32; j++)
+                St[umma::swz(32 * hf + j, bp, 64)] = umma::tf32r(s[32 * hf + j]);
             umma::fence_smem_to_async();
-            mbar_arrive(bS);
-            if (c >= c1) return;
-            named_sync(2, 128);
-            if (sid == 0) {
-                float* o = sv.S0 + ((int64_t)c * hv + h) * kD * kD;
+            mbar_arrive(&bS[hf]);
+        };
+        // chunk c's start state out, rounded, row-major (a warp stores 128 bytes of a row)
+        auto put_s0 = [&](int c) {
+            float* o = sv.S0 + ((int64_t)c * hv + h) * kD * kD + (int64_t)a0 * kD + bp;
 #pragma unroll
-                for (int x = 0; x < 4; x++)
-                    umma::bulk_store(o + (x * 128 + a0) * 32, St + x * 64 * 32, 64 * 32 * 4);
-                umma::bulk_commit();
-            }
-            float* ob = sv.S0b + ((int64_t)c * hv + h) * kD * kD;
-#pragma unroll
-            for (int j = 0; j < 64; j += 4)
-                *reinterpret_cast<float4*>(ob + umma::kidx(bp, a0 + j, kD)) =
-                    make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
+            for (int j = 0; j < 64; j++) o[j * kD] = umma::tf32r(s[j]);
         };
         // gam_L of chunk c, read one chunk ahead into a register
         auto gam_last = [&](int c) {
@@ -509,28 +496,30 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
             return sv.gam[(int64_t)h * sv.T + info.start + info.len - 1];
         };
         float gL = gam_last(c0);
-        if (c0 < c1) emit(c0);
+        if (c0 < c1) {
+            put_half(0);
+            put_half(1);
+            put_s0(c0);
+        }
         for (int c = c0; c < c1 && ok; c++) {
             const int it = c - c0;
             const float gL_next = gam_last(c + 1);
-            ok = umma::mbar_wait(mC, it & 1);
-            umma::fence_after_sync();
-            if (!ok) break;
             const float dl = expf(gL);
             gL = gL_next;
 #pragma unroll
-            for (int cc = 0; cc < 64; cc += 32) {   // S <- e^{gam_L} S + (B + S M)
+            for (int hf = 0; hf < 2; hf++) {   // S <- e^{gam_L} S + (B + S M), 32 rows at a time
+                ok = ok && umma::mbar_wait(&mC[hf], it & 1);
+                umma::fence_after_sync();
+                if (!ok) break;
                 float v[32];
-                umma::tmem_ld32(umma::tmem_at(tAcc[it & 1], cc), v);
+                umma::tmem_ld32(umma::tmem_at(tAcc[it & 1], 32 * hf), v);
 #pragma unroll
-                for (int u = 0; u < 32; u++) s[cc + u] = dl * s[cc + u] + v[u];
+                for (int u = 0; u < 32; u++) s[32 * hf + u] = dl * s[32 * hf + u] + v[u];
+                umma::fence_before_sync();
+                put_half(hf);
             }
-            if (sid == 0) umma::bulk_wait_read();   // the last start-state copy has read St
-            umma::fence_before_sync();
-            named_sync(2, 128);
-            emit(c + 1);
+            if (ok && c + 1 < c1) put_s0(c + 1);
         }
-        if (sid == 0) umma::bulk_wait_read();
         if (ok && S_final)
 #pragma unroll
             for (int j = 0; j < 64; j++) S_final[sbase + (int64_t)(a0 + j) * kD + bp] = s[j];
@@ -538,11 +527,16 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         // ---------------------------------------------------------- chain thread
         for (int c = c0; c < c1 && ok; c++) {
             const int it = c - c0;
-            ok = umma::mbar_wait(bS, it & 1) && umma::mbar_wait(bM, it & 1);
-            umma::fence_after_sync();
-            if (!ok) break;
-            umma::mma_ta(tAcc[it & 1], tM[it & 1], umma::swt(St, 64), 128, 64, 128, true);
-            umma::commit(mC);
+            ok = umma::mbar_wait(bM, it & 1);
+#pragma unroll
+            for (int hf = 0; hf < 2; hf++) {
+                ok = ok && umma::mbar_wait(&bS[hf], it & 1);
+                umma::fence_after_sync();
+                if (!ok) break;
+                umma::mma_ta(tAcc[it & 1] + 32 * hf, tM[it & 1], umma::swt(St + 32 * 32 * hf, 64),
+                             128, 32, 128, true);
+                umma::commit(&mC[hf]);
+            }
         }
     } else if (tid == 288) {
         // ---------------------------------------------------------- loader / products
@@ -561,6 +555,9 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         for (int c = c0; c < c1 && ok; c++) {
             const int it = c - c0, st = it & 1;
             ok = umma::mbar_wait(bSc, it & 1);   // chunk c scaled
+            // the state of chunk c - 1 is complete: chain product c - 2 is done and
+            // read, and its accumulator and M^T buffers (this chunk's) are free
+            if (it >= 1) ok = ok && umma::mbar_wait(&bS[1], (it - 1) & 1);
             umma::fence_after_sync();
             if (!ok) break;
             umma::mma(tAcc[st], umma::mnt(Km(st)), umma::mnt(Um(st)), 128, 64, 64, false);  // B^T
@@ -584,8 +581,8 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
 //   P  = D1 (.) e^{gam_i - gam_j} (.) [i >= j]          -- staged K-major
 //   D2 = P U (64 x 128)
 //   O  = D2 + e^{gam_i} D3 ; y = O rsqrt(mean(O^2)+eps) (1+w) gate(z)
-// Shared memory: Q, K, W swizzled 32 KB each, S0 64 KB (swizzled, rows a; one
-// bulk copy), U~ MN-major 32 KB (TMA; U is the B operand of P U, contracted
+// Shared memory: Q, K, W swizzled 32 KB each, S0 64 KB (swizzled, rows a), U~
+// MN-major 32 KB (all by TMA; U is the B operand of P U, contracted
 // over tokens, so U~ arrives MN-major and U is formed in place), P 16 KB.  The
 // next tile's Q, K, W and S0 are requested as soon as the first products are
 // done, its U~ once this tile's O (staged over U) has been stored; its chunk
@@ -634,7 +631,9 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
         umma::tma_rows(Qs, 64, &maps.q, kh, c.start, mA);
         umma::tma_rows(Ks, 64, &maps.k, kh, c.start, mA);
         umma::tma_rows(Ws, 64, &maps.W, h, c.start, mA);
-        umma::bulk_load(Ss, sv.S0 + ((int64_t)(tile % NT) * hv + h) * kD * kD, 128 * 128 * 4, mA);
+        const int s0row = ((tile % NT) * hv + h) * kD;   // S0 tile rows a = 0 .. 127
+        umma::tma_rows(Ss, 128, &maps.S0, 0, s0row, mA);
+        umma::tma_rows(Ss + 64 * 32, 128, &maps.S0, 0, s0row + 64, mA);
     };
     auto issue_u = [&](const ChunkInfo& c, int tile) {   // one thread
         umma::mbar_expect_tx(mU, 64 * 128 * 4);
@@ -850,6 +849,7 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
             e = make_rows_map(&maps.k_mn, a.qkv + (int64_t)a.hk * kD, a.hk, a.T, C, true);
         if (e == cudaSuccess)
             e = make_rows_map(&maps.v_mn, a.qkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C, true);
+        if (e == cudaSuccess) e = make_rows_map(&maps.S0, a.sv.S0, 1, (int64_t)a.NT * a.hv * kD, kD);
         if (e != cudaSuccess) return e;
         int dev = 0, nsm = 0;
         e = cudaGetDevice(&dev);

@@ -57,8 +57,7 @@ struct FwdSaved {
     float* beta;           // [Hv, T]
     float* W;              // [T, Hv, d]
     float* U;              // [T, Hv, d]  (U~ from prep, then U)
-    float* S0;             // [NT, Hv] tiles: chunk-start state, K-major rows a (row = d_v)
-    float* S0b;            // [NT, Hv] tiles: the same state, K-major rows b (row = d_k)
+    float* S0;             // [NT, Hv, d_v, d_k] chunk-start state, row-major, rounded to tf32
     float* Tm;             // [NT * Hv][2][64 * 64] (I + A)^-1 per chunk: K-major T, K-major T^T
     float* o;              // [T, Hv, d] core output (before the norm)
     float* rstd;           // [T, Hv] norm rstd
@@ -77,6 +76,9 @@ struct TileMaps {
     CUtensorMap dQv, dKv, dQv2, dKv2, dKv3;
     CUtensorMap dv;        // v channels of the conv-output gradient [T, C]
     CUtensorMap q_mn, k_mn, v_mn, U_mn, W_mn, dO_mn, dU_mn, dW_mn;
+    // the chunk-start states as rows (chunk Hv + head) 128 + a of 128 columns b:
+    // K-major (rows a; the output kernel) and MN-major (the state-facing kernel)
+    CUtensorMap S0, S0_mn;
 };
 cudaError_t make_rows_map(CUtensorMap* m, const float* base, int heads, int64_t T,
                           int64_t token_stride, bool mn_major = false);
@@ -124,6 +126,7 @@ struct BwdScratch {
     float* dgam;     // [T, Hv] partial dgamma from the state-facing terms
     float* dgam2;    // [T, Hv] the P / dP kernel's dgam terms (it runs beside the state pass)
     float* dgs;      // [T, Hv] dg (per token)
+    int32_t* dp_next;  // tile counter of the P / dP kernel (zeroed before its launch)
     float* nw_part;  // [NT * Hv, d] dnorm_w partials
 };
 

@@ -78,7 +78,8 @@ typedef enum {
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
 /* Problem dimensions.  This build supports d_k = d_v = 128, conv_k = 4,
- * chunk = 64, h_v % h_k == 0, io_dtype F32 or BF16. */
+ * chunk = 64, h_v % h_k == 0, io_dtype F32 or BF16, total_tokens < 2^31 and
+ * (64-token chunks) * h_v * 128 < 2^31 (GDN_ERR_UNSUPPORTED otherwise). */
 typedef struct {
     int32_t num_seqs;      /* N (the decode batch for gdn_recurrent_step)   */
     int64_t total_tokens;  /* T (= N for gdn_recurrent_step)                */

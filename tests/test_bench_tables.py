@@ -26,7 +26,7 @@ def test_traffic_entries_are_known_kernels_with_plausible_ratios():
 
 def test_every_chunk_kernel_has_a_cost():
     for name in ("conv_fwd", "gates", "chunk_prep", "chunk_state_fwd", "chunk_out_fwd",
-                 "chunk_norm_bwd", "chunk_bwd_local", "chunk_bwd_state", "chunk_bwd_dp",
+                 "chunk_norm_bwd", "chunk_bwd_local", "chunk_bwd_state_dp",
                  "chunk_bwd_sfacing", "chunk_bwd_wy", "gva_sum", "conv_bwd"):
         assert bench.kernel_cost(name, W, NT)[1] > 0, name
 
