@@ -313,52 +313,63 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
 }
 
 // ------------------------------------------------------------------ state pass
-// grid (2, Hv, N), 320 threads, one CTA per SM: CTA (slice, head, sequence)
+// grid (2, Hv, N), 448 threads, one CTA per SM: CTA (slice, head, sequence)
 // carries rows a0 .. a0 + 63 (a0 = 64 slice) of the fp32 state S [d_v x d_k]
 // through the sequence's chunks.  With fk_i = e^{gam_L - gam_i} (0 past the
 // chunk's length), a chunk's update S_end = e^{gam_L} S + U^T diag(fk) K with
 // U = U~ - W S^T is, transposed,
 //   S_end^T = e^{gam_L} S^T + M^T S^T + B^T,   M^T = -(diag(fk) K)^T W  (d_k x d_k),
 //                                              B^T = (diag(fk) K)^T U~  (this CTA's columns),
-// so one product per chunk waits on the state: M^T S^T (M = 128, K = 128,
-// tcgen05), with M^T read from tensor memory and S^T from shared memory,
-// accumulated onto B^T.  The e^{gam_L} S term is added in fp32: the state lives
-// in registers and never passes through tf32 itself.  That product runs as two
-// halves of 32 rows a (N = 32), each with its own completion and "S ready"
-// barrier: the tensor core computes one half while the state warps update the
-// other, so the chain advances by a half product plus a half update at a time.
+// so one product per chunk waits on the state: M^T S^T (M = 128, N = 64,
+// K = 128, tcgen05), with M^T read from tensor memory and S^T from shared
+// memory, accumulated onto B^T.  The e^{gam_L} S term is added in fp32: the
+// state lives in registers and never passes through tf32 itself.
 //
-// Four roles, coupled only by mbarriers (one phase per chunk each):
+// A tcgen05.mma of these shapes costs about as much to issue as to run, so the
+// chain product is one 16-instruction product per chunk, and the products that
+// do not depend on the state run ahead of it: M^T in three tensor-memory
+// buffers (chunk c's is computed while the chain works on c - 2 and c - 1),
+// B^T straight into the chain accumulator of its chunk (two buffers).  Each
+// buffer has a "free" barrier (signalled by the chain product or by the state
+// warps once they have read it) and "ready" barriers, one per buffer, so no
+// wait can fall two phases behind its barrier.
+//
+// Five roles, coupled only by mbarriers:
 //  - loader / product thread (warp 9): requests a chunk's K, W, U~ (TMA,
-//    MN-major, two stages, two chunks ahead) and, once the producers have
-//    scaled them and the state of the chunk before is complete (the chain
-//    product two chunks back done and read, whose tensor-memory buffers they
-//    reuse), issues the chunk's M^T and B^T products;
-//  - producers (warps 0-3): scale K by fk and round U~ in place ("scaled");
-//    once the products are done, round M^T to nearest tf32 in tensor memory
-//    ("M ready") and scale the next chunk; each thread's gate values are read
-//    one chunk ahead;
-//  - state warps (warps 4-7): thread (warp 4 + q, lane l) holds S[a][b'] for
-//    b' = 32 q + l and all 64 rows a; once a half of a chunk's chain product is
-//    done they update those 32 rows and write their tf32 copy (the chain's B
-//    operand, "S half ready"), then store the next chunk-start state;
-//  - chain thread (warp 8): issues each half of a chunk's chain product as soon
-//    as M and that half of S are ready.
+//    MN-major, two stages, two chunks ahead); once they are scaled, issues M^T
+//    into its buffer (free once the chain product three chunks back is done)
+//    and B^T into the chunk's accumulator (free once the state warps have read
+//    the result two chunks back); refills the stage when both are done;
+//  - scaling warps (0-3): scale K by fk and round U~ in place, walking the
+//    tiles in shared-memory order (conflict-free); gate values one chunk ahead;
+//  - rounding warps (10-13): once a chunk's M^T is done, round it to nearest
+//    tf32 in tensor memory and negate it ("M ready");
+//  - state warps (4-7): thread (warp 4 + q, lane l) holds S[a][b'] for
+//    b' = 32 q + l and all 64 rows a; once a chunk's chain product is done they
+//    read it (accumulator free), update S and write its tf32 copy (the chain's
+//    B operand, "S ready"), which one thread then stores as the next
+//    chunk-start state (one tensor store);
+//  - chain thread (warp 8): issues a chunk's chain product once M, B^T and S
+//    are ready, and commits it to "chain done" and to its M^T buffer's "free".
 // U itself is formed by the output kernel, which holds S0 anyway.  Output per
 // chunk: the chunk-start state rounded to tf32, row-major [a][b] (the output
 // kernel reads it K-major, the backward MN-major, through two tensor maps).
 //
 // Shared memory: S (rows a, swizzled K-major, 64 x 128) 32 KB and two stages
 // of K, W (MN-major, 32 KB each) and the U~ slice (MN-major, 64 x 64, 16 KB).
-// Tensor memory: two chain accumulators (M = 128, 64 columns) and two M^T
-// tiles (128 columns).
+// Tensor memory: two chain accumulators (M = 128, 64 columns) and three M^T
+// tiles (128 columns): all 512 columns.
 constexpr int kStFloats = 64 * 128;
 constexpr int kStageF = 2 * 64 * 128 + 64 * 64;   // K, W, U~ slice
-constexpr int kStateThreads = 320;
-constexpr size_t kStateSmem = sizeof(float) * (kStFloats + 2 * kStageF) + 9 * 8 + 8 + 1024;
+constexpr int kStateThreads = 448;
+constexpr int kStateBars = 17;
+constexpr size_t kStateSmem = sizeof(float) * (kStFloats + 2 * kStageF) + kStateBars * 8 + 8 + 1024;
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(umma::saddr(mbar)) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
 }
 
 __global__ void __launch_bounds__(kStateThreads, 1)
@@ -369,12 +380,15 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
     float* St = sm;                    // [64 (a)][128 (b)] swizzled K-major: S, rounded
     float* stage = St + kStFloats;     // [2] x {K, W: [64 (i)][128] MN-major; U~: [64 (i)][64 (a)]}
     uint64_t* mT = reinterpret_cast<uint64_t*>(stage + 2 * kStageF);   // [2] tiles per stage
-    uint64_t* mC = mT + 2;             // [2] chain product half done (commit)
-    uint64_t* mP = mC + 2;             // M^T, B^T products done (commit)
-    uint64_t* bSc = mP + 1;            // chunk scaled (producers)
-    uint64_t* bM = bSc + 1;            // M^T rounded (producers)
-    uint64_t* bS = bM + 1;             // [2] S half copy written (state warps)
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bS + 2);
+    uint64_t* mPm = mT + 2;            // [3] M^T product done, per buffer (commit)
+    uint64_t* mPb = mPm + 3;           // B^T product done (commit)
+    uint64_t* mC = mPb + 1;            // chain product done (commit)
+    uint64_t* bSc = mC + 1;            // chunk scaled (scaling warps)
+    uint64_t* bS = bSc + 1;            // S copy written (state warps)
+    uint64_t* bM = bS + 1;             // [3] M^T buffer rounded (rounding warps)
+    uint64_t* fM = bM + 3;             // [3] M^T buffer free (chain product commit)
+    uint64_t* fA = fM + 3;             // [2] accumulator read (state warps)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(fA + 2);
     auto Km = [&](int st) { return stage + st * kStageF; };
     auto Wm = [&](int st) { return stage + st * kStageF + 64 * 128; };
     auto Um = [&](int st) { return stage + st * kStageF + 2 * 64 * 128; };
@@ -384,80 +398,96 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
     const int64_t sbase = ((int64_t)n * hv + h) * kD * kD;
     const int c0 = sv.seq_chunk[n], c1 = sv.seq_chunk[n + 1];
     if (tid == 0) {
-        for (int b = 0; b < 2; b++) {
-            umma::mbar_init(&mT[b], 1);
-            umma::mbar_init(&mC[b], 1);
-            umma::mbar_init(&bS[b], 128);
-        }
-        umma::mbar_init(mP, 1);
+        umma::mbar_init(&mT[0], 1);
+        umma::mbar_init(&mT[1], 1);
+        umma::mbar_init(mPb, 1);
+        umma::mbar_init(mC, 1);
         umma::mbar_init(bSc, 128);
-        umma::mbar_init(bM, 128);
+        umma::mbar_init(bS, 128);
+        for (int b = 0; b < 3; b++) {
+            umma::mbar_init(&mPm[b], 1);
+            umma::mbar_init(&bM[b], 128);
+            umma::mbar_init(&fM[b], 1);
+        }
+        umma::mbar_init(&fA[0], 128);
+        umma::mbar_init(&fA[1], 128);
     }
     if (warp == 0) umma::tmem_alloc(tslot, 512);
     umma::fence_before_sync();
     __syncthreads();   // barriers initialised, tensor memory allocated
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t tAcc[2] = {tmem, tmem + 64}, tM[2] = {tmem + 128, tmem + 256};
+    auto tAcc = [&](int it) { return tmem + 64u * (uint32_t)(it & 1); };
+    auto tM = [&](int it) { return tmem + 128u + 128u * (uint32_t)(it % 3); };
     bool ok = true;
     if (warp < 4) {
-        // ---------------------------------------------------------- producers
-        // thread t scales row i = t / 2 of K (64 columns) and 32 values of U~;
-        // its gate values (gam_i, gam_L) are read one chunk ahead
-        const int i = tid >> 1;
-        auto gates = [&](int c, float& gi, float& gl, int& len) {
-            gi = gl = 0.f;
+        // ---------------------------------------------------------- scaling warps
+        // thread t scales the 16-byte pieces t + 128 q of K (rows (t / 8 + 16 q) % 64,
+        // gate rows r = t / 8 + 16 (q % 4)) and rounds pieces t + 128 q of U~
+        const int r0 = tid >> 3;
+        auto gates = [&](int c, float (&gi)[4], float& gl, int& len) {
+            gl = 0.f;
             len = 0;
+#pragma unroll
+            for (int u = 0; u < 4; u++) gi[u] = 0.f;
             if (c >= c1) return;
             const ChunkInfo info = sv.chunks[c];
             const float* g = sv.gam + (int64_t)h * sv.T + info.start;
-            gi = g[min(i, info.len - 1)];
+#pragma unroll
+            for (int u = 0; u < 4; u++) gi[u] = g[min(r0 + 16 * u, info.len - 1)];
             gl = g[info.len - 1];
             len = info.len;
         };
-        float gi, gl, gi_n, gl_n;
+        float gi[4], gl, gi_n[4], gl_n;
         int len, len_n;
         gates(c0, gi, gl, len);
-        gates(c0 + 1, gi_n, gl_n, len_n);
-        auto scale = [&](int c) {   // chunk c's tiles have been requested
+        for (int c = c0; c < c1 && ok; c++) {
             const int it = c - c0, st = it & 1;
-            const bool got = umma::mbar_wait(&mT[st], (it >> 1) & 1);
-            if (got) {
-                const float f = i < len ? expf(gl - gi) : 0.f;
-                float4 kv[16], uv[8];
-                float* kr = Km(st);
+            gates(c + 1, gi_n, gl_n, len_n);
+            ok = umma::mbar_wait(&mT[st], (it >> 1) & 1);   // chunk c's tiles
+            if (ok) {
+                float f[4];
 #pragma unroll
-                for (int q = 0; q < 16; q++)
-                    kv[q] = *reinterpret_cast<const float4*>(kr + umma::swz_mn(i, 64 * (tid & 1) + 4 * q));
+                for (int u = 0; u < 4; u++) f[u] = r0 + 16 * u < len ? expf(gl - gi[u]) : 0.f;
+                float4* kr = reinterpret_cast<float4*>(Km(st));
+                float4* ur = reinterpret_cast<float4*>(Um(st));
 #pragma unroll
-                for (int q = 0; q < 8; q++)
-                    uv[q] = *reinterpret_cast<const float4*>(Um(st) + 4 * (tid + 128 * q));
+                for (int q0 = 0; q0 < 16; q0 += 8) {
+                    float4 kv[8];
 #pragma unroll
-                for (int q = 0; q < 16; q++)
-                    *reinterpret_cast<float4*>(kr + umma::swz_mn(i, 64 * (tid & 1) + 4 * q)) =
-                        umma::tf32r(make_float4(f * kv[q].x, f * kv[q].y, f * kv[q].z, f * kv[q].w));
+                    for (int q = 0; q < 8; q++) kv[q] = kr[tid + 128 * (q0 + q)];
+#pragma unroll
+                    for (int q = 0; q < 8; q++) {
+                        const float fq = f[(q0 + q) & 3];
+                        kr[tid + 128 * (q0 + q)] = umma::tf32r(
+                            make_float4(fq * kv[q].x, fq * kv[q].y, fq * kv[q].z, fq * kv[q].w));
+                    }
+                }
+                float4 uv[8];
+#pragma unroll
+                for (int q = 0; q < 8; q++) uv[q] = ur[tid + 128 * q];
 #pragma unroll
                 for (int q = 0; q < 8; q++)   // U~ is stored exact (W arrives rounded)
-                    *reinterpret_cast<float4*>(Um(st) + 4 * (tid + 128 * q)) = umma::tf32r(uv[q]);
+                    ur[tid + 128 * q] = umma::tf32r(uv[q]);
             }
             umma::fence_smem_to_async();
             mbar_arrive(bSc);
-            return got;
-        };
-        if (c0 < c1) ok = scale(c0);
-        for (int c = c0; c < c1 && ok; c++) {
-            const int it = c - c0;
-            gi = gi_n;
+#pragma unroll
+            for (int u = 0; u < 4; u++) gi[u] = gi_n[u];
             gl = gl_n;
             len = len_n;
-            gates(c + 2, gi_n, gl_n, len_n);
-            ok = umma::mbar_wait(mP, it & 1);   // chunk c's M^T and B^T are done
+        }
+    } else if (warp >= 10) {
+        // ---------------------------------------------------------- rounding warps
+        for (int c = c0; c < c1 && ok; c++) {
+            const int it = c - c0;
+            ok = umma::mbar_wait(&mPm[it % 3], (it / 3) & 1);   // chunk c's M^T is done
             umma::fence_after_sync();
             if (!ok) break;
 #pragma unroll
             for (int cc = 0; cc < 128; cc += 32) {   // M^T = -(accumulator), rounded
                 float v[32];
-                const uint32_t ta = umma::tmem_at(tM[it & 1], cc);
+                const uint32_t ta = umma::tmem_at(tM(it), cc);
                 umma::tmem_ld32(ta, v);
 #pragma unroll
                 for (int u = 0; u < 32; u++) v[u] = umma::tf32r(-v[u]);
@@ -465,29 +495,30 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
             }
             umma::tmem_wait_st();
             umma::fence_before_sync();
-            mbar_arrive(bM);
-            if (c + 1 < c1) ok = scale(c + 1);
+            mbar_arrive(&bM[it % 3]);
         }
     } else if (warp < 8) {
         // ---------------------------------------------------------- state warps
-        const int q = warp - 4, bp = 32 * q + lane;
+        const int q = warp - 4, bp = 32 * q + lane, sid = tid - 128;
         float s[64];   // s[j] = S[a0 + j][bp]
 #pragma unroll
         for (int j = 0; j < 64; j++)
             s[j] = S_init ? S_init[sbase + (int64_t)(a0 + j) * kD + bp] : 0.f;
-        // rows 32 hf .. 32 hf + 31 into St (rounded), then "S half ready"
-        auto put_half = [&](int hf) {
+        // S into St (rounded), "S ready", then St out as chunk c's start state
+        // (one tensor store of the 64 rows: row-major, rounded)
+        auto put = [&](int c) {
+            if (sid == 0) umma::bulk_wait_read();   // the last store has read St
+            named_sync(2, 128);
 #pragma unroll
-            for (int j = 0; j < 32; j++)
-                St[umma::swz(32 * hf + j, bp, 64)] = umma::tf32r(s[32 * hf + j]);
+            for (int j = 0; j < 64; j++) St[umma::swz(j, bp, 64)] = umma::tf32r(s[j]);
             umma::fence_smem_to_async();
-            mbar_arrive(&bS[hf]);
-        };
-        // chunk c's start state out, rounded, row-major (a warp stores 128 bytes of a row)
-        auto put_s0 = [&](int c) {
-            float* o = sv.S0 + ((int64_t)c * hv + h) * kD * kD + (int64_t)a0 * kD + bp;
-#pragma unroll
-            for (int j = 0; j < 64; j++) o[j * kD] = umma::tf32r(s[j]);
+            mbar_arrive(bS);
+            if (c >= c1) return;
+            named_sync(2, 128);
+            if (sid == 0) {
+                umma::tma_store_rows(&maps.S0, 0, (c * hv + h) * kD + a0, St);
+                umma::bulk_commit();
+            }
         };
         // gam_L of chunk c, read one chunk ahead into a register
         auto gam_last = [&](int c) {
@@ -496,30 +527,27 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
             return sv.gam[(int64_t)h * sv.T + info.start + info.len - 1];
         };
         float gL = gam_last(c0);
-        if (c0 < c1) {
-            put_half(0);
-            put_half(1);
-            put_s0(c0);
-        }
+        if (c0 < c1) put(c0);
         for (int c = c0; c < c1 && ok; c++) {
             const int it = c - c0;
             const float gL_next = gam_last(c + 1);
+            ok = umma::mbar_wait(mC, it & 1);
+            umma::fence_after_sync();
+            if (!ok) break;
             const float dl = expf(gL);
             gL = gL_next;
 #pragma unroll
-            for (int hf = 0; hf < 2; hf++) {   // S <- e^{gam_L} S + (B + S M), 32 rows at a time
-                ok = ok && umma::mbar_wait(&mC[hf], it & 1);
-                umma::fence_after_sync();
-                if (!ok) break;
+            for (int cc = 0; cc < 64; cc += 32) {   // S <- e^{gam_L} S + (B + S M)
                 float v[32];
-                umma::tmem_ld32(umma::tmem_at(tAcc[it & 1], 32 * hf), v);
+                umma::tmem_ld32(umma::tmem_at(tAcc(it), cc), v);
 #pragma unroll
-                for (int u = 0; u < 32; u++) s[32 * hf + u] = dl * s[32 * hf + u] + v[u];
-                umma::fence_before_sync();
-                put_half(hf);
+                for (int u = 0; u < 32; u++) s[cc + u] = dl * s[cc + u] + v[u];
             }
-            if (ok && c + 1 < c1) put_s0(c + 1);
+            umma::fence_before_sync();
+            mbar_arrive(&fA[it & 1]);   // the accumulator is read
+            put(c + 1);
         }
+        if (sid == 0) umma::bulk_wait_read();
         if (ok && S_final)
 #pragma unroll
             for (int j = 0; j < 64; j++) S_final[sbase + (int64_t)(a0 + j) * kD + bp] = s[j];
@@ -527,16 +555,13 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         // ---------------------------------------------------------- chain thread
         for (int c = c0; c < c1 && ok; c++) {
             const int it = c - c0;
-            ok = umma::mbar_wait(bM, it & 1);
-#pragma unroll
-            for (int hf = 0; hf < 2; hf++) {
-                ok = ok && umma::mbar_wait(&bS[hf], it & 1);
-                umma::fence_after_sync();
-                if (!ok) break;
-                umma::mma_ta(tAcc[it & 1] + 32 * hf, tM[it & 1], umma::swt(St + 32 * 32 * hf, 64),
-                             128, 32, 128, true);
-                umma::commit(&mC[hf]);
-            }
+            ok = umma::mbar_wait(&bM[it % 3], (it / 3) & 1) && umma::mbar_wait(mPb, it & 1) &&
+                 umma::mbar_wait(bS, it & 1);
+            umma::fence_after_sync();
+            if (!ok) break;
+            umma::mma_ta(tAcc(it), tM(it), umma::swt(St, 64), 128, 64, 128, true);
+            umma::commit(mC);
+            umma::commit(&fM[it % 3]);
         }
     } else if (tid == 288) {
         // ---------------------------------------------------------- loader / products
@@ -555,15 +580,20 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         for (int c = c0; c < c1 && ok; c++) {
             const int it = c - c0, st = it & 1;
             ok = umma::mbar_wait(bSc, it & 1);   // chunk c scaled
-            // the state of chunk c - 1 is complete: chain product c - 2 is done and
-            // read, and its accumulator and M^T buffers (this chunk's) are free
-            if (it >= 1) ok = ok && umma::mbar_wait(&bS[1], (it - 1) & 1);
+            // M^T buffer it % 3: its last chain product (three chunks back) is done
+            if (it >= 3) ok = ok && umma::mbar_wait(&fM[it % 3], ((it / 3) - 1) & 1);
             umma::fence_after_sync();
             if (!ok) break;
-            umma::mma(tAcc[st], umma::mnt(Km(st)), umma::mnt(Um(st)), 128, 64, 64, false);  // B^T
-            umma::mma(tM[st], umma::mnt(Km(st)), umma::mnt(Wm(st)), 128, 128, 64, false);   // -M^T
-            umma::commit(mP);
-            ok = umma::mbar_wait(mP, it & 1);   // stage st consumed
+            umma::mma(tM(it), umma::mnt(Km(st)), umma::mnt(Wm(st)), 128, 128, 64, false);   // -M^T
+            umma::commit(&mPm[it % 3]);
+            // accumulator it & 1: the state warps have read it (two chunks back)
+            if (it >= 2) ok = umma::mbar_wait(&fA[it & 1], ((it / 2) - 1) & 1);
+            umma::fence_after_sync();
+            if (!ok) break;
+            umma::mma(tAcc(it), umma::mnt(Km(st)), umma::mnt(Um(st)), 128, 64, 64, false);  // B^T
+            umma::commit(mPb);
+            ok = umma::mbar_wait(&mPm[it % 3], (it / 3) & 1) &&
+                 umma::mbar_wait(mPb, it & 1);   // stage consumed
             if (ok) issue(c + 2);
         }
     }
