@@ -257,8 +257,9 @@ MMAS = {
     # Q K^T, Q S0^T, W S0^T (U = U~ - W S0^T), P U
     "chunk_out_fwd": [(64, 64, 128), (64, 128, 128), (64, 128, 128), (64, 128, 64)],
     "chunk_bwd_local": [(64, 64, 128), (64, 128, 64)],                  # K Q^T, P^T dO
-    # reverse state pass (2 row slices) and P / dP tiles, one launch
-    "chunk_bwd_state_dp": [(64, 64, 128), (64, 128, 64), (64, 128, 64)] * 2 +
+    # reverse state pass (2 row slices: K dS^T; B'^T = Q^T e^gam dO - W^T dU_local;
+    # W^T Ub) and P / dP tiles, one launch
+    "chunk_bwd_state_dp": [(64, 64, 128), (128, 64, 64), (128, 64, 64), (128, 64, 64)] * 2 +
                           [(64, 64, 128), (64, 64, 128), (64, 128, 64), (64, 128, 64)],
     "chunk_bwd_sfacing": [(128, 128, 128), (64, 128, 128)],            # [dO; dU] S0, U dS
     "chunk_bwd_wy": [(64, 64, 128)] * 3 + [(64, 256, 64), (64, 64, 64), (64, 64, 64),

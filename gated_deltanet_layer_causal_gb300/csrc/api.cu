@@ -117,6 +117,7 @@ BwdScratch carve_bwd(void* ws, const gdn_dims* d, int NT, int32_t** status, size
     s.dQv2 = c.take<float>(T * H * kD);
     s.dKv2 = c.take<float>(T * H * kD);
     s.dKv3 = c.take<float>(T * H * kD);
+    s.dUl = s.dKv3;   // dU_local until the WY kernel writes its dK part there
     s.dW = c.take<float>(T * H * kD);
     s.dS = c.take<float>((size_t)NT * H * kD * kD);
     s.dgam = c.take<float>(T * H);

@@ -180,228 +180,353 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
     if (!ok) return;
     if (L == 64) {
         if (tid == 0) {
-            umma::tma_store_rows(&maps.dU, h, ci.start, Qs);
+            umma::tma_store_rows(&maps.dKv3, h, ci.start, Qs);   // the dU_local buffer
             umma::bulk_commit();
             umma::bulk_wait_read();
         }
     } else {
-        umma::store_rows_sw(w.dU + ((int64_t)ci.start * hv + h) * kD, (int64_t)hv * kD, Qs, L);
+        umma::store_rows_sw(w.dUl + ((int64_t)ci.start * hv + h) * kD, (int64_t)hv * kD, Qs, L);
     }
 }
 
 // ------------------------------------------------------------------ B2: reverse state pass
-// One CTA per (slice, head, sequence), 256 threads, tcgen05, one CTA per SM
-// (the first CTAs of the combined launch below).  Carries a
-// 64-row slice (rows a) of dS from the last chunk of the sequence to the
-// first, in registers laid out like an M = 64 accumulator, and per chunk:
-//   D1 = K dS_slice^T                          (M = 64 tokens, N = 64, K = 128)
-//   dU = dU_local + diag(fk) D1                -> global (rounded) and Ub = -dU^T
-//   D2 = (diag(e^gam) dO)^T Q + Ub W           (M = 64, N = 128, K = 64 tokens)
-//   dS = e^{gam_L} dS + D2
-// storing dS at every chunk end.  K arrives swizzled, Q and W MN-major (they
-// are contracted over tokens); K and Q are rounded in place.  The dO /
-// dU_local slices are double-buffered; K is refetched as soon as D1 is done,
-// Q and W as soon as D2 is.  Tensor memory: D1 64 columns, D2 128.
+// One CTA per (slice, head, sequence), 320 threads, tcgen05, one CTA per SM (the
+// first CTAs of the combined launch below).  Carries rows a0 .. a0 + 63
+// (a0 = 64 slice) of dS, the gradient of the state S [d_v x d_k], from the last
+// chunk of the sequence to the first.  With dS the gradient at a chunk's end
+// and fk_i = e^{gam_L - gam_i} (0 past the chunk), per chunk:
+//   D1 = K dS^T                                 (M = 64 tokens, N = 64, K = 128)
+//   dU = dU_local + diag(fk) D1                 -> global (rounded)
+//   dS_start^T = e^{gam_L} dS^T + B'^T + W^T Ub,   Ub = -diag(fk) D1,
+//   B'^T = Q^T diag(e^gam) dO - W^T dU_local    (M = 128, N = 64, K = 64 tokens)
+// B' does not depend on dS: it is issued ahead into the chunk's accumulator, so
+// the chain per chunk is D1, the Ub epilogue, one 8-instruction product W^T Ub
+// and the update.  dS lives in registers as the transposed accumulator (thread
+// b holds rows a0 .. a0 + 63 of column b) and is stored at every chunk end as
+// its tf32 copy (D1's B operand), row-major, by one tensor store.
+// Roles, coupled by mbarriers (one phase per chunk, or per use of a buffer; a
+// barrier whose next phase could complete before a waiter has seen the current
+// one is split per buffer, so a parity wait never takes one phase for another):
+//  - scaling warps (0-3): scale the dO slice by e^gam, negate the dU_local
+//    slice, zero both past the chunk; round Q and K when they are not tf32;
+//    then the chunk's dU rows (D1 read from tensor memory, dU_local one chunk
+//    ahead in registers);
+//  - state warps (4-7): the Ub epilogue (D1 read, "Ub ready"), the update
+//    ("accumulator read", "dS ready", the dS store);
+//  - chain thread (warp 8): D1 once dS and K are ready, then W^T Ub once Ub and
+//    B' are; refills K (once D1 is read) and W (once W^T Ub is done);
+//  - product thread (warp 9): B' once Q, dO, dU_local are scaled and the
+//    accumulator is free; then refills Q, dO, dU_local.
+// dU_local arrives from its own buffer, so dU is written without a hazard.
+// Shared memory: dS copy 32 KB, K (K-major) 32 KB, W (MN-major) 2 x 32 KB, Q
+// (MN-major) 32 KB, dO and dU_local slices and Ub (MN-major, 64 x 64) 16 KB
+// each.  Tensor memory: two accumulators (M = 128, 64 columns) and D1 (M = 64,
+// 64 columns).
 constexpr int kSl = 64;
-constexpr int kB2Floats = 3 * 64 * 128 + 4 * 64 * kSl + kSl * kD + 2 * kSl * 64 + 3 * 64;
-constexpr size_t kB2Smem = sizeof(float) * kB2Floats + 5 * 8 + 8 + 1024;
+constexpr int kStateThreadsB = 320;
+constexpr int kB2Floats = 5 * 64 * 128 + 3 * 64 * 64;
+constexpr int kB2Bars = 15;
+constexpr size_t kB2Smem = sizeof(float) * kB2Floats + kB2Bars * 8 + 8 + 1024;
 
 __device__ __forceinline__ void bwd_state_cta(const TileMaps& maps, int sl, int h, int n, int hk,
                                               int hv, const float* dS_final, float* dS_init,
                                               const FwdSaved& sv, const BwdScratch& w) {
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
-    float* Kb = sm;                    // [64][128] swizzled K
-    float* Qm = Kb + 64 * 128;         // [64 (i)][128 (b)] MN-major Q
-    float* Wm = Qm + 64 * 128;         // [64 (i)][128 (b)] MN-major W (arrives rounded)
-    float* dOs = Wm + 64 * 128;        // [2][64][kSl] swizzled dO slices (arrive rounded)
-    float* dUs = dOs + 2 * 64 * kSl;   // [2][64][kSl] swizzled dU_local slices
-    float* dSt = dUs + 2 * 64 * kSl;   // [64 (a)][128 (b)] K-major, rounded
-    float* Ub = dSt + kSl * kD;        // [64 (a)][64 (i)] K-major: -dU, rounded
-    float* dOt = Ub + kSl * 64;        // [64 (a)][64 (i)] K-major: e^{gam_i} dO[i][a], rounded
-    float* gam = dOt + kSl * 64;       // [2][64]
-    float* eg = gam + 2 * 64;
-    uint64_t* mb = reinterpret_cast<uint64_t*>(eg + 64);   // K, Q/W, slices [2], MMA
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mb + 5);
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, half = warp >> 2;
+    float* dSt = sm;                   // [64 (a)][128 (b)] swizzled K-major: dS, rounded
+    float* Kk = dSt + 64 * 128;        // [64 (i)][128 (b)] swizzled K-major K
+    float* Wm0 = Kk + 64 * 128;        // [2][64 (i)][128 (b)] MN-major W (arrives rounded)
+    float* Qm = Wm0 + 2 * 64 * 128;    // [64 (i)][128 (b)] MN-major Q
+    float* dOs = Qm + 64 * 128;        // [64 (i)][64 (a)] MN-major dO slice (arrives rounded)
+    float* dUs = dOs + 64 * 64;        // [64 (i)][64 (a)] MN-major dU_local slice
+    float* Ub = dUs + 64 * 64;         // [64 (i)][64 (a)] MN-major -diag(fk) D1, rounded
+    uint64_t* mA = reinterpret_cast<uint64_t*>(Ub + 64 * 64);   // Q, dO, dU_local loaded
+    uint64_t* mK = mA + 1;             // K loaded
+    uint64_t* mW = mK + 1;             // [2] W loaded
+    uint64_t* bSc = mW + 2;            // Q, dO, dU_local scaled (scaling warps)
+    uint64_t* bK = bSc + 1;            // K ready (scaling warps)
+    uint64_t* mPb = bK + 1;            // [2] B'^T done, per accumulator (commit)
+    uint64_t* mD1 = mPb + 2;           // D1 done (commit)
+    uint64_t* bU = mD1 + 1;            // Ub written (state warps)
+    uint64_t* mC = bU + 1;             // W^T Ub done (commit)
+    uint64_t* bS = mC + 1;             // dS copy written (state warps)
+    uint64_t* fA = bS + 1;             // [2] accumulator read (state warps)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(fA + 2);
+    auto Wm = [&](int it) { return Wm0 + (it & 1) * 64 * 128; };
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int a0 = sl * kSl, kh = h / (hv / hk);
     const int64_t sbase = ((int64_t)n * hv + h) * kD * kD;
-    auto row = [&](const ChunkInfo& c, int r) { return (int64_t)c.start + min(r, c.len - 1); };
-    if (tid == 0)
-        for (int i = 0; i < 5; i++) umma::mbar_init(&mb[i], 1);
+    const int c0 = sv.seq_chunk[n], c1 = sv.seq_chunk[n + 1], nc = c1 - c0;
+    // iteration it works on chunk c1 - 1 - it
+    if (tid == 0) {
+        umma::mbar_init(mA, 1);
+        umma::mbar_init(mK, 1);
+        umma::mbar_init(&mW[0], 1);
+        umma::mbar_init(&mW[1], 1);
+        umma::mbar_init(bSc, 128);
+        umma::mbar_init(bK, 128);
+        umma::mbar_init(&mPb[0], 1);
+        umma::mbar_init(&mPb[1], 1);
+        umma::mbar_init(mD1, 1);
+        umma::mbar_init(bU, 128);
+        umma::mbar_init(mC, 1);
+        umma::mbar_init(bS, 128);
+        umma::mbar_init(&fA[0], 128);
+        umma::mbar_init(&fA[1], 128);
+    }
     if (warp == 0) umma::tmem_alloc(tslot, 256);
-    auto issue_small = [&](const ChunkInfo& c, int slot) {
-        if (tid == 0) {
-            float* o = dOs + slot * 64 * kSl;
-            float* u = dUs + slot * 64 * kSl;
-            umma::mbar_expect_tx(&mb[2 + slot], 2 * 64 * kSl * 4);
-            umma::tma_box(o, &maps.dO, a0, h, c.start, &mb[2 + slot]);
-            umma::tma_box(o + 64 * 32, &maps.dO, a0 + 32, h, c.start, &mb[2 + slot]);
-            umma::tma_box(u, &maps.dU, a0, h, c.start, &mb[2 + slot]);
-            umma::tma_box(u + 64 * 32, &maps.dU, a0 + 32, h, c.start, &mb[2 + slot]);
-        }
-        if (tid < 64)
-            cp_async4(gam + slot * 64 + tid, sv.gam + (int64_t)h * sv.T + row(c, tid), true);
-        cp_async_commit();
-    };
-    auto issue_k = [&](const ChunkInfo& c) {
-        umma::mbar_expect_tx(&mb[0], 64 * 128 * 4);
-        umma::tma_rows(Kb, 64, &maps.k, kh, c.start, &mb[0]);
-    };
-    auto issue_qw = [&](const ChunkInfo& c) {
-        umma::mbar_expect_tx(&mb[1], 2 * 64 * 128 * 4);
-        umma::tma_rows(Qm, 64, &maps.q_mn, kh, c.start, &mb[1]);
-        umma::tma_rows(Wm, 64, &maps.W_mn, h, c.start, &mb[1]);
-    };
-    // this thread's part of the slice: rows a = rl, rl + 8, columns
-    // b = 64 half + 8k + cf, + 1 (k < 8); ds[4k + 2hr + e] = dS[rl + 8hr][b + e]
-    const int rl = umma::frag_row_lo(), cf = umma::frag_col();
-    float ds[32];
-#pragma unroll
-    for (int k = 0; k < 8; k++)
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            const int a = rl + 8 * (e >> 1), b = 64 * half + 8 * k + cf + (e & 1);
-            ds[4 * k + e] = dS_final ? dS_final[sbase + (int64_t)(a0 + a) * kD + b] : 0.f;
-        }
-    auto write_dst = [&]() {
-#pragma unroll
-        for (int k = 0; k < 8; k++)
-#pragma unroll
-            for (int hr = 0; hr < 2; hr++)
-                *reinterpret_cast<float2*>(dSt + umma::kidx(rl + 8 * hr, 64 * half + 8 * k + cf, kD)) =
-                    make_float2(umma::tf32r(ds[4 * k + 2 * hr]), umma::tf32r(ds[4 * k + 2 * hr + 1]));
-    };
-    write_dst();
+    umma::fence_before_sync();
     __syncthreads();   // barriers initialised, tensor memory allocated
     umma::fence_after_sync();
-    const uint32_t tmem = *tslot, tD1 = tmem, tD2 = tmem + 64;
-    const int c0 = sv.seq_chunk[n], c1 = sv.seq_chunk[n + 1];
-    if (c0 < c1) {
-        const ChunkInfo last = sv.chunks[c1 - 1];
-        if (tid == 0) {
-            issue_k(last);
-            issue_qw(last);
-        }
-        issue_small(last, 0);
-    }
+    const uint32_t tmem = *tslot, tD1 = tmem + 128;
+    auto tAcc = [&](int it) { return tmem + 64u * (uint32_t)(it & 1); };
+    auto start_of = [&](int it) { return sv.chunks[c1 - 1 - it].start; };
     bool ok = true;
-    for (int ci = c1 - 1; ci >= c0 && ok; ci--) {
-        const int it = c1 - 1 - ci, slot = it & 1;
-        const ChunkInfo info = sv.chunks[ci];
-        const int L = info.len;
-        const bool more = ci - 1 >= c0;
-        const ChunkInfo prev = more ? sv.chunks[ci - 1] : info;
-        // gradient of the state at this chunk's end, stored as a K-major tile with
-        // rows b (the layout the state-facing kernel feeds to the tensor cores)
-        {
-            float* o = w.dS + ((int64_t)ci * hv + h) * kD * kD;
+    if (warp < 4) {
+        // ---------------------------------------------------------- scaling warps
+        // thread t: 16-byte pieces t + 128 q of the two slices (rows (t / 8 + 16 q) % 64)
+        const int r0 = tid >> 3;
+        auto gates = [&](int it, float (&eg)[4], int& len) {
+            len = 0;
 #pragma unroll
-            for (int k = 0; k < 8; k++)
+            for (int u = 0; u < 4; u++) eg[u] = 0.f;
+            if (it >= nc) return;
+            const ChunkInfo info = sv.chunks[c1 - 1 - it];
+            const float* g = sv.gam + (int64_t)h * sv.T + info.start;
 #pragma unroll
-                for (int e = 0; e < 4; e++)
-                    o[umma::kidx(64 * half + 8 * k + cf + (e & 1), a0 + rl + 8 * (e >> 1), kD)] =
-                        ds[4 * k + e];
-        }
-        cp_async_wait<0>();
-        ok = __syncthreads_and(umma::mbar_wait(&mb[2 + slot], (it >> 1) & 1));
-        if (!ok) break;
-        if (more) issue_small(prev, slot ^ 1);
-        const float* dOc = dOs + slot * 64 * kSl;
-        const float* dUc = dUs + slot * 64 * kSl;
-        const float* gc = gam + slot * 64;
-        if (tid < 64) eg[tid] = tid < L ? expf(gc[tid]) : 0.f;
-        const float gL = gc[L - 1];
-        ok = __syncthreads_and(umma::mbar_wait(&mb[0], it & 1));   // K; eg visible
-        if (!ok) break;
-        if (!sv.qkv_tf32) umma::tf32r_inplace(Kb, 64 * 128);
-        umma::fence_smem_to_async();
-        __syncthreads();
-        umma::fence_after_sync();
-        if (tid == 0) {
-            umma::mma(tD1, umma::swt(Kb, 64), umma::kmaj(dSt, kD), 64, kSl, kD, false);
-            umma::commit(&mb[4]);
-        }
-        // while D1 runs: dOt = (diag(e^gam) dO)^T, and Q rounded once it is in
-        for (int idx = tid; idx < kSl * 16; idx += 256) {
-            const int a = idx & (kSl - 1), i4 = idx / kSl;
-            float4 v = make_float4(dOc[umma::swz(4 * i4, a, 64)] * eg[4 * i4],
-                                   dOc[umma::swz(4 * i4 + 1, a, 64)] * eg[4 * i4 + 1],
-                                   dOc[umma::swz(4 * i4 + 2, a, 64)] * eg[4 * i4 + 2],
-                                   dOc[umma::swz(4 * i4 + 3, a, 64)] * eg[4 * i4 + 3]);
-            *reinterpret_cast<float4*>(dOt + umma::kidx(a, 4 * i4, 64)) = umma::tf32r(v);
-        }
-        ok = umma::mbar_wait(&mb[1], it & 1);   // Q, W
-        if (ok && !sv.qkv_tf32) umma::tf32r_inplace(Qm, 64 * 128);
-        ok = __syncthreads_and(ok && umma::mbar_wait(&mb[4], 0));   // D1
-        umma::fence_after_sync();
-        if (ok && more && tid == 0) issue_k(prev);   // K consumed
-        if (ok) {   // dU = dU_local + fk D1: rows i = rl, rl + 8, columns a = 32 half + 8k + cf, + 1
-            float v[16];
-            umma::tmem_ld_m64<4>(umma::tmem_at(tD1, 32 * half), v);
+            for (int u = 0; u < 4; u++) eg[u] = r0 + 16 * u < info.len ? expf(g[r0 + 16 * u]) : 0.f;
+            len = info.len;
+        };
+        float eg[4], eg_n[4];
+        int len, len_n;
+        gates(0, eg, len);
+        // the dU rows: D1 fragment rows rl, rl + 8 (columns 8 k + cf, + 1), their fk,
+        // and their dU_local values, read one iteration ahead (a load issued when
+        // needed would wait on memory shared with the P / dP tiles)
+        const int rl = umma::frag_row_lo(), cf = umma::frag_col();
+        auto urows = [&](int it, float (&u)[32], float& f_lo, float& f_hi, int& ln, int& st) {
+            f_lo = f_hi = 0.f;
+            ln = st = 0;
+#pragma unroll
+            for (int x = 0; x < 32; x++) u[x] = 0.f;
+            if (it >= nc) return;
+            const ChunkInfo info = sv.chunks[c1 - 1 - it];
+            const float* g = sv.gam + (int64_t)h * sv.T + info.start;
+            const float gL = g[info.len - 1];
+            f_lo = rl < info.len ? expf(gL - g[rl]) : 0.f;
+            f_hi = rl + 8 < info.len ? expf(gL - g[rl + 8]) : 0.f;
+            ln = info.len;
+            st = info.start;
 #pragma unroll
             for (int hr = 0; hr < 2; hr++) {
                 const int i = rl + 8 * hr;
-                const float f = i < L ? expf(gL - gc[i]) : 0.f;
+                if (i >= info.len) continue;
+                const float* src = w.dUl + ((int64_t)(info.start + i) * hv + h) * kD + a0 + cf;
 #pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    const int a = 32 * half + 8 * k + cf;
-                    float u0 = 0.f, u1 = 0.f;
-                    if (i < L) {
-                        const float2 ul = *reinterpret_cast<const float2*>(dUc + umma::swz(i, a, 64));
-                        u0 = ul.x + f * v[4 * k + 2 * hr];
-                        u1 = ul.y + f * v[4 * k + 2 * hr + 1];
-                        // stored rounded: later kernels use dU only as a tensor-core operand
-                        *reinterpret_cast<float2*>(w.dU + ((int64_t)(info.start + i) * hv + h) * kD +
-                                                   a0 + a) = make_float2(umma::tf32r(u0), umma::tf32r(u1));
-                    }
-                    Ub[umma::kidx(a, i, 64)] = umma::tf32r(-u0);
-                    Ub[umma::kidx(a + 1, i, 64)] = umma::tf32r(-u1);
+                for (int k = 0; k < 8; k++) {
+                    const float2 v = *reinterpret_cast<const float2*>(src + 8 * k);
+                    u[4 * k + 2 * hr] = v.x;
+                    u[4 * k + 2 * hr + 1] = v.y;
                 }
             }
-        }
-        umma::fence_smem_to_async();
-        umma::fence_before_sync();
-        __syncthreads();
-        umma::fence_after_sync();
-        if (ok && tid == 0) {
-            umma::mma(tD2, umma::kmaj(dOt, 64), umma::mnt(Qm), 64, kD, 64, false);
-            umma::mma(tD2, umma::kmaj(Ub, 64), umma::mnt(Wm), 64, kD, 64, true);
-            umma::commit(&mb[4]);
-        }
-        ok = __syncthreads_and(ok && umma::mbar_wait(&mb[4], 1));   // D2
-        umma::fence_after_sync();
-        if (!ok) break;
-        if (more && tid == 0) issue_qw(prev);   // Q, W consumed
-        {
-            float v[32];
-            umma::tmem_ld64_m64(umma::tmem_at(tD2, 64 * half), v);
-            const float dl = expf(gL);
+        };
+        float ul[32], uf_lo, uf_hi;
+        int ulen, ustart;
+        urows(0, ul, uf_lo, uf_hi, ulen, ustart);
+        for (int it = 0; it < nc && ok; it++) {
+            gates(it + 1, eg_n, len_n);
+            ok = umma::mbar_wait(mA, it & 1);
+            if (ok) {
+                float4* o4 = reinterpret_cast<float4*>(dOs);
+                float4* u4 = reinterpret_cast<float4*>(dUs);
 #pragma unroll
-            for (int e = 0; e < 32; e++) ds[e] = dl * ds[e] + v[e];
+                for (int q = 0; q < 8; q++) {
+                    const float e = eg[q & 3];
+                    const float m = r0 + 16 * (q & 3) < len ? -1.f : 0.f;
+                    const float4 ov = o4[tid + 128 * q], uv = u4[tid + 128 * q];
+                    o4[tid + 128 * q] = umma::tf32r(make_float4(e * ov.x, e * ov.y, e * ov.z, e * ov.w));
+                    u4[tid + 128 * q] = umma::tf32r(make_float4(m * uv.x, m * uv.y, m * uv.z, m * uv.w));
+                }
+                if (!sv.qkv_tf32) umma::tf32r_inplace(Qm, 64 * 128, 128);
+            }
+            umma::fence_smem_to_async();
+            umma::mbar_arrive(bSc);
+            ok = ok && umma::mbar_wait(mK, it & 1);
+            if (ok && !sv.qkv_tf32) umma::tf32r_inplace(Kk, 64 * 128, 128);
+            umma::fence_smem_to_async();
+            umma::mbar_arrive(bK);
+            // dU = dU_local + diag(fk) D1 for the rows inside the chunk (rounded: only
+            // ever a tensor-core operand later).  D1 is read before this thread's next
+            // "K ready", which the next D1 waits for.
+            ok = __all_sync(0xffffffffu, ok && umma::mbar_wait(mD1, it & 1));   // warp-uniform
+            umma::fence_after_sync();
+            if (ok) {
+                float d1[32];
+                umma::tmem_ld64_m64(umma::tmem_at(tD1, 0), d1);
+#pragma unroll
+                for (int hr = 0; hr < 2; hr++) {
+                    const int i = rl + 8 * hr;
+                    if (i >= ulen) continue;
+                    const float f = hr ? uf_hi : uf_lo;
+                    float* dst = w.dU + ((int64_t)(ustart + i) * hv + h) * kD + a0 + cf;
+#pragma unroll
+                    for (int k = 0; k < 8; k++)
+                        *reinterpret_cast<float2*>(dst + 8 * k) =
+                            make_float2(umma::tf32r(ul[4 * k + 2 * hr] + f * d1[4 * k + 2 * hr]),
+                                        umma::tf32r(ul[4 * k + 2 * hr + 1] + f * d1[4 * k + 2 * hr + 1]));
+                }
+            }
+            umma::fence_before_sync();
+            urows(it + 1, ul, uf_lo, uf_hi, ulen, ustart);
+#pragma unroll
+            for (int u = 0; u < 4; u++) eg[u] = eg_n[u];
+            len = len_n;
         }
-        write_dst();
-        umma::fence_smem_to_async();
-        umma::fence_before_sync();
-        __syncthreads();
+    } else if (warp < 8) {
+        // ---------------------------------------------------------- state warps
+        const int q = warp - 4, bp = 32 * q + lane, sid = tid - 128;
+        const int rl = umma::frag_row_lo(), cf = umma::frag_col();
+        float s[64];   // s[j] = dS[a0 + j][bp]
+#pragma unroll
+        for (int j = 0; j < 64; j++)
+            s[j] = dS_final ? dS_final[sbase + (int64_t)(a0 + j) * kD + bp] : 0.f;
+        // dS into its copy (rounded), "dS ready", then the copy out as the gradient
+        // at the end of chunk c (one tensor store: row-major, rounded)
+        auto put = [&](int c) {
+            if (sid == 0) umma::bulk_wait_read();   // the last store has read the copy
+            umma::named_sync(2, 128);
+#pragma unroll
+            for (int j = 0; j < 64; j++) dSt[umma::swz(j, bp, 64)] = umma::tf32r(s[j]);
+            umma::fence_smem_to_async();
+            umma::mbar_arrive(bS);
+            umma::named_sync(2, 128);
+            if (sid == 0) {
+                umma::tma_store_rows(&maps.dS, 0, (c * hv + h) * kD + a0, dSt);
+                umma::bulk_commit();
+            }
+            __syncwarp();   // converged again before the warp-wide tensor-memory loads
+        };
+        // gate values of iteration it: fk of rows rl, rl + 8 and e^{gam_L}
+        auto gates = [&](int it, float& f_lo, float& f_hi, float& dl, int& len, int& start) {
+            f_lo = f_hi = dl = 0.f;
+            len = start = 0;
+            if (it >= nc) return;
+            const ChunkInfo info = sv.chunks[c1 - 1 - it];
+            const float* g = sv.gam + (int64_t)h * sv.T + info.start;
+            const float gL = g[info.len - 1];
+            f_lo = rl < info.len ? expf(gL - g[rl]) : 0.f;
+            f_hi = rl + 8 < info.len ? expf(gL - g[rl + 8]) : 0.f;
+            dl = expf(gL);
+            len = info.len;
+            start = info.start;
+        };
+        float f_lo, f_hi, dl, f_lo_n, f_hi_n, dl_n;
+        int len, start, len_n, start_n;
+        gates(0, f_lo, f_hi, dl, len, start);
+        if (nc > 0) put(c1 - 1);
+        for (int it = 0; it < nc && ok; it++) {
+            gates(it + 1, f_lo_n, f_hi_n, dl_n, len_n, start_n);
+            ok = __all_sync(0xffffffffu, umma::mbar_wait(mD1, it & 1));   // warp-uniform
+            umma::fence_after_sync();
+            if (!ok) break;
+            float d1[32];   // D1 rows rl, rl + 8, columns 8 k + cf, + 1
+            umma::tmem_ld64_m64(umma::tmem_at(tD1, 0), d1);
+#pragma unroll
+            for (int k = 0; k < 8; k++) {   // Ub = -diag(fk) D1, rounded
+                const int a = 8 * k + cf;
+                *reinterpret_cast<float2*>(Ub + umma::swz_mn(rl, a, 64)) =
+                    make_float2(umma::tf32r(-f_lo * d1[4 * k]), umma::tf32r(-f_lo * d1[4 * k + 1]));
+                *reinterpret_cast<float2*>(Ub + umma::swz_mn(rl + 8, a, 64)) =
+                    make_float2(umma::tf32r(-f_hi * d1[4 * k + 2]), umma::tf32r(-f_hi * d1[4 * k + 3]));
+            }
+
+            umma::fence_smem_to_async();
+            umma::fence_before_sync();
+            umma::mbar_arrive(bU);
+            ok = __all_sync(0xffffffffu, umma::mbar_wait(mC, it & 1));   // warp-uniform
+            umma::fence_after_sync();
+            if (!ok) break;
+#pragma unroll
+            for (int cc = 0; cc < 64; cc += 32) {   // dS <- e^{gam_L} dS + B' + W^T Ub
+                float v[32];
+                umma::tmem_ld32(umma::tmem_at(tAcc(it), cc), v);
+#pragma unroll
+                for (int u = 0; u < 32; u++) s[cc + u] = dl * s[cc + u] + v[u];
+            }
+            umma::fence_before_sync();
+            umma::mbar_arrive(&fA[it & 1]);   // the accumulator is read
+            if (it + 1 < nc) put(c1 - 2 - it);
+            f_lo = f_lo_n;
+            f_hi = f_hi_n;
+            dl = dl_n;
+            len = len_n;
+            start = start_n;
+        }
+        if (sid == 0) umma::bulk_wait_read();
+        if (ok && dS_init)
+#pragma unroll
+            for (int j = 0; j < 64; j++) dS_init[sbase + (int64_t)(a0 + j) * kD + bp] = s[j];
+    } else if (tid == 256) {
+        // ---------------------------------------------------------- chain thread
+        auto issue_k = [&](int it) {
+            umma::mbar_expect_tx(mK, 64 * 128 * 4);
+            umma::tma_rows(Kk, 64, &maps.k, kh, start_of(it), mK);
+        };
+        auto issue_w = [&](int it) {
+            umma::mbar_expect_tx(&mW[it & 1], 64 * 128 * 4);
+            umma::tma_rows(Wm(it), 64, &maps.W_mn, h, start_of(it), &mW[it & 1]);
+        };
+        if (nc > 0) {
+            issue_k(0);
+            issue_w(0);
+        }
+        if (nc > 1) issue_w(1);
+        for (int it = 0; it < nc && ok; it++) {
+            ok = umma::mbar_wait(bS, it & 1);   // dS at this chunk's end: W^T Ub one back is done
+            if (ok && it >= 1 && it + 1 < nc) issue_w(it + 1);   // into that product's W
+            ok = ok && umma::mbar_wait(bK, it & 1);
+            umma::fence_after_sync();
+            if (!ok) break;
+            umma::mma(tD1, umma::swt(Kk, 64), umma::swt(dSt, 64), 64, 64, 128, false);
+            umma::commit(mD1);
+            ok = umma::mbar_wait(bU, it & 1);   // Ub written, D1 read: K is free
+            if (ok && it + 1 < nc) issue_k(it + 1);
+            ok = ok && umma::mbar_wait(&mPb[it & 1], (it >> 1) & 1) &&
+                 umma::mbar_wait(&mW[it & 1], (it >> 1) & 1);
+            umma::fence_after_sync();
+            if (!ok) break;
+            umma::mma(tAcc(it), umma::mnt(Wm(it)), umma::mnt(Ub, 64), 128, 64, 64, true);
+            umma::commit(mC);
+        }
+    } else if (tid == 288) {
+        // ---------------------------------------------------------- product thread
+        auto issue_a = [&](int it) {
+            const int st = start_of(it);
+            umma::mbar_expect_tx(mA, (64 * 128 + 2 * 64 * 64) * 4);
+            umma::tma_rows(Qm, 64, &maps.q_mn, kh, st, mA);
+            umma::tma_box(dOs, &maps.dO_mn, a0, h, st, mA);
+            umma::tma_box(dOs + 64 * 32, &maps.dO_mn, a0 + 32, h, st, mA);
+            umma::tma_box(dUs, &maps.dUl_mn, a0, h, st, mA);
+            umma::tma_box(dUs + 64 * 32, &maps.dUl_mn, a0 + 32, h, st, mA);
+        };
+        if (nc > 0) issue_a(0);
+        for (int it = 0; it < nc && ok; it++) {
+            ok = umma::mbar_wait(bSc, it & 1) && umma::mbar_wait(&mW[it & 1], (it >> 1) & 1);
+            // accumulator it & 1: the state warps have read it (two chunks back)
+            if (it >= 2) ok = ok && umma::mbar_wait(&fA[it & 1], ((it / 2) - 1) & 1);
+            umma::fence_after_sync();
+            if (!ok) break;
+            umma::mma(tAcc(it), umma::mnt(Qm), umma::mnt(dOs, 64), 128, 64, 64, false);
+            umma::mma(tAcc(it), umma::mnt(Wm(it)), umma::mnt(dUs, 64), 128, 64, 64, true);
+            umma::commit(&mPb[it & 1]);
+            ok = umma::mbar_wait(&mPb[it & 1], (it >> 1) & 1);   // Q, dO, dU_local consumed
+            if (ok && it + 1 < nc) issue_a(it + 1);
+        }
     }
     umma::fence_before_sync();
-    __syncthreads();
+    ok = __syncthreads_and(ok);
     if (warp == 0) umma::tmem_free(tmem, 256);
-    if (!ok) {
-        if (tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
-        return;
-    }
-    if (dS_init) {
-#pragma unroll
-        for (int k = 0; k < 8; k++)
-#pragma unroll
-            for (int hr = 0; hr < 2; hr++)
-                *reinterpret_cast<float2*>(dS_init + sbase + (int64_t)(a0 + rl + 8 * hr) * kD +
-                                           64 * half + 8 * k + cf) =
-                    make_float2(ds[4 * k + 2 * hr], ds[4 * k + 2 * hr + 1]);
-    }
+    if (!ok && tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
 }
 
 // ------------------------------------------------------------------ B3a: state-facing terms
@@ -428,8 +553,8 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
     float* sm = umma::align1024(sm_raw);
     float* A1 = sm;                      // [128][128] swizzled: rows 0-63 dO, 64-127 dU
     float* S0m = A1 + 128 * 128;         // [128 (a)][128 (b)] MN-major (arrives rounded)
-    float* DST = S0m + 128 * 128;        // [128 (b)][128 (a)] K-major
-    float* A2 = DST + 128 * 128;         // [64][128] swizzled: U
+    float* DSm = S0m + 128 * 128;        // [128 (a)][128 (b)] MN-major dS (arrives rounded)
+    float* A2 = DSm + 128 * 128;         // [64][128] swizzled: U
     float* eg = A2 + 64 * 128;
     float* fk = eg + 64;
     float* gam = fk + 64;
@@ -454,7 +579,6 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
     if (t >= ntiles) return;
     ChunkInfo ci = sv.chunks[t % NT];
     if (ci.len == 0) return;   // the device check of cu_seqlens failed: every chunk is empty
-    auto sbase = [&](int tile) { return ((int64_t)(tile % NT) * hv + tile / NT) * kD * kD; };
     auto issue_main = [&](const ChunkInfo& c, int tile) {   // one thread
         const int h = tile / NT;
         umma::mbar_expect_tx(mS, 3 * 64 * 128 * 4 + 128 * 128 * 4);
@@ -466,8 +590,10 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
         umma::tma_rows(S0m + 64 * 32, 128, &maps.S0_mn, 0, s0row + 64, mS);
     };
     auto issue_ds = [&](int tile) {   // one thread
+        const int row = ((tile % NT) * hv + tile / NT) * kD;   // dS tile rows a = 0 .. 127
         umma::mbar_expect_tx(mD, 128 * 128 * 4);
-        umma::bulk_load(DST, w.dS + sbase(tile), 128 * 128 * 4, mD);
+        umma::tma_rows(DSm, 128, &maps.dS_mn, 0, row, mD);
+        umma::tma_rows(DSm + 64 * 32, 128, &maps.dS_mn, 0, row + 64, mD);
     };
     auto gam_of = [&](const ChunkInfo& c, int tile) {
         return tid < 64 ? sv.gam[(int64_t)(tile / NT) * sv.T + c.start + min(tid, c.len - 1)] : 0.f;
@@ -499,23 +625,18 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
             umma::zero_tail_rows(A1, 128, 64, L);
             umma::zero_tail_rows(A2, 64, 0, L);
         }
-        {   // <dS, S0> over the staged tiles, before dS is rounded
+        {   // <dS, S0> over the staged tiles (same layout)
             float dot = 0.f;
-            for (int i = tid; i < 128 * 128; i += 256) {
-                const int a = i >> 7, b = i & 127;
-                dot += S0m[umma::swz_mn(a, b, 128)] * DST[umma::kidx(b, a, 128)];
-            }
+            for (int i = tid; i < 128 * 128; i += 256) dot += S0m[i] * DSm[i];
             dot = warp_sum(dot);
             if (lane == 0) red[warp] = dot;
         }
-        __syncthreads();
-        umma::tf32r_inplace(DST, 128 * 128);   // dS^T (dO, dU, U and S0 arrive rounded)
         umma::fence_smem_to_async();
-        __syncthreads();
+        __syncthreads();   // (dO, dU, U, S0 and dS arrive rounded)
         umma::fence_after_sync();
         if (tid == 0) {
             umma::mma(tmem, umma::swt(A1, 128), umma::mnt(S0m, 128), 128, 128, 128, false);
-            umma::mma(tmem + 128, umma::swt(A2, 64), umma::kmaj(DST, 128), 64, 128, 128, false);
+            umma::mma(tmem + 128, umma::swt(A2, 64), umma::mnt(DSm, 128), 64, 128, 128, false);
             umma::commit(mbar);
         }
         if (tid < 64) {
@@ -650,6 +771,8 @@ constexpr size_t kDpSmem = sizeof(float) * (kDpFloats + 4 * 64 + 2 * 64 + 64) + 
 
 __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv, int NT,
                                            const FwdSaved& sv, const BwdScratch& w) {
+    // 256 threads (warps 0-7) take part; the launch's other warps leave at once
+    if (threadIdx.x >= 256) return;
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
     float* Qs = sm;                    // [64][128] swizzled
@@ -701,7 +824,7 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
     }
     if (warp == 0) umma::tmem_alloc(tslot, 256);
     umma::fence_before_sync();
-    __syncthreads();
+    umma::named_sync(1, 256);
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t tQK = tmem, tDOU = tmem + 64, tDQ = tmem, tDK = tmem + 128;
@@ -714,18 +837,18 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         const int h = t / NT, L = ci.len;
         if (L == 0) break;   // the device check of cu_seqlens failed: every chunk is empty
         load_gam(gam, sv, ci, h);
-        ok = __syncthreads_and(umma::mbar_wait(mA, it & 1));   // Q, K, dO, U; gam visible
+        ok = umma::named_sync_and(1, 256, umma::mbar_wait(mA, it & 1));   // Q, K, dO, U; gam visible
         if (!ok) break;
         if (L < 64) {   // tail rows belong to the next sequence
-            umma::zero_tail_rows(Qs, 64, 0, L);
-            umma::zero_tail_rows(Ks, 64, 0, L);
-            umma::zero_tail_rows(dOs, 64, 0, L);
-            umma::zero_tail_rows(Us, 64, 0, L);
-            __syncthreads();
+            umma::zero_tail_rows(Qs, 64, 0, L, 256);
+            umma::zero_tail_rows(Ks, 64, 0, L, 256);
+            umma::zero_tail_rows(dOs, 64, 0, L, 256);
+            umma::zero_tail_rows(Us, 64, 0, L, 256);
+            umma::named_sync(1, 256);
         }
-        if (!sv.qkv_tf32) umma::tf32r_inplace(Qs, 2 * 64 * 128);   // Q, K
+        if (!sv.qkv_tf32) umma::tf32r_inplace(Qs, 2 * 64 * 128, 256);   // Q, K
         umma::fence_smem_to_async();
-        __syncthreads();
+        umma::named_sync(1, 256);
         umma::fence_after_sync();
         if (tid == 0) {
             umma::mma(tQK, umma::swt(Qs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
@@ -733,7 +856,7 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
             umma::commit(mM);
             claim[(it + 1) & 1] = atomicAdd(w.dp_next, 1);   // the next tile
         }
-        ok = __syncthreads_and(umma::mbar_wait(mM, 0));   // the claim is visible too
+        ok = umma::named_sync_and(1, 256, umma::mbar_wait(mM, 0));   // the claim is visible too
         umma::fence_after_sync();
         if (!ok) break;
         const int tn = claim[(it + 1) & 1];
@@ -779,16 +902,16 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
                 }
         }
         umma::fence_before_sync();
-        ok = __syncthreads_and(umma::mbar_wait(mB, it & 1));   // MN-major Q, K
+        ok = umma::named_sync_and(1, 256, umma::mbar_wait(mB, it & 1));   // MN-major Q, K
         if (!ok) break;
         if (L < 64) {
-            umma::zero_tail_rows(Qm, 64, 0, L);
-            umma::zero_tail_rows(Km, 64, 0, L);
-            __syncthreads();
+            umma::zero_tail_rows(Qm, 64, 0, L, 256);
+            umma::zero_tail_rows(Km, 64, 0, L, 256);
+            umma::named_sync(1, 256);
         }
-        if (!sv.qkv_tf32) umma::tf32r_inplace(Qm, 2 * 64 * 128);
+        if (!sv.qkv_tf32) umma::tf32r_inplace(Qm, 2 * 64 * 128, 256);
         umma::fence_smem_to_async();
-        __syncthreads();
+        umma::named_sync(1, 256);
         umma::fence_after_sync();
         if (tid == 0) {
             umma::mma(tDQ, umma::kmaj(dPR, 64), umma::mnt(Km), 64, 128, 64, false);
@@ -799,7 +922,7 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
             const float cs = (colp[tid] + colp[64 + tid]) + (colp[128 + tid] + colp[192 + tid]);
             w.dgam2[(int64_t)(ci.start + tid) * hv + h] = (rpart[tid] + rpart[64 + tid]) - cs;
         }
-        ok = __syncthreads_and(umma::mbar_wait(mM, 1));
+        ok = umma::named_sync_and(1, 256, umma::mbar_wait(mM, 1));
         umma::fence_after_sync();
         if (!ok) break;
         if (tid == 0 && tn < ntiles) issue_b(tn);   // the MN-major operands are consumed
@@ -823,25 +946,25 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
             put(w.dKv2, tDK);
         }
         umma::fence_before_sync();
-        __syncthreads();   // tensor memory read before the next tile's products reuse it
+        umma::named_sync(1, 256);   // tensor memory read before the next tile's products reuse it
         t = tn;
     }
     umma::fence_before_sync();
-    __syncthreads();
+    umma::named_sync(1, 256);
     if (warp == 0) umma::tmem_free(tmem, 256);
     if (!ok && tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
 }
 
 // ------------------------------------------------------------------ B2 + B3b in one launch
 // The reverse state pass holds one CTA per (slice, head, sequence) for its whole
-// sequence; for a few long sequences that leaves most SMs free.  One grid: CTAs
-// 0 .. n_state - 1 run the state pass (they come first, so they are resident
-// from the start), the rest run the P / dP tiles (independent of the state pass)
-// and fill the other SMs, then those the state pass frees.  No CTA waits on
-// another.
+// sequence; for a few long sequences that leaves most SMs free.  One grid of
+// 320-thread CTAs: CTAs 0 .. n_state - 1 run the state pass (they come first,
+// so they are resident from the start), the rest run the P / dP tiles
+// (independent of the state pass, on 256 of the threads) and fill the other
+// SMs, then those the state pass frees.  No CTA waits on another.
 constexpr size_t kStateDpSmem = kB2Smem > kDpSmem ? kB2Smem : kDpSmem;
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kStateThreadsB, 1)
 bwd_state_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, int n_state,
                     const float* dS_final, float* dS_init, FwdSaved sv, BwdScratch w) {
     const int b = blockIdx.x;
@@ -1410,6 +1533,10 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
             e = make_rows_map(&maps.dv, a.dqkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C);
         if (e == cudaSuccess)
             e = make_rows_map(&maps.S0_mn, a.sv.S0, 1, (int64_t)a.NT * a.hv * kD, kD, true);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dS, w.dS, 1, (int64_t)a.NT * a.hv * kD, kD);
+        if (e == cudaSuccess)
+            e = make_rows_map(&maps.dS_mn, w.dS, 1, (int64_t)a.NT * a.hv * kD, kD, true);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dUl_mn, w.dUl, a.hv, a.T, vs, true);
         if (e != cudaSuccess) return e;
         const int64_t rows = a.T * a.hv;
         {
@@ -1429,7 +1556,7 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
         const int n_dp = a.NT > 0 ? min(a.NT * a.hv, nsm) : 0;
         if (n_state + n_dp > 0) {
             GDN_PROF("chunk_bwd_state_dp", st);
-            bwd_state_dp_kernel<<<(unsigned)(n_state + n_dp), 256, kStateDpSmem, st>>>(
+            bwd_state_dp_kernel<<<(unsigned)(n_state + n_dp), kStateThreadsB, kStateDpSmem, st>>>(
                 maps, a.hk, a.hv, a.NT, n_state, a.dS_final, a.dS_init, a.sv, w);
         }
     }

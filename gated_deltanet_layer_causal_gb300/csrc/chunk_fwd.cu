@@ -330,20 +330,22 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
 // do not depend on the state run ahead of it: M^T in three tensor-memory
 // buffers (chunk c's is computed while the chain works on c - 2 and c - 1),
 // B^T straight into the chain accumulator of its chunk (two buffers).  Each
-// buffer has a "free" barrier (signalled by the chain product or by the state
-// warps once they have read it) and "ready" barriers, one per buffer, so no
-// wait can fall two phases behind its barrier.
+// buffer (and each stage) has its own "free" and "ready" barriers, so that the
+// phase after the one a thread waits for cannot complete before that thread has
+// passed its wait (a parity wait would otherwise take the newer phase for the
+// awaited one).
 //
 // Five roles, coupled only by mbarriers:
-//  - loader / product thread (warp 9): requests a chunk's K, W, U~ (TMA,
-//    MN-major, two stages, two chunks ahead); once they are scaled, issues M^T
+//  - product thread (warp 9): once a chunk's K, W, U~ are scaled, issues M^T
 //    into its buffer (free once the chain product three chunks back is done)
 //    and B^T into the chunk's accumulator (free once the state warps have read
-//    the result two chunks back); refills the stage when both are done;
+//    the result two chunks back);
 //  - scaling warps (0-3): scale K by fk and round U~ in place, walking the
 //    tiles in shared-memory order (conflict-free); gate values one chunk ahead;
 //  - rounding warps (10-13): once a chunk's M^T is done, round it to nearest
-//    tf32 in tensor memory and negate it ("M ready");
+//    tf32 in tensor memory and negate it ("M ready"); one of them requests
+//    each chunk's K, W, U~ (TMA, MN-major, two stages, two chunks ahead):
+//    chunk c + 2 into chunk c's stage once both products of chunk c are done;
 //  - state warps (4-7): thread (warp 4 + q, lane l) holds S[a][b'] for
 //    b' = 32 q + l and all 64 rows a; once a chunk's chain product is done they
 //    read it (accumulator free), update S and write its tf32 copy (the chain's
@@ -362,15 +364,9 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
 constexpr int kStFloats = 64 * 128;
 constexpr int kStageF = 2 * 64 * 128 + 64 * 64;   // K, W, U~ slice
 constexpr int kStateThreads = 448;
-constexpr int kStateBars = 17;
+constexpr int kStateBars = 19;
 constexpr size_t kStateSmem = sizeof(float) * (kStFloats + 2 * kStageF) + kStateBars * 8 + 8 + 1024;
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(umma::saddr(mbar)) : "memory");
-}
-__device__ __forceinline__ void named_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
-}
 
 __global__ void __launch_bounds__(kStateThreads, 1)
 state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const float* S_init,
@@ -381,10 +377,10 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
     float* stage = St + kStFloats;     // [2] x {K, W: [64 (i)][128] MN-major; U~: [64 (i)][64 (a)]}
     uint64_t* mT = reinterpret_cast<uint64_t*>(stage + 2 * kStageF);   // [2] tiles per stage
     uint64_t* mPm = mT + 2;            // [3] M^T product done, per buffer (commit)
-    uint64_t* mPb = mPm + 3;           // B^T product done (commit)
-    uint64_t* mC = mPb + 1;            // chain product done (commit)
-    uint64_t* bSc = mC + 1;            // chunk scaled (scaling warps)
-    uint64_t* bS = bSc + 1;            // S copy written (state warps)
+    uint64_t* mPb = mPm + 3;           // [2] B^T product done, per accumulator (commit)
+    uint64_t* mC = mPb + 2;            // chain product done (commit)
+    uint64_t* bSc = mC + 1;            // [2] chunk scaled, per stage (scaling warps)
+    uint64_t* bS = bSc + 2;            // S copy written (state warps)
     uint64_t* bM = bS + 1;             // [3] M^T buffer rounded (rounding warps)
     uint64_t* fM = bM + 3;             // [3] M^T buffer free (chain product commit)
     uint64_t* fA = fM + 3;             // [2] accumulator read (state warps)
@@ -400,9 +396,11 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
     if (tid == 0) {
         umma::mbar_init(&mT[0], 1);
         umma::mbar_init(&mT[1], 1);
-        umma::mbar_init(mPb, 1);
+        umma::mbar_init(&mPb[0], 1);
+        umma::mbar_init(&mPb[1], 1);
         umma::mbar_init(mC, 1);
-        umma::mbar_init(bSc, 128);
+        umma::mbar_init(&bSc[0], 128);
+        umma::mbar_init(&bSc[1], 128);
         umma::mbar_init(bS, 128);
         for (int b = 0; b < 3; b++) {
             umma::mbar_init(&mPm[b], 1);
@@ -471,7 +469,7 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
                     ur[tid + 128 * q] = umma::tf32r(uv[q]);
             }
             umma::fence_smem_to_async();
-            mbar_arrive(bSc);
+            umma::mbar_arrive(&bSc[st]);
 #pragma unroll
             for (int u = 0; u < 4; u++) gi[u] = gi_n[u];
             gl = gl_n;
@@ -479,9 +477,26 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         }
     } else if (warp >= 10) {
         // ---------------------------------------------------------- rounding warps
+        // thread 320 also requests each chunk's K, W, U~ (TMA, MN-major, two
+        // stages): chunk c + 2 into chunk c's stage once both its products are done
+        auto issue = [&](int c, int start) {
+            const int st = (c - c0) & 1;
+            umma::mbar_expect_tx(&mT[st], kStageF * 4);
+            umma::tma_rows(Km(st), 64, &maps.k_mn, kh, start, &mT[st]);
+            umma::tma_rows(Wm(st), 64, &maps.W_mn, h, start, &mT[st]);
+            umma::tma_box(Um(st), &maps.U_mn, a0, h, start, &mT[st]);
+            umma::tma_box(Um(st) + 64 * 32, &maps.U_mn, a0 + 32, h, start, &mT[st]);
+        };
+        const bool loader = tid == 320;
+        if (loader && c0 < c1) issue(c0, sv.chunks[c0].start);
+        if (loader && c0 + 1 < c1) issue(c0 + 1, sv.chunks[c0 + 1].start);
+        int start_n = loader && c0 + 2 < c1 ? sv.chunks[c0 + 2].start : 0;   // one chunk ahead
+        __syncwarp();   // converged again before the warp-wide tensor-memory accesses
         for (int c = c0; c < c1 && ok; c++) {
             const int it = c - c0;
-            ok = umma::mbar_wait(&mPm[it % 3], (it / 3) & 1);   // chunk c's M^T is done
+            const int start = start_n;
+            if (loader) start_n = c + 3 < c1 ? sv.chunks[c + 3].start : 0;
+            ok = __all_sync(0xffffffffu, umma::mbar_wait(&mPm[it % 3], (it / 3) & 1));   // M^T done
             umma::fence_after_sync();
             if (!ok) break;
 #pragma unroll
@@ -495,7 +510,12 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
             }
             umma::tmem_wait_st();
             umma::fence_before_sync();
-            mbar_arrive(&bM[it % 3]);
+            umma::mbar_arrive(&bM[it % 3]);
+            if (loader && c + 2 < c1) {   // B^T of chunk c done too: its stage is free
+                ok = umma::mbar_wait(&mPb[it & 1], (it >> 1) & 1);
+                if (ok) issue(c + 2, start);
+            }
+            ok = __all_sync(0xffffffffu, ok);   // (converged again)
         }
     } else if (warp < 8) {
         // ---------------------------------------------------------- state warps
@@ -508,17 +528,18 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         // (one tensor store of the 64 rows: row-major, rounded)
         auto put = [&](int c) {
             if (sid == 0) umma::bulk_wait_read();   // the last store has read St
-            named_sync(2, 128);
+            umma::named_sync(2, 128);
 #pragma unroll
             for (int j = 0; j < 64; j++) St[umma::swz(j, bp, 64)] = umma::tf32r(s[j]);
             umma::fence_smem_to_async();
-            mbar_arrive(bS);
+            umma::mbar_arrive(bS);
             if (c >= c1) return;
-            named_sync(2, 128);
+            umma::named_sync(2, 128);
             if (sid == 0) {
                 umma::tma_store_rows(&maps.S0, 0, (c * hv + h) * kD + a0, St);
                 umma::bulk_commit();
             }
+            __syncwarp();   // converged again before the warp-wide tensor-memory loads
         };
         // gam_L of chunk c, read one chunk ahead into a register
         auto gam_last = [&](int c) {
@@ -531,7 +552,7 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         for (int c = c0; c < c1 && ok; c++) {
             const int it = c - c0;
             const float gL_next = gam_last(c + 1);
-            ok = umma::mbar_wait(mC, it & 1);
+            ok = __all_sync(0xffffffffu, umma::mbar_wait(mC, it & 1));   // warp-uniform
             umma::fence_after_sync();
             if (!ok) break;
             const float dl = expf(gL);
@@ -544,7 +565,7 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
                 for (int u = 0; u < 32; u++) s[cc + u] = dl * s[cc + u] + v[u];
             }
             umma::fence_before_sync();
-            mbar_arrive(&fA[it & 1]);   // the accumulator is read
+            umma::mbar_arrive(&fA[it & 1]);   // the accumulator is read
             put(c + 1);
         }
         if (sid == 0) umma::bulk_wait_read();
@@ -555,8 +576,8 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
         // ---------------------------------------------------------- chain thread
         for (int c = c0; c < c1 && ok; c++) {
             const int it = c - c0;
-            ok = umma::mbar_wait(&bM[it % 3], (it / 3) & 1) && umma::mbar_wait(mPb, it & 1) &&
-                 umma::mbar_wait(bS, it & 1);
+            ok = umma::mbar_wait(&bM[it % 3], (it / 3) & 1) &&
+                 umma::mbar_wait(&mPb[it & 1], (it >> 1) & 1) && umma::mbar_wait(bS, it & 1);
             umma::fence_after_sync();
             if (!ok) break;
             umma::mma_ta(tAcc(it), tM(it), umma::swt(St, 64), 128, 64, 128, true);
@@ -564,22 +585,10 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
             umma::commit(&fM[it % 3]);
         }
     } else if (tid == 288) {
-        // ---------------------------------------------------------- loader / products
-        auto issue = [&](int c) {
-            if (c >= c1) return;
-            const int st = (c - c0) & 1;
-            const ChunkInfo info = sv.chunks[c];
-            umma::mbar_expect_tx(&mT[st], kStageF * 4);
-            umma::tma_rows(Km(st), 64, &maps.k_mn, kh, info.start, &mT[st]);
-            umma::tma_rows(Wm(st), 64, &maps.W_mn, h, info.start, &mT[st]);
-            umma::tma_box(Um(st), &maps.U_mn, a0, h, info.start, &mT[st]);
-            umma::tma_box(Um(st) + 64 * 32, &maps.U_mn, a0 + 32, h, info.start, &mT[st]);
-        };
-        issue(c0);
-        issue(c0 + 1);
+        // ---------------------------------------------------------- products
         for (int c = c0; c < c1 && ok; c++) {
             const int it = c - c0, st = it & 1;
-            ok = umma::mbar_wait(bSc, it & 1);   // chunk c scaled
+            ok = umma::mbar_wait(&bSc[st], (it >> 1) & 1);   // chunk c scaled
             // M^T buffer it % 3: its last chain product (three chunks back) is done
             if (it >= 3) ok = ok && umma::mbar_wait(&fM[it % 3], ((it / 3) - 1) & 1);
             umma::fence_after_sync();
@@ -591,10 +600,7 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
             umma::fence_after_sync();
             if (!ok) break;
             umma::mma(tAcc(it), umma::mnt(Km(st)), umma::mnt(Um(st)), 128, 64, 64, false);  // B^T
-            umma::commit(mPb);
-            ok = umma::mbar_wait(&mPm[it % 3], (it / 3) & 1) &&
-                 umma::mbar_wait(mPb, it & 1);   // stage consumed
-            if (ok) issue(c + 2);
+            umma::commit(&mPb[it & 1]);
         }
     }
     umma::fence_before_sync();

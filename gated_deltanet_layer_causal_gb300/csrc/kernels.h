@@ -79,6 +79,8 @@ struct TileMaps {
     // the chunk-start states as rows (chunk Hv + head) 128 + a of 128 columns b:
     // K-major (rows a; the output kernel) and MN-major (the state-facing kernel)
     CUtensorMap S0, S0_mn;
+    // the gradients of the chunk-end states (same rows), and dU_local MN-major
+    CUtensorMap dS, dS_mn, dUl_mn;
 };
 cudaError_t make_rows_map(CUtensorMap* m, const float* base, int heads, int64_t T,
                           int64_t token_stride, bool mn_major = false);
@@ -116,7 +118,10 @@ struct BwdScratch {
     int32_t* status; // device status word of the backward workspace
     float* dO;       // [T, Hv, d]
     float* dU;       // [T, Hv, d]
-    float* dS;       // [NT, Hv, d_k, d_v] gradient of the state at each chunk end, transposed
+    float* dS;       // [NT, Hv, d_v, d_k] gradient of the state at each chunk end, row-major,
+                     // rounded to tf32
+    float* dUl;      // [T, Hv, d] dU_local (the local kernel's part of dU); shares dKv3's
+                     // memory, which the WY kernel writes only after the state pass
     float* dQv;      // [T, Hv, d] per v-head dq^, state-facing part
     float* dKv;      // [T, Hv, d] per v-head dk^, state-facing part
     float* dQv2;     // [T, Hv, d] per v-head dq^, P / dP part

@@ -170,6 +170,28 @@ __device__ __forceinline__ void mma_ta(uint32_t d_tmem, uint32_t a_tmem, const O
     }
 }
 
+// Named barrier `id` over the first n threads of the CTA (n % 32 == 0; the
+// threads of a role that syncs without the rest).
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+}
+// The same with an AND reduction of v over the n threads.
+__device__ __forceinline__ bool named_sync_and(int id, int n, bool v) {
+    int r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.s32 p, %1, 0;\nbar.red.and.pred q, %2, %3, p;\n"
+        "selp.s32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((int)v), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+// Plain arrive (count 1) on `mbar`.
+__device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(saddr(mbar)) : "memory");
+}
+
 // Arrive on `mbar` once every MMA this thread issued so far has completed.
 __device__ __forceinline__ void commit(uint64_t* mbar) {
     asm volatile(
@@ -252,9 +274,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // Zero rows [r0, 64) of the 64-row block at `row0` of a swizzled tile (a chunk
 // shorter than 64 tokens: its tail rows hold the next sequence's tokens).
 // A whole 128-byte row is one box row, so the swizzle does not matter.
-__device__ __forceinline__ void zero_tail_rows(float* tile, int rows, int row0, int r0) {
+// nth: the threads taking part (0: the whole CTA).
+__device__ __forceinline__ void zero_tail_rows(float* tile, int rows, int row0, int r0, int nth = 0) {
     const int n = (64 - r0) * 32;   // floats per box
-    for (int e = threadIdx.x * 4; e < 4 * n; e += blockDim.x * 4) {
+    const int step = (nth ? nth : (int)blockDim.x) * 4;
+    for (int e = threadIdx.x * 4; e < 4 * n; e += step) {
         const int b = e / n, o = e % n;
         *reinterpret_cast<float4*>(tile + (b * rows + row0 + r0) * 32 + o) =
             make_float4(0.f, 0.f, 0.f, 0.f);
@@ -368,9 +392,11 @@ __device__ __forceinline__ float tf32r(float x) {
 __device__ __forceinline__ float4 tf32r(float4 v) {
     return make_float4(tf32r(v.x), tf32r(v.y), tf32r(v.z), tf32r(v.w));
 }
-// Round n floats (n % 4 == 0, 16-byte aligned) in place; whole CTA.
-__device__ __forceinline__ void tf32r_inplace(float* p, int n) {
-    for (int i = threadIdx.x * 4; i < n; i += blockDim.x * 4) {
+// Round n floats (n % 4 == 0, 16-byte aligned) in place; threads 0 .. nth - 1
+// (0: the whole CTA).
+__device__ __forceinline__ void tf32r_inplace(float* p, int n, int nth = 0) {
+    const int step = (nth ? nth : (int)blockDim.x) * 4;
+    for (int i = threadIdx.x * 4; i < n; i += step) {
         float4* q = reinterpret_cast<float4*>(p + i);
         *q = tf32r(*q);
     }
