@@ -214,18 +214,19 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
 //  - state warps (4-7): the Ub epilogue (D1 read, "Ub ready"), the update
 //    ("accumulator read", "dS ready", the dS store);
 //  - chain thread (warp 8): D1 once dS and K are ready, then W^T Ub once Ub and
-//    B' are; refills K (once D1 is read) and W (once W^T Ub is done);
+//    B' are; refills K (two buffers, once D1 is done) and W (once W^T Ub is
+//    done), prefetching both into L2 a chunk earlier;
 //  - product thread (warp 9): B' once Q, dO, dU_local are scaled and the
 //    accumulator is free; then refills Q, dO, dU_local.
 // dU_local arrives from its own buffer, so dU is written without a hazard.
-// Shared memory: dS copy 32 KB, K (K-major) 32 KB, W (MN-major) 2 x 32 KB, Q
+// Shared memory: dS copy 32 KB, K (K-major) 2 x 32 KB, W (MN-major) 32 KB, Q
 // (MN-major) 32 KB, dO and dU_local slices and Ub (MN-major, 64 x 64) 16 KB
 // each.  Tensor memory: two accumulators (M = 128, 64 columns) and D1 (M = 64,
 // 64 columns).
 constexpr int kSl = 64;
 constexpr int kStateThreadsB = 320;
 constexpr int kB2Floats = 5 * 64 * 128 + 3 * 64 * 64;
-constexpr int kB2Bars = 15;
+constexpr int kB2Bars = 16;
 constexpr size_t kB2Smem = sizeof(float) * kB2Floats + kB2Bars * 8 + 8 + 1024;
 
 __device__ __forceinline__ void bwd_state_cta(const TileMaps& maps, int sl, int h, int n, int hk,
@@ -234,16 +235,16 @@ __device__ __forceinline__ void bwd_state_cta(const TileMaps& maps, int sl, int 
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
     float* dSt = sm;                   // [64 (a)][128 (b)] swizzled K-major: dS, rounded
-    float* Kk = dSt + 64 * 128;        // [64 (i)][128 (b)] swizzled K-major K
-    float* Wm0 = Kk + 64 * 128;        // [2][64 (i)][128 (b)] MN-major W (arrives rounded)
-    float* Qm = Wm0 + 2 * 64 * 128;    // [64 (i)][128 (b)] MN-major Q
+    float* Kk0 = dSt + 64 * 128;       // [2][64 (i)][128 (b)] swizzled K-major K
+    float* Wm = Kk0 + 2 * 64 * 128;    // [64 (i)][128 (b)] MN-major W (arrives rounded)
+    float* Qm = Wm + 64 * 128;         // [64 (i)][128 (b)] MN-major Q
     float* dOs = Qm + 64 * 128;        // [64 (i)][64 (a)] MN-major dO slice (arrives rounded)
     float* dUs = dOs + 64 * 64;        // [64 (i)][64 (a)] MN-major dU_local slice
     float* Ub = dUs + 64 * 64;         // [64 (i)][64 (a)] MN-major -diag(fk) D1, rounded
     uint64_t* mA = reinterpret_cast<uint64_t*>(Ub + 64 * 64);   // Q, dO, dU_local loaded
-    uint64_t* mK = mA + 1;             // K loaded
-    uint64_t* mW = mK + 1;             // [2] W loaded
-    uint64_t* bSc = mW + 2;            // Q, dO, dU_local scaled (scaling warps)
+    uint64_t* mK = mA + 1;             // [2] K loaded, per buffer
+    uint64_t* mW = mK + 2;             // W loaded
+    uint64_t* bSc = mW + 1;            // Q, dO, dU_local scaled (scaling warps)
     uint64_t* bK = bSc + 1;            // K ready (scaling warps)
     uint64_t* mPb = bK + 1;            // [2] B'^T done, per accumulator (commit)
     uint64_t* mD1 = mPb + 2;           // D1 done (commit)
@@ -251,8 +252,9 @@ __device__ __forceinline__ void bwd_state_cta(const TileMaps& maps, int sl, int 
     uint64_t* mC = bU + 1;             // W^T Ub done (commit)
     uint64_t* bS = mC + 1;             // dS copy written (state warps)
     uint64_t* fA = bS + 1;             // [2] accumulator read (state warps)
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(fA + 2);
-    auto Wm = [&](int it) { return Wm0 + (it & 1) * 64 * 128; };
+    uint64_t* dR = fA + 2;             // D1 read by the scaling warps
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(dR + 1);
+    auto Kk = [&](int it) { return Kk0 + (it & 1) * 64 * 128; };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int a0 = sl * kSl, kh = h / (hv / hk);
     const int64_t sbase = ((int64_t)n * hv + h) * kD * kD;
@@ -260,9 +262,9 @@ __device__ __forceinline__ void bwd_state_cta(const TileMaps& maps, int sl, int 
     // iteration it works on chunk c1 - 1 - it
     if (tid == 0) {
         umma::mbar_init(mA, 1);
-        umma::mbar_init(mK, 1);
-        umma::mbar_init(&mW[0], 1);
-        umma::mbar_init(&mW[1], 1);
+        umma::mbar_init(&mK[0], 1);
+        umma::mbar_init(&mK[1], 1);
+        umma::mbar_init(mW, 1);
         umma::mbar_init(bSc, 128);
         umma::mbar_init(bK, 128);
         umma::mbar_init(&mPb[0], 1);
@@ -273,6 +275,7 @@ __device__ __forceinline__ void bwd_state_cta(const TileMaps& maps, int sl, int 
         umma::mbar_init(bS, 128);
         umma::mbar_init(&fA[0], 128);
         umma::mbar_init(&fA[1], 128);
+        umma::mbar_init(dR, 128);
     }
     if (warp == 0) umma::tmem_alloc(tslot, 256);
     umma::fence_before_sync();
@@ -284,39 +287,38 @@ __device__ __forceinline__ void bwd_state_cta(const TileMaps& maps, int sl, int 
     bool ok = true;
     if (warp < 4) {
         // ---------------------------------------------------------- scaling warps
-        // thread t: 16-byte pieces t + 128 q of the two slices (rows (t / 8 + 16 q) % 64)
+        // Per iteration it: K ready (the chain's next D1 waits for it), then the
+        // dU rows of chunk it (once D1 is done), then the dO / dU_local slices of
+        // chunk it + 1 (B' runs a chunk ahead).  A chunk's gate values and dU_local
+        // rows are read two iterations ahead and the exponentials taken at use: a
+        // load used at once would wait on memory shared with the P / dP tiles.
+        // Slices: thread t scales the 16-byte pieces t + 128 q (rows (t / 8 + 16 q) % 64).
+        // dU rows: D1 fragment rows rl, rl + 8, columns 8 k + cf, + 1.
         const int r0 = tid >> 3;
-        auto gates = [&](int it, float (&eg)[4], int& len) {
-            len = 0;
-#pragma unroll
-            for (int u = 0; u < 4; u++) eg[u] = 0.f;
-            if (it >= nc) return;
-            const ChunkInfo info = sv.chunks[c1 - 1 - it];
-            const float* g = sv.gam + (int64_t)h * sv.T + info.start;
-#pragma unroll
-            for (int u = 0; u < 4; u++) eg[u] = r0 + 16 * u < info.len ? expf(g[r0 + 16 * u]) : 0.f;
-            len = info.len;
-        };
-        float eg[4], eg_n[4];
-        int len, len_n;
-        gates(0, eg, len);
-        // the dU rows: D1 fragment rows rl, rl + 8 (columns 8 k + cf, + 1), their fk,
-        // and their dU_local values, read one iteration ahead (a load issued when
-        // needed would wait on memory shared with the P / dP tiles)
         const int rl = umma::frag_row_lo(), cf = umma::frag_col();
-        auto urows = [&](int it, float (&u)[32], float& f_lo, float& f_hi, int& ln, int& st) {
-            f_lo = f_hi = 0.f;
-            ln = st = 0;
+        struct Rows {
+            float g[4];            // gam of the slice rows r0 + 16 u
+            float glo, ghi, gL;    // gam of the dU rows and of the chunk's last token
+            int len, start;
+            float ul[32];          // dU_local of the dU rows (0 past the chunk)
+        };
+        auto load = [&](int it, Rows& r) {
+            r.len = r.start = 0;
+            r.glo = r.ghi = r.gL = 0.f;
 #pragma unroll
-            for (int x = 0; x < 32; x++) u[x] = 0.f;
+            for (int u = 0; u < 4; u++) r.g[u] = 0.f;
+#pragma unroll
+            for (int x = 0; x < 32; x++) r.ul[x] = 0.f;
             if (it >= nc) return;
             const ChunkInfo info = sv.chunks[c1 - 1 - it];
             const float* g = sv.gam + (int64_t)h * sv.T + info.start;
-            const float gL = g[info.len - 1];
-            f_lo = rl < info.len ? expf(gL - g[rl]) : 0.f;
-            f_hi = rl + 8 < info.len ? expf(gL - g[rl + 8]) : 0.f;
-            ln = info.len;
-            st = info.start;
+            r.len = info.len;
+            r.start = info.start;
+#pragma unroll
+            for (int u = 0; u < 4; u++) r.g[u] = g[min(r0 + 16 * u, info.len - 1)];
+            r.glo = g[min(rl, info.len - 1)];
+            r.ghi = g[min(rl + 8, info.len - 1)];
+            r.gL = g[info.len - 1];
 #pragma unroll
             for (int hr = 0; hr < 2; hr++) {
                 const int i = rl + 8 * hr;
@@ -325,39 +327,46 @@ __device__ __forceinline__ void bwd_state_cta(const TileMaps& maps, int sl, int 
 #pragma unroll
                 for (int k = 0; k < 8; k++) {
                     const float2 v = *reinterpret_cast<const float2*>(src + 8 * k);
-                    u[4 * k + 2 * hr] = v.x;
-                    u[4 * k + 2 * hr + 1] = v.y;
+                    r.ul[4 * k + 2 * hr] = v.x;
+                    r.ul[4 * k + 2 * hr + 1] = v.y;
                 }
             }
         };
-        float ul[32], uf_lo, uf_hi;
-        int ulen, ustart;
-        urows(0, ul, uf_lo, uf_hi, ulen, ustart);
-        for (int it = 0; it < nc && ok; it++) {
-            gates(it + 1, eg_n, len_n);
-            ok = umma::mbar_wait(mA, it & 1);
-            if (ok) {
+        // the dO / dU_local slices of chunk it: e^gam dO and -dU_local, zero past the
+        // chunk, rounded; Q rounded when it is not tf32
+        auto scale_a = [&](int it, const Rows& r) {
+            bool got = umma::mbar_wait(mA, it & 1);
+            if (got) {
                 float4* o4 = reinterpret_cast<float4*>(dOs);
                 float4* u4 = reinterpret_cast<float4*>(dUs);
 #pragma unroll
                 for (int q = 0; q < 8; q++) {
-                    const float e = eg[q & 3];
-                    const float m = r0 + 16 * (q & 3) < len ? -1.f : 0.f;
+                    const bool in = r0 + 16 * (q & 3) < r.len;
+                    const float e = in ? expf(r.g[q & 3]) : 0.f;
+                    const float m = in ? -1.f : 0.f;
                     const float4 ov = o4[tid + 128 * q], uv = u4[tid + 128 * q];
                     o4[tid + 128 * q] = umma::tf32r(make_float4(e * ov.x, e * ov.y, e * ov.z, e * ov.w));
                     u4[tid + 128 * q] = umma::tf32r(make_float4(m * uv.x, m * uv.y, m * uv.z, m * uv.w));
                 }
-                if (!sv.qkv_tf32) umma::tf32r_inplace(Qm, 64 * 128, 128);
+                if (!sv.qkv_tf32) umma::tf32r_inplace<128>(Qm, 64 * 128);
             }
             umma::fence_smem_to_async();
             umma::mbar_arrive(bSc);
-            ok = ok && umma::mbar_wait(mK, it & 1);
-            if (ok && !sv.qkv_tf32) umma::tf32r_inplace(Kk, 64 * 128, 128);
-            umma::fence_smem_to_async();
-            umma::mbar_arrive(bK);
+            return got;
+        };
+        Rows cur, nxt;   // chunks it and it + 1
+        load(0, cur);
+        load(1, nxt);
+        if (nc > 0) ok = scale_a(0, cur);
+        for (int it = 0; it < nc && ok; it++) {
+            if (!sv.qkv_tf32) {   // K rounded in place ("K ready"; else the chain waits the load)
+                ok = umma::mbar_wait(&mK[it & 1], (it >> 1) & 1);
+                if (ok) umma::tf32r_inplace<128>(Kk(it), 64 * 128);
+                umma::fence_smem_to_async();
+                umma::mbar_arrive(bK);
+            }
             // dU = dU_local + diag(fk) D1 for the rows inside the chunk (rounded: only
-            // ever a tensor-core operand later).  D1 is read before this thread's next
-            // "K ready", which the next D1 waits for.
+            // ever a tensor-core operand later).  "D1 read" lets the next D1 go.
             ok = __all_sync(0xffffffffu, ok && umma::mbar_wait(mD1, it & 1));   // warp-uniform
             umma::fence_after_sync();
             if (ok) {
@@ -366,21 +375,21 @@ __device__ __forceinline__ void bwd_state_cta(const TileMaps& maps, int sl, int 
 #pragma unroll
                 for (int hr = 0; hr < 2; hr++) {
                     const int i = rl + 8 * hr;
-                    if (i >= ulen) continue;
-                    const float f = hr ? uf_hi : uf_lo;
-                    float* dst = w.dU + ((int64_t)(ustart + i) * hv + h) * kD + a0 + cf;
+                    if (i >= cur.len) continue;
+                    const float f = expf(cur.gL - (hr ? cur.ghi : cur.glo));
+                    float* dst = w.dU + ((int64_t)(cur.start + i) * hv + h) * kD + a0 + cf;
 #pragma unroll
                     for (int k = 0; k < 8; k++)
-                        *reinterpret_cast<float2*>(dst + 8 * k) =
-                            make_float2(umma::tf32r(ul[4 * k + 2 * hr] + f * d1[4 * k + 2 * hr]),
-                                        umma::tf32r(ul[4 * k + 2 * hr + 1] + f * d1[4 * k + 2 * hr + 1]));
+                        *reinterpret_cast<float2*>(dst + 8 * k) = make_float2(
+                            umma::tf32r(cur.ul[4 * k + 2 * hr] + f * d1[4 * k + 2 * hr]),
+                            umma::tf32r(cur.ul[4 * k + 2 * hr + 1] + f * d1[4 * k + 2 * hr + 1]));
                 }
             }
             umma::fence_before_sync();
-            urows(it + 1, ul, uf_lo, uf_hi, ulen, ustart);
-#pragma unroll
-            for (int u = 0; u < 4; u++) eg[u] = eg_n[u];
-            len = len_n;
+            umma::mbar_arrive(dR);
+            if (ok && it + 1 < nc) ok = scale_a(it + 1, nxt);
+            cur = nxt;
+            load(it + 2, nxt);
         }
     } else if (warp < 8) {
         // ---------------------------------------------------------- state warps
@@ -468,34 +477,46 @@ __device__ __forceinline__ void bwd_state_cta(const TileMaps& maps, int sl, int 
             for (int j = 0; j < 64; j++) dS_init[sbase + (int64_t)(a0 + j) * kD + bp] = s[j];
     } else if (tid == 256) {
         // ---------------------------------------------------------- chain thread
+        // K of chunk it + 2 is requested once D1 of chunk it is done (two buffers);
+        // W of chunk it once the W^T Ub product one back is done (one buffer: its
+        // first reader, B', runs well before the second); both prefetched into L2
+        // earlier (memory is shared with the P / dP tiles)
         auto issue_k = [&](int it) {
-            umma::mbar_expect_tx(mK, 64 * 128 * 4);
-            umma::tma_rows(Kk, 64, &maps.k, kh, start_of(it), mK);
+            umma::mbar_expect_tx(&mK[it & 1], 64 * 128 * 4);
+            umma::tma_rows(Kk(it), 64, &maps.k, kh, start_of(it), &mK[it & 1]);
         };
         auto issue_w = [&](int it) {
-            umma::mbar_expect_tx(&mW[it & 1], 64 * 128 * 4);
-            umma::tma_rows(Wm(it), 64, &maps.W_mn, h, start_of(it), &mW[it & 1]);
+            umma::mbar_expect_tx(mW, 64 * 128 * 4);
+            umma::tma_rows(Wm, 64, &maps.W_mn, h, start_of(it), mW);
         };
         if (nc > 0) {
             issue_k(0);
             issue_w(0);
         }
-        if (nc > 1) issue_w(1);
+        if (nc > 1) {
+            issue_k(1);
+            umma::tma_prefetch_rows(&maps.W_mn, h, start_of(1));
+        }
+        if (nc > 2) umma::tma_prefetch_rows(&maps.k, kh, start_of(2));
         for (int it = 0; it < nc && ok; it++) {
             ok = umma::mbar_wait(bS, it & 1);   // dS at this chunk's end: W^T Ub one back is done
-            if (ok && it >= 1 && it + 1 < nc) issue_w(it + 1);   // into that product's W
-            ok = ok && umma::mbar_wait(bK, it & 1);
+            if (ok && it >= 1) issue_w(it);
+            if (ok && it + 2 < nc) umma::tma_prefetch_rows(&maps.W_mn, h, start_of(it + 2));
+            if (ok && it + 3 < nc) umma::tma_prefetch_rows(&maps.k, kh, start_of(it + 3));
+            ok = ok && (sv.qkv_tf32 ? umma::mbar_wait(&mK[it & 1], (it >> 1) & 1)
+                                    : umma::mbar_wait(bK, it & 1));
+            if (it >= 1) ok = ok && umma::mbar_wait(dR, (it - 1) & 1);   // D1 one back read
             umma::fence_after_sync();
             if (!ok) break;
-            umma::mma(tD1, umma::swt(Kk, 64), umma::swt(dSt, 64), 64, 64, 128, false);
+            umma::mma(tD1, umma::swt(Kk(it), 64), umma::swt(dSt, 64), 64, 64, 128, false);
             umma::commit(mD1);
-            ok = umma::mbar_wait(bU, it & 1);   // Ub written, D1 read: K is free
-            if (ok && it + 1 < nc) issue_k(it + 1);
-            ok = ok && umma::mbar_wait(&mPb[it & 1], (it >> 1) & 1) &&
-                 umma::mbar_wait(&mW[it & 1], (it >> 1) & 1);
+            ok = umma::mbar_wait(mD1, it & 1);   // D1 done: its K buffer is free
+            if (ok && it + 2 < nc) issue_k(it + 2);
+            ok = ok && umma::mbar_wait(bU, it & 1);   // Ub written
+            ok = ok && umma::mbar_wait(&mPb[it & 1], (it >> 1) & 1) && umma::mbar_wait(mW, it & 1);
             umma::fence_after_sync();
             if (!ok) break;
-            umma::mma(tAcc(it), umma::mnt(Wm(it)), umma::mnt(Ub, 64), 128, 64, 64, true);
+            umma::mma(tAcc(it), umma::mnt(Wm), umma::mnt(Ub, 64), 128, 64, 64, true);
             umma::commit(mC);
         }
     } else if (tid == 288) {
@@ -509,15 +530,26 @@ __device__ __forceinline__ void bwd_state_cta(const TileMaps& maps, int sl, int 
             umma::tma_box(dUs, &maps.dUl_mn, a0, h, st, mA);
             umma::tma_box(dUs + 64 * 32, &maps.dUl_mn, a0 + 32, h, st, mA);
         };
+        // Q, dO, dU_local of chunk it + 2 prefetched into L2 at iteration it
+        auto prefetch_a = [&](int it) {
+            const int st = start_of(it);
+            umma::tma_prefetch_rows(&maps.q_mn, kh, st);
+            umma::tma_prefetch_box(&maps.dO_mn, a0, h, st);
+            umma::tma_prefetch_box(&maps.dO_mn, a0 + 32, h, st);
+            umma::tma_prefetch_box(&maps.dUl_mn, a0, h, st);
+            umma::tma_prefetch_box(&maps.dUl_mn, a0 + 32, h, st);
+        };
         if (nc > 0) issue_a(0);
+        if (nc > 1) prefetch_a(1);
         for (int it = 0; it < nc && ok; it++) {
-            ok = umma::mbar_wait(bSc, it & 1) && umma::mbar_wait(&mW[it & 1], (it >> 1) & 1);
+            if (it + 2 < nc) prefetch_a(it + 2);
+            ok = umma::mbar_wait(bSc, it & 1) && umma::mbar_wait(mW, it & 1);
             // accumulator it & 1: the state warps have read it (two chunks back)
             if (it >= 2) ok = ok && umma::mbar_wait(&fA[it & 1], ((it / 2) - 1) & 1);
             umma::fence_after_sync();
             if (!ok) break;
             umma::mma(tAcc(it), umma::mnt(Qm), umma::mnt(dOs, 64), 128, 64, 64, false);
-            umma::mma(tAcc(it), umma::mnt(Wm(it)), umma::mnt(dUs, 64), 128, 64, 64, true);
+            umma::mma(tAcc(it), umma::mnt(Wm), umma::mnt(dUs, 64), 128, 64, 64, true);
             umma::commit(&mPb[it & 1]);
             ok = umma::mbar_wait(&mPb[it & 1], (it >> 1) & 1);   // Q, dO, dU_local consumed
             if (ok && it + 1 < nc) issue_a(it + 1);
@@ -840,13 +872,13 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         ok = umma::named_sync_and(1, 256, umma::mbar_wait(mA, it & 1));   // Q, K, dO, U; gam visible
         if (!ok) break;
         if (L < 64) {   // tail rows belong to the next sequence
-            umma::zero_tail_rows(Qs, 64, 0, L, 256);
-            umma::zero_tail_rows(Ks, 64, 0, L, 256);
-            umma::zero_tail_rows(dOs, 64, 0, L, 256);
-            umma::zero_tail_rows(Us, 64, 0, L, 256);
+            umma::zero_tail_rows<256>(Qs, 64, 0, L);
+            umma::zero_tail_rows<256>(Ks, 64, 0, L);
+            umma::zero_tail_rows<256>(dOs, 64, 0, L);
+            umma::zero_tail_rows<256>(Us, 64, 0, L);
             umma::named_sync(1, 256);
         }
-        if (!sv.qkv_tf32) umma::tf32r_inplace(Qs, 2 * 64 * 128, 256);   // Q, K
+        if (!sv.qkv_tf32) umma::tf32r_inplace<256>(Qs, 2 * 64 * 128);   // Q, K
         umma::fence_smem_to_async();
         umma::named_sync(1, 256);
         umma::fence_after_sync();
@@ -905,11 +937,11 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         ok = umma::named_sync_and(1, 256, umma::mbar_wait(mB, it & 1));   // MN-major Q, K
         if (!ok) break;
         if (L < 64) {
-            umma::zero_tail_rows(Qm, 64, 0, L, 256);
-            umma::zero_tail_rows(Km, 64, 0, L, 256);
+            umma::zero_tail_rows<256>(Qm, 64, 0, L);
+            umma::zero_tail_rows<256>(Km, 64, 0, L);
             umma::named_sync(1, 256);
         }
-        if (!sv.qkv_tf32) umma::tf32r_inplace(Qm, 2 * 64 * 128, 256);
+        if (!sv.qkv_tf32) umma::tf32r_inplace<256>(Qm, 2 * 64 * 128);
         umma::fence_smem_to_async();
         umma::named_sync(1, 256);
         umma::fence_after_sync();

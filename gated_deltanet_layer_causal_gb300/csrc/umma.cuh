@@ -253,6 +253,23 @@ __device__ __forceinline__ void tma_box(float* dst, const CUtensorMap* map, int 
         : "memory");
 }
 
+// Prefetch into L2 what tma_rows / tma_box would load (no shared memory, no
+// barrier): a later load of the same tile then hits L2.
+__device__ __forceinline__ void tma_prefetch_rows(const CUtensorMap* map, int head, int t0) {
+#pragma unroll
+    for (int b = 0; b < 4; b++)
+        asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(
+                         reinterpret_cast<uint64_t>(map)),
+                     "r"(b * 32), "r"(head), "r"(t0)
+                     : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_box(const CUtensorMap* map, int x, int head, int t0) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(head), "r"(t0)
+                 : "memory");
+}
+
 // Contiguous copy shared -> global (both 16-byte aligned, bytes % 16 == 0), in
 // the calling thread's bulk group.
 __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
@@ -274,10 +291,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // Zero rows [r0, 64) of the 64-row block at `row0` of a swizzled tile (a chunk
 // shorter than 64 tokens: its tail rows hold the next sequence's tokens).
 // A whole 128-byte row is one box row, so the swizzle does not matter.
-// nth: the threads taking part (0: the whole CTA).
-__device__ __forceinline__ void zero_tail_rows(float* tile, int rows, int row0, int r0, int nth = 0) {
+// NTH: the threads taking part, 0 .. NTH - 1 (0: the whole CTA).
+template <int NTH = 0>
+__device__ __forceinline__ void zero_tail_rows(float* tile, int rows, int row0, int r0) {
     const int n = (64 - r0) * 32;   // floats per box
-    const int step = (nth ? nth : (int)blockDim.x) * 4;
+    const int step = (NTH ? NTH : (int)blockDim.x) * 4;
     for (int e = threadIdx.x * 4; e < 4 * n; e += step) {
         const int b = e / n, o = e % n;
         *reinterpret_cast<float4*>(tile + (b * rows + row0 + r0) * 32 + o) =
@@ -392,10 +410,11 @@ __device__ __forceinline__ float tf32r(float x) {
 __device__ __forceinline__ float4 tf32r(float4 v) {
     return make_float4(tf32r(v.x), tf32r(v.y), tf32r(v.z), tf32r(v.w));
 }
-// Round n floats (n % 4 == 0, 16-byte aligned) in place; threads 0 .. nth - 1
+// Round n floats (n % 4 == 0, 16-byte aligned) in place; threads 0 .. NTH - 1
 // (0: the whole CTA).
-__device__ __forceinline__ void tf32r_inplace(float* p, int n, int nth = 0) {
-    const int step = (nth ? nth : (int)blockDim.x) * 4;
+template <int NTH = 0>
+__device__ __forceinline__ void tf32r_inplace(float* p, int n) {
+    const int step = (NTH ? NTH : (int)blockDim.x) * 4;
     for (int i = threadIdx.x * 4; i < n; i += step) {
         float4* q = reinterpret_cast<float4*>(p + i);
         *q = tf32r(*q);
