@@ -263,7 +263,7 @@ MMAS = {
                           [(64, 64, 128), (64, 64, 128), (64, 128, 64), (64, 128, 64)],
     "chunk_bwd_sfacing": [(128, 128, 128), (64, 128, 128)],            # [dO; dU] S0, U dS
     "chunk_bwd_wy": [(64, 64, 128)] * 3 + [(64, 256, 64), (64, 64, 64), (64, 64, 64),
-                                           (64, 128, 64), (64, 128, 64)],
+                                           (64, 128, 64)],   # ..., (dKK + dKK^T) K
 }
 
 

@@ -1013,13 +1013,13 @@ bwd_state_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int N
 // + gridDim.x, ... (chunk = t % NT, head = t / NT).  Per tile, tcgen05, with T
 // saved by the forward:
 //   D_kk = K K^T, D_dt1 = dW K^T, D_dt2 = dU V^T          (64 x 64)
-//   D_tw = T^T [dW | dU]                                  (64 x 256)
+//   D_tw = T^T [dW | dU]                                  (64 x 256, one product)
 //   dT = D_dt1 diag(beta e^gam) + D_dt2 diag(beta)
 //   dV = diag(beta) T^T dU ; dK += diag(beta e^gam) T^T dW
 //   dbeta_j += e^{gam_j} (T^T dW)_j . K_j + (T^T dU)_j . V_j ; dgam_j += beta_j e^{gam_j} (..)
 //   Y^T = T dT^T ; dA = -T^T Y (strictly lower) ; dKK = dA (.) beta_j Gam
 //   dbeta_j += sum_m dA (.) GamKK ; dgam_j += beta_j (..) ; dgam_m -= sum_j beta_j (..)
-//   dK += dKK K + dKK^T K
+//   dK += (dKK + dKK^T) K   (one product: the two triangles are disjoint)
 // then dg = reverse in-chunk cumsum of the total dgam, and the gate gradients.
 // The next tile's operands are requested in three groups as their space frees
 // up: dW, dU (K-major) and T^T once dA is formed, dW, dU (MN-major) and V once
@@ -1051,9 +1051,8 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     float* DTR = GKK + 64 * 64;        // [64 (i)][64 (j)] K-major dT
     float* TR = DTR + 64 * 64;         // [64 (m)][64 (j)] K-major T
     float* YT = TR + 64 * 64;          // [64 (m)][64 (i)] K-major Y^T
-    float* dKR = YT + 64 * 64;         // [64 (j)][64 (m)] K-major dKK
-    float* dKC = dKR + 64 * 64;        // [64 (j)][64 (m)] K-major dKK^T
-    float* Km = dKC + 64 * 64;         // [64 (m)][128 (b)] MN-major K (over dU_mn, after stage 1)
+    float* dKS = YT + 64 * 64;         // [64 (j)][64 (m)] K-major dKK + dKK^T (disjoint triangles)
+    float* Km = dKS + 2 * 64 * 64;     // [64 (m)][128 (b)] MN-major K (over dU_mn, after stage 1)
     float* Rm = Vs;                    // [64][65] row-major
     float* gam = TC + 64 * 64;
     float* eg = gam + 64;
@@ -1171,8 +1170,8 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
             umma::mma(tKK, umma::swt(Ks, 64), umma::swt(Ks, 64), 64, 64, 128, false);
             umma::mma(tDT1, umma::swt(dWs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
             umma::mma(tDT2, umma::swt(dUs, 64), umma::swt(Vs, 64), 64, 64, 128, false);
-            umma::mma(tTW, umma::kmaj(TC, 64), umma::mnt(dWm), 64, 128, 64, false);
-            umma::mma(tTW + 128, umma::kmaj(TC, 64), umma::mnt(dUm), 64, 128, 64, false);
+            // T^T [dW | dU]: the two MN-major tiles are adjacent, one N = 256 product
+            umma::mma(tTW, umma::kmaj(TC, 64), umma::mnt(dWm), 64, 256, 64, false);
             umma::commit(mbar);
         }
         ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
@@ -1300,17 +1299,22 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
                     const int r = rl + 8 * hr;
                     const float br = bet[r], gr = gam[r];
                     const float2 gk = *reinterpret_cast<const float2*>(GKK + umma::kidx(r, m, 64));
-                    float dk[2];
 #pragma unroll
                     for (int e = 0; e < 2; e++) {
                         const float dA = m + e < r ? -v[4 * k + 2 * hr + e] : 0.f;
                         const float x = dA * (e == 0 ? gk.x : gk.y);
                         rs[hr] += x;
                         cs[k][e] += br * x;
-                        dk[e] = umma::tf32r(m + e < r ? dA * br * expf(gr - gam[m + e]) : 0.f);
-                        dKC[umma::kidx(m + e, r, 64)] = dk[e];
+                        // dKK is strictly lower: (r, m) and its mirror are written by the
+                        // thread of the lower element only, the diagonal by its own
+                        if (m + e < r) {
+                            const float dk = umma::tf32r(dA * br * expf(gr - gam[m + e]));
+                            dKS[umma::kidx(r, m + e, 64)] = dk;
+                            dKS[umma::kidx(m + e, r, 64)] = dk;
+                        } else if (m + e == r) {
+                            dKS[umma::kidx(r, r, 64)] = 0.f;
+                        }
                     }
-                    *reinterpret_cast<float2*>(dKR + umma::kidx(r, m, 64)) = make_float2(dk[0], dk[1]);
                 }
             }
             rs[0] = umma::row_quad_sum(rs[0]);
@@ -1332,8 +1336,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         __syncthreads();
         umma::fence_after_sync();
         if (tid == 0) {
-            umma::mma(tX, umma::kmaj(dKR, 64), umma::mnt(Km), 64, 128, 64, false);   // dKK K
-            umma::mma(tX, umma::kmaj(dKC, 64), umma::mnt(Km), 64, 128, 64, true);    // + dKK^T K
+            umma::mma(tX, umma::kmaj(dKS, 64), umma::mnt(Km), 64, 128, 64, false);   // (dKK + dKK^T) K
             umma::commit(mbar);
             // Gam (.) KK, dT, T, Y^T and T^T are consumed: the next tile's dW, dU, T^T
             if (next) issue_w(cn, tn);
