@@ -238,14 +238,18 @@ class DecodeStep:
 # proportional to the chunks it processes).  Valid for the kernels as captured;
 # a kernel changed since then is left out (its traffic reports null).
 TRAFFIC_64K = {
-    "conv_fwd": 3620528128,
-    "gates": 12666880,
-    "chunk_prep": 6522421248,
-    "chunk_norm_bwd": 5315454976,
-    "chunk_bwd_local": 4015650816,
-    "chunk_bwd_wy": 10133276672,
-    "gva_sum": 9023150080,
-    "conv_bwd": 5371113472,
+    "conv_fwd": 3619241984,
+    "gates": 12664832,
+    "chunk_prep": 6523840512,
+    "chunk_state_fwd": 6643978240,
+    "chunk_out_fwd": 12141393920,
+    "chunk_norm_bwd": 5317441536,
+    "chunk_bwd_local": 4016689152,
+    "chunk_bwd_state_dp": 18212042752,
+    "chunk_bwd_sfacing": 17401223168,
+    "chunk_bwd_wy": 10145630208,
+    "gva_sum": 9024364544,
+    "conv_bwd": 5372211200,
 }
 
 # tcgen05 / mma.sync products each chunk kernel issues per (chunk, v-head) tile,
