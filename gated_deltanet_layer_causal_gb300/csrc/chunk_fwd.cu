@@ -817,19 +817,29 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
         }
         umma::fence_before_sync();
         __syncthreads();
+        // this warp's eight rows: all reads first, then the math and the stores
+        // (independent rows, so their latencies overlap); rows past the chunk are
+        // read from the staging tile but not stored
+        float4 o4s[8];
+        float rss[8];
 #pragma unroll
         for (int q = 0; q < 8; q++) {
             const int r = warp + 8 * q;
-            if (r >= L) break;
-            const int64_t tok = ci.start + r;
-            const int64_t off = (tok * hv + h) * kD + lane * 4;
-            const float4 o4 = *reinterpret_cast<const float4*>(Or + umma::swz(r, lane * 4, 64));
-            st4(sv.o + off, o4);
-            if (o_out) st4(o_out + off, o4);
-            if (z) {
-                const float rs = rsqrtf((ssq[r] + ssq[64 + r]) * (1.f / kD) + norm_eps);
-                st4(y_out + off, gated_norm4(o4, rs, w4, zr[q], gate));
-                if (lane == 0) sv.rstd[tok * hv + h] = rs;
+            o4s[q] = *reinterpret_cast<const float4*>(Or + umma::swz(r, lane * 4, 64));
+            rss[q] = rsqrtf((ssq[r] + ssq[64 + r]) * (1.f / kD) + norm_eps);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            const int r = warp + 8 * q;
+            if (r < L) {
+                const int64_t tok = ci.start + r;
+                const int64_t off = (tok * hv + h) * kD + lane * 4;
+                st4(sv.o + off, o4s[q]);
+                if (o_out) st4(o_out + off, o4s[q]);
+                if (z) {
+                    st4(y_out + off, gated_norm4(o4s[q], rss[q], w4, zr[q], gate));
+                    if (lane == 0) sv.rstd[tok * hv + h] = rss[q];
+                }
             }
         }
         umma::fence_smem_to_async();   // O staging -> the next U~ load
