@@ -258,8 +258,8 @@ MMAS = {
     "chunk_prep": [(64, 64, 128), (64, 128, 64), (64, 128, 64)],        # K K^T, W, U~
     # per 64-row slice (2): the chain M^T S^T, B^T = (fk K)^T U~, -M^T = (fk K)^T W
     "chunk_state_fwd": [(128, 64, 128), (128, 64, 64), (128, 128, 64)] * 2,
-    # Q K^T, Q S0^T, W S0^T (U = U~ - W S0^T), P U
-    "chunk_out_fwd": [(64, 64, 128), (64, 128, 128), (64, 128, 128), (64, 128, 64)],
+    # [Q; W] [K; S0]^T (Q K^T, Q S0^T, W S0^T and an unused W K^T), [P; 0] U
+    "chunk_out_fwd": [(128, 192, 128), (128, 128, 64)],
     "chunk_bwd_local": [(64, 64, 128), (64, 128, 64)],                  # K Q^T, P^T dO
     # reverse state pass (2 row slices: K dS^T; B'^T = Q^T e^gam dO - W^T dU_local;
     # W^T Ub) and P / dP tiles, one launch

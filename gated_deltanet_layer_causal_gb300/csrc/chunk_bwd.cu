@@ -563,7 +563,8 @@ __device__ __forceinline__ void bwd_state_cta(const TileMaps& maps, int sl, int 
 
 // ------------------------------------------------------------------ B3a: state-facing terms
 // Persistent: one CTA per SM walks the (chunk, head) tiles t = blockIdx.x,
-// + gridDim.x, ... (chunk = t % NT, head = t / NT).  Per tile, tcgen05:
+// + gridDim.x, ... (chunk = t / Hv, head = t % Hv: the v-heads of a chunk run
+// side by side, so the q / k tiles they share come from DRAM once).  Per tile, tcgen05:
 //   [X; Y] = [dO; dU] S0     (one M=128, N=128, K=128 MMA; X = dO S0, Y = dU S0)
 //   dK~    = U dS            (M=64, N=128, K=128)
 // then dQ partial = e^gam X, dW = -Y, dK partial = fk dK~, and the dgam terms
@@ -609,26 +610,26 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
     const int ntiles = NT * hv;
     int t = blockIdx.x;
     if (t >= ntiles) return;
-    ChunkInfo ci = sv.chunks[t % NT];
+    ChunkInfo ci = sv.chunks[t / hv];
     if (ci.len == 0) return;   // the device check of cu_seqlens failed: every chunk is empty
     auto issue_main = [&](const ChunkInfo& c, int tile) {   // one thread
-        const int h = tile / NT;
+        const int h = tile % hv;
         umma::mbar_expect_tx(mS, 3 * 64 * 128 * 4 + 128 * 128 * 4);
         umma::tma_rows(A1, 128, &maps.dO, h, c.start, mS);
         umma::tma_rows(A1 + 64 * 32, 128, &maps.dU, h, c.start, mS);
         umma::tma_rows(A2, 64, &maps.U, h, c.start, mS);
-        const int s0row = ((tile % NT) * hv + h) * kD;   // S0 tile rows a = 0 .. 127
+        const int s0row = ((tile / hv) * hv + h) * kD;   // S0 tile rows a = 0 .. 127
         umma::tma_rows(S0m, 128, &maps.S0_mn, 0, s0row, mS);
         umma::tma_rows(S0m + 64 * 32, 128, &maps.S0_mn, 0, s0row + 64, mS);
     };
     auto issue_ds = [&](int tile) {   // one thread
-        const int row = ((tile % NT) * hv + tile / NT) * kD;   // dS tile rows a = 0 .. 127
+        const int row = ((tile / hv) * hv + tile % hv) * kD;   // dS tile rows a = 0 .. 127
         umma::mbar_expect_tx(mD, 128 * 128 * 4);
         umma::tma_rows(DSm, 128, &maps.dS_mn, 0, row, mD);
         umma::tma_rows(DSm + 64 * 32, 128, &maps.dS_mn, 0, row + 64, mD);
     };
     auto gam_of = [&](const ChunkInfo& c, int tile) {
-        return tid < 64 ? sv.gam[(int64_t)(tile / NT) * sv.T + c.start + min(tid, c.len - 1)] : 0.f;
+        return tid < 64 ? sv.gam[(int64_t)(tile % hv) * sv.T + c.start + min(tid, c.len - 1)] : 0.f;
     };
     if (tid == 0) {
         for (int k = 0; k < 4; k++) umma::mbar_init(&mbar[k], 1);
@@ -645,9 +646,9 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
     const int c0 = half * 64;
     bool ok = true;
     for (int it = 0;; it++) {
-        const int h = t / NT, kh = h / (hv / hk), L = ci.len;
+        const int h = t % hv, kh = h / (hv / hk), L = ci.len;
         const int tn = t + (int)gridDim.x;
-        const ChunkInfo cn = tn < ntiles ? sv.chunks[tn % NT] : ci;
+        const ChunkInfo cn = tn < ntiles ? sv.chunks[tn / hv] : ci;
         if (tid < 64) gam[tid] = g_cur;
         ok = umma::mbar_wait(mS, it & 1);
         ok = __syncthreads_and(ok && umma::mbar_wait(mD, it & 1));   // gam visible
@@ -783,8 +784,8 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
 
 // ------------------------------------------------------------------ B3b: P / dP terms
 // Persistent: up to one CTA per SM (the last CTAs of the combined launch
-// below), each claiming (chunk, head) tiles from a counter (chunk = t % NT,
-// head = t / NT), so CTAs that start late -- on the SMs the reverse state pass
+// below), each claiming (chunk, head) tiles from a counter (chunk = t / Hv,
+// head = t % Hv), so CTAs that start late -- on the SMs the reverse state pass
 // holds -- simply take fewer tiles.  Per tile, tcgen05:
 //   D_qk = Q K^T, D_dou = dO U^T                         (64 x 64 each)
 //   dPm = D_dou (.) Gam (.) [i>=j];  R = dPm (.) D_qk
@@ -826,9 +827,9 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ntiles = NT * hv;
     auto issue_a = [&](int tile) {   // one thread
-        const ChunkInfo c = sv.chunks[tile % NT];
+        const ChunkInfo c = sv.chunks[tile / hv];
         if (c.len == 0) return;
-        const int h = tile / NT, kh = h / (hv / hk);
+        const int h = tile % hv, kh = h / (hv / hk);
         umma::mbar_expect_tx(mA, 4 * 64 * 128 * 4);
         umma::tma_rows(Qs, 64, &maps.q, kh, c.start, mA);
         umma::tma_rows(Ks, 64, &maps.k, kh, c.start, mA);
@@ -836,9 +837,9 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         umma::tma_rows(Us, 64, &maps.U, h, c.start, mA);
     };
     auto issue_b = [&](int tile) {   // one thread
-        const ChunkInfo c = sv.chunks[tile % NT];
+        const ChunkInfo c = sv.chunks[tile / hv];
         if (c.len == 0) return;
-        const int kh = (tile / NT) / (hv / hk);
+        const int kh = (tile % hv) / (hv / hk);
         umma::mbar_expect_tx(mB, 2 * 64 * 128 * 4);
         umma::tma_rows(Qm, 64, &maps.q_mn, kh, c.start, mB);
         umma::tma_rows(Km, 64, &maps.k_mn, kh, c.start, mB);
@@ -865,8 +866,8 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
     int t = claim[0];
     bool ok = true;
     for (int it = 0; t < ntiles; it++) {
-        const ChunkInfo ci = sv.chunks[t % NT];
-        const int h = t / NT, L = ci.len;
+        const ChunkInfo ci = sv.chunks[t / hv];
+        const int h = t % hv, L = ci.len;
         if (L == 0) break;   // the device check of cu_seqlens failed: every chunk is empty
         load_gam(gam, sv, ci, h);
         ok = umma::named_sync_and(1, 256, umma::mbar_wait(mA, it & 1));   // Q, K, dO, U; gam visible
@@ -888,6 +889,21 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
             umma::commit(mM);
             claim[(it + 1) & 1] = atomicAdd(w.dp_next, 1);   // the next tile
         }
+        // while the products run: the decay factors e^{gam_r - gam_j} [j <= r] of this
+        // thread's fragment
+        float dec[16];
+#pragma unroll
+        for (int hr = 0; hr < 2; hr++) {
+            const int r = rl + 8 * hr;
+            const float gr = gam[r];
+#pragma unroll
+            for (int k = 0; k < 4; k++)
+#pragma unroll
+                for (int e = 0; e < 2; e++) {
+                    const int j = half * 32 + 8 * k + cf + e;
+                    dec[4 * k + 2 * hr + e] = j <= r ? expf(gr - gam[j]) : 0.f;
+                }
+        }
         ok = umma::named_sync_and(1, 256, umma::mbar_wait(mM, 0));   // the claim is visible too
         umma::fence_after_sync();
         if (!ok) break;
@@ -908,8 +924,7 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
                     float d[2];
 #pragma unroll
                     for (int e = 0; e < 2; e++) {
-                        const float gm = j + e <= r ? expf(gam[r] - gam[j + e]) : 0.f;
-                        const float x = du[4 * k + 2 * hr + e] * gm;
+                        const float x = du[4 * k + 2 * hr + e] * dec[4 * k + 2 * hr + e];
                         const float R = x * qk[4 * k + 2 * hr + e];
                         rs[hr] += R;
                         cs[k][e] += R;
@@ -1010,7 +1025,8 @@ bwd_state_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int N
 
 // ------------------------------------------------------------------ B3c: WY terms and gates
 // Persistent: one CTA per SM walks the (chunk, head) tiles t = blockIdx.x,
-// + gridDim.x, ... (chunk = t % NT, head = t / NT).  Per tile, tcgen05, with T
+// + gridDim.x, ... (chunk = t / Hv, head = t % Hv: the v-heads of a chunk run
+// side by side, so the q / k tiles they share come from DRAM once).  Per tile, tcgen05, with T
 // saved by the forward:
 //   D_kk = K K^T, D_dt1 = dW K^T, D_dt2 = dU V^T          (64 x 64)
 //   D_tw = T^T [dW | dU]                                  (64 x 256, one product)
@@ -1075,43 +1091,46 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     const int ntiles = NT * hv;
     int t = blockIdx.x;
     if (t >= ntiles) return;
-    ChunkInfo ci = sv.chunks[t % NT];
+    ChunkInfo ci = sv.chunks[t / hv];
     if (ci.len == 0) return;   // the device check of cu_seqlens failed: every chunk is empty
     auto Tg_of = [&](int tile) {   // T, then T^T, written by the forward
-        return sv.Tm + ((int64_t)(tile % NT) * hv + tile / NT) * 2 * 64 * 64;
+        return sv.Tm + ((int64_t)(tile / hv) * hv + tile % hv) * 2 * 64 * 64;
     };
     auto issue_w = [&](const ChunkInfo& c, int tile) {   // one thread
-        const int h = tile / NT;
+        const int h = tile % hv;
         umma::mbar_expect_tx(mW, 2 * 64 * 128 * 4 + 64 * 64 * 4);
         umma::tma_rows(dWs, 64, &maps.dW, h, c.start, mW);
         umma::tma_rows(dUs, 64, &maps.dU, h, c.start, mW);
         umma::bulk_load(TC, Tg_of(tile) + 64 * 64, 64 * 64 * 4, mW);
     };
     auto issue_m = [&](const ChunkInfo& c, int tile) {   // one thread
-        const int h = tile / NT;
+        const int h = tile % hv;
         umma::mbar_expect_tx(mM, 3 * 64 * 128 * 4);
         umma::tma_rows(dWm, 64, &maps.dW_mn, h, c.start, mM);
         umma::tma_rows(dUm, 64, &maps.dU_mn, h, c.start, mM);
         umma::tma_rows(Vs, 64, &maps.v, h, c.start, mM);
     };
     auto issue_k = [&](const ChunkInfo& c, int tile) {   // one thread
-        const int kh = tile / NT / (hv / hk);
+        const int kh = tile % hv / (hv / hk);
         umma::mbar_expect_tx(mK, 64 * 128 * 4);
         umma::tma_rows(Ks, 64, &maps.k, kh, c.start, mK);
     };
     // gate inputs of a tile for thread tid < 64: gam, beta, a + dt_bias and the
     // dgam terms of the other kernels (used at the very end)
-    struct Gates { float g, b, xa, dgin; };
+    // (kept as loaded: the values are first used in the tile's own iteration, so
+    // the loads stay in flight meanwhile)
+    struct Gates { float g, b; IO a; float dg1, dg2; };
     auto gates_of = [&](const ChunkInfo& c, int tile) {
-        Gates q{0.f, 0.f, 0.f, 0.f};
+        Gates q{0.f, 0.f, from_f<IO>(0.f), 0.f, 0.f};
         if (tid < 64) {
-            const int h = tile / NT;
+            const int h = tile % hv;
             q.g = sv.gam[(int64_t)h * sv.T + c.start + min(tid, c.len - 1)];
             if (tid < c.len) {
                 const int64_t tok = c.start + tid;
                 q.b = sv.beta[(int64_t)h * sv.T + tok];
-                q.xa = to_f(av[tok * hv + h]) + dt_bias[h];
-                q.dgin = w.dgam[tok * hv + h] + w.dgam2[tok * hv + h];
+                q.a = av[tok * hv + h];
+                q.dg1 = w.dgam[tok * hv + h];
+                q.dg2 = w.dgam2[tok * hv + h];
             }
         }
         return q;
@@ -1123,6 +1142,9 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         issue_k(ci, t);
     }
     Gates gcur = gates_of(ci, t);
+    // chunk entries are loaded a tile before they are needed: cn (the next tile's)
+    // is at hand at the top of an iteration, c2 (the one after) is requested there
+    ChunkInfo cn = t + (int)gridDim.x < ntiles ? sv.chunks[(t + (int)gridDim.x) / hv] : ci;
     if (warp == 0) umma::tmem_alloc(tslot, 512);
     umma::fence_before_sync();
     __syncthreads();
@@ -1136,11 +1158,19 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     const int rl = umma::frag_row_lo(), cf = umma::frag_col();   // fragment rows rl, rl + 8
     bool ok = true;
     for (int it = 0;; it++) {
-        const int h = t / NT, kh = h / (hv / hk), L = ci.len, chunk = t % NT;
-        const int tn = t + (int)gridDim.x;
-        const ChunkInfo cn = tn < ntiles ? sv.chunks[tn % NT] : ci;
+        const int h = t % hv, kh = h / (hv / hk), L = ci.len, chunk = t / hv;
+        const int tn = t + (int)gridDim.x, t2 = tn + (int)gridDim.x;
+        const ChunkInfo c2 = t2 < ntiles ? sv.chunks[t2 / hv] : cn;
         auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
         const float Aexp = expf(A_log[h]);
+        if (tid == 32 && tn < ntiles && cn.len > 0) {   // the next tile's inputs into L2
+            const int hn = tn % hv;
+            umma::tma_prefetch_rows(&maps.dW, hn, cn.start);
+            umma::tma_prefetch_rows(&maps.dU, hn, cn.start);
+            umma::tma_prefetch_rows(&maps.v, hn, cn.start);
+            umma::tma_prefetch_rows(&maps.k, hn / (hv / hk), cn.start);
+            umma::bulk_prefetch(Tg_of(tn), 2 * 64 * 64 * 4);
+        }
         if (tid < 64) {
             gam[tid] = gcur.g;
             bet[tid] = gcur.b;
@@ -1174,6 +1204,21 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
             umma::mma(tTW, umma::kmaj(TC, 64), umma::mnt(dWm), 64, 256, 64, false);
             umma::commit(mbar);
         }
+        // while the products run: the decay factors e^{gam_r - gam_j} [j < r] of this
+        // thread's fragment of the 64 x 64 products (Gam (.) KK and dKK use the same pairs)
+        float dec[16];
+#pragma unroll
+        for (int hr = 0; hr < 2; hr++) {
+            const int r = rl + 8 * hr;
+            const float gr = gam[r];
+#pragma unroll
+            for (int k = 0; k < 4; k++)
+#pragma unroll
+                for (int e = 0; e < 2; e++) {
+                    const int j = half * 32 + 8 * k + cf + e;
+                    dec[4 * k + 2 * hr + e] = j < r ? expf(gr - gam[j]) : 0.f;
+                }
+        }
         ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
         umma::fence_after_sync();
         if (!ok) break;
@@ -1192,12 +1237,11 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
 #pragma unroll
                 for (int hr = 0; hr < 2; hr++) {
                     const int r = rl + 8 * hr;
-                    const float gr = gam[r];
 #pragma unroll
                     for (int k = 0; k < 4; k++) {
                         const int j = half * 32 + 8 * k + cf, q = 4 * k + 2 * hr;
-                        const float g0 = j < r ? expf(gr - gam[j]) * kk[q] : 0.f;
-                        const float g1 = j + 1 < r ? expf(gr - gam[j + 1]) * kk[q + 1] : 0.f;
+                        const float g0 = dec[q] * kk[q];
+                        const float g1 = dec[q + 1] * kk[q + 1];
                         const float d0 = t1[q] * be[j] + t2[q] * bet[j];
                         const float d1 = t1[q + 1] * be[j + 1] + t2[q + 1] * bet[j + 1];
                         *reinterpret_cast<float2*>(GKK + umma::kidx(r, j, 64)) = make_float2(g0, g1);
@@ -1241,8 +1285,8 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
             dbs[tid] += eg[tid] * rp[tid] + rp[64 + tid];
             dgs[tid] += be[tid] * rp[tid];
         }
-        const bool next = tn < ntiles && cn.len > 0;   // the entry has arrived by now
-        const Gates gnext = next ? gates_of(cn, tn) : Gates{0.f, 0.f, 0.f, 0.f};
+        const bool next = tn < ntiles && cn.len > 0;
+        const Gates gnext = next ? gates_of(cn, tn) : Gates{0.f, 0.f, from_f<IO>(0.f), 0.f, 0.f};
         // stage 2 operands: T arrived as a K-major tile, K as an MN-major tile
         ok = __syncthreads_and(umma::mbar_wait(mT, it & 1));
         if (!ok) break;
@@ -1297,7 +1341,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
 #pragma unroll
                 for (int hr = 0; hr < 2; hr++) {
                     const int r = rl + 8 * hr;
-                    const float br = bet[r], gr = gam[r];
+                    const float br = bet[r];
                     const float2 gk = *reinterpret_cast<const float2*>(GKK + umma::kidx(r, m, 64));
 #pragma unroll
                     for (int e = 0; e < 2; e++) {
@@ -1308,7 +1352,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
                         // dKK is strictly lower: (r, m) and its mirror are written by the
                         // thread of the lower element only, the diagonal by its own
                         if (m + e < r) {
-                            const float dk = umma::tf32r(dA * br * expf(gr - gam[m + e]));
+                            const float dk = umma::tf32r(dA * br * dec[4 * k + 2 * hr + e]);
                             dKS[umma::kidx(r, m + e, 64)] = dk;
                             dKS[umma::kidx(m + e, r, 64)] = dk;
                         } else if (m + e == r) {
@@ -1381,7 +1425,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
             umma::store_rows_sw(w.dKv3 + ((int64_t)ci.start * hv + h) * kD, (int64_t)hv * kD, Ks, L);
         }
         // ---- dg = reverse cumsum of dgam; gates
-        if (tid < 64) sc[tid] = tid < L ? dgs[tid] + gcur.dgin : 0.f;
+        if (tid < 64) sc[tid] = tid < L ? dgs[tid] + (gcur.dg1 + gcur.dg2) : 0.f;
         __syncthreads();
         if (tid < 32) {
             float a = sc[63 - 2 * lane], b = sc[62 - 2 * lane], s = a + b;
@@ -1399,8 +1443,9 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         if (tid < L) {
             const int64_t tok = ci.start + tid;
             const float dg = rk[tid];
-            const float gval = -Aexp * softplusf_(gcur.xa);
-            const float dav = dg * (-Aexp) * sigmoidf_(gcur.xa);
+            const float xa = to_f(gcur.a) + dt_bias[h];
+            const float gval = -Aexp * softplusf_(xa);
+            const float dav = dg * (-Aexp) * sigmoidf_(xa);
             const float bb = bet[tid];
             da[tok * hv + h] = from_f<IO>(dav);
             db[tok * hv + h] = from_f<IO>(dbs[tid] * bb * (1.f - bb));
@@ -1424,6 +1469,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         if (!next) break;
         gcur = gnext;
         ci = cn;
+        cn = c2;
         t = tn;
     }
     if (tid == 0) umma::bulk_wait_read();

@@ -115,7 +115,8 @@ gates_kernel(const IO* __restrict__ av, const IO* __restrict__ bv, const float* 
 
 // ------------------------------------------------------------------ prep
 // Persistent: one CTA per SM walks the (chunk, head) tiles t = blockIdx.x,
-// + gridDim.x, ... (chunk = t % NT, head = t / NT).  Per tile, tcgen05, with
+// + gridDim.x, ... (chunk = t / Hv, head = t % Hv: the v-heads of a chunk run
+// side by side, so the q / k tiles they share come from DRAM once).  Per tile, tcgen05, with
 // the gates from gates_kernel:
 //   D1 = K K^T (64 x 64)  ->  A = beta_i e^{gam_i-gam_j} D1 (j < i)
 //   T  = (I + A)^-1        (forward substitution on the CUDA cores; saved)
@@ -156,10 +157,10 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
     const int ntiles = NT * hv;
     int t = blockIdx.x;
     if (t >= ntiles) return;
-    ChunkInfo ci = sv.chunks[t % NT];
+    ChunkInfo ci = sv.chunks[t / hv];
     if (ci.len == 0) return;   // the device check of cu_seqlens failed: every chunk is empty
     auto issue = [&](const ChunkInfo& c, int tile) {   // one thread
-        const int h = tile / NT, kh = h / (hv / hk);
+        const int h = tile % hv, kh = h / (hv / hk);
         umma::mbar_expect_tx(mA, 3 * 64 * 128 * 4);
         umma::tma_rows(Ks, 64, &maps.k, kh, c.start, mA);
         umma::tma_rows(Km, 64, &maps.k_mn, kh, c.start, mA);
@@ -167,7 +168,7 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
     };
     // padding rows continue the last gam (g = 0), beta = 0
     auto gates_of = [&](const ChunkInfo& c, int tile, float& gm, float& bt) {
-        const int h = tile / NT;
+        const int h = tile % hv;
         gm = tid < 64 ? sv.gam[(int64_t)h * sv.T + c.start + min(tid, c.len - 1)] : 0.f;
         bt = tid < c.len ? sv.beta[(int64_t)h * sv.T + c.start + tid] : 0.f;
     };
@@ -178,6 +179,9 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
     }
     float g_cur = 0.f, b_cur = 0.f;
     gates_of(ci, t, g_cur, b_cur);
+    // chunk entries are loaded a tile before they are needed: cn (the next tile's)
+    // is at hand at the top of an iteration, c2 (the one after) is requested there
+    ChunkInfo cn = t + (int)gridDim.x < ntiles ? sv.chunks[(t + (int)gridDim.x) / hv] : ci;
     if (warp == 0) umma::tmem_alloc(tslot, 512);
     umma::fence_before_sync();
     __syncthreads();
@@ -187,13 +191,18 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
     const int half = warp >> 2;
     bool ok = true;
     for (int it = 0;; it++) {
-        const int h = t / NT, L = ci.len;
-        const int tn = t + (int)gridDim.x;
-        const ChunkInfo cn = tn < ntiles ? sv.chunks[tn % NT] : ci;
+        const int h = t % hv, L = ci.len;
+        const int tn = t + (int)gridDim.x, t2 = tn + (int)gridDim.x;
+        const ChunkInfo c2 = t2 < ntiles ? sv.chunks[t2 / hv] : cn;
         if (tid < 64) {
             gam[tid] = g_cur;
             bet[tid] = b_cur;
             be[tid] = b_cur * expf(g_cur);
+        }
+        if (tid == 32 && tn < ntiles && cn.len > 0) {   // the next tile's inputs into L2
+            const int hn = tn % hv;
+            umma::tma_prefetch_rows(&maps.k, hn / (hv / hk), cn.start);
+            umma::tma_prefetch_rows(&maps.v_mn, hn, cn.start);
         }
         if (tid == 0) umma::bulk_wait_read();   // the last tile's stores have read W / U~
         ok = __syncthreads_and(umma::mbar_wait(mA, it & 1));   // K, V; gates visible
@@ -233,7 +242,7 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
             }
         }
         __syncthreads();
-        const bool next = tn < ntiles && cn.len > 0;   // the entry has arrived by now
+        const bool next = tn < ntiles && cn.len > 0;
         float g_next = 0.f, b_next = 0.f;
         if (next) gates_of(cn, tn, g_next, b_next);
         tril_inverse64(As, kLdA, Tr, kLdA, Tk);   // Tk doubles as scratch
@@ -256,7 +265,7 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
             umma::commit(mbar);
         }
         {   // T for the backward, as K-major rows i and as K-major rows j (T^T), rounded
-            float* Tg = sv.Tm + ((int64_t)(t % NT) * hv + h) * 2 * 64 * 64;
+            float* Tg = sv.Tm + ((int64_t)(t / hv) * hv + h) * 2 * 64 * 64;
             for (int idx = tid; idx < 64 * 16; idx += 256) {
                 const int r = idx & 63, c4 = idx >> 6;
                 st4(Tg + umma::kidx(r, 4 * c4, 64),
@@ -303,6 +312,7 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
         g_cur = g_next;
         b_cur = b_next;
         ci = cn;
+        cn = c2;
         t = tn;
     }
     if (tid == 0) umma::bulk_wait_read();
@@ -611,22 +621,33 @@ state_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, const fl
 
 // ------------------------------------------------------------------ output + norm
 // Persistent: one CTA per SM walks the (chunk, head) tiles t = blockIdx.x,
-// + gridDim.x, ... (chunk = t % NT, head = t / NT).  Per tile, tcgen05:
-//   D1 = Q K^T (64 x 64),  D3 = Q S0^T,  DU = W S0^T (64 x 128)  -- issued together
-//   U  = U~ - DU  (rounded; the B operand below, and stored for the backward)
+// + gridDim.x, ... (chunk = t / Hv, head = t % Hv: the v-heads of a chunk run
+// side by side, so the q / k tiles they share come from DRAM once).  Per tile, tcgen05:
+//   [Q; W] [K; S0]^T   one M = 128, N = 192, K = 128 product: rows 0-63 give
+//                      D1 = Q K^T (columns 0-63) and D3 = Q S0^T (64-191),
+//                      rows 64-127 give DU = W S0^T (columns 64-191)
 //   P  = D1 (.) e^{gam_i - gam_j} (.) [i >= j]          -- staged K-major
-//   D2 = P U (64 x 128)
+//   U  = U~ - DU  (rounded; the B operand below, and stored for the backward)
+//   D2 = [P; 0] U   (M = 128: rows 0-63 of the accumulator, like D3)
 //   O  = D2 + e^{gam_i} D3 ; y = O rsqrt(mean(O^2)+eps) (1+w) gate(z)
-// Shared memory: Q, K, W swizzled 32 KB each, S0 64 KB (swizzled, rows a), U~
-// MN-major 32 KB (all by TMA; U is the B operand of P U, contracted
-// over tokens, so U~ arrives MN-major and U is formed in place), P 16 KB.  The
-// next tile's Q, K, W and S0 are requested as soon as the first products are
-// done, its U~ once this tile's O (staged over U) has been stored; its chunk
-// entry and gate values are loaded into registers meanwhile, and each warp
-// fetches the z rows of its norm rows into registers while the products run.
-// Tensor memory: 448 fp32 columns, allocated once.
-constexpr int kOutFloats = 64 * 128 * 3 + 128 * 128 + 64 * 128 + 64 * 64;
-constexpr size_t kOutSmem = sizeof(float) * (kOutFloats + 64 * 2 + 2 * 64 + 16) + 64 + 1024;
+// Stacking Q over W and K over S0 makes the three first products one product
+// of 16 instructions (a tcgen05.mma of M = 64 costs about as much as one of
+// M = 128), and puts P (rows 0-63) and DU (rows 64-127) in different halves of
+// the tensor-memory lanes, so the P epilogue (warps 0, 1, 4, 5) and the U
+// epilogue (warps 2, 3, 6, 7) run at the same time.
+// Shared memory: [Q; W] 64 KB and [K; S0] 96 KB swizzled (TMA into one tile
+// each, rows 128 / 192 apart per box), U~ MN-major 32 KB (then U, then O staged,
+// swizzled), [P; 0] 32 KB K-major (rows 64-127 zero, written once).  The next
+// tile's Q, W, K and S0 are requested as soon as the first product is done, its
+// U~ once this tile's O (staged over U) has been stored; all of them are
+// prefetched into L2 a tile ahead, and its chunk entry and gate values are
+// loaded into registers meanwhile.  While the first product runs, each warp
+// requests the z rows of its norm rows (converted only when used) and the P
+// warps compute their decay factors.  U goes back in place of U~ by one tensor
+// store while P U runs, o by one tensor store from the O staging tile.  Tensor
+// memory: 320 fp32 columns (512 allocated), once.
+constexpr int kOutFloats = 128 * 128 + 192 * 128 + 64 * 128 + 128 * 64;
+constexpr size_t kOutSmem = sizeof(float) * (kOutFloats + 64 * 2 + 2 * 64 + 16) + 32 + 1024;
 
 // Rows 0 .. L-1 of a 64-row MN-major tile to a row-major global tensor, one warp per row.
 __device__ __forceinline__ void store_rows_mn(float* dst, int64_t stride, const float* src, int L) {
@@ -642,42 +663,53 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
                const float* norm_w, float norm_eps, int gate, IO* o_out, IO* y_out, FwdSaved sv) {
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
-    float* Qs = sm;                    // [64][128] swizzled
-    float* Ks = Qs + 64 * 128;         // [64][128] swizzled
-    float* Ws = Ks + 64 * 128;         // [64][128] swizzled (arrives rounded)
-    float* Ss = Ws + 64 * 128;         // [128 (a)][128 (b)] swizzled K-major (arrives rounded)
-    float* Us = Ss + 128 * 128;        // [64 (j)][128 (a)] MN-major U~, then U; then O, swizzled
-    float* Ps = Us + 64 * 128;         // [64 (i)][64 (j)] K-major
-    float* gam = Ps + 64 * 64;
+    float* QW = sm;                    // [4 boxes][128 rows][32]: rows 0-63 Q, 64-127 W (arrives rounded)
+    float* KS = QW + 128 * 128;        // [4 boxes][192 rows][32]: rows 0-63 K, 64-191 S0 (rows a)
+    float* Us = KS + 192 * 128;        // [64 (j)][128 (a)] MN-major U~, then U; then O, swizzled
+    float* P2 = Us + 64 * 128;         // [128 (i)][64 (j)] K-major: P, then zero rows
+    float* gam = P2 + 128 * 64;
     float* eg = gam + 64;
     float* ssq = eg + 64;              // [2][64] partial sums of squares
     uint64_t* mbar = reinterpret_cast<uint64_t*>(ssq + 2 * 64 + 16);   // MMA
-    uint64_t* mA = mbar + 1;           // Q, K, W, S0
+    uint64_t* mA = mbar + 1;           // Q, W, K, S0
     uint64_t* mU = mA + 1;             // U~
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mU + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ntiles = NT * hv;
     int t = blockIdx.x;
     if (t >= ntiles) return;
-    ChunkInfo ci = sv.chunks[t % NT];
+    ChunkInfo ci = sv.chunks[t / hv];
     if (ci.len == 0) return;   // the device check of cu_seqlens failed: every chunk is empty
     auto issue_a = [&](const ChunkInfo& c, int tile) {   // one thread
-        const int h = tile / NT, kh = h / (hv / hk);
-        umma::mbar_expect_tx(mA, 3 * 64 * 128 * 4 + 128 * 128 * 4);
-        umma::tma_rows(Qs, 64, &maps.q, kh, c.start, mA);
-        umma::tma_rows(Ks, 64, &maps.k, kh, c.start, mA);
-        umma::tma_rows(Ws, 64, &maps.W, h, c.start, mA);
-        const int s0row = ((tile % NT) * hv + h) * kD;   // S0 tile rows a = 0 .. 127
-        umma::tma_rows(Ss, 128, &maps.S0, 0, s0row, mA);
-        umma::tma_rows(Ss + 64 * 32, 128, &maps.S0, 0, s0row + 64, mA);
+        const int h = tile % hv, kh = h / (hv / hk);
+        umma::mbar_expect_tx(mA, (128 * 128 + 192 * 128) * 4);
+        umma::tma_rows(QW, 128, &maps.q, kh, c.start, mA);
+        umma::tma_rows(QW + 64 * 32, 128, &maps.W, h, c.start, mA);
+        umma::tma_rows(KS, 192, &maps.k, kh, c.start, mA);
+        const int s0row = ((tile / hv) * hv + h) * kD;   // S0 tile rows a = 0 .. 127
+        umma::tma_rows(KS + 64 * 32, 192, &maps.S0, 0, s0row, mA);
+        umma::tma_rows(KS + 128 * 32, 192, &maps.S0, 0, s0row + 64, mA);
     };
     auto issue_u = [&](const ChunkInfo& c, int tile) {   // one thread
         umma::mbar_expect_tx(mU, 64 * 128 * 4);
-        umma::tma_rows(Us, 64, &maps.U_mn, tile / NT, c.start, mU);
+        umma::tma_rows(Us, 64, &maps.U_mn, tile % hv, c.start, mU);
     };
+    auto prefetch_in = [&](const ChunkInfo& c, int tile) {   // one thread: what issue_a / issue_u load, into L2
+        const int hp = tile % hv, khp = hp / (hv / hk);
+        const int s0p = ((tile / hv) * hv + hp) * kD;
+        umma::tma_prefetch_rows(&maps.q, khp, c.start);
+        umma::tma_prefetch_rows(&maps.k, khp, c.start);
+        umma::tma_prefetch_rows(&maps.W, hp, c.start);
+        umma::tma_prefetch_rows(&maps.S0, 0, s0p);
+        umma::tma_prefetch_rows(&maps.S0, 0, s0p + 64);
+        umma::tma_prefetch_rows(&maps.U_mn, hp, c.start);
+    };
+    // chunk entries are loaded a tile before they are needed: cn (the next tile's)
+    // is at hand at the top of an iteration, c2 (the one after) is requested there
+    ChunkInfo cn = t + (int)gridDim.x < ntiles ? sv.chunks[(t + (int)gridDim.x) / hv] : ci;
     // padding rows continue the last gate value (g = 0)
     auto gam_of = [&](const ChunkInfo& c, int tile) {
-        return tid < 64 ? sv.gam[(int64_t)(tile / NT) * sv.T + c.start + min(tid, c.len - 1)] : 0.f;
+        return tid < 64 ? sv.gam[(int64_t)(tile % hv) * sv.T + c.start + min(tid, c.len - 1)] : 0.f;
     };
     if (tid == 0) {
         umma::mbar_init(mbar, 1);
@@ -686,92 +718,98 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
         issue_a(ci, t);
         issue_u(ci, t);
     }
+    for (int e = tid; e < 64 * 64; e += 256) P2[64 * 64 + e] = 0.f;   // rows 64-127 of [P; 0]
     float g_cur = gam_of(ci, t);
     if (warp == 0) umma::tmem_alloc(tslot, 512);
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t tD1 = tmem, tD3 = tmem + 64, tD2 = tmem + 192, tDU = tmem + 320;
-    const int win = warp & 3, half = warp >> 2;
-    const int i = win * 16 + lane;     // row held by lanes 0..15 (M = 64 layout)
+    const uint32_t tF = tmem, tD2 = tmem + 192;   // first product (192 columns), P U (128)
+    const int q4 = warp & 3, half = warp >> 2;
+    const int row = 32 * (q4 & 1) + lane;   // this thread's accumulator row within its lane half
     const float4 w4 = z ? ld4(norm_w + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
     bool ok = true;
     for (int it = 0;; it++) {
-        const int h = t / NT, L = ci.len;
-        const int tn = t + (int)gridDim.x;
-        const ChunkInfo cn = tn < ntiles ? sv.chunks[tn % NT] : ci;
+        const int h = t % hv, L = ci.len;
+        const int tn = t + (int)gridDim.x, t2 = tn + (int)gridDim.x;
+        const ChunkInfo c2 = t2 < ntiles ? sv.chunks[t2 / hv] : cn;
         if (tid < 64) {
             gam[tid] = g_cur;
             eg[tid] = tid < L ? expf(g_cur) : 0.f;
         }
-        ok = __syncthreads_and(umma::mbar_wait(mA, it & 1));   // Q, K, W, S0; gam visible
+        if (tid == 32 && tn < ntiles && cn.len > 0) prefetch_in(cn, tn);
+        ok = __syncthreads_and(umma::mbar_wait(mA, it & 1));   // Q, W, K, S0; gam visible
         if (!ok) break;
         if (L < 64) {   // tail rows belong to the next sequence
-            umma::zero_tail_rows(Qs, 64, 0, L);
-            umma::zero_tail_rows(Ks, 64, 0, L);
-            umma::zero_tail_rows(Ws, 64, 0, L);
+            umma::zero_tail_rows(QW, 128, 0, L);
+            umma::zero_tail_rows(QW, 128, 64, L);
+            umma::zero_tail_rows(KS, 192, 0, L);
             __syncthreads();
         }
-        if (!sv.qkv_tf32) umma::tf32r_inplace(Qs, 64 * 128 * 2);   // Q, K (W and S0 arrive rounded)
+        if (!sv.qkv_tf32) {   // Q and K (W and S0 arrive rounded: rounding them again changes nothing)
+            umma::tf32r_inplace(QW, 128 * 128);
+            umma::tf32r_inplace(KS, 64 * 128 * 3);
+        }
         umma::fence_smem_to_async();
         __syncthreads();
         umma::fence_after_sync();
         if (tid == 0) {
-            umma::mma(tD1, umma::swt(Qs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
-            umma::mma(tD3, umma::swt(Qs, 64), umma::swt(Ss, 128), 64, 128, 128, false);
-            umma::mma(tDU, umma::swt(Ws, 64), umma::swt(Ss, 128), 64, 128, 128, false);
+            umma::mma(tF, umma::swt(QW, 128), umma::swt(KS, 192), 128, 192, 128, false);
             umma::commit(mbar);
         }
-        // this warp's norm rows r = warp + 8 q: their z values, into registers
-        float4 zr[8];
+        // this warp's norm rows r = warp + 8 q: their z values, into registers (used
+        // last; rows past the chunk repeat its last row and are not stored)
+        raw4_t<IO> zr[8];
         if (z) {
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
-                const int r = warp + 8 * q;
-                zr[q] = r < L ? ld4(z + (((int64_t)ci.start + r) * hv + h) * kD + lane * 4)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int q = 0; q < 8; q++)
+                zr[q] = ld4_raw(z + (((int64_t)ci.start + min(warp + 8 * q, L - 1)) * hv + h) * kD + lane * 4);
+        }
+        // while the product runs, on the warps that form P: the decay factors
+        // e^{gam_i - gam_j} [i >= j] of this thread's row of P, by the hardware
+        // exponential (a few ulp; P is rounded to tf32 next)
+        float dec[32];
+        if (q4 < 2) {
+            const float gi = gam[row];
+#pragma unroll
+            for (int k = 0; k < 32; k++) {
+                const int j = 32 * half + k;
+                dec[k] = j <= row ? __expf(gi - gam[j]) : 0.f;
             }
         }
         ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
         umma::fence_after_sync();
         if (!ok) break;
         const bool next = tn < ntiles && cn.len > 0;
-        if (next && tid == 0) issue_a(cn, tn);   // Q, K, W, S0 consumed
+        if (next && tid == 0) issue_a(cn, tn);   // Q, W, K, S0 consumed
         const float g_next = next ? gam_of(cn, tn) : 0.f;
-        const int rl = umma::frag_row_lo(), cf = umma::frag_col();
-        {   // P = D1 (.) Gam (.) M  -> K-major rows i; 32 columns per warp, all lanes
-            float v[16];
-            umma::tmem_ld_m64<4>(umma::tmem_at(tD1, half * 32), v);
-#pragma unroll
-            for (int hr = 0; hr < 2; hr++) {
-                const int r = rl + 8 * hr;
-                const float gr = gam[r];
-#pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    const int j = half * 32 + 8 * k + cf;
-                    const float p0 = j <= r ? v[4 * k + 2 * hr] * expf(gr - gam[j]) : 0.f;
-                    const float p1 = j + 1 <= r ? v[4 * k + 2 * hr + 1] * expf(gr - gam[j + 1]) : 0.f;
-                    *reinterpret_cast<float2*>(Ps + umma::kidx(r, j, 64)) =
-                        make_float2(umma::tf32r(p0), umma::tf32r(p1));
-                }
-            }
-        }
-        ok = umma::mbar_wait(mU, it & 1);   // U~
-        if (ok) {   // U = U~ - W S0^T in place (rounded), rows past the chunk zero
+        if (q4 < 2) {
+            // P = D1 (.) Gam (.) M -> K-major rows i; row i = row, columns j = 32 half .. + 31
             float v[32];
-            umma::tmem_ld64_m64(umma::tmem_at(tDU, 64 * half), v);
+            umma::tmem_ld32(umma::tmem_at(tF, 32 * half), v);
 #pragma unroll
-            for (int hr = 0; hr < 2; hr++) {
-                const int r = rl + 8 * hr;
+            for (int k = 0; k < 32; k += 4)
+                *reinterpret_cast<float4*>(P2 + umma::kidx(row, 32 * half + k, 64)) = umma::tf32r(
+                    make_float4(v[k] * dec[k], v[k + 1] * dec[k + 1], v[k + 2] * dec[k + 2], v[k + 3] * dec[k + 3]));
+        } else {
+            // U = U~ - W S0^T in place (rounded), rows past the chunk zero; row i = row,
+            // columns a = 64 half .. + 63 (accumulator rows 64-127, columns 64-191)
+            ok = __all_sync(0xffffffffu, umma::mbar_wait(mU, it & 1));   // U~ (warp-uniform)
+            if (ok) {
+                const int i = row;
 #pragma unroll
-                for (int k = 0; k < 8; k++) {
-                    const int c = 64 * half + 8 * k + cf;
-                    float2* p = reinterpret_cast<float2*>(Us + umma::swz_mn(r, c));
-                    const float2 u = *p;
-                    *p = r < L ? make_float2(umma::tf32r(u.x - v[4 * k + 2 * hr]),
-                                             umma::tf32r(u.y - v[4 * k + 2 * hr + 1]))
-                               : make_float2(0.f, 0.f);
+                for (int cc = 0; cc < 64; cc += 32) {
+                    float v[32];
+                    umma::tmem_ld32(umma::tmem_at(tF, 64 + 64 * half + cc), v);
+#pragma unroll
+                    for (int k = 0; k < 32; k += 4) {
+                        float4* p = reinterpret_cast<float4*>(Us + umma::swz_mn(i, 64 * half + cc + k));
+                        const float4 u = *p;
+                        *p = i < L ? umma::tf32r(make_float4(u.x - v[k], u.y - v[k + 1], u.z - v[k + 2],
+                                                             u.w - v[k + 3]))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                 }
             }
         }
@@ -780,43 +818,56 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
         ok = __syncthreads_and(ok);
         umma::fence_after_sync();
         if (!ok) break;
+        // U for the backward (only ever a tensor-core operand: stored rounded) while
+        // P U runs: a whole chunk by one tensor store in place of U~, a partial one
+        // row by row
         if (tid == 0) {
-            umma::mma(tD2, umma::kmaj(Ps, 64), umma::mnt(Us), 64, 128, 64, false);
+            umma::mma(tD2, umma::kmaj(P2, 64), umma::mnt(Us), 128, 128, 64, false);
             umma::commit(mbar);
+            if (L == 64) {
+                umma::tma_store_rows(&maps.U_mn, h, ci.start, Us);
+                umma::bulk_commit();
+            }
         }
-        // U for the backward (only ever a tensor-core operand: stored rounded), row by
-        // row while P U runs
-        store_rows_mn(sv.U + ((int64_t)ci.start * hv + h) * kD, (int64_t)hv * kD, Us, L);
+        if (L < 64) store_rows_mn(sv.U + ((int64_t)ci.start * hv + h) * kD, (int64_t)hv * kD, Us, L);
+        if (tid == 0) umma::bulk_wait_read();   // the U store has read the tile O goes over
         ok = __syncthreads_and(umma::mbar_wait(mbar, 1));   // and the U rows are read
         umma::fence_after_sync();
         if (!ok) break;
-        // O = D2 + e^{gam_i} D3, staged as a swizzled tile over U (consumed);
-        // the norm and the stores then run row by row on all lanes, one warp
-        // per row, fully coalesced
+        // O = D2 + e^{gam_i} D3 (accumulator rows 0-63: warps 0, 1, 4, 5), staged as a
+        // swizzled tile over U (consumed) and stored from there by one tensor store;
+        // the norm and the y stores then run row by row on all lanes, one warp per
+        // row, fully coalesced
         float* Or = Us;
-        {
+        if (q4 < 2) {
+            const int i = row;
+            const float e = eg[i];
             float ss = 0.f;
-            for (int cc = 0; cc < 64; cc += 16) {
-                float v2[16], v3[16];
-                umma::tmem_ld16(umma::tmem_at(tD2, half * 64 + cc), v2);
-                umma::tmem_ld16(umma::tmem_at(tD3, half * 64 + cc), v3);
-                if (lane < 16) {
 #pragma unroll
-                    for (int u = 0; u < 16; u += 4) {
-                        float4 x;
-                        x.x = v2[u] + eg[i] * v3[u];
-                        x.y = v2[u + 1] + eg[i] * v3[u + 1];
-                        x.z = v2[u + 2] + eg[i] * v3[u + 2];
-                        x.w = v2[u + 3] + eg[i] * v3[u + 3];
-                        ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
-                        *reinterpret_cast<float4*>(Or + umma::swz(i, half * 64 + cc + u, 64)) = x;
-                    }
+            for (int cc = 0; cc < 64; cc += 32) {
+                float v2[32], v3[32];
+                umma::tmem_ld32(umma::tmem_at(tD2, 64 * half + cc), v2);
+                umma::tmem_ld32(umma::tmem_at(tF, 64 + 64 * half + cc), v3);
+#pragma unroll
+                for (int k = 0; k < 32; k += 4) {
+                    float4 x;
+                    x.x = v2[k] + e * v3[k];
+                    x.y = v2[k + 1] + e * v3[k + 1];
+                    x.z = v2[k + 2] + e * v3[k + 2];
+                    x.w = v2[k + 3] + e * v3[k + 3];
+                    ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+                    *reinterpret_cast<float4*>(Or + umma::swz(i, 64 * half + cc + k, 64)) = x;
                 }
             }
-            if (lane < 16) ssq[half * 64 + i] = ss;
+            ssq[half * 64 + i] = ss;
         }
+        umma::fence_smem_to_async();
         umma::fence_before_sync();
         __syncthreads();
+        if (L == 64 && tid == 0) {   // o (fp32, for the backward) by one tensor store
+            umma::tma_store_rows(&maps.o, h, ci.start, Or);
+            umma::bulk_commit();
+        }
         // this warp's eight rows: all reads first, then the math and the stores
         // (independent rows, so their latencies overlap); rows past the chunk are
         // read from the staging tile but not stored
@@ -834,20 +885,24 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
             if (r < L) {
                 const int64_t tok = ci.start + r;
                 const int64_t off = (tok * hv + h) * kD + lane * 4;
-                st4(sv.o + off, o4s[q]);
+                if (L < 64) st4(sv.o + off, o4s[q]);   // (a whole chunk's went by tensor store)
                 if (o_out) st4(o_out + off, o4s[q]);
                 if (z) {
-                    st4(y_out + off, gated_norm4(o4s[q], rss[q], w4, zr[q], gate));
+                    st4(y_out + off, gated_norm4(o4s[q], rss[q], w4, cvt4(zr[q]), gate));
                     if (lane == 0) sv.rstd[tok * hv + h] = rss[q];
                 }
             }
         }
-        umma::fence_smem_to_async();   // O staging -> the next U~ load
+        umma::fence_smem_to_async();   // O staging reads -> the next U~ load
         __syncthreads();               // O and the sums of squares are read
         if (!next) break;
-        if (tid == 0) issue_u(cn, tn);
+        if (tid == 0) {
+            umma::bulk_wait_read();    // the o store has read the staging tile
+            issue_u(cn, tn);
+        }
         g_cur = g_next;
         ci = cn;
+        cn = c2;
         t = tn;
     }
     if (tid == 0) umma::bulk_wait_read();
@@ -889,6 +944,7 @@ static cudaError_t chunk_fwd_t(const ChunkArgs& a, cudaStream_t st) {
         if (e == cudaSuccess) e = make_rows_map(&maps.W, a.sv.W, a.hv, a.T, (int64_t)a.hv * kD);
         if (e == cudaSuccess)
             e = make_rows_map(&maps.U_mn, a.sv.U, a.hv, a.T, (int64_t)a.hv * kD, true);
+        if (e == cudaSuccess) e = make_rows_map(&maps.o, a.sv.o, a.hv, a.T, (int64_t)a.hv * kD);
         if (e == cudaSuccess)
             e = make_rows_map(&maps.W_mn, a.sv.W, a.hv, a.T, (int64_t)a.hv * kD, true);
         if (e == cudaSuccess)

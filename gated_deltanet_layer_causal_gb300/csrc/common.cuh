@@ -31,6 +31,17 @@ __device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
     float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
     return make_float4(a.x, a.y, b.x, b.y);
 }
+// The same 4 elements as loaded, converted later by cvt4: a load whose value is
+// first used long after it is issued stays in flight meanwhile.
+__device__ __forceinline__ float4 ld4_raw(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ uint2 ld4_raw(const __nv_bfloat16* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ float4 cvt4(float4 v) { return v; }
+__device__ __forceinline__ float4 cvt4(uint2 u) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+template <class T> using raw4_t = decltype(ld4_raw(static_cast<const T*>(nullptr)));
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 __device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
@@ -41,7 +52,11 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
 }
 
 // ----------------------------------------------------------------- math
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + __expf(-x)); }
+// The hardware exponential and reciprocal (a few ulp): the kernels that apply
+// these gates run few warps per SM, where the full-precision reciprocal's
+// dependent refinement steps are exposed latency.  Below x = -87 the result is
+// 0 where the true value is under 2^-125.
+__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 __device__ __forceinline__ float siluf_(float x) { return x * sigmoidf_(x); }
 
 // Output gate of the gated norm (prime-rl #3860 "Summary": GatedDeltaNet takes

@@ -71,7 +71,7 @@ struct FwdSaved {
 constexpr int kTileCols = 128;
 struct TileMaps {
     CUtensorMap q, k, v;   // q / k / v channels of the conv output [T, C]
-    CUtensorMap W, U;      // [T, Hv, d]
+    CUtensorMap W, U, o;   // [T, Hv, d]
     CUtensorMap dO, dU, dW;
     CUtensorMap dQv, dKv, dQv2, dKv2, dKv3;
     CUtensorMap dv;        // v channels of the conv-output gradient [T, C]

@@ -263,6 +263,13 @@ __device__ __forceinline__ void tma_prefetch_rows(const CUtensorMap* map, int he
                      "r"(b * 32), "r"(head), "r"(t0)
                      : "memory");
 }
+// Prefetch `bytes` (a multiple of 16) of contiguous global memory at p
+// (16-byte aligned) into L2.
+__device__ __forceinline__ void bulk_prefetch(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(reinterpret_cast<uint64_t>(p)),
+                 "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_box(const CUtensorMap* map, int x, int head, int t0) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
