@@ -77,7 +77,8 @@ chunk_norm_bwd_kernel(const float* __restrict__ o, const IO* __restrict__ z,
 }
 
 // ------------------------------------------------------------------ B1: local
-// grid (NT, Hv), 256 threads, tcgen05.
+// grid NT * Hv (block = chunk * Hv + head: the v-heads of a chunk run side by
+// side, so the q / k tiles they share come from DRAM once), 256 threads, tcgen05.
 //   D1 = K Q^T (64 x 64)  ->  P^T[j][i] = D1[j][i] e^{gam_i-gam_j} [i >= j]
 //   D2 = P^T dO           ->  dU_local (64 x 128)
 // Shared memory: Q, K swizzled and dO MN-major, 32 KB each (TMA; dO is the B
@@ -101,10 +102,10 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
     uint64_t* mbl = mbar + 1;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
     // the P / dP kernel, launched after this one, claims its tiles from this counter
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *w.dp_next = 0;
-    const ChunkInfo ci = sv.chunks[blockIdx.x];
+    if (blockIdx.x == 0 && threadIdx.x == 0) *w.dp_next = 0;
+    const ChunkInfo ci = sv.chunks[blockIdx.x / hv];
     if (ci.len == 0) return;
-    const int h = blockIdx.y, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
+    const int h = blockIdx.x % hv, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
     const int warp = tid >> 5;
     if (tid == 0) {
         umma::mbar_init(mbar, 1);
@@ -134,24 +135,36 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
         umma::mma(tD1, umma::swt(Ks, 64), umma::swt(Qs, 64), 64, 64, 128, false);
         umma::commit(mbar);
     }
+    // while the product runs: the decay factors e^{gam_i - gam_j} [i >= j] of this
+    // thread's fragment (rows j, columns i)
+    const int half = warp >> 2;
+    const int rl = umma::frag_row_lo(), cf = umma::frag_col();
+    float dec[16];
+#pragma unroll
+    for (int hr = 0; hr < 2; hr++) {
+        const int jr = rl + 8 * hr;
+        const float gj = gam[jr];
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+                const int i = half * 32 + 8 * k + cf + e;
+                dec[4 * k + 2 * hr + e] = i >= jr ? expf(gam[i] - gj) : 0.f;
+            }
+    }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
-    const int half = warp >> 2;
     if (ok) {   // P^T[j][i], 32 columns per warp, all lanes
         float v[16];
         umma::tmem_ld_m64<4>(umma::tmem_at(tD1, half * 32), v);
-        const int rl = umma::frag_row_lo(), cf = umma::frag_col();
 #pragma unroll
         for (int hr = 0; hr < 2; hr++) {
             const int jr = rl + 8 * hr;
-            const float gj = gam[jr];
 #pragma unroll
             for (int k = 0; k < 4; k++) {
-                const int i = half * 32 + 8 * k + cf;
-                const float p0 = i >= jr ? v[4 * k + 2 * hr] * expf(gam[i] - gj) : 0.f;
-                const float p1 = i + 1 >= jr ? v[4 * k + 2 * hr + 1] * expf(gam[i + 1] - gj) : 0.f;
+                const int i = half * 32 + 8 * k + cf, q = 4 * k + 2 * hr;
                 *reinterpret_cast<float2*>(PT + umma::kidx(jr, i, 64)) =
-                    make_float2(umma::tf32r(p0), umma::tf32r(p1));
+                    make_float2(umma::tf32r(v[q] * dec[q]), umma::tf32r(v[q + 1] * dec[q + 1]));
             }
         }
     }
@@ -822,13 +835,11 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
     uint64_t* mA = reinterpret_cast<uint64_t*>(gam + 64);   // swizzled operands
     uint64_t* mB = mA + 1;             // MN-major operands
     uint64_t* mM = mB + 1;             // MMA
-    int32_t* claim = reinterpret_cast<int32_t*>(mM + 1);   // [2] claimed tile, slot per parity
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(claim + 2);
+    int32_t* claim = reinterpret_cast<int32_t*>(mM + 1);   // [3] claimed tiles, slot it % 3
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(claim + 3);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ntiles = NT * hv;
-    auto issue_a = [&](int tile) {   // one thread
-        const ChunkInfo c = sv.chunks[tile / hv];
-        if (c.len == 0) return;
+    auto issue_a = [&](const ChunkInfo& c, int tile) {   // one thread
         const int h = tile % hv, kh = h / (hv / hk);
         umma::mbar_expect_tx(mA, 4 * 64 * 128 * 4);
         umma::tma_rows(Qs, 64, &maps.q, kh, c.start, mA);
@@ -836,9 +847,7 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         umma::tma_rows(dOs, 64, &maps.dO, h, c.start, mA);
         umma::tma_rows(Us, 64, &maps.U, h, c.start, mA);
     };
-    auto issue_b = [&](int tile) {   // one thread
-        const ChunkInfo c = sv.chunks[tile / hv];
-        if (c.len == 0) return;
+    auto issue_b = [&](const ChunkInfo& c, int tile) {   // one thread
         const int kh = (tile % hv) / (hv / hk);
         umma::mbar_expect_tx(mB, 2 * 64 * 128 * 4);
         umma::tma_rows(Qm, 64, &maps.q_mn, kh, c.start, mB);
@@ -850,9 +859,13 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         umma::mbar_init(mM, 1);
         const int t0 = atomicAdd(w.dp_next, 1);
         claim[0] = t0;
+        claim[1] = atomicAdd(w.dp_next, 1);
         if (t0 < ntiles) {
-            issue_a(t0);
-            issue_b(t0);
+            const ChunkInfo c0 = sv.chunks[t0 / hv];
+            if (c0.len > 0) {
+                issue_a(c0, t0);
+                issue_b(c0, t0);
+            }
         }
     }
     if (warp == 0) umma::tmem_alloc(tslot, 256);
@@ -863,13 +876,20 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
     const uint32_t tQK = tmem, tDOU = tmem + 64, tDQ = tmem, tDK = tmem + 128;
     const int win = warp & 3, half = warp >> 2;
     const int rl = umma::frag_row_lo(), cf = umma::frag_col();
-    int t = claim[0];
+    // Tiles are claimed two ahead (the claim for iteration it + 2 is made during
+    // iteration it), so a tile's chunk entry is loaded an iteration before its
+    // operands are requested and its gate values an iteration before they are
+    // used: no thread waits on a global load at the top of a tile.
+    int t = claim[0], tn = claim[1];
+    ChunkInfo ci = t < ntiles ? sv.chunks[t / hv] : ChunkInfo{0, 0, 0, 0};
+    ChunkInfo cn = tn < ntiles ? sv.chunks[tn / hv] : ci;
+    float g_cur = 0.f;
+    if (tid < 64 && t < ntiles) g_cur = sv.gam[(int64_t)(t % hv) * sv.T + ci.start + min(tid, ci.len - 1)];
     bool ok = true;
     for (int it = 0; t < ntiles; it++) {
-        const ChunkInfo ci = sv.chunks[t / hv];
         const int h = t % hv, L = ci.len;
         if (L == 0) break;   // the device check of cu_seqlens failed: every chunk is empty
-        load_gam(gam, sv, ci, h);
+        if (tid < 64) gam[tid] = g_cur;
         ok = umma::named_sync_and(1, 256, umma::mbar_wait(mA, it & 1));   // Q, K, dO, U; gam visible
         if (!ok) break;
         if (L < 64) {   // tail rows belong to the next sequence
@@ -887,7 +907,7 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
             umma::mma(tQK, umma::swt(Qs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
             umma::mma(tDOU, umma::swt(dOs, 64), umma::swt(Us, 64), 64, 64, 128, false);
             umma::commit(mM);
-            claim[(it + 1) & 1] = atomicAdd(w.dp_next, 1);   // the next tile
+            claim[(it + 2) % 3] = atomicAdd(w.dp_next, 1);   // the tile after the next
         }
         // while the products run: the decay factors e^{gam_r - gam_j} [j <= r] of this
         // thread's fragment
@@ -907,8 +927,11 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         ok = umma::named_sync_and(1, 256, umma::mbar_wait(mM, 0));   // the claim is visible too
         umma::fence_after_sync();
         if (!ok) break;
-        const int tn = claim[(it + 1) & 1];
-        if (tid == 0 && tn < ntiles) issue_a(tn);   // the swizzled operands are consumed
+        const int t2 = claim[(it + 2) % 3];
+        ChunkInfo c2 = cn;   // used an iteration later
+        if (t2 < ntiles) c2 = sv.chunks[t2 / hv];
+        const bool next = tn < ntiles && cn.len > 0;
+        if (tid == 0 && next) issue_a(cn, tn);   // the swizzled operands are consumed
         {   // 32 columns per warp, all lanes; R row / column sums by shuffles
             float qk[16], du[16];
             umma::tmem_ld_m64<4>(umma::tmem_at(tQK, half * 32), qk);
@@ -965,6 +988,8 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
             umma::mma(tDK, umma::kmaj(dPC, 64), umma::mnt(Qm), 64, 128, 64, false);
             umma::commit(mM);
         }
+        float g_next = 0.f;   // the next tile's gate values, used an iteration later
+        if (tid < 64 && next) g_next = sv.gam[(int64_t)(tn % hv) * sv.T + cn.start + min(tid, cn.len - 1)];
         if (tid < 64 && tid < L) {   // dgam from R: row sums minus column sums (fixed order)
             const float cs = (colp[tid] + colp[64 + tid]) + (colp[128 + tid] + colp[192 + tid]);
             w.dgam2[(int64_t)(ci.start + tid) * hv + h] = (rpart[tid] + rpart[64 + tid]) - cs;
@@ -972,7 +997,7 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         ok = umma::named_sync_and(1, 256, umma::mbar_wait(mM, 1));
         umma::fence_after_sync();
         if (!ok) break;
-        if (tid == 0 && tn < ntiles) issue_b(tn);   // the MN-major operands are consumed
+        if (tid == 0 && next) issue_b(cn, tn);   // the MN-major operands are consumed
         {   // D_dq, D_dk rows rl, rl + 8 (those inside the chunk) straight to the partials
             const int64_t o_lo = ((int64_t)(ci.start + rl) * hv + h) * kD;
             const int64_t o_hi = o_lo + (int64_t)8 * hv * kD;
@@ -995,6 +1020,10 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         umma::fence_before_sync();
         umma::named_sync(1, 256);   // tensor memory read before the next tile's products reuse it
         t = tn;
+        tn = t2;
+        ci = cn;
+        cn = c2;
+        g_cur = g_next;
     }
     umma::fence_before_sync();
     umma::named_sync(1, 256);
@@ -1037,9 +1066,10 @@ bwd_state_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int N
 //   dbeta_j += sum_m dA (.) GamKK ; dgam_j += beta_j (..) ; dgam_m -= sum_j beta_j (..)
 //   dK += (dKK + dKK^T) K   (one product: the two triangles are disjoint)
 // then dg = reverse in-chunk cumsum of the total dgam, and the gate gradients.
-// The next tile's operands are requested in three groups as their space frees
-// up: dW, dU (K-major) and T^T once dA is formed, dW, dU (MN-major) and V once
-// the last product is done, K once this tile's dK store has read it; its gate
+// The next tile's operands are requested in two groups as their space frees
+// up: dW, dU (K-major) and T^T once dA is formed, dW, dU (MN-major), V and K
+// once the last product is done (dK goes to global memory straight from the
+// fragments); all of them are prefetched into L2 a tile ahead, and its gate
 // inputs are loaded into registers meanwhile.  Tensor memory allocated once.
 constexpr int kWyFloats = 4 * 64 * 128 + 256 * 64 + 64 * 64;   // stage-1 operands
 constexpr size_t kWySmem = sizeof(float) * (kWyFloats + 10 * 64 + 2 * 64 + 16) + 64 + 1024;
@@ -1160,9 +1190,10 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     for (int it = 0;; it++) {
         const int h = t % hv, kh = h / (hv / hk), L = ci.len, chunk = t / hv;
         const int tn = t + (int)gridDim.x, t2 = tn + (int)gridDim.x;
-        const ChunkInfo c2 = t2 < ntiles ? sv.chunks[t2 / hv] : cn;
+        ChunkInfo c2 = cn;
+        if (t2 < ntiles) c2 = sv.chunks[t2 / hv];
         auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
-        const float Aexp = expf(A_log[h]);
+        const float alog = A_log[h], dtb = dt_bias[h];   // first used at the end of the tile
         if (tid == 32 && tn < ntiles && cn.len > 0) {   // the next tile's inputs into L2
             const int hn = tn % hv;
             umma::tma_prefetch_rows(&maps.dW, hn, cn.start);
@@ -1394,35 +1425,31 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         ok = __syncthreads_and(umma::mbar_wait(mbar, 1));
         umma::fence_after_sync();
         if (!ok) break;
-        // dKK, K (MN-major) and V (with the column sums over it) are consumed: the
-        // next tile's dW, dU (MN-major) and V
-        if (next && tid == 0) issue_m(cn, tn);
-        // dK part = dKK product + diag(beta e^gam) T^T dW, staged as a swizzled
-        // tile in the K space (consumed) and stored whole
+        // dKK, K (both layouts) and V (with the column sums over it) are consumed:
+        // the next tile's dW, dU (MN-major), V and K
+        if (next && tid == 0) {
+            issue_m(cn, tn);
+            issue_k(cn, tn);
+        }
+        // dK part = dKK product + diag(beta e^gam) T^T dW, rows rl, rl + 8 (those
+        // inside the chunk) straight from the fragments
         {
             float vk[32], vw[32];
             umma::tmem_ld64_m64(umma::tmem_at(tX, half * 64), vk);
             umma::tmem_ld64_m64(umma::tmem_at(tTW, half * 64), vw);
             const float bl = be[rl], bh = be[rl + 8];
+            float* dk_lo = w.dKv3 + ((int64_t)(ci.start + rl) * hv + h) * kD;
+            float* dk_hi = dk_lo + (int64_t)8 * hv * kD;
 #pragma unroll
             for (int k = 0; k < 8; k++) {
-                vk[4 * k] += bl * vw[4 * k];
-                vk[4 * k + 1] += bl * vw[4 * k + 1];
-                vk[4 * k + 2] += bh * vw[4 * k + 2];
-                vk[4 * k + 3] += bh * vw[4 * k + 3];
+                const int c = half * 64 + 8 * k + cf;
+                if (rl < L)
+                    *reinterpret_cast<float2*>(dk_lo + c) =
+                        make_float2(vk[4 * k] + bl * vw[4 * k], vk[4 * k + 1] + bl * vw[4 * k + 1]);
+                if (rl + 8 < L)
+                    *reinterpret_cast<float2*>(dk_hi + c) =
+                        make_float2(vk[4 * k + 2] + bh * vw[4 * k + 2], vk[4 * k + 3] + bh * vw[4 * k + 3]);
             }
-            umma::frag_to_sw(Ks, vk, half * 64, 1.f, 1.f);
-        }
-        umma::fence_smem_to_async();
-        umma::fence_before_sync();
-        __syncthreads();
-        if (L == 64) {
-            if (tid == 0) {
-                umma::tma_store_rows(&maps.dKv3, h, ci.start, Ks);
-                umma::bulk_commit();
-            }
-        } else {
-            umma::store_rows_sw(w.dKv3 + ((int64_t)ci.start * hv + h) * kD, (int64_t)hv * kD, Ks, L);
         }
         // ---- dg = reverse cumsum of dgam; gates
         if (tid < 64) sc[tid] = tid < L ? dgs[tid] + (gcur.dg1 + gcur.dg2) : 0.f;
@@ -1443,7 +1470,8 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         if (tid < L) {
             const int64_t tok = ci.start + tid;
             const float dg = rk[tid];
-            const float xa = to_f(gcur.a) + dt_bias[h];
+            const float Aexp = expf(alog);
+            const float xa = to_f(gcur.a) + dtb;
             const float gval = -Aexp * softplusf_(xa);
             const float dav = dg * (-Aexp) * sigmoidf_(xa);
             const float bb = bet[tid];
@@ -1462,8 +1490,6 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
         if (tid == 0) {
             gate_part[((int64_t)chunk * hv + h) * 2 + 0] = red[0] + red[1];
             gate_part[((int64_t)chunk * hv + h) * 2 + 1] = red[2] + red[3];
-            umma::bulk_wait_read();   // the dK tile store has read its shared memory
-            if (next) issue_k(cn, tn);
         }
         __syncthreads();   // gate sums and the tile's scalars are read
         if (!next) break;
@@ -1628,7 +1654,7 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
                                               w.nw_part);
         }
         GDN_PROF("chunk_bwd_local", st);
-        bwd_local_kernel<<<dim3(a.NT, a.hv), 256, kB1Smem, st>>>(maps, a.hk, a.hv, a.sv, w);
+        bwd_local_kernel<<<a.NT * a.hv, 256, kB1Smem, st>>>(maps, a.hk, a.hv, a.sv, w);
     }
     {
         // the reverse state pass (CTAs 0 .. n_state - 1) and the P / dP tiles

@@ -167,10 +167,13 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
         umma::tma_rows(Vm, 64, &maps.v_mn, h, c.start, mA);
     };
     // padding rows continue the last gam (g = 0), beta = 0
+    // (predicated loads: the values are first used a tile later)
     auto gates_of = [&](const ChunkInfo& c, int tile, float& gm, float& bt) {
         const int h = tile % hv;
-        gm = tid < 64 ? sv.gam[(int64_t)h * sv.T + c.start + min(tid, c.len - 1)] : 0.f;
-        bt = tid < c.len ? sv.beta[(int64_t)h * sv.T + c.start + tid] : 0.f;
+        gm = 0.f;
+        bt = 0.f;
+        if (tid < 64) gm = sv.gam[(int64_t)h * sv.T + c.start + min(tid, c.len - 1)];
+        if (tid < c.len) bt = sv.beta[(int64_t)h * sv.T + c.start + tid];
     };
     if (tid == 0) {
         umma::mbar_init(mbar, 1);
@@ -193,12 +196,15 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
     for (int it = 0;; it++) {
         const int h = t % hv, L = ci.len;
         const int tn = t + (int)gridDim.x, t2 = tn + (int)gridDim.x;
-        const ChunkInfo c2 = t2 < ntiles ? sv.chunks[t2 / hv] : cn;
+        ChunkInfo c2 = cn;
+        if (t2 < ntiles) c2 = sv.chunks[t2 / hv];
         if (tid < 64) {
             gam[tid] = g_cur;
             bet[tid] = b_cur;
             be[tid] = b_cur * expf(g_cur);
         }
+        float g_next = 0.f, b_next = 0.f;   // the next tile's gates, requested here
+        if (tn < ntiles && cn.len > 0) gates_of(cn, tn, g_next, b_next);
         if (tid == 32 && tn < ntiles && cn.len > 0) {   // the next tile's inputs into L2
             const int hn = tn % hv;
             umma::tma_prefetch_rows(&maps.k, hn / (hv / hk), cn.start);
@@ -221,34 +227,45 @@ prep_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, FwdSa
             umma::mma(tD1, umma::swt(Ks, 64), umma::swt(Ks, 64), 64, 64, 128, false);
             umma::commit(mbar);
         }
+        // while the product runs: beta_i e^{gam_i - gam_j} [j < i] of this thread's
+        // fragment of the 64 x 64 product
+        const int rl = umma::frag_row_lo(), cf = umma::frag_col();
+        float dec[16];
+#pragma unroll
+        for (int hr = 0; hr < 2; hr++) {
+            const int r = rl + 8 * hr;
+            const float br = bet[r], gr = gam[r];
+#pragma unroll
+            for (int k = 0; k < 4; k++)
+#pragma unroll
+                for (int e = 0; e < 2; e++) {
+                    const int j = half * 32 + 8 * k + cf + e;
+                    dec[4 * k + 2 * hr + e] = j < r ? br * expf(gr - gam[j]) : 0.f;
+                }
+        }
         ok = __syncthreads_and(umma::mbar_wait(mbar, 0));
         umma::fence_after_sync();
         if (!ok) break;
         {   // A = beta_i e^{gam_i - gam_j} D1 (j < i); 32 columns per warp, all lanes
             float v[16];
             umma::tmem_ld_m64<4>(umma::tmem_at(tD1, half * 32), v);
-            const int rl = umma::frag_row_lo(), cf = umma::frag_col();
 #pragma unroll
             for (int hr = 0; hr < 2; hr++) {
                 const int r = rl + 8 * hr;
-                const float br = bet[r], gr = gam[r];
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
-                    const int j = half * 32 + 8 * k + cf;
-                    *reinterpret_cast<float2*>(As + r * kLdA + j) = make_float2(
-                        j < r ? br * expf(gr - gam[j]) * v[4 * k + 2 * hr] : 0.f,
-                        j + 1 < r ? br * expf(gr - gam[j + 1]) * v[4 * k + 2 * hr + 1] : 0.f);
+                    const int j = half * 32 + 8 * k + cf, q = 4 * k + 2 * hr;
+                    *reinterpret_cast<float2*>(As + r * kLdA + j) =
+                        make_float2(dec[q] * v[q], dec[q + 1] * v[q + 1]);
                 }
             }
         }
         __syncthreads();
         const bool next = tn < ntiles && cn.len > 0;
-        float g_next = 0.f, b_next = 0.f;
-        if (next) gates_of(cn, tn, g_next, b_next);
         tril_inverse64(As, kLdA, Tr, kLdA, Tk);   // Tk doubles as scratch
         __syncthreads();
-        for (int idx = tid; idx < 64 * 16; idx += 256) {   // T diag(.) -> K-major rows i
-            const int r = idx >> 4, c = (idx & 15) * 4;
+        for (int idx = tid; idx < 64 * 16; idx += 256) {   // T diag(.) -> K-major rows i (lane = row)
+            const int r = idx & 63, c = (idx >> 6) * 4;
             const float4 t4 = *reinterpret_cast<const float4*>(Tr + r * kLdA + c);
             *reinterpret_cast<float4*>(Tk + umma::kidx(r, c, 64)) = umma::tf32r(
                 make_float4(t4.x * be[c], t4.y * be[c + 1], t4.z * be[c + 2], t4.w * be[c + 3]));
@@ -707,9 +724,12 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
     // chunk entries are loaded a tile before they are needed: cn (the next tile's)
     // is at hand at the top of an iteration, c2 (the one after) is requested there
     ChunkInfo cn = t + (int)gridDim.x < ntiles ? sv.chunks[(t + (int)gridDim.x) / hv] : ci;
-    // padding rows continue the last gate value (g = 0)
+    // padding rows continue the last gate value (g = 0); a predicated load, first
+    // used a tile later
     auto gam_of = [&](const ChunkInfo& c, int tile) {
-        return tid < 64 ? sv.gam[(int64_t)(tile % hv) * sv.T + c.start + min(tid, c.len - 1)] : 0.f;
+        float g = 0.f;
+        if (tid < 64) g = sv.gam[(int64_t)(tile % hv) * sv.T + c.start + min(tid, c.len - 1)];
+        return g;
     };
     if (tid == 0) {
         umma::mbar_init(mbar, 1);
@@ -730,33 +750,42 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
     const int row = 32 * (q4 & 1) + lane;   // this thread's accumulator row within its lane half
     const float4 w4 = z ? ld4(norm_w + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
     bool ok = true;
+    // issued: this tile's first product was issued at the end of the previous
+    // iteration (a whole chunk, operands already tf32), so it runs while that
+    // tile's norm and stores do; its gate values are in shared memory then too
+    bool issued = false;
     for (int it = 0;; it++) {
         const int h = t % hv, L = ci.len;
         const int tn = t + (int)gridDim.x, t2 = tn + (int)gridDim.x;
-        const ChunkInfo c2 = t2 < ntiles ? sv.chunks[t2 / hv] : cn;
-        if (tid < 64) {
+        ChunkInfo c2 = cn;
+        if (t2 < ntiles) c2 = sv.chunks[t2 / hv];
+        if (tid < 64 && !issued) {
             gam[tid] = g_cur;
             eg[tid] = tid < L ? expf(g_cur) : 0.f;
         }
         if (tid == 32 && tn < ntiles && cn.len > 0) prefetch_in(cn, tn);
+        float g_next = 0.f;   // the next tile's gate values, requested here
+        if (tn < ntiles && cn.len > 0) g_next = gam_of(cn, tn);
         ok = __syncthreads_and(umma::mbar_wait(mA, it & 1));   // Q, W, K, S0; gam visible
         if (!ok) break;
-        if (L < 64) {   // tail rows belong to the next sequence
-            umma::zero_tail_rows(QW, 128, 0, L);
-            umma::zero_tail_rows(QW, 128, 64, L);
-            umma::zero_tail_rows(KS, 192, 0, L);
+        if (!issued) {
+            if (L < 64) {   // tail rows belong to the next sequence
+                umma::zero_tail_rows(QW, 128, 0, L);
+                umma::zero_tail_rows(QW, 128, 64, L);
+                umma::zero_tail_rows(KS, 192, 0, L);
+                __syncthreads();
+            }
+            if (!sv.qkv_tf32) {   // Q and K (W and S0 arrive rounded: rounding them again changes nothing)
+                umma::tf32r_inplace(QW, 128 * 128);
+                umma::tf32r_inplace(KS, 64 * 128 * 3);
+            }
+            umma::fence_smem_to_async();
             __syncthreads();
-        }
-        if (!sv.qkv_tf32) {   // Q and K (W and S0 arrive rounded: rounding them again changes nothing)
-            umma::tf32r_inplace(QW, 128 * 128);
-            umma::tf32r_inplace(KS, 64 * 128 * 3);
-        }
-        umma::fence_smem_to_async();
-        __syncthreads();
-        umma::fence_after_sync();
-        if (tid == 0) {
-            umma::mma(tF, umma::swt(QW, 128), umma::swt(KS, 192), 128, 192, 128, false);
-            umma::commit(mbar);
+            umma::fence_after_sync();
+            if (tid == 0) {
+                umma::mma(tF, umma::swt(QW, 128), umma::swt(KS, 192), 128, 192, 128, false);
+                umma::commit(mbar);
+            }
         }
         // this warp's norm rows r = warp + 8 q: their z values, into registers (used
         // last; rows past the chunk repeat its last row and are not stored)
@@ -783,7 +812,6 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
         if (!ok) break;
         const bool next = tn < ntiles && cn.len > 0;
         if (next && tid == 0) issue_a(cn, tn);   // Q, W, K, S0 consumed
-        const float g_next = next ? gam_of(cn, tn) : 0.f;
         if (q4 < 2) {
             // P = D1 (.) Gam (.) M -> K-major rows i; row i = row, columns j = 32 half .. + 31
             float v[32];
@@ -864,6 +892,21 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
         umma::fence_smem_to_async();
         umma::fence_before_sync();
         __syncthreads();
+        umma::fence_after_sync();
+        // the next tile's first product, now that tensor memory is read, when it
+        // needs no preparation (a whole chunk with tf32 operands); its gate values
+        // go to shared memory (the norm below does not read them)
+        const bool early = next && cn.len == 64 && sv.qkv_tf32;
+        if (early) {
+            if (tid < 64) {
+                gam[tid] = g_next;
+                eg[tid] = expf(g_next);
+            }
+            if (tid == 0 && umma::mbar_wait(mA, (it + 1) & 1)) {   // on a timeout the wait at the top fails
+                umma::mma(tF, umma::swt(QW, 128), umma::swt(KS, 192), 128, 192, 128, false);
+                umma::commit(mbar);
+            }
+        }
         if (L == 64 && tid == 0) {   // o (fp32, for the backward) by one tensor store
             umma::tma_store_rows(&maps.o, h, ci.start, Or);
             umma::bulk_commit();
@@ -900,6 +943,7 @@ out_fwd_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT, co
             umma::bulk_wait_read();    // the o store has read the staging tile
             issue_u(cn, tn);
         }
+        issued = early;
         g_cur = g_next;
         ci = cn;
         cn = c2;

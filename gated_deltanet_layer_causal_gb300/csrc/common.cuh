@@ -175,72 +175,104 @@ __device__ __forceinline__ NormRowGrad norm_row_bwd(float4 o4, float4 z4, float4
 }
 
 // T = (I + A)^-1 for strictly lower A [64][lda] (unit lower-triangular
-// inverse), 256 threads.  Blocked: the four 16 x 16 diagonal blocks by forward
-// substitution (T_ij = -sum_{m=j}^{i-1} A_im T_mj, one thread per column), then
-// two merge levels of the block formula
+// inverse), 256 threads; lda and ldt multiples of 4, As and Ts 16-byte aligned.
+// Blocked: the four 16 x 16 diagonal blocks by forward substitution
+// (T_ij = -sum_{m=j}^{i-1} A_im T_mj, one thread per column), then two merge
+// levels of the block formula
 //   [[L11, 0], [L21, L22]]^-1 = [[T11, 0], [-T22 L21 T11, T22]]
-// (16 -> 32, then 32 -> 64) as small products on the CUDA cores.
-// X is 32 x 32 scratch.
+// (16 -> 32, then 32 -> 64) as small products on the CUDA cores.  Every sum
+// runs over m in ascending order.  The substitution is right-looking (each new
+// T_mj is added into the partial sums of the rows below at once), so its
+// dependent chain is one multiply-add per row; the products run m-outermost with
+// each thread's rows of the left factor read four at a time (broadcast float4)
+// and each value of the right factor read once for all its rows, the zeros of
+// the triangular factors included in the sums.  X is 32 x 32 scratch.
 __device__ __forceinline__ void tril_inverse64(const float* As, int lda, float* Ts, int ldt,
                                                float* X) {
     const int tid = threadIdx.x;
     for (int e = tid; e < kChunk * kChunk; e += 256) Ts[(e >> 6) * ldt + (e & 63)] = 0.f;
     __syncthreads();
     if (tid < kChunk) {   // diagonal blocks: thread = column c, solved in registers
-        // column c of a block's inverse solves (I + A_bb) x = e_c by forward
-        // substitution; columns are independent and A_bb is read by broadcast
         const int c = tid, b0 = c & ~15, cl = c & 15;
-        float x[16];
+        float x[16], acc[16];
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-            float acc = 0.f;
+        for (int i = 0; i < 16; i++) acc[i] = 0.f;
 #pragma unroll
-            for (int m = 0; m < i; m++) acc += As[(b0 + i) * lda + b0 + m] * x[m];
-            x[i] = i == cl ? 1.f : (i > cl ? -acc : 0.f);
+        for (int m = 0; m < 16; m++) {
+            x[m] = m == cl ? 1.f : (m > cl ? -acc[m] : 0.f);
+#pragma unroll
+            for (int i = m + 1; i < 16; i++) acc[i] += As[(b0 + i) * lda + b0 + m] * x[m];
         }
 #pragma unroll
         for (int i = 0; i < 16; i++) Ts[(b0 + i) * ldt + c] = x[i];
     }
     __syncthreads();
-    // 16 -> 32: for the pairs (0,1) and (2,3) of 16-blocks, X = L21 T11, T21 = -T22 X
+    // 16 -> 32: for the pairs (0,1) and (2,3) of 16-blocks, X = L21 T11, T21 = -T22 X;
+    // thread: rows i and i + 8 of pair p, column jj
     {
-        const int p = tid >> 7, e = tid & 127;          // pair, element group
-        const int r0 = 32 * p, r1 = r0 + 16;
+        const int p = tid >> 7, e = tid & 127;
+        const int r0 = 32 * p, r1 = r0 + 16, i = e >> 4, jj = e & 15;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int q = 0; q < 2; q++) {
-            const int i = (e >> 4) + 8 * q, jj = e & 15;
-            float acc = 0.f;
-            for (int m = 0; m < 16; m++) acc += As[(r1 + i) * lda + r0 + m] * Ts[(r0 + m) * ldt + r0 + jj];
-            X[p * 256 + i * 16 + jj] = acc;
+        for (int m = 0; m < 16; m += 4) {
+            const float4 l0 = *reinterpret_cast<const float4*>(As + (r1 + i) * lda + r0 + m);
+            const float4 l1 = *reinterpret_cast<const float4*>(As + (r1 + i + 8) * lda + r0 + m);
+            const float t0 = Ts[(r0 + m) * ldt + r0 + jj], t1 = Ts[(r0 + m + 1) * ldt + r0 + jj];
+            const float t2 = Ts[(r0 + m + 2) * ldt + r0 + jj], t3 = Ts[(r0 + m + 3) * ldt + r0 + jj];
+            a0 += l0.x * t0; a0 += l0.y * t1; a0 += l0.z * t2; a0 += l0.w * t3;
+            a1 += l1.x * t0; a1 += l1.y * t1; a1 += l1.z * t2; a1 += l1.w * t3;
         }
+        X[p * 256 + i * 16 + jj] = a0;
+        X[p * 256 + (i + 8) * 16 + jj] = a1;
         __syncthreads();
+        a0 = 0.f;
+        a1 = 0.f;
 #pragma unroll
-        for (int q = 0; q < 2; q++) {
-            const int i = (e >> 4) + 8 * q, jj = e & 15;
-            float acc = 0.f;
-            for (int m = 0; m <= i; m++) acc += Ts[(r1 + i) * ldt + r1 + m] * X[p * 256 + m * 16 + jj];
-            Ts[(r1 + i) * ldt + r0 + jj] = -acc;
+        for (int m = 0; m < 16; m += 4) {
+            const float4 l0 = *reinterpret_cast<const float4*>(Ts + (r1 + i) * ldt + r1 + m);
+            const float4 l1 = *reinterpret_cast<const float4*>(Ts + (r1 + i + 8) * ldt + r1 + m);
+            const float x0 = X[p * 256 + m * 16 + jj], x1 = X[p * 256 + (m + 1) * 16 + jj];
+            const float x2 = X[p * 256 + (m + 2) * 16 + jj], x3 = X[p * 256 + (m + 3) * 16 + jj];
+            a0 += l0.x * x0; a0 += l0.y * x1; a0 += l0.z * x2; a0 += l0.w * x3;
+            a1 += l1.x * x0; a1 += l1.y * x1; a1 += l1.z * x2; a1 += l1.w * x3;
         }
+        Ts[(r1 + i) * ldt + r0 + jj] = -a0;
+        Ts[(r1 + i + 8) * ldt + r0 + jj] = -a1;
     }
     __syncthreads();
-    // 32 -> 64: X = L21 T11 (32 x 32), T21 = -T22 X
+    // 32 -> 64: X = L21 T11 (32 x 32), T21 = -T22 X; thread: rows i0 + 8 q, column jj
     {
         const int jj = tid & 31, i0 = tid >> 5;
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const int i = i0 + 8 * q;
-            float acc = 0.f;
-            for (int m = 0; m < 32; m++) acc += As[(32 + i) * lda + m] * Ts[m * ldt + jj];
-            X[i * 32 + jj] = acc;
+        for (int m = 0; m < 32; m += 4) {
+            float t[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) t[u] = Ts[(m + u) * ldt + jj];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const float4 l = *reinterpret_cast<const float4*>(As + (32 + i0 + 8 * q) * lda + m);
+                a[q] += l.x * t[0]; a[q] += l.y * t[1]; a[q] += l.z * t[2]; a[q] += l.w * t[3];
+            }
         }
+#pragma unroll
+        for (int q = 0; q < 4; q++) X[(i0 + 8 * q) * 32 + jj] = a[q];
         __syncthreads();
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const int i = i0 + 8 * q;
-            float acc = 0.f;
-            for (int m = 0; m <= i; m++) acc += Ts[(32 + i) * ldt + 32 + m] * X[m * 32 + jj];
-            Ts[(32 + i) * ldt + jj] = -acc;
+        for (int q = 0; q < 4; q++) a[q] = 0.f;
+#pragma unroll
+        for (int m = 0; m < 32; m += 4) {
+            float x[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) x[u] = X[(m + u) * 32 + jj];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const float4 l = *reinterpret_cast<const float4*>(Ts + (32 + i0 + 8 * q) * ldt + 32 + m);
+                a[q] += l.x * x[0]; a[q] += l.y * x[1]; a[q] += l.z * x[2]; a[q] += l.w * x[3];
+            }
         }
+#pragma unroll
+        for (int q = 0; q < 4; q++) Ts[(32 + i0 + 8 * q) * ldt + jj] = -a[q];
     }
     __syncthreads();
 }
