@@ -82,7 +82,8 @@ chunk_norm_bwd_kernel(const float* __restrict__ o, const IO* __restrict__ z,
 //   D1 = K Q^T (64 x 64)  ->  P^T[j][i] = D1[j][i] e^{gam_i-gam_j} [i >= j]
 //   D2 = P^T dO           ->  dU_local (64 x 128)
 // Shared memory: Q, K swizzled and dO MN-major, 32 KB each (TMA; dO is the B
-// operand of P^T dO, contracted over tokens, so it is read as loaded); P^T
+// operand of P^T dO, contracted over tokens, so it is read as loaded, and has
+// its own barrier: K Q^T and P^T do not wait for it); P^T
 // (16 KB) takes the K space once K Q^T is done.  About 97 KB: two CTAs per SM.
 // Tensor memory: 192 fp32 columns (256 allocated).
 constexpr int kB1Floats = 64 * 128 * 3;
@@ -99,8 +100,9 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
     float* PT = Ks;                    // [64 (j)][64 (i)] K-major, after K Q^T
     float* gam = dOs + 64 * 128;
     uint64_t* mbar = reinterpret_cast<uint64_t*>(gam + 64 + 16);
-    uint64_t* mbl = mbar + 1;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbl + 1);
+    uint64_t* mbl = mbar + 1;          // Q, K
+    uint64_t* mbo = mbl + 1;           // dO (first needed by the second product)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbo + 1);
     // the P / dP kernel, launched after this one, claims its tiles from this counter
     if (blockIdx.x == 0 && threadIdx.x == 0) *w.dp_next = 0;
     const ChunkInfo ci = sv.chunks[blockIdx.x / hv];
@@ -110,10 +112,12 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
     if (tid == 0) {
         umma::mbar_init(mbar, 1);
         umma::mbar_init(mbl, 1);
-        umma::mbar_expect_tx(mbl, 3 * 64 * 128 * 4);
+        umma::mbar_init(mbo, 1);
+        umma::mbar_expect_tx(mbl, 2 * 64 * 128 * 4);
         umma::tma_rows(Qs, 64, &maps.q, kh, ci.start, mbl);
         umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
-        umma::tma_rows(dOs, 64, &maps.dO_mn, h, ci.start, mbl);
+        umma::mbar_expect_tx(mbo, 64 * 128 * 4);
+        umma::tma_rows(dOs, 64, &maps.dO_mn, h, ci.start, mbo);
     }
     load_gam(gam, sv, ci, h);
     if (warp == 0) umma::tmem_alloc(tslot, 256);
@@ -122,7 +126,6 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
     if (L < 64) {   // tail rows belong to the next sequence
         umma::zero_tail_rows(Qs, 64, 0, L);
         umma::zero_tail_rows(Ks, 64, 0, L);
-        umma::zero_tail_rows(dOs, 64, 0, L);
         __syncthreads();
     }
     if (!sv.qkv_tf32) umma::tf32r_inplace(Qs, 2 * 64 * 128);
@@ -170,7 +173,12 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
-    __syncthreads();
+    ok = __syncthreads_and(ok && umma::mbar_wait(mbo, 0));
+    if (L < 64) {
+        umma::zero_tail_rows(dOs, 64, 0, L);
+        umma::fence_smem_to_async();
+        __syncthreads();
+    }
     umma::fence_after_sync();
     if (ok && tid == 0) {
         umma::mma(tD2, umma::kmaj(PT, 64), umma::mnt(dOs), 64, 128, 64, false);
@@ -797,9 +805,11 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
 
 // ------------------------------------------------------------------ B3b: P / dP terms
 // Persistent: up to one CTA per SM (the last CTAs of the combined launch
-// below), each claiming (chunk, head) tiles from a counter (chunk = t / Hv,
-// head = t % Hv), so CTAs that start late -- on the SMs the reverse state pass
-// holds -- simply take fewer tiles.  Per tile, tcgen05:
+// below), each claiming (chunk, head) tiles from a counter (chunk = NT - 1 -
+// t / Hv, head = t % Hv: last chunk first, like the reverse state pass running
+// beside them, so the q / k / dO tiles both read are in L2 for the second), so
+// CTAs that start late -- on the SMs the reverse state pass holds -- simply take
+// fewer tiles.  Per tile, tcgen05:
 //   D_qk = Q K^T, D_dou = dO U^T                         (64 x 64 each)
 //   dPm = D_dou (.) Gam (.) [i>=j];  R = dPm (.) D_qk
 //     dgam_i += sum_j R_ij, dgam_j -= sum_i R_ij
@@ -861,7 +871,7 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         claim[0] = t0;
         claim[1] = atomicAdd(w.dp_next, 1);
         if (t0 < ntiles) {
-            const ChunkInfo c0 = sv.chunks[t0 / hv];
+            const ChunkInfo c0 = sv.chunks[NT - 1 - t0 / hv];
             if (c0.len > 0) {
                 issue_a(c0, t0);
                 issue_b(c0, t0);
@@ -881,8 +891,8 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
     // operands are requested and its gate values an iteration before they are
     // used: no thread waits on a global load at the top of a tile.
     int t = claim[0], tn = claim[1];
-    ChunkInfo ci = t < ntiles ? sv.chunks[t / hv] : ChunkInfo{0, 0, 0, 0};
-    ChunkInfo cn = tn < ntiles ? sv.chunks[tn / hv] : ci;
+    ChunkInfo ci = t < ntiles ? sv.chunks[NT - 1 - t / hv] : ChunkInfo{0, 0, 0, 0};
+    ChunkInfo cn = tn < ntiles ? sv.chunks[NT - 1 - tn / hv] : ci;
     float g_cur = 0.f;
     if (tid < 64 && t < ntiles) g_cur = sv.gam[(int64_t)(t % hv) * sv.T + ci.start + min(tid, ci.len - 1)];
     bool ok = true;
@@ -929,7 +939,7 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         if (!ok) break;
         const int t2 = claim[(it + 2) % 3];
         ChunkInfo c2 = cn;   // used an iteration later
-        if (t2 < ntiles) c2 = sv.chunks[t2 / hv];
+        if (t2 < ntiles) c2 = sv.chunks[NT - 1 - t2 / hv];
         const bool next = tn < ntiles && cn.len > 0;
         if (tid == 0 && next) issue_a(cn, tn);   // the swizzled operands are consumed
         {   // 32 columns per warp, all lanes; R row / column sums by shuffles

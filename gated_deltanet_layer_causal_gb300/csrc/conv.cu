@@ -20,7 +20,10 @@ namespace gdn {
 
 constexpr int kConvWarps = 8;
 constexpr int kConvRun = 64;   // tokens per warp
-constexpr int kConvRing = 3;   // backward: four-token steps each lane holds in its copy ring
+// backward: four-token steps each lane holds in its copy ring (two CTAs of
+// eight warps per SM fit either way)
+template <class T>
+constexpr int conv_ring() { return sizeof(T) == 2 ? 4 : 3; }
 constexpr int kConvFwdRing = 4;   // forward: the same, input rows only
 
 template <class T>
@@ -28,12 +31,12 @@ constexpr size_t conv_fwd_smem() {
     return (size_t)kConvFwdRing * 4 * kConvWarps * 32 * 4 * sizeof(T);
 }
 
-// Backward shared memory: per lane a ring of kConvRing steps, each four rows of
+// Backward shared memory: per lane a ring of conv_ring steps, each four rows of
 // the incoming gradient (float4) and four new input rows (4 x T); reused for
 // the dw reduction at the end.
 template <class T>
 constexpr size_t conv_bwd_smem() {
-    return (size_t)kConvRing * 4 * kConvWarps * 32 * (sizeof(float4) + 4 * sizeof(T));
+    return (size_t)conv_ring<T>() * 4 * kConvWarps * 32 * (sizeof(float4) + 4 * sizeof(T));
 }
 
 __device__ __forceinline__ int seq_of(const int32_t* cu, int N, int64_t t) {
@@ -328,6 +331,7 @@ conv_bwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const T* c
     extern __shared__ __align__(16) unsigned char conv_smem[];
     constexpr int kThr = kConvWarps * 32;
     float4* dq_ring = reinterpret_cast<float4*>(conv_smem);                   // [ring][4][kThr]
+    constexpr int kConvRing = conv_ring<T>();
     T* x_ring = reinterpret_cast<T*>(conv_smem + kConvRing * 4 * kThr * sizeof(float4));   // [ring][4][kThr][4]
     auto red = reinterpret_cast<float (*)[kD][kConvK]>(conv_smem);            // [warp][kD][kConvK]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
