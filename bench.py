@@ -238,18 +238,18 @@ class DecodeStep:
 # proportional to the chunks it processes).  Valid for the kernels as captured;
 # a kernel changed since then is left out (its traffic reports null).
 TRAFFIC_64K = {
-    "conv_fwd": 3619241984,
-    "gates": 12664832,
-    "chunk_prep": 6523840512,
-    "chunk_state_fwd": 6643978240,
-    "chunk_out_fwd": 12141393920,
-    "chunk_norm_bwd": 5317441536,
-    "chunk_bwd_local": 4016689152,
-    "chunk_bwd_state_dp": 18212042752,
-    "chunk_bwd_sfacing": 17401223168,
-    "chunk_bwd_wy": 10145630208,
-    "gva_sum": 9024364544,
-    "conv_bwd": 5372211200,
+    "conv_fwd": 3628328960,
+    "gates": 12656640,
+    "chunk_prep": 6499381248,
+    "chunk_state_fwd": 6637580288,
+    "chunk_out_fwd": 12032487424,
+    "chunk_norm_bwd": 5312882688,
+    "chunk_bwd_local": 4010577920,
+    "chunk_bwd_state_dp": 17946427392,
+    "chunk_bwd_sfacing": 16923162624,
+    "chunk_bwd_wy": 10025461760,
+    "gva_sum": 9023236096,
+    "conv_bwd": 5371858944,
 }
 
 # tcgen05 / mma.sync products each chunk kernel issues per (chunk, v-head) tile,
