@@ -819,9 +819,9 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
 // 32 KB each (the B operands of the products over tokens), dPm in both
 // orientations 16 KB each.  The next tile's swizzled operands are requested as
 // soon as the first products are done, its MN-major ones as soon as the second
-// are; D_dq and D_dk go from tensor memory straight to global memory.  Tensor
-// memory: 256 fp32 columns (D_dq / D_dk reuse the columns of the first
-// products), allocated once.
+// are; D_dq and D_dk go from tensor memory straight to global memory while the
+// next tile's first products run.  Tensor memory: D_dq / D_dk in columns 0-255,
+// the first products in 256-383 (512 allocated), once.
 constexpr int kDpFloats = 6 * 64 * 128 + 2 * 64 * 64;
 constexpr size_t kDpSmem = sizeof(float) * (kDpFloats + 4 * 64 + 2 * 64 + 64) + 4 * 8 + 8 + 1024;
 
@@ -878,14 +878,36 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
             }
         }
     }
-    if (warp == 0) umma::tmem_alloc(tslot, 256);
+    if (warp == 0) umma::tmem_alloc(tslot, 512);
     umma::fence_before_sync();
     umma::named_sync(1, 256);
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t tQK = tmem, tDOU = tmem + 64, tDQ = tmem, tDK = tmem + 128;
     const int win = warp & 3, half = warp >> 2;
     const int rl = umma::frag_row_lo(), cf = umma::frag_col();
+    // D_dq / D_dk in columns 0-255, the first products in 256-383: a tile's D_dq and
+    // D_dk go out while the next tile's first products run
+    const uint32_t tDQ = tmem, tDK = tmem + 128, tQK = tmem + 256, tDOU = tmem + 320;
+    // D_dq, D_dk rows rl, rl + 8 (those inside the chunk) of the tile at token
+    // `start`, v-head hp, straight from tensor memory to the partials
+    auto put_tile = [&](int64_t start, int hp, int Lp) {
+        const int64_t o_lo = ((start + rl) * hv + hp) * kD;
+        const int64_t o_hi = o_lo + (int64_t)8 * hv * kD;
+        auto put = [&](float* dst, uint32_t tcol) {
+            float v[32];
+            umma::tmem_ld64_m64(umma::tmem_at(tcol, half * 64), v);
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                const int c = half * 64 + 8 * k + cf;
+                if (rl < Lp)
+                    *reinterpret_cast<float2*>(dst + o_lo + c) = make_float2(v[4 * k], v[4 * k + 1]);
+                if (rl + 8 < Lp)
+                    *reinterpret_cast<float2*>(dst + o_hi + c) = make_float2(v[4 * k + 2], v[4 * k + 3]);
+            }
+        };
+        put(w.dQv2, tDQ);
+        put(w.dKv2, tDK);
+    };
     // Tiles are claimed two ahead (the claim for iteration it + 2 is made during
     // iteration it), so a tile's chunk entry is loaded an iteration before its
     // operands are requested and its gate values an iteration before they are
@@ -896,6 +918,8 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
     float g_cur = 0.f;
     if (tid < 64 && t < ntiles) g_cur = sv.gam[(int64_t)(t % hv) * sv.T + ci.start + min(tid, ci.len - 1)];
     bool ok = true;
+    int64_t p_start = -1;   // the previous tile, whose D_dq / D_dk are still to go out
+    int p_h = 0, p_L = 0;
     for (int it = 0; t < ntiles; it++) {
         const int h = t % hv, L = ci.len;
         if (L == 0) break;   // the device check of cu_seqlens failed: every chunk is empty
@@ -919,6 +943,7 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
             umma::commit(mM);
             claim[(it + 2) % 3] = atomicAdd(w.dp_next, 1);   // the tile after the next
         }
+        if (p_start >= 0) put_tile(p_start, p_h, p_L);
         // while the products run: the decay factors e^{gam_r - gam_j} [j <= r] of this
         // thread's fragment
         float dec[16];
@@ -934,6 +959,7 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
                     dec[4 * k + 2 * hr + e] = j <= r ? expf(gr - gam[j]) : 0.f;
                 }
         }
+        umma::fence_before_sync();   // (the previous tile's tensor-memory reads)
         ok = umma::named_sync_and(1, 256, umma::mbar_wait(mM, 0));   // the claim is visible too
         umma::fence_after_sync();
         if (!ok) break;
@@ -1008,25 +1034,9 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         umma::fence_after_sync();
         if (!ok) break;
         if (tid == 0 && next) issue_b(cn, tn);   // the MN-major operands are consumed
-        {   // D_dq, D_dk rows rl, rl + 8 (those inside the chunk) straight to the partials
-            const int64_t o_lo = ((int64_t)(ci.start + rl) * hv + h) * kD;
-            const int64_t o_hi = o_lo + (int64_t)8 * hv * kD;
-            auto put = [&](float* dst, uint32_t tcol) {
-                float v[32];
-                umma::tmem_ld64_m64(umma::tmem_at(tcol, half * 64), v);
-#pragma unroll
-                for (int k = 0; k < 8; k++) {
-                    const int c = half * 64 + 8 * k + cf;
-                    if (rl < L)
-                        *reinterpret_cast<float2*>(dst + o_lo + c) = make_float2(v[4 * k], v[4 * k + 1]);
-                    if (rl + 8 < L)
-                        *reinterpret_cast<float2*>(dst + o_hi + c) =
-                            make_float2(v[4 * k + 2], v[4 * k + 3]);
-                }
-            };
-            put(w.dQv2, tDQ);
-            put(w.dKv2, tDK);
-        }
+        p_start = ci.start;   // D_dq, D_dk go out at the next tile's first products
+        p_h = h;
+        p_L = L;
         umma::fence_before_sync();
         umma::named_sync(1, 256);   // tensor memory read before the next tile's products reuse it
         t = tn;
@@ -1035,9 +1045,10 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         cn = c2;
         g_cur = g_next;
     }
+    if (ok && p_start >= 0) put_tile(p_start, p_h, p_L);   // the last tile
     umma::fence_before_sync();
     umma::named_sync(1, 256);
-    if (warp == 0) umma::tmem_free(tmem, 256);
+    if (warp == 0) umma::tmem_free(tmem, 512);
     if (!ok && tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
 }
 
