@@ -245,10 +245,8 @@ TRAFFIC_64K = {
     "chunk_out_fwd": 12032487424,
     "chunk_norm_bwd": 5312882688,
     "chunk_bwd_local": 4010577920,
-    "chunk_bwd_state_dp": 17946427392,
     "chunk_bwd_sfacing": 16923162624,
     "chunk_bwd_wy": 10025461760,
-    "gva_sum": 9023236096,
     "conv_bwd": 5371858944,
 }
 
@@ -262,20 +260,29 @@ MMAS = {
     "chunk_out_fwd": [(128, 192, 128), (128, 128, 64)],
     "chunk_bwd_local": [(64, 64, 128), (64, 128, 64)],                  # K Q^T, P^T dO
     # reverse state pass (2 row slices: K dS^T; B'^T = Q^T e^gam dO - W^T dU_local;
-    # W^T Ub) and P / dP tiles, one launch
+    # W^T Ub) and the P / dP groups' per-v-head dO U^T, one launch
     "chunk_bwd_state_dp": [(64, 64, 128), (128, 64, 64), (128, 64, 64), (128, 64, 64)] * 2 +
-                          [(64, 64, 128), (64, 64, 128), (64, 128, 64), (64, 128, 64)],
+                          [(64, 64, 128)],
     "chunk_bwd_sfacing": [(128, 128, 128), (64, 128, 128)],            # [dO; dU] S0, U dS
     "chunk_bwd_wy": [(64, 64, 128)] * 3 + [(64, 256, 64), (64, 64, 64), (64, 64, 64),
                                            (64, 128, 64)],   # ..., (dKK + dKK^T) K
 }
 
 
-def kernel_flops(name: str, NT: int, hv: int):
-    """Tensor-core FLOPs of one launch: the kernel's products per tile x tiles."""
+# products issued once per (chunk, k-head) group: the P / dP groups' Q K^T and
+# D_dq = dPs K, D_dk = dPs^T Q (q, k and so these are shared by the group's v-heads)
+MMAS_KH = {
+    "chunk_bwd_state_dp": [(64, 64, 128), (64, 128, 64), (64, 128, 64)],
+}
+
+
+def kernel_flops(name: str, NT: int, hv: int, hk: int):
+    """Tensor-core FLOPs of one launch: the kernel's products per (chunk, v-head)
+    tile x tiles, plus those per (chunk, k-head) group x groups."""
     if name not in MMAS:
         return None
-    return sum(2 * m * n * k for m, n, k in MMAS[name]) * NT * hv
+    return (sum(2 * m * n * k for m, n, k in MMAS[name]) * NT * hv +
+            sum(2 * m * n * k for m, n, k in MMAS_KH.get(name, [])) * NT * hk)
 
 
 def kernel_cost(name: str, w: synth.Workload, NT: int):
@@ -300,10 +307,10 @@ def kernel_cost(name: str, w: synth.Workload, NT: int):
         "chunk_norm_bwd": tv + 2 * act + tv + act,
         "chunk_bwd_local": 2 * tk + tv + g + tv,
         "chunk_bwd_state_dp": (2 * tk + 3 * tv + g + tv + S) +     # state pass
-                              (2 * tk + 2 * tv + g + 2 * tv + 2 * g),  # P / dP tiles
+                              (2 * tk + 2 * tv + g + 2 * tk + 2 * g),  # P / dP groups
         "chunk_bwd_sfacing": 2 * S + 3 * tv + 2 * tk + g + 3 * tv + g,
         "chunk_bwd_wy": tk + tv + 2 * tv + 2 * Tt + 3 * g + gates + 2 * tv + gates + g,
-        "gva_sum": 5 * tv + 2 * tk,
+        "gva_sum": 3 * tv + 4 * tk,
     }
     return "hbm", table.get(name), "B"
 
@@ -404,7 +411,7 @@ def run_ours(args, rank, world, dev):
     name, (nl, tot_ms) = max(prof.items(), key=lambda kv: kv[1][1])
     avg_ms = tot_ms / nl
     _, ibytes, _ = kernel_cost(name, w, NT)
-    flops = kernel_flops(name, NT, w.h_v)
+    flops = kernel_flops(name, NT, w.h_v, w.h_k)
     traffic = (TRAFFIC_64K.get(name) if args.workload == "qwen38_flash_64k" and not args.tokens
                else None)
     if flops is not None:   # a chunk kernel: tensor pipe

@@ -114,8 +114,8 @@ BwdScratch carve_bwd(void* ws, const gdn_dims* d, int NT, int32_t** status, size
     s.dU = c.take<float>(T * H * kD);
     s.dQv = c.take<float>(T * H * kD);
     s.dKv = c.take<float>(T * H * kD);
-    s.dQv2 = c.take<float>(T * H * kD);
-    s.dKv2 = c.take<float>(T * H * kD);
+    s.dQv2 = c.take<float>(T * (size_t)d->h_k * kD);   // per k-head (the P / dP groups)
+    s.dKv2 = c.take<float>(T * (size_t)d->h_k * kD);
     s.dKv3 = c.take<float>(T * H * kD);
     s.dUl = s.dKv3;   // dU_local until the WY kernel writes its dK part there
     s.dW = c.take<float>(T * H * kD);

@@ -805,25 +805,28 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
 
 // ------------------------------------------------------------------ B3b: P / dP terms
 // Persistent: up to one CTA per SM (the last CTAs of the combined launch
-// below), each claiming (chunk, head) tiles from a counter (chunk = NT - 1 -
-// t / Hv, head = t % Hv: last chunk first, like the reverse state pass running
-// beside them, so the q / k / dO tiles both read are in L2 for the second), so
-// CTAs that start late -- on the SMs the reverse state pass holds -- simply take
-// fewer tiles.  Per tile, tcgen05:
-//   D_qk = Q K^T, D_dou = dO U^T                         (64 x 64 each)
-//   dPm = D_dou (.) Gam (.) [i>=j];  R = dPm (.) D_qk
-//     dgam_i += sum_j R_ij, dgam_j -= sum_i R_ij
-//   D_dq = dPm K,  D_dk = dPm^T Q                        (64 x 128 each)
-// added to the per-v-head dQ / dK partials.  Shared memory: Q, K, dO, U
-// swizzled 32 KB each (the first products' operands), Q and K again MN-major
-// 32 KB each (the B operands of the products over tokens), dPm in both
-// orientations 16 KB each.  The next tile's swizzled operands are requested as
-// soon as the first products are done, its MN-major ones as soon as the second
-// are; D_dq and D_dk go from tensor memory straight to global memory while the
-// next tile's first products run.  Tensor memory: D_dq / D_dk in columns 0-255,
-// the first products in 256-383 (512 allocated), once.
+// below), each claiming (chunk, k-head) groups from a counter (chunk = NT - 1 -
+// g / H_k, k-head = g % H_k: last chunk first, like the reverse state pass
+// running beside them), so CTAs that start late -- on the SMs the reverse state
+// pass holds -- simply take fewer groups.  A group is the G = H_v / H_k v-heads
+// that share the k-head's q and k, handled one after another.  Per group, tcgen05:
+//   D_qk = Q K^T                                         (once: q, k are shared)
+//   per v-head h:  D_dou = dO_h U_h^T;  dPm_h = D_dou (.) Gam_h (.) [i>=j];
+//                  R = dPm_h (.) D_qk:  dgam_h,i += sum_j R_ij, dgam_h,j -= sum_i R_ij
+//   dPs = sum_h dPm_h (fp32, in registers; rounded once)
+//   D_dq = dPs K,  D_dk = dPs^T Q                        (64 x 128 each, once)
+// -- the group's whole dQ / dK share from these terms, written once per k-head
+// (sum_h dPm_h K = (sum_h dPm_h) K because K is the same for every h).  Shared
+// memory: Q, K swizzled and MN-major (the latter the B operands of the products
+// over tokens), 32 KB each; one v-head's dO, U swizzled, 32 KB each; dPs in both
+// orientations 16 KB each.  The next group's swizzled Q, K are requested once
+// D_qk is done, its MN-major ones once D_dq / D_dk are; the next v-head's dO, U
+// (of this group or the next) once the current D_dou is done.  D_dq and D_dk go
+// from tensor memory straight to global memory while the next group's first
+// products run.  Tensor memory: D_dq / D_dk in columns 0-255, D_qk and D_dou in
+// 256-383 (512 allocated), once.
 constexpr int kDpFloats = 6 * 64 * 128 + 2 * 64 * 64;
-constexpr size_t kDpSmem = sizeof(float) * (kDpFloats + 4 * 64 + 2 * 64 + 64) + 4 * 8 + 8 + 1024;
+constexpr size_t kDpSmem = sizeof(float) * (kDpFloats + 4 * 64 + 2 * 64 + 64) + 6 * 8 + 16 + 1024;
 
 __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv, int NT,
                                            const FwdSaved& sv, const BwdScratch& w) {
@@ -842,39 +845,46 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
     float* colp = dPC + 64 * 64;       // [4 row windows][64] column sums of R
     float* rpart = colp + 4 * 64;      // [2][64] row sums of R
     float* gam = rpart + 2 * 64;
-    uint64_t* mA = reinterpret_cast<uint64_t*>(gam + 64);   // swizzled operands
-    uint64_t* mB = mA + 1;             // MN-major operands
-    uint64_t* mM = mB + 1;             // MMA
-    int32_t* claim = reinterpret_cast<int32_t*>(mM + 1);   // [3] claimed tiles, slot it % 3
+    uint64_t* mQ = reinterpret_cast<uint64_t*>(gam + 64);   // swizzled Q, K
+    uint64_t* mB = mQ + 1;             // MN-major Q, K
+    uint64_t* mO = mB + 1;             // dO, U of one v-head
+    uint64_t* mM = mO + 1;             // MMA (G + 2 commits per group)
+    int32_t* claim = reinterpret_cast<int32_t*>(mM + 1);   // [3] claimed groups, slot gi % 3
     uint32_t* tslot = reinterpret_cast<uint32_t*>(claim + 3);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int ntiles = NT * hv;
-    auto issue_a = [&](const ChunkInfo& c, int tile) {   // one thread
-        const int h = tile % hv, kh = h / (hv / hk);
-        umma::mbar_expect_tx(mA, 4 * 64 * 128 * 4);
-        umma::tma_rows(Qs, 64, &maps.q, kh, c.start, mA);
-        umma::tma_rows(Ks, 64, &maps.k, kh, c.start, mA);
-        umma::tma_rows(dOs, 64, &maps.dO, h, c.start, mA);
-        umma::tma_rows(Us, 64, &maps.U, h, c.start, mA);
+    const int G = hv / hk, ngroups = NT * hk;
+    auto entry = [&](int g) { return sv.chunks[NT - 1 - g / hk]; };
+    auto issue_q = [&](const ChunkInfo& c, int g) {   // one thread
+        const int kh = g % hk;
+        umma::mbar_expect_tx(mQ, 2 * 64 * 128 * 4);
+        umma::tma_rows(Qs, 64, &maps.q, kh, c.start, mQ);
+        umma::tma_rows(Ks, 64, &maps.k, kh, c.start, mQ);
     };
-    auto issue_b = [&](const ChunkInfo& c, int tile) {   // one thread
-        const int kh = (tile % hv) / (hv / hk);
+    auto issue_b = [&](const ChunkInfo& c, int g) {   // one thread
+        const int kh = g % hk;
         umma::mbar_expect_tx(mB, 2 * 64 * 128 * 4);
         umma::tma_rows(Qm, 64, &maps.q_mn, kh, c.start, mB);
         umma::tma_rows(Km, 64, &maps.k_mn, kh, c.start, mB);
     };
+    auto issue_o = [&](const ChunkInfo& c, int h) {   // one thread
+        umma::mbar_expect_tx(mO, 2 * 64 * 128 * 4);
+        umma::tma_rows(dOs, 64, &maps.dO, h, c.start, mO);
+        umma::tma_rows(Us, 64, &maps.U, h, c.start, mO);
+    };
     if (tid == 0) {
-        umma::mbar_init(mA, 1);
+        umma::mbar_init(mQ, 1);
         umma::mbar_init(mB, 1);
+        umma::mbar_init(mO, 1);
         umma::mbar_init(mM, 1);
-        const int t0 = atomicAdd(w.dp_next, 1);
-        claim[0] = t0;
+        const int g0 = atomicAdd(w.dp_next, 1);
+        claim[0] = g0;
         claim[1] = atomicAdd(w.dp_next, 1);
-        if (t0 < ntiles) {
-            const ChunkInfo c0 = sv.chunks[NT - 1 - t0 / hv];
+        if (g0 < ngroups) {
+            const ChunkInfo c0 = entry(g0);
             if (c0.len > 0) {
-                issue_a(c0, t0);
-                issue_b(c0, t0);
+                issue_q(c0, g0);
+                issue_b(c0, g0);
+                issue_o(c0, (g0 % hk) * G);
             }
         }
     }
@@ -883,16 +893,14 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
     umma::named_sync(1, 256);
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
+    const uint32_t tDQ = tmem, tDK = tmem + 128, tQK = tmem + 256, tDOU = tmem + 320;
     const int win = warp & 3, half = warp >> 2;
     const int rl = umma::frag_row_lo(), cf = umma::frag_col();
-    // D_dq / D_dk in columns 0-255, the first products in 256-383: a tile's D_dq and
-    // D_dk go out while the next tile's first products run
-    const uint32_t tDQ = tmem, tDK = tmem + 128, tQK = tmem + 256, tDOU = tmem + 320;
-    // D_dq, D_dk rows rl, rl + 8 (those inside the chunk) of the tile at token
-    // `start`, v-head hp, straight from tensor memory to the partials
-    auto put_tile = [&](int64_t start, int hp, int Lp) {
-        const int64_t o_lo = ((start + rl) * hv + hp) * kD;
-        const int64_t o_hi = o_lo + (int64_t)8 * hv * kD;
+    // D_dq, D_dk rows rl, rl + 8 (those inside the chunk) of the group at token
+    // `start`, k-head khp, straight from tensor memory to the per-k-head partials
+    auto put_group = [&](int64_t start, int khp, int Lp) {
+        const int64_t o_lo = ((start + rl) * hk + khp) * kD;
+        const int64_t o_hi = o_lo + (int64_t)8 * hk * kD;
         auto put = [&](float* dst, uint32_t tcol) {
             float v[32];
             umma::tmem_ld64_m64(umma::tmem_at(tcol, half * 64), v);
@@ -908,29 +916,28 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         put(w.dQv2, tDQ);
         put(w.dKv2, tDK);
     };
-    // Tiles are claimed two ahead (the claim for iteration it + 2 is made during
-    // iteration it), so a tile's chunk entry is loaded an iteration before its
-    // operands are requested and its gate values an iteration before they are
-    // used: no thread waits on a global load at the top of a tile.
-    int t = claim[0], tn = claim[1];
-    ChunkInfo ci = t < ntiles ? sv.chunks[NT - 1 - t / hv] : ChunkInfo{0, 0, 0, 0};
-    ChunkInfo cn = tn < ntiles ? sv.chunks[NT - 1 - tn / hv] : ci;
+    // Groups are claimed two ahead (the claim for group iteration gi + 2 is made
+    // during iteration gi), so a group's chunk entry is loaded an iteration before
+    // its operands are requested; a v-head's gate values are loaded a v-head
+    // before they are used.
+    int g = claim[0], gn = claim[1];
+    ChunkInfo ci = g < ngroups ? entry(g) : ChunkInfo{0, 0, 0, 0};
+    ChunkInfo cn = gn < ngroups ? entry(gn) : ci;
     float g_cur = 0.f;
-    if (tid < 64 && t < ntiles) g_cur = sv.gam[(int64_t)(t % hv) * sv.T + ci.start + min(tid, ci.len - 1)];
+    if (tid < 64 && g < ngroups) g_cur = sv.gam[(int64_t)((g % hk) * G) * sv.T + ci.start + min(tid, ci.len - 1)];
     bool ok = true;
-    int64_t p_start = -1;   // the previous tile, whose D_dq / D_dk are still to go out
-    int p_h = 0, p_L = 0;
-    for (int it = 0; t < ntiles; it++) {
-        const int h = t % hv, L = ci.len;
+    int64_t p_start = -1;   // the previous group, whose D_dq / D_dk are still to go out
+    int p_kh = 0, p_L = 0;
+    uint32_t nm = 0;        // MMA commits waited so far (mM parity)
+    uint32_t no = 0;        // v-head loads waited so far (mO parity)
+    for (int gi = 0; g < ngroups; gi++) {
+        const int kh = g % hk, L = ci.len;
         if (L == 0) break;   // the device check of cu_seqlens failed: every chunk is empty
-        if (tid < 64) gam[tid] = g_cur;
-        ok = umma::named_sync_and(1, 256, umma::mbar_wait(mA, it & 1));   // Q, K, dO, U; gam visible
+        ok = umma::named_sync_and(1, 256, umma::mbar_wait(mQ, gi & 1));   // Q, K
         if (!ok) break;
         if (L < 64) {   // tail rows belong to the next sequence
             umma::zero_tail_rows<256>(Qs, 64, 0, L);
             umma::zero_tail_rows<256>(Ks, 64, 0, L);
-            umma::zero_tail_rows<256>(dOs, 64, 0, L);
-            umma::zero_tail_rows<256>(Us, 64, 0, L);
             umma::named_sync(1, 256);
         }
         if (!sv.qkv_tf32) umma::tf32r_inplace<256>(Qs, 2 * 64 * 128);   // Q, K
@@ -939,76 +946,132 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
         umma::fence_after_sync();
         if (tid == 0) {
             umma::mma(tQK, umma::swt(Qs, 64), umma::swt(Ks, 64), 64, 64, 128, false);
-            umma::mma(tDOU, umma::swt(dOs, 64), umma::swt(Us, 64), 64, 64, 128, false);
             umma::commit(mM);
-            claim[(it + 2) % 3] = atomicAdd(w.dp_next, 1);   // the tile after the next
+            claim[(gi + 2) % 3] = atomicAdd(w.dp_next, 1);   // the group after the next
         }
-        if (p_start >= 0) put_tile(p_start, p_h, p_L);
-        // while the products run: the decay factors e^{gam_r - gam_j} [j <= r] of this
-        // thread's fragment
-        float dec[16];
-#pragma unroll
-        for (int hr = 0; hr < 2; hr++) {
-            const int r = rl + 8 * hr;
-            const float gr = gam[r];
-#pragma unroll
-            for (int k = 0; k < 4; k++)
-#pragma unroll
-                for (int e = 0; e < 2; e++) {
-                    const int j = half * 32 + 8 * k + cf + e;
-                    dec[4 * k + 2 * hr + e] = j <= r ? expf(gr - gam[j]) : 0.f;
-                }
-        }
-        umma::fence_before_sync();   // (the previous tile's tensor-memory reads)
-        ok = umma::named_sync_and(1, 256, umma::mbar_wait(mM, 0));   // the claim is visible too
+        if (p_start >= 0) put_group(p_start, p_kh, p_L);   // while D_qk runs
+        umma::fence_before_sync();   // (those tensor-memory reads)
+        ok = umma::named_sync_and(1, 256, umma::mbar_wait(mM, nm & 1));   // the claim is visible too
+        nm++;
         umma::fence_after_sync();
         if (!ok) break;
-        const int t2 = claim[(it + 2) % 3];
+        const int g2 = claim[(gi + 2) % 3];
         ChunkInfo c2 = cn;   // used an iteration later
-        if (t2 < ntiles) c2 = sv.chunks[NT - 1 - t2 / hv];
-        const bool next = tn < ntiles && cn.len > 0;
-        if (tid == 0 && next) issue_a(cn, tn);   // the swizzled operands are consumed
-        {   // 32 columns per warp, all lanes; R row / column sums by shuffles
-            float qk[16], du[16];
-            umma::tmem_ld_m64<4>(umma::tmem_at(tQK, half * 32), qk);
-            umma::tmem_ld_m64<4>(umma::tmem_at(tDOU, half * 32), du);
-            float rs[2] = {0.f, 0.f}, cs[4][2];
+        if (g2 < ngroups) c2 = entry(g2);
+        const bool next = gn < ngroups && cn.len > 0;
+        if (tid == 0 && next) issue_q(cn, gn);   // the swizzled Q, K are consumed
+        float qk[16];
+        umma::tmem_ld_m64<4>(umma::tmem_at(tQK, half * 32), qk);
+        float ps[16];   // sum over the group's v-heads of dPm, this thread's fragment
+#pragma unroll
+        for (int q = 0; q < 16; q++) ps[q] = 0.f;
+        for (int j = 0; j < G && ok; j++) {
+            const int h = kh * G + j;
+            // the next v-head's gate values (this group's, else the next group's first)
+            float g_next = 0.f;
+            if (tid < 64) {
+                if (j + 1 < G)
+                    g_next = sv.gam[(int64_t)(h + 1) * sv.T + ci.start + min(tid, L - 1)];
+                else if (next)
+                    g_next = sv.gam[(int64_t)((gn % hk) * G) * sv.T + cn.start + min(tid, cn.len - 1)];
+            }
+            if (tid < 64) gam[tid] = g_cur;
+            ok = umma::named_sync_and(1, 256, umma::mbar_wait(mO, no & 1));   // dO, U; gam visible
+            no++;
+            if (!ok) break;
+            if (L < 64) {
+                umma::zero_tail_rows<256>(dOs, 64, 0, L);
+                umma::zero_tail_rows<256>(Us, 64, 0, L);
+                umma::fence_smem_to_async();
+                umma::named_sync(1, 256);
+            }
+            umma::fence_after_sync();
+            if (tid == 0) {
+                umma::mma(tDOU, umma::swt(dOs, 64), umma::swt(Us, 64), 64, 64, 128, false);
+                umma::commit(mM);
+            }
+            // while the product runs: the decay factors e^{gam_r - gam_j} [j <= r] of
+            // this thread's fragment
+            float dec[16];
+#pragma unroll
+            for (int hr = 0; hr < 2; hr++) {
+                const int r = rl + 8 * hr;
+                const float gr = gam[r];
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+#pragma unroll
+                    for (int e = 0; e < 2; e++) {
+                        const int jj = half * 32 + 8 * k + cf + e;
+                        dec[4 * k + 2 * hr + e] = jj <= r ? expf(gr - gam[jj]) : 0.f;
+                    }
+            }
+            ok = umma::named_sync_and(1, 256, umma::mbar_wait(mM, nm & 1));
+            nm++;
+            umma::fence_after_sync();
+            if (!ok) break;
+            if (tid == 0) {   // dO, U consumed: the next v-head's
+                if (j + 1 < G) issue_o(ci, h + 1);
+                else if (next) issue_o(cn, (gn % hk) * G);
+            }
+            {   // dPm_h, R row / column sums by shuffles; dPm_h into the group sum
+                float du[16];
+                umma::tmem_ld_m64<4>(umma::tmem_at(tDOU, half * 32), du);
+                float rs[2] = {0.f, 0.f}, cs[4][2];
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    cs[k][0] = cs[k][1] = 0.f;
+#pragma unroll
+                    for (int hr = 0; hr < 2; hr++)
+#pragma unroll
+                        for (int e = 0; e < 2; e++) {
+                            const int q = 4 * k + 2 * hr + e;
+                            const float x = du[q] * dec[q];
+                            const float R = x * qk[q];
+                            rs[hr] += R;
+                            cs[k][e] += R;
+                            ps[q] += x;
+                        }
+                }
+                rs[0] = umma::row_quad_sum(rs[0]);
+                rs[1] = umma::row_quad_sum(rs[1]);
+                if ((lane & 3) == 0) {
+                    rpart[half * 64 + rl] = rs[0];
+                    rpart[half * 64 + rl + 8] = rs[1];
+                }
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+#pragma unroll
+                    for (int e = 0; e < 2; e++) {
+                        const float c = umma::col_oct_sum(cs[k][e]);
+                        if (lane < 4) colp[win * 64 + half * 32 + 8 * k + 2 * lane + e] = c;
+                    }
+            }
+            umma::fence_before_sync();
+            umma::named_sync(1, 256);   // R sums written; D_dou read
+            if (tid < 64 && tid < L) {   // dgam from R: row sums minus column sums (fixed order)
+                const float cs = (colp[tid] + colp[64 + tid]) + (colp[128 + tid] + colp[192 + tid]);
+                w.dgam2[(int64_t)(ci.start + tid) * hv + h] = (rpart[tid] + rpart[64 + tid]) - cs;
+            }
+            umma::named_sync(1, 256);   // R sums read before the next v-head's
+            g_cur = g_next;
+        }
+        if (!ok) break;
+        {   // dPs rounded, in both orientations
 #pragma unroll
             for (int k = 0; k < 4; k++) {
-                const int j = half * 32 + 8 * k + cf;
-                cs[k][0] = cs[k][1] = 0.f;
+                const int jj = half * 32 + 8 * k + cf;
 #pragma unroll
                 for (int hr = 0; hr < 2; hr++) {
                     const int r = rl + 8 * hr;
-                    float d[2];
-#pragma unroll
-                    for (int e = 0; e < 2; e++) {
-                        const float x = du[4 * k + 2 * hr + e] * dec[4 * k + 2 * hr + e];
-                        const float R = x * qk[4 * k + 2 * hr + e];
-                        rs[hr] += R;
-                        cs[k][e] += R;
-                        d[e] = umma::tf32r(x);
-                        dPC[umma::kidx(j + e, r, 64)] = d[e];
-                    }
-                    *reinterpret_cast<float2*>(dPR + umma::kidx(r, j, 64)) = make_float2(d[0], d[1]);
+                    const float d0 = umma::tf32r(ps[4 * k + 2 * hr]), d1 = umma::tf32r(ps[4 * k + 2 * hr + 1]);
+                    dPC[umma::kidx(jj, r, 64)] = d0;
+                    dPC[umma::kidx(jj + 1, r, 64)] = d1;
+                    *reinterpret_cast<float2*>(dPR + umma::kidx(r, jj, 64)) = make_float2(d0, d1);
                 }
             }
-            rs[0] = umma::row_quad_sum(rs[0]);
-            rs[1] = umma::row_quad_sum(rs[1]);
-            if ((lane & 3) == 0) {
-                rpart[half * 64 + rl] = rs[0];
-                rpart[half * 64 + rl + 8] = rs[1];
-            }
-#pragma unroll
-            for (int k = 0; k < 4; k++)
-#pragma unroll
-                for (int e = 0; e < 2; e++) {
-                    const float c = umma::col_oct_sum(cs[k][e]);
-                    if (lane < 4) colp[win * 64 + half * 32 + 8 * k + 2 * lane + e] = c;
-                }
         }
-        umma::fence_before_sync();
-        ok = umma::named_sync_and(1, 256, umma::mbar_wait(mB, it & 1));   // MN-major Q, K
+        umma::fence_smem_to_async();
+        ok = umma::named_sync_and(1, 256, umma::mbar_wait(mB, gi & 1));   // MN-major Q, K
         if (!ok) break;
         if (L < 64) {
             umma::zero_tail_rows<256>(Qm, 64, 0, L);
@@ -1024,28 +1087,22 @@ __device__ __forceinline__ void bwd_dp_cta(const TileMaps& maps, int hk, int hv,
             umma::mma(tDK, umma::kmaj(dPC, 64), umma::mnt(Qm), 64, 128, 64, false);
             umma::commit(mM);
         }
-        float g_next = 0.f;   // the next tile's gate values, used an iteration later
-        if (tid < 64 && next) g_next = sv.gam[(int64_t)(tn % hv) * sv.T + cn.start + min(tid, cn.len - 1)];
-        if (tid < 64 && tid < L) {   // dgam from R: row sums minus column sums (fixed order)
-            const float cs = (colp[tid] + colp[64 + tid]) + (colp[128 + tid] + colp[192 + tid]);
-            w.dgam2[(int64_t)(ci.start + tid) * hv + h] = (rpart[tid] + rpart[64 + tid]) - cs;
-        }
-        ok = umma::named_sync_and(1, 256, umma::mbar_wait(mM, 1));
+        ok = umma::named_sync_and(1, 256, umma::mbar_wait(mM, nm & 1));
+        nm++;
         umma::fence_after_sync();
         if (!ok) break;
-        if (tid == 0 && next) issue_b(cn, tn);   // the MN-major operands are consumed
-        p_start = ci.start;   // D_dq, D_dk go out at the next tile's first products
-        p_h = h;
+        if (tid == 0 && next) issue_b(cn, gn);   // the MN-major operands are consumed
+        p_start = ci.start;   // D_dq, D_dk go out at the next group's first product
+        p_kh = kh;
         p_L = L;
         umma::fence_before_sync();
-        umma::named_sync(1, 256);   // tensor memory read before the next tile's products reuse it
-        t = tn;
-        tn = t2;
+        umma::named_sync(1, 256);   // tensor memory read before the next group's products reuse it
+        g = gn;
+        gn = g2;
         ci = cn;
         cn = c2;
-        g_cur = g_next;
     }
-    if (ok && p_start >= 0) put_tile(p_start, p_h, p_L);   // the last tile
+    if (ok && p_start >= 0) put_group(p_start, p_kh, p_L);   // the last group
     umma::fence_before_sync();
     umma::named_sync(1, 256);
     if (warp == 0) umma::tmem_free(tmem, 512);
@@ -1527,7 +1584,8 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
 }
 
 // ------------------------------------------------------------------ B4: GVA sum
-// dqkv q/k channels of k-head kh = sum over its G v-heads in order j = 0..G-1.
+// dqkv q/k channels of k-head kh = the P / dP part (per k-head) plus, in order
+// j = 0..G-1, the state-facing and WY parts of its G v-heads.
 __global__ void gva_sum_kernel(const float* __restrict__ dQv, const float* __restrict__ dKv,
                                const float* __restrict__ dQv2, const float* __restrict__ dKv2,
                                const float* __restrict__ dKv3, int64_t T, int hk, int hv,
@@ -1538,14 +1596,14 @@ __global__ void gva_sum_kernel(const float* __restrict__ dQv, const float* __res
     const int c4 = (int)(idx % 32) * 4;
     const int kh = (int)(idx / 32 % hk);
     const int64_t t = idx / 32 / hk;
-    float4 q = zero4(), k = zero4();
+    // the P / dP part is per k-head already (summed over its v-heads)
+    const int64_t okh = (t * hk + kh) * kD + c4;
+    float4 q = ld4(dQv2 + okh), k = ld4(dKv2 + okh);
     for (int j = 0; j < G; j++) {
         const int64_t off = (t * hv + kh * G + j) * kD + c4;
-        const float4 a1 = ld4(dQv + off), a2 = ld4(dQv2 + off);
-        const float4 b1 = ld4(dKv + off), b2 = ld4(dKv2 + off), b3 = ld4(dKv3 + off);
-        const float4 a = make_float4(a1.x + a2.x, a1.y + a2.y, a1.z + a2.z, a1.w + a2.w);
-        const float4 b = make_float4(b1.x + b2.x + b3.x, b1.y + b2.y + b3.y, b1.z + b2.z + b3.z,
-                                     b1.w + b2.w + b3.w);
+        const float4 a = ld4(dQv + off);
+        const float4 b1 = ld4(dKv + off), b3 = ld4(dKv3 + off);
+        const float4 b = make_float4(b1.x + b3.x, b1.y + b3.y, b1.z + b3.z, b1.w + b3.w);
         q.x += a.x; q.y += a.y; q.z += a.z; q.w += a.w;
         k.x += b.x; k.y += b.y; k.z += b.z; k.w += b.w;
     }
@@ -1654,8 +1712,6 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
             e = make_rows_map(&maps.q_mn, a.qkv, a.hk, a.T, C, true);
         if (e == cudaSuccess) e = make_rows_map(&maps.dQv, w.dQv, a.hv, a.T, vs);
         if (e == cudaSuccess) e = make_rows_map(&maps.dKv, w.dKv, a.hv, a.T, vs);
-        if (e == cudaSuccess) e = make_rows_map(&maps.dQv2, w.dQv2, a.hv, a.T, vs);
-        if (e == cudaSuccess) e = make_rows_map(&maps.dKv2, w.dKv2, a.hv, a.T, vs);
         if (e == cudaSuccess) e = make_rows_map(&maps.dKv3, w.dKv3, a.hv, a.T, vs);
         if (e == cudaSuccess)
             e = make_rows_map(&maps.dv, a.dqkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C);
@@ -1681,7 +1737,7 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
         // the reverse state pass (CTAs 0 .. n_state - 1) and the P / dP tiles
         // (persistent CTAs claiming tiles from a counter) in one grid
         const int n_state = (kD / kSl) * a.hv * a.N;
-        const int n_dp = a.NT > 0 ? min(a.NT * a.hv, nsm) : 0;
+        const int n_dp = a.NT > 0 ? min(a.NT * a.hk, nsm) : 0;
         if (n_state + n_dp > 0) {
             GDN_PROF("chunk_bwd_state_dp", st);
             bwd_state_dp_kernel<<<(unsigned)(n_state + n_dp), kStateThreadsB, kStateDpSmem, st>>>(

@@ -73,7 +73,7 @@ struct TileMaps {
     CUtensorMap q, k, v;   // q / k / v channels of the conv output [T, C]
     CUtensorMap W, U, o;   // [T, Hv, d]
     CUtensorMap dO, dU, dW;
-    CUtensorMap dQv, dKv, dQv2, dKv2, dKv3;
+    CUtensorMap dQv, dKv, dKv3;
     CUtensorMap dv;        // v channels of the conv-output gradient [T, C]
     CUtensorMap q_mn, k_mn, v_mn, U_mn, W_mn, dO_mn, dU_mn, dW_mn;
     // the chunk-start states as rows (chunk Hv + head) 128 + a of 128 columns b:
@@ -124,8 +124,8 @@ struct BwdScratch {
                      // memory, which the WY kernel writes only after the state pass
     float* dQv;      // [T, Hv, d] per v-head dq^, state-facing part
     float* dKv;      // [T, Hv, d] per v-head dk^, state-facing part
-    float* dQv2;     // [T, Hv, d] per v-head dq^, P / dP part
-    float* dKv2;     // [T, Hv, d] per v-head dk^, P / dP part
+    float* dQv2;     // [T, Hk, d] per k-head dq^, P / dP part (summed over its v-heads)
+    float* dKv2;     // [T, Hk, d] per k-head dk^, P / dP part (summed over its v-heads)
     float* dKv3;     // [T, Hv, d] per v-head dk^, WY part
     float* dW;       // [T, Hv, d]
     float* dgam;     // [T, Hv] partial dgamma from the state-facing terms

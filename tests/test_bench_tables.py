@@ -43,7 +43,7 @@ def test_path_cost_is_the_method_accounting():
 def test_chunk_kernels_have_tensor_flops():
     total = 0
     for name in bench.MMAS:
-        f = bench.kernel_flops(name, NT, W.h_v)
+        f = bench.kernel_flops(name, NT, W.h_v, W.h_k)
         assert f and f % (NT * W.h_v) == 0, name
         total += f
     # every product the kernels issue, recomputed ones included (the forward
@@ -51,4 +51,4 @@ def test_chunk_kernels_have_tensor_flops():
     # and the output kernel's stacked products carry an unused W K^T and a zero
     # half): ~2.5 TFLOP
     assert 2.3e12 < total < 2.6e12
-    assert bench.kernel_flops("conv_fwd", NT, W.h_v) is None
+    assert bench.kernel_flops("conv_fwd", NT, W.h_v, W.h_k) is None
