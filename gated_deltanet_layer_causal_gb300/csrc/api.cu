@@ -112,8 +112,8 @@ BwdScratch carve_bwd(void* ws, const gdn_dims* d, int NT, int32_t** status, size
     s.status = *status;
     s.dO = c.take<float>(T * H * kD);
     s.dU = c.take<float>(T * H * kD);
-    s.dQv = c.take<float>(T * H * kD);
-    s.dKv = c.take<float>(T * H * kD);
+    s.dQv = c.take<float>(T * (size_t)d->h_k * kD);    // per k-head (state-facing groups)
+    s.dKv = c.take<float>(T * (size_t)d->h_k * kD);
     s.dQv2 = c.take<float>(T * (size_t)d->h_k * kD);   // per k-head (the P / dP groups)
     s.dKv2 = c.take<float>(T * (size_t)d->h_k * kD);
     s.dKv3 = c.take<float>(T * H * kD);

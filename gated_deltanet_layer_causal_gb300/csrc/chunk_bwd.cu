@@ -583,20 +583,24 @@ __device__ __forceinline__ void bwd_state_cta(const TileMaps& maps, int sl, int 
 }
 
 // ------------------------------------------------------------------ B3a: state-facing terms
-// Persistent: one CTA per SM walks the (chunk, head) tiles t = blockIdx.x,
-// + gridDim.x, ... (chunk = t / Hv, head = t % Hv: the v-heads of a chunk run
-// side by side, so the q / k tiles they share come from DRAM once).  Per tile, tcgen05:
+// Persistent: one CTA per SM walks (chunk, k-head) groups g = blockIdx.x,
+// + gridDim.x, ... (chunk = g / Hk, k-head = g % Hk), each as the tiles of its
+// G = Hv / Hk v-heads in turn.  Per tile, tcgen05:
 //   [X; Y] = [dO; dU] S0     (one M=128, N=128, K=128 MMA; X = dO S0, Y = dU S0)
 //   dK~    = U dS            (M=64, N=128, K=128)
-// then dQ partial = e^gam X, dW = -Y, dK partial = fk dK~, and the dgam terms
+// then dW = -Y, and the dgam terms
 //   dgam_i += e^{gam_i} X_i . Q_i,  dgam_j -= Z_j = fk_j dK~_j . K_j,
-//   dgam_{L-1} += sum_j Z_j + e^{gam_L} <dS, S0>.
+//   dgam_{L-1} += sum_j Z_j + e^{gam_L} <dS, S0>;
+// the dQ part e^gam X and the dK part fk dK~ are added, v-head by v-head in
+// order, into tensor-memory sums and written once per k-head at the group's last
+// v-head (the q / k gradient of a k-head is the sum over its v-heads: a third
+// of the bytes at G = 3, written here and read by the GVA sum).
 // Shared memory: [dO; dU] 64 KB and U 32 KB swizzled, S0 64 KB MN-major (rows a,
 // the contraction dimension of [dO; dU] S0; all by TMA), dS^T 64 KB K-major
 // rows b (one bulk copy).  dS^T is free once the
 // products are done and takes the next tile's at once; the other tiles hold
 // this tile's Q, K and staged outputs until its stores have read them.
-// Tensor memory: 256 fp32 columns, allocated once.
+// Tensor memory: the products' 256 fp32 columns and the two sums' 256, once.
 constexpr int kSfFloats = 128 * 128 * 3 + 64 * 128;
 constexpr size_t kB3aSmem = sizeof(float) * (kSfFloats + 64 * 3 + 2 * 128 + 16) + 64 + 1024;
 
@@ -628,9 +632,12 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
     float* SW = A1 + 64 * 128;           // [64][128] swizzled
     float* SK = A2;                      // [64][128] swizzled
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int ntiles = NT * hv;
-    int t = blockIdx.x;
-    if (t >= ntiles) return;
+    const int G = hv / hk, ngroups = NT * hk;
+    // a CTA walks (chunk, k-head) groups g = blockIdx.x, + gridDim.x, ..., each as
+    // its G v-head tiles t = chunk H_v + k-head G + j in turn
+    auto first_tile = [&](int g) { return (g / hk) * hv + (g % hk) * G; };
+    if ((int)blockIdx.x >= ngroups) return;
+    int t = first_tile(blockIdx.x);
     ChunkInfo ci = sv.chunks[t / hv];
     if (ci.len == 0) return;   // the device check of cu_seqlens failed: every chunk is empty
     auto issue_main = [&](const ChunkInfo& c, int tile) {   // one thread
@@ -658,18 +665,23 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
         issue_ds(t);
     }
     float g_cur = gam_of(ci, t);
-    if (warp == 0) umma::tmem_alloc(tslot, 256);
+    if (warp == 0) umma::tmem_alloc(tslot, 512);
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tslot;
+    // the group's dQ and dK parts, summed over its v-heads in order: dQ in the
+    // layout of the X rows (lanes 0-63), dK in that of the M = 64 product
+    const uint32_t tQacc = tmem + 256, tKacc = tmem + 384;
     const int half = warp >> 2, win = warp & 3;
     const int c0 = half * 64;
     bool ok = true;
     for (int it = 0;; it++) {
-        const int h = t % hv, kh = h / (hv / hk), L = ci.len;
-        const int tn = t + (int)gridDim.x;
-        const ChunkInfo cn = tn < ntiles ? sv.chunks[tn / hv] : ci;
+        const int h = t % hv, kh = h / G, L = ci.len, jh = h % G;
+        const bool first = jh == 0, last = jh == G - 1;
+        const int gnext = (t / hv) * hk + kh + (int)gridDim.x;   // the next group
+        const int tn = last ? (gnext < ngroups ? first_tile(gnext) : -1) : t + 1;
+        const ChunkInfo cn = tn < 0 ? ci : (last ? sv.chunks[tn / hv] : ci);
         if (tid < 64) gam[tid] = g_cur;
         ok = umma::mbar_wait(mS, it & 1);
         ok = __syncthreads_and(ok && umma::mbar_wait(mD, it & 1));   // gam visible
@@ -700,7 +712,7 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
         ok = __syncthreads_and(umma::mbar_wait(mbar, it & 1));
         umma::fence_after_sync();
         if (!ok) break;
-        const bool next = tn < ntiles && cn.len > 0;
+        const bool next = tn >= 0 && cn.len > 0;
         if (tid == 0) {
             umma::mbar_expect_tx(mQ, 2 * 64 * 128 * 4);
             umma::tma_rows(Qr, 64, &maps.q, kh, ci.start, mQ);
@@ -719,14 +731,27 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
                 umma::tmem_ld16(umma::tmem_at(tmem, c0 + cc), v);
                 if (r < 64) {
                     const float e = eg[r];
+                    float a[16];
+                    if (first) {
+#pragma unroll
+                        for (int u = 0; u < 16; u++) a[u] = 0.f;
+                    } else {
+                        umma::tmem_ld16(umma::tmem_at(tQacc, c0 + cc), a);
+                    }
 #pragma unroll
                     for (int u = 0; u < 16; u += 4) {
                         const float4 q4 = *reinterpret_cast<const float4*>(
                             Qr + umma::swz(r, c0 + cc + u, 64));
                         part += v[u] * q4.x + v[u + 1] * q4.y + v[u + 2] * q4.z + v[u + 3] * q4.w;
-                        *reinterpret_cast<float4*>(SQ + umma::swz(r, c0 + cc + u, 64)) =
-                            make_float4(e * v[u], e * v[u + 1], e * v[u + 2], e * v[u + 3]);
+                        a[u] += e * v[u];
+                        a[u + 1] += e * v[u + 1];
+                        a[u + 2] += e * v[u + 2];
+                        a[u + 3] += e * v[u + 3];
+                        if (last)
+                            *reinterpret_cast<float4*>(SQ + umma::swz(r, c0 + cc + u, 64)) =
+                                make_float4(a[u], a[u + 1], a[u + 2], a[u + 3]);
                     }
+                    if (!last) umma::tmem_st16(umma::tmem_at(tQacc, c0 + cc), a);
                 } else {
 #pragma unroll
                     for (int u = 0; u < 16; u += 4)   // dW: a tensor-core operand only, rounded
@@ -754,7 +779,25 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
             pl += __shfl_xor_sync(0xffffffffu, pl, 2);
             ph += __shfl_xor_sync(0xffffffffu, ph, 1);
             ph += __shfl_xor_sync(0xffffffffu, ph, 2);
-            umma::frag_to_sw(SK, v, c0, fk[rl], fk[rh]);
+            {   // the dK part fk dK~ into the group's sum; staged at the last v-head
+                float a[32];
+                if (first) {
+#pragma unroll
+                    for (int u = 0; u < 32; u++) a[u] = 0.f;
+                } else {
+                    umma::tmem_ld64_m64(umma::tmem_at(tKacc, c0), a);
+                }
+                const float fl = fk[rl], fh = fk[rh];
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    a[4 * k] += fl * v[4 * k];
+                    a[4 * k + 1] += fl * v[4 * k + 1];
+                    a[4 * k + 2] += fh * v[4 * k + 2];
+                    a[4 * k + 3] += fh * v[4 * k + 3];
+                }
+                if (last) umma::frag_to_sw(SK, a, c0, 1.f, 1.f);
+                else umma::tmem_st64_m64(umma::tmem_at(tKacc, c0), a);
+            }
             if ((lane & 3) == 0) {
                 rpart[half * 128 + 64 + rl] = rl < L ? fk[rl] * pl : 0.f;
                 rpart[half * 128 + 64 + rh] = rh < L ? fk[rh] * ph : 0.f;
@@ -763,18 +806,24 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
         umma::fence_smem_to_async();
         umma::fence_before_sync();
         __syncthreads();
+        // dW per v-head; the dQ, dK parts once per k-head, at its last v-head
         if (L == 64) {
             if (tid == 0) {
-                umma::tma_store_rows(&maps.dQv, h, ci.start, SQ);
                 umma::tma_store_rows(&maps.dW, h, ci.start, SW);
-                umma::tma_store_rows(&maps.dKv, h, ci.start, SK);
+                if (last) {
+                    umma::tma_store_rows(&maps.dQv, kh, ci.start, SQ);
+                    umma::tma_store_rows(&maps.dKv, kh, ci.start, SK);
+                }
                 umma::bulk_commit();
             }
         } else {
             const int64_t off = ((int64_t)ci.start * hv + h) * kD, st = (int64_t)hv * kD;
-            umma::store_rows_sw(w.dQv + off, st, SQ, L);
             umma::store_rows_sw(w.dW + off, st, SW, L);
-            umma::store_rows_sw(w.dKv + off, st, SK, L);
+            if (last) {
+                const int64_t ok2 = ((int64_t)ci.start * hk + kh) * kD, sk = (int64_t)hk * kD;
+                umma::store_rows_sw(w.dQv + ok2, sk, SQ, L);
+                umma::store_rows_sw(w.dKv + ok2, sk, SK, L);
+            }
         }
         if (tid < 64 && tid < L) {
             float g = (rpart[tid] + rpart[128 + tid]) - (rpart[64 + tid] + rpart[192 + tid]);
@@ -799,7 +848,7 @@ bwd_sfacing_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int NT
     if (tid == 0) umma::bulk_wait_read();   // the tile stores have read shared memory
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_free(tmem, 256);
+    if (warp == 0) umma::tmem_free(tmem, 512);
     if (!ok && tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
 }
 
@@ -1584,8 +1633,8 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
 }
 
 // ------------------------------------------------------------------ B4: GVA sum
-// dqkv q/k channels of k-head kh = the P / dP part (per k-head) plus, in order
-// j = 0..G-1, the state-facing and WY parts of its G v-heads.
+// dqkv q/k channels of k-head kh = its state-facing and P / dP parts (per
+// k-head) plus, in order j = 0..G-1, the WY parts of its G v-heads.
 __global__ void gva_sum_kernel(const float* __restrict__ dQv, const float* __restrict__ dKv,
                                const float* __restrict__ dQv2, const float* __restrict__ dKv2,
                                const float* __restrict__ dKv3, int64_t T, int hk, int hv,
@@ -1596,15 +1645,15 @@ __global__ void gva_sum_kernel(const float* __restrict__ dQv, const float* __res
     const int c4 = (int)(idx % 32) * 4;
     const int kh = (int)(idx / 32 % hk);
     const int64_t t = idx / 32 / hk;
-    // the P / dP part is per k-head already (summed over its v-heads)
+    // the state-facing and P / dP parts are per k-head already (summed over its
+    // v-heads); the WY part per v-head
     const int64_t okh = (t * hk + kh) * kD + c4;
-    float4 q = ld4(dQv2 + okh), k = ld4(dKv2 + okh);
+    const float4 a1 = ld4(dQv + okh), a2 = ld4(dQv2 + okh);
+    const float4 b1 = ld4(dKv + okh), b2 = ld4(dKv2 + okh);
+    float4 q = make_float4(a1.x + a2.x, a1.y + a2.y, a1.z + a2.z, a1.w + a2.w);
+    float4 k = make_float4(b1.x + b2.x, b1.y + b2.y, b1.z + b2.z, b1.w + b2.w);
     for (int j = 0; j < G; j++) {
-        const int64_t off = (t * hv + kh * G + j) * kD + c4;
-        const float4 a = ld4(dQv + off);
-        const float4 b1 = ld4(dKv + off), b3 = ld4(dKv3 + off);
-        const float4 b = make_float4(b1.x + b3.x, b1.y + b3.y, b1.z + b3.z, b1.w + b3.w);
-        q.x += a.x; q.y += a.y; q.z += a.z; q.w += a.w;
+        const float4 b = ld4(dKv3 + (t * hv + kh * G + j) * kD + c4);
         k.x += b.x; k.y += b.y; k.z += b.z; k.w += b.w;
     }
     st4(dqkv + t * C + kh * kD + c4, q);
@@ -1710,8 +1759,8 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
             e = make_rows_map(&maps.k_mn, a.qkv + (int64_t)a.hk * kD, a.hk, a.T, C, true);
         if (e == cudaSuccess)
             e = make_rows_map(&maps.q_mn, a.qkv, a.hk, a.T, C, true);
-        if (e == cudaSuccess) e = make_rows_map(&maps.dQv, w.dQv, a.hv, a.T, vs);
-        if (e == cudaSuccess) e = make_rows_map(&maps.dKv, w.dKv, a.hv, a.T, vs);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dQv, w.dQv, a.hk, a.T, (int64_t)a.hk * kD);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dKv, w.dKv, a.hk, a.T, (int64_t)a.hk * kD);
         if (e == cudaSuccess) e = make_rows_map(&maps.dKv3, w.dKv3, a.hv, a.T, vs);
         if (e == cudaSuccess)
             e = make_rows_map(&maps.dv, a.dqkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C);
@@ -1747,7 +1796,7 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
     if (a.NT > 0) {
         {
             GDN_PROF("chunk_bwd_sfacing", st);
-            bwd_sfacing_kernel<<<min(a.NT * a.hv, nsm), 256, kB3aSmem, st>>>(maps, a.hk, a.hv,
+            bwd_sfacing_kernel<<<min(a.NT * a.hk, nsm), 256, kB3aSmem, st>>>(maps, a.hk, a.hv,
                                                                                a.NT, a.sv, w);
         }
         GDN_PROF("chunk_bwd_wy", st);

@@ -122,8 +122,8 @@ struct BwdScratch {
                      // rounded to tf32
     float* dUl;      // [T, Hv, d] dU_local (the local kernel's part of dU); shares dKv3's
                      // memory, which the WY kernel writes only after the state pass
-    float* dQv;      // [T, Hv, d] per v-head dq^, state-facing part
-    float* dKv;      // [T, Hv, d] per v-head dk^, state-facing part
+    float* dQv;      // [T, Hk, d] per k-head dq^, state-facing part (summed over its v-heads)
+    float* dKv;      // [T, Hk, d] per k-head dk^, state-facing part (summed over its v-heads)
     float* dQv2;     // [T, Hk, d] per k-head dq^, P / dP part (summed over its v-heads)
     float* dKv2;     // [T, Hk, d] per k-head dk^, P / dP part (summed over its v-heads)
     float* dKv3;     // [T, Hv, d] per v-head dk^, WY part

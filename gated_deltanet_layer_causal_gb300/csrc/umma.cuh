@@ -448,6 +448,17 @@ __device__ __forceinline__ void tmem_ld_m64(uint32_t taddr, float (&v)[4 * NB]) 
 __device__ __forceinline__ void tmem_ld64_m64(uint32_t taddr, float (&v)[32]) {
     tmem_ld_m64<8>(taddr, v);
 }
+// The inverse of tmem_ld64_m64 (eight 16x256b stores), then wait until the
+// stores have completed.
+__device__ __forceinline__ void tmem_st64_m64(uint32_t taddr, const float (&v)[32]) {
+#pragma unroll
+    for (int k = 0; k < 8; k++)
+        asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(taddr + 8 * k),
+                     "r"(__float_as_uint(v[4 * k])), "r"(__float_as_uint(v[4 * k + 1])),
+                     "r"(__float_as_uint(v[4 * k + 2])), "r"(__float_as_uint(v[4 * k + 3]))
+                     : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
 
 // Write this thread's part of an M = 64 fragment (tmem_ld64_m64) into columns
 // c0 .. c0 + 63 of a swizzled [64][128] tile, rows scaled by s_lo / s_hi (the
