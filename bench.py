@@ -245,7 +245,6 @@ TRAFFIC_64K = {
     "chunk_out_fwd": 12032487424,
     "chunk_norm_bwd": 5312882688,
     "chunk_bwd_local": 4010577920,
-    "chunk_bwd_wy": 10025461760,
     "conv_bwd": 5371858944,
 }
 
@@ -308,8 +307,8 @@ def kernel_cost(name: str, w: synth.Workload, NT: int):
         "chunk_bwd_state_dp": (2 * tk + 3 * tv + g + tv + S) +     # state pass
                               (2 * tk + 2 * tv + g + 2 * tk + 2 * g),  # P / dP groups
         "chunk_bwd_sfacing": 2 * S + 3 * tv + 2 * tk + g + tv + 2 * tk + g,
-        "chunk_bwd_wy": tk + tv + 2 * tv + 2 * Tt + 3 * g + gates + 2 * tv + gates + g,
-        "gva_sum": tv + 6 * tk,
+        "chunk_bwd_wy": tk + tv + 2 * tv + 2 * Tt + 3 * g + gates + tv + tk + gates + g,
+        "gva_sum": 7 * tk,
     }
     return "hbm", table.get(name), "B"
 

@@ -1245,9 +1245,19 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mT + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int C = (2 * hk + hv) * kD;
-    const int ntiles = NT * hv;
-    int t = blockIdx.x;
-    if (t >= ntiles) return;
+    const int G = hv / hk, ngroups = NT * hk;
+    // a CTA walks (chunk, k-head) groups g = blockIdx.x, + gridDim.x, ..., each as
+    // its G v-head tiles t = chunk H_v + k-head G + j in turn; next_tile is the
+    // tile after t in that walk (-1: none)
+    auto first_tile = [&](int g) { return (g / hk) * hv + (g % hk) * G; };
+    auto next_tile = [&](int tt) {
+        if (tt < 0) return -1;
+        if (tt % G != G - 1) return tt + 1;
+        const int gn = (tt / hv) * hk + (tt % hv) / G + (int)gridDim.x;
+        return gn < ngroups ? first_tile(gn) : -1;
+    };
+    if ((int)blockIdx.x >= ngroups) return;
+    int t = first_tile(blockIdx.x);
     ChunkInfo ci = sv.chunks[t / hv];
     if (ci.len == 0) return;   // the device check of cu_seqlens failed: every chunk is empty
     auto Tg_of = [&](int tile) {   // T, then T^T, written by the forward
@@ -1301,7 +1311,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     Gates gcur = gates_of(ci, t);
     // chunk entries are loaded a tile before they are needed: cn (the next tile's)
     // is at hand at the top of an iteration, c2 (the one after) is requested there
-    ChunkInfo cn = t + (int)gridDim.x < ntiles ? sv.chunks[(t + (int)gridDim.x) / hv] : ci;
+    ChunkInfo cn = next_tile(t) >= 0 ? sv.chunks[next_tile(t) / hv] : ci;
     if (warp == 0) umma::tmem_alloc(tslot, 512);
     umma::fence_before_sync();
     __syncthreads();
@@ -1314,14 +1324,16 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
     const int win = warp & 3, half = warp >> 2;
     const int rl = umma::frag_row_lo(), cf = umma::frag_col();   // fragment rows rl, rl + 8
     bool ok = true;
+    float kacc[32];   // the group's dK part, summed over its v-heads in order (fragment)
     for (int it = 0;; it++) {
-        const int h = t % hv, kh = h / (hv / hk), L = ci.len, chunk = t / hv;
-        const int tn = t + (int)gridDim.x, t2 = tn + (int)gridDim.x;
+        const int h = t % hv, kh = h / G, L = ci.len, chunk = t / hv;
+        const bool first = h % G == 0, last = h % G == G - 1;
+        const int tn = next_tile(t), t2 = next_tile(tn);
         ChunkInfo c2 = cn;
-        if (t2 < ntiles) c2 = sv.chunks[t2 / hv];
+        if (t2 >= 0) c2 = sv.chunks[t2 / hv];
         auto row = [&](int r) { return (int64_t)ci.start + min(r, L - 1); };
         const float alog = A_log[h], dtb = dt_bias[h];   // first used at the end of the tile
-        if (tid == 32 && tn < ntiles && cn.len > 0) {   // the next tile's inputs into L2
+        if (tid == 32 && tn >= 0 && cn.len > 0) {   // the next tile's inputs into L2
             const int hn = tn % hv;
             umma::tma_prefetch_rows(&maps.dW, hn, cn.start);
             umma::tma_prefetch_rows(&maps.dU, hn, cn.start);
@@ -1443,7 +1455,7 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
             dbs[tid] += eg[tid] * rp[tid] + rp[64 + tid];
             dgs[tid] += be[tid] * rp[tid];
         }
-        const bool next = tn < ntiles && cn.len > 0;
+        const bool next = tn >= 0 && cn.len > 0;
         const Gates gnext = next ? gates_of(cn, tn) : Gates{0.f, 0.f, from_f<IO>(0.f), 0.f, 0.f};
         // stage 2 operands: T arrived as a K-major tile, K as an MN-major tile
         ok = __syncthreads_and(umma::mbar_wait(mT, it & 1));
@@ -1558,24 +1570,33 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
             issue_m(cn, tn);
             issue_k(cn, tn);
         }
-        // dK part = dKK product + diag(beta e^gam) T^T dW, rows rl, rl + 8 (those
-        // inside the chunk) straight from the fragments
+        // dK part = dKK product + diag(beta e^gam) T^T dW into the group's sum; at
+        // its last v-head, rows rl, rl + 8 (those inside the chunk) of the k-head's
+        // sum straight from the registers
         {
             float vk[32], vw[32];
             umma::tmem_ld64_m64(umma::tmem_at(tX, half * 64), vk);
             umma::tmem_ld64_m64(umma::tmem_at(tTW, half * 64), vw);
             const float bl = be[rl], bh = be[rl + 8];
-            float* dk_lo = w.dKv3 + ((int64_t)(ci.start + rl) * hv + h) * kD;
-            float* dk_hi = dk_lo + (int64_t)8 * hv * kD;
 #pragma unroll
             for (int k = 0; k < 8; k++) {
-                const int c = half * 64 + 8 * k + cf;
-                if (rl < L)
-                    *reinterpret_cast<float2*>(dk_lo + c) =
-                        make_float2(vk[4 * k] + bl * vw[4 * k], vk[4 * k + 1] + bl * vw[4 * k + 1]);
-                if (rl + 8 < L)
-                    *reinterpret_cast<float2*>(dk_hi + c) =
-                        make_float2(vk[4 * k + 2] + bh * vw[4 * k + 2], vk[4 * k + 3] + bh * vw[4 * k + 3]);
+                const float d0 = vk[4 * k] + bl * vw[4 * k], d1 = vk[4 * k + 1] + bl * vw[4 * k + 1];
+                const float d2 = vk[4 * k + 2] + bh * vw[4 * k + 2], d3 = vk[4 * k + 3] + bh * vw[4 * k + 3];
+                kacc[4 * k] = first ? d0 : kacc[4 * k] + d0;
+                kacc[4 * k + 1] = first ? d1 : kacc[4 * k + 1] + d1;
+                kacc[4 * k + 2] = first ? d2 : kacc[4 * k + 2] + d2;
+                kacc[4 * k + 3] = first ? d3 : kacc[4 * k + 3] + d3;
+            }
+            if (last) {
+                float* dk_lo = w.dKv3 + ((int64_t)(ci.start + rl) * hk + kh) * kD;
+                float* dk_hi = dk_lo + (int64_t)8 * hk * kD;
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    const int c = half * 64 + 8 * k + cf;
+                    if (rl < L) *reinterpret_cast<float2*>(dk_lo + c) = make_float2(kacc[4 * k], kacc[4 * k + 1]);
+                    if (rl + 8 < L)
+                        *reinterpret_cast<float2*>(dk_hi + c) = make_float2(kacc[4 * k + 2], kacc[4 * k + 3]);
+                }
             }
         }
         // ---- dg = reverse cumsum of dgam; gates
@@ -1633,8 +1654,8 @@ bwd_wy_kernel(const __grid_constant__ TileMaps maps, const IO* __restrict__ av,
 }
 
 // ------------------------------------------------------------------ B4: GVA sum
-// dqkv q/k channels of k-head kh = its state-facing and P / dP parts (per
-// k-head) plus, in order j = 0..G-1, the WY parts of its G v-heads.
+// dqkv q/k channels of k-head kh = the sum of its state-facing, P / dP and WY
+// parts, each already summed over the k-head's G v-heads (fixed order).
 __global__ void gva_sum_kernel(const float* __restrict__ dQv, const float* __restrict__ dKv,
                                const float* __restrict__ dQv2, const float* __restrict__ dKv2,
                                const float* __restrict__ dKv3, int64_t T, int hk, int hv,
@@ -1645,17 +1666,13 @@ __global__ void gva_sum_kernel(const float* __restrict__ dQv, const float* __res
     const int c4 = (int)(idx % 32) * 4;
     const int kh = (int)(idx / 32 % hk);
     const int64_t t = idx / 32 / hk;
-    // the state-facing and P / dP parts are per k-head already (summed over its
-    // v-heads); the WY part per v-head
+    // every part is per k-head already (summed over its v-heads by its kernel)
     const int64_t okh = (t * hk + kh) * kD + c4;
     const float4 a1 = ld4(dQv + okh), a2 = ld4(dQv2 + okh);
-    const float4 b1 = ld4(dKv + okh), b2 = ld4(dKv2 + okh);
-    float4 q = make_float4(a1.x + a2.x, a1.y + a2.y, a1.z + a2.z, a1.w + a2.w);
-    float4 k = make_float4(b1.x + b2.x, b1.y + b2.y, b1.z + b2.z, b1.w + b2.w);
-    for (int j = 0; j < G; j++) {
-        const float4 b = ld4(dKv3 + (t * hv + kh * G + j) * kD + c4);
-        k.x += b.x; k.y += b.y; k.z += b.z; k.w += b.w;
-    }
+    const float4 b1 = ld4(dKv + okh), b2 = ld4(dKv2 + okh), b3 = ld4(dKv3 + okh);
+    const float4 q = make_float4(a1.x + a2.x, a1.y + a2.y, a1.z + a2.z, a1.w + a2.w);
+    const float4 k = make_float4(b1.x + b2.x + b3.x, b1.y + b2.y + b3.y, b1.z + b2.z + b3.z,
+                                 b1.w + b2.w + b3.w);
     st4(dqkv + t * C + kh * kD + c4, q);
     st4(dqkv + t * C + (int64_t)hk * kD + kh * kD + c4, k);
 }
@@ -1800,7 +1817,7 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
                                                                                a.NT, a.sv, w);
         }
         GDN_PROF("chunk_bwd_wy", st);
-        bwd_wy_kernel<IO><<<min(a.NT * a.hv, nsm), 256, kWySmem, st>>>(
+        bwd_wy_kernel<IO><<<min(a.NT * a.hk, nsm), 256, kWySmem, st>>>(
             maps, (const IO*)a.a, (const IO*)a.b, a.A_log, a.dt_bias, a.hk, a.hv, a.NT, a.dqkv,
             (IO*)a.da, (IO*)a.db, gate_part, a.sv, w);
     }

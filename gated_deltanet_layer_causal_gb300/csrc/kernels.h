@@ -126,7 +126,8 @@ struct BwdScratch {
     float* dKv;      // [T, Hk, d] per k-head dk^, state-facing part (summed over its v-heads)
     float* dQv2;     // [T, Hk, d] per k-head dq^, P / dP part (summed over its v-heads)
     float* dKv2;     // [T, Hk, d] per k-head dk^, P / dP part (summed over its v-heads)
-    float* dKv3;     // [T, Hv, d] per v-head dk^, WY part
+    float* dKv3;     // [T, Hk, d] per k-head dk^, WY part (summed over its v-heads); the
+                     // [T, Hv, d] dU_local before (dUl, allocated at that size)
     float* dW;       // [T, Hv, d]
     float* dgam;     // [T, Hv] partial dgamma from the state-facing terms
     float* dgam2;    // [T, Hv] the P / dP kernel's dgam terms (it runs beside the state pass)
