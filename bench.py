@@ -238,14 +238,18 @@ class DecodeStep:
 # proportional to the chunks it processes).  Valid for the kernels as captured;
 # a kernel changed since then is left out (its traffic reports null).
 TRAFFIC_64K = {
-    "conv_fwd": 3628328960,
-    "gates": 12656640,
-    "chunk_prep": 6499381248,
-    "chunk_state_fwd": 6637580288,
-    "chunk_out_fwd": 12032487424,
-    "chunk_norm_bwd": 5312882688,
-    "chunk_bwd_local": 4010577920,
-    "conv_bwd": 5371858944,
+    "conv_fwd": 3629008896,
+    "gates": 12654592,
+    "chunk_prep": 6495193088,
+    "chunk_state_fwd": 6638098432,
+    "chunk_out_fwd": 12040353792,
+    "chunk_norm_bwd": 5308260352,
+    "chunk_bwd_local": 4012881920,
+    "chunk_bwd_state_dp": 13663719424,
+    "chunk_bwd_sfacing": 14880937984,
+    "chunk_bwd_wy": 9023643648,
+    "gva_sum": 3445714944,
+    "conv_bwd": 5371770880,
 }
 
 # tcgen05 / mma.sync products each chunk kernel issues per (chunk, v-head) tile,
