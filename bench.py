@@ -244,7 +244,6 @@ TRAFFIC_64K = {
     "chunk_state_fwd": 6638098432,
     "chunk_out_fwd": 12040353792,
     "chunk_norm_bwd": 5308260352,
-    "chunk_bwd_local": 4012881920,
     "chunk_bwd_state_dp": 13663719424,
     "chunk_bwd_sfacing": 14880937984,
     "chunk_bwd_wy": 9023643648,
@@ -260,7 +259,7 @@ MMAS = {
     "chunk_state_fwd": [(128, 64, 128), (128, 64, 64), (128, 128, 64)] * 2,
     # [Q; W] [K; S0]^T (Q K^T, Q S0^T, W S0^T and an unused W K^T), [P; 0] U
     "chunk_out_fwd": [(128, 192, 128), (128, 128, 64)],
-    "chunk_bwd_local": [(64, 64, 128), (64, 128, 64)],                  # K Q^T, P^T dO
+    "chunk_bwd_local": [(64, 128, 64)],                                 # P^T dO
     # reverse state pass (2 row slices: K dS^T; B'^T = Q^T e^gam dO - W^T dU_local;
     # W^T Ub) and the P / dP groups' per-v-head dO U^T, one launch
     "chunk_bwd_state_dp": [(64, 64, 128), (128, 64, 64), (128, 64, 64), (128, 64, 64)] * 2 +
@@ -271,9 +270,11 @@ MMAS = {
 }
 
 
-# products issued once per (chunk, k-head) group: the P / dP groups' Q K^T and
-# D_dq = dPs K, D_dk = dPs^T Q (q, k and so these are shared by the group's v-heads)
+# products issued once per (chunk, k-head) group: the local backward's K Q^T, the
+# P / dP groups' Q K^T and D_dq = dPs K, D_dk = dPs^T Q (q, k and so these are
+# shared by the group's v-heads)
 MMAS_KH = {
+    "chunk_bwd_local": [(64, 64, 128)],                                 # K Q^T
     "chunk_bwd_state_dp": [(64, 64, 128), (64, 128, 64), (64, 128, 64)],
 }
 

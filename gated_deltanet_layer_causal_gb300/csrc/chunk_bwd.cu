@@ -77,15 +77,17 @@ chunk_norm_bwd_kernel(const float* __restrict__ o, const IO* __restrict__ z,
 }
 
 // ------------------------------------------------------------------ B1: local
-// grid NT * Hv (block = chunk * Hv + head: the v-heads of a chunk run side by
-// side, so the q / k tiles they share come from DRAM once), 256 threads, tcgen05.
-//   D1 = K Q^T (64 x 64)  ->  P^T[j][i] = D1[j][i] e^{gam_i-gam_j} [i >= j]
-//   D2 = P^T dO           ->  dU_local (64 x 128)
-// Shared memory: Q, K swizzled and dO MN-major, 32 KB each (TMA; dO is the B
-// operand of P^T dO, contracted over tokens, so it is read as loaded, and has
-// its own barrier: K Q^T and P^T do not wait for it); P^T
-// (16 KB) takes the K space once K Q^T is done.  About 97 KB: two CTAs per SM.
-// Tensor memory: 192 fp32 columns (256 allocated).
+// grid NT * Hk (block = chunk * Hk + k-head), 256 threads, tcgen05: a CTA takes
+// the G = Hv / Hk v-heads that share the k-head's q and k, one after another.
+//   D1 = K Q^T (64 x 64, once)
+//   per v-head h:  P^T_h[j][i] = D1[j][i] e^{gam_h,i - gam_h,j} [i >= j]
+//                  dU_local_h = P^T_h dO_h     (64 x 128)
+// Shared memory: Q, K swizzled and one v-head's dO MN-major, 32 KB each (TMA; dO
+// is the B operand of P^T dO, contracted over tokens, so it is read as loaded,
+// and has its own barrier: K Q^T and P^T do not wait for it; the next v-head's is
+// requested once the current product is done).  P^T (16 KB) takes the K space
+// once K Q^T is done, dU_local is staged in the Q space and stored whole.  About
+// 97 KB: two CTAs per SM.  Tensor memory: 192 fp32 columns (256 allocated).
 constexpr int kB1Floats = 64 * 128 * 3;
 constexpr size_t kB1Smem = sizeof(float) * (kB1Floats + 64 + 16) + 64 + 1024;
 
@@ -94,20 +96,20 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
                  BwdScratch w) {
     extern __shared__ float sm_raw[];
     float* sm = umma::align1024(sm_raw);
-    float* Qs = sm;                    // [64][128] swizzled
+    float* Qs = sm;                    // [64][128] swizzled; then dU_local staged
     float* Ks = Qs + 64 * 128;         // [64][128] swizzled
     float* dOs = Ks + 64 * 128;        // [64 (i)][128 (a)] MN-major dO (arrives rounded)
     float* PT = Ks;                    // [64 (j)][64 (i)] K-major, after K Q^T
     float* gam = dOs + 64 * 128;
     uint64_t* mbar = reinterpret_cast<uint64_t*>(gam + 64 + 16);
     uint64_t* mbl = mbar + 1;          // Q, K
-    uint64_t* mbo = mbl + 1;           // dO (first needed by the second product)
+    uint64_t* mbo = mbl + 1;           // dO of one v-head
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbo + 1);
-    // the P / dP kernel, launched after this one, claims its tiles from this counter
+    // the P / dP kernel, launched after this one, claims its work from this counter
     if (blockIdx.x == 0 && threadIdx.x == 0) *w.dp_next = 0;
-    const ChunkInfo ci = sv.chunks[blockIdx.x / hv];
+    const ChunkInfo ci = sv.chunks[blockIdx.x / hk];
     if (ci.len == 0) return;
-    const int h = blockIdx.x % hv, kh = h / (hv / hk), tid = threadIdx.x, L = ci.len;
+    const int kh = blockIdx.x % hk, G = hv / hk, tid = threadIdx.x, L = ci.len;
     const int warp = tid >> 5;
     if (tid == 0) {
         umma::mbar_init(mbar, 1);
@@ -117,9 +119,15 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
         umma::tma_rows(Qs, 64, &maps.q, kh, ci.start, mbl);
         umma::tma_rows(Ks, 64, &maps.k, kh, ci.start, mbl);
         umma::mbar_expect_tx(mbo, 64 * 128 * 4);
-        umma::tma_rows(dOs, 64, &maps.dO_mn, h, ci.start, mbo);
+        umma::tma_rows(dOs, 64, &maps.dO_mn, kh * G, ci.start, mbo);
     }
-    load_gam(gam, sv, ci, h);
+    // gate values of a v-head, loaded a v-head before they are used
+    auto gam_of = [&](int h) {
+        float g = 0.f;
+        if (tid < 64) g = sv.gam[(int64_t)h * sv.T + ci.start + min(tid, L - 1)];
+        return g;
+    };
+    float g_cur = gam_of(kh * G);
     if (warp == 0) umma::tmem_alloc(tslot, 256);
     __syncthreads();
     bool ok = __syncthreads_and(umma::mbar_wait(mbl, 0));
@@ -138,76 +146,77 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
         umma::mma(tD1, umma::swt(Ks, 64), umma::swt(Qs, 64), 64, 64, 128, false);
         umma::commit(mbar);
     }
-    // while the product runs: the decay factors e^{gam_i - gam_j} [i >= j] of this
-    // thread's fragment (rows j, columns i)
-    const int half = warp >> 2;
-    const int rl = umma::frag_row_lo(), cf = umma::frag_col();
-    float dec[16];
-#pragma unroll
-    for (int hr = 0; hr < 2; hr++) {
-        const int jr = rl + 8 * hr;
-        const float gj = gam[jr];
-#pragma unroll
-        for (int k = 0; k < 4; k++)
-#pragma unroll
-            for (int e = 0; e < 2; e++) {
-                const int i = half * 32 + 8 * k + cf + e;
-                dec[4 * k + 2 * hr + e] = i >= jr ? expf(gam[i] - gj) : 0.f;
-            }
-    }
     ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 0));
     umma::fence_after_sync();
-    if (ok) {   // P^T[j][i], 32 columns per warp, all lanes
-        float v[16];
-        umma::tmem_ld_m64<4>(umma::tmem_at(tD1, half * 32), v);
+    const int half = warp >> 2;
+    const int rl = umma::frag_row_lo(), cf = umma::frag_col();
+    float d1[16];   // this thread's fragment of K Q^T, for every v-head
+    if (ok) umma::tmem_ld_m64<4>(umma::tmem_at(tD1, half * 32), d1);
+    for (int jh = 0; jh < G && ok; jh++) {
+        const int h = kh * G + jh;
+        const float g_next = jh + 1 < G ? gam_of(h + 1) : 0.f;
+        if (tid < 64) gam[tid] = g_cur;
+        __syncthreads();   // gam visible; the last v-head's P^T read by its product
+        {   // P^T[j][i], 32 columns per warp, all lanes
 #pragma unroll
-        for (int hr = 0; hr < 2; hr++) {
-            const int jr = rl + 8 * hr;
+            for (int hr = 0; hr < 2; hr++) {
+                const int jr = rl + 8 * hr;
+                const float gj = gam[jr];
 #pragma unroll
-            for (int k = 0; k < 4; k++) {
-                const int i = half * 32 + 8 * k + cf, q = 4 * k + 2 * hr;
-                *reinterpret_cast<float2*>(PT + umma::kidx(jr, i, 64)) =
-                    make_float2(umma::tf32r(v[q] * dec[q]), umma::tf32r(v[q + 1] * dec[q + 1]));
+                for (int k = 0; k < 4; k++) {
+                    const int i = half * 32 + 8 * k + cf, q = 4 * k + 2 * hr;
+                    const float p0 = i >= jr ? d1[q] * expf(gam[i] - gj) : 0.f;
+                    const float p1 = i + 1 >= jr ? d1[q + 1] * expf(gam[i + 1] - gj) : 0.f;
+                    *reinterpret_cast<float2*>(PT + umma::kidx(jr, i, 64)) =
+                        make_float2(umma::tf32r(p0), umma::tf32r(p1));
+                }
             }
         }
-    }
-    umma::fence_smem_to_async();
-    umma::fence_before_sync();
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbo, 0));
-    if (L < 64) {
-        umma::zero_tail_rows(dOs, 64, 0, L);
         umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        ok = __syncthreads_and(umma::mbar_wait(mbo, jh & 1));
+        if (!ok) break;
+        if (L < 64) {
+            umma::zero_tail_rows(dOs, 64, 0, L);
+            umma::fence_smem_to_async();
+            __syncthreads();
+        }
+        umma::fence_after_sync();
+        if (tid == 0) {
+            umma::mma(tD2, umma::kmaj(PT, 64), umma::mnt(dOs), 64, 128, 64, false);
+            umma::commit(mbar);
+            umma::bulk_wait_read();   // the last v-head's dU_local store has read the Q space
+        }
+        ok = __syncthreads_and(umma::mbar_wait(mbar, (jh + 1) & 1));
+        umma::fence_after_sync();
+        if (!ok) break;
+        if (tid == 0 && jh + 1 < G) {   // dO consumed: the next v-head's
+            umma::mbar_expect_tx(mbo, 64 * 128 * 4);
+            umma::tma_rows(dOs, 64, &maps.dO_mn, h + 1, ci.start, mbo);
+        }
+        {   // dU_local staged as a swizzled tile in the Q space, stored whole
+            float v[32];
+            umma::tmem_ld64_m64(umma::tmem_at(tD2, half * 64), v);
+            umma::frag_to_sw(Qs, v, half * 64, 1.f, 1.f);
+        }
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
         __syncthreads();
+        if (L == 64) {
+            if (tid == 0) {
+                umma::tma_store_rows(&maps.dKv3, h, ci.start, Qs);   // the dU_local buffer
+                umma::bulk_commit();
+            }
+        } else {
+            umma::store_rows_sw(w.dUl + ((int64_t)ci.start * hv + h) * kD, (int64_t)hv * kD, Qs, L);
+        }
+        g_cur = g_next;
     }
-    umma::fence_after_sync();
-    if (ok && tid == 0) {
-        umma::mma(tD2, umma::kmaj(PT, 64), umma::mnt(dOs), 64, 128, 64, false);
-        umma::commit(mbar);
-    }
-    ok = __syncthreads_and(ok && umma::mbar_wait(mbar, 1));
-    umma::fence_after_sync();
-    // dU_local staged as a swizzled tile in the Q space (consumed), stored whole
-    if (ok) {
-        float v[32];
-        umma::tmem_ld64_m64(umma::tmem_at(tD2, half * 64), v);
-        umma::frag_to_sw(Qs, v, half * 64, 1.f, 1.f);
-    } else if (tid == 0) {
-        atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
-    }
-    umma::fence_smem_to_async();
+    if (tid == 0) umma::bulk_wait_read();
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 256);
-    if (!ok) return;
-    if (L == 64) {
-        if (tid == 0) {
-            umma::tma_store_rows(&maps.dKv3, h, ci.start, Qs);   // the dU_local buffer
-            umma::bulk_commit();
-            umma::bulk_wait_read();
-        }
-    } else {
-        umma::store_rows_sw(w.dUl + ((int64_t)ci.start * hv + h) * kD, (int64_t)hv * kD, Qs, L);
-    }
+    if (!ok && tid == 0) atomicExch(w.status, 5);   // GDN_ERR_DEVICE_TIMEOUT
 }
 
 // ------------------------------------------------------------------ B2: reverse state pass
@@ -1797,7 +1806,7 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
                                               w.nw_part);
         }
         GDN_PROF("chunk_bwd_local", st);
-        bwd_local_kernel<<<a.NT * a.hv, 256, kB1Smem, st>>>(maps, a.hk, a.hv, a.sv, w);
+        bwd_local_kernel<<<a.NT * a.hk, 256, kB1Smem, st>>>(maps, a.hk, a.hv, a.sv, w);
     }
     {
         // the reverse state pass (CTAs 0 .. n_state - 1) and the P / dP tiles

@@ -47,7 +47,7 @@ def test_chunk_kernels_have_tensor_flops():
     total = 0
     for name in bench.MMAS:
         f = bench.kernel_flops(name, NT, W.h_v, W.h_k)
-        assert f and f % (NT * W.h_v) == 0, name
+        assert f and f % (NT * W.h_k) == 0, name
         total += f
     # every product the kernels issue, recomputed ones included (the forward
     # state pass builds each chunk's d_k x d_k transition in both row slices,
