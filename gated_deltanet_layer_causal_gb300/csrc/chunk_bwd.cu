@@ -27,13 +27,6 @@ namespace gdn {
 
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
-// gam with padding rows continuing the last valid value (keeps Gam finite)
-__device__ __forceinline__ void load_gam(float* gam, const FwdSaved& sv, const ChunkInfo& ci,
-                                         int h) {
-    const int tid = threadIdx.x;
-    if (tid < 64) gam[tid] = sv.gam[(int64_t)h * sv.T + ci.start + min(tid, ci.len - 1)];
-}
-
 // ------------------------------------------------------------------ B0: gated-norm backward
 // rows = T * Hv rows of d_v = 128, one warp per row, 64 rows per CTA (many CTAs
 // per SM: a streaming pass).  dO is stored fp32 and tf32-rounded (it is only
@@ -1669,7 +1662,7 @@ __global__ void gva_sum_kernel(const float* __restrict__ dQv, const float* __res
                                const float* __restrict__ dQv2, const float* __restrict__ dKv2,
                                const float* __restrict__ dKv3, int64_t T, int hk, int hv,
                                float* __restrict__ dqkv) {
-    const int G = hv / hk, C = (2 * hk + hv) * kD;
+    const int C = (2 * hk + hv) * kD;
     int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // over T * hk * 32
     if (idx >= T * hk * 32) return;
     const int c4 = (int)(idx % 32) * 4;
