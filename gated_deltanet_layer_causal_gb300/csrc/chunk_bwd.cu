@@ -197,7 +197,7 @@ bwd_local_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, FwdSaved
         __syncthreads();
         if (L == 64) {
             if (tid == 0) {
-                umma::tma_store_rows(&maps.dKv3, h, ci.start, Qs);   // the dU_local buffer
+                umma::tma_store_rows(&maps.dUl, h, ci.start, Qs);
                 umma::bulk_commit();
             }
         } else {
@@ -1182,9 +1182,10 @@ bwd_state_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int N
 }
 
 // ------------------------------------------------------------------ B3c: WY terms and gates
-// Persistent: one CTA per SM walks the (chunk, head) tiles t = blockIdx.x,
-// + gridDim.x, ... (chunk = t / Hv, head = t % Hv: the v-heads of a chunk run
-// side by side, so the q / k tiles they share come from DRAM once).  Per tile, tcgen05, with T
+// Persistent: one CTA per SM walks (chunk, k-head) groups g = blockIdx.x,
+// + gridDim.x, ... (chunk = g / Hk, k-head = g % Hk), each as the tiles of its
+// G = Hv / Hk v-heads in turn (neighbouring SMs hold neighbouring groups of one
+// chunk, so the tiles they read come from DRAM once).  Per tile, tcgen05, with T
 // saved by the forward:
 //   D_kk = K K^T, D_dt1 = dW K^T, D_dt2 = dU V^T          (64 x 64)
 //   D_tw = T^T [dW | dU]                                  (64 x 256, one product)
@@ -1195,6 +1196,8 @@ bwd_state_dp_kernel(const __grid_constant__ TileMaps maps, int hk, int hv, int N
 //   dbeta_j += sum_m dA (.) GamKK ; dgam_j += beta_j (..) ; dgam_m -= sum_j beta_j (..)
 //   dK += (dKK + dKK^T) K   (one product: the two triangles are disjoint)
 // then dg = reverse in-chunk cumsum of the total dgam, and the gate gradients.
+// The dK part is summed over the group's v-heads in registers, in order, and
+// written once per k-head at the group's last v-head.
 // The next tile's operands are requested in two groups as their space frees
 // up: dW, dU (K-major) and T^T once dA is formed, dW, dU (MN-major), V and K
 // once the last product is done (dK goes to global memory straight from the
@@ -1736,13 +1739,10 @@ __global__ void colsum_stage2_kernel(const float* __restrict__ tmp, float* __res
 }
 
 // ------------------------------------------------------------------ launcher
-// The reverse state pass runs one CTA per (64-row slice, head, sequence) and
-// leaves most SMs idle for its whole duration; the P / dP kernel does not
-// depend on it, so it runs beside it: the state pass goes to a high-priority
-// side stream forked from and joined back into the caller's stream.  The side
-// stream and its two events are created once per device; the fork / join
-// sequence is enqueued under a lock, so concurrent calls on one device do not
-// interleave their events.
+// Everything on the caller's stream, in order: gated-norm backward, local
+// backward, the reverse state pass with the P / dP groups beside it (one
+// launch), state-facing terms, WY terms and gates, the GVA sum, then the
+// deterministic reductions of the per-head gate sums and the norm weight.
 
 template <class IO>
 static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStream_t st) {
@@ -1780,7 +1780,7 @@ static cudaError_t chunk_bwd_t(const ChunkArgs& a, const BwdScratch& w, cudaStre
             e = make_rows_map(&maps.q_mn, a.qkv, a.hk, a.T, C, true);
         if (e == cudaSuccess) e = make_rows_map(&maps.dQv, w.dQv, a.hk, a.T, (int64_t)a.hk * kD);
         if (e == cudaSuccess) e = make_rows_map(&maps.dKv, w.dKv, a.hk, a.T, (int64_t)a.hk * kD);
-        if (e == cudaSuccess) e = make_rows_map(&maps.dKv3, w.dKv3, a.hv, a.T, vs);
+        if (e == cudaSuccess) e = make_rows_map(&maps.dUl, w.dUl, a.hv, a.T, vs);
         if (e == cudaSuccess)
             e = make_rows_map(&maps.dv, a.dqkv + (int64_t)2 * a.hk * kD, a.hv, a.T, C);
         if (e == cudaSuccess)

@@ -73,7 +73,7 @@ struct TileMaps {
     CUtensorMap q, k, v;   // q / k / v channels of the conv output [T, C]
     CUtensorMap W, U, o;   // [T, Hv, d]
     CUtensorMap dO, dU, dW;
-    CUtensorMap dQv, dKv, dKv3;
+    CUtensorMap dQv, dKv, dUl;
     CUtensorMap dv;        // v channels of the conv-output gradient [T, C]
     CUtensorMap q_mn, k_mn, v_mn, U_mn, W_mn, dO_mn, dU_mn, dW_mn;
     // the chunk-start states as rows (chunk Hv + head) 128 + a of 128 columns b:
