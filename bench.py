@@ -320,8 +320,8 @@ def kernel_cost(name: str, w: synth.Workload, NT: int):
 
 
 def path_cost(w: synth.Workload):
-    """Algorithmic bytes and FLOPs of one step of the whole path (SURVEY-style
-    accounting: inputs read and outputs written once, saved activations free;
+    """Algorithmic bytes and FLOPs of one step of the whole path (the method's
+    minimum: inputs read and outputs written once, saved activations free;
     MMA FLOPs only, no recompute).  Per token, bf16, c = 64, d = 128:
       fwd bytes: x 2C + a, b 2*2H + z 2Hd + y 2Hd
       bwd bytes: dy, z 2*2Hd + x 2C + a, b 2*2H read; dx 2C, dz 2Hd, da, db 2*2H
