@@ -56,7 +56,7 @@ def parse():
     p.add_argument("--tokens", type=int, default=0,
                    help="profiling case: only the first TOKENS tokens of the workload, as one "
                         "sequence (0 = the whole workload)")
-    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-tokens", type=int, default=4096,
